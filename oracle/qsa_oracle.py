@@ -1,0 +1,301 @@
+"""CPU fp64 oracle for indexer-selected (QSA-style) block-sparse attention.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path imports this module: only
+the tests, the smoke check and the benchmark's CPU-baseline leg may call it. It
+shares no code with the CUDA library (no kernels, headers, tables or helpers);
+the two meet only in the seeded inputs they both consume.
+
+It is the plain definition of the method, written for readability, not speed:
+logical per-sequence token arrays (no paging), numpy fp64 arithmetic, a library
+matmul and a library sort as the only building blocks.
+
+Sources (web pages, cited by title and section):
+  [VA6]   "Agentic shootout -- Atlas x Flash-Next research", report
+          "Flash-Next support: vLLM vs Atlas", section (a) item 6 "QSA sparse
+          attention + indexer": one compressed key per complete group of
+          `compress_ratio` tokens (mean-pool), weight-free scoring of the query
+          against the compressed keys, block top-k with budget/ratio groups,
+          expansion of the selected groups back to token indices
+          (budget + ratio - 1 wide, -1 padded), sparse paged GQA attention.
+  [PR16]  same page, "PR 16 review: qwen4exp serving in Atlas (Claude's
+          review)", section (a), QSA bullet: 4-token mean-pooled blocks,
+          relu-score, top-512 + tail, inert at <= 2051 visible tokens.
+  [LC3]   same page, "Flash-Next support: llama.cpp vs Atlas", section (a)
+          item 3: blocks cut the position line; the incomplete tail block is
+          always visible; incomplete blocks are not scored.
+  [INV1]  "Atlas Flash-Next defect investigations", Report A, Defect 1,
+          proposed fix: rewind sets ingested -= dropped, pooled =
+          ingested / ratio; decode at pos requires pos == ingested.
+  The score formula sum_h w_h * ReLU(q_h . k_b) is the relu-score of [PR16];
+  w == 1 is the weight-free case of [VA6].
+
+Readings taken where the pages are silent (each is also listed in the design
+notes): the row's own token is visible (V = pos + 1); a block completed by the
+row's own token competes in the top-K (it is not force-kept); ties go to the
+lower block index; output indices ascending, -1 padded; GQA head h uses KV head
+floor(h * Hkv / Hq); softmax scale 1/sqrt(D); the final output is rounded to
+bf16 (round to nearest even).
+
+Every function is pinned by tests that do not re-derive it (closed forms,
+brute force on tiny inputs, special cases, invariants, hand-worked examples).
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Optional, Tuple
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# bf16 <-> fp64
+# ---------------------------------------------------------------------------
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Exact value of bf16 bit patterns (uint16) as float64."""
+    b = np.asarray(bits).astype(np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """Round float64 values to bf16 (8 significant bits), nearest-even, directly
+    from fp64 (no intermediate fp32 rounding). Overflow goes to +-inf, NaN to
+    the canonical quiet NaN, and values below 2^-126 use the subnormal quantum
+    2^-133."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    out = np.empty(x.shape, dtype=np.float64)
+    finite = np.isfinite(a)
+    m, e = np.frexp(np.where(finite & (a > 0), a, 1.0))   # a = m * 2^e, m in [0.5, 1)
+    lead = np.maximum(e - 1, -126)                         # exponent of the leading bit
+    quantum = np.ldexp(1.0, lead - 7)
+    r = np.rint(a / quantum) * quantum                    # rint: half to even
+    r = np.where(a > 0, r, 0.0)
+    r = np.where(r >= 2.0 ** 128, np.inf, r)
+    out[...] = np.where(finite, r, np.inf)
+    out = np.copysign(out, x)
+    bits = (out.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    bits = np.where(np.isnan(x), np.uint16(0x7FC0), bits)
+    return bits.astype(np.uint16)
+
+
+def round_bf16(x) -> np.ndarray:
+    """Value of x after rounding to bf16."""
+    return bf16_bits_to_f64(f64_to_bf16_bits(x))
+
+
+# ---------------------------------------------------------------------------
+# Per-sequence indexer state (append / pool / rewind)
+# ---------------------------------------------------------------------------
+
+
+class DesyncError(RuntimeError):
+    """An append at a position other than the number of ingested tokens."""
+
+
+class CapacityError(RuntimeError):
+    """An append beyond the sequence's capacity."""
+
+
+def pool_block(raw_bits) -> np.ndarray:
+    """Compressed key of one block: the mean of its `ratio` raw index keys,
+    rounded to bf16 ([VA6] mean-pool; [PR16] "4-token mean-pooled blocks")."""
+    raw = bf16_bits_to_f64(raw_bits)
+    return f64_to_bf16_bits(raw.mean(axis=0))
+
+
+class SeqState:
+    """Logical token arrays of one sequence: K, V, raw index keys (bf16 bits),
+    the compressed key of every complete block, and the ingested counter.
+
+    Block b covers logical positions [b*ratio, (b+1)*ratio) ([LC3]: blocks cut
+    the position line). A block is complete once all of its tokens have been
+    ingested; only complete blocks have compressed keys.
+    """
+
+    def __init__(self, ratio: int, n_kv_heads: int, head_dim: int, idx_dim: int,
+                 capacity: int):
+        self.ratio = ratio
+        self.capacity = capacity
+        self.K = np.zeros((capacity, n_kv_heads, head_dim), np.uint16)
+        self.V = np.zeros((capacity, n_kv_heads, head_dim), np.uint16)
+        self.idx_raw = np.zeros((capacity, idx_dim), np.uint16)
+        self.idx_blk = np.zeros((capacity // ratio, idx_dim), np.uint16)
+        self.ingested = 0
+
+    @property
+    def n_blocks(self) -> int:
+        """pooled = ingested / ratio ([INV1])."""
+        return self.ingested // self.ratio
+
+    def append(self, pos: int, k_bits, v_bits, idx_bits) -> None:
+        """Ingest n new tokens at positions pos..pos+n-1.
+
+        Requires pos == ingested ([INV1]: decode at pos requires
+        pos == ingested). Every block completed by the new tokens is pooled
+        from the raw keys it holds now."""
+        k_bits = np.asarray(k_bits, np.uint16)
+        n = k_bits.shape[0]
+        if pos != self.ingested:
+            raise DesyncError(f"append at pos {pos} but {self.ingested} tokens ingested")
+        if pos + n > self.capacity:
+            raise CapacityError(f"append of {n} at pos {pos} exceeds capacity {self.capacity}")
+        self.K[pos:pos + n] = k_bits
+        self.V[pos:pos + n] = np.asarray(v_bits, np.uint16)
+        self.idx_raw[pos:pos + n] = np.asarray(idx_bits, np.uint16)
+        r = self.ratio
+        first_done = pos // r            # first block that may complete now
+        last_done = (pos + n) // r       # blocks [first_done, last_done) are complete
+        for b in range(first_done, last_done):
+            self.idx_blk[b] = pool_block(self.idx_raw[b * r:(b + 1) * r])
+        self.ingested = pos + n
+
+    def rewind(self, n_drop: int) -> None:
+        """Drop the last n_drop tokens ([INV1]: ingested -= dropped,
+        pooled = ingested / ratio). Rows past the new end are dead; a block
+        that becomes incomplete is re-pooled from its new raw rows when it is
+        completed again."""
+        if n_drop < 0 or n_drop > self.ingested:
+            raise ValueError(f"rewind of {n_drop} with {self.ingested} ingested")
+        self.ingested -= n_drop
+
+
+# ---------------------------------------------------------------------------
+# One query row: score, select, expand, attend
+# ---------------------------------------------------------------------------
+
+
+def block_scores(q_idx_bits, w, blk_bits) -> np.ndarray:
+    """s_b = sum_h w_h * max(0, q_h . k_b) for every complete block b, fp64.
+
+    q_idx_bits [H_I, d_I] bf16 bits, w [H_I] float, blk_bits [n_blk, d_I]."""
+    q = bf16_bits_to_f64(q_idx_bits)
+    k = bf16_bits_to_f64(blk_bits)
+    dots = q @ k.T                              # [H_I, n_blk]
+    return np.asarray(w, np.float64) @ np.maximum(dots, 0.0)
+
+
+def select_blocks(scores, topk: int) -> np.ndarray:
+    """Top-K blocks by (score descending, block index ascending), returned in
+    ascending block order. With n_blk <= K every block is selected, which makes
+    a visible prefix of at most budget + ratio - 1 tokens exactly dense
+    ([PR16]: inert at <= 2051 visible tokens for budget 2048, ratio 4)."""
+    s = np.asarray(scores, np.float64)
+    n = s.shape[0]
+    if n <= topk:
+        return np.arange(n, dtype=np.int64)
+    order = np.lexsort((np.arange(n), -s))     # last key is primary
+    return np.sort(order[:topk])
+
+
+def token_set(sel, n_blk: int, visible: int, ratio: int) -> np.ndarray:
+    """Selected blocks expanded to token positions, plus the tail
+    [n_blk*ratio, visible) of the incomplete block ([VA6] expansion; [LC3]
+    tail always visible). Ascending."""
+    sel = np.asarray(sel, np.int64)
+    body = (sel[:, None] * ratio + np.arange(ratio)[None, :]).reshape(-1)
+    tail = np.arange(n_blk * ratio, visible, dtype=np.int64)
+    return np.concatenate([body, tail])
+
+
+def kv_head_of(h: int, n_q_heads: int, n_kv_heads: int) -> int:
+    """GQA: contiguous groups of Hq/Hkv query heads share one KV head."""
+    return (h * n_kv_heads) // n_q_heads
+
+
+def gqa_attention(q_bits, k_bits, v_bits) -> np.ndarray:
+    """Softmax attention of each query head over the given token rows, fp64.
+
+    q_bits [Hq, D]; k_bits, v_bits [T, Hkv, D]. Scale 1/sqrt(D), max
+    subtracted before exponentiation. Returns [Hq, D] float64 (unrounded)."""
+    q = bf16_bits_to_f64(q_bits)
+    k = bf16_bits_to_f64(k_bits)
+    v = bf16_bits_to_f64(v_bits)
+    hq, d = q.shape
+    hkv = k.shape[1]
+    out = np.empty((hq, d), np.float64)
+    for h in range(hq):
+        g = kv_head_of(h, hq, hkv)
+        s = (k[:, g, :] @ q[h]) / math.sqrt(d)
+        p = np.exp(s - s.max())
+        out[h] = (p @ v[:, g, :]) / p.sum()
+    return out
+
+
+def attend_row(state: SeqState, pos: int, q_idx_bits, w, q_bits, topk: int) -> Dict:
+    """The whole path for one query row at logical position pos.
+
+    The row's token is already ingested, so V = pos + 1 tokens are visible and
+    n_blk = V // ratio blocks are complete."""
+    r = state.ratio
+    visible = pos + 1
+    if visible > state.ingested:
+        raise DesyncError(f"row at pos {pos} but only {state.ingested} ingested")
+    n_blk = visible // r
+    if n_blk > topk:
+        scores = block_scores(q_idx_bits, w, state.idx_blk[:n_blk])
+    else:
+        scores = None                        # everything is selected; no scoring needed
+    sel = select_blocks(scores if scores is not None else np.zeros(n_blk), topk)
+    toks = token_set(sel, n_blk, visible, r)
+    out = gqa_attention(q_bits, state.K[toks], state.V[toks])
+    return {"n_blk": n_blk, "scores": scores, "sel": sel, "tokens": toks,
+            "out": out, "out_bf16": f64_to_bf16_bits(out)}
+
+
+def padded_selection(sel, topk: int) -> np.ndarray:
+    """Selection as a fixed-width row: ascending ids, -1 padded to K."""
+    row = np.full(topk, -1, np.int64)
+    row[: len(sel)] = sel
+    return row
+
+
+# ---------------------------------------------------------------------------
+# Independent dense attention (used only to pin the sparse path below the
+# inert bound)
+# ---------------------------------------------------------------------------
+
+
+def dense_attention(q_bits, k_bits, v_bits, n_kv_heads: int) -> np.ndarray:
+    """Plain causal-prefix attention over ALL given tokens, coded separately
+    from gqa_attention: per head, weights = exp(s - logsumexp(s))."""
+    from scipy.special import logsumexp
+
+    q = bf16_bits_to_f64(q_bits)
+    k = bf16_bits_to_f64(k_bits)
+    v = bf16_bits_to_f64(v_bits)
+    hq, d = q.shape
+    group = hq // n_kv_heads
+    out = np.zeros((hq, d))
+    for g in range(n_kv_heads):
+        for j in range(group):
+            h = g * group + j
+            logits = np.einsum("td,d->t", k[:, g, :], q[h]) * (d ** -0.5)
+            wts = np.exp(logits - logsumexp(logits))
+            out[h] = np.einsum("t,td->d", wts, v[:, g, :])
+    return out
+
+
+# ---------------------------------------------------------------------------
+# A batch of rows in the library's layout: n_seq sequences, R rows each,
+# row j of sequence i at position pos0[i] + j, appended before attending.
+# ---------------------------------------------------------------------------
+
+
+def step(states: List[SeqState], pos0: List[int], k_new, v_new, idx_new,
+         q_idx, w, q, topk: int, rows_per_seq: int) -> List[Dict]:
+    """Append each sequence's R new tokens, then run every row.
+
+    k_new/v_new [n_seq*R, Hkv, D], idx_new [n_seq*R, d_I], q_idx
+    [n_seq*R, H_I, d_I], w [n_seq*R, H_I], q [n_seq*R, Hq, D] (bf16 bits
+    except w). Returns one result dict per row, sequence-major."""
+    R = rows_per_seq
+    for i, st in enumerate(states):
+        sl = slice(i * R, (i + 1) * R)
+        st.append(pos0[i], k_new[sl], v_new[sl], idx_new[sl])
+    out = []
+    for i, st in enumerate(states):
+        for j in range(R):
+            row = i * R + j
+            out.append(attend_row(st, pos0[i] + j, q_idx[row], w[row], q[row], topk))
+    return out

@@ -1,0 +1,128 @@
+"""Planted mistakes: each test plants one plausible bug in the oracle (on the
+CPU, by monkeypatching) and checks that at least one pin then fails. A pin
+suite that still passes with the bug would not be able to tell it apart."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import qsa_oracle as O
+from tests import test_oracle_pins as P
+from tests.conftest import read_golden_cases
+
+
+def _cases():
+    return read_golden_cases("worked_example.txt")
+
+
+def _fails(fn, *args):
+    try:
+        fn(*args)
+    except AssertionError:
+        return True
+    return False
+
+
+def no_relu(q_idx_bits, w, blk_bits):
+    q = O.bf16_bits_to_f64(q_idx_bits); k = O.bf16_bits_to_f64(blk_bits)
+    return np.asarray(w, np.float64) @ (q @ k.T)
+
+
+def relu_outside(q_idx_bits, w, blk_bits):
+    q = O.bf16_bits_to_f64(q_idx_bits); k = O.bf16_bits_to_f64(blk_bits)
+    return np.maximum(np.asarray(w, np.float64) @ (q @ k.T), 0.0)
+
+
+def tie_to_higher(scores, topk):
+    s = np.asarray(scores, np.float64); n = len(s)
+    if n <= topk:
+        return np.arange(n)
+    order = np.lexsort((-np.arange(n), -s))
+    return np.sort(order[:topk])
+
+
+def rank_order(scores, topk):
+    s = np.asarray(scores, np.float64); n = len(s)
+    if n <= topk:
+        return np.arange(n)
+    return np.lexsort((np.arange(n), -s))[:topk]
+
+
+def no_tail(sel, n_blk, visible, ratio):
+    sel = np.asarray(sel, np.int64)
+    return (sel[:, None] * ratio + np.arange(ratio)[None, :]).reshape(-1)
+
+
+def kv_head_modulo(h, hq, hkv):
+    return h % hkv
+
+
+def pool_sum(raw_bits):
+    return O.f64_to_bf16_bits(O.bf16_bits_to_f64(raw_bits).sum(axis=0))
+
+
+def truncating_bf16(x):
+    x = np.asarray(x, np.float64)
+    return (x.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def attention_scale_1_over_d(q_bits, k_bits, v_bits):
+    q = O.bf16_bits_to_f64(q_bits); k = O.bf16_bits_to_f64(k_bits); v = O.bf16_bits_to_f64(v_bits)
+    hq, d = q.shape; hkv = k.shape[1]
+    out = np.empty((hq, d))
+    for h in range(hq):
+        g = O.kv_head_of(h, hq, hkv)
+        s = (k[:, g, :] @ q[h]) / d
+        p = np.exp(s - s.max())
+        out[h] = (p @ v[:, g, :]) / p.sum()
+    return out
+
+
+def visible_excludes_own_token(state, pos, q_idx_bits, w, q_bits, topk):
+    r = state.ratio
+    visible = pos
+    n_blk = visible // r
+    scores = O.block_scores(q_idx_bits, w, state.idx_blk[:n_blk]) if n_blk > topk else None
+    sel = O.select_blocks(scores if scores is not None else np.zeros(n_blk), topk)
+    toks = O.token_set(sel, n_blk, visible, r)
+    out = O.gqa_attention(q_bits, state.K[toks], state.V[toks])
+    return {"n_blk": n_blk, "scores": scores, "sel": sel, "tokens": toks, "out": out,
+            "out_bf16": O.f64_to_bf16_bits(out)}
+
+
+class StickyRewind(O.SeqState):
+    def rewind(self, n_drop):
+        if n_drop < 0 or n_drop > self.ingested:
+            raise ValueError("bad rewind")
+        # bug: forgets to move the counter
+
+
+MUTATIONS = [
+    ("block_scores", no_relu, [P.test_score_closed_forms]),
+    ("block_scores", relu_outside, [P.test_score_closed_forms]),
+    ("select_blocks", tie_to_higher, [P.test_selection_special_cases]),
+    ("select_blocks", rank_order, [P.test_worked_example_scores_and_selection]),
+    ("token_set", no_tail, [P.test_inert_bound_from_pages]),
+    ("kv_head_of", kv_head_modulo, [P.test_gqa_head_mapping_contiguous_groups]),
+    ("pool_block", pool_sum, [P.test_worked_example_blocks]),
+    ("f64_to_bf16_bits", truncating_bf16, [P.test_bf16_rounding_hand_cases]),
+    ("gqa_attention", attention_scale_1_over_d, [P.test_worked_example_attention]),
+    ("attend_row", visible_excludes_own_token, [P.test_dense_identity_at_and_below_inert_bound]),
+    ("SeqState", StickyRewind, [P.test_counter_discipline]),
+]
+
+
+@pytest.mark.parametrize("name,bug,pins", MUTATIONS, ids=[f"{m[0]}:{m[1].__name__}" for m in MUTATIONS])
+def test_planted_mistake_is_caught(monkeypatch, name, bug, pins):
+    monkeypatch.setattr(O, name, bug)
+    args = {P.test_worked_example_blocks: (_cases(),),
+            P.test_worked_example_scores_and_selection: (_cases(),),
+            P.test_worked_example_attention: (_cases(),)}
+    caught = []
+    for pin in pins:
+        try:
+            pin(*args.get(pin, ()))
+            caught.append(False)
+        except AssertionError:
+            caught.append(True)
+    assert any(caught), f"no pin caught the planted mistake in {name}"

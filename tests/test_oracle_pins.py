@@ -1,0 +1,404 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself:
+values printed on the pages, hand-worked examples, closed forms, library
+routines, brute force on tiny inputs, special cases and invariants.
+
+Pages cited: "Agentic shootout -- Atlas x Flash-Next research" (reports
+"Flash-Next support: vLLM vs Atlas" (a)6, "PR 16 review ... (Claude's
+review)" (a), "Flash-Next support: llama.cpp vs Atlas" (a)3) and "Atlas
+Flash-Next defect investigations" (Report A Defect 1, Report P Defect 5).
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import qsa_oracle as O
+from tests.conftest import read_golden_table
+
+pytestmark = pytest.mark.filterwarnings("ignore::DeprecationWarning")
+
+
+def bf16(vals):
+    """bf16 bit patterns of values, via torch's own fp32 -> bf16 conversion."""
+    t = torch.as_tensor(np.asarray(vals, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().astype(np.uint16)
+
+
+def state_from_raw(raw, ratio, idx_dim, capacity=None):
+    raw = np.asarray(raw, np.float32).reshape(-1, idx_dim)
+    n = raw.shape[0]
+    st = O.SeqState(ratio, 1, 4, idx_dim, capacity or max(n, 4))
+    z = np.zeros((n, 1, 4), np.uint16)
+    st.append(0, z, z, bf16(raw))
+    return st
+
+
+# ---------------------------------------------------------------------------
+# bf16 rounding: library routine + hand cases
+# ---------------------------------------------------------------------------
+
+def test_bf16_rounding_matches_torch_on_fp32_values():
+    rng = np.random.default_rng(1)
+    bits = rng.integers(0, 2**32, size=200000, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    ref = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    got = O.f64_to_bf16_bits(x.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_rounding_hand_cases():
+    # spacing at 1.0 is 2^-7: 1 + 2^-8 is a tie -> even (1.0);
+    # 1 + 3*2^-8 is a tie between 1+2^-7 (odd) and 1+2^-6 (even) -> 1+2^-6
+    assert O.round_bf16(1 + 2**-8) == 1.0
+    assert O.round_bf16(1 + 3 * 2**-8) == 1 + 2**-6
+    assert O.round_bf16(1 + 2**-8 + 2**-30) == 1 + 2**-7     # above the tie
+    assert O.round_bf16(-(1 + 2**-8)) == -1.0
+    # fp64-only information must not be lost to a double rounding via fp32:
+    # 1 + 2^-8 + 2^-40 rounds up in one step, but to 1.0 through fp32
+    assert O.round_bf16(1 + 2**-8 + 2**-40) == 1 + 2**-7
+    assert math.isinf(O.round_bf16(2.0**128 * 0.9999999))
+    assert O.round_bf16(2.0**-133) == 2.0**-133               # smallest subnormal
+    assert O.round_bf16(2.0**-135) == 0.0
+
+
+# ---------------------------------------------------------------------------
+# Pooling
+# ---------------------------------------------------------------------------
+
+def test_pool_hand_cases(golden_cases):
+    c = golden_cases["pool_round"]
+    raw = bf16(np.array(c["raw"]).reshape(-1, 1))
+    assert O.bf16_bits_to_f64(O.pool_block(raw))[0] == c["blk"][0][0]
+    raw = bf16(np.array([[1.0], [2.0], [3.0], [5.0]]))       # 11/4 exact
+    assert O.bf16_bits_to_f64(O.pool_block(raw))[0] == 2.75
+
+
+def test_worked_example_blocks(golden_cases):
+    for name in ("select", "tie"):
+        c = golden_cases[name]
+        r = int(c["ratio"][0][0])
+        st = state_from_raw(c["raw"], r, 2)
+        assert st.n_blocks == len(c["blk"])
+        got = O.bf16_bits_to_f64(st.idx_blk[: st.n_blocks])
+        assert np.array_equal(got, np.array(c["blk"]))
+
+
+def test_pool_of_integer_keys_is_exact():
+    # ratio 4, integer keys in [-8, 8]: every mean is a multiple of 1/4 with
+    # magnitude <= 8, exact in bf16, so the pooled key equals the exact mean
+    rng = np.random.default_rng(3)
+    raw = rng.integers(-8, 9, size=(64, 32)).astype(np.float64)
+    st = state_from_raw(raw, 4, 32)
+    exact = raw.reshape(16, 4, 32).mean(axis=1)
+    assert np.array_equal(O.bf16_bits_to_f64(st.idx_blk[:16]), exact)
+
+
+# ---------------------------------------------------------------------------
+# Scores
+# ---------------------------------------------------------------------------
+
+def test_worked_example_scores_and_selection(golden_cases):
+    for name in ("select", "tie"):
+        c = golden_cases[name]
+        r = int(c["ratio"][0][0])
+        K = int(c["budget"][0][0]) // r
+        st = state_from_raw(c["raw"], r, 2)
+        s = O.block_scores(bf16(c["q_idx"]), np.array(c["w"][0]), st.idx_blk[: st.n_blocks])
+        assert np.array_equal(s, np.array(c["scores"][0]))
+        sel = O.select_blocks(s, K)
+        assert sel.tolist() == [int(v) for v in c["sel"][0]]
+        toks = O.token_set(sel, st.n_blocks, int(c["visible"][0][0]), r)
+        assert toks.tolist() == [int(v) for v in c["tokens"][0]]
+
+
+def test_score_closed_forms():
+    e0 = np.zeros(8); e0[0] = 1
+    k = np.array([[3, -1, 2, 0, 0, 0, 0, 5], [-4, 1, 1, 1, 1, 1, 1, 1]], np.float64)
+    # one head, unit query: score = max(0, k[0])
+    s = O.block_scores(bf16([e0]), [1.0], bf16(k))
+    assert s.tolist() == [3.0, 0.0]
+    # two heads, w = (0.5, 2): head 0 reads dim 0, head 1 reads dim 7
+    e7 = np.zeros(8); e7[7] = 1
+    s = O.block_scores(bf16([e0, e7]), [0.5, 2.0], bf16(k))
+    assert s.tolist() == [0.5 * 3 + 2 * 5, 0.5 * 0 + 2 * 1]
+    # the ReLU acts per head, before the weighted head sum: a negative head
+    # cannot cancel a positive one
+    s = O.block_scores(bf16([e0, -e0]), [1.0, 1.0], bf16(k))
+    assert s.tolist() == [3.0, 4.0]
+
+
+def test_score_invariants():
+    rng = np.random.default_rng(5)
+    q = rng.integers(-8, 9, size=(6, 16)).astype(np.float64)
+    k = rng.integers(-8, 9, size=(40, 16)).astype(np.float64)
+    w = 2.0 ** rng.integers(-2, 2, size=6)
+    s = O.block_scores(bf16(q), w, bf16(k))
+    perm = rng.permutation(6)
+    assert np.array_equal(O.block_scores(bf16(q[perm]), w[perm], bf16(k)), s)
+    assert np.array_equal(O.block_scores(bf16(q), 2 * w, bf16(k)), 2 * s)
+    # w == 1 (weight-free) equals the sum of per-head ReLU dots
+    s1 = O.block_scores(bf16(q), np.ones(6), bf16(k))
+    brute = [sum(max(0.0, float(np.dot(q[h], k[b]))) for h in range(6)) for b in range(40)]
+    assert s1.tolist() == brute
+
+
+# ---------------------------------------------------------------------------
+# Selection
+# ---------------------------------------------------------------------------
+
+def brute_topk(scores, K):
+    idx = sorted(range(len(scores)), key=lambda b: (-scores[b], b))
+    return sorted(idx[:K]) if len(scores) > K else list(range(len(scores)))
+
+
+def test_selection_brute_force_with_ties():
+    rng = np.random.default_rng(7)
+    for trial in range(300):
+        n = int(rng.integers(1, 64))
+        K = int(rng.integers(1, 20))
+        H = int(rng.integers(1, 5))
+        q = rng.integers(-1, 2, size=(H, 4)).astype(np.float64)
+        k = rng.integers(-1, 2, size=(n, 4)).astype(np.float64)
+        s = O.block_scores(bf16(q), np.ones(H), bf16(k))
+        assert O.select_blocks(s, K).tolist() == brute_topk(s.tolist(), K)
+
+
+def test_selection_special_cases():
+    K = 5
+    assert O.select_blocks(np.full(12, 3.5), K).tolist() == [0, 1, 2, 3, 4]
+    assert O.select_blocks(np.zeros(12), K).tolist() == [0, 1, 2, 3, 4]
+    assert O.select_blocks(np.arange(12.0), K).tolist() == [7, 8, 9, 10, 11]
+    assert O.select_blocks(np.arange(12.0)[::-1].copy(), K).tolist() == [0, 1, 2, 3, 4]
+    assert O.select_blocks(np.arange(3.0), K).tolist() == [0, 1, 2]   # n <= K
+    # all heads ReLU'd to zero -> all scores 0 -> the first K blocks
+    q = -np.ones((2, 4)); k = np.ones((9, 4))
+    s = O.block_scores(bf16(q), [1.0, 1.0], bf16(k))
+    assert O.select_blocks(s, 3).tolist() == [0, 1, 2]
+
+
+def test_raising_an_unselected_block_enters_the_set():
+    rng = np.random.default_rng(11)
+    s = rng.permutation(50).astype(np.float64)       # distinct scores
+    K = 8
+    sel = O.select_blocks(s, K)
+    out = next(b for b in range(50) if b not in sel)
+    weakest = min(sel, key=lambda b: s[b])
+    s2 = s.copy(); s2[out] = s[sel].max() + 1
+    sel2 = O.select_blocks(s2, K)
+    assert out in sel2 and weakest not in sel2
+    assert set(sel2) == (set(sel) - {weakest}) | {out}
+
+
+# ---------------------------------------------------------------------------
+# Inert bound and token set (values printed on the pages)
+# ---------------------------------------------------------------------------
+
+def test_inert_bound_from_pages():
+    for budget, ratio, topk, bound, width in [[int(v) for v in row] for row in read_golden_table("inert_bound.txt")]:
+        assert budget // ratio == topk
+        # visible == bound: every complete block fits in the budget -> dense
+        n_blk = bound // ratio
+        assert n_blk <= topk
+        sel = O.select_blocks(np.arange(float(n_blk)), topk)
+        toks = O.token_set(sel, n_blk, bound, ratio)
+        assert toks.tolist() == list(range(bound))
+        # visible == bound + 1: one block too many -> selection active
+        n_blk = (bound + 1) // ratio
+        assert n_blk == topk + 1
+        sel = O.select_blocks(np.arange(float(n_blk)), topk)
+        assert len(sel) == topk and 0 not in sel
+        # the widest token set is K * ratio + (ratio - 1) = the buffer width
+        worst = max(len(O.token_set(np.arange(min(v // ratio, topk)), v // ratio, v, ratio))
+                    for v in range(bound - 8, bound + 40))
+        assert worst == width
+
+
+def test_indexer_memory_from_pages():
+    for tokens, d, ratio, raw_b, blk_b, total_mb in read_golden_table("indexer_memory.txt"):
+        st = O.SeqState(int(ratio), 1, 4, int(d), int(tokens))
+        assert st.idx_raw.nbytes == int(raw_b)
+        assert st.idx_blk.nbytes == int(blk_b)
+        assert round((st.idx_raw.nbytes + st.idx_blk.nbytes) / 1e6, 1) == float(total_mb)
+
+
+# ---------------------------------------------------------------------------
+# Attention
+# ---------------------------------------------------------------------------
+
+def test_worked_example_attention(golden_cases):
+    c = golden_cases["attend"]
+    q = bf16(c["q"])
+    k = bf16(np.array(c["k"]).reshape(2, 1, 4))
+    v = bf16(np.array(c["v"]).reshape(2, 1, 4))
+    out = O.gqa_attention(q, k, v)
+    assert np.allclose(out[0], c["out"][0], rtol=0, atol=1e-15)
+    assert O.bf16_bits_to_f64(O.f64_to_bf16_bits(out))[0].tolist() == c["out_bf16"][0]
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(13)
+    D = 16
+    q = bf16(rng.standard_normal((4, D)))
+    # one token: the output is that token's V row of the head's group
+    k = bf16(rng.standard_normal((1, 2, D))); v = bf16(rng.standard_normal((1, 2, D)))
+    out = O.gqa_attention(q, k, v)
+    vv = O.bf16_bits_to_f64(v)
+    assert np.array_equal(out, vv[0][[0, 0, 1, 1]])
+    # all V rows equal: the output is that row whatever the weights
+    k = bf16(rng.standard_normal((9, 2, D)))
+    row = rng.standard_normal((2, D))
+    v = bf16(np.broadcast_to(row, (9, 2, D)))
+    out = O.gqa_attention(q, k, v)
+    assert np.allclose(out, O.bf16_bits_to_f64(v)[0][[0, 0, 1, 1]], atol=1e-14)
+    # q == 0: uniform weights -> the mean of the V rows
+    v = bf16(rng.standard_normal((9, 2, D)))
+    out = O.gqa_attention(bf16(np.zeros((4, D))), k, v)
+    vv = O.bf16_bits_to_f64(v)
+    assert np.allclose(out, vv.mean(axis=0)[[0, 0, 1, 1]], atol=1e-14)
+
+
+def test_attention_textbook_single_head():
+    # Hq = Hkv = 1: out = sum_t softmax(q.k_t / sqrt(D))_t v_t, written out
+    rng = np.random.default_rng(17)
+    D, T = 8, 5
+    q = rng.standard_normal(D); k = rng.standard_normal((T, D)); v = rng.standard_normal((T, D))
+    qb, kb, vb = bf16([q]), bf16(k.reshape(T, 1, D)), bf16(v.reshape(T, 1, D))
+    qv, kv, vv = (O.bf16_bits_to_f64(x) for x in (qb, kb, vb))
+    e = [math.exp(float(np.dot(qv[0], kv[t, 0])) / math.sqrt(D)) for t in range(T)]
+    want = sum(e[t] * vv[t, 0] for t in range(T)) / sum(e)
+    assert np.allclose(O.gqa_attention(qb, kb, vb)[0], want, atol=1e-13)
+
+
+def test_gqa_head_mapping_contiguous_groups():
+    # Hq = 4, Hkv = 2: heads 0,1 -> kv 0 and heads 2,3 -> kv 1
+    D = 8
+    k = bf16(np.zeros((3, 2, D)))
+    v = np.zeros((3, 2, D)); v[:, 0, :] = 1.0; v[:, 1, :] = -2.0
+    out = O.gqa_attention(bf16(np.ones((4, D))), k, bf16(v))
+    assert out[:, 0].tolist() == [1.0, 1.0, -2.0, -2.0]
+    assert [O.kv_head_of(h, 32, 4) for h in (0, 7, 8, 31)] == [0, 0, 1, 3]
+
+
+def make_state(rng, n, ratio=4, hkv=2, D=16, dI=8, cap=None):
+    st = O.SeqState(ratio, hkv, D, dI, cap or n + 16)
+    st.append(0, bf16(rng.standard_normal((n, hkv, D))), bf16(rng.standard_normal((n, hkv, D))),
+              bf16(rng.integers(-8, 9, size=(n, dI))))
+    return st
+
+
+def test_dense_identity_at_and_below_inert_bound():
+    rng = np.random.default_rng(19)
+    ratio, budget = 4, 32
+    bound = budget + ratio - 1
+    st = make_state(rng, bound + 5, ratio)
+    for V in (17, 1, 2, 3, 4, 5, bound - 1, bound):
+        q = bf16(rng.standard_normal((4, 16)))
+        qi = bf16(rng.integers(-8, 9, size=(3, 8))); w = np.ones(3)
+        res = O.attend_row(st, V - 1, qi, w, q, budget // ratio)
+        assert res["tokens"].tolist() == list(range(V))
+        dense = O.dense_attention(q, st.K[:V], st.V[:V], 2)
+        assert np.max(np.abs(res["out"] - dense)) <= 1e-12
+    # one past the bound: selection is active and drops exactly one block
+    res = O.attend_row(st, bound, qi, w, q, budget // ratio)
+    assert res["n_blk"] == budget // ratio + 1 and len(res["sel"]) == budget // ratio
+    assert len(res["tokens"]) == budget
+
+
+def test_ablation_of_unselected_tokens():
+    rng = np.random.default_rng(23)
+    ratio, topk = 4, 4
+    st = make_state(rng, 61, ratio)
+    q = bf16(rng.standard_normal((4, 16)))
+    qi = bf16(rng.integers(-8, 9, size=(3, 8))); w = np.array([1.0, 0.5, 2.0])
+    res = O.attend_row(st, 60, qi, w, q, topk)
+    unsel = np.setdiff1d(np.arange(61), res["tokens"])
+    assert len(unsel) > 0
+    st.K[unsel] = bf16(rng.standard_normal((len(unsel), 2, 16)))
+    st.V[unsel] = bf16(rng.standard_normal((len(unsel), 2, 16)))
+    res2 = O.attend_row(st, 60, qi, w, q, topk)
+    assert np.array_equal(res2["out"], res["out"])
+    t = res["tokens"][0]
+    st.V[t] = bf16(rng.standard_normal((2, 16)))
+    res3 = O.attend_row(st, 60, qi, w, q, topk)
+    assert not np.array_equal(res3["out"], res["out"])
+
+
+# ---------------------------------------------------------------------------
+# State: append / rewind / chunking / counters
+# ---------------------------------------------------------------------------
+
+def rows(rng, n, hkv=2, D=16, dI=8):
+    return (bf16(rng.standard_normal((n, hkv, D))), bf16(rng.standard_normal((n, hkv, D))),
+            bf16(rng.integers(-8, 9, size=(n, dI))))
+
+
+def same_state(a, b):
+    n = a.ingested
+    return (a.ingested == b.ingested and np.array_equal(a.K[:n], b.K[:n])
+            and np.array_equal(a.V[:n], b.V[:n]) and np.array_equal(a.idx_raw[:n], b.idx_raw[:n])
+            and np.array_equal(a.idx_blk[: a.n_blocks], b.idx_blk[: b.n_blocks]))
+
+
+def test_chunked_and_token_by_token_append_agree():
+    rng = np.random.default_rng(29)
+    k, v, i = rows(rng, 37)
+    one = O.SeqState(4, 2, 16, 8, 64); one.append(0, k, v, i)
+    chunks = O.SeqState(4, 2, 16, 8, 64)
+    for a, b in ((0, 5), (5, 6), (6, 20), (20, 37)):
+        chunks.append(a, k[a:b], v[a:b], i[a:b])
+    tok = O.SeqState(4, 2, 16, 8, 64)
+    for t in range(37):
+        tok.append(t, k[t:t + 1], v[t:t + 1], i[t:t + 1])
+    assert same_state(one, chunks) and same_state(one, tok)
+    assert one.n_blocks == 9
+
+
+def test_rewind_then_reappend_equals_never_drafting():
+    rng = np.random.default_rng(31)
+    k, v, i = rows(rng, 30)
+    dk, dv, di = rows(rng, 3)
+    ref = O.SeqState(4, 2, 16, 8, 64); ref.append(0, k, v, i)
+    st = O.SeqState(4, 2, 16, 8, 64); st.append(0, k[:27], v[:27], i[:27])
+    st.append(27, dk, dv, di)          # three draft tokens complete block 6 (tokens 24..27)
+    st.rewind(3)
+    assert st.ingested == 27 and st.n_blocks == 6
+    st.append(27, k[27:], v[27:], i[27:])
+    assert same_state(st, ref)
+    # the re-completed block 6 was pooled from the new raw rows
+    assert np.array_equal(st.idx_blk[6], O.pool_block(i[24:28]))
+    assert not np.array_equal(O.pool_block(np.concatenate([i[24:27], di[:1]])), st.idx_blk[6])
+
+
+def test_counter_discipline():
+    rng = np.random.default_rng(37)
+    k, v, i = rows(rng, 8)
+    st = O.SeqState(4, 2, 16, 8, 10)
+    st.append(0, k[:4], v[:4], i[:4])
+    assert st.ingested == 4
+    with pytest.raises(O.DesyncError):
+        st.append(5, k[4:5], v[4:5], i[4:5])       # pos != ingested
+    with pytest.raises(O.DesyncError):
+        st.append(3, k[4:5], v[4:5], i[4:5])
+    with pytest.raises(O.CapacityError):
+        st.append(4, np.concatenate([k, k[:1]]), np.concatenate([v, v[:1]]), np.concatenate([i, i[:1]]))
+    with pytest.raises(ValueError):
+        st.rewind(5)
+    st.rewind(4)
+    assert st.ingested == 0 and st.n_blocks == 0
+
+
+def test_verify_rows_are_causal():
+    # three rows appended together; row j sees pos0 + j + 1 tokens
+    rng = np.random.default_rng(41)
+    st = make_state(rng, 38, 4)                     # 38 tokens already cached
+    k, v, i = rows(rng, 3)
+    st.append(38, k, v, i)
+    q = bf16(rng.standard_normal((4, 16)))
+    qi = bf16(rng.integers(-8, 9, size=(3, 8))); w = np.ones(3)
+    for j in range(3):
+        res = O.attend_row(st, 38 + j, qi, w, q, 4)
+        assert res["tokens"].max() == 38 + j
+        assert res["n_blk"] == (38 + j + 1) // 4
