@@ -1,0 +1,599 @@
+#!/usr/bin/env python
+"""Benchmark of indexer-selected sparse attention decode on GB300.
+
+Workload: steady-state decode, batch 32, each sequence with a 32768-token
+prefix, ratio 4, budget 2048 (K = 512 blocks, inert bound 2051), indexer
+64 heads x 128, main attention 32 q / 4 kv heads x 128, bf16 paged KV (64-token
+pages, randomly permuted page table). One step = one fused qsa_decode call
+(append, index score, top-K select, gather attention, split merge, counter
+commit) for the 32 rows, replayed as a CUDA graph.
+
+L2: six independent batches of 32 sequences rotate step by step, so the
+202 MB a step reads come from HBM (1.2 GB between two uses of a batch, L2 is
+129 MB). Positions advance on the device each step; prefixes start below
+32768 so that the mean prefix over the run is 32768.
+
+One JSON line (rank 0): value = query rows/s over all ranks; roofline of the
+dominant kernel (per-stage CUDA-event timing); e2e through host buffers;
+cpu_baseline = the CPU oracle on a bounded sample; nvidia-smi clocks sampled
+during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode query-rows/sec and achieved HBM GB/s (% of roofline) at batch×prefix"
+WORKLOAD_ID = 2            # steady-state decode, batch 32 x 32k prefix
+N_BATCHES = 6              # default rotating independent batches (L2 defeat)
+KERNELS_PER_STEP = 6       # append, score, select, attention, merge, commit
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=30)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--breakdown-steps", type=int, default=600)
+    ap.add_argument("--e2e-steps", type=int, default=600)
+    ap.add_argument("--oracle-rows", type=int, default=64, help="rows per CPU worker in the cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--n-batches", type=int, default=N_BATCHES,
+                    help="rotating batches of 32 sequences (fewer: smaller device footprint, for profiling)")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes / flops (per row), from the method's definition
+# ---------------------------------------------------------------------------
+
+def row_work(sh, visible):
+    n_blk = visible // sh.ratio
+    tail = visible - n_blk * sh.ratio
+    active = n_blk > sh.topk
+    n_tok = min(n_blk, sh.topk) * sh.ratio + tail
+    score_b = (n_blk * sh.idx_dim * 2 + sh.n_idx_heads * sh.idx_dim * 2 + 4 * sh.n_idx_heads) if active else 0
+    attn_b = n_tok * sh.n_kv_heads * sh.head_dim * 2 * 2 + 2 * sh.n_q_heads * sh.head_dim * 2
+    append_b = (2 * sh.n_kv_heads * sh.head_dim + sh.idx_dim) * 2
+    score_f = 2 * sh.n_idx_heads * sh.idx_dim * n_blk if active else 0
+    attn_f = 4 * sh.n_q_heads * sh.head_dim * n_tok
+    return dict(score_bytes=score_b, attn_bytes=attn_b, append_bytes=append_b,
+                score_flops=score_f, attn_flops=attn_f, n_tok=n_tok, n_blk=n_blk)
+
+
+def sum_work(sh, visibles):
+    tot = {}
+    for v in visibles:
+        for k, x in row_work(sh, v).items():
+            tot[k] = tot.get(k, 0) + x
+    return tot
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self, t0, t1):
+        """Samples whose host timestamp falls in [t0, t1] (wall clock)."""
+        import datetime
+        sm, mx, reasons, n_all = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 10:
+                continue
+            n_all += 1
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            if not (t0 - 0.05 <= ts <= t1 + 0.05):
+                continue
+            try:
+                sm.append(float(parts[2])); mx.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[6:10]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_total": n_all}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def traffic_for(kernel_key):
+    """ncu DRAM bytes per launch for a kernel, if the committed counters were
+    taken on the kernel source as it is now."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(kernel_key)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, ent["source"])
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if h != ent.get("sha256"):
+        return None
+    return ent["bytes_per_launch_full_size"]
+
+
+def run_gpu(args):
+    import torch
+
+    from indexer_selected_sparse_gb300 import qsa as Q
+    from indexer_selected_sparse_gb300 import synth as S
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    NB = args.n_batches
+    wl = S.workload(WORKLOAD_ID)
+    sh = wl.shapes
+    cfg = Q.Config.of(sh)
+    B = wl.n_seq
+    K, W = args.steps, args.warmup
+    total_steps = W + K + args.breakdown_steps + args.e2e_steps + 4
+    adv_per_batch = math.ceil((W + K + args.e2e_steps + 4) / NB)
+    # center the prefixes of the main timed region on 32768
+    start = wl.prefixes[0] - W // NB - K // (2 * NB)
+    start = max(start, 8)
+    n_slots = B * NB
+    P = sh.page_size
+    max_pages = math.ceil((start + adv_per_batch + 8) / P)
+    pt = S.page_table(wl.seed + 1000 * rank, n_slots, max_pages, contiguous=False)
+    cache = Q.PagedCache(cfg, pt, n_slots * max_pages, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    # prefix: every sequence filled through the library's own append
+    t_setup = time.time()
+    chunk = 8192
+    for s in range(n_slots):
+        a = 0
+        while a < start:
+            m = min(chunk, start - a)
+            k, v, ix = S.token_rows(sh, wl.seed, s, torch.arange(a, a + m), device=dev)
+            rows = Q.Rows(torch.tensor([s], device=dev), torch.tensor([a], device=dev, dtype=torch.int32), m)
+            Q.qsa_append(cfg, rows, cache, k, v, ix, status)
+            a += m
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, Q.qsa_strerror(int(status.item()))
+    setup_s = time.time() - t_setup
+
+    # per batch: step inputs (one set per batch, re-appended at advancing positions)
+    ws = Q.workspace(cfg, B, cache.max_blocks, device=dev)
+    batches = []
+    for b in range(NB):
+        ids = torch.arange(b * B, (b + 1) * B, dtype=torch.int32, device=dev)
+        pos0 = torch.full((B,), start, dtype=torch.int32, device=dev)
+        ks, vs, iis, qs, qis, wss = [], [], [], [], [], []
+        for s in range(b * B, (b + 1) * B):
+            k, v, ix = S.token_rows(sh, wl.seed, s, torch.tensor([start]), device=dev)
+            q, qi, w = S.query_rows(sh, wl.seed, s, torch.tensor([start]), device=dev)
+            ks.append(k); vs.append(v); iis.append(ix); qs.append(q); qis.append(qi); wss.append(w)
+        cat = lambda xs: torch.cat(xs).contiguous()
+        batches.append(dict(ids=ids, pos0=pos0, k=cat(ks), v=cat(vs), idx=cat(iis), q=cat(qs),
+                            q_idx=cat(qis), w=cat(wss),
+                            out=torch.empty(B, sh.n_q_heads, sh.head_dim, dtype=torch.bfloat16, device=dev)))
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def decode_call(bt, advance=True):
+        rows = Q.Rows(bt["ids"], bt["pos0"], 1, advance=advance)
+        Q.qsa_decode(cfg, rows, cache, bt["k"], bt["v"], bt["idx"], bt["q_idx"], bt["w"], bt["q"],
+                     bt["out"], ws, status)
+
+    graphs = []
+    for bt in batches:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            decode_call(bt)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    # host-side mirror of the positions (for the exact algorithmic bytes)
+    hpos = [start] * NB
+
+    def replay(i):
+        graphs[i % NB].replay()
+        hpos[i % NB] += 1
+
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            replay(i)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, Q.qsa_strerror(int(status.item()))
+
+    # ---- timed region: K fused steps
+    # exact visible counts of every row of every timed step
+    sim = list(hpos)
+    visibles = []
+    for i in range(W, W + K):
+        b = i % NB
+        visibles += [sim[b] + 1] * B
+        sim[b] += 1
+    vis_dev = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    smi_id = vis_dev.split(",")[local].strip() if vis_dev else str(local)
+    clk = ClockSampler(smi_id)
+    time.sleep(0.5)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(W, W + K):
+            replay(i)
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    clk.stop()
+    clocks = clk.summary(t0, t1)
+    ms = ev0.elapsed_time(ev1) / K
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    st = int(status.item())
+    assert st == 0, f"device status {st}: {Q.qsa_strerror(st)}"
+    rows_per_step = B * world
+    value = rows_per_step / (ms * 1e-3)
+    work = sum_work(sh, visibles)
+    step_bytes = (work["score_bytes"] + work["attn_bytes"] + work["append_bytes"]) / K
+    hbm_gbs, tf_peak, peak_kind = measured_peaks()
+    step_gbs = step_bytes / (ms * 1e-3) / 1e9
+
+    # ---- per-stage timing (same workload, stage entry points, events between)
+    roofline, stage_ms, stage_bytes, stage_flops = None, {}, {}, {}
+    if args.breakdown_steps > 0:
+        roofline, stage_ms, stage_bytes, stage_flops = stage_breakdown(
+            args, Q, torch, cfg, sh, cache, batches, ws, status, stream, hpos, NB, B, hbm_gbs, peak_kind)
+
+    out_e2e = run_e2e(args, Q, torch, cfg, cache, batches, ws, status, stream, NB, B, rows_per_step,
+                      decode_call, dist, dev)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return make_line(wl, sh, B, K, W, world, value, ms, visibles, step_bytes, step_gbs, hbm_gbs, NB,
+                     roofline, stage_ms, stage_bytes, stage_flops, out_e2e, clocks, setup_s), rank, world
+
+
+def stage_breakdown(args, Q, torch, cfg, sh, cache, batches, ws, status, stream, hpos, NB, B, hbm_gbs,
+                    peak_kind):
+    dev = cache.k_pool.device
+    ld = (cache.max_blocks + 3) // 4 * 4
+    scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
+    sel = torch.empty(B, cfg.topk, dtype=torch.int32, device=dev)
+    nsel = torch.empty(B, dtype=torch.int32, device=dev)
+    one = torch.ones(B, dtype=torch.int32, device=dev)
+    stage_graphs = []
+    for bt in batches:
+        rows = Q.Rows(bt["ids"], bt["pos0"], 1)
+        gs = []
+        for fn in (lambda: Q.qsa_append(cfg, rows, cache, bt["k"], bt["v"], bt["idx"], status),
+                   lambda: Q.qsa_index_score(cfg, rows, cache, bt["q_idx"], bt["w"], scores, ld, status),
+                   lambda: Q.qsa_topk_select(cfg, rows, scores, ld, sel, nsel, status),
+                   lambda: Q.qsa_gather_attn(cfg, rows, cache, bt["q"], sel, nsel, bt["out"], ws, status),
+                   lambda: Q.qsa_rewind(cfg, bt["ids"], one, cache.ingested, status)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            gs.append(g)
+        stage_graphs.append(gs)
+    torch.cuda.synchronize()
+    KB = args.breakdown_steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(KB)]
+    with torch.cuda.stream(stream):
+        for i in range(KB):
+            gs = stage_graphs[i % NB]
+            e = evs[i]
+            for j in range(4):
+                e[j].record(stream)
+                gs[j].replay()
+            e[4].record(stream)
+            gs[4].replay()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, Q.qsa_strerror(int(status.item()))
+    names = ["append", "index_score", "topk_select", "gather_attn"]
+    stage_ms = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(KB)) / KB for j, n in enumerate(names)}
+    bvis = []
+    for i in range(KB):
+        bvis += [hpos[i % NB] + 1] * B
+    bw = sum_work(sh, bvis)
+    stage_bytes = {"append": bw["append_bytes"] / KB, "index_score": bw["score_bytes"] / KB,
+                   "gather_attn": bw["attn_bytes"] / KB, "topk_select": 0}
+    stage_flops = {"index_score": bw["score_flops"] / KB, "gather_attn": bw["attn_flops"] / KB}
+    dominant = max(stage_ms, key=lambda n: stage_ms[n])
+    if dominant == "topk_select":
+        dominant = "gather_attn" if stage_ms["gather_attn"] >= stage_ms["index_score"] else "index_score"
+    ach = stage_bytes[dominant] / (stage_ms[dominant] * 1e-3) / 1e9
+    roofline = {"kernel": {"gather_attn": "attn_kernel<4> + merge_kernel", "index_score": "score_kernel<128,64>",
+                           "append": "append_kernel"}[dominant],
+                "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_gbs, "unit": "GB/s",
+                "frac": round(ach / hbm_gbs, 4), "peak_kind": peak_kind + " (hbm_gbs, copy)",
+                "traffic": traffic_for(dominant),
+                "algorithmic_bytes_per_launch": int(stage_bytes[dominant]),
+                "launch_ms": round(stage_ms[dominant], 5)}
+    return roofline, stage_ms, stage_bytes, stage_flops
+
+
+def run_e2e(args, Q, torch, cfg, cache, batches, ws, status, stream, NB, B, rows_per_step, decode_call,
+            dist, dev):
+    # ---- end to end: host buffers, H2D inputs + fused step + D2H output per step
+    e2e = None
+    KE = args.e2e_steps
+    if KE > 0:
+        host = []
+        e2e_graphs = []
+        for bt in batches:
+            hb = {k: bt[k].cpu().pin_memory() for k in ("k", "v", "idx", "q_idx", "w", "q")}
+            hb["out"] = torch.empty_like(bt["out"], device="cpu").pin_memory()
+            host.append(hb)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for k in ("k", "v", "idx", "q_idx", "w", "q"):
+                    bt[k].copy_(hb[k], non_blocking=True)
+                decode_call(bt)
+                hb["out"].copy_(bt["out"], non_blocking=True)
+            e2e_graphs.append(g)
+        torch.cuda.synchronize()
+        h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in ("k", "v", "idx", "q_idx", "w", "q"))
+        d2h = host[0]["out"].numel() * host[0]["out"].element_size()
+        e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(KE):
+                e2e_graphs[i % NB].replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1) / KE
+        if dist is not None:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        assert int(status.item()) == 0, Q.qsa_strerror(int(status.item()))
+        e2e = {"value": round(rows_per_step / (ems * 1e-3), 1), "unit": "rows/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ems, 5),
+               "path": "pinned host inputs -> H2D -> qsa_decode -> D2H output, per step (CUDA graph)"}
+    return e2e
+
+
+def make_line(wl, sh, B, K, W, world, value, ms, visibles, step_bytes, step_gbs, hbm_gbs, NB,
+              roofline, stage_ms, stage_bytes, stage_flops, e2e, clocks, setup_s):
+    vmin, vmax = min(visibles), max(visibles)
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": B, "prefix": wl.prefixes[0],
+                   "prefix_range_timed": [vmin - 1, vmax - 1],
+                   "mean_prefix_timed": round(sum(visibles) / len(visibles) - 1, 1),
+                   "ratio": sh.ratio, "budget": sh.budget, "topk": sh.topk, "idx_heads": sh.n_idx_heads,
+                   "idx_dim": sh.idx_dim, "q_heads": sh.n_q_heads, "kv_heads": sh.n_kv_heads,
+                   "head_dim": sh.head_dim, "page_size": sh.page_size,
+                   "l2": f"inputs larger than L2: {NB} rotating batches of {B} sequences, "
+                         f"{step_bytes / 1e6:.1f} MB per step, {NB * step_bytes / 1e9:.2f} GB per rotation",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "graph": "one CUDA graph per batch, positions advanced on the device"},
+        "achieved_gbs": round(step_gbs, 1),
+        "hbm_roofline_frac": round(step_gbs / hbm_gbs, 4),
+        "roofline": roofline,
+        "stages_ms": {k: round(v, 5) for k, v in stage_ms.items()},
+        "stages_gbs": {k: round(stage_bytes[k] / (stage_ms[k] * 1e-3) / 1e9, 1) for k in stage_ms if stage_bytes.get(k)},
+        "stages_tflops": {k: round(stage_flops[k] / (stage_ms[k] * 1e-3) / 1e12, 1) for k in stage_flops},
+        "e2e": e2e,
+        "gpu_launches": KERNELS_PER_STEP * K,
+        "clocks": clocks,
+        "setup_s": round(setup_s, 1),
+    }
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+
+def _oracle_worker(job):
+    """Runs in a spawned process: builds one sequence's oracle state at the
+    workload's prefix from the seeded generator (untimed), then times `rows`
+    decode rows (append the token, score, select, attend, then rewind so every
+    row sees the same prefix)."""
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["OMP_NUM_THREADS"] = "1"
+    os.environ["MKL_NUM_THREADS"] = "1"
+    import numpy as np
+    import torch
+    torch.set_num_threads(1)
+    from indexer_selected_sparse_gb300 import synth as S
+    from oracle import qsa_oracle as O
+
+    seq, prefix, n_warm, n_rows, wl_id = job
+    wl = S.workload(wl_id)
+    sh = wl.shapes
+
+    def b(t):
+        return t.contiguous().view(torch.int16).numpy().astype(np.uint16)
+
+    # index keys for every position; K/V rows only where the row attends (the
+    # row is the same every time, so its token set is fixed): the oracle's
+    # state holds zeros for K/V rows it never reads
+    pos = torch.arange(prefix + 1)
+    _, _, ix = S.token_rows(S.Shapes(sh.ratio, sh.budget, sh.n_idx_heads, sh.idx_dim, 1, 1, 8),
+                            wl.seed, seq, pos)
+    q, qi, w = S.query_rows(sh, wl.seed, seq, pos[prefix:])
+    qb, qib, wn = b(q[0]), b(qi[0]), w[0].numpy()
+    st = O.SeqState(sh.ratio, sh.n_kv_heads, sh.head_dim, sh.idx_dim, prefix + 1)
+    z = np.zeros((prefix, sh.n_kv_heads, sh.head_dim), np.uint16)
+    st.append(0, z, z, b(ix[:prefix]))
+    kn, vn, _ = S.token_rows(sh, wl.seed, seq, pos[prefix:])
+    kb, vb, ib = b(kn), b(vn), b(ix[prefix:])
+    st.append(prefix, kb, vb, ib)
+    toks = O.attend_row(st, prefix, qib, wn, qb, sh.topk)["tokens"]
+    st.rewind(1)
+    need = torch.from_numpy(toks[toks < prefix])
+    kt, vt, _ = S.token_rows(sh, wl.seed, seq, need)
+    st.K[need.numpy()] = b(kt)
+    st.V[need.numpy()] = b(vt)
+    times = []
+    for r in range(n_warm + n_rows):
+        t0 = time.perf_counter()
+        st.append(prefix, kb, vb, ib)
+        O.attend_row(st, prefix, qib, wn, qb, sh.topk)
+        st.rewind(1)
+        t1 = time.perf_counter()
+        if r >= n_warm:
+            times.append((t0, t1))
+    return times
+
+
+def oracle_pool_run(n_workers, prefix, n_warm, rows_per_worker):
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    jobs = [(s, prefix, n_warm, rows_per_worker, WORKLOAD_ID) for s in range(n_workers)]
+    with ctx.Pool(n_workers) as pool:
+        res = pool.map(_oracle_worker, jobs)
+    return res
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for l in f:
+                if l.lower().startswith(("model name", "cpu part")):
+                    return l.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def cpu_baseline(rows_per_worker):
+    n = min(os.cpu_count() or 1, 16)
+    res = oracle_pool_run(n, 32768, 1, rows_per_worker)
+    starts = [r[0][0] for r in res]
+    ends = [r[-1][1] for r in res]
+    wall = max(ends) - min(starts)
+    rows = sum(len(r) for r in res)
+    per_row = statistics.median([t1 - t0 for r in res for (t0, t1) in r])
+    return {"value": round(rows / wall, 2), "unit": "rows/s", "cores": n, "kind": "oracle",
+            "sample": f"{n} worker processes x {rows_per_worker} decode rows each (1 BLAS thread each), "
+                      f"one sequence per worker at prefix 32768 of the batch-32 x 32k workload; "
+                      f"each row = append + score + select + attend, then rewind",
+            "single_thread_rows_per_s": round(1.0 / per_row, 2), "cpu": cpu_model()}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    n = min(os.cpu_count() or 1, 16)
+    K, W = args.steps, args.warmup
+    # a step = one decode row (of the batch's 32) on the CPU; the K steps are
+    # spread over n worker processes that run in parallel
+    res = oracle_pool_run(n, 32768, max(1, math.ceil(W / n)), math.ceil(K / n))
+    starts = [r[0][0] for r in res]
+    ends = [r[-1][1] for r in res]
+    wall = max(ends) - min(starts)
+    rows = sum(len(r) for r in res)
+    value = rows / wall
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "rows/s",
+            "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(wall / K * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "steady-decode b32 prefix32768 r4 B2048 HI64xdI128 Hq32/Hkv4",
+                       "sample": f"each step: one decode row; {rows} rows over {n} CPU worker processes"},
+            "cpu_baseline": {"value": round(value, 2), "unit": "rows/s", "cores": n, "kind": "oracle",
+                             "sample": f"{rows} decode rows at prefix 32768 over {n} workers", "cpu": cpu_model()},
+            "e2e": {"value": round(value, 2), "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    out, rank, world = run_gpu(args)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(args.oracle_rows)
+        else:
+            out["cpu_baseline"] = None
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

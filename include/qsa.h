@@ -1,0 +1,240 @@
+/*
+ * qsa.h -- C ABI of libqsa: indexer-selected (QSA-style) block-sparse attention
+ * on one GB300 (sm_103a).
+ *
+ * For every query row the path (1) scores each complete compressed block of
+ * `ratio` tokens as  s_b = sum_h w_h * max(0, q_I,h . k_I,b),  (2) keeps the
+ * K = budget/ratio best blocks (ties to the lower block index) plus the
+ * incomplete tail block, and (3) runs GQA softmax attention (scale 1/sqrt(D))
+ * over the raw K/V rows of the kept tokens, gathered from a paged cache.
+ *
+ * Sources (web pages, by title and section):
+ *   [VA6]  "Agentic shootout -- Atlas x Flash-Next research", report
+ *          "Flash-Next support: vLLM vs Atlas", (a) item 6 "QSA sparse
+ *          attention + indexer": mean-pooled compressed keys whose page table
+ *          follows the main KV cache, weight-free scoring, block top-k with
+ *          budget/ratio groups, expansion to budget + ratio - 1 token indices
+ *          (-1 padded), one opaque index -> KV update -> sparse attend step.
+ *   [PR16] same page, "PR 16 review: qwen4exp serving in Atlas (Claude's
+ *          review)", (a): relu-score top-512 + tail, inert <= 2051 visible.
+ *   [LC3]  same page, "Flash-Next support: llama.cpp vs Atlas", (a) item 3:
+ *          blocks cut the position line; the tail block is always visible.
+ *   [VP5]  same page, "Flash-Next support: vLLM vs Atlas" (d) item 10: alias
+ *          the compressed cache's page mapping to the main block table at
+ *          1/ratio density.
+ *   [INV]  "Atlas Flash-Next defect investigations", Report A: Defect 1
+ *          (decode at pos requires pos == ingested; rewind sets
+ *          ingested -= dropped), Defect 4 (16-byte alignment of every base
+ *          pointer and pitch; sticky CUDA errors are fatal), Defect 5
+ *          (capacity is checked when tokens are appended, never mid-step).
+ *
+ * Conventions for every entry point
+ *   - Pointers marked "device" are device memory owned by the caller; the
+ *     library never allocates, frees, synchronises, or copies device data to
+ *     the host. All work is enqueued on the caller's `stream`, in order.
+ *   - Tensors are dense, row-major, C-contiguous, with the shapes given.
+ *     bf16 values are passed as their 16-bit patterns (qsa_bf16).
+ *   - Every pointer that a kernel reads or writes with vector accesses
+ *     (pools, K/V/q inputs, outputs, workspace) must be 16-byte aligned.
+ *   - Every call returns a qsa_status. Host-detected problems are returned
+ *     before anything is enqueued. Problems only the device can see (a
+ *     position that does not match the ingested counter, a page id outside the
+ *     pool, a position beyond the page table) are written to the caller's
+ *     device word `*status` with an atomic first-error-wins compare-and-swap;
+ *     the caller reads it after synchronising. A non-zero status means the
+ *     outputs of that step are undefined.
+ *   - The fused step (qsa_decode) makes no host synchronisation and no
+ *     allocation, so it can be captured in a CUDA graph.
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t qsa_bf16; /* bit pattern of a bfloat16 value */
+
+typedef enum qsa_status {
+  QSA_OK = 0,
+  QSA_ERR_INVALID_ARG = 1,  /* null or misaligned pointer, bad size or stride */
+  QSA_ERR_UNSUPPORTED = 2,  /* configuration outside the supported set */
+  QSA_ERR_CAPACITY = 3,     /* append beyond the pages the table provides */
+  QSA_ERR_WORKSPACE = 4,    /* workspace smaller than qsa_workspace_bytes() */
+  QSA_ERR_CUDA = 5,         /* a launch failed (recoverable) */
+  QSA_ERR_CUDA_FATAL = 6,   /* sticky CUDA error: the context is lost */
+  QSA_ERR_DESYNC = 7,       /* device: append position != ingested counter */
+  QSA_ERR_PAGE = 8,         /* device: page id outside [0, num_pages) */
+  QSA_ERR_REWIND = 9        /* device: rewind by more than was ingested */
+} qsa_status;
+
+/* Shape of the method. Supported set (checked by qsa_config_check):
+ *   ratio      power of two in [2, 16]          tokens per compressed block
+ *   budget     multiple of ratio                token budget, K = budget/ratio
+ *   K          1 <= K <= 2048
+ *   n_idx_heads (H_I) in [1, 64]                indexer query heads
+ *   idx_dim    (d_I) 64 or 128                  indexer key/query dim
+ *   n_q_heads  (Hq), n_kv_heads (Hkv) in {1,2,4}, Hq % Hkv == 0,
+ *              Hq / Hkv <= 8                    GQA
+ *   head_dim   (D) 128
+ *   page_size  (P) 64, multiple of ratio        tokens per cache page
+ * The indexer has one key head (MQA), as the pages require. */
+typedef struct qsa_config {
+  int ratio;
+  int budget;
+  int n_idx_heads;
+  int idx_dim;
+  int n_q_heads;
+  int n_kv_heads;
+  int head_dim;
+  int page_size;
+} qsa_config;
+
+/* The query rows of one step. The step appends rows_per_seq (R) tokens to
+ * each of n_seq sequences; every appended token is a query row. Rows are
+ * sequence-major: row i*R + j is token j of sequence i, at logical position
+ * pos0[i] + j, and it sees V = pos0[i] + j + 1 tokens (its own included;
+ * rows of one sequence are causal among themselves).
+ *   decode:  R = 1;   speculative verify: R = draft rows + 1;
+ *   chunked prefill:  n_seq = 1, R = chunk length.
+ * seq_ids must be distinct within a call. */
+typedef struct qsa_rows {
+  int n_seq;
+  int rows_per_seq;
+  const int32_t *seq_ids;   /* device [n_seq]: slot in page_table / ingested */
+  int32_t *pos0;            /* device [n_seq]: position of the first row */
+  const int32_t *pos0_host; /* optional host copy of pos0 (NULL if absent);
+                               when given, capacity is checked on the host
+                               and reported as QSA_ERR_CAPACITY before any
+                               launch */
+  int advance;              /* non-zero: qsa_append / qsa_decode also add R to
+                               pos0[i] on the device when they advance the
+                               ingested counter, as the step's last action, so
+                               a step captured in a CUDA graph can be replayed
+                               for consecutive decode steps without the
+                               positions and counters drifting apart
+                               ("Agentic shootout", "PR 16 review: qwen4exp
+                               serving in Atlas", (c) item 4: the ingested
+                               counter froze at the capture step while the
+                               sequence advanced) */
+} qsa_rows;
+
+/* Paged cache of all sequences ([VA6], [VP5]). Logical token t of the
+ * sequence in slot s lives in page page_table[s][t / P] at offset t % P.
+ * Compressed block b of that sequence lives in the same page id of the block
+ * pool, at row (b % (P/ratio)): the block pool shares the main page table at
+ * 1/ratio density. All pools have num_pages pages. */
+typedef struct qsa_cache {
+  const int32_t *page_table; /* device [n_slots, max_pages] */
+  int n_slots;
+  int max_pages;             /* pages per sequence: capacity max_pages * P */
+  int num_pages;             /* pages in each pool */
+  qsa_bf16 *k_pool;          /* device [num_pages, P, Hkv, D] */
+  qsa_bf16 *v_pool;          /* device [num_pages, P, Hkv, D] */
+  qsa_bf16 *idxraw_pool;     /* device [num_pages, P, d_I]   raw index keys */
+  qsa_bf16 *idxblk_pool;     /* device [num_pages, P/ratio, d_I] block keys */
+  int32_t *ingested;         /* device [n_slots]: tokens ingested per slot */
+} qsa_cache;
+
+/* Message for a status code (static string). */
+const char *qsa_strerror(int status);
+
+/* 0 (QSA_OK) if the configuration is in the supported set above, else
+ * QSA_ERR_UNSUPPORTED (QSA_ERR_INVALID_ARG for a NULL pointer). */
+int qsa_config_check(const qsa_config *cfg);
+
+/* Bytes of workspace that qsa_decode and qsa_gather_attn need for up to
+ * max_rows query rows and up to max_blocks_per_row complete blocks per row
+ * (max_blocks_per_row >= max_pages * P / ratio covers every row). Returns 0 on
+ * an invalid configuration. */
+size_t qsa_workspace_bytes(const qsa_config *cfg, int max_rows, int max_blocks_per_row);
+
+/* Append: ingest R new tokens per sequence ([VA6] KV update + raw key store +
+ * group compress; [INV] Defect 1 counter discipline).
+ * For each sequence i (slot s = seq_ids[i]) the kernel first checks
+ * pos0[i] == ingested[s] (else QSA_ERR_DESYNC, nothing written for i) and
+ * pos0[i] + R <= max_pages * P (else QSA_ERR_CAPACITY). It then writes the
+ * tokens' K, V and raw index-key rows into the pools, pools every block the
+ * new tokens complete (k_b = bf16_rne(sum_j raw_{b*ratio+j} / ratio), fp32
+ * sum), and sets ingested[s] = pos0[i] + R.
+ *   k_new, v_new  device [n_seq*R, Hkv, D] bf16
+ *   idx_k_new     device [n_seq*R, d_I] bf16
+ *   status        device int32, see conventions */
+int qsa_append(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
+               const qsa_bf16 *k_new, const qsa_bf16 *v_new, const qsa_bf16 *idx_k_new,
+               int32_t *status, cudaStream_t stream);
+
+/* Rewind ([INV] Defect 1 fix: ingested -= dropped, pooled = ingested/ratio):
+ * for each i, ingested[seq_ids[i]] -= n_drop[i]. A negative n_drop or one
+ * larger than the ingested count leaves the counter unchanged and records
+ * QSA_ERR_REWIND. Rows past the new end become dead and are overwritten by
+ * the next append; a block made incomplete is re-pooled from its new raw rows
+ * when an append completes it again.
+ *   seq_ids, n_drop  device [n_seq] int32 */
+int qsa_rewind(const qsa_config *cfg, int n_seq, const int32_t *seq_ids, const int32_t *n_drop,
+               int32_t *ingested, int32_t *status, cudaStream_t stream);
+
+/* Index score ([PR16] relu-score, [VA6] scoring against compressed keys):
+ * for every row with n_blk = V / ratio > K complete blocks, writes
+ * scores[row * ld_scores + b] = sum_h w[row,h] * max(0, q_idx[row,h,:] . k_b)
+ * for b < n_blk (bf16 products, fp32 accumulation). Rows with n_blk <= K are
+ * skipped: every block is selected there, so no score is needed.
+ *   q_idx   device [rows, H_I, d_I] bf16
+ *   w       device [rows, H_I] fp32
+ *   scores  device [rows, ld_scores] fp32; ld_scores >= max_pages*P/ratio,
+ *           multiple of 4
+ *   status  optional device int32 (NULL: device-detected problems are not
+ *           recorded); the same holds for qsa_topk_select and qsa_gather_attn */
+int qsa_index_score(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
+                    const qsa_bf16 *q_idx, const float *w, float *scores, int ld_scores,
+                    int32_t *status, cudaStream_t stream);
+
+/* Top-K select ([VA6] block top-k; ties to the lower block index): for every
+ * row, if n_blk <= K all blocks are selected; otherwise the K blocks with
+ * the largest score under the total order (score descending, block index
+ * ascending). Writes sel[row*K + i] ascending, padded with -1 to K entries,
+ * and n_sel[row] = number of selected blocks. Scores are compared as fp32
+ * (+0 and -0 are equal).
+ *   scores  device [rows, ld_scores] fp32 (from qsa_index_score)
+ *   sel     device [rows, K] int32;  n_sel  device [rows] int32 */
+int qsa_topk_select(const qsa_config *cfg, const qsa_rows *rows, const float *scores,
+                    int ld_scores, int32_t *sel, int32_t *n_sel, int32_t *status,
+                    cudaStream_t stream);
+
+/* Gather attention ([VA6] sparse paged GQA; [LC3] tail always visible): for
+ * every row, the token set T = {b*ratio + j : b in sel, j < ratio} U
+ * [n_blk*ratio, V) is gathered through the page table, and each query head h
+ * (KV head g = h*Hkv/Hq) gets o_h = sum_{t in T} softmax_t(q_h . K_t,g /
+ * sqrt(D)) V_t,g, split across CTAs and merged, rounded to bf16.
+ *   q    device [rows, Hq, D] bf16
+ *   sel, n_sel as written by qsa_topk_select
+ *   out  device [rows, Hq, D] bf16
+ *   ws   device workspace of ws_bytes >= qsa_workspace_bytes(cfg, rows, *) */
+int qsa_gather_attn(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
+                    const qsa_bf16 *q, const int32_t *sel, const int32_t *n_sel, qsa_bf16 *out,
+                    void *ws, size_t ws_bytes, int32_t *status, cudaStream_t stream);
+
+/* The fused step ([VA6]: one opaque index -> KV update -> sparse attend
+ * transaction): qsa_append, then qsa_index_score, qsa_topk_select and
+ * qsa_gather_attn for every appended row. Makes no host synchronisation and
+ * no allocation; capturable in a CUDA graph. The device status word collects
+ * errors of all stages.
+ *   sel_out, n_sel_out  optional device [rows, K] / [rows] int32 (NULL: kept
+ *                       in the workspace)
+ *   ws                  device workspace, ws_bytes >=
+ *                       qsa_workspace_bytes(cfg, rows, max_pages*P/ratio) */
+int qsa_decode(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
+               const qsa_bf16 *k_new, const qsa_bf16 *v_new, const qsa_bf16 *idx_k_new,
+               const qsa_bf16 *q_idx, const float *w, const qsa_bf16 *q,
+               int32_t *sel_out, int32_t *n_sel_out, qsa_bf16 *out,
+               void *ws, size_t ws_bytes, int32_t *status, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H */

@@ -1,0 +1,182 @@
+// Append, commit and rewind: the per-sequence indexer state.
+//
+// Append writes the new tokens' K/V rows into the paged KV pools and their raw
+// index keys into the raw-key pool, and pools every block the new tokens
+// complete ("Agentic shootout", "Flash-Next support: vLLM vs Atlas", (a) item
+// 6: one compressed key per complete group of compress_ratio tokens,
+// mean-pooled; its page mapping follows the main KV cache). The ingested
+// counter is checked before anything is written and advanced by a separate
+// commit kernel afterwards, so every CTA of a long append reads the same
+// pre-append value ("Atlas Flash-Next defect investigations", Report A,
+// Defect 1: decode at pos requires pos == ingested; rewind subtracts the
+// dropped tokens).
+#include "qsa_internal.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int kAppendTokensPerCta = 32;
+constexpr int kAppendThreads = 256;
+
+__global__ void __launch_bounds__(kAppendThreads)
+append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
+              const int32_t *__restrict__ pos0, const int32_t *__restrict__ page_table,
+              int max_pages, int num_pages, uint16_t *__restrict__ k_pool,
+              uint16_t *__restrict__ v_pool, uint16_t *__restrict__ raw_pool,
+              uint16_t *__restrict__ blk_pool, const int32_t *__restrict__ ingested,
+              const uint16_t *__restrict__ k_new, const uint16_t *__restrict__ v_new,
+              const uint16_t *__restrict__ idx_new, int32_t *status) {
+  const int i = blockIdx.x;
+  const int s = seq_ids[i];
+  const int p0 = pos0[i];
+  const int P = sh.page;
+  const int cap = max_pages * P;
+  const bool lead = (threadIdx.x == 0 && blockIdx.y == 0);
+  if (ingested[s] != p0) {
+    if (lead) report(status, QSA_ERR_DESYNC);
+    return;
+  }
+  if (p0 < 0 || p0 + R > cap) {
+    if (lead) report(status, QSA_ERR_CAPACITY);
+    return;
+  }
+  const int32_t *ptab = page_table + static_cast<size_t>(s) * max_pages;
+  const int t_begin = blockIdx.y * kAppendTokensPerCta;
+  const int t_end = min(R, t_begin + kAppendTokensPerCta);
+  if (t_begin >= t_end) return;
+
+  // 1. copy rows: per token, Hkv*D/8 uint4 of K, the same of V, d_I/8 of raw key
+  const int kv16 = sh.hkv * sh.d / 8;
+  const int ix16 = sh.d_idx / 8;
+  const int per_tok = 2 * kv16 + ix16;
+  const int n_work = (t_end - t_begin) * per_tok;
+  for (int e = threadIdx.x; e < n_work; e += blockDim.x) {
+    const int tl = e / per_tok;
+    const int c = e - tl * per_tok;
+    const int j = t_begin + tl;
+    const int pos = p0 + j;
+    const int page = ptab[pos >> sh.log2_page];
+    if (page < 0 || page >= num_pages) {
+      report(status, QSA_ERR_PAGE);
+      continue;
+    }
+    const size_t slot = static_cast<size_t>(page) * P + (pos & (P - 1));
+    const size_t row = static_cast<size_t>(i) * R + j;
+    const uint4 *src;
+    uint4 *dst;
+    if (c < kv16) {
+      src = reinterpret_cast<const uint4 *>(k_new + row * kv16 * 8) + c;
+      dst = reinterpret_cast<uint4 *>(k_pool + slot * kv16 * 8) + c;
+    } else if (c < 2 * kv16) {
+      src = reinterpret_cast<const uint4 *>(v_new + row * kv16 * 8) + (c - kv16);
+      dst = reinterpret_cast<uint4 *>(v_pool + slot * kv16 * 8) + (c - kv16);
+    } else {
+      src = reinterpret_cast<const uint4 *>(idx_new + row * ix16 * 8) + (c - 2 * kv16);
+      dst = reinterpret_cast<uint4 *>(raw_pool + slot * ix16 * 8) + (c - 2 * kv16);
+    }
+    *dst = __ldg(src);
+  }
+
+  // 2. pool the blocks whose last token is one of this CTA's tokens: block b
+  // completes at position b*r + r - 1, so b in [first/r, last/r).
+  const int r = sh.ratio;
+  const int first_pos = p0 + t_begin;
+  const int last_pos = p0 + t_end;
+  const int b_lo = first_pos >> sh.log2_ratio;
+  const int b_hi = last_pos >> sh.log2_ratio;
+  const int half = sh.d_idx / 2;
+  const int bpp = P >> sh.log2_ratio;  // blocks per page
+  const float inv_r = 1.0f / static_cast<float>(r);
+  for (int e = threadIdx.x; e < (b_hi - b_lo) * half; e += blockDim.x) {
+    const int b = b_lo + e / half;
+    const int d2 = (e % half) * 2;
+    float s0 = 0.f, s1 = 0.f;
+    bool ok = true;
+    for (int jj = 0; jj < r; ++jj) {
+      const int pos = b * r + jj;
+      const uint16_t *src;
+      if (pos >= p0) {
+        src = idx_new + (static_cast<size_t>(i) * R + (pos - p0)) * sh.d_idx + d2;
+      } else {
+        const int page = ptab[pos >> sh.log2_page];
+        if (page < 0 || page >= num_pages) {
+          ok = false;
+          break;
+        }
+        src = raw_pool + (static_cast<size_t>(page) * P + (pos & (P - 1))) * sh.d_idx + d2;
+      }
+      const uint32_t two = *reinterpret_cast<const uint32_t *>(src);
+      s0 += bf16_bits_to_float(static_cast<uint16_t>(two & 0xFFFF));
+      s1 += bf16_bits_to_float(static_cast<uint16_t>(two >> 16));
+    }
+    const int page_b = ptab[(b * r) >> sh.log2_page];
+    if (!ok || page_b < 0 || page_b >= num_pages) {
+      report(status, QSA_ERR_PAGE);
+      continue;
+    }
+    uint16_t *dst = blk_pool + (static_cast<size_t>(page_b) * bpp + (b & (bpp - 1))) * sh.d_idx + d2;
+    *reinterpret_cast<uint32_t *>(dst) = pack_bf16(s0 * inv_r, s1 * inv_r);
+  }
+}
+
+__global__ void commit_kernel(int n_seq, int R, int capacity, const int32_t *__restrict__ seq_ids,
+                              int32_t *__restrict__ pos0, int32_t *__restrict__ ingested,
+                              int advance) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_seq) return;
+  const int s = seq_ids[i];
+  const int p0 = pos0[i];
+  if (ingested[s] == p0 && p0 >= 0 && p0 + R <= capacity) {
+    ingested[s] = p0 + R;
+    if (advance) pos0[i] = p0 + R;
+  }
+}
+
+__global__ void rewind_kernel(int n_seq, const int32_t *__restrict__ seq_ids,
+                              const int32_t *__restrict__ n_drop, int32_t *__restrict__ ingested,
+                              int32_t *status) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_seq) return;
+  const int s = seq_ids[i];
+  const int n = n_drop[i];
+  const int cur = ingested[s];
+  if (n < 0 || n > cur) {
+    report(status, QSA_ERR_REWIND);
+    return;
+  }
+  ingested[s] = cur - n;
+}
+
+}  // namespace
+
+cudaError_t launch_append(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
+                          const int32_t *pos0, const int32_t *page_table, int max_pages,
+                          int num_pages, uint16_t *k_pool, uint16_t *v_pool,
+                          uint16_t *idxraw_pool, uint16_t *idxblk_pool, const int32_t *ingested,
+                          const uint16_t *k_new, const uint16_t *v_new,
+                          const uint16_t *idx_k_new, int32_t *status, cudaStream_t st) {
+  if (n_seq == 0 || R == 0) return cudaSuccess;
+  dim3 grid(n_seq, (R + kAppendTokensPerCta - 1) / kAppendTokensPerCta);
+  append_kernel<<<grid, kAppendThreads, 0, st>>>(sh, R, seq_ids, pos0, page_table, max_pages,
+                                                 num_pages, k_pool, v_pool, idxraw_pool,
+                                                 idxblk_pool, ingested, k_new, v_new, idx_k_new,
+                                                 status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_commit(int n_seq, int R, int capacity, const int32_t *seq_ids,
+                          int32_t *pos0, int32_t *ingested, int advance, cudaStream_t st) {
+  if (n_seq == 0 || R == 0) return cudaSuccess;
+  commit_kernel<<<(n_seq + 127) / 128, 128, 0, st>>>(n_seq, R, capacity, seq_ids, pos0, ingested,
+                                                     advance);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rewind(int n_seq, const int32_t *seq_ids, const int32_t *n_drop,
+                          int32_t *ingested, int32_t *status, cudaStream_t st) {
+  if (n_seq == 0) return cudaSuccess;
+  rewind_kernel<<<(n_seq + 127) / 128, 128, 0, st>>>(n_seq, seq_ids, n_drop, ingested, status);
+  return cudaGetLastError();
+}
+
+}  // namespace qsa

@@ -1,0 +1,396 @@
+// Sparse GQA attention over the gathered token set, split across CTAs, and
+// the merge of the splits ("Agentic shootout", "Flash-Next support: vLLM vs
+// Atlas", (a) item 6: sparse paged GQA over the selected token indices, read
+// straight from the cache pages; "Flash-Next support: llama.cpp vs Atlas",
+// (a) item 3: the incomplete tail block is always visible, and (e) risk 1:
+// flash-decode over scattered slots needs a gather + flash pass).
+//
+// Token set of a row with V visible tokens, n_blk = V/ratio complete blocks
+// and n_sel selected blocks (ascending ids in sel):
+//   slot j <  n_sel*ratio : token sel[j/ratio]*ratio + j%ratio
+//   slot j >= n_sel*ratio : token n_blk*ratio + (j - n_sel*ratio)   (the tail)
+// n_slots = n_sel*ratio + (V - n_blk*ratio) <= budget + ratio - 1.
+//
+// CTA (split, row) takes a contiguous range of slots. Each stage gathers the
+// K and V rows of kChunk slots for all KV heads with 16-byte cp.async
+// (3-stage pipeline) into an XOR-swizzled shared tile. Warp w owns KV head
+// w % Hkv and a 16-slot sub-tile. Per sub-tile:
+//   S^T[16 tok x 8 heads] = K[16 x 128] . Q^T   (tokens on M: m16n8k16 x8)
+//   online softmax per head column (exp2, scale folded with log2 e)
+//   P^T -> B operand via movmatrix.trans; P split as bf16 hi + bf16 lo so the
+//   weights keep ~16 significant bits
+//   O^T[128 x 8] += V^T . P^T                   (ldmatrix.trans of V, x16)
+// The split writes (m, l, acc) in fp32; the merge kernel combines splits and
+// rounds o = acc / l to bf16.
+#include "qsa_internal.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int kAttnThreads = 128;
+constexpr int kAttnWarps = 4;
+constexpr int kStages = 3;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int HKV>
+struct AttnGeom {
+  static constexpr int kWarpsPerHead = kAttnWarps / HKV;
+  static constexpr int kChunk = 16 * kWarpsPerHead;           // slots per stage
+  static constexpr int kThreadsPerSlot = kAttnThreads / kChunk;
+  static constexpr int kRowBytes = kHeadDim * 2;              // 256
+  static constexpr int kHalfStage = kChunk * HKV * kRowBytes;  // K (or V) bytes per stage
+  static constexpr int kStageBytes = 2 * kHalfStage;
+};
+
+__device__ __forceinline__ int slot_token(int j, int n_body, int log2r, int r, int tail0,
+                                          const int32_t *sel_row) {
+  return j < n_body ? sel_row[j >> log2r] * r + (j & (r - 1)) : tail0 + (j - n_body);
+}
+
+template <int HKV>
+__global__ void __launch_bounds__(kAttnThreads)
+attn_kernel(Shape sh, int R, int n_split, int split_len, const int32_t *__restrict__ seq_ids,
+            const int32_t *__restrict__ pos0, CacheView cv, const uint16_t *__restrict__ q,
+            const int32_t *__restrict__ sel, const int32_t *__restrict__ n_sel_arr,
+            float *__restrict__ part_m, float *__restrict__ part_l, float *__restrict__ part_acc,
+            int32_t *status) {
+  using G = AttnGeom<HKV>;
+  extern __shared__ __align__(128) uint8_t smem[];
+
+  const int row = blockIdx.y;
+  const int sp = blockIdx.x;
+  const int i = row / R;
+  const int s = seq_ids[i];
+  const int visible = pos0[i] + (row - i * R) + 1;
+  const int r = sh.ratio;
+  const bool row_ok = visible >= 1 && visible <= cv.max_pages * sh.page;
+  if (!row_ok && sp == 0 && threadIdx.x == 0) report(status, QSA_ERR_CAPACITY);
+  const int n_blk = row_ok ? (visible >> sh.log2_ratio) : 0;
+  const int n_sel = row_ok ? min(max(n_sel_arr[row], 0), min(n_blk, sh.topk)) : 0;
+  const int n_body = n_sel * r;
+  const int tail0 = n_blk * r;
+  const int n_slots = row_ok ? n_body + (visible - tail0) : 0;
+  const int slot_lo = min(n_slots, sp * split_len);
+  const int slot_hi = min(n_slots, slot_lo + split_len);
+  const int n_chunks = (slot_hi - slot_lo + G::kChunk - 1) / G::kChunk;
+  const int32_t *sel_row = sel + static_cast<size_t>(row) * sh.topk;
+  const int32_t *ptab = cv.page_table + static_cast<size_t>(s) * cv.max_pages;
+  const int P = sh.page;
+  const int group = sh.hq / HKV;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = warp % HKV;            // KV head of this warp
+  const int sub = warp / HKV;          // 16-slot sub-tile of the stage
+  const int smem_u = smem_u32(smem);
+
+  // ---- gather of one stage: thread -> (slot, 16 of its 32*HKV 16-byte pieces)
+  const int my_slot = tid / G::kThreadsPerSlot;
+  const int my_part = tid % G::kThreadsPerSlot;
+  auto load_stage = [&](int chunk_idx, int buf) {
+    const int j = slot_lo + chunk_idx * G::kChunk + my_slot;
+    const uint16_t *kbase = cv.k_pool, *vbase = cv.v_pool;
+    int bytes = 0;
+    if (j < slot_hi) {
+      const int t = slot_token(j, n_body, sh.log2_ratio, r, tail0, sel_row);
+      const int page = (t >= 0 && t < visible) ? ptab[t >> sh.log2_page] : -1;
+      if (page >= 0 && page < cv.num_pages) {
+        const size_t off = (static_cast<size_t>(page) * P + (t & (P - 1))) * HKV * kHeadDim;
+        kbase = cv.k_pool + off;
+        vbase = cv.v_pool + off;
+        bytes = 16;
+      } else {
+        report(status, QSA_ERR_PAGE);
+      }
+    }
+    const uint32_t stage = smem_u + buf * G::kStageBytes;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int piece = my_part + G::kThreadsPerSlot * u;  // in [0, 32*HKV)
+      const int kv = piece / (16 * HKV);
+      const int rem = piece % (16 * HKV);
+      const int gg = rem >> 4, c16 = rem & 15;
+      const uint16_t *src = (kv ? vbase : kbase) + (bytes ? gg * kHeadDim + c16 * 8 : 0);
+      const uint32_t dst = stage + kv * G::kHalfStage + (gg * G::kChunk + my_slot) * G::kRowBytes +
+                           ((c16 ^ (my_slot & 7)) << 4);
+      cp_async16(dst, src, bytes);
+    }
+  };
+
+  // ---- Q^T fragments (B operand of S^T = K Q^T) for the warp's 8 heads
+  uint32_t qf[8][2];
+  {
+    const int hl = lane >> 2;
+    const bool ok = hl < group;
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+        q + (static_cast<size_t>(row) * sh.hq + g * group + (ok ? hl : 0)) * kHeadDim);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qf[ks][0] = ok ? qrow[ks * 8 + (lane & 3)] : 0u;
+      qf[ks][1] = ok ? qrow[ks * 8 + 4 + (lane & 3)] : 0u;
+    }
+  }
+
+  float acc[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[mt][c] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+  const float scale = kLog2e * rsqrtf(static_cast<float>(kHeadDim));
+
+#pragma unroll
+  for (int st = 0; st < kStages - 1; ++st) {
+    if (st < n_chunks) load_stage(st, st);
+    cp_async_commit();
+  }
+
+  for (int c = 0; c < n_chunks; ++c) {
+    cp_async_wait<kStages - 2>();
+    __syncthreads();
+    {
+      const int nxt = c + kStages - 1;
+      if (nxt < n_chunks) load_stage(nxt, nxt % kStages);
+      cp_async_commit();
+    }
+    const int buf = c % kStages;
+    const uint32_t kt = smem_u + buf * G::kStageBytes + (g * G::kChunk + sub * 16) * G::kRowBytes;
+    const uint32_t vt = kt + G::kHalfStage;
+
+    // S^T = K . Q^T
+    float sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int rr = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int cc = 2 * ks + (lane >> 4);
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(kt + rr * G::kRowBytes + ((cc ^ (rr & 7)) << 4), a0, a1, a2, a3);
+      mma_bf16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+    }
+    // mask slots past the split's end, scale to the log2 domain
+    const int j0 = slot_lo + c * G::kChunk + sub * 16 + (lane >> 2);
+    const bool v0 = j0 < slot_hi, v1 = (j0 + 8) < slot_hi;
+    float s0 = v0 ? sa[0] * scale : -INFINITY;
+    float s1 = v0 ? sa[1] * scale : -INFINITY;
+    float s2 = v1 ? sa[2] * scale : -INFINITY;
+    float s3 = v1 ? sa[3] * scale : -INFINITY;
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+    const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(m_run[0] - ref0), al1 = exp2f(m_run[1] - ref1);
+    const float p0 = exp2f(s0 - ref0), p1 = exp2f(s1 - ref1);
+    const float p2 = exp2f(s2 - ref0), p3 = exp2f(s3 - ref1);
+    l_run[0] = l_run[0] * al0 + p0 + p2;
+    l_run[1] = l_run[1] * al1 + p1 + p3;
+    m_run[0] = mn0;
+    m_run[1] = mn1;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      acc[mt][0] *= al0;
+      acc[mt][1] *= al1;
+      acc[mt][2] *= al0;
+      acc[mt][3] *= al1;
+    }
+    // P^T as B operand, hi + lo bf16
+    const uint32_t hi_top = pack_bf16(p0, p1), hi_bot = pack_bf16(p2, p3);
+    const __nv_bfloat162 ht = *reinterpret_cast<const __nv_bfloat162 *>(&hi_top);
+    const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162 *>(&hi_bot);
+    const uint32_t lo_top = pack_bf16(p0 - __low2float(ht), p1 - __high2float(ht));
+    const uint32_t lo_bot = pack_bf16(p2 - __low2float(hb), p3 - __high2float(hb));
+    const uint32_t bh0 = movmatrix_t(hi_top), bh1 = movmatrix_t(hi_bot);
+    const uint32_t bl0 = movmatrix_t(lo_top), bl1 = movmatrix_t(lo_bot);
+    // O^T += V^T . P^T
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int tok = (lane & 7) + ((lane >> 4) << 3);
+      const int cc = 2 * mt + ((lane >> 3) & 1);
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(vt + tok * G::kRowBytes + ((cc ^ (tok & 7)) << 4), a0, a1, a2, a3);
+      mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
+      mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
+    }
+  }
+  cp_async_wait<0>();
+
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], o);
+    l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], o);
+  }
+
+  // ---- combine warps that share a KV head (Hkv < 4), then write the split
+  if constexpr (G::kWarpsPerHead > 1) {
+    __syncthreads();  // stages are free now; reuse them as scratch
+    float *red = reinterpret_cast<float *>(smem);
+    // per warp: m[8], l[8], acc[8 heads][128 dims]
+    float *mine = red + warp * (16 + 8 * kHeadDim);
+    if (lane < 4) {
+      mine[2 * lane] = m_run[0];
+      mine[2 * lane + 1] = m_run[1];
+      mine[8 + 2 * lane] = l_run[0];
+      mine[8 + 2 * lane + 1] = l_run[1];
+    }
+    __syncthreads();
+    float mx[2], scl[2], lsum[2] = {0.f, 0.f};
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) {
+      const int col = 2 * (lane & 3) + c2;
+      float m = -INFINITY;
+      for (int w2 = g; w2 < kAttnWarps; w2 += HKV) m = fmaxf(m, red[w2 * (16 + 8 * kHeadDim) + col]);
+      mx[c2] = m;
+      const float ref = m == -INFINITY ? 0.f : m;
+      for (int w2 = g; w2 < kAttnWarps; w2 += HKV) {
+        const float* o = red + w2 * (16 + 8 * kHeadDim);
+        lsum[c2] += o[8 + col] * exp2f(o[col] - ref);
+      }
+      scl[c2] = exp2f((c2 ? m_run[1] : m_run[0]) - ref);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d0 = mt * 16 + (lane >> 2);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int col = 2 * (lane & 3) + (c & 1);
+        const int d = d0 + (c >> 1) * 8;
+        mine[16 + col * kHeadDim + d] = acc[mt][c] * scl[c & 1];
+      }
+    }
+    __syncthreads();
+    if (sub == 0) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int d0 = mt * 16 + (lane >> 2);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int col = 2 * (lane & 3) + (c & 1);
+          const int d = d0 + (c >> 1) * 8;
+          float v = 0.f;
+          for (int w2 = g; w2 < kAttnWarps; w2 += HKV) v += red[w2 * (16 + 8 * kHeadDim) + 16 + col * kHeadDim + d];
+          acc[mt][c] = v;
+        }
+      }
+      m_run[0] = mx[0];
+      m_run[1] = mx[1];
+      l_run[0] = lsum[0];
+      l_run[1] = lsum[1];
+    }
+  }
+  if (sub != 0) return;
+
+  const size_t base = (static_cast<size_t>(row) * n_split + sp) * sh.hq + g * group;
+#pragma unroll
+  for (int c2 = 0; c2 < 2; ++c2) {
+    const int col = 2 * (lane & 3) + c2;
+    if (lane < 4 && col < group) {
+      part_m[base + col] = m_run[c2];
+      part_l[base + col] = l_run[c2];
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const int d0 = mt * 16 + (lane >> 2);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int col = 2 * (lane & 3) + (c & 1);
+      if (col < group) part_acc[(base + col) * kHeadDim + d0 + (c >> 1) * 8] = acc[mt][c];
+    }
+  }
+}
+
+// One CTA per (row, head): 128 threads, one per output dim.
+__global__ void __launch_bounds__(kHeadDim)
+merge_kernel(int hq, int n_split, const float *__restrict__ part_m,
+             const float *__restrict__ part_l, const float *__restrict__ part_acc,
+             uint16_t *__restrict__ out) {
+  const int row = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+  const size_t b0 = static_cast<size_t>(row) * n_split * hq + h;
+  float m = -INFINITY;
+  for (int s = 0; s < n_split; ++s) m = fmaxf(m, part_m[b0 + static_cast<size_t>(s) * hq]);
+  const float ref = m == -INFINITY ? 0.f : m;
+  float l = 0.f, a = 0.f;
+  for (int s = 0; s < n_split; ++s) {
+    const size_t k = b0 + static_cast<size_t>(s) * hq;
+    const float wgt = exp2f(part_m[k] - ref);
+    l += wgt * part_l[k];
+    a += wgt * part_acc[k * kHeadDim + d];
+  }
+  const float o = l > 0.f ? a / l : 0.f;
+  __nv_bfloat16 ob = __float2bfloat16_rn(o);
+  out[(static_cast<size_t>(row) * hq + h) * kHeadDim + d] = *reinterpret_cast<uint16_t *>(&ob);
+}
+
+struct SplitPlan {
+  int n_split, split_len;
+};
+
+// Every row is cut into splits of a fixed number of slots, whatever the batch
+// shape, so the reduction order of a row (and hence its bf16 output) is the
+// same in decode, verify and chunked-prefill form: chunked and single-shot
+// prefill agree bit for bit.
+constexpr int kSplitSlots = 128;
+
+SplitPlan plan_splits(const Shape &sh, int rows) {
+  (void)rows;
+  const int max_slots = sh.budget + sh.ratio - 1;
+  return {(max_slots + kSplitSlots - 1) / kSplitSlots, kSplitSlots};
+}
+
+template <int HKV>
+cudaError_t launch_attn_t(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
+                          const int32_t *pos0, const CacheView &cv, const uint16_t *q,
+                          const int32_t *sel, const int32_t *n_sel, uint16_t *out, void *partials,
+                          int32_t *status, cudaStream_t st) {
+  const int rows = n_seq * R;
+  const SplitPlan pl = plan_splits(sh, rows);
+  float *pm = static_cast<float *>(partials);
+  float *pl_ = pm + static_cast<size_t>(rows) * pl.n_split * sh.hq;
+  float *pa = pl_ + static_cast<size_t>(rows) * pl.n_split * sh.hq;
+  const size_t smem = kStages * AttnGeom<HKV>::kStageBytes;
+  auto kern = attn_kernel<HKV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(pl.n_split, rows), kAttnThreads, smem, st>>>(sh, R, pl.n_split, pl.split_len, seq_ids,
+                                                           pos0, cv, q, sel, n_sel, pm, pl_, pa,
+                                                           status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  merge_kernel<<<dim3(rows, sh.hq), kHeadDim, 0, st>>>(sh.hq, pl.n_split, pm, pl_, pa, out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int attn_splits(const Shape &sh, int rows) { return plan_splits(sh, rows).n_split; }
+
+size_t attn_partial_bytes(const Shape &sh, int rows) {
+  // the partial buffers for `rows` rows; fewer rows use more splits, so take
+  // the largest rows x splits product over every row count up to `rows`
+  size_t worst = 0;
+  for (int r = 1; r <= rows; ++r) {
+    const size_t v = static_cast<size_t>(r) * plan_splits(sh, r).n_split;
+    if (v > worst) worst = v;
+  }
+  return worst * sh.hq * (kHeadDim + 2) * sizeof(float);
+}
+
+cudaError_t launch_attn(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
+                        const int32_t *pos0, const CacheView &cv, const uint16_t *q,
+                        const int32_t *sel, const int32_t *n_sel, uint16_t *out, void *partials,
+                        int32_t *status, cudaStream_t st) {
+  if (n_seq == 0 || R == 0) return cudaSuccess;
+  switch (sh.hkv) {
+    case 1: return launch_attn_t<1>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, st);
+    case 2: return launch_attn_t<2>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, st);
+    case 4: return launch_attn_t<4>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace qsa

@@ -1,0 +1,134 @@
+// Internal definitions shared by the libqsa translation units.
+//
+// Layouts (all row-major, bf16 as 16-bit patterns):
+//   k_pool, v_pool  [num_pages][P][Hkv][D]     a token's K (or V) row for all
+//                                                KV heads is Hkv*D*2 contiguous bytes
+//   idxraw_pool     [num_pages][P][d_I]
+//   idxblk_pool     [num_pages][P/ratio][d_I]   shares the page table at 1/ratio density
+//   page_table      [n_slots][max_pages] int32
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/qsa.h"
+
+namespace qsa {
+
+constexpr int kMaxTopK = 2048;
+constexpr int kHeadDim = 128;
+
+// Device-side status codes go through a first-error-wins CAS.
+__device__ __forceinline__ void report(int32_t *status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// --- launch parameter blocks ---------------------------------------------
+
+struct CacheView {
+  const int32_t *page_table;
+  int max_pages;
+  int num_pages;
+  const uint16_t *k_pool;
+  const uint16_t *v_pool;
+  const uint16_t *idxraw_pool;
+  const uint16_t *idxblk_pool;
+};
+
+struct Shape {
+  int ratio, budget, topk, h_idx, d_idx, hq, hkv, d, page;
+  int log2_ratio, log2_page;
+};
+
+// --- PTX wrappers ---------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte async copy global -> shared; src_bytes = 0 fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                          uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose an 8x8 b16 matrix held in the standard fragment layout
+// (thread t holds row t/4, columns 2*(t%4), 2*(t%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Order-preserving map of an fp32 score to uint32 (larger score -> larger key);
+// -0 is folded onto +0 first so that the two compare equal.
+__device__ __forceinline__ uint32_t score_key(float s) {
+  uint32_t u = __float_as_uint(s + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// --- launchers (defined in the .cu files, called by the C entry points) ----
+
+cudaError_t launch_append(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
+                          const int32_t *pos0, const int32_t *page_table, int max_pages,
+                          int num_pages, uint16_t *k_pool, uint16_t *v_pool,
+                          uint16_t *idxraw_pool, uint16_t *idxblk_pool, const int32_t *ingested,
+                          const uint16_t *k_new, const uint16_t *v_new,
+                          const uint16_t *idx_k_new, int32_t *status, cudaStream_t st);
+cudaError_t launch_commit(int n_seq, int R, int capacity, const int32_t *seq_ids,
+                          int32_t *pos0, int32_t *ingested, int advance, cudaStream_t st);
+cudaError_t launch_rewind(int n_seq, const int32_t *seq_ids, const int32_t *n_drop,
+                          int32_t *ingested, int32_t *status, cudaStream_t st);
+cudaError_t launch_score(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
+                         const int32_t *pos0, const CacheView &cv, const uint16_t *q_idx,
+                         const float *w, float *scores, int ld_scores, int32_t *status,
+                         cudaStream_t st);
+cudaError_t launch_select(const Shape &sh, int n_seq, int R, const int32_t *pos0,
+                          const float *scores, int ld_scores, int32_t *sel, int32_t *n_sel,
+                          int max_blocks, int cap_tokens, int32_t *status, cudaStream_t st);
+int attn_splits(const Shape &sh, int rows);
+size_t attn_partial_bytes(const Shape &sh, int rows);
+cudaError_t launch_attn(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
+                        const int32_t *pos0, const CacheView &cv, const uint16_t *q,
+                        const int32_t *sel, const int32_t *n_sel, uint16_t *out, void *partials,
+                        int32_t *status, cudaStream_t st);
+
+}  // namespace qsa

@@ -1,0 +1,283 @@
+"""Thin ctypes binding over libqsa (include/qsa.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels. PyTorch provides device memory and the current stream. Importing this
+module loads the library and fails loudly if it has not been built; there is
+no fallback implementation.
+
+The functions keep the C names (qsa_append, qsa_rewind, qsa_index_score,
+qsa_topk_select, qsa_gather_attn, qsa_decode, qsa_config_check,
+qsa_workspace_bytes, qsa_strerror). A non-zero return raises QsaError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqsa.so")
+
+QSA_OK = 0
+QSA_ERR_INVALID_ARG = 1
+QSA_ERR_UNSUPPORTED = 2
+QSA_ERR_CAPACITY = 3
+QSA_ERR_WORKSPACE = 4
+QSA_ERR_CUDA = 5
+QSA_ERR_CUDA_FATAL = 6
+QSA_ERR_DESYNC = 7
+QSA_ERR_PAGE = 8
+QSA_ERR_REWIND = 9
+
+EXPORTED = ("qsa_strerror", "qsa_config_check", "qsa_workspace_bytes", "qsa_append",
+            "qsa_rewind", "qsa_index_score", "qsa_topk_select", "qsa_gather_attn", "qsa_decode")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"libqsa is not built ({_LIB_PATH} missing): run "
+            "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    return ctypes.CDLL(_LIB_PATH)
+
+
+LIB = _load()
+LIB_PATH = _LIB_PATH
+
+
+class qsa_config(ctypes.Structure):
+    _fields_ = [("ratio", ctypes.c_int), ("budget", ctypes.c_int), ("n_idx_heads", ctypes.c_int),
+                ("idx_dim", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("page_size", ctypes.c_int)]
+
+
+class qsa_rows(ctypes.Structure):
+    _fields_ = [("n_seq", ctypes.c_int), ("rows_per_seq", ctypes.c_int),
+                ("seq_ids", ctypes.c_void_p), ("pos0", ctypes.c_void_p),
+                ("pos0_host", ctypes.c_void_p), ("advance", ctypes.c_int)]
+
+
+class qsa_cache(ctypes.Structure):
+    _fields_ = [("page_table", ctypes.c_void_p), ("n_slots", ctypes.c_int),
+                ("max_pages", ctypes.c_int), ("num_pages", ctypes.c_int),
+                ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("idxraw_pool", ctypes.c_void_p), ("idxblk_pool", ctypes.c_void_p),
+                ("ingested", ctypes.c_void_p)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_CFG = ctypes.POINTER(qsa_config)
+_ROWS = ctypes.POINTER(qsa_rows)
+_CACHE = ctypes.POINTER(qsa_cache)
+
+LIB.qsa_strerror.restype = ctypes.c_char_p
+LIB.qsa_strerror.argtypes = [_I]
+LIB.qsa_config_check.restype = _I
+LIB.qsa_config_check.argtypes = [_CFG]
+LIB.qsa_workspace_bytes.restype = ctypes.c_size_t
+LIB.qsa_workspace_bytes.argtypes = [_CFG, _I, _I]
+LIB.qsa_append.restype = _I
+LIB.qsa_append.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P]
+LIB.qsa_rewind.restype = _I
+LIB.qsa_rewind.argtypes = [_CFG, _I, _P, _P, _P, _P, _P]
+LIB.qsa_index_score.restype = _I
+LIB.qsa_index_score.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _I, _P, _P]
+LIB.qsa_topk_select.restype = _I
+LIB.qsa_topk_select.argtypes = [_CFG, _ROWS, _P, _I, _P, _P, _P, _P]
+LIB.qsa_gather_attn.restype = _I
+LIB.qsa_gather_attn.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+LIB.qsa_decode.restype = _I
+LIB.qsa_decode.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                           ctypes.c_size_t, _P, _P]
+
+
+class QsaError(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str = ""):
+        self.code = code
+        msg = f"{where}: {qsa_strerror(code)} (status {code})"
+        super().__init__(msg + (f"; {detail}" if detail else ""))
+
+
+def qsa_strerror(code: int) -> str:
+    return LIB.qsa_strerror(int(code)).decode()
+
+
+def _check(rc: int, where: str, detail: str = "") -> None:
+    if rc != QSA_OK:
+        raise QsaError(rc, where, detail)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libqsa must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+# ---------------------------------------------------------------------------
+# Marshalling helpers
+# ---------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class Config:
+    ratio: int
+    budget: int
+    n_idx_heads: int
+    idx_dim: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int = 128
+    page_size: int = 64
+
+    def c(self) -> qsa_config:
+        return qsa_config(self.ratio, self.budget, self.n_idx_heads, self.idx_dim,
+                          self.n_q_heads, self.n_kv_heads, self.head_dim, self.page_size)
+
+    @property
+    def topk(self) -> int:
+        return self.budget // self.ratio
+
+    @classmethod
+    def of(cls, shapes) -> "Config":
+        return cls(shapes.ratio, shapes.budget, shapes.n_idx_heads, shapes.idx_dim,
+                   shapes.n_q_heads, shapes.n_kv_heads, shapes.head_dim, shapes.page_size)
+
+
+class PagedCache:
+    """Device pools of a paged indexer + KV cache, allocated with torch.
+
+    page_table: [n_slots, max_pages] int32 (host or device; copied to device)."""
+
+    def __init__(self, cfg: Config, page_table: torch.Tensor, num_pages: int, device="cuda"):
+        self.cfg = cfg
+        P = cfg.page_size
+        self.page_table = page_table.to(device=device, dtype=torch.int32).contiguous()
+        self.n_slots, self.max_pages = self.page_table.shape
+        self.num_pages = num_pages
+        self.k_pool = torch.zeros(num_pages, P, cfg.n_kv_heads, cfg.head_dim, dtype=torch.bfloat16, device=device)
+        self.v_pool = torch.zeros_like(self.k_pool)
+        self.idxraw_pool = torch.zeros(num_pages, P, cfg.idx_dim, dtype=torch.bfloat16, device=device)
+        self.idxblk_pool = torch.zeros(num_pages, P // cfg.ratio, cfg.idx_dim, dtype=torch.bfloat16, device=device)
+        self.ingested = torch.zeros(self.n_slots, dtype=torch.int32, device=device)
+
+    @property
+    def capacity(self) -> int:
+        return self.max_pages * self.cfg.page_size
+
+    @property
+    def max_blocks(self) -> int:
+        return self.capacity // self.cfg.ratio
+
+    def c(self) -> qsa_cache:
+        return qsa_cache(_ptr(self.page_table), self.n_slots, self.max_pages, self.num_pages,
+                         _ptr(self.k_pool), _ptr(self.v_pool), _ptr(self.idxraw_pool),
+                         _ptr(self.idxblk_pool), _ptr(self.ingested))
+
+
+class Rows:
+    """Row layout of a step: n_seq sequences x R rows, sequence-major."""
+
+    def __init__(self, seq_ids: torch.Tensor, pos0: torch.Tensor, rows_per_seq: int,
+                 pos0_host: Optional[torch.Tensor] = None, advance: bool = False):
+        self.seq_ids = seq_ids.to(torch.int32).contiguous()
+        self.pos0 = pos0 if (pos0.dtype == torch.int32 and pos0.is_contiguous()) else pos0.to(torch.int32).contiguous()
+        self.R = rows_per_seq
+        self.pos0_host = None if pos0_host is None else pos0_host.to(torch.int32).cpu().contiguous()
+        self.advance = bool(advance)
+
+    @property
+    def n_seq(self) -> int:
+        return self.seq_ids.numel()
+
+    @property
+    def n_rows(self) -> int:
+        return self.n_seq * self.R
+
+    def c(self) -> qsa_rows:
+        return qsa_rows(self.n_seq, self.R, _ptr(self.seq_ids), _ptr(self.pos0),
+                        None if self.pos0_host is None else _ptr(self.pos0_host), int(self.advance))
+
+
+# ---------------------------------------------------------------------------
+# Entry points (same names as the C ABI)
+# ---------------------------------------------------------------------------
+
+def qsa_config_check(cfg: Config) -> int:
+    return LIB.qsa_config_check(ctypes.byref(cfg.c()))
+
+
+def qsa_workspace_bytes(cfg: Config, max_rows: int, max_blocks_per_row: int) -> int:
+    return LIB.qsa_workspace_bytes(ctypes.byref(cfg.c()), max_rows, max_blocks_per_row)
+
+
+def qsa_append(cfg: Config, rows: Rows, cache: PagedCache, k_new, v_new, idx_k_new, status,
+               stream=None) -> None:
+    rc = LIB.qsa_append(ctypes.byref(cfg.c()), ctypes.byref(rows.c()), ctypes.byref(cache.c()),
+                        _ptr(k_new, torch.bfloat16), _ptr(v_new, torch.bfloat16),
+                        _ptr(idx_k_new, torch.bfloat16), _ptr(status, torch.int32), _stream(stream))
+    _check(rc, "qsa_append", f"capacity {cache.capacity} tokens per sequence" if rc == QSA_ERR_CAPACITY else "")
+
+
+def qsa_rewind(cfg: Config, seq_ids, n_drop, ingested, status, stream=None) -> None:
+    rc = LIB.qsa_rewind(ctypes.byref(cfg.c()), seq_ids.numel(), _ptr(seq_ids, torch.int32),
+                        _ptr(n_drop, torch.int32), _ptr(ingested, torch.int32),
+                        _ptr(status, torch.int32), _stream(stream))
+    _check(rc, "qsa_rewind")
+
+
+def qsa_index_score(cfg: Config, rows: Rows, cache: PagedCache, q_idx, w, scores, ld_scores: int,
+                    status=None, stream=None) -> None:
+    rc = LIB.qsa_index_score(ctypes.byref(cfg.c()), ctypes.byref(rows.c()), ctypes.byref(cache.c()),
+                             _ptr(q_idx, torch.bfloat16), _ptr(w, torch.float32),
+                             _ptr(scores, torch.float32), ld_scores, _ptr(status, torch.int32),
+                             _stream(stream))
+    _check(rc, "qsa_index_score")
+
+
+def qsa_topk_select(cfg: Config, rows: Rows, scores, ld_scores: int, sel, n_sel, status=None,
+                    stream=None) -> None:
+    rc = LIB.qsa_topk_select(ctypes.byref(cfg.c()), ctypes.byref(rows.c()),
+                             _ptr(scores, torch.float32), ld_scores, _ptr(sel, torch.int32),
+                             _ptr(n_sel, torch.int32), _ptr(status, torch.int32), _stream(stream))
+    _check(rc, "qsa_topk_select")
+
+
+def qsa_gather_attn(cfg: Config, rows: Rows, cache: PagedCache, q, sel, n_sel, out, ws,
+                    status=None, stream=None) -> None:
+    rc = LIB.qsa_gather_attn(ctypes.byref(cfg.c()), ctypes.byref(rows.c()), ctypes.byref(cache.c()),
+                             _ptr(q, torch.bfloat16), _ptr(sel, torch.int32), _ptr(n_sel, torch.int32),
+                             _ptr(out, torch.bfloat16), _ptr(ws), ws.numel() * ws.element_size(),
+                             _ptr(status, torch.int32), _stream(stream))
+    _check(rc, "qsa_gather_attn")
+
+
+def qsa_decode(cfg: Config, rows: Rows, cache: PagedCache, k_new, v_new, idx_k_new, q_idx, w, q,
+               out, ws, status, sel_out=None, n_sel_out=None, stream=None) -> None:
+    rc = LIB.qsa_decode(ctypes.byref(cfg.c()), ctypes.byref(rows.c()), ctypes.byref(cache.c()),
+                        _ptr(k_new, torch.bfloat16), _ptr(v_new, torch.bfloat16),
+                        _ptr(idx_k_new, torch.bfloat16), _ptr(q_idx, torch.bfloat16),
+                        _ptr(w, torch.float32), _ptr(q, torch.bfloat16),
+                        _ptr(sel_out, torch.int32), _ptr(n_sel_out, torch.int32),
+                        _ptr(out, torch.bfloat16), _ptr(ws), ws.numel() * ws.element_size(),
+                        _ptr(status, torch.int32), _stream(stream))
+    _check(rc, "qsa_decode", f"capacity {cache.capacity} tokens per sequence" if rc == QSA_ERR_CAPACITY else "")
+
+
+def workspace(cfg: Config, max_rows: int, max_blocks_per_row: int, device="cuda") -> torch.Tensor:
+    """A device workspace of qsa_workspace_bytes() bytes (uint8)."""
+    n = qsa_workspace_bytes(cfg, max_rows, max_blocks_per_row)
+    if n == 0:
+        raise QsaError(QSA_ERR_UNSUPPORTED, "qsa_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)

@@ -137,10 +137,11 @@ class Shapes:
         return self.budget + self.ratio - 1
 
 
-def token_rows(sh: Shapes, seed: int, seq: int, positions, epoch=0, device="cpu"):
+def token_rows(sh: Shapes, seed: int, seq: int, positions, epoch=0, device="cpu", int_range=(-8, 8)):
     """K, V, raw index key rows for the given token positions of one sequence.
 
     Returns (k [n, Hkv, D] bf16, v [n, Hkv, D] bf16, idx_k [n, d_I] bf16).
+    Index keys are integers uniform in int_range (inclusive).
     """
     pos = _as_i64(positions, device)
     n = pos.numel()
@@ -149,11 +150,11 @@ def token_rows(sh: Shapes, seed: int, seq: int, positions, epoch=0, device="cpu"
     ib = token_base(seed, STREAM_IDX_K, epoch, seq, pos, device)
     k = normal_bf16(kb, sh.n_kv_heads * sh.head_dim).reshape(n, sh.n_kv_heads, sh.head_dim)
     v = normal_bf16(vb, sh.n_kv_heads * sh.head_dim).reshape(n, sh.n_kv_heads, sh.head_dim)
-    ik = int_bf16(ib, sh.idx_dim).reshape(n, sh.idx_dim)
+    ik = int_bf16(ib, sh.idx_dim, *int_range).reshape(n, sh.idx_dim)
     return k, v, ik
 
 
-def query_rows(sh: Shapes, seed: int, seq: int, positions, epoch=0, device="cpu"):
+def query_rows(sh: Shapes, seed: int, seq: int, positions, epoch=0, device="cpu", int_range=(-8, 8)):
     """Query-side inputs of the rows at the given positions of one sequence.
 
     Returns (q [n, Hq, D] bf16, q_idx [n, H_I, d_I] bf16, w [n, H_I] fp32).
@@ -164,7 +165,7 @@ def query_rows(sh: Shapes, seed: int, seq: int, positions, epoch=0, device="cpu"
     ib = token_base(seed, STREAM_Q_IDX, epoch, seq, pos, device)
     wb = token_base(seed, STREAM_W, epoch, seq, pos, device)
     q = normal_bf16(qb, sh.n_q_heads * sh.head_dim).reshape(n, sh.n_q_heads, sh.head_dim)
-    qi = int_bf16(ib, sh.n_idx_heads * sh.idx_dim).reshape(n, sh.n_idx_heads, sh.idx_dim)
+    qi = int_bf16(ib, sh.n_idx_heads * sh.idx_dim, *int_range).reshape(n, sh.n_idx_heads, sh.idx_dim)
     w = pow2_weights(wb, sh.n_idx_heads).reshape(n, sh.n_idx_heads)
     return q, qi, w
 

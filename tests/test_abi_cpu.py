@@ -1,0 +1,118 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every entry point include/qsa.h declares, validates
+configurations and arguments on the host, and the oracle and the product
+never import each other."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qsa.h")
+
+
+@pytest.fixture(scope="module")
+def Q():
+    from indexer_selected_sparse_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build_library()
+    from indexer_selected_sparse_gb300 import qsa
+    return qsa
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|int|size_t)\s*(qsa_\w+)\s*\(", text, re.M)))
+
+
+def test_every_declared_symbol_is_exported(Q):
+    names = declared_functions()
+    assert len(names) >= 9
+    lib = ctypes.CDLL(Q.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in qsa.h but not exported"
+    assert set(names) == set(Q.EXPORTED)
+
+
+def test_config_check(Q):
+    ok = Q.Config(4, 2048, 64, 128, 32, 4)
+    assert Q.qsa_config_check(ok) == Q.QSA_OK
+    assert Q.qsa_config_check(Q.Config(4, 256, 4, 64, 8, 1)) == Q.QSA_OK
+    bad = [Q.Config(3, 2048, 64, 128, 32, 4),     # ratio not a power of two
+           Q.Config(4, 2050, 64, 128, 32, 4),     # budget not a multiple of ratio
+           Q.Config(4, 8196, 64, 128, 32, 4),     # K > 2048
+           Q.Config(4, 2048, 65, 128, 32, 4),     # too many index heads
+           Q.Config(4, 2048, 64, 96, 32, 4),      # d_I
+           Q.Config(4, 2048, 64, 128, 32, 3),     # Hkv
+           Q.Config(4, 2048, 64, 128, 64, 4),     # group of 16
+           Q.Config(4, 2048, 64, 128, 32, 4, head_dim=64),
+           Q.Config(4, 2048, 64, 128, 32, 4, page_size=32)]
+    for c in bad:
+        assert Q.qsa_config_check(c) == Q.QSA_ERR_UNSUPPORTED, c
+
+
+def test_workspace_bytes(Q):
+    c = Q.Config(4, 2048, 64, 128, 32, 4)
+    a = Q.qsa_workspace_bytes(c, 32, 8200)
+    b = Q.qsa_workspace_bytes(c, 64, 8200)
+    assert a > 32 * 8200 * 4 and b > a
+    assert Q.qsa_workspace_bytes(Q.Config(3, 2048, 64, 128, 32, 4), 32, 8200) == 0
+
+
+def test_strerror(Q):
+    assert Q.qsa_strerror(0) == "ok"
+    assert "ingested" in Q.qsa_strerror(Q.QSA_ERR_DESYNC)
+    assert "page" in Q.qsa_strerror(Q.QSA_ERR_CAPACITY)
+    assert Q.qsa_strerror(1234) == "unknown status"
+
+
+def test_null_arguments_rejected_on_host(Q):
+    cfg = Q.Config(4, 2048, 64, 128, 32, 4).c()
+    lib = Q.LIB
+    assert lib.qsa_append(ctypes.byref(cfg), None, None, None, None, None, None, None) == Q.QSA_ERR_INVALID_ARG
+    assert lib.qsa_decode(ctypes.byref(cfg), None, None, None, None, None, None, None, None, None, None,
+                          None, None, 0, None, None) == Q.QSA_ERR_INVALID_ARG
+    rows = Q.qsa_rows(2, 1, None, None, None, 0)
+    assert lib.qsa_index_score(ctypes.byref(cfg), ctypes.byref(rows), None, None, None, None, 0, None,
+                               None) == Q.QSA_ERR_INVALID_ARG
+    assert lib.qsa_rewind(ctypes.byref(cfg), 1, None, None, None, None, None) == Q.QSA_ERR_INVALID_ARG
+    # misaligned pointers are rejected before any launch
+    cache = Q.qsa_cache(16, 1, 4, 4, 16, 16, 16, 16, 16)
+    rows = Q.qsa_rows(1, 1, 16, 16, None, 0)
+    assert lib.qsa_append(ctypes.byref(cfg), ctypes.byref(rows), ctypes.byref(cache), 18, 16, 16, 16,
+                          None) == Q.QSA_ERR_INVALID_ARG
+    # too many rows for one launch grid
+    rows = Q.qsa_rows(70000, 1, 16, 16, None, 0)
+    assert lib.qsa_append(ctypes.byref(cfg), ctypes.byref(rows), ctypes.byref(cache), 16, 16, 16, 16,
+                          16) == Q.QSA_ERR_INVALID_ARG
+
+
+def test_host_capacity_check(Q):
+    import numpy as np
+    cfg = Q.Config(4, 256, 4, 64, 8, 1).c()
+    cache = Q.qsa_cache(16, 1, 4, 4, 16, 16, 16, 16, 16)      # 4 pages x 64 = 256 tokens
+    pos = (ctypes.c_int32 * 1)(250)
+    rows = Q.qsa_rows(1, 7, 16, 16, ctypes.cast(pos, ctypes.c_void_p), 0)
+    assert Q.LIB.qsa_append(ctypes.byref(cfg), ctypes.byref(rows), ctypes.byref(cache), 16, 16, 16, 16,
+                            16) == Q.QSA_ERR_CAPACITY
+
+
+def test_missing_library_fails_loudly(Q, monkeypatch):
+    monkeypatch.setattr(Q, "_LIB_PATH", "/nonexistent/libqsa.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        Q._load()
+
+
+def test_oracle_and_product_do_not_import_each_other():
+    pkg = os.path.join(ROOT, "indexer_selected_sparse_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle", text, re.M), f
+                assert "qsa_oracle" not in text, f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith(".py"):
+            text = open(os.path.join(ROOT, "oracle", f)).read()
+            assert "indexer_selected_sparse_gb300" not in text, f

@@ -1,0 +1,174 @@
+"""GPU parity against the CPU oracle on the five workloads, at their full sizes
+and in the launch configuration the benchmark times (the fused qsa_decode).
+
+Selected block sets must match bit-exactly; outputs within max-abs 2e-2 and
+rel-L2 1e-3 of the bf16-rounded oracle. At full size the oracle runs on
+sampled rows, which it computes one by one from the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+from indexer_selected_sparse_gb300 import synth as S
+from oracle import qsa_oracle as O
+from tests.gpu_harness import GpuState, OracleSeq, bits, compare_row
+
+pytestmark = pytest.mark.gpu
+
+
+def check_rows(g: GpuState, res, seqs_sampled, pos0, R, oracles):
+    topk = g.cfg.topk
+    sel = res["sel"].cpu().numpy()
+    nsel = res["n_sel"].cpu().numpy()
+    out = bits(res["out"])
+    errs = []
+    for i, s in enumerate(g.slots):
+        if s not in seqs_sampled:
+            continue
+        for j in range(R):
+            row = i * R + j
+            ref = oracles[s].row(pos0[i] + j)
+            errs.append(compare_row(out[row], sel[row], int(nsel[row]), ref, topk))
+    return errs
+
+
+def test_tiny_decode_every_row_and_pools():
+    wl = S.workload(1)
+    g = GpuState(wl)
+    g.append_prefix(chunk=1000)
+    pos0 = list(wl.prefixes)
+    res = g.decode(pos0, 1)
+    g.check_status()
+    assert g.cache.ingested.cpu().tolist()[: wl.n_seq] == [p + 1 for p in pos0]
+    orc = OracleSeq(wl, 0, pos0[0] + 1, lazy_kv=False)
+    # pools: raw keys, K/V rows and every compressed key bit-exact
+    n = pos0[0] + 1
+    assert np.array_equal(g.logical_rows(g.cache.idxraw_pool, 0, np.arange(n)), orc.st.idx_raw[:n])
+    assert np.array_equal(g.logical_rows(g.cache.k_pool, 0, np.arange(n)), orc.st.K[:n])
+    assert np.array_equal(g.logical_rows(g.cache.v_pool, 0, np.arange(n)), orc.st.V[:n])
+    nb = n // wl.shapes.ratio
+    assert np.array_equal(g.logical_blocks(0, nb), orc.st.idx_blk[:nb])
+    check_rows(g, res, {0}, pos0, 1, {0: orc})
+
+
+def test_steady_decode_batch32_prefix32k_four_steps():
+    wl = S.workload(2)
+    g = GpuState(wl, extra_tokens=16)
+    g.append_prefix()
+    sampled = [0, 13, 31]
+    oracles = {s: OracleSeq(wl, s, wl.prefixes[0] + 4) for s in sampled}
+    pos0 = list(wl.prefixes)
+    for step in range(4):                       # the tail cycles 1 -> 2 -> 3 -> 0
+        res = g.decode(pos0, 1)
+        g.check_status()
+        pos0 = [p + 1 for p in pos0]
+        assert g.cache.ingested.cpu().tolist() == pos0
+        assert (res["n_sel"].cpu() == wl.shapes.topk).all()
+        check_rows(g, res, set(sampled), [p - 1 for p in pos0], 1, oracles)
+
+
+def test_ragged_decode_batch64_eight_steps():
+    wl = S.workload(3)
+    g = GpuState(wl, extra_tokens=16)
+    g.append_prefix()
+    pre = wl.prefixes
+    by = {p: i for i, p in enumerate(pre)}
+    longest = int(np.argmax(pre))
+    sampled = sorted({by[2050], by[2051], by[2052], by[600], longest, 7, 40})
+    oracles = {s: OracleSeq(wl, s, pre[s] + 8) for s in sampled}
+    pos0 = list(pre)
+    for step in range(8):
+        res = g.decode(pos0, 1)
+        g.check_status()
+        pos0 = [p + 1 for p in pos0]
+        assert g.cache.ingested.cpu().tolist() == pos0     # ingested == pos after every append
+        check_rows(g, res, set(sampled), [p - 1 for p in pos0], 1, oracles)
+        nsel = res["n_sel"].cpu().numpy()
+        vis = np.array(pos0)
+        dense = vis // wl.shapes.ratio <= wl.shapes.topk
+        assert np.array_equal(nsel[dense], vis[dense] // wl.shapes.ratio)
+        assert (nsel[~dense] == wl.shapes.topk).all()
+
+
+def test_verify_then_rewind_then_decode():
+    wl = S.workload(4)
+    R = wl.rows_per_seq
+    g = GpuState(wl, extra_tokens=16)
+    g.append_prefix()
+    sampled = [0, 5, 15]
+    p = wl.prefixes[0]
+    # verify: R causal rows per sequence, each with its own top-K
+    oracles = {s: OracleSeq(wl, s, p + R) for s in sampled}
+    res = g.decode([p] * wl.n_seq, R)
+    g.check_status()
+    check_rows(g, res, set(sampled), [p] * wl.n_seq, R, oracles)
+    # reject 0..2 rows per sequence and rewind the counters
+    rej = S.reject_counts(wl.seed, wl.n_seq)
+    g.rewind(rej)
+    g.check_status()
+    pos0 = [p + R - r for r in rej]
+    assert g.cache.ingested.cpu().tolist() == pos0
+    # four decode steps with fresh rows at the re-used positions
+    steps = wl.extra["decode_after"]
+    oracles = {s: OracleSeq(wl, s, pos0[s] + steps, hist=g.hist[s]) for s in sampled}
+    outs = []
+    for step in range(steps):
+        res = g.decode(pos0, 1)
+        g.check_status()
+        check_rows(g, res, set(sampled), pos0, 1, oracles)
+        outs.append((bits(res["out"]), res["sel"].cpu().numpy()))
+        pos0 = [q + 1 for q in pos0]
+        assert g.cache.ingested.cpu().tolist() == pos0
+    # never drafting: append the accepted tokens directly, decode the same steps
+    h = GpuState(wl, extra_tokens=16)
+    for s in h.slots:
+        h.hist[s] = g.hist[s]
+    h.append_prefix()
+    acc = [R - r for r in rej]
+    h.decode([p] * wl.n_seq, 1)   # first accepted token (every sequence keeps >= 1)
+    for extra in range(1, R):
+        idx = [i for i in range(wl.n_seq) if acc[i] > extra]
+        if idx:
+            h.decode([p + extra] * len(idx), 1, seqs=idx)
+    h.check_status()
+    q0 = [p + a for a in acc]
+    assert h.cache.ingested.cpu().tolist() == q0
+    for step in range(steps):
+        res = h.decode(q0, 1)
+        o, s_ = outs[step]
+        assert np.array_equal(bits(res["out"]), o)
+        assert np.array_equal(res["sel"].cpu().numpy(), s_)
+        q0 = [q + 1 for q in q0]
+
+
+def test_chunked_prefill_8193_rows():
+    wl = S.workload(5)
+    g = GpuState(wl, extra_tokens=16)
+    g.append_prefix()
+    p = wl.prefixes[0]
+    C = wl.rows_per_seq
+    res = g.decode([p], C)
+    g.check_status()
+    orc = OracleSeq(wl, 0, p + C)
+    sel = res["sel"].cpu().numpy(); nsel = res["n_sel"].cpu().numpy(); out = bits(res["out"])
+    for j in list(range(0, C, 512)) + [1, 2, 3, 4, C - 2, C - 1]:
+        ref = orc.row(p + j)
+        compare_row(out[j], sel[j], int(nsel[j]), ref, g.cfg.topk)
+    # chunks {4096, 4097} give the same sets and outputs, bit for bit
+    h = GpuState(wl, extra_tokens=16)
+    h.append_prefix()
+    r1 = h.decode([p], 4096, inputs=slice_inputs(res["inputs"], 0, 4096))
+    r2 = h.decode([p + 4096], 4097, inputs=slice_inputs(res["inputs"], 4096, C))
+    assert np.array_equal(np.concatenate([bits(r1["out"]), bits(r2["out"])]), out)
+    assert np.array_equal(np.concatenate([r1["sel"].cpu().numpy(), r2["sel"].cpu().numpy()]), sel)
+    # the last rows again token by token as decode steps
+    k = GpuState(wl, extra_tokens=16)
+    k.append_prefix()
+    k.decode([p], C - 8, inputs=slice_inputs(res["inputs"], 0, C - 8))
+    for j in range(C - 8, C):
+        r = k.decode([p + j], 1, inputs=slice_inputs(res["inputs"], j, j + 1))
+        assert np.array_equal(bits(r["out"])[0], out[j])
+        assert np.array_equal(r["sel"].cpu().numpy()[0], sel[j])
+
+
+def slice_inputs(inp, a, b):
+    return {k: v[a:b].contiguous() for k, v in inp.items()}
