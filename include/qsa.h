@@ -233,6 +233,29 @@ int qsa_decode(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cac
                int32_t *sel_out, int32_t *n_sel_out, qsa_bf16 *out,
                void *ws, size_t ws_bytes, int32_t *status, cudaStream_t stream);
 
+/* Size of the fixed scratch array behind qsa_gather_attn_static. */
+#define QSA_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* Gather attention without a workspace (the pages have no counterpart; this
+ * is a convenience of this library). Same computation, arguments and outputs
+ * as qsa_gather_attn, minus ws / ws_bytes: the split partials live in a
+ * QSA_STATIC_SCRATCH_BYTES array compiled into the library, for callers that
+ * cannot allocate device memory themselves (a plugin that only receives the
+ * framework's input and output tensors, or a loop where cudaMalloc is not
+ * allowed). The call allocates nothing.
+ *   - Every GPU that loads the library holds that array until the process
+ *     exits. A call whose partials would not fit (about 283 KB per row at
+ *     Hq = 32, budget 2048: up to 118 rows) returns QSA_ERR_WORKSPACE.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents; calls that overlap on the GPU race and give wrong results.
+ *     Nothing in it needs to start at zero.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture. */
+int qsa_gather_attn_static(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
+                           const qsa_bf16 *q, const int32_t *sel, const int32_t *n_sel,
+                           qsa_bf16 *out, int32_t *status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

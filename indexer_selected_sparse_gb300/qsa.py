@@ -32,7 +32,9 @@ QSA_ERR_PAGE = 8
 QSA_ERR_REWIND = 9
 
 EXPORTED = ("qsa_strerror", "qsa_config_check", "qsa_workspace_bytes", "qsa_append",
-            "qsa_rewind", "qsa_index_score", "qsa_topk_select", "qsa_gather_attn", "qsa_decode")
+            "qsa_rewind", "qsa_index_score", "qsa_topk_select", "qsa_gather_attn", "qsa_decode",
+            "qsa_gather_attn_static")
+QSA_STATIC_SCRATCH_BYTES = 32 << 20
 
 
 def _load() -> ctypes.CDLL:
@@ -89,6 +91,8 @@ LIB.qsa_topk_select.restype = _I
 LIB.qsa_topk_select.argtypes = [_CFG, _ROWS, _P, _I, _P, _P, _P, _P]
 LIB.qsa_gather_attn.restype = _I
 LIB.qsa_gather_attn.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+LIB.qsa_gather_attn_static.restype = _I
+LIB.qsa_gather_attn_static.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P]
 LIB.qsa_decode.restype = _I
 LIB.qsa_decode.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                            ctypes.c_size_t, _P, _P]
@@ -261,6 +265,17 @@ def qsa_gather_attn(cfg: Config, rows: Rows, cache: PagedCache, q, sel, n_sel, o
                              _ptr(out, torch.bfloat16), _ptr(ws), ws.numel() * ws.element_size(),
                              _ptr(status, torch.int32), _stream(stream))
     _check(rc, "qsa_gather_attn")
+
+
+def qsa_gather_attn_static(cfg: Config, rows: Rows, cache: PagedCache, q, sel, n_sel, out,
+                           status=None, stream=None) -> None:
+    """qsa_gather_attn for callers that cannot pass a workspace: the split
+    partials live in a fixed array inside the library (shared by every call on
+    the device; calls must not overlap on the GPU). Allocates nothing."""
+    rc = LIB.qsa_gather_attn_static(ctypes.byref(cfg.c()), ctypes.byref(rows.c()), ctypes.byref(cache.c()),
+                                    _ptr(q, torch.bfloat16), _ptr(sel, torch.int32), _ptr(n_sel, torch.int32),
+                                    _ptr(out, torch.bfloat16), _ptr(status, torch.int32), _stream(stream))
+    _check(rc, "qsa_gather_attn_static")
 
 
 def qsa_decode(cfg: Config, rows: Rows, cache: PagedCache, k_new, v_new, idx_k_new, q_idx, w, q,
