@@ -37,7 +37,7 @@ if ROOT not in sys.path:
 METRIC = "decode query-rows/sec and achieved HBM GB/s (% of roofline) at batch×prefix"
 WORKLOAD_ID = 2            # steady-state decode, batch 32 x 32k prefix
 N_BATCHES = 6              # default rotating independent batches (L2 defeat)
-KERNELS_PER_STEP = 6       # append, score, select, attention, merge, commit
+KERNELS_PER_STEP = 5       # append, score, select, attention, merge (+ commit)
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -375,7 +375,7 @@ def stage_breakdown(args, Q, torch, cfg, sh, cache, batches, ws, status, stream,
     if dominant == "topk_select":
         dominant = "gather_attn" if stage_ms["gather_attn"] >= stage_ms["index_score"] else "index_score"
     ach = stage_bytes[dominant] / (stage_ms[dominant] * 1e-3) / 1e9
-    roofline = {"kernel": {"gather_attn": "attn_kernel<4> + merge_kernel", "index_score": "score_kernel<128,64>",
+    roofline = {"kernel": {"gather_attn": "attn_kernel<4> + merge_kernel", "index_score": "score_tc_kernel<128>",
                            "append": "append_kernel"}[dominant],
                 "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_gbs, "unit": "GB/s",
                 "frac": round(ach / hbm_gbs, 4), "peak_kind": peak_kind + " (hbm_gbs, copy)",

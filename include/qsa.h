@@ -69,7 +69,9 @@ typedef enum qsa_status {
   QSA_ERR_CUDA_FATAL = 6,   /* sticky CUDA error: the context is lost */
   QSA_ERR_DESYNC = 7,       /* device: append position != ingested counter */
   QSA_ERR_PAGE = 8,         /* device: page id outside [0, num_pages) */
-  QSA_ERR_REWIND = 9        /* device: rewind by more than was ingested */
+  QSA_ERR_REWIND = 9,       /* device: rewind by more than was ingested */
+  QSA_ERR_TIMEOUT = 10      /* device: an internal wait of a kernel expired (1 s);
+                               the kernel released its resources and returned */
 } qsa_status;
 
 /* Shape of the method. Supported set (checked by qsa_config_check):

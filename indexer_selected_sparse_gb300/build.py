@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libqsa.so")
 SOURCES = ["qsa_api.cu", "qsa_append.cu", "qsa_score.cu", "qsa_select.cu", "qsa_attn.cu",
-           "qsa_static.cu"]
+           "qsa_static.cu", "qsa_score_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -156,6 +156,7 @@ const char *qsa_strerror(int status) {
     case QSA_ERR_DESYNC: return "append position does not match the ingested counter";
     case QSA_ERR_PAGE: return "page id outside the pool";
     case QSA_ERR_REWIND: return "rewind by more tokens than were ingested";
+    case QSA_ERR_TIMEOUT: return "an internal wait of a kernel expired";
     default: return "unknown status";
   }
 }
@@ -188,7 +189,7 @@ int qsa_append(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cac
                                 cache->ingested, k_new, v_new, idx_k_new, status, stream);
   if (e == cudaSuccess)
     e = launch_commit(rows->n_seq, rows->rows_per_seq, cache->max_pages * cfg->page_size,
-                      rows->seq_ids, rows->pos0, cache->ingested, rows->advance, stream);
+                      rows->seq_ids, rows->pos0, cache->ingested, rows->advance, false, stream);
   return cuda_status(e);
 }
 
@@ -215,7 +216,7 @@ int qsa_index_score(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache
   if (ld_scores < max_blk || ld_scores % 4 != 0) return QSA_ERR_INVALID_ARG;
   const Shape sh = make_shape(cfg);
   return cuda_status(launch_score(sh, rows->n_seq, rows->rows_per_seq, rows->seq_ids, rows->pos0,
-                                  view(cache), q_idx, w, scores, ld_scores, status, stream));
+                                  view(cache), q_idx, w, scores, ld_scores, status, false, stream));
 }
 
 int qsa_topk_select(const qsa_config *cfg, const qsa_rows *rows, const float *scores,
@@ -232,7 +233,7 @@ int qsa_topk_select(const qsa_config *cfg, const qsa_rows *rows, const float *sc
   return cuda_status(launch_select(sh, rows->n_seq, rows->rows_per_seq, rows->pos0, scores,
                                    ld_scores, sel, n_sel, ld_scores,
                                    cap > 0x7fffffff ? 0x7fffffff : static_cast<int>(cap), status,
-                                   stream));
+                                   false, stream));
 }
 
 int qsa_gather_attn(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
@@ -249,7 +250,8 @@ int qsa_gather_attn(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache
   const Shape sh = make_shape(cfg);
   if (ws_bytes < attn_partial_bytes(sh, n_rows)) return QSA_ERR_WORKSPACE;
   return cuda_status(launch_attn(sh, rows->n_seq, rows->rows_per_seq, rows->seq_ids, rows->pos0,
-                                 view(cache), q, sel, n_sel, out, ws, status, stream));
+                                 view(cache), q, sel, n_sel, out, ws, status, false, CommitArgs{},
+                                 stream));
 }
 
 int qsa_decode(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
@@ -288,18 +290,23 @@ int qsa_decode(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cac
                                 v_new, idx_k_new, status, stream);
   if (e == cudaSuccess)
     e = launch_score(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, q_idx, w, scores, ld,
-                     status, stream);
+                     status, true, stream);
   if (e == cudaSuccess)
     e = launch_select(sh, rows->n_seq, R, rows->pos0, scores, ld, sel, n_sel, ld, cap_tokens,
-                      status, stream);
+                      status, true, stream);
+  // the counter (and, with rows->advance, pos0) moves last, inside the merge
+  // kernel: every stage before it reads the pre-step position
+  CommitArgs commit;
+  commit.n_seq = rows->n_seq;
+  commit.R = R;
+  commit.capacity = cap_tokens;
+  commit.advance = rows->advance;
+  commit.seq_ids = rows->seq_ids;
+  commit.pos0 = rows->pos0;
+  commit.ingested = cache->ingested;
   if (e == cudaSuccess)
     e = launch_attn(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, q, sel, n_sel, out,
-                    base + L.partials, status, stream);
-  // the counter (and, with rows->advance, pos0) moves last: every stage above
-  // reads the pre-step position
-  if (e == cudaSuccess)
-    e = launch_commit(rows->n_seq, R, cap_tokens, rows->seq_ids, rows->pos0, cache->ingested,
-                      rows->advance, stream);
+                    base + L.partials, status, true, commit, stream);
   return cuda_status(e);
 }
 

@@ -26,6 +26,7 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
               uint16_t *__restrict__ blk_pool, const int32_t *__restrict__ ingested,
               const uint16_t *__restrict__ k_new, const uint16_t *__restrict__ v_new,
               const uint16_t *__restrict__ idx_new, int32_t *status) {
+  pdl_trigger();  // the first kernel of the step: its successor may start its prologue
   const int i = blockIdx.x;
   const int s = seq_ids[i];
   const int p0 = pos0[i];
@@ -122,6 +123,7 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
 __global__ void commit_kernel(int n_seq, int R, int capacity, const int32_t *__restrict__ seq_ids,
                               int32_t *__restrict__ pos0, int32_t *__restrict__ ingested,
                               int advance) {
+  pdl_wait();  // every earlier kernel of the step reads pos0 / ingested
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n_seq) return;
   const int s = seq_ids[i];
@@ -165,11 +167,10 @@ cudaError_t launch_append(const Shape &sh, int n_seq, int R, const int32_t *seq_
 }
 
 cudaError_t launch_commit(int n_seq, int R, int capacity, const int32_t *seq_ids,
-                          int32_t *pos0, int32_t *ingested, int advance, cudaStream_t st) {
+                          int32_t *pos0, int32_t *ingested, int advance, bool pdl, cudaStream_t st) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
-  commit_kernel<<<(n_seq + 127) / 128, 128, 0, st>>>(n_seq, R, capacity, seq_ids, pos0, ingested,
-                                                     advance);
-  return cudaGetLastError();
+  return launch_kernel(pdl, commit_kernel, dim3((n_seq + 127) / 128), dim3(128), 0, st, n_seq, R,
+                       capacity, seq_ids, pos0, ingested, advance);
 }
 
 cudaError_t launch_rewind(int n_seq, const int32_t *seq_ids, const int32_t *n_drop,

@@ -20,8 +20,8 @@
 //   P^T -> B operand via movmatrix.trans; P split as bf16 hi + bf16 lo so the
 //   weights keep ~16 significant bits
 //   O^T[128 x 8] += V^T . P^T                   (ldmatrix.trans of V, x16)
-// The split writes (m, l, acc) in fp32; the merge kernel combines splits and
-// rounds o = acc / l to bf16.
+// The split writes (m, l, acc) in fp32; the merge kernel combines the splits in
+// split order and rounds o = acc / l to bf16.
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -30,6 +30,7 @@ namespace {
 constexpr int kAttnThreads = 128;
 constexpr int kAttnWarps = 4;
 constexpr int kStages = 3;
+constexpr int kSplitSlots = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int HKV>
@@ -56,7 +57,12 @@ attn_kernel(Shape sh, int R, int n_split, int split_len, const int32_t *__restri
             int32_t *status) {
   using G = AttnGeom<HKV>;
   extern __shared__ __align__(128) uint8_t smem[];
+  // after the stage buffers: the token row (page * P + offset) of every slot of
+  // this split, or -1
+  int32_t *slot_row = reinterpret_cast<int32_t *>(smem + kStages * G::kStageBytes);
 
+  pdl_wait();  // sel / n_sel come from the select kernel
+  pdl_trigger();
   const int row = blockIdx.y;
   const int sp = blockIdx.x;
   const int i = row / R;
@@ -70,8 +76,9 @@ attn_kernel(Shape sh, int R, int n_split, int split_len, const int32_t *__restri
   const int n_body = n_sel * r;
   const int tail0 = n_blk * r;
   const int n_slots = row_ok ? n_body + (visible - tail0) : 0;
-  const int slot_lo = min(n_slots, sp * split_len);
-  const int slot_hi = min(n_slots, slot_lo + split_len);
+  const int seg = split_len;  // fixed cut: independent of the batch
+  const int slot_lo = min(n_slots, sp * seg);
+  const int slot_hi = min(n_slots, slot_lo + seg);
   const int n_chunks = (slot_hi - slot_lo + G::kChunk - 1) / G::kChunk;
   const int32_t *sel_row = sel + static_cast<size_t>(row) * sh.topk;
   const int32_t *ptab = cv.page_table + static_cast<size_t>(s) * cv.max_pages;
@@ -83,24 +90,37 @@ attn_kernel(Shape sh, int R, int n_split, int split_len, const int32_t *__restri
   const int sub = warp / HKV;          // 16-slot sub-tile of the stage
   const int smem_u = smem_u32(smem);
 
+  // ---- resolve every slot of the split to its token row once, all in parallel:
+  // the stage loads below then need no global lookups
+  // the table covers whole stages: entries past the split's end are -1
+  const int table = (seg + G::kChunk - 1) / G::kChunk * G::kChunk;
+  for (int x = tid; x < table; x += kAttnThreads) {
+    const int j = slot_lo + x;
+    int rowidx = -1;
+    if (j < slot_hi) {
+      const int t = slot_token(j, n_body, sh.log2_ratio, r, tail0, sel_row);
+      const int page = (t >= 0 && t < visible) ? ptab[t >> sh.log2_page] : -1;
+      if (page >= 0 && page < cv.num_pages)
+        rowidx = page * P + (t & (P - 1));
+      else
+        report(status, QSA_ERR_PAGE);
+    }
+    slot_row[x] = rowidx;
+  }
+  __syncthreads();
+
   // ---- gather of one stage: thread -> (slot, 16 of its 32*HKV 16-byte pieces)
   const int my_slot = tid / G::kThreadsPerSlot;
   const int my_part = tid % G::kThreadsPerSlot;
   auto load_stage = [&](int chunk_idx, int buf) {
-    const int j = slot_lo + chunk_idx * G::kChunk + my_slot;
+    const int rowidx = slot_row[chunk_idx * G::kChunk + my_slot];
     const uint16_t *kbase = cv.k_pool, *vbase = cv.v_pool;
     int bytes = 0;
-    if (j < slot_hi) {
-      const int t = slot_token(j, n_body, sh.log2_ratio, r, tail0, sel_row);
-      const int page = (t >= 0 && t < visible) ? ptab[t >> sh.log2_page] : -1;
-      if (page >= 0 && page < cv.num_pages) {
-        const size_t off = (static_cast<size_t>(page) * P + (t & (P - 1))) * HKV * kHeadDim;
-        kbase = cv.k_pool + off;
-        vbase = cv.v_pool + off;
-        bytes = 16;
-      } else {
-        report(status, QSA_ERR_PAGE);
-      }
+    if (rowidx >= 0) {
+      const size_t off = static_cast<size_t>(rowidx) * HKV * kHeadDim;
+      kbase = cv.k_pool + off;
+      vbase = cv.v_pool + off;
+      bytes = 16;
     }
     const uint32_t stage = smem_u + buf * G::kStageBytes;
 #pragma unroll
@@ -281,60 +301,91 @@ attn_kernel(Shape sh, int R, int n_split, int split_len, const int32_t *__restri
       l_run[1] = lsum[1];
     }
   }
-  if (sub != 0) return;
-
   const size_t base = (static_cast<size_t>(row) * n_split + sp) * sh.hq + g * group;
+  if (sub == 0) {
 #pragma unroll
-  for (int c2 = 0; c2 < 2; ++c2) {
-    const int col = 2 * (lane & 3) + c2;
-    if (lane < 4 && col < group) {
-      part_m[base + col] = m_run[c2];
-      part_l[base + col] = l_run[c2];
+    for (int c2 = 0; c2 < 2; ++c2) {
+      const int col = 2 * (lane & 3) + c2;
+      if (lane < 4 && col < group) {
+        part_m[base + col] = m_run[c2];
+        part_l[base + col] = l_run[c2];
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d0 = mt * 16 + (lane >> 2);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int col = 2 * (lane & 3) + (c & 1);
+        if (col < group) part_acc[(base + col) * kHeadDim + d0 + (c >> 1) * 8] = acc[mt][c];
+      }
     }
   }
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const int d0 = mt * 16 + (lane >> 2);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int col = 2 * (lane & 3) + (c & 1);
-      if (col < group) part_acc[(base + col) * kHeadDim + d0 + (c >> 1) * 8] = acc[mt][c];
-    }
-  }
+
 }
 
-// One CTA per (row, head): 128 threads, one per output dim.
-__global__ void __launch_bounds__(kHeadDim)
-merge_kernel(int hq, int n_split, const float *__restrict__ part_m,
+// Split merge: one CTA per (row, KV head): 256 threads, thread t combines
+// dims 4*(t%32) .. +3 of query head (KV head's first head + t/32) over the
+// splits, in split order, so the result does not depend on how the splits were
+// scheduled. In the fused step the CTA (0, 0) also commits the step (advances
+// ingested, and pos0 when asked): every earlier kernel of the step, including
+// the attention kernel this one waits for, has finished reading them.
+constexpr int kMergeThreads = 256;
+
+__global__ void __launch_bounds__(kMergeThreads)
+merge_kernel(int hq, int hkv, int n_split, const float *__restrict__ part_m,
              const float *__restrict__ part_l, const float *__restrict__ part_acc,
-             uint16_t *__restrict__ out) {
-  const int row = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+             uint16_t *__restrict__ out, CommitArgs cm) {
+  pdl_wait();  // the split partials come from the attention kernel
+  pdl_trigger();
+  const int row = blockIdx.x, g = blockIdx.y, t = threadIdx.x;
+  if (cm.n_seq > 0 && row == 0 && g == 0) {
+    for (int i = t; i < cm.n_seq; i += kMergeThreads) {
+      const int s = cm.seq_ids[i];
+      const int p0 = cm.pos0[i];
+      if (cm.ingested[s] == p0 && p0 >= 0 && p0 + cm.R <= cm.capacity) {
+        cm.ingested[s] = p0 + cm.R;
+        if (cm.advance) cm.pos0[i] = p0 + cm.R;
+      }
+    }
+  }
+  const int group = hq / hkv;
+  const int hl = t >> 5;
+  if (hl >= group) return;
+  const int h = g * group + hl;
+  const int d4 = (t & 31) * 4;
   const size_t b0 = static_cast<size_t>(row) * n_split * hq + h;
   float m = -INFINITY;
-  for (int s = 0; s < n_split; ++s) m = fmaxf(m, part_m[b0 + static_cast<size_t>(s) * hq]);
+  for (int s = 0; s < n_split; ++s) m = fmaxf(m, __ldg(&part_m[b0 + static_cast<size_t>(s) * hq]));
   const float ref = m == -INFINITY ? 0.f : m;
-  float l = 0.f, a = 0.f;
+  float l = 0.f;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
   for (int s = 0; s < n_split; ++s) {
     const size_t k = b0 + static_cast<size_t>(s) * hq;
-    const float wgt = exp2f(part_m[k] - ref);
-    l += wgt * part_l[k];
-    a += wgt * part_acc[k * kHeadDim + d];
+    const float wgt = exp2f(__ldg(&part_m[k]) - ref);
+    l += wgt * __ldg(&part_l[k]);
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(part_acc + k * kHeadDim + d4));
+    a.x += wgt * v.x;
+    a.y += wgt * v.y;
+    a.z += wgt * v.z;
+    a.w += wgt * v.w;
   }
-  const float o = l > 0.f ? a / l : 0.f;
-  __nv_bfloat16 ob = __float2bfloat16_rn(o);
-  out[(static_cast<size_t>(row) * hq + h) * kHeadDim + d] = *reinterpret_cast<uint16_t *>(&ob);
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  uint2 packed;
+  packed.x = pack_bf16(a.x * inv, a.y * inv);
+  packed.y = pack_bf16(a.z * inv, a.w * inv);
+  *reinterpret_cast<uint2 *>(out + (static_cast<size_t>(row) * hq + h) * kHeadDim + d4) = packed;
 }
 
 struct SplitPlan {
   int n_split, split_len;
 };
 
-// Every row is cut into splits of a fixed number of slots, whatever the batch
-// shape, so the reduction order of a row (and hence its bf16 output) is the
-// same in decode, verify and chunked-prefill form: chunked and single-shot
-// prefill agree bit for bit.
-constexpr int kSplitSlots = 128;
-
+// Every row is cut into splits of kSplitSlots slots whatever the batch shape, so
+// the reduction order of a row (and hence its bf16 output) is the same in
+// decode, verify and chunked-prefill form: chunked and single-shot prefill agree
+// bit for bit.
 SplitPlan plan_splits(const Shape &sh, int rows) {
   (void)rows;
   const int max_slots = sh.budget + sh.ratio - 1;
@@ -345,24 +396,26 @@ template <int HKV>
 cudaError_t launch_attn_t(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                           const int32_t *pos0, const CacheView &cv, const uint16_t *q,
                           const int32_t *sel, const int32_t *n_sel, uint16_t *out, void *partials,
-                          int32_t *status, cudaStream_t st) {
+                          int32_t *status, bool pdl, const CommitArgs &commit, cudaStream_t st) {
   const int rows = n_seq * R;
   const SplitPlan pl = plan_splits(sh, rows);
+  const size_t n_part = static_cast<size_t>(rows) * pl.n_split * sh.hq;
   float *pm = static_cast<float *>(partials);
-  float *pl_ = pm + static_cast<size_t>(rows) * pl.n_split * sh.hq;
-  float *pa = pl_ + static_cast<size_t>(rows) * pl.n_split * sh.hq;
-  const size_t smem = kStages * AttnGeom<HKV>::kStageBytes;
+  float *pl_ = pm + n_part;
+  float *pa = pl_ + n_part;
+  // slot table: the longest split rounded up to whole stages
+  const int table = (pl.split_len + AttnGeom<HKV>::kChunk - 1) / AttnGeom<HKV>::kChunk * AttnGeom<HKV>::kChunk;
+  const size_t smem = kStages * AttnGeom<HKV>::kStageBytes + table * sizeof(int32_t);
   auto kern = attn_kernel<HKV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<dim3(pl.n_split, rows), kAttnThreads, smem, st>>>(sh, R, pl.n_split, pl.split_len, seq_ids,
-                                                           pos0, cv, q, sel, n_sel, pm, pl_, pa,
-                                                           status);
-  e = cudaGetLastError();
+  e = launch_kernel(pdl, kern, dim3(pl.n_split, rows), dim3(kAttnThreads), smem, st, sh, R, pl.n_split,
+                    pl.split_len, seq_ids, pos0, cv, q, sel, n_sel, pm, pl_, pa, status);
   if (e != cudaSuccess) return e;
-  merge_kernel<<<dim3(rows, sh.hq), kHeadDim, 0, st>>>(sh.hq, pl.n_split, pm, pl_, pa, out);
-  return cudaGetLastError();
+  return launch_kernel(pdl, merge_kernel, dim3(rows, sh.hkv), dim3(kMergeThreads), 0, st, sh.hq, sh.hkv,
+                       pl.n_split, static_cast<const float *>(pm), static_cast<const float *>(pl_),
+                       static_cast<const float *>(pa), out, commit);
 }
 
 }  // namespace
@@ -370,25 +423,20 @@ cudaError_t launch_attn_t(const Shape &sh, int n_seq, int R, const int32_t *seq_
 int attn_splits(const Shape &sh, int rows) { return plan_splits(sh, rows).n_split; }
 
 size_t attn_partial_bytes(const Shape &sh, int rows) {
-  // the partial buffers for `rows` rows; fewer rows use more splits, so take
-  // the largest rows x splits product over every row count up to `rows`
-  size_t worst = 0;
-  for (int r = 1; r <= rows; ++r) {
-    const size_t v = static_cast<size_t>(r) * plan_splits(sh, r).n_split;
-    if (v > worst) worst = v;
-  }
-  return worst * sh.hq * (kHeadDim + 2) * sizeof(float);
+  // split partials (m, l, acc) of every row
+  const size_t parts = static_cast<size_t>(rows) * plan_splits(sh, rows).n_split;
+  return parts * sh.hq * (kHeadDim + 2) * sizeof(float);
 }
 
 cudaError_t launch_attn(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                         const int32_t *pos0, const CacheView &cv, const uint16_t *q,
                         const int32_t *sel, const int32_t *n_sel, uint16_t *out, void *partials,
-                        int32_t *status, cudaStream_t st) {
+                        int32_t *status, bool pdl, const CommitArgs &commit, cudaStream_t st) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
   switch (sh.hkv) {
-    case 1: return launch_attn_t<1>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, st);
-    case 2: return launch_attn_t<2>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, st);
-    case 4: return launch_attn_t<4>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, st);
+    case 1: return launch_attn_t<1>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st);
+    case 2: return launch_attn_t<2>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st);
+    case 4: return launch_attn_t<4>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st);
     default: return cudaErrorInvalidValue;
   }
 }

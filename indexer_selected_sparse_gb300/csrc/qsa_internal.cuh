@@ -105,7 +105,37 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// --- programmatic dependent launch ----------------------------------------
+// Inside the fused step every kernel after the first is launched with
+// programmatic stream serialization: it may start while its predecessor is
+// still draining, runs its independent prologue, and waits (griddepcontrol.wait)
+// before reading anything an earlier kernel of the step writes. A kernel lets
+// its successor launch only after its own wait has returned, so a kernel never
+// overlaps one that is two steps back. Outside a programmatic launch the wait
+// returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // --- launchers (defined in the .cu files, called by the C entry points) ----
+// pdl: launch as a programmatic dependent of the previous kernel on the stream
 
 cudaError_t launch_append(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                           const int32_t *pos0, const int32_t *page_table, int max_pages,
@@ -114,21 +144,38 @@ cudaError_t launch_append(const Shape &sh, int n_seq, int R, const int32_t *seq_
                           const uint16_t *k_new, const uint16_t *v_new,
                           const uint16_t *idx_k_new, int32_t *status, cudaStream_t st);
 cudaError_t launch_commit(int n_seq, int R, int capacity, const int32_t *seq_ids,
-                          int32_t *pos0, int32_t *ingested, int advance, cudaStream_t st);
+                          int32_t *pos0, int32_t *ingested, int advance, bool pdl, cudaStream_t st);
 cudaError_t launch_rewind(int n_seq, const int32_t *seq_ids, const int32_t *n_drop,
                           int32_t *ingested, int32_t *status, cudaStream_t st);
 cudaError_t launch_score(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                          const int32_t *pos0, const CacheView &cv, const uint16_t *q_idx,
-                         const float *w, float *scores, int ld_scores, int32_t *status,
+                         const float *w, float *scores, int ld_scores, int32_t *status, bool pdl,
                          cudaStream_t st);
+bool score_tc_supported(const Shape &sh);
+cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
+                            const int32_t *pos0, const CacheView &cv, const uint16_t *q_idx,
+                            const float *w, float *scores, int ld, int32_t *status, bool pdl,
+                            cudaStream_t st);
 cudaError_t launch_select(const Shape &sh, int n_seq, int R, const int32_t *pos0,
                           const float *scores, int ld_scores, int32_t *sel, int32_t *n_sel,
-                          int max_blocks, int cap_tokens, int32_t *status, cudaStream_t st);
+                          int max_blocks, int cap_tokens, int32_t *status, bool pdl,
+                          cudaStream_t st);
 int attn_splits(const Shape &sh, int rows);
 size_t attn_partial_bytes(const Shape &sh, int rows);
+// The step's counter commit, folded into the last kernel of the fused step
+// (n_seq == 0: nothing to commit).
+struct CommitArgs {
+  int n_seq = 0;
+  int R = 0;
+  int capacity = 0;
+  int advance = 0;
+  const int32_t *seq_ids = nullptr;
+  int32_t *pos0 = nullptr;
+  int32_t *ingested = nullptr;
+};
 cudaError_t launch_attn(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                         const int32_t *pos0, const CacheView &cv, const uint16_t *q,
                         const int32_t *sel, const int32_t *n_sel, uint16_t *out, void *partials,
-                        int32_t *status, cudaStream_t st);
+                        int32_t *status, bool pdl, const CommitArgs &commit, cudaStream_t st);
 
 }  // namespace qsa

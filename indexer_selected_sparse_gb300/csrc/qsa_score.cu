@@ -31,6 +31,8 @@ score_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
   uint8_t *qs = smem + kTileBlocks * DI * 2;              // [NH][DI] bf16, swizzled
   float *ws = reinterpret_cast<float *>(qs + NH * DI * 2);  // [NH]
 
+  pdl_wait();  // the compressed keys come from the append kernel
+  pdl_trigger();
   const int row = blockIdx.y;
   const int i = row / R;
   const int visible = pos0[i] + (row - i * R) + 1;
@@ -135,7 +137,7 @@ score_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
 template <int DI, int NH>
 cudaError_t launch_score_t(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                            const int32_t *pos0, const CacheView &cv, const uint16_t *q_idx,
-                           const float *w, float *scores, int ld, int32_t *status,
+                           const float *w, float *scores, int ld, int32_t *status, bool pdl,
                            cudaStream_t st) {
   const size_t smem = kTileBlocks * DI * 2 + NH * DI * 2 + NH * 4;
   auto kern = score_kernel<DI, NH>;
@@ -143,26 +145,30 @@ cudaError_t launch_score_t(const Shape &sh, int n_seq, int R, const int32_t *seq
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid((ld + kTileBlocks - 1) / kTileBlocks, n_seq * R);
-  kern<<<grid, kScoreThreads, smem, st>>>(sh, R, seq_ids, pos0, cv, q_idx, w, scores, ld, status);
-  return cudaGetLastError();
+  return launch_kernel(pdl, kern, grid, dim3(kScoreThreads), smem, st, sh, R, seq_ids, pos0, cv, q_idx,
+                       w, scores, ld, status);
 }
 
 }  // namespace
 
 cudaError_t launch_score(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                          const int32_t *pos0, const CacheView &cv, const uint16_t *q_idx,
-                         const float *w, float *scores, int ld_scores, int32_t *status,
+                         const float *w, float *scores, int ld_scores, int32_t *status, bool pdl,
                          cudaStream_t st) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
+  // tcgen05 path whenever the TMA page boxes fit (8..32 blocks per page);
+  // the mma.sync kernel below covers the remaining shapes (ratio 16)
+  if (score_tc_supported(sh))
+    return launch_score_tc(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, pdl, st);
   const int nh = sh.h_idx <= 16 ? 16 : (sh.h_idx <= 32 ? 32 : 64);
   if (sh.d_idx == 128) {
-    if (nh == 16) return launch_score_t<128, 16>(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, st);
-    if (nh == 32) return launch_score_t<128, 32>(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, st);
-    return launch_score_t<128, 64>(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, st);
+    if (nh == 16) return launch_score_t<128, 16>(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, pdl, st);
+    if (nh == 32) return launch_score_t<128, 32>(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, pdl, st);
+    return launch_score_t<128, 64>(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, pdl, st);
   }
-  if (nh == 16) return launch_score_t<64, 16>(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, st);
-  if (nh == 32) return launch_score_t<64, 32>(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, st);
-  return launch_score_t<64, 64>(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, st);
+  if (nh == 16) return launch_score_t<64, 16>(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, pdl, st);
+  if (nh == 32) return launch_score_t<64, 32>(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, pdl, st);
+  return launch_score_t<64, 64>(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, pdl, st);
 }
 
 }  // namespace qsa

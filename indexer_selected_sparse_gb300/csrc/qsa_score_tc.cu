@@ -1,0 +1,598 @@
+// Index score on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// s_b = sum_h w_h * max(0, q_I,h . k_b) for every complete block b of a row
+// ("Agentic shootout", "PR 16 review: qwen4exp serving in Atlas (Claude's
+// review)", (a): relu-score over mean-pooled blocks; "Flash-Next support: vLLM
+// vs Atlas", (a) item 6: the query is scored against the compressed keys).
+//
+// One CTA scores one tile of 128 consecutive blocks for a group of G <= 4
+// consecutive rows of one sequence (decode: G = 1; verify and prefill rows of a
+// sequence share the key tile). The contraction is
+//     D[128 blocks, N] = K_tile[128, d_I] . Q_group^T[d_I, N],  N = G * H_I
+// with blocks on M, so each TMEM lane holds one block and the ReLU * w head sum
+// is a reduction inside one thread.
+//   * TMA (cp.async.bulk.tensor, 128B swizzle) gathers the tile page by page:
+//     one box of (blocks per page) x 64 dims per page and half of d_I, straight
+//     from the paged compressed-key pool; the query rows of the group are one box
+//     per half. The smem layout is the K-major SWIZZLE_128B canonical layout
+//     (8-row x 128-byte atoms, 1024-byte stride between 8-row groups).
+//   * One thread issues d_I/16 tcgen05.mma (kind::f16, bf16 in, fp32 accumulate
+//     in TMEM) and commits them to an mbarrier.
+//   * Four warps read their 32 TMEM lanes with tcgen05.ld and write the scores.
+// Every mbarrier wait is bounded in time; on expiry the CTA records
+// QSA_ERR_TIMEOUT, waits (bounded) for its own copies, frees its TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "qsa_internal.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int kTcTileBlocks = 128;
+constexpr int kTcMaxGroup = 4;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+
+// ---- PTX wrappers (tcgen05 / mbarrier / TMA) --------------------------------
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// K-major, SWIZZLE_128B shared-memory matrix descriptor: start address, LBO
+// (unused for swizzled K-major, set to 16 B), SBO = 1024 B between 8-row groups,
+// descriptor version 1, layout type 2 (128B swizzle).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct TcArgs {
+  Shape sh;
+  int R;               // rows per sequence
+  int G;               // rows per group
+  int groups_per_seq;  // ceil(R / G)
+  int npad;            // MMA N (multiple of 16, <= 256)
+  int hp;              // TMEM columns per row of the group (H_I, or npad when G == 1)
+  int ncols;           // TMEM columns allocated (power of two >= 32)
+  int bpp_log2;        // log2(blocks per page)
+  const int32_t *seq_ids;
+  const int32_t *pos0;
+  const int32_t *page_table;
+  int max_pages;
+  int num_pages;
+  const float *w;
+  float *scores;
+  int ld;
+  int32_t *status;
+  int n_groups;        // groups of rows (n_seq * groups_per_seq)
+};
+
+constexpr int kPThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
+constexpr int kMaxStages = 6;
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait that also gives up when another role has aborted the CTA.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                   int32_t *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      report(status, QSA_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Tiles of 128 blocks that group g needs (0 when its last row is dense or its
+// position is outside the page table; the select kernel reports the latter).
+__device__ __forceinline__ int group_tiles(const TcArgs &a, int g) {
+  const int i = g / a.groups_per_seq;
+  const int j0 = (g - i * a.groups_per_seq) * a.G;
+  const int g_rows = min(a.G, a.R - j0);
+  const int p0 = a.pos0[i];
+  const int vis_last = p0 + j0 + g_rows;
+  if (p0 + j0 + 1 < 1 || vis_last > a.max_pages * a.sh.page) return 0;
+  const int nb = vis_last >> a.sh.log2_ratio;
+  return nb > a.sh.topk ? (nb + kTcTileBlocks - 1) / kTcTileBlocks : 0;
+}
+
+// The work of a CTA is a contiguous range of the (group, tile) items in
+// group-major order; every role walks the same range independently.
+struct Walker {
+  int g, t, tiles, left;
+};
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+// Warp-cooperative: total items, then this CTA's first item.
+__device__ Walker walker_start(const TcArgs &a, int n_groups, int lane) {
+  int total = 0;
+  for (int g0 = 0; g0 < n_groups; g0 += 32) {
+    const int g = g0 + lane;
+    const int tl = g < n_groups ? group_tiles(a, g) : 0;
+    total += __shfl_sync(0xffffffffu, warp_incl_scan(tl, lane), 31);
+  }
+  const long long first = static_cast<long long>(total) * blockIdx.x / gridDim.x;
+  const long long last = static_cast<long long>(total) * (blockIdx.x + 1) / gridDim.x;
+  Walker w{n_groups, 0, 0, static_cast<int>(last - first)};
+  if (w.left <= 0) return w;
+  int base = 0;
+  for (int g0 = 0; g0 < n_groups; g0 += 32) {
+    const int g = g0 + lane;
+    const int tl = g < n_groups ? group_tiles(a, g) : 0;
+    const int incl = warp_incl_scan(tl, lane);
+    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+    if (base + tot > first) {
+      const unsigned m = __ballot_sync(0xffffffffu, base + incl > first);
+      const int src = __ffs(m) - 1;
+      const int tl_s = __shfl_sync(0xffffffffu, tl, src);
+      const int incl_s = __shfl_sync(0xffffffffu, incl, src);
+      w.g = g0 + src;
+      w.tiles = tl_s;
+      w.t = static_cast<int>(first - (base + incl_s - tl_s));
+      return w;
+    }
+    base += tot;
+  }
+  return w;
+}
+
+__device__ __forceinline__ void walker_next(Walker &w, const TcArgs &a, int n_groups) {
+  --w.left;
+  if (++w.t < w.tiles) return;
+  w.t = 0;
+  do {
+    ++w.g;
+    w.tiles = w.g < n_groups ? group_tiles(a, w.g) : 0;
+  } while (w.g < n_groups && w.tiles == 0 && w.left > 0);
+  if (w.g >= n_groups) w.left = 0;
+}
+
+// A batch of up to 32 / pages_in_tile consecutive tiles of one group, as the
+// producer warp sees it: lane L holds the page id of page L of the batch.
+struct Batch {
+  int nb = 0;        // tiles in the batch
+  int row0 = 0;      // first row of the group
+  int pg = 0;        // this lane's page id
+  bool have = false; // this lane's page holds a visible block
+};
+
+__device__ __forceinline__ Batch load_batch(const TcArgs &a, const Walker &w, int lane, int per_batch,
+                                            int pages_in_tile, int bpp) {
+  Batch b;
+  const int i = w.g / a.groups_per_seq;
+  const int j0 = (w.g - i * a.groups_per_seq) * a.G;
+  const int g_rows = min(a.G, a.R - j0);
+  b.row0 = i * a.R + j0;
+  b.nb = min(min(per_batch, w.tiles - w.t), w.left);
+  const int nblk_last = (a.pos0[i] + j0 + g_rows) >> a.sh.log2_ratio;
+  const int32_t *ptab = a.page_table + static_cast<size_t>(a.seq_ids[i]) * a.max_pages;
+  const int pidx = w.t * pages_in_tile + lane;
+  b.have = lane < b.nb * pages_in_tile && pidx * bpp < nblk_last;
+  b.pg = b.have ? ptab[pidx] : 0;
+  return b;
+}
+
+// Shared memory (1024-aligned): [A stages: S x DI/64 halves x 128 rows x 128 B]
+// [B slots: 2 x DI/64 halves x npad rows x 128 B][epilogue weights: npad floats]
+// [barriers][tmem address][abort flag]
+template <int DI>
+__global__ void __launch_bounds__(kPThreads, 1)
+score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_constant__ CUtensorMap tm_q,
+                TcArgs a, int n_stages) {
+  constexpr int HALVES = DI / 64;
+  constexpr int A_HALF = kTcTileBlocks * 128;
+  constexpr int A_STAGE = HALVES * A_HALF;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u = smem_u32(smem_raw);
+  const uint32_t base_u = (raw_u + 1023u) & ~1023u;
+  uint8_t *base = smem_raw + (base_u - raw_u);
+  const int S = n_stages;
+  const uint32_t a_u = base_u;
+  const uint32_t b_half = a.npad * 128;
+  const uint32_t b_slot = HALVES * b_half;
+  const uint32_t b_u = a_u + S * A_STAGE;
+  float *ws = reinterpret_cast<float *>(base + S * A_STAGE + 2 * b_slot);  // 4 x kTcMaxGroup x 64 floats
+  const uint32_t bars = smem_u32(ws + 4 * kTcMaxGroup * 64);
+  // barrier addresses
+  auto a_full = [&](int s) { return bars + 8u * s; };
+  auto a_empty = [&](int s) { return bars + 8u * (kMaxStages + s); };
+  auto b_full = [&](int s) { return bars + 8u * (2 * kMaxStages + s); };
+  auto b_empty = [&](int s) { return bars + 8u * (2 * kMaxStages + 2 + s); };
+  auto t_full = [&](int s) { return bars + 8u * (2 * kMaxStages + 4 + s); };
+  auto t_empty = [&](int s) { return bars + 8u * (2 * kMaxStages + 6 + s); };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ws + 4 * kTcMaxGroup * 64 + 2 * (2 * kMaxStages + 8));
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const Shape &sh = a.sh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_groups = a.n_groups;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(a_full(s), 1);
+      mbar_init(a_empty(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(b_full(s), 1);
+      mbar_init(b_empty(s), 1);
+      mbar_init(t_full(s), 1);
+      mbar_init(t_empty(s), 128);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 2 * a.ncols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int bpp = 1 << a.bpp_log2;
+  const int pages_in_tile = kTcTileBlocks >> a.bpp_log2;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    // Tiles are issued in batches of consecutive tiles of one group: lane L
+    // holds the page id of page L of the batch. The page ids of the next batch
+    // are loaded before the current batch's copies are issued, so no
+    // global-memory latency sits between two batches.
+    Walker w = walker_start(a, n_groups, lane);
+    const int per_batch = 32 / pages_in_tile;
+    Batch cur = load_batch(a, w, lane, per_batch, pages_in_tile, bpp);
+    pdl_wait();  // the compressed keys come from the append kernel
+    pdl_trigger();
+    int cur_g = -1, gseq = -1, k = 0;
+    bool ok = true;
+    while (ok && w.left > 0) {
+      Walker wn = w;
+      for (int it = 0; it < cur.nb; ++it) walker_next(wn, a, n_groups);
+      const Batch nxt = wn.left > 0 ? load_batch(a, wn, lane, per_batch, pages_in_tile, bpp) : Batch{};
+      if (w.g != cur_g) {
+        ++gseq;
+        const int bs = gseq & 1;
+        if (gseq >= 2 && !mbar_wait_or_abort(b_empty(bs), ((gseq >> 1) - 1) & 1, abort_flag, a.status)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(b_full(bs), b_slot);
+#pragma unroll
+          for (int hh = 0; hh < HALVES; ++hh)
+            tma_load_2d(b_u + bs * b_slot + hh * b_half, &tm_q, b_full(bs), hh * 64, cur.row0 * sh.h_idx);
+        }
+        cur_g = w.g;
+      }
+      if (cur.have && (cur.pg < 0 || cur.pg >= a.num_pages)) report(a.status, QSA_ERR_PAGE);
+      const unsigned have_mask = __ballot_sync(0xffffffffu, cur.have);
+      for (int it = 0; it < cur.nb; ++it, ++k) {
+        const int s = k % S;
+        if (k >= S && !mbar_wait_or_abort(a_empty(s), ((k / S) - 1) & 1, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        const unsigned mine = (pages_in_tile == 32 ? 0xffffffffu : ((1u << pages_in_tile) - 1u))
+                              << (it * pages_in_tile);
+        const int n_load = __popc(have_mask & mine);
+        if (lane == 0) mbar_arrive_expect_tx(a_full(s), static_cast<uint32_t>(n_load) * HALVES * bpp * 128);
+        __syncwarp();
+        if (cur.have && ((mine >> lane) & 1u)) {
+          const int slot = lane - it * pages_in_tile;
+#pragma unroll
+          for (int hh = 0; hh < HALVES; ++hh)
+            tma_load_2d(a_u + s * A_STAGE + hh * A_HALF + slot * bpp * 128, &tm_keys, a_full(s), hh * 64,
+                        cur.pg * bpp);
+        }
+      }
+      w = wn;
+      cur = nxt;
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    Walker w = walker_start(a, n_groups, lane);
+    int cur_g = -1, gseq = -1;
+    const uint32_t idesc = idesc_bf16_f32(kTcTileBlocks, a.npad);
+    for (int k = 0; w.left > 0; ++k) {
+      const int s = k % S;
+      const int buf = k & 1;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait_or_abort(a_full(s), (k / S) & 1, abort_flag, a.status);
+      int bs = gseq & 1;
+      if (w.g != cur_g) {
+        ++gseq;
+        bs = gseq & 1;
+        if (lane == 0 && ok) ok = mbar_wait_or_abort(b_full(bs), (gseq >> 1) & 1, abort_flag, a.status);
+        cur_g = w.g;
+      }
+      if (lane == 0 && ok && k >= 2) ok = mbar_wait_or_abort(t_empty(buf), ((k >> 1) - 1) & 1, abort_flag, a.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t d = tmem + buf * a.ncols;
+#pragma unroll
+        for (int kk = 0; kk < DI / 16; ++kk) {
+          const int hh = kk >> 2, k4 = kk & 3;
+          const uint64_t ad = smem_desc_sw128(a_u + s * A_STAGE + hh * A_HALF + k4 * 32);
+          const uint64_t bd = smem_desc_sw128(b_u + bs * b_slot + hh * b_half + k4 * 32);
+          tc_mma(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(a_empty(s));
+        tc_commit(t_full(buf));
+      }
+      walker_next(w, a, n_groups);
+      if (lane == 0 && (w.left <= 0 || w.g != cur_g)) tc_commit(b_empty(bs));
+    }
+  } else {
+    // ---------------- epilogue (warps 2-5, TMEM lane quarter = warp % 4) ----------------
+    const int q = warp & 3;
+    Walker w = walker_start(a, n_groups, lane);
+    const int chunks = a.hp >> 4;  // 16-column TMEM loads per row (<= 4)
+    // this warp's copy of the group's head weights: [G][64]
+    float *wq = ws + (warp - 2) * (kTcMaxGroup * 64);
+    int cur_g = -1, j0 = 0, g_rows = 0, row0 = 0, p0 = 0;
+    for (int k = 0; w.left > 0; ++k) {
+      const int buf = k & 1;
+      if (w.g != cur_g) {
+        const int i = w.g / a.groups_per_seq;
+        j0 = (w.g - i * a.groups_per_seq) * a.G;
+        g_rows = min(a.G, a.R - j0);
+        row0 = i * a.R + j0;
+        p0 = a.pos0[i];
+        __syncwarp();
+        for (int c = lane; c < kTcMaxGroup * 64; c += 32) {
+          const int j = c >> 6, h = c & 63;
+          wq[c] = (j < g_rows && h < sh.h_idx) ? a.w[static_cast<size_t>(row0 + j) * sh.h_idx + h] : 0.f;
+        }
+        __syncwarp();
+        cur_g = w.g;
+      }
+      if (!mbar_wait_or_abort(t_full(buf), (k >> 1) & 1, abort_flag, a.status)) break;
+      tc_fence_after();
+      const int blk = w.t * kTcTileBlocks + q * 32 + lane;
+      const uint32_t lane_addr = tmem + buf * a.ncols + (static_cast<uint32_t>(q * 32) << 16);
+      for (int j = 0; j < a.G; ++j) {
+        float v[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (c < chunks) tmem_ld16(lane_addr + j * a.hp + c * 16, v[c]);
+        tmem_ld_wait();
+        const float *wrow = wq + j * 64;  // zero beyond H_I
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (c < chunks) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) acc += wrow[c * 16 + t] * fmaxf(v[c][t], 0.f);
+          }
+        }
+        if (j < g_rows) {
+          const int nb = (p0 + j0 + j + 1) >> sh.log2_ratio;  // blocks visible to row j
+          if (nb > sh.topk && blk < nb) a.scores[static_cast<size_t>(row0 + j) * a.ld + blk] = acc;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(t_empty(buf));
+      walker_next(w, a, n_groups);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    // give this CTA's own copies and MMAs time to land before its shared memory
+    // and TMEM are released (bounded)
+    const unsigned long long t0 = global_ns();
+    while (global_ns() - t0 < 2000000ull) {
+    }
+  }
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 2 * a.ncols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2D bf16 tensor map [rows][cols] (row stride cols*2 bytes), box box_cols x box_rows,
+// 128-byte swizzle.
+bool encode_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+               uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int pow2_at_least(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+bool score_tc_supported(const Shape &sh) {
+  const int bpp = sh.page >> sh.log2_ratio;
+  return bpp >= 8 && bpp <= 32 && (sh.d_idx == 64 || sh.d_idx == 128) && sh.h_idx <= 64;
+}
+
+cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
+                            const int32_t *pos0, const CacheView &cv, const uint16_t *q_idx,
+                            const float *w, float *scores, int ld, int32_t *status, bool pdl,
+                            cudaStream_t st) {
+  if (n_seq == 0 || R == 0) return cudaSuccess;
+  TcArgs a;
+  a.sh = sh;
+  a.R = R;
+  a.G = (sh.h_idx % 16 == 0) ? min(min(R, kTcMaxGroup), 256 / sh.h_idx) : 1;
+  a.groups_per_seq = (R + a.G - 1) / a.G;
+  a.npad = (a.G * sh.h_idx + 15) / 16 * 16;
+  a.hp = (a.G == 1) ? a.npad : sh.h_idx;
+  a.ncols = pow2_at_least(a.npad);
+  a.bpp_log2 = sh.log2_page - sh.log2_ratio;
+  a.seq_ids = seq_ids;
+  a.pos0 = pos0;
+  a.page_table = cv.page_table;
+  a.max_pages = cv.max_pages;
+  a.num_pages = cv.num_pages;
+  a.w = w;
+  a.scores = scores;
+  a.ld = ld;
+  a.status = status;
+
+  CUtensorMap tm_keys, tm_q;
+  const int bpp = 1 << a.bpp_log2;
+  const long long total_rows = static_cast<long long>(n_seq) * R;
+  if (!encode_2d(&tm_keys, cv.idxblk_pool, sh.d_idx, static_cast<uint64_t>(cv.num_pages) * bpp, 64, bpp))
+    return cudaErrorInvalidValue;
+  if (!encode_2d(&tm_q, q_idx, sh.d_idx, static_cast<uint64_t>(total_rows) * sh.h_idx, 64, a.npad))
+    return cudaErrorInvalidValue;
+
+  a.n_groups = n_seq * a.groups_per_seq;
+  const int halves = sh.d_idx / 64;
+  const size_t a_stage = static_cast<size_t>(halves) * kTcTileBlocks * 128;
+  const size_t b_slots = 2ull * halves * a.npad * 128;
+  const size_t fixed = 1024 + b_slots + 4 * kTcMaxGroup * 64 * 4 + 8 * (2 * kMaxStages + 8) + 16;
+  const size_t smem_cap = 227 * 1024;
+  int stages = static_cast<int>((smem_cap - fixed) / a_stage);
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return cudaErrorInvalidValue;
+  size_t smem = fixed + stages * a_stage;
+  // TMEM: resident CTAs x 2 accumulators x ncols must stay within the SM's 512
+  // columns so tcgen05.alloc never waits on another CTA; raise the shared
+  // memory request until at most 512 / (2 ncols) CTAs fit on an SM.
+  const size_t sm_smem = 233472;  // shared memory per SM (228 KB)
+  const int max_ctas = 512 / (2 * a.ncols);
+  const size_t min_smem = sm_smem / (max_ctas + 1) - 1024 + 1;
+  if (smem < min_smem) smem = min_smem;
+  auto kern = sh.d_idx == 128 ? score_tc_kernel<128> : score_tc_kernel<64>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPThreads, smem)) != cudaSuccess)
+    return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  if (per_sm > max_ctas) per_sm = max_ctas;
+  return launch_kernel(pdl, kern, dim3(sms * per_sm), dim3(kPThreads), smem, st, tm_keys, tm_q, a, stages);
+  return cudaGetLastError();
+}
+
+}  // namespace qsa

@@ -107,7 +107,7 @@ extern "C" int qsa_gather_attn_static(const qsa_config *cfg, const qsa_rows *row
   cv.idxraw_pool = cache->idxraw_pool;
   cv.idxblk_pool = cache->idxblk_pool;
   e = launch_attn(sh, rows->n_seq, rows->rows_per_seq, rows->seq_ids, rows->pos0, cv, q, sel, n_sel,
-                  out, scratch, status, stream);
+                  out, scratch, status, false, CommitArgs{}, stream);
   if (e == cudaSuccess) return QSA_OK;
   if (e == cudaErrorIllegalAddress || e == cudaErrorLaunchFailure || e == cudaErrorMisalignedAddress ||
       e == cudaErrorIllegalInstruction)

@@ -30,6 +30,7 @@ QSA_ERR_CUDA_FATAL = 6
 QSA_ERR_DESYNC = 7
 QSA_ERR_PAGE = 8
 QSA_ERR_REWIND = 9
+QSA_ERR_TIMEOUT = 10
 
 EXPORTED = ("qsa_strerror", "qsa_config_check", "qsa_workspace_bytes", "qsa_append",
             "qsa_rewind", "qsa_index_score", "qsa_topk_select", "qsa_gather_attn", "qsa_decode",
