@@ -201,7 +201,8 @@ int qsa_index_score(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache
  * ascending). Writes sel[row*K + i] ascending, padded with -1 to K entries,
  * and n_sel[row] = number of selected blocks. Scores are compared as fp32
  * (+0 and -0 are equal).
- *   scores  device [rows, ld_scores] fp32 (from qsa_index_score)
+ *   scores  device [rows, ld_scores] fp32 (from qsa_index_score), 16-byte
+ *           aligned, ld_scores a multiple of 4 (else QSA_ERR_INVALID_ARG)
  *   sel     device [rows, K] int32;  n_sel  device [rows] int32 */
 int qsa_topk_select(const qsa_config *cfg, const qsa_rows *rows, const float *scores,
                     int ld_scores, int32_t *sel, int32_t *n_sel, int32_t *status,

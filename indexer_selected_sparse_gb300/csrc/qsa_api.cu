@@ -226,7 +226,9 @@ int qsa_topk_select(const qsa_config *cfg, const qsa_rows *rows, const float *sc
   if ((rc = check_cfg(cfg)) != QSA_OK) return rc;
   if ((rc = check_rows(rows)) != QSA_OK) return rc;
   if (static_cast<long long>(rows->n_seq) * rows->rows_per_seq == 0) return QSA_OK;
-  if (!scores || !sel || !n_sel || ld_scores < 1) return QSA_ERR_INVALID_ARG;
+  // rows are read with 16-byte loads
+  if (!scores || !sel || !n_sel || !aligned16(scores) || ld_scores < 4 || ld_scores % 4 != 0)
+    return QSA_ERR_INVALID_ARG;
   const Shape sh = make_shape(cfg);
   // rows whose visible count exceeds ld_scores * ratio are rejected in-kernel
   const long long cap = static_cast<long long>(ld_scores) * cfg->ratio + cfg->ratio - 1;

@@ -4,52 +4,66 @@
 // budget + ratio - 1 visible tokens).
 //
 // One CTA per row. Scores become order-preserving uint32 keys (-0 folded onto
-// +0) held in shared memory. The keys of a row share their high bits (same
-// sign and exponent), so the radix digits are taken from the window of bits in
-// which the row's smallest and largest keys differ, 11 bits at a time, most
-// significant first: each pass histograms the keys that match the prefix fixed
-// so far and a block-wide suffix scan finds the digit that holds the K-th
-// largest key. After at most three passes the K-th largest key T is exact, and
-// so is the number of ties at T that must be taken. A stable compaction then
-// emits, in ascending block order, every block with key > T and the
-// lowest-indexed blocks with key == T: exactly the top-K under (score desc,
-// index asc). The selection stays on the device, so a step that contains it can
-// be captured in a CUDA graph.
+// +0) held in shared memory, each taken relative to the row's smallest key so
+// that the radix digits span exactly the range the row covers. Digits are 11
+// bits, most significant first: a pass histograms the keys that match the
+// prefix fixed so far and a block-wide suffix scan finds the digit that holds
+// the K-th largest key. Only the first pass reads every key: the keys of the
+// chosen digit are gathered into a candidate list, which one warp ranks
+// directly when it is short and further passes refine otherwise. The K-th
+// largest key T is then exact, and so is the number of ties at T that must be
+// taken. A stable compaction emits, in ascending block order, every block with
+// key > T and the lowest-indexed blocks with key == T: exactly the top-K under
+// (score desc, index asc). The selection stays on the device, so a step that
+// contains it can be captured in a CUDA graph.
 #include "qsa_internal.cuh"
 
 namespace qsa {
 namespace {
 
 constexpr int kSelThreads = 1024;
-constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kMaxSmemKeys = 48 * 1024;  // 192 KB of keys held on chip
+constexpr int kSelWarps = kSelThreads / 32;  // <= 32: the scan keeps one total per lane
+constexpr int kMaxSmemKeys = 48 * 1024 - 4096;  // keys held on chip (176 KB) ...
+constexpr int kCandMax = 4096;                   // ... plus the candidate list (16 KB)
+constexpr int kDirectMax = 64;  // candidate lists this short are ranked by one warp
 constexpr int kDigit = 11;
-constexpr int kBins = 1 << kDigit;       // 2048: two bins per thread
+constexpr int kBins = 1 << kDigit;
+constexpr int kBinsPerThread = kBins / kSelThreads;
+constexpr int kBatch = 8;  // keys a thread loads before it histograms them
 
-// Exclusive prefix sum over the CTA; `tmp` holds kSelWarps ints.
-__device__ __forceinline__ int block_exclusive_scan(int v, int *tmp) {
+// Exclusive prefix sums over the CTA of a pair of counts, with one barrier: every
+// warp scans the per-warp totals itself. Two calls must be separated by a barrier
+// (the next call overwrites `tmp`).
+__device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2 *tmp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
+  int2 x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    const int yx = __shfl_up_sync(0xffffffffu, x.x, o);
+    const int yy = __shfl_up_sync(0xffffffffu, x.y, o);
+    if (lane >= o) {
+      x.x += yx;
+      x.y += yy;
+    }
   }
   if (lane == 31) tmp[warp] = x;
   __syncthreads();
-  if (warp == 0) {
-    int t = tmp[lane];
+  int2 t = lane < kSelWarps ? tmp[lane] : make_int2(0, 0);
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int yx = __shfl_up_sync(0xffffffffu, t.x, o);
+    const int yy = __shfl_up_sync(0xffffffffu, t.y, o);
+    if (lane >= o) {
+      t.x += yx;
+      t.y += yy;
     }
-    tmp[lane] = t;  // inclusive totals per warp
   }
-  __syncthreads();
-  const int before = warp > 0 ? tmp[warp - 1] : 0;
-  __syncthreads();
-  return before + x - v;
+  const int src = warp > 0 ? warp - 1 : 0;
+  int2 before;
+  before.x = __shfl_sync(0xffffffffu, t.x, src);
+  before.y = __shfl_sync(0xffffffffu, t.y, src);
+  if (warp == 0) before = make_int2(0, 0);
+  return make_int2(before.x + x.x - v.x, before.y + x.y - v.y);
 }
 
 // Histogram update; a warp whose active lanes all hold the same digit (a run of
@@ -66,15 +80,212 @@ __device__ __forceinline__ void hist_add(int *hist, uint32_t digit, bool active)
   }
 }
 
+// Key sources. Every key is taken relative to the row's smallest key, so the
+// radix digits cover the range the row's keys actually span: scores of one row
+// share sign and exponent bits, and digits of the raw key would pile most of the
+// row into a few histogram bins.
+struct SmemKeys {  // keys staged in shared memory
+  const uint32_t *p;
+  uint32_t base;
+  __device__ __forceinline__ uint32_t operator()(int x) const { return p[x] - base; }
+  // four keys from a 16-byte aligned position (x a multiple of 4)
+  __device__ __forceinline__ uint4 get4(int x) const {
+    uint4 v = *reinterpret_cast<const uint4 *>(p + x);
+    return make_uint4(v.x - base, v.y - base, v.z - base, v.w - base);
+  }
+};
+struct GlobalScores {  // fp32 scores read from global memory (rows too long for shared memory)
+  const float *p;
+  uint32_t base;
+  __device__ __forceinline__ uint32_t operator()(int x) const { return score_key(p[x]) - base; }
+  __device__ __forceinline__ uint4 get4(int x) const {
+    const float4 v = *reinterpret_cast<const float4 *>(p + x);
+    return make_uint4(score_key(v.x) - base, score_key(v.y) - base, score_key(v.z) - base,
+                      score_key(v.w) - base);
+  }
+};
+
+// One radix pass over a list of keys: histogram of the digit (k >> shift) & dmask
+// of the keys matching `prefix` under `mask`, then the digit that holds the
+// remaining-th largest key. Updates prefix / mask / remaining. `hist` is all
+// zero on entry and is left all zero.
+template <typename Src>
+__device__ __forceinline__ void radix_pass(Src list, int m, int shift, uint32_t dmask,
+                                           uint32_t &prefix, uint32_t &mask, int &remaining,
+                                           int *hist, int2 *scan_tmp, int *s_res) {
+  const int tid = threadIdx.x;
+  for (int base = 0; base < m; base += kBatch * kSelThreads) {  // warp-uniform trip count
+    uint32_t k[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int x = base + b * kSelThreads + tid;
+      k[b] = x < m ? list(x) : 0u;
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int x = base + b * kSelThreads + tid;
+      hist_add(hist, (k[b] >> shift) & dmask, x < m && (k[b] & mask) == prefix);
+    }
+  }
+  __syncthreads();
+  // thread t owns the kBinsPerThread digits below kBins - kBinsPerThread * t:
+  // a suffix scan from the top digit finds the digit of the remaining-th largest
+  const int top_bin = kBins - 1 - kBinsPerThread * threadIdx.x;
+  int c[kBinsPerThread];
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    c[j] = hist[top_bin - j];
+    hist[top_bin - j] = 0;  // only this thread reads these bins
+    sum += c[j];
+  }
+  int above = block_exclusive_scan2(make_int2(sum, 0), scan_tmp).x;
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    if (above < remaining && remaining <= above + c[j]) {
+      s_res[0] = top_bin - j;
+      s_res[1] = above;
+    }
+    above += c[j];
+  }
+  __syncthreads();
+  prefix |= static_cast<uint32_t>(s_res[0]) << shift;
+  mask |= dmask << shift;
+  remaining -= s_res[1];
+}
+
+// Selection for one row whose keys (relative to the row minimum) span
+// [0, range]: the exact K-th largest key, then the stable compaction.
+template <typename Src>
+__device__ __forceinline__ void select_row(Src src, int n, int K, uint32_t range, uint32_t *cand,
+                                           int32_t *out, int *hist, int2 *scan_tmp, int *s_res,
+                                           int *s_ncand) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int top = range ? 31 - __clz(range) : -1;  // highest bit any key of the row sets
+  const uint32_t low_bits = (top >= 31) ? 0xffffffffu : (top >= 0 ? ((2u << top) - 1u) : 0u);
+  uint32_t prefix = 0u;
+  uint32_t mask = ~low_bits;
+  int remaining = K;  // how many of the still-undecided keys must be taken
+  if (top >= 0) {
+    // first pass over every key of the row
+    int width = min(kDigit, top + 1);
+    int shift = top + 1 - width;
+    radix_pass(src, n, shift, (1u << width) - 1u, prefix, mask, remaining, hist, scan_tmp, s_res);
+    top = shift - 1;
+    if (top >= 0) {
+      // the keys of the chosen digit become a short candidate list (when they fit)
+      for (int base = 0; base < n; base += kSelThreads) {
+        const int x = base + tid;
+        const uint32_t k = x < n ? src(x) : 0u;
+        const bool c = x < n && (k & mask) == prefix;
+        const unsigned bal = __ballot_sync(0xffffffffu, c);
+        int off = 0;
+        if (lane == 0 && bal) off = atomicAdd(s_ncand, __popc(bal));
+        off = __shfl_sync(0xffffffffu, off, 0);
+        const int pos = off + __popc(bal & ((1u << lane) - 1u));
+        if (c && pos < kCandMax) cand[pos] = k;
+      }
+      __syncthreads();
+      const int nc = *s_ncand;
+      if (nc <= kDirectMax) {
+        // one warp ranks the candidates directly: the remaining-th largest has
+        // fewer than `remaining` candidates above it and at least that many at
+        // or above it
+        if (warp == 0) {
+          const uint32_t a = lane < nc ? cand[lane] : 0u;
+          const uint32_t b = lane + 32 < nc ? cand[lane + 32] : 0u;
+          int ga = 0, ea = 0, gb = 0, eb = 0;
+          for (int j = 0; j < nc; ++j) {
+            const uint32_t v = cand[j];
+            ga += v > a;
+            ea += v == a;
+            gb += v > b;
+            eb += v == b;
+          }
+          if (lane < nc && ga < remaining && remaining <= ga + ea) {
+            s_res[0] = static_cast<int>(a);
+            s_res[1] = remaining - ga;
+          }
+          if (lane + 32 < nc && gb < remaining && remaining <= gb + eb) {
+            s_res[0] = static_cast<int>(b);
+            s_res[1] = remaining - gb;
+          }
+        }
+        __syncthreads();
+        prefix = static_cast<uint32_t>(s_res[0]);
+        remaining = s_res[1];
+      } else if (nc <= kCandMax) {
+        while (top >= 0) {
+          width = min(kDigit, top + 1);
+          shift = top + 1 - width;
+          radix_pass(SmemKeys{cand, 0u}, nc, shift, (1u << width) - 1u, prefix, mask, remaining,
+                     hist, scan_tmp, s_res);
+          top = shift - 1;
+        }
+      } else {
+        while (top >= 0) {
+          width = min(kDigit, top + 1);
+          shift = top + 1 - width;
+          radix_pass(src, n, shift, (1u << width) - 1u, prefix, mask, remaining, hist, scan_tmp,
+                     s_res);
+          top = shift - 1;
+        }
+      }
+    }
+  }
+  const uint32_t thr = prefix;  // the K-th largest key
+  const int need = remaining;   // ties at thr to take (>= 1)
+
+  // stable compaction: thread t scans a contiguous chunk (a multiple of 4 keys,
+  // read 4 at a time); one scan gives both the keys above thr and the ties
+  // before the chunk
+  const int chunk = ((n + kSelThreads - 1) / kSelThreads + 3) & ~3;
+  const int lo = min(n, tid * chunk), hi = min(n, lo + chunk);
+  int gt = 0, eq = 0;
+  for (int x = lo; x < hi; x += 4) {
+    const uint4 v = src.get4(x);
+    const uint32_t d[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (x + j < hi) {
+        gt += d[j] > thr;
+        eq += d[j] == thr;
+      }
+    }
+  }
+  const int2 pre = block_exclusive_scan2(make_int2(gt, eq), scan_tmp);
+  int o = pre.x + min(pre.y, need);  // blocks emitted by the chunks before this one
+  int tie_rank = pre.y;
+  for (int x = lo; x < hi; x += 4) {
+    const uint4 v = src.get4(x);
+    const uint32_t d[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (x + j >= hi) continue;
+      if (d[j] > thr) {
+        if (o < K) out[o] = x + j;
+        ++o;
+      } else if (d[j] == thr) {
+        if (tie_rank < need) {
+          if (o < K) out[o] = x + j;
+          ++o;
+        }
+        ++tie_rank;
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kSelThreads)
 select_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__restrict__ scores,
               int ld, int32_t *__restrict__ sel, int32_t *__restrict__ n_sel, int smem_keys,
               int cap_tokens, int32_t *status) {
-  extern __shared__ uint32_t keys[];
+  // [smem_keys] row keys, then [kCandMax] candidates
+  extern __shared__ __align__(16) uint32_t keys[];
   __shared__ int hist[kBins];
-  __shared__ int scan_tmp[kSelWarps];
+  __shared__ int2 scan_tmp[kSelWarps];
   __shared__ uint32_t red_min[kSelWarps], red_max[kSelWarps];
-  __shared__ int s_digit, s_above;
+  __shared__ int s_res[2], s_ncand;
 
   const int row = blockIdx.x;
   const int i = row / R;
@@ -102,34 +313,29 @@ select_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__
     return;
   }
 
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) hist[kBinsPerThread * tid + j] = 0;
+  if (tid == 0) s_ncand = 0;
   pdl_wait();  // scores come from the score kernel
   pdl_trigger();
+  uint32_t *cand = keys + smem_keys;
   const float *srow = scores + static_cast<size_t>(row) * ld;
-  const bool cached = n <= smem_keys;
+  const bool on_chip = n <= smem_keys;
   uint32_t kmin = 0xffffffffu, kmax = 0u;
-  if (cached) {
+  {
     // 16-byte loads: ld is a multiple of 4, so the row start is 16-byte aligned
     const float4 *s4 = reinterpret_cast<const float4 *>(srow);
     const int n4 = n >> 2;
     for (int x = tid; x < n4; x += kSelThreads) {
       const float4 v = s4[x];
       const uint32_t k0 = score_key(v.x), k1 = score_key(v.y), k2 = score_key(v.z), k3 = score_key(v.w);
-      keys[4 * x] = k0;
-      keys[4 * x + 1] = k1;
-      keys[4 * x + 2] = k2;
-      keys[4 * x + 3] = k3;
+      if (on_chip) *reinterpret_cast<uint4 *>(keys + 4 * x) = make_uint4(k0, k1, k2, k3);
       kmin = min(kmin, min(min(k0, k1), min(k2, k3)));
       kmax = max(kmax, max(max(k0, k1), max(k2, k3)));
     }
     for (int x = 4 * n4 + tid; x < n; x += kSelThreads) {
       const uint32_t k = score_key(srow[x]);
-      keys[x] = k;
-      kmin = min(kmin, k);
-      kmax = max(kmax, k);
-    }
-  } else {
-    for (int x = tid; x < n; x += kSelThreads) {
-      const uint32_t k = score_key(srow[x]);
+      if (on_chip) keys[x] = k;
       kmin = min(kmin, k);
       kmax = max(kmax, k);
     }
@@ -144,85 +350,18 @@ select_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__
     red_max[warp] = kmax;
   }
   __syncthreads();
-  kmin = red_min[lane];
-  kmax = red_max[lane];
+  kmin = lane < kSelWarps ? red_min[lane] : 0xffffffffu;
+  kmax = lane < kSelWarps ? red_max[lane] : 0u;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
     kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
   }
-  auto key_at = [&](int x) -> uint32_t { return cached ? keys[x] : score_key(srow[x]); };
-
-  // bits above the window are common to every key of the row
-  const uint32_t diff = kmin ^ kmax;
-  int top = diff ? 31 - __clz(diff) : -1;  // highest differing bit
-  const uint32_t low_bits = (top >= 31) ? 0xffffffffu : (top >= 0 ? ((2u << top) - 1u) : 0u);
-  uint32_t prefix = kmax & ~low_bits;
-  uint32_t mask = ~low_bits;
-  int remaining = K;  // how many of the still-undecided keys must be taken
-  const int n_iter = (n + kSelThreads - 1) / kSelThreads;
-#pragma unroll 1
-  while (top >= 0) {
-    const int width = min(kDigit, top + 1);
-    const int shift = top + 1 - width;
-    const uint32_t dmask = (1u << width) - 1u;
-    hist[2 * tid] = 0;
-    hist[2 * tid + 1] = 0;
-    __syncthreads();
-    for (int it = 0; it < n_iter; ++it) {  // warp-uniform trip count
-      const int x = it * kSelThreads + tid;
-      const uint32_t k = x < n ? key_at(x) : 0u;
-      const bool act = x < n && (k & mask) == prefix;
-      hist_add(hist, (k >> shift) & dmask, act);
-    }
-    __syncthreads();
-    // thread t owns digits (kBins-1-2t) and (kBins-2-2t): a suffix scan from the
-    // top digit finds the digit that holds the remaining-th largest key
-    const int c_hi = hist[kBins - 1 - 2 * tid], c_lo = hist[kBins - 2 - 2 * tid];
-    const int above = block_exclusive_scan(c_hi + c_lo, scan_tmp);
-    if (above < remaining && remaining <= above + c_hi) {
-      s_digit = kBins - 1 - 2 * tid;
-      s_above = above;
-    } else if (above + c_hi < remaining && remaining <= above + c_hi + c_lo) {
-      s_digit = kBins - 2 - 2 * tid;
-      s_above = above + c_hi;
-    }
-    __syncthreads();
-    prefix |= static_cast<uint32_t>(s_digit) << shift;
-    mask |= dmask << shift;
-    remaining -= s_above;
-    top = shift - 1;
-    __syncthreads();
-  }
-  const uint32_t thr = prefix;  // the K-th largest key
-  const int need = remaining;   // ties at thr to take (>= 1)
-
-  // stable compaction over contiguous per-thread chunks
-  const int chunk = (n + kSelThreads - 1) / kSelThreads;
-  const int lo = min(n, tid * chunk), hi = min(n, lo + chunk);
-  int gt = 0, eq = 0;
-  for (int x = lo; x < hi; ++x) {
-    const uint32_t k = key_at(x);
-    gt += k > thr;
-    eq += k == thr;
-  }
-  const int tie_base = block_exclusive_scan(eq, scan_tmp);
-  const int take_eq = min(max(need - tie_base, 0), eq);
-  int o = block_exclusive_scan(gt + take_eq, scan_tmp);
-  int tie_rank = tie_base;
-  for (int x = lo; x < hi; ++x) {
-    const uint32_t k = key_at(x);
-    if (k > thr) {
-      if (o < K) out[o] = x;
-      ++o;
-    } else if (k == thr) {
-      if (tie_rank < need) {
-        if (o < K) out[o] = x;
-        ++o;
-      }
-      ++tie_rank;
-    }
-  }
+  if (on_chip)
+    select_row(SmemKeys{keys, kmin}, n, K, kmax - kmin, cand, out, hist, scan_tmp, s_res, &s_ncand);
+  else
+    select_row(GlobalScores{srow, kmin}, n, K, kmax - kmin, cand, out, hist, scan_tmp, s_res,
+               &s_ncand);
   if (tid == 0) n_sel[row] = K;
 }
 
@@ -233,8 +372,9 @@ cudaError_t launch_select(const Shape &sh, int n_seq, int R, const int32_t *pos0
                           int max_blocks, int cap_tokens, int32_t *status, bool pdl,
                           cudaStream_t st) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
+  // rows of more than kMaxSmemKeys blocks read their scores from global memory
   const int cap = max_blocks < kMaxSmemKeys ? max_blocks : kMaxSmemKeys;
-  const size_t smem = static_cast<size_t>(cap) * 4;
+  const size_t smem = (static_cast<size_t>(cap) + kCandMax) * 4;
   cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;

@@ -48,6 +48,7 @@ STREAM_W = 6
 STREAM_PAGES = 7
 STREAM_PREFIX = 8
 STREAM_REJECT = 9
+STREAM_SCORES = 10
 
 
 def _mul32(x: torch.Tensor, c: int) -> torch.Tensor:
@@ -243,6 +244,44 @@ def workload(i: int) -> Workload:
         return Workload("chunked-prefill b1 prefix24576 chunk8193 r4 B2048", 4, SHAPES_MAIN,
                         [24576], 8193, form="prefill")
     raise ValueError(f"no workload {i}")
+
+
+SCORE_KINDS = ("spread", "nonneg", "cluster", "few_values", "signed_zero")
+
+
+def select_scores(seed: int, n_rows: int, n: int, kind: str) -> torch.Tensor:
+    """Synthetic block-score rows [n_rows, n] (fp32) for exercising top-K
+    selection on its own, each kind a score distribution a row can have:
+      spread       signed, uniform in [-4, 4)
+      nonneg       exponential(1) with about 1 in 32 exactly zero (a weighted
+                   ReLU sum with non-negative weights)
+      cluster      1 + u * 2^-10 (a narrow cluster) with one huge and one tiny
+                   outlier per row, so the row's key range is wide while most
+                   keys share their high bits
+      few_values   one of {-1, -0.0, +0.0, 0.5, 1}: heavy ties
+      signed_zero  +0.0 or -0.0 except about 1 in 64 positive values"""
+    rows = torch.arange(n_rows, dtype=torch.int64)[:, None]
+    cols = torch.arange(n, dtype=torch.int64)[None, :]
+    b = token_base(seed, STREAM_SCORES, 0, rows, cols)
+    u = b.to(torch.float64) / 4294967296.0
+    if kind == "spread":
+        x = u * 8.0 - 4.0
+    elif kind == "nonneg":
+        x = -torch.log1p(-u)
+        x = torch.where((b & 31) == 0, torch.zeros_like(x), x)
+    elif kind == "cluster":
+        x = 1.0 + u * 2.0 ** -10
+        x[:, 7 % n] = 1e30
+        x[:, 11 % n] = -1e30
+    elif kind == "few_values":
+        vals = torch.tensor([-1.0, -0.0, 0.0, 0.5, 1.0], dtype=torch.float64)
+        x = vals[b % 5]
+    elif kind == "signed_zero":
+        x = torch.where((b & 1) == 0, torch.zeros_like(u), -torch.zeros_like(u))
+        x = torch.where(((b >> 1) & 63) == 0, 1.0 + u, x)
+    else:
+        raise ValueError(f"unknown score kind {kind}")
+    return x.to(torch.float32)
 
 
 def reject_counts(seed: int, n_seq: int, max_reject: int = 2) -> List[int]:

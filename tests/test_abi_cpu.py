@@ -82,6 +82,11 @@ def test_null_arguments_rejected_on_host(Q):
     rows = Q.qsa_rows(1, 1, 16, 16, None, 0)
     assert lib.qsa_append(ctypes.byref(cfg), ctypes.byref(rows), ctypes.byref(cache), 18, 16, 16, 16,
                           None) == Q.QSA_ERR_INVALID_ARG
+    # select reads score rows with 16-byte loads: misaligned base or odd stride
+    assert lib.qsa_topk_select(ctypes.byref(cfg), ctypes.byref(rows), 20, 1024, 16, 16, 16,
+                               None) == Q.QSA_ERR_INVALID_ARG
+    assert lib.qsa_topk_select(ctypes.byref(cfg), ctypes.byref(rows), 16, 1022, 16, 16, 16,
+                               None) == Q.QSA_ERR_INVALID_ARG
     # too many rows for one launch grid
     rows = Q.qsa_rows(70000, 1, 16, 16, None, 0)
     assert lib.qsa_append(ctypes.byref(cfg), ctypes.byref(rows), ctypes.byref(cache), 16, 16, 16, 16,

@@ -1,0 +1,64 @@
+"""Top-K selection on its own: qsa_topk_select on synthetic score rows against
+the oracle's exact top-K (score descending, block index ascending), bit-exact.
+
+The score distributions cover every way the kernel can settle the K-th largest
+key: spread scores (a short candidate list ranked directly), a narrow cluster
+inside a wide range (a long candidate list refined by further passes, or, past
+the candidate capacity, passes over the whole row), heavy ties and signed
+zeros (ties taken by the lower block index, -0 equal to +0), and rows longer
+than the kernel keeps in shared memory (keys read from global memory)."""
+import numpy as np
+import pytest
+import torch
+
+from indexer_selected_sparse_gb300 import synth as S
+from oracle import qsa_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+Q = pytest.importorskip("indexer_selected_sparse_gb300.qsa")
+
+
+def run_select(ratio, budget, ns, kind, seed):
+    cfg = Q.Config(ratio, budget, 64, 128, 32, 4)
+    K = cfg.topk
+    ld = (max(ns) + 3) // 4 * 4
+    scores = S.select_scores(seed, len(ns), ld, kind)
+    # visible = n * ratio + (ratio - 1): the incomplete tail does not change n
+    pos0 = torch.tensor([n * ratio + ratio - 2 for n in ns], dtype=torch.int32)
+    rows = Q.Rows(torch.arange(len(ns), dtype=torch.int32, device="cuda"), pos0.cuda(), 1)
+    sel = torch.full((len(ns), K), -7, dtype=torch.int32, device="cuda")
+    nsel = torch.full((len(ns),), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Q.qsa_topk_select(cfg, rows, scores.cuda(), ld, sel, nsel, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    sel = sel.cpu().numpy()
+    nsel = nsel.cpu().numpy()
+    for r, n in enumerate(ns):
+        want = O.select_blocks(scores[r, :n].numpy().astype(np.float64), K)
+        assert nsel[r] == len(want), (kind, n)
+        assert np.array_equal(sel[r, : len(want)], want), (kind, n, r)
+        assert (sel[r, len(want):] == -1).all()
+
+
+@pytest.mark.parametrize("kind", S.SCORE_KINDS)
+def test_select_k512_on_chip(kind):
+    # K = 512; rows from just above K to 16384 blocks (64k tokens)
+    run_select(4, 2048, [513, 600, 4000, 8192, 8193, 16384], kind, seed=21)
+
+
+@pytest.mark.parametrize("kind", ["spread", "cluster", "few_values"])
+def test_select_rows_beyond_shared_memory(kind):
+    # ratio 2: 100000 blocks is more than the kernel stages on chip
+    run_select(2, 1024, [100000, 45056, 45057], kind, seed=22)
+
+
+@pytest.mark.parametrize("kind", ["spread", "nonneg", "cluster"])
+def test_select_k2048(kind):
+    run_select(4, 8192, [2049, 5000, 20000], kind, seed=23)
+
+
+def test_select_dense_rows_take_every_block():
+    # n <= K: every block, in order, padded with -1
+    run_select(4, 2048, [1, 2, 511, 512], "spread", seed=24)

@@ -58,3 +58,15 @@ def test_ragged_prefixes_cover_the_boundary():
     assert len(p) == 64 and {2050, 2051, 2052} <= set(p)
     assert min(p) >= 512 and max(p) <= 131072
     assert sum(1 for x in p if x < 2050) >= 3 and sum(1 for x in p if x > 8192) >= 20
+
+
+def test_select_scores_kinds_are_seeded_and_shaped():
+    for kind in S.SCORE_KINDS:
+        a = S.select_scores(5, 3, 257, kind)
+        b = S.select_scores(5, 3, 257, kind)
+        assert a.shape == (3, 257) and a.dtype == torch.float32
+        assert torch.equal(a, b) and torch.isfinite(a).all()
+    z = S.select_scores(5, 2, 4096, "signed_zero")
+    assert (torch.signbit(z) & (z == 0)).any() and (~torch.signbit(z) & (z == 0)).any()
+    c = S.select_scores(5, 2, 4096, "cluster")
+    assert c.max() > 1e29 and c.min() < -1e29
