@@ -110,6 +110,7 @@ attn_kernel(Shape sh, int R, int n_split, int split_len, const int32_t *__restri
   __syncthreads();
 
   // ---- gather of one stage: thread -> (slot, 16 of its 32*HKV 16-byte pieces)
+  const uint64_t stream_policy = l2_evict_first();
   const int my_slot = tid / G::kThreadsPerSlot;
   const int my_part = tid % G::kThreadsPerSlot;
   auto load_stage = [&](int chunk_idx, int buf) {
@@ -132,7 +133,7 @@ attn_kernel(Shape sh, int R, int n_split, int split_len, const int32_t *__restri
       const uint16_t *src = (kv ? vbase : kbase) + (bytes ? gg * kHeadDim + c16 * 8 : 0);
       const uint32_t dst = stage + kv * G::kHalfStage + (gg * G::kChunk + my_slot) * G::kRowBytes +
                            ((c16 ^ (my_slot & 7)) << 4);
-      cp_async16(dst, src, bytes);
+      cp_async16_stream(dst, src, bytes, stream_policy);
     }
   };
 
@@ -324,12 +325,16 @@ attn_kernel(Shape sh, int R, int n_split, int split_len, const int32_t *__restri
 
 }
 
-// Split merge: one CTA per (row, KV head): 256 threads, thread t combines
-// dims 4*(t%32) .. +3 of query head (KV head's first head + t/32) over the
-// splits, in split order, so the result does not depend on how the splits were
-// scheduled. In the fused step the CTA (0, 0) also commits the step (advances
-// ingested, and pos0 when asked): every earlier kernel of the step, including
-// the attention kernel this one waits for, has finished reading them.
+// Split merge: one CTA per (row, KV head), one warp per query head of the KV
+// head's group; lane t owns dims 4t .. 4t+3. Up to 32 splits, every load is
+// issued before any arithmetic (lane j fetches the running max m and sum l of
+// split j, and every lane fetches its dims of all split outputs), so the merge
+// costs one memory round trip; the weights 2^(m_s - max) then reach every lane
+// by shuffle. More splits are taken 32 at a time. The sums run in split order,
+// so the result does not depend on how the splits were scheduled. In the fused
+// step the CTA (0, 0) also commits the step (advances ingested, and pos0 when
+// asked): every earlier kernel of the step, including the attention kernel this
+// one waits for, has finished reading them.
 constexpr int kMergeThreads = 256;
 
 __global__ void __launch_bounds__(kMergeThreads)
@@ -350,32 +355,63 @@ merge_kernel(int hq, int hkv, int n_split, const float *__restrict__ part_m,
     }
   }
   const int group = hq / hkv;
-  const int hl = t >> 5;
+  const int hl = t >> 5, lane = t & 31;
   if (hl >= group) return;
   const int h = g * group + hl;
-  const int d4 = (t & 31) * 4;
   const size_t b0 = static_cast<size_t>(row) * n_split * hq + h;
-  float m = -INFINITY;
-  for (int s = 0; s < n_split; ++s) m = fmaxf(m, __ldg(&part_m[b0 + static_cast<size_t>(s) * hq]));
+  const float *acc_base = part_acc + b0 * kHeadDim + lane * 4;
+  const size_t acc_step = static_cast<size_t>(hq) * kHeadDim;
+  // the first 32 splits' loads all go out before anything waits on them
+  float4 v[32];
+  int cnt = min(32, n_split);
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (j < cnt) v[j] = __ldg(reinterpret_cast<const float4 *>(acc_base + j * acc_step));
+  float m_mine = -INFINITY, l_mine = 0.f;
+  if (lane < cnt) {
+    m_mine = __ldg(&part_m[b0 + static_cast<size_t>(lane) * hq]);
+    l_mine = __ldg(&part_l[b0 + static_cast<size_t>(lane) * hq]);
+  }
+  float m = m_mine;
+  for (int s = lane + 32; s < n_split; s += 32) m = fmaxf(m, __ldg(&part_m[b0 + static_cast<size_t>(s) * hq]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   const float ref = m == -INFINITY ? 0.f : m;
   float l = 0.f;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int s = 0; s < n_split; ++s) {
-    const size_t k = b0 + static_cast<size_t>(s) * hq;
-    const float wgt = exp2f(__ldg(&part_m[k]) - ref);
-    l += wgt * __ldg(&part_l[k]);
-    const float4 v = __ldg(reinterpret_cast<const float4 *>(part_acc + k * kHeadDim + d4));
-    a.x += wgt * v.x;
-    a.y += wgt * v.y;
-    a.z += wgt * v.z;
-    a.w += wgt * v.w;
+  for (int s0 = 0; s0 < n_split; s0 += 32) {
+    if (s0 > 0) {
+      cnt = min(32, n_split - s0);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < cnt) v[j] = __ldg(reinterpret_cast<const float4 *>(acc_base + (s0 + j) * acc_step));
+      m_mine = -INFINITY;
+      l_mine = 0.f;
+      if (lane < cnt) {
+        m_mine = __ldg(&part_m[b0 + static_cast<size_t>(s0 + lane) * hq]);
+        l_mine = __ldg(&part_l[b0 + static_cast<size_t>(s0 + lane) * hq]);
+      }
+    }
+    const float w = lane < cnt ? exp2f(m_mine - ref) : 0.f;
+    l += w * l_mine;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      if (j < cnt) {
+        a.x += wj * v[j].x;
+        a.y += wj * v[j].y;
+        a.z += wj * v[j].z;
+        a.w += wj * v[j].w;
+      }
+    }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   const float inv = l > 0.f ? 1.f / l : 0.f;
   uint2 packed;
   packed.x = pack_bf16(a.x * inv, a.y * inv);
   packed.y = pack_bf16(a.z * inv, a.w * inv);
-  *reinterpret_cast<uint2 *>(out + (static_cast<size_t>(row) * hq + h) * kHeadDim + d4) = packed;
+  *reinterpret_cast<uint2 *>(out + (static_cast<size_t>(row) * hq + h) * kHeadDim + lane * 4) = packed;
 }
 
 struct SplitPlan {

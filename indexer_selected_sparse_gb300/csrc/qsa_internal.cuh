@@ -52,6 +52,20 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int sr
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                "r"(src_bytes));
 }
+// L2 policy for data read once per step (the gathered K/V rows, the compressed
+// keys): evicted first, so that what the step re-reads (page tables, scores,
+// selections, split partials) and the kernels' code stay in L2 across steps.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void cp_async16_stream(uint32_t dst, const void *src, int src_bytes,
+                                                  uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes), "l"(policy)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {

@@ -72,6 +72,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// The same with an L2 cache policy (the key stream is read once per step).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int c0, int c1, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                "r"(ncols));
@@ -341,6 +351,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_consta
     // are loaded before the current batch's copies are issued, so no
     // global-memory latency sits between two batches.
     Walker w = walker_start(a, n_groups, lane);
+    const uint64_t stream_policy = l2_evict_first();
     const int per_batch = 32 / pages_in_tile;
     Batch cur = load_batch(a, w, lane, per_batch, pages_in_tile, bpp);
     pdl_wait();  // the compressed keys come from the append kernel
@@ -380,8 +391,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_consta
           const int slot = lane - it * pages_in_tile;
 #pragma unroll
           for (int hh = 0; hh < HALVES; ++hh)
-            tma_load_2d(a_u + s * A_STAGE + hh * A_HALF + slot * bpp * 128, &tm_keys, a_full(s), hh * 64,
-                        cur.pg * bpp);
+            tma_load_2d_hint(a_u + s * A_STAGE + hh * A_HALF + slot * bpp * 128, &tm_keys, a_full(s),
+                             hh * 64, cur.pg * bpp, stream_policy);
         }
       }
       w = wn;
