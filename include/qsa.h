@@ -247,8 +247,8 @@ int qsa_decode(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cac
  * framework's input and output tensors, or a loop where cudaMalloc is not
  * allowed). The call allocates nothing.
  *   - Every GPU that loads the library holds that array until the process
- *     exits. A call whose partials would not fit (about 283 KB per row at
- *     Hq = 32, budget 2048: up to 118 rows) returns QSA_ERR_WORKSPACE.
+ *     exits. A call whose partials would not fit (about 316 KB per row at
+ *     Hq = 32, budget 2048: up to 106 rows) returns QSA_ERR_WORKSPACE.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents; calls that overlap on the GPU race and give wrong results.
  *     Nothing in it needs to start at zero.

@@ -11,9 +11,13 @@
 //   slot j >= n_sel*ratio : token n_blk*ratio + (j - n_sel*ratio)   (the tail)
 // n_slots = n_sel*ratio + (V - n_blk*ratio) <= budget + ratio - 1.
 //
-// CTA (split, row) takes a contiguous range of slots. Each stage gathers the
-// K and V rows of kChunk slots for all KV heads with 16-byte cp.async
-// (3-stage pipeline) into an XOR-swizzled shared tile. Warp w owns KV head
+// A unit of work is one split (a fixed range of kSplitSlots slots) of one row.
+// A CTA takes up to kMaxUnitsPerCta units (u = blockIdx.x + k * gridDim.x),
+// resolves the slots of all of them to cache rows once, and streams their
+// chunks through one pipeline, so the loads of the next unit are in flight
+// while the current one finishes. Each stage gathers the K and V rows of kChunk
+// slots for all KV heads with 16-byte cp.async (3-stage pipeline) into an
+// XOR-swizzled shared tile. Warp w owns KV head
 // w % Hkv and a 16-slot sub-tile. Per sub-tile:
 //   S^T[16 tok x 8 heads] = K[16 x 128] . Q^T   (tokens on M: m16n8k16 x8)
 //   online softmax per head column (exp2, scale folded with log2 e)
@@ -22,6 +26,8 @@
 //   O^T[128 x 8] += V^T . P^T                   (ldmatrix.trans of V, x16)
 // The split writes (m, l, acc) in fp32; the merge kernel combines the splits in
 // split order and rounds o = acc / l to bf16.
+#include <algorithm>
+
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -30,7 +36,8 @@ namespace {
 constexpr int kAttnThreads = 128;
 constexpr int kAttnWarps = 4;
 constexpr int kStages = 3;
-constexpr int kSplitSlots = 128;
+constexpr int kSplitSlots = 112;  // 7 stages of 16 slots
+constexpr int kMaxUnitsPerCta = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int HKV>
@@ -48,64 +55,97 @@ __device__ __forceinline__ int slot_token(int j, int n_body, int log2r, int r, i
   return j < n_body ? sel_row[j >> log2r] * r + (j & (r - 1)) : tail0 + (j - n_body);
 }
 
+// One unit: split `sp` of row `row`, its slot range and token-set layout.
+struct AttnUnit {
+  int row, sp, seq, visible, n_body, tail0, slot_lo, slot_hi, n_chunks;
+};
+
 template <int HKV>
 __global__ void __launch_bounds__(kAttnThreads)
-attn_kernel(Shape sh, int R, int n_split, int split_len, const int32_t *__restrict__ seq_ids,
+attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int32_t *__restrict__ seq_ids,
             const int32_t *__restrict__ pos0, CacheView cv, const uint16_t *__restrict__ q,
             const int32_t *__restrict__ sel, const int32_t *__restrict__ n_sel_arr,
             float *__restrict__ part_m, float *__restrict__ part_l, float *__restrict__ part_acc,
             int32_t *status) {
   using G = AttnGeom<HKV>;
+  static_assert(kSplitSlots <= kAttnThreads, "one slot-table entry per thread and unit");
   extern __shared__ __align__(128) uint8_t smem[];
-  // after the stage buffers: the token row (page * P + offset) of every slot of
-  // this split, or -1
+  // after the stage buffers: per unit, the cache row (page * P + offset) of
+  // every slot of its split, or -1; then the scratch of the warp combine
+  const int table = (split_len + G::kChunk - 1) / G::kChunk * G::kChunk;
   int32_t *slot_row = reinterpret_cast<int32_t *>(smem + kStages * G::kStageBytes);
+  float *red = reinterpret_cast<float *>(slot_row + kMaxUnitsPerCta * table);
+  __shared__ AttnUnit s_unit[kMaxUnitsPerCta];
 
   pdl_wait();  // sel / n_sel come from the select kernel
   pdl_trigger();
-  const int row = blockIdx.y;
-  const int sp = blockIdx.x;
-  const int i = row / R;
-  const int s = seq_ids[i];
-  const int visible = pos0[i] + (row - i * R) + 1;
-  const int r = sh.ratio;
-  const bool row_ok = visible >= 1 && visible <= cv.max_pages * sh.page;
-  if (!row_ok && sp == 0 && threadIdx.x == 0) report(status, QSA_ERR_CAPACITY);
-  const int n_blk = row_ok ? (visible >> sh.log2_ratio) : 0;
-  const int n_sel = row_ok ? min(max(n_sel_arr[row], 0), min(n_blk, sh.topk)) : 0;
-  const int n_body = n_sel * r;
-  const int tail0 = n_blk * r;
-  const int n_slots = row_ok ? n_body + (visible - tail0) : 0;
-  const int seg = split_len;  // fixed cut: independent of the batch
-  const int slot_lo = min(n_slots, sp * seg);
-  const int slot_hi = min(n_slots, slot_lo + seg);
-  const int n_chunks = (slot_hi - slot_lo + G::kChunk - 1) / G::kChunk;
-  const int32_t *sel_row = sel + static_cast<size_t>(row) * sh.topk;
-  const int32_t *ptab = cv.page_table + static_cast<size_t>(s) * cv.max_pages;
-  const int P = sh.page;
-  const int group = sh.hq / HKV;
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = warp % HKV;            // KV head of this warp
   const int sub = warp / HKV;          // 16-slot sub-tile of the stage
   const int smem_u = smem_u32(smem);
+  const int r = sh.ratio;
+  const int P = sh.page;
+  const int group = sh.hq / HKV;
+  const int nu = min(kMaxUnitsPerCta, (n_units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                          static_cast<int>(gridDim.x));
 
-  // ---- resolve every slot of the split to its token row once, all in parallel:
-  // the stage loads below then need no global lookups
-  // the table covers whole stages: entries past the split's end are -1
-  const int table = (seg + G::kChunk - 1) / G::kChunk * G::kChunk;
-  for (int x = tid; x < table; x += kAttnThreads) {
-    const int j = slot_lo + x;
-    int rowidx = -1;
-    if (j < slot_hi) {
-      const int t = slot_token(j, n_body, sh.log2_ratio, r, tail0, sel_row);
-      const int page = (t >= 0 && t < visible) ? ptab[t >> sh.log2_page] : -1;
-      if (page >= 0 && page < cv.num_pages)
-        rowidx = page * P + (t & (P - 1));
-      else
-        report(status, QSA_ERR_PAGE);
+  // ---- the units of this CTA
+  if (tid < nu) {
+    AttnUnit U;
+    const int u = blockIdx.x + tid * gridDim.x;
+    U.row = u / n_split;
+    U.sp = u - U.row * n_split;
+    const int i = U.row / R;
+    U.seq = seq_ids[i];
+    U.visible = pos0[i] + (U.row - i * R) + 1;
+    const bool row_ok = U.visible >= 1 && U.visible <= cv.max_pages * P;
+    if (!row_ok && U.sp == 0) report(status, QSA_ERR_CAPACITY);
+    const int n_blk = row_ok ? (U.visible >> sh.log2_ratio) : 0;
+    const int n_sel = row_ok ? min(max(n_sel_arr[U.row], 0), min(n_blk, sh.topk)) : 0;
+    U.n_body = n_sel * r;
+    U.tail0 = n_blk * r;
+    const int n_slots = row_ok ? U.n_body + (U.visible - U.tail0) : 0;
+    U.slot_lo = min(n_slots, U.sp * split_len);  // fixed cut: independent of the batch
+    U.slot_hi = min(n_slots, U.slot_lo + split_len);
+    U.n_chunks = (U.slot_hi - U.slot_lo + G::kChunk - 1) / G::kChunk;
+    s_unit[tid] = U;
+  }
+  __syncthreads();
+
+  // ---- resolve every slot of every unit to its cache row, all in parallel:
+  // the stage loads below need no global lookups. Entries past a split's end
+  // (the table covers whole stages) are -1.
+  {
+    int tok[kMaxUnitsPerCta];
+#pragma unroll
+    for (int k = 0; k < kMaxUnitsPerCta; ++k) {
+      tok[k] = -1;
+      if (k < nu && tid < table) {
+        const AttnUnit &U = s_unit[k];
+        const int j = U.slot_lo + tid;
+        if (j < U.slot_hi)
+          tok[k] = slot_token(j, U.n_body, sh.log2_ratio, r, U.tail0, sel + static_cast<size_t>(U.row) * sh.topk);
+      }
     }
-    slot_row[x] = rowidx;
+#pragma unroll
+    for (int k = 0; k < kMaxUnitsPerCta; ++k) {
+      if (k < nu && tid < table) {
+        const AttnUnit &U = s_unit[k];
+        const int j = U.slot_lo + tid;
+        int rowidx = -1;
+        if (j < U.slot_hi) {
+          const int t = tok[k];
+          const int page = (t >= 0 && t < U.visible)
+                               ? cv.page_table[static_cast<size_t>(U.seq) * cv.max_pages + (t >> sh.log2_page)]
+                               : -1;
+          if (page >= 0 && page < cv.num_pages)
+            rowidx = page * P + (t & (P - 1));
+          else
+            report(status, QSA_ERR_PAGE);
+        }
+        slot_row[k * table + tid] = rowidx;
+      }
+    }
   }
   __syncthreads();
 
@@ -113,8 +153,8 @@ attn_kernel(Shape sh, int R, int n_split, int split_len, const int32_t *__restri
   const uint64_t stream_policy = l2_evict_first();
   const int my_slot = tid / G::kThreadsPerSlot;
   const int my_part = tid % G::kThreadsPerSlot;
-  auto load_stage = [&](int chunk_idx, int buf) {
-    const int rowidx = slot_row[chunk_idx * G::kChunk + my_slot];
+  auto load_stage = [&](int unit, int chunk_idx, int buf) {
+    const int rowidx = slot_row[unit * table + chunk_idx * G::kChunk + my_slot];
     const uint16_t *kbase = cv.k_pool, *vbase = cv.v_pool;
     int bytes = 0;
     if (rowidx >= 0) {
@@ -136,154 +176,150 @@ attn_kernel(Shape sh, int R, int n_split, int split_len, const int32_t *__restri
       cp_async16_stream(dst, src, bytes, stream_policy);
     }
   };
-
-  // ---- Q^T fragments (B operand of S^T = K Q^T) for the warp's 8 heads
-  uint32_t qf[8][2];
-  {
-    const int hl = lane >> 2;
-    const bool ok = hl < group;
-    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-        q + (static_cast<size_t>(row) * sh.hq + g * group + (ok ? hl : 0)) * kHeadDim);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qf[ks][0] = ok ? qrow[ks * 8 + (lane & 3)] : 0u;
-      qf[ks][1] = ok ? qrow[ks * 8 + 4 + (lane & 3)] : 0u;
+  // the load cursor runs kStages - 1 chunks ahead of the compute, across units
+  int lk = 0, lc = 0;
+  auto issue_next = [&](int buf) {
+    while (lk < nu && lc >= s_unit[lk].n_chunks) {
+      ++lk;
+      lc = 0;
     }
-  }
-
-  float acc[8][4];
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[mt][c] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
-  const float scale = kLog2e * rsqrtf(static_cast<float>(kHeadDim));
-
+    if (lk < nu) {
+      load_stage(lk, lc, buf);
+      ++lc;
+    }
+  };
 #pragma unroll
   for (int st = 0; st < kStages - 1; ++st) {
-    if (st < n_chunks) load_stage(st, st);
+    issue_next(st);
     cp_async_commit();
   }
 
-  for (int c = 0; c < n_chunks; ++c) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();
+  const float scale = kLog2e * rsqrtf(static_cast<float>(kHeadDim));
+  int gidx = 0;  // chunks computed so far (all units)
+  for (int k = 0; k < nu; ++k) {
+    const AttnUnit U = s_unit[k];
+    // ---- Q^T fragments (B operand of S^T = K Q^T) for the warp's 8 heads
+    uint32_t qf[8][2];
     {
-      const int nxt = c + kStages - 1;
-      if (nxt < n_chunks) load_stage(nxt, nxt % kStages);
-      cp_async_commit();
-    }
-    const int buf = c % kStages;
-    const uint32_t kt = smem_u + buf * G::kStageBytes + (g * G::kChunk + sub * 16) * G::kRowBytes;
-    const uint32_t vt = kt + G::kHalfStage;
-
-    // S^T = K . Q^T
-    float sa[4] = {0.f, 0.f, 0.f, 0.f};
+      const int hl = lane >> 2;
+      const bool ok = hl < group;
+      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+          q + (static_cast<size_t>(U.row) * sh.hq + g * group + (ok ? hl : 0)) * kHeadDim);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int rr = (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int cc = 2 * ks + (lane >> 4);
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(kt + rr * G::kRowBytes + ((cc ^ (rr & 7)) << 4), a0, a1, a2, a3);
-      mma_bf16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+      for (int ks = 0; ks < 8; ++ks) {
+        qf[ks][0] = ok ? qrow[ks * 8 + (lane & 3)] : 0u;
+        qf[ks][1] = ok ? qrow[ks * 8 + 4 + (lane & 3)] : 0u;
+      }
     }
-    // mask slots past the split's end, scale to the log2 domain
-    const int j0 = slot_lo + c * G::kChunk + sub * 16 + (lane >> 2);
-    const bool v0 = j0 < slot_hi, v1 = (j0 + 8) < slot_hi;
-    float s0 = v0 ? sa[0] * scale : -INFINITY;
-    float s1 = v0 ? sa[1] * scale : -INFINITY;
-    float s2 = v1 ? sa[2] * scale : -INFINITY;
-    float s3 = v1 ? sa[3] * scale : -INFINITY;
-    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+    float acc[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[mt][c] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+
+    for (int c = 0; c < U.n_chunks; ++c, ++gidx) {
+      cp_async_wait<kStages - 2>();
+      __syncthreads();
+      issue_next((gidx + kStages - 1) % kStages);
+      cp_async_commit();
+      const int buf = gidx % kStages;
+      const uint32_t kt = smem_u + buf * G::kStageBytes + (g * G::kChunk + sub * 16) * G::kRowBytes;
+      const uint32_t vt = kt + G::kHalfStage;
+
+      // S^T = K . Q^T
+      float sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int rr = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int cc = 2 * ks + (lane >> 4);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kt + rr * G::kRowBytes + ((cc ^ (rr & 7)) << 4), a0, a1, a2, a3);
+        mma_bf16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+      }
+      // mask slots past the split's end, scale to the log2 domain
+      const int j0 = U.slot_lo + c * G::kChunk + sub * 16 + (lane >> 2);
+      const bool v0 = j0 < U.slot_hi, v1 = (j0 + 8) < U.slot_hi;
+      float s0 = v0 ? sa[0] * scale : -INFINITY;
+      float s1 = v0 ? sa[1] * scale : -INFINITY;
+      float s2 = v1 ? sa[2] * scale : -INFINITY;
+      float s3 = v1 ? sa[3] * scale : -INFINITY;
+      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+      const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = exp2f(m_run[0] - ref0), al1 = exp2f(m_run[1] - ref1);
+      const float p0 = exp2f(s0 - ref0), p1 = exp2f(s1 - ref1);
+      const float p2 = exp2f(s2 - ref0), p3 = exp2f(s3 - ref1);
+      l_run[0] = l_run[0] * al0 + p0 + p2;
+      l_run[1] = l_run[1] * al1 + p1 + p3;
+      m_run[0] = mn0;
+      m_run[1] = mn1;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        acc[mt][0] *= al0;
+        acc[mt][1] *= al1;
+        acc[mt][2] *= al0;
+        acc[mt][3] *= al1;
+      }
+      // P^T as B operand, hi + lo bf16
+      const uint32_t hi_top = pack_bf16(p0, p1), hi_bot = pack_bf16(p2, p3);
+      const __nv_bfloat162 ht = *reinterpret_cast<const __nv_bfloat162 *>(&hi_top);
+      const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162 *>(&hi_bot);
+      const uint32_t lo_top = pack_bf16(p0 - __low2float(ht), p1 - __high2float(ht));
+      const uint32_t lo_bot = pack_bf16(p2 - __low2float(hb), p3 - __high2float(hb));
+      const uint32_t bh0 = movmatrix_t(hi_top), bh1 = movmatrix_t(hi_bot);
+      const uint32_t bl0 = movmatrix_t(lo_top), bl1 = movmatrix_t(lo_bot);
+      // O^T += V^T . P^T
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int tok = (lane & 7) + ((lane >> 4) << 3);
+        const int cc = 2 * mt + ((lane >> 3) & 1);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vt + tok * G::kRowBytes + ((cc ^ (tok & 7)) << 4), a0, a1, a2, a3);
+        mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
+        mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
+      }
+    }
+
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], o);
+      l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], o);
     }
-    const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-    const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = exp2f(m_run[0] - ref0), al1 = exp2f(m_run[1] - ref1);
-    const float p0 = exp2f(s0 - ref0), p1 = exp2f(s1 - ref1);
-    const float p2 = exp2f(s2 - ref0), p3 = exp2f(s3 - ref1);
-    l_run[0] = l_run[0] * al0 + p0 + p2;
-    l_run[1] = l_run[1] * al1 + p1 + p3;
-    m_run[0] = mn0;
-    m_run[1] = mn1;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      acc[mt][0] *= al0;
-      acc[mt][1] *= al1;
-      acc[mt][2] *= al0;
-      acc[mt][3] *= al1;
-    }
-    // P^T as B operand, hi + lo bf16
-    const uint32_t hi_top = pack_bf16(p0, p1), hi_bot = pack_bf16(p2, p3);
-    const __nv_bfloat162 ht = *reinterpret_cast<const __nv_bfloat162 *>(&hi_top);
-    const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162 *>(&hi_bot);
-    const uint32_t lo_top = pack_bf16(p0 - __low2float(ht), p1 - __high2float(ht));
-    const uint32_t lo_bot = pack_bf16(p2 - __low2float(hb), p3 - __high2float(hb));
-    const uint32_t bh0 = movmatrix_t(hi_top), bh1 = movmatrix_t(hi_bot);
-    const uint32_t bl0 = movmatrix_t(lo_top), bl1 = movmatrix_t(lo_bot);
-    // O^T += V^T . P^T
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const int tok = (lane & 7) + ((lane >> 4) << 3);
-      const int cc = 2 * mt + ((lane >> 3) & 1);
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4_t(vt + tok * G::kRowBytes + ((cc ^ (tok & 7)) << 4), a0, a1, a2, a3);
-      mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
-      mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
-    }
-  }
-  cp_async_wait<0>();
 
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], o);
-    l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], o);
-  }
-
-  // ---- combine warps that share a KV head (Hkv < 4), then write the split
-  if constexpr (G::kWarpsPerHead > 1) {
-    __syncthreads();  // stages are free now; reuse them as scratch
-    float *red = reinterpret_cast<float *>(smem);
-    // per warp: m[8], l[8], acc[8 heads][128 dims]
-    float *mine = red + warp * (16 + 8 * kHeadDim);
-    if (lane < 4) {
-      mine[2 * lane] = m_run[0];
-      mine[2 * lane + 1] = m_run[1];
-      mine[8 + 2 * lane] = l_run[0];
-      mine[8 + 2 * lane + 1] = l_run[1];
-    }
-    __syncthreads();
-    float mx[2], scl[2], lsum[2] = {0.f, 0.f};
-#pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) {
-      const int col = 2 * (lane & 3) + c2;
-      float m = -INFINITY;
-      for (int w2 = g; w2 < kAttnWarps; w2 += HKV) m = fmaxf(m, red[w2 * (16 + 8 * kHeadDim) + col]);
-      mx[c2] = m;
-      const float ref = m == -INFINITY ? 0.f : m;
-      for (int w2 = g; w2 < kAttnWarps; w2 += HKV) {
-        const float* o = red + w2 * (16 + 8 * kHeadDim);
-        lsum[c2] += o[8 + col] * exp2f(o[col] - ref);
+    // ---- combine warps that share a KV head (Hkv < 4), then write the split
+    if constexpr (G::kWarpsPerHead > 1) {
+      __syncthreads();  // the previous unit's combine has finished reading `red`
+      // per warp: m[8], l[8], acc[8 heads][128 dims]
+      float *mine = red + warp * (16 + 8 * kHeadDim);
+      if (lane < 4) {
+        mine[2 * lane] = m_run[0];
+        mine[2 * lane + 1] = m_run[1];
+        mine[8 + 2 * lane] = l_run[0];
+        mine[8 + 2 * lane + 1] = l_run[1];
       }
-      scl[c2] = exp2f((c2 ? m_run[1] : m_run[0]) - ref);
-    }
+      __syncthreads();
+      float mx[2], scl[2], lsum[2] = {0.f, 0.f};
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const int d0 = mt * 16 + (lane >> 2);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int col = 2 * (lane & 3) + (c & 1);
-        const int d = d0 + (c >> 1) * 8;
-        mine[16 + col * kHeadDim + d] = acc[mt][c] * scl[c & 1];
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int col = 2 * (lane & 3) + c2;
+        float m = -INFINITY;
+        for (int w2 = g; w2 < kAttnWarps; w2 += HKV) m = fmaxf(m, red[w2 * (16 + 8 * kHeadDim) + col]);
+        mx[c2] = m;
+        const float ref = m == -INFINITY ? 0.f : m;
+        for (int w2 = g; w2 < kAttnWarps; w2 += HKV) {
+          const float *o = red + w2 * (16 + 8 * kHeadDim);
+          lsum[c2] += o[8 + col] * exp2f(o[col] - ref);
+        }
+        scl[c2] = exp2f((c2 ? m_run[1] : m_run[0]) - ref);
       }
-    }
-    __syncthreads();
-    if (sub == 0) {
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const int d0 = mt * 16 + (lane >> 2);
@@ -291,38 +327,51 @@ attn_kernel(Shape sh, int R, int n_split, int split_len, const int32_t *__restri
         for (int c = 0; c < 4; ++c) {
           const int col = 2 * (lane & 3) + (c & 1);
           const int d = d0 + (c >> 1) * 8;
-          float v = 0.f;
-          for (int w2 = g; w2 < kAttnWarps; w2 += HKV) v += red[w2 * (16 + 8 * kHeadDim) + 16 + col * kHeadDim + d];
-          acc[mt][c] = v;
+          mine[16 + col * kHeadDim + d] = acc[mt][c] * scl[c & 1];
         }
       }
-      m_run[0] = mx[0];
-      m_run[1] = mx[1];
-      l_run[0] = lsum[0];
-      l_run[1] = lsum[1];
-    }
-  }
-  const size_t base = (static_cast<size_t>(row) * n_split + sp) * sh.hq + g * group;
-  if (sub == 0) {
+      __syncthreads();
+      if (sub == 0) {
 #pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) {
-      const int col = 2 * (lane & 3) + c2;
-      if (lane < 4 && col < group) {
-        part_m[base + col] = m_run[c2];
-        part_l[base + col] = l_run[c2];
+        for (int mt = 0; mt < 8; ++mt) {
+          const int d0 = mt * 16 + (lane >> 2);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int col = 2 * (lane & 3) + (c & 1);
+            const int d = d0 + (c >> 1) * 8;
+            float v = 0.f;
+            for (int w2 = g; w2 < kAttnWarps; w2 += HKV) v += red[w2 * (16 + 8 * kHeadDim) + 16 + col * kHeadDim + d];
+            acc[mt][c] = v;
+          }
+        }
+        m_run[0] = mx[0];
+        m_run[1] = mx[1];
+        l_run[0] = lsum[0];
+        l_run[1] = lsum[1];
       }
     }
+    const size_t base = (static_cast<size_t>(U.row) * n_split + U.sp) * sh.hq + g * group;
+    if (sub == 0) {
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const int d0 = mt * 16 + (lane >> 2);
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int col = 2 * (lane & 3) + c2;
+        if (lane < 4 && col < group) {
+          part_m[base + col] = m_run[c2];
+          part_l[base + col] = l_run[c2];
+        }
+      }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int col = 2 * (lane & 3) + (c & 1);
-        if (col < group) part_acc[(base + col) * kHeadDim + d0 + (c >> 1) * 8] = acc[mt][c];
+      for (int mt = 0; mt < 8; ++mt) {
+        const int d0 = mt * 16 + (lane >> 2);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int col = 2 * (lane & 3) + (c & 1);
+          if (col < group) part_acc[(base + col) * kHeadDim + d0 + (c >> 1) * 8] = acc[mt][c];
+        }
       }
     }
   }
-
+  cp_async_wait<0>();
 }
 
 // Split merge: one CTA per (row, KV head), one warp per query head of the KV
@@ -428,6 +477,18 @@ SplitPlan plan_splits(const Shape &sh, int rows) {
   return {(max_slots + kSplitSlots - 1) / kSplitSlots, kSplitSlots};
 }
 
+// Resident CTAs of the attention kernel on the current device (the grid is at
+// least this many CTAs when there are enough units, so every CTA stays busy).
+template <int HKV>
+int attn_resident_ctas(size_t smem) {
+  int dev = 0, sms = 0, occ = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_kernel<HKV>, kAttnThreads, smem) != cudaSuccess)
+    return 0;
+  return sms * occ;
+}
+
 template <int HKV>
 cudaError_t launch_attn_t(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                           const int32_t *pos0, const CacheView &cv, const uint16_t *q,
@@ -439,15 +500,23 @@ cudaError_t launch_attn_t(const Shape &sh, int n_seq, int R, const int32_t *seq_
   float *pm = static_cast<float *>(partials);
   float *pl_ = pm + n_part;
   float *pa = pl_ + n_part;
-  // slot table: the longest split rounded up to whole stages
+  // per unit a slot table covering whole stages; the warp-combine scratch when
+  // several warps share a KV head
   const int table = (pl.split_len + AttnGeom<HKV>::kChunk - 1) / AttnGeom<HKV>::kChunk * AttnGeom<HKV>::kChunk;
-  const size_t smem = kStages * AttnGeom<HKV>::kStageBytes + table * sizeof(int32_t);
+  const size_t red_bytes = AttnGeom<HKV>::kWarpsPerHead > 1 ? kAttnWarps * (16 + 8 * kHeadDim) * sizeof(float) : 0;
+  const size_t smem = kStages * AttnGeom<HKV>::kStageBytes + kMaxUnitsPerCta * table * sizeof(int32_t) + red_bytes;
   auto kern = attn_kernel<HKV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  e = launch_kernel(pdl, kern, dim3(pl.n_split, rows), dim3(kAttnThreads), smem, st, sh, R, pl.n_split,
-                    pl.split_len, seq_ids, pos0, cv, q, sel, n_sel, pm, pl_, pa, status);
+  const long long n_units = static_cast<long long>(rows) * pl.n_split;
+  long long grid = (n_units + kMaxUnitsPerCta - 1) / kMaxUnitsPerCta;
+  grid = std::max<long long>(grid, attn_resident_ctas<HKV>(smem));
+  grid = std::min(grid, n_units);
+  if (n_units > 0x7fffffff) return cudaErrorInvalidValue;
+  e = launch_kernel(pdl, kern, dim3(static_cast<unsigned>(grid)), dim3(kAttnThreads), smem, st, sh, R,
+                    static_cast<int>(n_units), pl.n_split, pl.split_len, seq_ids, pos0, cv, q, sel, n_sel, pm,
+                    pl_, pa, status);
   if (e != cudaSuccess) return e;
   return launch_kernel(pdl, merge_kernel, dim3(rows, sh.hkv), dim3(kMergeThreads), 0, st, sh.hq, sh.hkv,
                        pl.n_split, static_cast<const float *>(pm), static_cast<const float *>(pl_),

@@ -246,7 +246,7 @@ def workload(i: int) -> Workload:
     raise ValueError(f"no workload {i}")
 
 
-SCORE_KINDS = ("spread", "nonneg", "cluster", "few_values", "signed_zero")
+SCORE_KINDS = ("spread", "nonneg", "cluster", "few_values", "signed_zero", "relu_sum")
 
 
 def select_scores(seed: int, n_rows: int, n: int, kind: str) -> torch.Tensor:
@@ -259,7 +259,10 @@ def select_scores(seed: int, n_rows: int, n: int, kind: str) -> torch.Tensor:
                    outlier per row, so the row's key range is wide while most
                    keys share their high bits
       few_values   one of {-1, -0.0, +0.0, 0.5, 1}: heavy ties
-      signed_zero  +0.0 or -0.0 except about 1 in 64 positive values"""
+      signed_zero  +0.0 or -0.0 except about 1 in 64 positive values
+      relu_sum     about N(270, 70^2), clipped at 0: the shape of a row of
+                   sum_h w_h ReLU(q_h . k) over 64 heads with the decode
+                   workload's bf16 inputs (Irwin-Hall of 12 uniforms)"""
     rows = torch.arange(n_rows, dtype=torch.int64)[:, None]
     cols = torch.arange(n, dtype=torch.int64)[None, :]
     b = token_base(seed, STREAM_SCORES, 0, rows, cols)
@@ -279,6 +282,9 @@ def select_scores(seed: int, n_rows: int, n: int, kind: str) -> torch.Tensor:
     elif kind == "signed_zero":
         x = torch.where((b & 1) == 0, torch.zeros_like(u), -torch.zeros_like(u))
         x = torch.where(((b >> 1) & 63) == 0, 1.0 + u, x)
+    elif kind == "relu_sum":
+        u12 = draws(b, 12).to(torch.float64) / 4294967296.0
+        x = torch.clamp(270.0 + 70.0 * (u12.sum(-1) - 6.0), min=0.0)
     else:
         raise ValueError(f"unknown score kind {kind}")
     return x.to(torch.float32)

@@ -51,7 +51,8 @@ def test_static_scratch_rejects_too_many_rows():
     sh = S.SHAPES_MAIN
     Q = pytest.importorskip("indexer_selected_sparse_gb300.qsa")
     cfg = Q.Config.of(sh)
-    per_row = 17 * sh.n_q_heads * (128 + 2) * 4          # split partials of one row (17 splits)
+    n_split = -(-(sh.budget + sh.ratio - 1) // 112)      # fixed 112-slot splits of the widest row
+    per_row = n_split * sh.n_q_heads * (128 + 2) * 4      # its split partials (m, l, acc)
     too_many = Q.QSA_STATIC_SCRATCH_BYTES // per_row + 1
     ids = torch.arange(too_many, dtype=torch.int32, device="cuda")
     rows = Q.Rows(ids, torch.zeros_like(ids), 1)
