@@ -4,17 +4,19 @@
 // budget + ratio - 1 visible tokens).
 //
 // One CTA per row. Scores become order-preserving uint32 keys (-0 folded onto
-// +0) held in shared memory, each taken relative to the row's smallest key so
-// that the radix digits span exactly the range the row covers. Digits are 11
-// bits, most significant first: a pass histograms the keys that match the
-// prefix fixed so far and a block-wide suffix scan finds the digit that holds
-// the K-th largest key. Only the first pass reads every key: the keys of the
-// chosen digit are gathered into a candidate list, which one warp ranks
-// directly when it is short and further passes refine otherwise. The K-th
-// largest key T is then exact, and so is the number of ties at T that must be
-// taken. A stable compaction emits, in ascending block order, every block with
-// key > T and the lowest-indexed blocks with key == T: exactly the top-K under
-// (score desc, index asc). The selection stays on the device, so a step that
+// +0), each taken relative to the row's smallest key so that the radix digits
+// span exactly the range the row covers. Digits are 11 bits, most significant
+// first: a pass histograms the keys that match the prefix fixed so far and a
+// block-wide suffix scan finds the digit that holds the K-th largest key. Only
+// the first pass reads every key: the keys of the chosen digit are gathered
+// into a candidate list, which one warp ranks directly when it is short and
+// further passes refine otherwise. The K-th largest key T is then exact, and so
+// is the number of ties at T that must be taken. A stable compaction emits, in
+// ascending block order, every block with key > T and the lowest-indexed blocks
+// with key == T: exactly the top-K under (score desc, index asc).
+// Rows of up to 16k blocks keep their keys in registers and compact through
+// bitmaps; longer rows stage their keys in shared memory (or, past that, read
+// them from global memory). The selection stays on the device, so a step that
 // contains it can be captured in a CUDA graph.
 #include "qsa_internal.cuh"
 
@@ -66,18 +68,34 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2 *tmp) {
   return make_int2(before.x + x.x - v.x, before.y + x.y - v.y);
 }
 
-// Histogram update; a warp whose active lanes all hold the same digit (a run of
-// equal scores) makes one atomic instead of 32 that would serialise.
-__device__ __forceinline__ void hist_add(int *hist, uint32_t digit, bool active) {
-  const unsigned act = __ballot_sync(0xffffffffu, active);
-  if (!active) return;
-  const int leader = __ffs(act) - 1;
-  const uint32_t d0 = __shfl_sync(act, digit, leader);
-  if (__all_sync(act, digit == d0)) {
-    if ((threadIdx.x & 31) == leader) atomicAdd(&hist[digit], __popc(act));
-  } else {
-    atomicAdd(&hist[digit], 1);
+// After a histogram pass (hist filled, then a barrier): the digit that holds
+// the remaining-th largest key. Thread t owns the kBinsPerThread digits below
+// kBins - kBinsPerThread * t; a suffix scan from the top digit finds it. Updates
+// prefix / mask / remaining and leaves `hist` all zero.
+__device__ __forceinline__ void digit_search(int shift, uint32_t dmask, uint32_t &prefix, uint32_t &mask,
+                                             int &remaining, int *hist, int2 *scan_tmp, int *s_res) {
+  const int top_bin = kBins - 1 - kBinsPerThread * threadIdx.x;
+  int c[kBinsPerThread];
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    c[j] = hist[top_bin - j];
+    hist[top_bin - j] = 0;  // only this thread reads these bins
+    sum += c[j];
   }
+  int above = block_exclusive_scan2(make_int2(sum, 0), scan_tmp).x;
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    if (above < remaining && remaining <= above + c[j]) {
+      s_res[0] = top_bin - j;
+      s_res[1] = above;
+    }
+    above += c[j];
+  }
+  __syncthreads();
+  prefix |= static_cast<uint32_t>(s_res[0]) << shift;
+  mask |= dmask << shift;
+  remaining -= s_res[1];
 }
 
 // Key sources. Every key is taken relative to the row's smallest key, so the
@@ -124,34 +142,11 @@ __device__ __forceinline__ void radix_pass(Src list, int m, int shift, uint32_t 
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int x = base + b * kSelThreads + tid;
-      hist_add(hist, (k[b] >> shift) & dmask, x < m && (k[b] & mask) == prefix);
+      if (x < m && (k[b] & mask) == prefix) atomicAdd(&hist[(k[b] >> shift) & dmask], 1);
     }
   }
   __syncthreads();
-  // thread t owns the kBinsPerThread digits below kBins - kBinsPerThread * t:
-  // a suffix scan from the top digit finds the digit of the remaining-th largest
-  const int top_bin = kBins - 1 - kBinsPerThread * threadIdx.x;
-  int c[kBinsPerThread];
-  int sum = 0;
-#pragma unroll
-  for (int j = 0; j < kBinsPerThread; ++j) {
-    c[j] = hist[top_bin - j];
-    hist[top_bin - j] = 0;  // only this thread reads these bins
-    sum += c[j];
-  }
-  int above = block_exclusive_scan2(make_int2(sum, 0), scan_tmp).x;
-#pragma unroll
-  for (int j = 0; j < kBinsPerThread; ++j) {
-    if (above < remaining && remaining <= above + c[j]) {
-      s_res[0] = top_bin - j;
-      s_res[1] = above;
-    }
-    above += c[j];
-  }
-  __syncthreads();
-  prefix |= static_cast<uint32_t>(s_res[0]) << shift;
-  mask |= dmask << shift;
-  remaining -= s_res[1];
+  digit_search(shift, dmask, prefix, mask, remaining, hist, scan_tmp, s_res);
 }
 
 // Selection for one row whose keys (relative to the row minimum) span
@@ -276,50 +271,210 @@ __device__ __forceinline__ void select_row(Src src, int n, int K, uint32_t range
   }
 }
 
-__global__ void __launch_bounds__(kSelThreads)
-select_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__restrict__ scores,
-              int ld, int32_t *__restrict__ sel, int32_t *__restrict__ n_sel, int smem_keys,
-              int cap_tokens, int32_t *status) {
-  // [smem_keys] row keys, then [kCandMax] candidates
-  extern __shared__ __align__(16) uint32_t keys[];
-  __shared__ int hist[kBins];
-  __shared__ int2 scan_tmp[kSelWarps];
-  __shared__ uint32_t red_min[kSelWarps], red_max[kSelWarps];
-  __shared__ int s_res[2], s_ncand;
+// ---------------------------------------------------------------------------
+// Rows of at most NV * 4 * kSelThreads blocks: thread t holds the keys of
+// blocks 4 * (v * kSelThreads + t) + j (v < NV, j < 4) in registers for the
+// whole selection, so the histogram and the candidate gather are one pass each
+// with independent work per thread. The compaction marks the blocks above the
+// threshold, and the ties at it, in two bitmaps; one scan over the bitmap words
+// (at most 512) then emits the selected blocks in index order.
+// ---------------------------------------------------------------------------
+constexpr int kMaxBitmapWords = 16 * kSelThreads / 32;  // rows of up to 16k blocks
 
-  const int row = blockIdx.x;
-  const int i = row / R;
-  const int visible = pos0[i] + (row - i * R) + 1;
-  const int n = visible >> sh.log2_ratio;
-  const int K = sh.topk;
-  int32_t *out = sel + static_cast<size_t>(row) * K;
+// Candidates of the chosen digit: a warp with any candidate reserves its slots
+// with one atomic.
+__device__ __forceinline__ void offer_candidate(uint32_t k, bool c, uint32_t *cand, int *s_ncand) {
+  const unsigned bal = __ballot_sync(0xffffffffu, c);
+  if (bal == 0u) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(bal) - 1;
+  int off = 0;
+  if (lane == leader) off = atomicAdd(s_ncand, __popc(bal));
+  off = __shfl_sync(0xffffffffu, off, leader);
+  const int pos = off + __popc(bal & ((1u << lane) - 1u));
+  if (c && pos < kCandMax) cand[pos] = k;
+}
+
+template <int NV>
+__device__ __forceinline__ void select_in_registers(const float *__restrict__ srow, int n, int K,
+                                                    int32_t *__restrict__ out, uint32_t *keys,
+                                                    uint32_t *cand, int *hist, int2 *scan_tmp, int *s_res,
+                                                    int *s_ncand, uint32_t *red_min, uint32_t *red_max,
+                                                    uint32_t *sel_bits, uint32_t *tie_bits) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-  if (visible < 1 || visible > cap_tokens || n > ld) {
-    pdl_wait();
-    pdl_trigger();
-    for (int x = tid; x < K; x += kSelThreads) out[x] = -1;
-    if (tid == 0) {
-      n_sel[row] = 0;
-      report(status, QSA_ERR_CAPACITY);
-    }
-    return;
-  }
-  if (n <= K) {  // every block is selected: exactly dense attention
-    pdl_wait();
-    pdl_trigger();
-    for (int x = tid; x < K; x += kSelThreads) out[x] = x < n ? x : -1;
-    if (tid == 0) n_sel[row] = n;
-    return;
-  }
-
+  const int n4 = (n + 3) >> 2;  // 16-byte groups covering the row (ld is a multiple of 4)
+  const float4 *s4 = reinterpret_cast<const float4 *>(srow);
+  uint32_t d[NV][4];
 #pragma unroll
-  for (int j = 0; j < kBinsPerThread; ++j) hist[kBinsPerThread * tid + j] = 0;
-  if (tid == 0) s_ncand = 0;
-  pdl_wait();  // scores come from the score kernel
-  pdl_trigger();
-  uint32_t *cand = keys + smem_keys;
-  const float *srow = scores + static_cast<size_t>(row) * ld;
+  for (int v = 0; v < NV; ++v) {
+    const int x = v * kSelThreads + tid;
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (x < n4) f = s4[x];
+    d[v][0] = score_key(f.x);
+    d[v][1] = score_key(f.y);
+    d[v][2] = score_key(f.z);
+    d[v][3] = score_key(f.w);
+  }
+  auto valid = [&](int v, int j) { return 4 * (v * kSelThreads + tid) + j < n; };
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (valid(v, j)) {
+        kmin = min(kmin, d[v][j]);
+        kmax = max(kmax, d[v][j]);
+      }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if (lane == 0) {
+    red_min[warp] = kmin;
+    red_max[warp] = kmax;
+  }
+  __syncthreads();
+  kmin = lane < kSelWarps ? red_min[lane] : 0xffffffffu;
+  kmax = lane < kSelWarps ? red_max[lane] : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[v][j] -= kmin;  // invalid entries are never read
+
+  const uint32_t range = kmax - kmin;
+  int top = range ? 31 - __clz(range) : -1;
+  const uint32_t low_bits = (top >= 31) ? 0xffffffffu : (top >= 0 ? ((2u << top) - 1u) : 0u);
+  uint32_t prefix = 0u;
+  uint32_t mask = ~low_bits;
+  int remaining = K;
+  if (top >= 0) {
+    int width = min(kDigit, top + 1);
+    int shift = top + 1 - width;
+    const uint32_t dmask = (1u << width) - 1u;
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (valid(v, j)) atomicAdd(&hist[d[v][j] >> shift], 1);  // d <= range: the digit fits
+    __syncthreads();
+    digit_search(shift, dmask, prefix, mask, remaining, hist, scan_tmp, s_res);
+    top = shift - 1;
+    if (top >= 0) {
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          offer_candidate(d[v][j], valid(v, j) && (d[v][j] & mask) == prefix, cand, s_ncand);
+      __syncthreads();
+      const int nc = *s_ncand;
+      if (nc <= kDirectMax) {
+        // one warp ranks the candidates: the remaining-th largest has fewer than
+        // `remaining` candidates above it and at least that many at or above it
+        if (warp == 0) {
+          const uint32_t a = lane < nc ? cand[lane] : 0u;
+          const uint32_t b = lane + 32 < nc ? cand[lane + 32] : 0u;
+          int ga = 0, ea = 0, gb = 0, eb = 0;
+          for (int i = 0; i < nc; ++i) {
+            const uint32_t c = __shfl_sync(0xffffffffu, i < 32 ? a : b, i & 31);
+            ga += c > a;
+            ea += c == a;
+            gb += c > b;
+            eb += c == b;
+          }
+          if (lane < nc && ga < remaining && remaining <= ga + ea) {
+            s_res[0] = static_cast<int>(a);
+            s_res[1] = remaining - ga;
+          }
+          if (lane + 32 < nc && gb < remaining && remaining <= gb + eb) {
+            s_res[0] = static_cast<int>(b);
+            s_res[1] = remaining - gb;
+          }
+        }
+        __syncthreads();
+        prefix = static_cast<uint32_t>(s_res[0]);
+        remaining = s_res[1];
+      } else {
+        // long candidate lists: further passes over the list, or, when it
+        // overflowed, over the whole row staged in shared memory
+        const uint32_t *list = cand;
+        int m = nc;
+        if (nc > kCandMax) {
+#pragma unroll
+          for (int v = 0; v < NV; ++v)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (valid(v, j)) keys[4 * (v * kSelThreads + tid) + j] = d[v][j];
+          __syncthreads();
+          list = keys;
+          m = n;
+        }
+        while (top >= 0) {
+          width = min(kDigit, top + 1);
+          shift = top + 1 - width;
+          radix_pass(SmemKeys{list, 0u}, m, shift, (1u << width) - 1u, prefix, mask, remaining, hist,
+                     scan_tmp, s_res);
+          top = shift - 1;
+        }
+      }
+    }
+  }
+  const uint32_t thr = prefix;  // the K-th largest key
+  const int need = remaining;   // ties at thr to take (>= 1)
+
+  // ---- compaction through the bitmaps (zeroed at kernel start)
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (!valid(v, j)) continue;
+      const int idx = 4 * (v * kSelThreads + tid) + j;
+      const uint32_t bit = 1u << (idx & 31);
+      if (d[v][j] > thr)
+        atomicOr(&sel_bits[idx >> 5], bit);
+      else if (d[v][j] == thr)
+        atomicOr(&tie_bits[idx >> 5], bit);
+    }
+  __syncthreads();
+  const int n_words = (n + 31) >> 5;  // <= kMaxBitmapWords <= kSelThreads
+  uint32_t sw = 0u, tw = 0u;
+  if (tid < n_words) {
+    sw = sel_bits[tid];
+    tw = tie_bits[tid];
+  }
+  const int2 pre = block_exclusive_scan2(make_int2(__popc(sw), __popc(tw)), scan_tmp);
+  if (tid < n_words) {
+    // the ties before this word come first: take the lowest-indexed `need`
+    const int take = min(max(need - pre.y, 0), __popc(tw));
+    uint32_t taken = 0u, rest = tw;
+    for (int q = 0; q < take; ++q) {
+      const uint32_t low = rest & (0u - rest);
+      taken |= low;
+      rest ^= low;
+    }
+    uint32_t all = sw | taken;
+    int o = pre.x + min(pre.y, need);
+    while (all) {
+      const int b = __ffs(all) - 1;
+      all &= all - 1u;
+      if (o < K) out[o] = 32 * tid + b;
+      ++o;
+    }
+  }
+}
+
+// Longer rows: keys staged in shared memory (or read from global memory when
+// the row does not fit there either).
+__device__ __noinline__ void select_general(const float *__restrict__ srow, int n, int K,
+                                            int32_t *__restrict__ out, uint32_t *keys, uint32_t *cand,
+                                            int smem_keys, int *hist, int2 *scan_tmp, int *s_res,
+                                            int *s_ncand, uint32_t *red_min, uint32_t *red_max) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool on_chip = n <= smem_keys;
   uint32_t kmin = 0xffffffffu, kmax = 0u;
   {
@@ -358,10 +513,73 @@ select_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__
     kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
   }
   if (on_chip)
-    select_row(SmemKeys{keys, kmin}, n, K, kmax - kmin, cand, out, hist, scan_tmp, s_res, &s_ncand);
+    select_row(SmemKeys{keys, kmin}, n, K, kmax - kmin, cand, out, hist, scan_tmp, s_res, s_ncand);
   else
-    select_row(GlobalScores{srow, kmin}, n, K, kmax - kmin, cand, out, hist, scan_tmp, s_res,
-               &s_ncand);
+    select_row(GlobalScores{srow, kmin}, n, K, kmax - kmin, cand, out, hist, scan_tmp, s_res, s_ncand);
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+select_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__restrict__ scores,
+              int ld, int32_t *__restrict__ sel, int32_t *__restrict__ n_sel, int smem_keys,
+              int cap_tokens, int32_t *status) {
+  // [smem_keys] row keys, then [kCandMax] candidates
+  extern __shared__ __align__(16) uint32_t keys[];
+  __shared__ int hist[kBins];
+  __shared__ int2 scan_tmp[kSelWarps];
+  __shared__ uint32_t red_min[kSelWarps], red_max[kSelWarps];
+  __shared__ int s_res[2], s_ncand;
+  __shared__ uint32_t sel_bits[kMaxBitmapWords], tie_bits[kMaxBitmapWords];
+
+  const int row = blockIdx.x;
+  const int i = row / R;
+  const int visible = pos0[i] + (row - i * R) + 1;
+  const int n = visible >> sh.log2_ratio;
+  const int K = sh.topk;
+  int32_t *out = sel + static_cast<size_t>(row) * K;
+  const int tid = threadIdx.x;
+
+  if (visible < 1 || visible > cap_tokens || n > ld) {
+    pdl_wait();
+    pdl_trigger();
+    for (int x = tid; x < K; x += kSelThreads) out[x] = -1;
+    if (tid == 0) {
+      n_sel[row] = 0;
+      report(status, QSA_ERR_CAPACITY);
+    }
+    return;
+  }
+  if (n <= K) {  // every block is selected: exactly dense attention
+    pdl_wait();
+    pdl_trigger();
+    for (int x = tid; x < K; x += kSelThreads) out[x] = x < n ? x : -1;
+    if (tid == 0) n_sel[row] = n;
+    return;
+  }
+
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) hist[kBinsPerThread * tid + j] = 0;
+  if (tid == 0) s_ncand = 0;
+  for (int x = tid; x < kMaxBitmapWords; x += kSelThreads) {
+    sel_bits[x] = 0u;
+    tie_bits[x] = 0u;
+  }
+  pdl_wait();  // scores come from the score kernel
+  pdl_trigger();
+  uint32_t *cand = keys + smem_keys;
+  const float *srow = scores + static_cast<size_t>(row) * ld;
+  // rows up to 16k blocks (64k tokens at ratio 4) keep their keys in registers
+  if (n <= 4 * kSelThreads) {
+    select_in_registers<1>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max,
+                           sel_bits, tie_bits);
+  } else if (n <= 8 * kSelThreads) {
+    select_in_registers<2>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max,
+                           sel_bits, tie_bits);
+  } else if (n <= 16 * kSelThreads) {
+    select_in_registers<4>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max,
+                           sel_bits, tie_bits);
+  } else {
+    select_general(srow, n, K, out, keys, cand, smem_keys, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
+  }
   if (tid == 0) n_sel[row] = K;
 }
 

@@ -6,7 +6,9 @@ key: spread scores (a short candidate list ranked directly), a narrow cluster
 inside a wide range (a long candidate list refined by further passes, or, past
 the candidate capacity, passes over the whole row), heavy ties and signed
 zeros (ties taken by the lower block index, -0 equal to +0), and rows longer
-than the kernel keeps in shared memory (keys read from global memory)."""
+than the kernel keeps in shared memory (keys read from global memory). Rows up
+to about 110k blocks are selected by a cluster of CTAs that each hold a part of
+the row; longer rows by one CTA per row."""
 import numpy as np
 import pytest
 import torch
@@ -52,6 +54,12 @@ def test_select_k512_on_chip(kind):
 def test_select_rows_beyond_shared_memory(kind):
     # ratio 2: 100000 blocks is more than the kernel stages on chip
     run_select(2, 1024, [100000, 45056, 45057], kind, seed=22)
+
+
+@pytest.mark.parametrize("kind", ["spread", "relu_sum", "few_values"])
+def test_select_single_cta_path_for_very_long_rows(kind):
+    # a score stride of 120000 blocks is past what the cluster path holds on chip
+    run_select(2, 1024, [120000, 60000, 513], kind, seed=25)
 
 
 @pytest.mark.parametrize("kind", ["spread", "nonneg", "cluster"])
