@@ -6,9 +6,10 @@ key: spread scores (a short candidate list ranked directly), a narrow cluster
 inside a wide range (a long candidate list refined by further passes, or, past
 the candidate capacity, passes over the whole row), heavy ties and signed
 zeros (ties taken by the lower block index, -0 equal to +0), and rows longer
-than the kernel keeps in shared memory (keys read from global memory). Rows up
-to about 110k blocks are selected by a cluster of CTAs that each hold a part of
-the row; longer rows by one CTA per row."""
+than the kernel keeps in shared memory (keys read from global memory). Rows of
+up to 16k blocks keep their keys in registers, longer rows up to about 45k
+blocks in shared memory, and longer ones read them from global memory: the
+cases below cover all three."""
 import numpy as np
 import pytest
 import torch
@@ -57,8 +58,8 @@ def test_select_rows_beyond_shared_memory(kind):
 
 
 @pytest.mark.parametrize("kind", ["spread", "relu_sum", "few_values"])
-def test_select_single_cta_path_for_very_long_rows(kind):
-    # a score stride of 120000 blocks is past what the cluster path holds on chip
+def test_select_very_long_rows_and_a_short_one_in_one_launch(kind):
+    # 120000 and 60000 blocks read from global memory, 513 kept in registers
     run_select(2, 1024, [120000, 60000, 513], kind, seed=25)
 
 
