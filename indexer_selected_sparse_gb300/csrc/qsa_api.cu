@@ -186,7 +186,7 @@ int qsa_append(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cac
   cudaError_t e = launch_append(sh, rows->n_seq, rows->rows_per_seq, rows->seq_ids, rows->pos0,
                                 cache->page_table, cache->max_pages, cache->num_pages,
                                 cache->k_pool, cache->v_pool, cache->idxraw_pool, cache->idxblk_pool,
-                                cache->ingested, k_new, v_new, idx_k_new, status, stream);
+                                cache->ingested, k_new, v_new, idx_k_new, status, false, stream);
   if (e == cudaSuccess)
     e = launch_commit(rows->n_seq, rows->rows_per_seq, cache->max_pages * cfg->page_size,
                       rows->seq_ids, rows->pos0, cache->ingested, rows->advance, false, stream);
@@ -289,7 +289,7 @@ int qsa_decode(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cac
   cudaError_t e = launch_append(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cache->page_table,
                                 cache->max_pages, cache->num_pages, cache->k_pool, cache->v_pool,
                                 cache->idxraw_pool, cache->idxblk_pool, cache->ingested, k_new,
-                                v_new, idx_k_new, status, stream);
+                                v_new, idx_k_new, status, true, stream);
   if (e == cudaSuccess)
     e = launch_score(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, q_idx, w, scores, ld,
                      status, true, stream);

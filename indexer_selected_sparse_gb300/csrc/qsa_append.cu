@@ -27,6 +27,7 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
               const uint16_t *__restrict__ k_new, const uint16_t *__restrict__ v_new,
               const uint16_t *__restrict__ idx_new, int32_t *status) {
   pdl_trigger();  // the first kernel of the step: its successor may start its prologue
+  pdl_wait();     // the previous step's commit (ingested, pos0) when launched as a dependent
   const int i = blockIdx.x;
   const int s = seq_ids[i];
   const int p0 = pos0[i];
@@ -156,14 +157,12 @@ cudaError_t launch_append(const Shape &sh, int n_seq, int R, const int32_t *seq_
                           int num_pages, uint16_t *k_pool, uint16_t *v_pool,
                           uint16_t *idxraw_pool, uint16_t *idxblk_pool, const int32_t *ingested,
                           const uint16_t *k_new, const uint16_t *v_new,
-                          const uint16_t *idx_k_new, int32_t *status, cudaStream_t st) {
+                          const uint16_t *idx_k_new, int32_t *status, bool pdl, cudaStream_t st) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
   dim3 grid(n_seq, (R + kAppendTokensPerCta - 1) / kAppendTokensPerCta);
-  append_kernel<<<grid, kAppendThreads, 0, st>>>(sh, R, seq_ids, pos0, page_table, max_pages,
-                                                 num_pages, k_pool, v_pool, idxraw_pool,
-                                                 idxblk_pool, ingested, k_new, v_new, idx_k_new,
-                                                 status);
-  return cudaGetLastError();
+  return launch_kernel(pdl, append_kernel, grid, dim3(kAppendThreads), 0, st, sh, R, seq_ids, pos0, page_table,
+                       max_pages, num_pages, k_pool, v_pool, idxraw_pool, idxblk_pool, ingested, k_new, v_new,
+                       idx_k_new, status);
 }
 
 cudaError_t launch_commit(int n_seq, int R, int capacity, const int32_t *seq_ids,

@@ -38,6 +38,7 @@ constexpr int kAttnWarps = 4;
 constexpr int kStages = 3;
 constexpr int kSplitSlots = 112;  // 7 stages of 16 slots
 constexpr int kMaxUnitsPerCta = 4;
+constexpr int kPageCache = 2048;  // page-table entries a CTA copies to shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int HKV>
@@ -55,9 +56,11 @@ __device__ __forceinline__ int slot_token(int j, int n_body, int log2r, int r, i
   return j < n_body ? sel_row[j >> log2r] * r + (j & (r - 1)) : tail0 + (j - n_body);
 }
 
-// One unit: split `sp` of row `row`, its slot range and token-set layout.
+// One unit: split `sp` of row `row`, its slot range and token-set layout, and
+// where its sequence's page-table row sits in the CTA's page cache (-1: read
+// from global memory).
 struct AttnUnit {
-  int row, sp, seq, visible, n_body, tail0, slot_lo, slot_hi, n_chunks;
+  int row, sp, seq, visible, n_blk, n_body, tail0, slot_lo, slot_hi, n_chunks, pc_off;
 };
 
 template <int HKV>
@@ -71,14 +74,14 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
   static_assert(kSplitSlots <= kAttnThreads, "one slot-table entry per thread and unit");
   extern __shared__ __align__(128) uint8_t smem[];
   // after the stage buffers: per unit, the cache row (page * P + offset) of
-  // every slot of its split, or -1; then the scratch of the warp combine
+  // every slot of its split, or -1; the page cache; the scratch of the warp
+  // combine
   const int table = (split_len + G::kChunk - 1) / G::kChunk * G::kChunk;
   int32_t *slot_row = reinterpret_cast<int32_t *>(smem + kStages * G::kStageBytes);
-  float *red = reinterpret_cast<float *>(slot_row + kMaxUnitsPerCta * table);
+  int32_t *page_cache = slot_row + kMaxUnitsPerCta * table;
+  float *red = reinterpret_cast<float *>(page_cache + kPageCache);
   __shared__ AttnUnit s_unit[kMaxUnitsPerCta];
 
-  pdl_wait();  // sel / n_sel come from the select kernel
-  pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = warp % HKV;            // KV head of this warp
   const int sub = warp / HKV;          // 16-slot sub-tile of the stage
@@ -89,7 +92,9 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
   const int nu = min(kMaxUnitsPerCta, (n_units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                                           static_cast<int>(gridDim.x));
 
-  // ---- the units of this CTA
+  // ---- before the wait, everything the select kernel does not write: the
+  // units' rows and positions, their sequences' page-table rows (copied to the
+  // page cache) and the first unit's query
   if (tid < nu) {
     AttnUnit U;
     const int u = blockIdx.x + tid * gridDim.x;
@@ -100,7 +105,52 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
     U.visible = pos0[i] + (U.row - i * R) + 1;
     const bool row_ok = U.visible >= 1 && U.visible <= cv.max_pages * P;
     if (!row_ok && U.sp == 0) report(status, QSA_ERR_CAPACITY);
-    const int n_blk = row_ok ? (U.visible >> sh.log2_ratio) : 0;
+    U.n_blk = row_ok ? (U.visible >> sh.log2_ratio) : -1;  // -1: nothing to attend
+    U.pc_off = -1;
+    s_unit[tid] = U;
+  }
+  __syncthreads();
+  if (tid == 0) {  // page-cache room, in unit order, while it lasts
+    int used = 0;
+    for (int k = 0; k < nu; ++k) {
+      const int need = s_unit[k].n_blk >= 0 ? (s_unit[k].visible + P - 1) >> sh.log2_page : 0;
+      if (need > 0 && used + need <= kPageCache) {
+        s_unit[k].pc_off = used;
+        used += need;
+      }
+    }
+  }
+  __syncthreads();
+  for (int k = 0; k < nu; ++k) {
+    const AttnUnit &U = s_unit[k];
+    if (U.pc_off < 0) continue;
+    const int need = (U.visible + P - 1) >> sh.log2_page;
+    const int32_t *src = cv.page_table + static_cast<size_t>(U.seq) * cv.max_pages;
+    for (int e = tid; e < need; e += kAttnThreads) page_cache[U.pc_off + e] = src[e];
+  }
+  // Q^T fragments (B operand of S^T = K Q^T) of a unit for the warp's 8 heads
+  auto load_q = [&](int row, uint32_t (&qf)[8][2]) {
+    const int hl = lane >> 2;
+    const bool ok = hl < group;
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+        q + (static_cast<size_t>(row) * sh.hq + g * group + (ok ? hl : 0)) * kHeadDim);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qf[ks][0] = ok ? qrow[ks * 8 + (lane & 3)] : 0u;
+      qf[ks][1] = ok ? qrow[ks * 8 + 4 + (lane & 3)] : 0u;
+    }
+  };
+  uint32_t qf[8][2];
+  load_q(s_unit[0].row, qf);
+
+  pdl_wait();  // sel / n_sel come from the select kernel
+  pdl_trigger();
+
+  // ---- the units' slot ranges (the selected count comes from the select kernel)
+  if (tid < nu) {
+    AttnUnit &U = s_unit[tid];
+    const bool row_ok = U.n_blk >= 0;
+    const int n_blk = row_ok ? U.n_blk : 0;
     const int n_sel = row_ok ? min(max(n_sel_arr[U.row], 0), min(n_blk, sh.topk)) : 0;
     U.n_body = n_sel * r;
     U.tail0 = n_blk * r;
@@ -108,7 +158,6 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
     U.slot_lo = min(n_slots, U.sp * split_len);  // fixed cut: independent of the batch
     U.slot_hi = min(n_slots, U.slot_lo + split_len);
     U.n_chunks = (U.slot_hi - U.slot_lo + G::kChunk - 1) / G::kChunk;
-    s_unit[tid] = U;
   }
   __syncthreads();
 
@@ -135,9 +184,10 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
         int rowidx = -1;
         if (j < U.slot_hi) {
           const int t = tok[k];
-          const int page = (t >= 0 && t < U.visible)
-                               ? cv.page_table[static_cast<size_t>(U.seq) * cv.max_pages + (t >> sh.log2_page)]
-                               : -1;
+          int page = -1;
+          if (t >= 0 && t < U.visible)
+            page = U.pc_off >= 0 ? page_cache[U.pc_off + (t >> sh.log2_page)]
+                                 : cv.page_table[static_cast<size_t>(U.seq) * cv.max_pages + (t >> sh.log2_page)];
           if (page >= 0 && page < cv.num_pages)
             rowidx = page * P + (t & (P - 1));
           else
@@ -198,19 +248,7 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
   int gidx = 0;  // chunks computed so far (all units)
   for (int k = 0; k < nu; ++k) {
     const AttnUnit U = s_unit[k];
-    // ---- Q^T fragments (B operand of S^T = K Q^T) for the warp's 8 heads
-    uint32_t qf[8][2];
-    {
-      const int hl = lane >> 2;
-      const bool ok = hl < group;
-      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-          q + (static_cast<size_t>(U.row) * sh.hq + g * group + (ok ? hl : 0)) * kHeadDim);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        qf[ks][0] = ok ? qrow[ks * 8 + (lane & 3)] : 0u;
-        qf[ks][1] = ok ? qrow[ks * 8 + 4 + (lane & 3)] : 0u;
-      }
-    }
+    if (k > 0) load_q(U.row, qf);
     float acc[8][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
@@ -500,11 +538,12 @@ cudaError_t launch_attn_t(const Shape &sh, int n_seq, int R, const int32_t *seq_
   float *pm = static_cast<float *>(partials);
   float *pl_ = pm + n_part;
   float *pa = pl_ + n_part;
-  // per unit a slot table covering whole stages; the warp-combine scratch when
-  // several warps share a KV head
+  // per unit a slot table covering whole stages; the page cache; the
+  // warp-combine scratch when several warps share a KV head
   const int table = (pl.split_len + AttnGeom<HKV>::kChunk - 1) / AttnGeom<HKV>::kChunk * AttnGeom<HKV>::kChunk;
   const size_t red_bytes = AttnGeom<HKV>::kWarpsPerHead > 1 ? kAttnWarps * (16 + 8 * kHeadDim) * sizeof(float) : 0;
-  const size_t smem = kStages * AttnGeom<HKV>::kStageBytes + kMaxUnitsPerCta * table * sizeof(int32_t) + red_bytes;
+  const size_t smem = kStages * AttnGeom<HKV>::kStageBytes + (kMaxUnitsPerCta * table + kPageCache) * sizeof(int32_t) +
+                      red_bytes;
   auto kern = attn_kernel<HKV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));

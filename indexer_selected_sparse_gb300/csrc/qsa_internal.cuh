@@ -156,7 +156,7 @@ cudaError_t launch_append(const Shape &sh, int n_seq, int R, const int32_t *seq_
                           int num_pages, uint16_t *k_pool, uint16_t *v_pool,
                           uint16_t *idxraw_pool, uint16_t *idxblk_pool, const int32_t *ingested,
                           const uint16_t *k_new, const uint16_t *v_new,
-                          const uint16_t *idx_k_new, int32_t *status, cudaStream_t st);
+                          const uint16_t *idx_k_new, int32_t *status, bool pdl, cudaStream_t st);
 cudaError_t launch_commit(int n_seq, int R, int capacity, const int32_t *seq_ids,
                           int32_t *pos0, int32_t *ingested, int advance, bool pdl, cudaStream_t st);
 cudaError_t launch_rewind(int n_seq, const int32_t *seq_ids, const int32_t *n_drop,

@@ -271,19 +271,31 @@ struct Batch {
   bool have = false; // this lane's page holds a visible block
 };
 
-__device__ __forceinline__ Batch load_batch(const TcArgs &a, const Walker &w, int lane, int per_batch,
-                                            int pages_in_tile, int bpp) {
+// What a batch needs of its group: the first row, the blocks visible to its
+// last row and its sequence's page-table row. Loaded once per group, so a new
+// batch of the same group issues its page-id load without waiting on others.
+struct GroupInfo {
+  int g = -1, row0 = 0, nblk_last = 0;
+  const int32_t *ptab = nullptr;
+};
+
+__device__ __forceinline__ Batch load_batch(const TcArgs &a, const Walker &w, GroupInfo &gi, int lane,
+                                            int per_batch, int pages_in_tile, int bpp) {
+  if (w.g != gi.g) {
+    const int i = w.g / a.groups_per_seq;
+    const int j0 = (w.g - i * a.groups_per_seq) * a.G;
+    const int g_rows = min(a.G, a.R - j0);
+    gi.row0 = i * a.R + j0;
+    gi.nblk_last = (a.pos0[i] + j0 + g_rows) >> a.sh.log2_ratio;
+    gi.ptab = a.page_table + static_cast<size_t>(a.seq_ids[i]) * a.max_pages;
+    gi.g = w.g;
+  }
   Batch b;
-  const int i = w.g / a.groups_per_seq;
-  const int j0 = (w.g - i * a.groups_per_seq) * a.G;
-  const int g_rows = min(a.G, a.R - j0);
-  b.row0 = i * a.R + j0;
+  b.row0 = gi.row0;
   b.nb = min(min(per_batch, w.tiles - w.t), w.left);
-  const int nblk_last = (a.pos0[i] + j0 + g_rows) >> a.sh.log2_ratio;
-  const int32_t *ptab = a.page_table + static_cast<size_t>(a.seq_ids[i]) * a.max_pages;
   const int pidx = w.t * pages_in_tile + lane;
-  b.have = lane < b.nb * pages_in_tile && pidx * bpp < nblk_last;
-  b.pg = b.have ? ptab[pidx] : 0;
+  b.have = lane < b.nb * pages_in_tile && pidx * bpp < gi.nblk_last;
+  b.pg = b.have ? gi.ptab[pidx] : 0;
   return b;
 }
 
@@ -348,12 +360,14 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_consta
     // ---------------- TMA producer ----------------
     // Tiles are issued in batches of consecutive tiles of one group: lane L
     // holds the page id of page L of the batch. The page ids of the next batch
-    // are loaded before the current batch's copies are issued, so no
-    // global-memory latency sits between two batches.
+    // are loaded before the current batch's copies are issued, and the group's
+    // page-table row is cached, so no global-memory latency sits between two
+    // batches of a group.
     Walker w = walker_start(a, n_groups, lane);
     const uint64_t stream_policy = l2_evict_first();
     const int per_batch = 32 / pages_in_tile;
-    Batch cur = load_batch(a, w, lane, per_batch, pages_in_tile, bpp);
+    GroupInfo gi;
+    Batch cur = load_batch(a, w, gi, lane, per_batch, pages_in_tile, bpp);
     pdl_wait();  // the compressed keys come from the append kernel
     pdl_trigger();
     int cur_g = -1, gseq = -1, k = 0;
@@ -361,7 +375,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_consta
     while (ok && w.left > 0) {
       Walker wn = w;
       for (int it = 0; it < cur.nb; ++it) walker_next(wn, a, n_groups);
-      const Batch nxt = wn.left > 0 ? load_batch(a, wn, lane, per_batch, pages_in_tile, bpp) : Batch{};
+      const Batch nxt = wn.left > 0 ? load_batch(a, wn, gi, lane, per_batch, pages_in_tile, bpp) : Batch{};
       if (w.g != cur_g) {
         ++gseq;
         const int bs = gseq & 1;
