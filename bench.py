@@ -53,6 +53,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--n-batches", type=int, default=N_BATCHES,
                     help="rotating batches of 32 sequences (fewer: smaller device footprint, for profiling)")
+    ap.add_argument("--legs", default="decode,prefill",
+                    help="comma list of legs to run: decode (the headline), prefill (chunked-prefill "
+                         "index scoring against the bf16 tensor peak, and the fused prefill step)")
+    ap.add_argument("--prefill-steps", type=int, default=10)
+    ap.add_argument("--prefill-warmup", type=int, default=3)
     return ap.parse_args()
 
 
@@ -493,6 +498,120 @@ def make_line(wl, sh, B, K, W, world, value, ms, visibles, step_bytes, step_gbs,
 
 
 # ---------------------------------------------------------------------------
+# chunked-prefill leg: index scoring on the tensor cores, and the fused step
+# ---------------------------------------------------------------------------
+
+PREFILL_WORKLOAD_ID = 5    # one sequence, 8193-token chunk appended to a 24576-token prefix
+
+
+def run_prefill(args, dev):
+    """Chunked prefill: one sequence, an 8193-row chunk on a 24576-token prefix
+    (ratio 4, budget 2048, indexer 64 x 128). Every chunk row scores all blocks
+    visible to it (6144..8192), which is a causal 8192-block x (8193 x 64) x 128
+    bf16 contraction plus the ReLU * w epilogue. The compressed keys of the
+    sequence (2 MB) are L2-resident by the nature of the workload (every row
+    reads them); the score rows written (269 MB) exceed L2.
+
+    Times qsa_index_score alone (the tensor-core kernel, against the bf16
+    peak), the other stage entry points, and the whole fused step
+    (qsa_decode of the 8193 rows, the chunk rewound between steps)."""
+    import torch
+
+    from indexer_selected_sparse_gb300 import qsa as Q
+    from indexer_selected_sparse_gb300 import synth as S
+
+    wl = S.workload(PREFILL_WORKLOAD_ID)
+    sh = wl.shapes
+    cfg = Q.Config.of(sh)
+    p, C = wl.prefixes[0], wl.rows_per_seq
+    max_pages = math.ceil((p + C + 8) / sh.page_size)
+    cache = Q.PagedCache(cfg, S.page_table(wl.seed, 1, max_pages, contiguous=False), max_pages, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    seq = torch.zeros(1, dtype=torch.int32, device=dev)
+    a = 0
+    while a < p:
+        m = min(8192, p - a)
+        k, v, ix = S.token_rows(sh, wl.seed, 0, torch.arange(a, a + m), device=dev)
+        Q.qsa_append(cfg, Q.Rows(seq, torch.tensor([a], dtype=torch.int32, device=dev), m), cache, k, v, ix, status)
+        a += m
+    pos = torch.arange(p, p + C)
+    k, v, ix = S.token_rows(sh, wl.seed, 0, pos, device=dev)
+    q, qi, w = S.query_rows(sh, wl.seed, 0, pos, device=dev)
+    rows = Q.Rows(seq, torch.tensor([p], dtype=torch.int32, device=dev), C)
+    ws = Q.workspace(cfg, C, cache.max_blocks, device=dev)
+    out = torch.empty(C, sh.n_q_heads, sh.head_dim, dtype=torch.bfloat16, device=dev)
+    drop = torch.tensor([C], dtype=torch.int32, device=dev)
+    ld = (cache.max_blocks + 3) // 4 * 4
+    scores = torch.empty(C, ld, dtype=torch.float32, device=dev)
+    sel = torch.empty(C, cfg.topk, dtype=torch.int32, device=dev)
+    nsel = torch.empty(C, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def fused():
+        Q.qsa_decode(cfg, rows, cache, k, v, ix, qi, w, q, out, ws, status, stream=stream)
+
+    def rewind():
+        Q.qsa_rewind(cfg, seq, drop, cache.ingested, status, stream=stream)
+
+    def timed(fn, n, after=None):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                if after is not None:
+                    after()
+        torch.cuda.synchronize()
+        return sum(e0.elapsed_time(e1) for e0, e1 in evs) / n
+
+    W, K = max(args.prefill_warmup, 1), max(args.prefill_steps, 1)
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            fused()
+            rewind()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, Q.qsa_strerror(int(status.item()))
+    step_ms = timed(fused, K, after=rewind)
+    with torch.cuda.stream(stream):
+        fused()  # leave the chunk appended for the stage entry points
+    torch.cuda.synchronize()
+    score_fn = lambda: Q.qsa_index_score(cfg, rows, cache, qi, w, scores, ld, status, stream=stream)
+    select_fn = lambda: Q.qsa_topk_select(cfg, rows, scores, ld, sel, nsel, status, stream=stream)
+    attn_fn = lambda: Q.qsa_gather_attn(cfg, rows, cache, q, sel, nsel, out, ws, status, stream=stream)
+    stage_ms = {}
+    for name, fn in (("index_score", score_fn), ("topk_select", select_fn), ("gather_attn", attn_fn)):
+        with torch.cuda.stream(stream):
+            for _ in range(W):
+                fn()
+        stage_ms[name] = timed(fn, K)
+    assert int(status.item()) == 0, Q.qsa_strerror(int(status.item()))
+
+    visibles = [p + j + 1 for j in range(C)]
+    work = sum_work(sh, visibles)
+    _, tf_burst, peak_kind = measured_peaks()
+    score_tflops = work["score_flops"] / (stage_ms["index_score"] * 1e-3) / 1e12
+    attn_tflops = work["attn_flops"] / (stage_ms["gather_attn"] * 1e-3) / 1e12
+    return {
+        "workload": wl.name, "rows": C, "prefix": p,
+        "index_score": {"kernel": "score_tc_kernel<128>", "bound": "tensor",
+                        "achieved": round(score_tflops, 1), "peak": tf_burst, "unit": "TFLOP/s",
+                        "frac": round(score_tflops / tf_burst, 4),
+                        "peak_kind": peak_kind + " (bf16_tflops, burst: the kernel is timed alone)",
+                        "flops_per_launch": int(work["score_flops"]),
+                        "launch_ms": round(stage_ms["index_score"], 4)},
+        "stages_ms": {k_: round(v_, 4) for k_, v_ in stage_ms.items()},
+        "gather_attn_tflops": round(attn_tflops, 1),
+        "fused_step_ms": round(step_ms, 4),
+        "rows_per_s": round(C / (step_ms * 1e-3), 1),
+        "timing": f"{K} launches after {W} warm-up, CUDA events on the launching stream; "
+                  "fused step = qsa_decode of the chunk (append, score, select, attend, merge), "
+                  "rewound between steps outside the events",
+    }
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle (cpu_baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
 
@@ -618,7 +737,20 @@ def main():
     if args.impl == "reference":
         run_reference(args)
         return
+    legs = {x.strip() for x in args.legs.split(",") if x.strip()}
+    if "decode" not in legs:
+        # prefill leg alone (profiling): one line with the prefill object only
+        import torch
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        pre = run_prefill(args, torch.device("cuda", local))
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps({"prefill": pre}), flush=True)
+        return
     out, rank, world = run_gpu(args)
+    if "prefill" in legs:
+        import torch
+        out["prefill"] = run_prefill(args, torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))))
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(args.oracle_rows)
