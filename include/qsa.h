@@ -128,8 +128,16 @@ typedef struct qsa_rows {
 /* Paged cache of all sequences ([VA6], [VP5]). Logical token t of the
  * sequence in slot s lives in page page_table[s][t / P] at offset t % P.
  * Compressed block b of that sequence lives in the same page id of the block
- * pool, at row (b % (P/ratio)): the block pool shares the main page table at
- * 1/ratio density. All pools have num_pages pages. */
+ * pool, as block row rr = b % (P/ratio) of that page: the block pool shares
+ * the main page table at 1/ratio density. All pools have num_pages pages.
+ *
+ * Inside a block-pool page (P/ratio rows of d_I bf16 values) the rows are
+ * stored in tiles of G = min(P/ratio, 8) rows by 8 values: element (rr, d)
+ * sits at
+ *     ((rr / G) * (d_I / 8) + d / 8) * 8 * G + (rr % G) * 8 + d % 8
+ * (the tensor cores' K-major core-matrix order), so one contiguous copy of a
+ * page is a ready operand of the scoring contraction. The block pool is
+ * written only by qsa_append and read only by qsa_index_score / qsa_decode. */
 typedef struct qsa_cache {
   const int32_t *page_table; /* device [n_slots, max_pages] */
   int n_slots;
@@ -138,7 +146,7 @@ typedef struct qsa_cache {
   qsa_bf16 *k_pool;          /* device [num_pages, P, Hkv, D] */
   qsa_bf16 *v_pool;          /* device [num_pages, P, Hkv, D] */
   qsa_bf16 *idxraw_pool;     /* device [num_pages, P, d_I]   raw index keys */
-  qsa_bf16 *idxblk_pool;     /* device [num_pages, P/ratio, d_I] block keys */
+  qsa_bf16 *idxblk_pool;     /* device [num_pages, P/ratio * d_I] block keys (tiled, above) */
   int32_t *ingested;         /* device [n_slots]: tokens ingested per slot */
 } qsa_cache;
 

@@ -116,7 +116,9 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
       report(status, QSA_ERR_PAGE);
       continue;
     }
-    uint16_t *dst = blk_pool + (static_cast<size_t>(page_b) * bpp + (b & (bpp - 1))) * sh.d_idx + d2;
+    // d2 is even, so (d2, d2 + 1) are adjacent in the tiled page layout
+    uint16_t *dst = blk_pool + static_cast<size_t>(page_b) * bpp * sh.d_idx +
+                    blk_elem_offset(b & (bpp - 1), d2, bpp, sh.d_idx);
     *reinterpret_cast<uint32_t *>(dst) = pack_bf16(s0 * inv_r, s1 * inv_r);
   }
 }

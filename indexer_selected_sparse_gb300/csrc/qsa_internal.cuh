@@ -4,7 +4,8 @@
 //   k_pool, v_pool  [num_pages][P][Hkv][D]     a token's K (or V) row for all
 //                                                KV heads is Hkv*D*2 contiguous bytes
 //   idxraw_pool     [num_pages][P][d_I]
-//   idxblk_pool     [num_pages][P/ratio][d_I]   shares the page table at 1/ratio density
+//   idxblk_pool     [num_pages][P/ratio * d_I]  shares the page table at 1/ratio density;
+//                                                rows tiled in 8 x 8 core matrices (blk_elem_offset)
 //   page_table      [n_slots][max_pages] int32
 #pragma once
 
@@ -22,6 +23,15 @@ constexpr int kHeadDim = 128;
 // Device-side status codes go through a first-error-wins CAS.
 __device__ __forceinline__ void report(int32_t *status, int code) {
   if (status) atomicCAS(status, 0, code);
+}
+
+// Offset (in elements) of element (rr, d) of a block-pool page: rows in tiles of
+// G = min(blocks per page, 8) rows x 8 values, tiles ordered row-group major,
+// then 8-value chunk; inside a tile row-major. For 8 or more blocks per page a
+// page is a run of the tensor cores' K-major core matrices (8 rows x 16 bytes).
+__host__ __device__ __forceinline__ int blk_elem_offset(int rr, int d, int bpp, int d_idx) {
+  const int g = bpp < 8 ? bpp : 8;
+  return ((rr / g) * (d_idx >> 3) + (d >> 3)) * (g << 3) + (rr % g) * 8 + (d & 7);
 }
 
 // --- launch parameter blocks ---------------------------------------------

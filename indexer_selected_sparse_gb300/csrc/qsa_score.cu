@@ -58,8 +58,8 @@ score_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
     if (b < n_blk) {
       const int page = ptab[b >> bpp_log2];
       if (page >= 0 && page < cv.num_pages) {
-        src = cv.idxblk_pool +
-              ((static_cast<size_t>(page) << bpp_log2) + (b & ((1 << bpp_log2) - 1))) * DI + c * 8;
+        src = cv.idxblk_pool + (static_cast<size_t>(page) << bpp_log2) * DI +
+              blk_elem_offset(b & ((1 << bpp_log2) - 1), c * 8, 1 << bpp_log2, DI);
         bytes = 16;
       } else {
         report(status, QSA_ERR_PAGE);

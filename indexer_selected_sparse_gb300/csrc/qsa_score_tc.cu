@@ -11,14 +11,21 @@
 //     D[128 blocks, N] = K_tile[128, d_I] . Q_group^T[d_I, N],  N = G * H_I
 // with blocks on M, so each TMEM lane holds one block and the ReLU * w head sum
 // is a reduction inside one thread.
-//   * TMA (cp.async.bulk.tensor, 128B swizzle) gathers the tile page by page:
-//     one box of (blocks per page) x 64 dims per page and half of d_I, straight
-//     from the paged compressed-key pool; the query rows of the group are one box
-//     per half. The smem layout is the K-major SWIZZLE_128B canonical layout
-//     (8-row x 128-byte atoms, 1024-byte stride between 8-row groups).
+//   * The compressed-key pool stores each page as the tensor cores' K-major
+//     core matrices (8 blocks x 16 bytes), so the tile is gathered with one bulk
+//     copy per page (cp.async.bulk, 4 KB at ratio 4, d_I = 128) straight into an
+//     MMA-ready, unswizzled K-major layout: core matrices adjacent in K are 128 B
+//     apart, 8-block groups d_I * 16 B apart. The query rows of the group come
+//     in by TMA (cp.async.bulk.tensor, 128B swizzle), one box per 64 dims.
 //   * One thread issues d_I/16 tcgen05.mma (kind::f16, bf16 in, fp32 accumulate
 //     in TMEM) and commits them to an mbarrier.
-//   * Four warps read their 32 TMEM lanes with tcgen05.ld and write the scores.
+//   * 4 * G epilogue warps, one per (row of the group, TMEM lane quarter), read
+//     their 32 lanes with tcgen05.ld: the warp holds its row's head columns in
+//     registers, hands the TMEM buffer back at once, and reduces them with
+//     paired fp32 FMAs (fma.rn.f32x2) in four independent chains combined in a
+//     fixed order -- the same for every group size, so a row's score does not
+//     depend on the batch shape. TMEM holds two accumulators, so the epilogue of
+//     one tile overlaps the MMA of the next.
 // Every mbarrier wait is bounded in time; on expiry the CTA records
 // QSA_ERR_TIMEOUT, waits (bounded) for its own copies, frees its TMEM and exits.
 #include <cuda.h>
@@ -53,13 +60,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
+// Test for the completion of the phase with the given parity; while it is not
+// complete the thread may be suspended (not polling) until it completes or
+// kSuspendNs pass.
+constexpr uint32_t kSuspendNs = 100000;  // 100 us
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -72,13 +83,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-// The same with an L2 cache policy (the key stream is read once per step).
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                                 int c0, int c1, uint64_t policy) {
+// Contiguous global -> shared bulk copy completing on an mbarrier, with an L2
+// cache policy. Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                               uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
-      "[%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
 
@@ -110,6 +122,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 
+// K-major, unswizzled shared-memory matrix descriptor: start address, LBO = byte
+// distance between core matrices adjacent in K, SBO = byte distance between
+// 8-row groups, descriptor version 1, layout type 0 (no swizzle).
+__device__ __forceinline__ uint64_t smem_desc_interleave(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>((lbo & 0x3FFFF) >> 4) << 16;
+  d |= static_cast<uint64_t>((sbo & 0x3FFFF) >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
@@ -130,7 +154,7 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 }
 
 // 16 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
   uint32_t r[16];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
@@ -141,6 +165,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
       : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// (d0, d1) += (a0 * b0, a1 * b1), each a fused multiply-add rounded to nearest.
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rd, {%0, %1};\n fma.rn.f32x2 rd, ra, rb, rd;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -160,6 +191,7 @@ struct TcArgs {
   const int32_t *page_table;
   int max_pages;
   int num_pages;
+  const uint16_t *keys;  // compressed-key pool (tiled pages)
   const float *w;
   float *scores;
   int ld;
@@ -167,8 +199,13 @@ struct TcArgs {
   int n_groups;        // groups of rows (n_seq * groups_per_seq)
 };
 
-constexpr int kPThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
+constexpr int kMaxEpiWarps = 4 * kTcMaxGroup;  // one per (row of the group, TMEM lane quarter)
+constexpr int kMaxThreads = 64 + 32 * kMaxEpiWarps;  // warp 0: TMA producer, warp 1: MMA issuer, then epilogue
 constexpr int kMaxStages = 6;
+constexpr int kRowCols = 64;  // head columns of one row, at most
+// shared memory of the epilogue: per warp the weights of its row [kRowCols]
+constexpr int kEpiFloats = kMaxEpiWarps * kRowCols;
+constexpr int kNumBars = 2 * kMaxStages + 8;
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -300,15 +337,13 @@ __device__ __forceinline__ Batch load_batch(const TcArgs &a, const Walker &w, Gr
 }
 
 // Shared memory (1024-aligned): [A stages: S x DI/64 halves x 128 rows x 128 B]
-// [B slots: 2 x DI/64 halves x npad rows x 128 B][epilogue weights: npad floats]
+// [B slots: 2 x DI/64 halves x npad rows x 128 B][epilogue: kEpiFloats floats]
 // [barriers][tmem address][abort flag]
 template <int DI>
-__global__ void __launch_bounds__(kPThreads, 1)
-score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_constant__ CUtensorMap tm_q,
-                TcArgs a, int n_stages) {
+__global__ void __launch_bounds__(kMaxThreads, 1)
+score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages) {
   constexpr int HALVES = DI / 64;
-  constexpr int A_HALF = kTcTileBlocks * 128;
-  constexpr int A_STAGE = HALVES * A_HALF;
+  constexpr int A_STAGE = kTcTileBlocks * DI * 2;  // one tile of keys, tiled pages back to back
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base_u = (raw_u + 1023u) & ~1023u;
@@ -318,8 +353,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_consta
   const uint32_t b_half = a.npad * 128;
   const uint32_t b_slot = HALVES * b_half;
   const uint32_t b_u = a_u + S * A_STAGE;
-  float *ws = reinterpret_cast<float *>(base + S * A_STAGE + 2 * b_slot);  // 4 x kTcMaxGroup x 64 floats
-  const uint32_t bars = smem_u32(ws + 4 * kTcMaxGroup * 64);
+  float *ws = reinterpret_cast<float *>(base + S * A_STAGE + 2 * b_slot);  // kEpiFloats floats
+  const uint32_t bars = smem_u32(ws + kEpiFloats);
   // barrier addresses
   auto a_full = [&](int s) { return bars + 8u * s; };
   auto a_empty = [&](int s) { return bars + 8u * (kMaxStages + s); };
@@ -327,7 +362,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_consta
   auto b_empty = [&](int s) { return bars + 8u * (2 * kMaxStages + 2 + s); };
   auto t_full = [&](int s) { return bars + 8u * (2 * kMaxStages + 4 + s); };
   auto t_empty = [&](int s) { return bars + 8u * (2 * kMaxStages + 6 + s); };
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ws + 4 * kTcMaxGroup * 64 + 2 * (2 * kMaxStages + 8));
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ws + kEpiFloats + 2 * kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const Shape &sh = a.sh;
@@ -343,7 +378,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_consta
       mbar_init(b_full(s), 1);
       mbar_init(b_empty(s), 1);
       mbar_init(t_full(s), 1);
-      mbar_init(t_empty(s), 128);
+      mbar_init(t_empty(s), 32 * 4 * a.G);  // every epilogue thread
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -355,6 +390,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_consta
   const uint32_t tmem = *tmem_slot;
   const int bpp = 1 << a.bpp_log2;
   const int pages_in_tile = kTcTileBlocks >> a.bpp_log2;
+  const uint32_t page_bytes = static_cast<uint32_t>(bpp) * DI * 2;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -388,8 +424,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_consta
         }
         cur_g = w.g;
       }
-      if (cur.have && (cur.pg < 0 || cur.pg >= a.num_pages)) report(a.status, QSA_ERR_PAGE);
-      const unsigned have_mask = __ballot_sync(0xffffffffu, cur.have);
+      // a page id outside the pool is reported and not copied (its blocks score garbage)
+      const bool bad_page = cur.have && (cur.pg < 0 || cur.pg >= a.num_pages);
+      if (bad_page) report(a.status, QSA_ERR_PAGE);
+      const bool load = cur.have && !bad_page;
+      const unsigned have_mask = __ballot_sync(0xffffffffu, load);
       for (int it = 0; it < cur.nb; ++it, ++k) {
         const int s = k % S;
         if (k >= S && !mbar_wait_or_abort(a_empty(s), ((k / S) - 1) & 1, abort_flag, a.status)) {
@@ -399,14 +438,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_consta
         const unsigned mine = (pages_in_tile == 32 ? 0xffffffffu : ((1u << pages_in_tile) - 1u))
                               << (it * pages_in_tile);
         const int n_load = __popc(have_mask & mine);
-        if (lane == 0) mbar_arrive_expect_tx(a_full(s), static_cast<uint32_t>(n_load) * HALVES * bpp * 128);
+        if (lane == 0) mbar_arrive_expect_tx(a_full(s), static_cast<uint32_t>(n_load) * page_bytes);
         __syncwarp();
-        if (cur.have && ((mine >> lane) & 1u)) {
+        if (load && ((mine >> lane) & 1u)) {
           const int slot = lane - it * pages_in_tile;
-#pragma unroll
-          for (int hh = 0; hh < HALVES; ++hh)
-            tma_load_2d_hint(a_u + s * A_STAGE + hh * A_HALF + slot * bpp * 128, &tm_keys, a_full(s),
-                             hh * 64, cur.pg * bpp, stream_policy);
+          bulk_load_hint(a_u + s * A_STAGE + slot * page_bytes, a.keys + static_cast<size_t>(cur.pg) * bpp * DI,
+                         page_bytes, a_full(s), stream_policy);
         }
       }
       w = wn;
@@ -438,7 +475,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_consta
 #pragma unroll
         for (int kk = 0; kk < DI / 16; ++kk) {
           const int hh = kk >> 2, k4 = kk & 3;
-          const uint64_t ad = smem_desc_sw128(a_u + s * A_STAGE + hh * A_HALF + k4 * 32);
+          // K step kk: core matrices 2kk and 2kk+1 along K
+          const uint64_t ad = smem_desc_interleave(a_u + s * A_STAGE + kk * 256, 128, DI * 16);
           const uint64_t bd = smem_desc_sw128(b_u + bs * b_slot + hh * b_half + k4 * 32);
           tc_mma(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
         }
@@ -449,12 +487,15 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_consta
       if (lane == 0 && (w.left <= 0 || w.g != cur_g)) tc_commit(b_empty(bs));
     }
   } else {
-    // ---------------- epilogue (warps 2-5, TMEM lane quarter = warp % 4) ----------------
+    // ---------------- epilogue (warps 2 .. 2 + 4G) ----------------
+    // Warp 2 + e reads TMEM lane quarter q = warp % 4 (its own 32 lanes) and
+    // reduces row j = e / 4 of the group over all head columns of that row.
+    const int e = warp - 2;
     const int q = warp & 3;
+    const int j = e >> 2;  // < G: the block has 4G epilogue warps
     Walker w = walker_start(a, n_groups, lane);
-    const int chunks = a.hp >> 4;  // 16-column TMEM loads per row (<= 4)
-    // this warp's copy of the group's head weights: [G][64]
-    float *wq = ws + (warp - 2) * (kTcMaxGroup * 64);
+    const int n16 = a.hp >> 4;  // 16-column TMEM loads of the row (hp a multiple of 16, <= 64)
+    float *wrow = ws + e * kRowCols;  // this warp's row weights, zero beyond H_I
     int cur_g = -1, j0 = 0, g_rows = 0, row0 = 0, p0 = 0;
     for (int k = 0; w.left > 0; ++k) {
       const int buf = k & 1;
@@ -465,39 +506,41 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_keys, const __grid_consta
         row0 = i * a.R + j0;
         p0 = a.pos0[i];
         __syncwarp();
-        for (int c = lane; c < kTcMaxGroup * 64; c += 32) {
-          const int j = c >> 6, h = c & 63;
-          wq[c] = (j < g_rows && h < sh.h_idx) ? a.w[static_cast<size_t>(row0 + j) * sh.h_idx + h] : 0.f;
-        }
+        for (int c = lane; c < kRowCols; c += 32)
+          wrow[c] = (j < g_rows && c < sh.h_idx) ? a.w[static_cast<size_t>(row0 + j) * sh.h_idx + c] : 0.f;
         __syncwarp();
         cur_g = w.g;
       }
       if (!mbar_wait_or_abort(t_full(buf), (k >> 1) & 1, abort_flag, a.status)) break;
       tc_fence_after();
-      const int blk = w.t * kTcTileBlocks + q * 32 + lane;
-      const uint32_t lane_addr = tmem + buf * a.ncols + (static_cast<uint32_t>(q * 32) << 16);
-      for (int j = 0; j < a.G; ++j) {
-        float v[4][16];
+      const uint32_t lane_addr =
+          tmem + buf * a.ncols + (static_cast<uint32_t>(q * 32) << 16) + j * a.hp;
+      float v[kRowCols];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (c < chunks) tmem_ld16(lane_addr + j * a.hp + c * 16, v[c]);
-        tmem_ld_wait();
-        const float *wrow = wq + j * 64;  // zero beyond H_I
-        float acc = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (c < chunks) {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) acc += wrow[c * 16 + t] * fmaxf(v[c][t], 0.f);
-          }
-        }
-        if (j < g_rows) {
-          const int nb = (p0 + j0 + j + 1) >> sh.log2_ratio;  // blocks visible to row j
-          if (nb > sh.topk && blk < nb) a.scores[static_cast<size_t>(row0 + j) * a.ld + blk] = acc;
-        }
-      }
+      for (int c = 0; c < kRowCols / 16; ++c)
+        if (c < n16) tmem_ld16(lane_addr + c * 16, v + c * 16);
+      tmem_ld_wait();
+      // the row is in registers: hand the TMEM buffer back to the MMA warp
       tc_fence_before();
       mbar_arrive(t_empty(buf));
+      const float4 *w4 = reinterpret_cast<const float4 *>(wrow);
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < kRowCols / 8; ++c) {
+        if (c < 2 * n16) {
+          const float4 wa = w4[2 * c], wb = w4[2 * c + 1];
+          ffma2(acc[0], acc[1], wa.x, wa.y, fmaxf(v[8 * c], 0.f), fmaxf(v[8 * c + 1], 0.f));
+          ffma2(acc[2], acc[3], wa.z, wa.w, fmaxf(v[8 * c + 2], 0.f), fmaxf(v[8 * c + 3], 0.f));
+          ffma2(acc[4], acc[5], wb.x, wb.y, fmaxf(v[8 * c + 4], 0.f), fmaxf(v[8 * c + 5], 0.f));
+          ffma2(acc[6], acc[7], wb.z, wb.w, fmaxf(v[8 * c + 6], 0.f), fmaxf(v[8 * c + 7], 0.f));
+        }
+      }
+      const float sc = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+      if (j < g_rows) {
+        const int nb = (p0 + j0 + j + 1) >> sh.log2_ratio;  // blocks visible to row j
+        const int blk = w.t * kTcTileBlocks + q * 32 + lane;
+        if (nb > sh.topk && blk < nb) a.scores[static_cast<size_t>(row0 + j) * a.ld + blk] = sc;
+      }
       walker_next(w, a, n_groups);
     }
   }
@@ -575,24 +618,22 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   a.page_table = cv.page_table;
   a.max_pages = cv.max_pages;
   a.num_pages = cv.num_pages;
+  a.keys = cv.idxblk_pool;
   a.w = w;
   a.scores = scores;
   a.ld = ld;
   a.status = status;
 
-  CUtensorMap tm_keys, tm_q;
-  const int bpp = 1 << a.bpp_log2;
+  CUtensorMap tm_q;
   const long long total_rows = static_cast<long long>(n_seq) * R;
-  if (!encode_2d(&tm_keys, cv.idxblk_pool, sh.d_idx, static_cast<uint64_t>(cv.num_pages) * bpp, 64, bpp))
-    return cudaErrorInvalidValue;
   if (!encode_2d(&tm_q, q_idx, sh.d_idx, static_cast<uint64_t>(total_rows) * sh.h_idx, 64, a.npad))
     return cudaErrorInvalidValue;
 
   a.n_groups = n_seq * a.groups_per_seq;
   const int halves = sh.d_idx / 64;
-  const size_t a_stage = static_cast<size_t>(halves) * kTcTileBlocks * 128;
+  const size_t a_stage = static_cast<size_t>(kTcTileBlocks) * sh.d_idx * 2;
   const size_t b_slots = 2ull * halves * a.npad * 128;
-  const size_t fixed = 1024 + b_slots + 4 * kTcMaxGroup * 64 * 4 + 8 * (2 * kMaxStages + 8) + 16;
+  const size_t fixed = 1024 + b_slots + kEpiFloats * 4 + 8 * kNumBars + 16;
   const size_t smem_cap = 227 * 1024;
   int stages = static_cast<int>((smem_cap - fixed) / a_stage);
   if (stages > kMaxStages) stages = kMaxStages;
@@ -612,11 +653,12 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   int dev = 0, sms = 0, per_sm = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPThreads, smem)) != cudaSuccess)
+  const int threads = 64 + 128 * a.G;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem)) != cudaSuccess)
     return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   if (per_sm > max_ctas) per_sm = max_ctas;
-  return launch_kernel(pdl, kern, dim3(sms * per_sm), dim3(kPThreads), smem, st, tm_keys, tm_q, a, stages);
+  return launch_kernel(pdl, kern, dim3(sms * per_sm), dim3(threads), smem, st, tm_q, a, stages);
   return cudaGetLastError();
 }
 

@@ -174,7 +174,8 @@ class PagedCache:
         self.k_pool = torch.zeros(num_pages, P, cfg.n_kv_heads, cfg.head_dim, dtype=torch.bfloat16, device=device)
         self.v_pool = torch.zeros_like(self.k_pool)
         self.idxraw_pool = torch.zeros(num_pages, P, cfg.idx_dim, dtype=torch.bfloat16, device=device)
-        self.idxblk_pool = torch.zeros(num_pages, P // cfg.ratio, cfg.idx_dim, dtype=torch.bfloat16, device=device)
+        # block keys: P/ratio rows of idx_dim per page, stored tiled (see qsa.h)
+        self.idxblk_pool = torch.zeros(num_pages, (P // cfg.ratio) * cfg.idx_dim, dtype=torch.bfloat16, device=device)
         self.ingested = torch.zeros(self.n_slots, dtype=torch.int32, device=device)
 
     @property

@@ -26,6 +26,16 @@ def bf16_value(b: np.ndarray) -> np.ndarray:
     return O.bf16_bits_to_f64(b)
 
 
+def block_pool_index(bpp: int, d_idx: int) -> np.ndarray:
+    """[bpp, d_idx] element offsets of a block-pool page in the library's tiled
+    page layout (tiles of min(bpp, 8) rows x 8 values, row-group major, then
+    8-value chunk, row-major inside a tile), as the C ABI header documents."""
+    g = min(bpp, 8)
+    rr = np.arange(bpp)[:, None]
+    d = np.arange(d_idx)[None, :]
+    return ((rr // g) * (d_idx // 8) + d // 8) * (8 * g) + (rr % g) * 8 + d % 8
+
+
 class History:
     """Per-sequence record of which epoch wrote each position (positions
     re-appended after a rewind carry fresh random rows)."""
@@ -163,7 +173,7 @@ class GpuState:
         b = np.arange(n_blk)
         pages = pt[b // bpp]
         blk = self.cache.idxblk_pool.view(torch.int16).cpu().numpy().astype(np.uint16)
-        return blk[pages, b % bpp]
+        return blk[pages[:, None], block_pool_index(bpp, sh.idx_dim)[b % bpp]]
 
     def logical_rows(self, pool: torch.Tensor, s: int, positions: np.ndarray) -> np.ndarray:
         P = self.sh.page_size
