@@ -155,6 +155,12 @@ cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 bloc
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
+  // every kernel of the library asks for the largest shared-memory carveout, so an
+  // SM that runs one of them can take a CTA of the next without first draining
+  // to change its L1 / shared-memory split
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
