@@ -26,8 +26,10 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
               uint16_t *__restrict__ blk_pool, const int32_t *__restrict__ ingested,
               const uint16_t *__restrict__ k_new, const uint16_t *__restrict__ v_new,
               const uint16_t *__restrict__ idx_new, int32_t *status) {
-  pdl_trigger();  // the first kernel of the step: its successor may start its prologue
-  pdl_wait();     // the previous step's commit (ingested, pos0) when launched as a dependent
+  // the previous step's commit (ingested, pos0) when launched as a dependent; only
+  // then may the score kernel start: its prologue reads the positions
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x;
   const int s = seq_ids[i];
   const int p0 = pos0[i];

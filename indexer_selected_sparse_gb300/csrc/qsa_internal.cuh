@@ -130,13 +130,14 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 }
 
 // --- programmatic dependent launch ----------------------------------------
-// Inside the fused step every kernel after the first is launched with
-// programmatic stream serialization: it may start while its predecessor is
-// still draining, runs its independent prologue, and waits (griddepcontrol.wait)
-// before reading anything an earlier kernel of the step writes. A kernel lets
-// its successor launch only after its own wait has returned, so a kernel never
-// overlaps one that is two steps back. Outside a programmatic launch the wait
-// returns at once.
+// Inside the fused step every kernel is launched with programmatic stream
+// serialization: it may start while its predecessor is still draining, runs its
+// independent prologue, and waits (griddepcontrol.wait) before reading anything
+// its predecessor writes. A kernel lets its successor launch only after its own
+// wait has returned, so a prologue may read what the kernel two back wrote (the
+// score kernel's prologue reads the positions the previous step's merge
+// committed), and a kernel never overlaps one that is two back. Outside a
+// programmatic launch the wait returns at once.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
