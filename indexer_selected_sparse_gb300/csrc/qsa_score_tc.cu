@@ -304,6 +304,7 @@ __device__ __forceinline__ void walker_next(Walker &w, const TcArgs &a, int n_gr
 struct Batch {
   int nb = 0;        // tiles in the batch
   int row0 = 0;      // first row of the group
+  int nblk_old = 0;  // blocks of the sequence complete before this step's appends
   int pg = 0;        // this lane's page id
   bool have = false; // this lane's page holds a visible block
 };
@@ -312,7 +313,7 @@ struct Batch {
 // last row and its sequence's page-table row. Loaded once per group, so a new
 // batch of the same group issues its page-id load without waiting on others.
 struct GroupInfo {
-  int g = -1, row0 = 0, nblk_last = 0;
+  int g = -1, row0 = 0, nblk_last = 0, nblk_old = 0;
   const int32_t *ptab = nullptr;
 };
 
@@ -324,11 +325,13 @@ __device__ __forceinline__ Batch load_batch(const TcArgs &a, const Walker &w, Gr
     const int g_rows = min(a.G, a.R - j0);
     gi.row0 = i * a.R + j0;
     gi.nblk_last = (a.pos0[i] + j0 + g_rows) >> a.sh.log2_ratio;
+    gi.nblk_old = a.pos0[i] >> a.sh.log2_ratio;
     gi.ptab = a.page_table + static_cast<size_t>(a.seq_ids[i]) * a.max_pages;
     gi.g = w.g;
   }
   Batch b;
   b.row0 = gi.row0;
+  b.nblk_old = gi.nblk_old;
   b.nb = min(min(per_batch, w.tiles - w.t), w.left);
   const int pidx = w.t * pages_in_tile + lane;
   b.have = lane < b.nb * pages_in_tile && pidx * bpp < gi.nblk_last;
@@ -398,16 +401,17 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     // holds the page id of page L of the batch. The page ids of the next batch
     // are loaded before the current batch's copies are issued, and the group's
     // page-table row is cached, so no global-memory latency sits between two
-    // batches of a group.
+    // batches of a group. Tiles whose blocks were all complete before this step
+    // (pooled by earlier steps) need nothing from the append kernel: up to a
+    // ring's worth of them is issued before the dependency wait, so their HBM
+    // latency overlaps the append.
     Walker w = walker_start(a, n_groups, lane);
     const uint64_t stream_policy = l2_evict_first();
     const int per_batch = 32 / pages_in_tile;
     GroupInfo gi;
     Batch cur = load_batch(a, w, gi, lane, per_batch, pages_in_tile, bpp);
-    pdl_wait();  // the compressed keys come from the append kernel
-    pdl_trigger();
     int cur_g = -1, gseq = -1, k = 0;
-    bool ok = true;
+    bool ok = true, waited = false;
     while (ok && w.left > 0) {
       Walker wn = w;
       for (int it = 0; it < cur.nb; ++it) walker_next(wn, a, n_groups);
@@ -431,6 +435,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       const unsigned have_mask = __ballot_sync(0xffffffffu, load);
       for (int it = 0; it < cur.nb; ++it, ++k) {
         const int s = k % S;
+        if (!waited && (k >= S || (w.t + it + 1) * kTcTileBlocks > cur.nblk_old)) {
+          pdl_wait();  // blocks completed by this step come from the append kernel
+          pdl_trigger();
+          waited = true;
+        }
         if (k >= S && !mbar_wait_or_abort(a_empty(s), ((k / S) - 1) & 1, abort_flag, a.status)) {
           ok = false;
           break;
@@ -448,6 +457,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       }
       w = wn;
       cur = nxt;
+    }
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
