@@ -243,6 +243,34 @@ def attend_row(state: SeqState, pos: int, q_idx_bits, w, q_bits, topk: int) -> D
             "out": out, "out_bf16": f64_to_bf16_bits(out)}
 
 
+def attend_row_reused(state: SeqState, pos: int, sel, sel_pos: int, q_bits) -> Dict:
+    """Attention of the row at logical position pos with a block selection made
+    earlier, by the row at sel_pos <= pos ("Flash-Next support: vLLM vs Atlas",
+    (a) item 6, MTP: later draft steps reuse the step-0 selection while the side
+    caches keep updating; "Flash-Next support: llama.cpp vs Atlas", (a) item 3:
+    a shared indexer layer reuses the previous full layer's top-k).
+
+    Reading (the pages give no token-set rule for reuse): the token set is the
+    reused blocks plus every token from the selection's complete-block boundary
+    up to the row, sel x ratio  U  [((sel_pos + 1) // ratio) * ratio, pos + 1);
+    the tail stays always visible, including blocks completed since the
+    selection was made. With sel_pos == pos this is attend_row's token set."""
+    r = state.ratio
+    visible = pos + 1
+    if visible > state.ingested:
+        raise DesyncError(f"row at pos {pos} but only {state.ingested} ingested")
+    if not 0 <= sel_pos <= pos:
+        raise ValueError(f"selection position {sel_pos} is not in [0, {pos}]")
+    n_blk_sel = (sel_pos + 1) // r
+    sel = np.asarray(sel, np.int64)
+    if sel.size and (sel.min() < 0 or sel.max() >= n_blk_sel):
+        raise ValueError("reused selection names a block that was not complete at sel_pos")
+    toks = token_set(sel, n_blk_sel, visible, r)
+    out = gqa_attention(q_bits, state.K[toks], state.V[toks])
+    return {"n_blk_sel": n_blk_sel, "sel": sel, "tokens": toks, "out": out,
+            "out_bf16": f64_to_bf16_bits(out)}
+
+
 def padded_selection(sel, topk: int) -> np.ndarray:
     """Selection as a fixed-width row: ascending ids, -1 padded to K."""
     row = np.full(topk, -1, np.int64)

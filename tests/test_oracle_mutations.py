@@ -90,6 +90,17 @@ def visible_excludes_own_token(state, pos, q_idx_bits, w, q_bits, topk):
             "out_bf16": O.f64_to_bf16_bits(out)}
 
 
+def reuse_tail_from_current_blocks(state, pos, sel, sel_pos, q_bits):
+    # bug: the tail starts at the row's own block boundary, so the tokens of
+    # blocks completed since the selection was made are dropped
+    r = state.ratio
+    visible = pos + 1
+    toks = O.token_set(np.asarray(sel, np.int64), visible // r, visible, r)
+    out = O.gqa_attention(q_bits, state.K[toks], state.V[toks])
+    return {"n_blk_sel": visible // r, "sel": sel, "tokens": toks, "out": out,
+            "out_bf16": O.f64_to_bf16_bits(out)}
+
+
 class StickyRewind(O.SeqState):
     def rewind(self, n_drop):
         if n_drop < 0 or n_drop > self.ingested:
@@ -109,6 +120,7 @@ MUTATIONS = [
     ("gqa_attention", attention_scale_1_over_d, [P.test_worked_example_attention]),
     ("attend_row", visible_excludes_own_token, [P.test_dense_identity_at_and_below_inert_bound]),
     ("SeqState", StickyRewind, [P.test_counter_discipline]),
+    ("attend_row_reused", reuse_tail_from_current_blocks, [P.test_reused_dense_selection_stays_exactly_dense]),
 ]
 
 

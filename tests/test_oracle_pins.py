@@ -326,6 +326,56 @@ def test_ablation_of_unselected_tokens():
     assert not np.array_equal(res3["out"], res["out"])
 
 
+def test_reused_selection_at_its_own_position_is_attend_row():
+    # a shared indexer layer reuses the top-k of the full layer at the same position
+    rng = np.random.default_rng(29)
+    ratio, topk = 4, 4
+    st = make_state(rng, 61, ratio)
+    for pos in (60, 41, 18):
+        q = bf16(rng.standard_normal((4, 16)))
+        qi = bf16(rng.integers(-8, 9, size=(3, 8))); w = np.array([1.0, 0.5, 2.0])
+        ref = O.attend_row(st, pos, qi, w, q, topk)
+        got = O.attend_row_reused(st, pos, ref["sel"], pos, q)
+        assert np.array_equal(got["tokens"], ref["tokens"])
+        assert np.array_equal(got["out_bf16"], ref["out_bf16"])
+
+
+def test_reused_dense_selection_stays_exactly_dense():
+    # a selection made at or below the inert bound holds every block; reused at a
+    # later position (past the bound, blocks completed since) it must still
+    # cover every visible token: exactly dense attention
+    rng = np.random.default_rng(31)
+    ratio, budget = 4, 32
+    bound = budget + ratio - 1
+    st = make_state(rng, bound + 12, ratio)
+    qi = bf16(rng.integers(-8, 9, size=(3, 8))); w = np.ones(3)
+    for sel_V in (bound, bound - 2, 9):
+        sel = O.attend_row(st, sel_V - 1, qi, w, bf16(rng.standard_normal((4, 16))), budget // ratio)["sel"]
+        for V in (sel_V, sel_V + 1, sel_V + 3, sel_V + 4, bound + 12):
+            q = bf16(rng.standard_normal((4, 16)))
+            got = O.attend_row_reused(st, V - 1, sel, sel_V - 1, q)
+            assert got["tokens"].tolist() == list(range(V))
+            dense = O.dense_attention(q, st.K[:V], st.V[:V], 2)
+            assert np.max(np.abs(got["out"] - dense)) <= 1e-12
+
+
+def test_reused_sparse_selection_token_set():
+    rng = np.random.default_rng(37)
+    ratio, topk = 4, 4
+    st = make_state(rng, 80, ratio)
+    qi = bf16(rng.integers(-8, 9, size=(3, 8))); w = np.array([1.0, 0.5, 2.0])
+    q = bf16(rng.standard_normal((4, 16)))
+    ref = O.attend_row(st, 60, qi, w, q, topk)       # 61 visible: 15 blocks, tail {60}
+    for pos in (60, 61, 62, 63, 64, 70, 79):
+        got = O.attend_row_reused(st, pos, ref["sel"], 60, q)
+        body = [b * ratio + j for b in ref["sel"] for j in range(ratio)]
+        assert got["tokens"].tolist() == body + list(range(60, pos + 1))
+    with pytest.raises(ValueError):
+        O.attend_row_reused(st, 59, ref["sel"], 60, q)       # selection from the future
+    with pytest.raises(O.DesyncError):
+        O.attend_row_reused(st, 80, ref["sel"], 60, q)       # row not ingested
+
+
 # ---------------------------------------------------------------------------
 # State: append / rewind / chunking / counters
 # ---------------------------------------------------------------------------
