@@ -57,6 +57,8 @@ def parse():
                     help="comma list of legs to run: decode (the headline), prefill (chunked-prefill "
                          "index scoring against the bf16 tensor peak, and the fused prefill step)")
     ap.add_argument("--prefill-steps", type=int, default=10)
+    ap.add_argument("--reuse-steps", type=int, default=300,
+                    help="decode steps with a reused selection (MTP draft steps); 0 skips the leg")
     ap.add_argument("--prefill-warmup", type=int, default=3)
     return ap.parse_args()
 
@@ -202,7 +204,7 @@ def run_gpu(args):
     B = wl.n_seq
     K, W = args.steps, args.warmup
     total_steps = W + K + args.breakdown_steps + args.e2e_steps + 4
-    adv_per_batch = math.ceil((W + K + min(K, 600) + args.e2e_steps + 4) / NB)
+    adv_per_batch = math.ceil((W + K + min(K, 600) + args.e2e_steps + 4) / NB) + (62 if args.reuse_steps > 0 else 0)
     # center the prefixes of the main timed region on 32768
     start = wl.prefixes[0] - W // NB - K // (2 * NB)
     start = max(start, 8)
@@ -359,7 +361,69 @@ def run_gpu(args):
     out = make_line(wl, sh, B, K, W, world, value, ms, visibles, step_bytes, step_gbs, hbm_gbs, NB,
                     roofline, stage_ms, stage_bytes, stage_flops, out_e2e, clocks, setup_s)
     out["ms_per_step_one_graph_per_step"] = round(ms_single, 5)
+    if args.reuse_steps > 0:
+        out["reuse"] = run_reuse(args, Q, torch, cfg, sh, cache, batches, ws, status, stream, NB, B, hbm_gbs)
     return out, rank, world
+
+
+def run_reuse(args, Q, torch, cfg, sh, cache, batches, ws, status, stream, NB, B, hbm_gbs):
+    """Decode steps that reuse the step-0 selection (MTP draft steps): append,
+    then attention over the reused blocks plus the tail since; no scoring or
+    selection. Each batch selects once (untimed), then takes up to 60 reuse
+    steps: the token set grows by one per step and must stay within the split
+    plan (qsa_max_attend_tokens)."""
+    dev = cache.k_pool.device
+    per_batch = min(60, max(1, args.reuse_steps // NB))
+    limit = Q.qsa_max_attend_tokens(cfg) - sh.topk * sh.ratio - sh.ratio
+    per_batch = max(1, min(per_batch, limit))
+    torch.cuda.synchronize()
+    cur = [int(bt["pos0"][0].item()) for bt in batches]  # every sequence of a batch is at one position
+    sels, nsels, selpos = [], [], []
+    for b, bt in enumerate(batches):
+        sel = torch.empty(B, cfg.topk, dtype=torch.int32, device=dev)
+        nsel = torch.empty(B, dtype=torch.int32, device=dev)
+        selpos.append(torch.full((B,), cur[b], dtype=torch.int32, device=dev))
+        rows = Q.Rows(bt["ids"], bt["pos0"], 1, advance=True)
+        with torch.cuda.stream(stream):
+            Q.qsa_decode(cfg, rows, cache, bt["k"], bt["v"], bt["idx"], bt["q_idx"], bt["w"], bt["q"],
+                         bt["out"], ws, status, sel_out=sel, n_sel_out=nsel, stream=stream)
+        sels.append(sel); nsels.append(nsel)
+    rot = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(rot, stream=stream):
+        for b, bt in enumerate(batches):
+            Q.qsa_decode_reuse(cfg, Q.Rows(bt["ids"], bt["pos0"], 1, advance=True), cache, bt["k"], bt["v"],
+                               bt["idx"], bt["q"], sels[b], nsels[b], selpos[b], bt["out"], ws, status,
+                               stream=stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        rot.replay()  # warm-up rotation
+        e0.record(stream)
+        for _ in range(per_batch - 1):
+            rot.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st == 0, f"device status {st}: {Q.qsa_strerror(st)}"
+    steps = (per_batch - 1) * NB
+    ms = e0.elapsed_time(e1) / steps
+    # algorithmic bytes: the reused token set (K + V of every KV head), q, o, appends
+    # timed rows: batch b at positions cur[b] + 2 .. cur[b] + per_batch
+    tot = 0
+    for r in range(per_batch - 1):
+        for b in range(NB):
+            V = cur[b] + 2 + r + 1
+            tail = V - ((cur[b] + 1) // sh.ratio) * sh.ratio
+            n_tok = sh.topk * sh.ratio + tail
+            tot += B * (n_tok * sh.n_kv_heads * sh.head_dim * 4 + 2 * sh.n_q_heads * sh.head_dim * 2
+                        + (2 * sh.n_kv_heads * sh.head_dim + sh.idx_dim) * 2)
+    gbs = tot / steps / (ms * 1e-3) / 1e9
+    return {"what": "decode steps reusing the step-0 selection (MTP draft steps): append + attention "
+                    "over the reused blocks and the tail since, no scoring or selection",
+            "steps": steps, "ms_per_step": round(ms, 5), "rows_per_s": round(B / (ms * 1e-3), 1),
+            "achieved_gbs": round(gbs, 1), "hbm_roofline_frac": round(gbs / hbm_gbs, 4),
+            "bytes": "reused token set K+V, q, o, appended rows"}
 
 
 def stage_breakdown(args, Q, torch, cfg, sh, cache, batches, ws, status, stream, hpos, NB, B, hbm_gbs,

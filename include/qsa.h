@@ -70,8 +70,11 @@ typedef enum qsa_status {
   QSA_ERR_DESYNC = 7,       /* device: append position != ingested counter */
   QSA_ERR_PAGE = 8,         /* device: page id outside [0, num_pages) */
   QSA_ERR_REWIND = 9,       /* device: rewind by more than was ingested */
-  QSA_ERR_TIMEOUT = 10      /* device: an internal wait of a kernel expired (1 s);
+  QSA_ERR_TIMEOUT = 10,     /* device: an internal wait of a kernel expired (1 s);
                                the kernel released its resources and returned */
+  QSA_ERR_REUSE = 11        /* device: a reused selection's position is not in
+                               [0, row position], or its token set exceeds
+                               qsa_max_attend_tokens() */
 } qsa_status;
 
 /* Shape of the method. Supported set (checked by qsa_config_check):
@@ -243,6 +246,44 @@ int qsa_decode(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cac
                const qsa_bf16 *q_idx, const float *w, const qsa_bf16 *q,
                int32_t *sel_out, int32_t *n_sel_out, qsa_bf16 *out,
                void *ws, size_t ws_bytes, int32_t *status, cudaStream_t stream);
+
+/* Tokens one row's attention can take: the split plan covers
+ * ceil((budget + ratio - 1) / 112) splits of 112 tokens. A reused selection
+ * (below) may be used while its token set stays within this count. Returns 0
+ * on an invalid configuration. */
+int qsa_max_attend_tokens(const qsa_config *cfg);
+
+/* Gather attention with a reused selection ("Agentic shootout", "Flash-Next
+ * support: vLLM vs Atlas", (a) item 6: with MTP, later draft steps reuse the
+ * step-0 selection while the side caches keep updating; "Flash-Next support:
+ * llama.cpp vs Atlas", (a) item 3: a shared indexer layer reuses the previous
+ * full layer's top-k). sel / n_sel were selected by the row at position
+ * sel_pos[row] <= the row's position (for a shared layer, the same position).
+ * The row attends over the reused blocks plus every token from that
+ * position's block boundary to the row:
+ *     T = {b*ratio + j : b in sel, j < ratio}  U  [((sel_pos+1)/ratio)*ratio, V).
+ * Nothing is scored or selected. |T| must stay <= qsa_max_attend_tokens(),
+ * else QSA_ERR_REUSE is recorded (as for sel_pos outside [0, position]).
+ *   sel_pos  device [rows] int32
+ *   other arguments as qsa_gather_attn */
+int qsa_gather_attn_reuse(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
+                          const qsa_bf16 *q, const int32_t *sel, const int32_t *n_sel,
+                          const int32_t *sel_pos, qsa_bf16 *out, void *ws, size_t ws_bytes,
+                          int32_t *status, cudaStream_t stream);
+
+/* The fused step with a reused selection: qsa_append (the side caches keep
+ * updating: raw keys, pooled blocks, K/V, counters), then
+ * qsa_gather_attn_reuse for every appended row, then the counter commit.
+ * Skips index scoring and top-K selection. No host synchronisation, no
+ * allocation; capturable in a CUDA graph. Arguments as qsa_decode without the
+ * indexer query and weights, plus the reused selection (sel, n_sel, sel_pos;
+ * device [rows, K], [rows], [rows] int32). ws_bytes >= qsa_workspace_bytes(cfg,
+ * rows, max_pages*P/ratio). */
+int qsa_decode_reuse(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
+                     const qsa_bf16 *k_new, const qsa_bf16 *v_new, const qsa_bf16 *idx_k_new,
+                     const qsa_bf16 *q, const int32_t *sel, const int32_t *n_sel,
+                     const int32_t *sel_pos, qsa_bf16 *out, void *ws, size_t ws_bytes,
+                     int32_t *status, cudaStream_t stream);
 
 /* Size of the fixed scratch array behind qsa_gather_attn_static. */
 #define QSA_STATIC_SCRATCH_BYTES (32u << 20)

@@ -157,11 +157,17 @@ const char *qsa_strerror(int status) {
     case QSA_ERR_PAGE: return "page id outside the pool";
     case QSA_ERR_REWIND: return "rewind by more tokens than were ingested";
     case QSA_ERR_TIMEOUT: return "an internal wait of a kernel expired";
+    case QSA_ERR_REUSE: return "reused selection: position outside [0, row position] or token set beyond qsa_max_attend_tokens()";
     default: return "unknown status";
   }
 }
 
 int qsa_config_check(const qsa_config *cfg) { return check_cfg(cfg); }
+
+int qsa_max_attend_tokens(const qsa_config *cfg) {
+  if (check_cfg(cfg) != QSA_OK) return 0;
+  return attn_max_tokens(make_shape(cfg));
+}
 
 size_t qsa_workspace_bytes(const qsa_config *cfg, int max_rows, int max_blocks_per_row) {
   if (check_cfg(cfg) != QSA_OK || max_rows < 0 || max_blocks_per_row < 0) return 0;
@@ -309,6 +315,66 @@ int qsa_decode(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cac
   if (e == cudaSuccess)
     e = launch_attn(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, q, sel, n_sel, out,
                     base + L.partials, status, true, commit, stream);
+  return cuda_status(e);
+}
+
+int qsa_gather_attn_reuse(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
+                          const qsa_bf16 *q, const int32_t *sel, const int32_t *n_sel,
+                          const int32_t *sel_pos, qsa_bf16 *out, void *ws, size_t ws_bytes,
+                          int32_t *status, cudaStream_t stream) {
+  int rc;
+  if ((rc = check_cfg(cfg)) != QSA_OK) return rc;
+  if ((rc = check_rows(rows)) != QSA_OK) return rc;
+  if ((rc = check_cache(cache, true, false)) != QSA_OK) return rc;
+  const int n_rows = rows->n_seq * rows->rows_per_seq;
+  if (n_rows == 0) return QSA_OK;
+  if (!q || !sel || !n_sel || !sel_pos || !out || !ws || !aligned16(q) || !aligned16(out) || !aligned16(ws))
+    return QSA_ERR_INVALID_ARG;
+  const Shape sh = make_shape(cfg);
+  if (ws_bytes < attn_partial_bytes(sh, n_rows)) return QSA_ERR_WORKSPACE;
+  return cuda_status(launch_attn(sh, rows->n_seq, rows->rows_per_seq, rows->seq_ids, rows->pos0,
+                                 view(cache), q, sel, n_sel, out, ws, status, false, CommitArgs{},
+                                 stream, sel_pos));
+}
+
+int qsa_decode_reuse(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
+                     const qsa_bf16 *k_new, const qsa_bf16 *v_new, const qsa_bf16 *idx_k_new,
+                     const qsa_bf16 *q, const int32_t *sel, const int32_t *n_sel,
+                     const int32_t *sel_pos, qsa_bf16 *out, void *ws, size_t ws_bytes,
+                     int32_t *status, cudaStream_t stream) {
+  int rc;
+  if ((rc = check_cfg(cfg)) != QSA_OK) return rc;
+  if ((rc = check_rows(rows)) != QSA_OK) return rc;
+  if ((rc = check_cache(cache, true, true)) != QSA_OK) return rc;
+  if (!cache->ingested || !status) return QSA_ERR_INVALID_ARG;
+  const int n_rows = rows->n_seq * rows->rows_per_seq;
+  if (n_rows == 0) return QSA_OK;
+  if (!k_new || !v_new || !idx_k_new || !q || !sel || !n_sel || !sel_pos || !out || !ws)
+    return QSA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(idx_k_new) || !aligned16(q) ||
+      !aligned16(out) || !aligned16(ws))
+    return QSA_ERR_INVALID_ARG;
+  if ((rc = host_capacity_check(rows, cache, cfg->page_size)) != QSA_OK) return rc;
+  const Shape sh = make_shape(cfg);
+  const int cap_tokens = cache->max_pages * cfg->page_size;
+  const WsLayout L = ws_layout(sh, n_rows, ld_for(cap_tokens / cfg->ratio));
+  if (ws_bytes < L.total) return QSA_ERR_WORKSPACE;
+  const int R = rows->rows_per_seq;
+  cudaError_t e = launch_append(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cache->page_table,
+                                cache->max_pages, cache->num_pages, cache->k_pool, cache->v_pool,
+                                cache->idxraw_pool, cache->idxblk_pool, cache->ingested, k_new,
+                                v_new, idx_k_new, status, true, stream);
+  CommitArgs commit;
+  commit.n_seq = rows->n_seq;
+  commit.R = R;
+  commit.capacity = cap_tokens;
+  commit.advance = rows->advance;
+  commit.seq_ids = rows->seq_ids;
+  commit.pos0 = rows->pos0;
+  commit.ingested = cache->ingested;
+  if (e == cudaSuccess)
+    e = launch_attn(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, view(cache), q, sel, n_sel, out,
+                    static_cast<uint8_t *>(ws) + L.partials, status, true, commit, stream, sel_pos);
   return cuda_status(e);
 }
 

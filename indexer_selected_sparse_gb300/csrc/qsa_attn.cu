@@ -69,7 +69,7 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
             const int32_t *__restrict__ pos0, CacheView cv, const uint16_t *__restrict__ q,
             const int32_t *__restrict__ sel, const int32_t *__restrict__ n_sel_arr,
             float *__restrict__ part_m, float *__restrict__ part_l, float *__restrict__ part_acc,
-            int32_t *status) {
+            int32_t *status, const int32_t *__restrict__ sel_pos) {
   using G = AttnGeom<HKV>;
   static_assert(kSplitSlots <= kAttnThreads, "one slot-table entry per thread and unit");
   extern __shared__ __align__(128) uint8_t smem[];
@@ -146,15 +146,34 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
   pdl_wait();  // sel / n_sel come from the select kernel
   pdl_trigger();
 
-  // ---- the units' slot ranges (the selected count comes from the select kernel)
+  // ---- the units' slot ranges (the selected count comes from the select kernel).
+  // A reused selection (sel_pos given) was made by the row at sel_pos[row]: its
+  // blocks are complete at that position, and the tail runs from that block
+  // boundary to the row ("Flash-Next support: vLLM vs Atlas", (a) item 6, MTP
+  // skip_topk; "Flash-Next support: llama.cpp vs Atlas", (a) item 3, shared
+  // indexer layers).
   if (tid < nu) {
     AttnUnit &U = s_unit[tid];
-    const bool row_ok = U.n_blk >= 0;
-    const int n_blk = row_ok ? U.n_blk : 0;
+    bool row_ok = U.n_blk >= 0;
+    int n_blk = row_ok ? U.n_blk : 0;
+    if (row_ok && sel_pos) {
+      const int ps = sel_pos[U.row];
+      if (ps < 0 || ps >= U.visible) {
+        if (U.sp == 0) report(status, QSA_ERR_REUSE);
+        row_ok = false;
+        n_blk = 0;
+      } else {
+        n_blk = (ps + 1) >> sh.log2_ratio;
+      }
+    }
     const int n_sel = row_ok ? min(max(n_sel_arr[U.row], 0), min(n_blk, sh.topk)) : 0;
     U.n_body = n_sel * r;
     U.tail0 = n_blk * r;
-    const int n_slots = row_ok ? U.n_body + (U.visible - U.tail0) : 0;
+    int n_slots = row_ok ? U.n_body + (U.visible - U.tail0) : 0;
+    if (n_slots > n_split * split_len) {  // a reused selection too old for the split plan
+      if (U.sp == 0) report(status, QSA_ERR_REUSE);
+      n_slots = n_split * split_len;
+    }
     U.slot_lo = min(n_slots, U.sp * split_len);  // fixed cut: independent of the batch
     U.slot_hi = min(n_slots, U.slot_lo + split_len);
     U.n_chunks = (U.slot_hi - U.slot_lo + G::kChunk - 1) / G::kChunk;
@@ -531,7 +550,8 @@ template <int HKV>
 cudaError_t launch_attn_t(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                           const int32_t *pos0, const CacheView &cv, const uint16_t *q,
                           const int32_t *sel, const int32_t *n_sel, uint16_t *out, void *partials,
-                          int32_t *status, bool pdl, const CommitArgs &commit, cudaStream_t st) {
+                          int32_t *status, bool pdl, const CommitArgs &commit, cudaStream_t st,
+                          const int32_t *sel_pos) {
   const int rows = n_seq * R;
   const SplitPlan pl = plan_splits(sh, rows);
   const size_t n_part = static_cast<size_t>(rows) * pl.n_split * sh.hq;
@@ -555,7 +575,7 @@ cudaError_t launch_attn_t(const Shape &sh, int n_seq, int R, const int32_t *seq_
   if (n_units > 0x7fffffff) return cudaErrorInvalidValue;
   e = launch_kernel(pdl, kern, dim3(static_cast<unsigned>(grid)), dim3(kAttnThreads), smem, st, sh, R,
                     static_cast<int>(n_units), pl.n_split, pl.split_len, seq_ids, pos0, cv, q, sel, n_sel, pm,
-                    pl_, pa, status);
+                    pl_, pa, status, sel_pos);
   if (e != cudaSuccess) return e;
   return launch_kernel(pdl, merge_kernel, dim3(rows, sh.hkv), dim3(kMergeThreads), 0, st, sh.hq, sh.hkv,
                        pl.n_split, static_cast<const float *>(pm), static_cast<const float *>(pl_),
@@ -566,6 +586,11 @@ cudaError_t launch_attn_t(const Shape &sh, int n_seq, int R, const int32_t *seq_
 
 int attn_splits(const Shape &sh, int rows) { return plan_splits(sh, rows).n_split; }
 
+int attn_max_tokens(const Shape &sh) {
+  const SplitPlan pl = plan_splits(sh, 1);
+  return pl.n_split * pl.split_len;
+}
+
 size_t attn_partial_bytes(const Shape &sh, int rows) {
   // split partials (m, l, acc) of every row
   const size_t parts = static_cast<size_t>(rows) * plan_splits(sh, rows).n_split;
@@ -575,12 +600,13 @@ size_t attn_partial_bytes(const Shape &sh, int rows) {
 cudaError_t launch_attn(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                         const int32_t *pos0, const CacheView &cv, const uint16_t *q,
                         const int32_t *sel, const int32_t *n_sel, uint16_t *out, void *partials,
-                        int32_t *status, bool pdl, const CommitArgs &commit, cudaStream_t st) {
+                        int32_t *status, bool pdl, const CommitArgs &commit, cudaStream_t st,
+                        const int32_t *sel_pos) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
   switch (sh.hkv) {
-    case 1: return launch_attn_t<1>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st);
-    case 2: return launch_attn_t<2>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st);
-    case 4: return launch_attn_t<4>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st);
+    case 1: return launch_attn_t<1>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st, sel_pos);
+    case 2: return launch_attn_t<2>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st, sel_pos);
+    case 4: return launch_attn_t<4>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st, sel_pos);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -204,9 +204,14 @@ struct CommitArgs {
   int32_t *pos0 = nullptr;
   int32_t *ingested = nullptr;
 };
+// sel_pos (optional, device [rows]): the selection is reused from the row at that
+// position (its tail starts at that position's block boundary)
 cudaError_t launch_attn(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                         const int32_t *pos0, const CacheView &cv, const uint16_t *q,
                         const int32_t *sel, const int32_t *n_sel, uint16_t *out, void *partials,
-                        int32_t *status, bool pdl, const CommitArgs &commit, cudaStream_t st);
+                        int32_t *status, bool pdl, const CommitArgs &commit, cudaStream_t st,
+                        const int32_t *sel_pos = nullptr);
+// tokens a row's attention can take (splits x split length)
+int attn_max_tokens(const Shape &sh);
 
 }  // namespace qsa

@@ -31,10 +31,12 @@ QSA_ERR_DESYNC = 7
 QSA_ERR_PAGE = 8
 QSA_ERR_REWIND = 9
 QSA_ERR_TIMEOUT = 10
+QSA_ERR_REUSE = 11
 
 EXPORTED = ("qsa_strerror", "qsa_config_check", "qsa_workspace_bytes", "qsa_append",
             "qsa_rewind", "qsa_index_score", "qsa_topk_select", "qsa_gather_attn", "qsa_decode",
-            "qsa_gather_attn_static")
+            "qsa_gather_attn_static", "qsa_max_attend_tokens", "qsa_gather_attn_reuse",
+            "qsa_decode_reuse")
 QSA_STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -94,6 +96,13 @@ LIB.qsa_gather_attn.restype = _I
 LIB.qsa_gather_attn.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 LIB.qsa_gather_attn_static.restype = _I
 LIB.qsa_gather_attn_static.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P]
+LIB.qsa_max_attend_tokens.restype = _I
+LIB.qsa_max_attend_tokens.argtypes = [_CFG]
+LIB.qsa_gather_attn_reuse.restype = _I
+LIB.qsa_gather_attn_reuse.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+LIB.qsa_decode_reuse.restype = _I
+LIB.qsa_decode_reuse.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                 _P, _P]
 LIB.qsa_decode.restype = _I
 LIB.qsa_decode.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                            ctypes.c_size_t, _P, _P]
@@ -290,6 +299,36 @@ def qsa_decode(cfg: Config, rows: Rows, cache: PagedCache, k_new, v_new, idx_k_n
                         _ptr(out, torch.bfloat16), _ptr(ws), ws.numel() * ws.element_size(),
                         _ptr(status, torch.int32), _stream(stream))
     _check(rc, "qsa_decode", f"capacity {cache.capacity} tokens per sequence" if rc == QSA_ERR_CAPACITY else "")
+
+
+def qsa_max_attend_tokens(cfg: Config) -> int:
+    return LIB.qsa_max_attend_tokens(ctypes.byref(cfg.c()))
+
+
+def qsa_gather_attn_reuse(cfg: Config, rows: Rows, cache: PagedCache, q, sel, n_sel, sel_pos, out, ws,
+                          status=None, stream=None) -> None:
+    """Gather attention with a selection made earlier by the row at sel_pos
+    (MTP draft steps, shared indexer layers): reused blocks plus every token
+    from that position's block boundary to the row."""
+    rc = LIB.qsa_gather_attn_reuse(ctypes.byref(cfg.c()), ctypes.byref(rows.c()), ctypes.byref(cache.c()),
+                                   _ptr(q, torch.bfloat16), _ptr(sel, torch.int32), _ptr(n_sel, torch.int32),
+                                   _ptr(sel_pos, torch.int32), _ptr(out, torch.bfloat16), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _ptr(status, torch.int32), _stream(stream))
+    _check(rc, "qsa_gather_attn_reuse")
+
+
+def qsa_decode_reuse(cfg: Config, rows: Rows, cache: PagedCache, k_new, v_new, idx_k_new, q, sel, n_sel,
+                     sel_pos, out, ws, status, stream=None) -> None:
+    """The fused step with a reused selection: append (side caches keep
+    updating), then attention over the reused token set; no scoring or
+    selection."""
+    rc = LIB.qsa_decode_reuse(ctypes.byref(cfg.c()), ctypes.byref(rows.c()), ctypes.byref(cache.c()),
+                              _ptr(k_new, torch.bfloat16), _ptr(v_new, torch.bfloat16),
+                              _ptr(idx_k_new, torch.bfloat16), _ptr(q, torch.bfloat16),
+                              _ptr(sel, torch.int32), _ptr(n_sel, torch.int32), _ptr(sel_pos, torch.int32),
+                              _ptr(out, torch.bfloat16), _ptr(ws), ws.numel() * ws.element_size(),
+                              _ptr(status, torch.int32), _stream(stream))
+    _check(rc, "qsa_decode_reuse", f"capacity {cache.capacity} tokens per sequence" if rc == QSA_ERR_CAPACITY else "")
 
 
 def workspace(cfg: Config, max_rows: int, max_blocks_per_row: int, device="cuda") -> torch.Tensor:
