@@ -104,6 +104,70 @@ def pool_block(raw_bits) -> np.ndarray:
     return f64_to_bf16_bits(raw.mean(axis=0))
 
 
+# ---------------------------------------------------------------------------
+# Pre-indexer ("Agentic shootout", "Flash-Next support: vLLM vs Atlas", (a)
+# item 6: the indexer normalises its q/k heads with Gemma RMSNorm and applies
+# the same RoPE as main attention; a compressed key is mean-pool, then Gemma
+# RMSNorm, then RoPE at the group's first position. The report on the fused
+# pre-indexer kernel adds: RMSNorm scales by weight + 1 with fp32 accumulation,
+# NeoX RoPE, head_dim 128 with rotary 64.)
+# ---------------------------------------------------------------------------
+
+
+class PreIndexer:
+    """Parameters of the pre-indexer. The pages leave epsilon and the RoPE base
+    open: both are inputs. gamma_q / gamma_k: per-dimension gains (the norm
+    multiplies by 1 + gamma). rotary_dim: leading dimensions rotated (NeoX:
+    dimension i pairs with i + rotary_dim / 2); 0 disables RoPE."""
+
+    def __init__(self, gamma_q, gamma_k, eps: float, theta: float, rotary_dim: int):
+        self.gamma_q = np.asarray(gamma_q, np.float64)
+        self.gamma_k = np.asarray(gamma_k, np.float64)
+        self.eps = float(eps)
+        self.theta = float(theta)
+        self.rotary_dim = int(rotary_dim)
+
+
+def gemma_rmsnorm(x, gamma, eps: float) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) * (1 + gamma), over the last axis, fp64."""
+    x = np.asarray(x, np.float64)
+    rms = np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return x / rms * (1.0 + np.asarray(gamma, np.float64))
+
+
+def rope_neox(x, pos, rotary_dim: int, theta: float) -> np.ndarray:
+    """NeoX rotary embedding at position pos over the last axis: for
+    i < rotary_dim/2 the pair (x_i, x_{i+rotary_dim/2}) is rotated by the angle
+    pos * theta^(-2i/rotary_dim); dimensions >= rotary_dim are unchanged."""
+    x = np.array(x, np.float64)
+    if rotary_dim == 0:
+        return x
+    half = rotary_dim // 2
+    i = np.arange(half, dtype=np.float64)
+    ang = float(pos) * theta ** (-2.0 * i / rotary_dim)
+    c, s = np.cos(ang), np.sin(ang)
+    x1 = x[..., :half].copy()
+    x2 = x[..., half:rotary_dim].copy()
+    x[..., :half] = x1 * c - x2 * s
+    x[..., half:rotary_dim] = x2 * c + x1 * s
+    return x
+
+
+def pre_index_query(q_bits, pos: int, pre: PreIndexer) -> np.ndarray:
+    """Index query heads [H_I, d_I] of the row at pos: Gemma RMSNorm per head,
+    then RoPE at the row's position; bf16 bits."""
+    q = bf16_bits_to_f64(q_bits)
+    return f64_to_bf16_bits(rope_neox(gemma_rmsnorm(q, pre.gamma_q, pre.eps), pos, pre.rotary_dim, pre.theta))
+
+
+def pool_block_pre(raw_bits, first_pos: int, pre: PreIndexer) -> np.ndarray:
+    """Compressed key of the block whose first token is at first_pos: the mean
+    of its raw index keys, then Gemma RMSNorm, then RoPE at first_pos; bf16."""
+    raw = bf16_bits_to_f64(raw_bits)
+    k = gemma_rmsnorm(raw.mean(axis=0), pre.gamma_k, pre.eps)
+    return f64_to_bf16_bits(rope_neox(k, first_pos, pre.rotary_dim, pre.theta))
+
+
 class SeqState:
     """Logical token arrays of one sequence: K, V, raw index keys (bf16 bits),
     the compressed key of every complete block, and the ingested counter.
@@ -114,8 +178,9 @@ class SeqState:
     """
 
     def __init__(self, ratio: int, n_kv_heads: int, head_dim: int, idx_dim: int,
-                 capacity: int):
+                 capacity: int, pre: "PreIndexer" = None):
         self.ratio = ratio
+        self.pre = pre  # compressed keys through the pre-indexer when given
         self.capacity = capacity
         self.K = np.zeros((capacity, n_kv_heads, head_dim), np.uint16)
         self.V = np.zeros((capacity, n_kv_heads, head_dim), np.uint16)
@@ -147,7 +212,10 @@ class SeqState:
         first_done = pos // r            # first block that may complete now
         last_done = (pos + n) // r       # blocks [first_done, last_done) are complete
         for b in range(first_done, last_done):
-            self.idx_blk[b] = pool_block(self.idx_raw[b * r:(b + 1) * r])
+            if self.pre is None:
+                self.idx_blk[b] = pool_block(self.idx_raw[b * r:(b + 1) * r])
+            else:
+                self.idx_blk[b] = pool_block_pre(self.idx_raw[b * r:(b + 1) * r], b * r, self.pre)
         self.ingested = pos + n
 
     def rewind(self, n_drop: int) -> None:

@@ -101,6 +101,26 @@ def reuse_tail_from_current_blocks(state, pos, sel, sel_pos, q_bits):
             "out_bf16": O.f64_to_bf16_bits(out)}
 
 
+def pool_pre_rope_then_norm(raw_bits, first_pos, pre):
+    # bug: RoPE before the norm (the per-dimension gain lands on rotated values)
+    raw = O.bf16_bits_to_f64(raw_bits)
+    k = O.rope_neox(raw.mean(axis=0), first_pos, pre.rotary_dim, pre.theta)
+    return O.f64_to_bf16_bits(O.gemma_rmsnorm(k, pre.gamma_k, pre.eps))
+
+
+def pool_pre_at_last_position(raw_bits, first_pos, pre):
+    # bug: RoPE at the block's last token instead of its first
+    raw = O.bf16_bits_to_f64(raw_bits)
+    k = O.gemma_rmsnorm(raw.mean(axis=0), pre.gamma_k, pre.eps)
+    return O.f64_to_bf16_bits(O.rope_neox(k, first_pos + raw.shape[0] - 1, pre.rotary_dim, pre.theta))
+
+
+def norm_without_unit_offset(x, gamma, eps):
+    # bug: scales by gamma instead of 1 + gamma
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * np.asarray(gamma, np.float64)
+
+
 class StickyRewind(O.SeqState):
     def rewind(self, n_drop):
         if n_drop < 0 or n_drop > self.ingested:
@@ -121,6 +141,9 @@ MUTATIONS = [
     ("attend_row", visible_excludes_own_token, [P.test_dense_identity_at_and_below_inert_bound]),
     ("SeqState", StickyRewind, [P.test_counter_discipline]),
     ("attend_row_reused", reuse_tail_from_current_blocks, [P.test_reused_dense_selection_stays_exactly_dense]),
+    ("pool_block_pre", pool_pre_rope_then_norm, [P.test_pre_indexed_blocks_norm_then_rope_at_the_first_position]),
+    ("pool_block_pre", pool_pre_at_last_position, [P.test_pre_indexed_blocks_norm_then_rope_at_the_first_position]),
+    ("gemma_rmsnorm", norm_without_unit_offset, [P.test_gemma_rmsnorm_closed_forms]),
 ]
 
 

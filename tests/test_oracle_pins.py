@@ -377,6 +377,77 @@ def test_reused_sparse_selection_token_set():
 
 
 # ---------------------------------------------------------------------------
+# Pre-indexer: Gemma RMSNorm and NeoX RoPE
+# ---------------------------------------------------------------------------
+
+def test_gemma_rmsnorm_closed_forms():
+    g0 = np.zeros(4)
+    assert np.allclose(O.gemma_rmsnorm(np.full(4, 3.0), g0, 0.0), 1.0, atol=1e-15)
+    assert np.allclose(O.gemma_rmsnorm(np.full(4, -0.5), g0, 0.0), -1.0, atol=1e-15)
+    # [3, 4]: mean square 12.5, rms 5 / sqrt(2); gain 1 + gamma
+    got = O.gemma_rmsnorm(np.array([3.0, 4.0]), np.array([0.0, 1.0]), 0.0)
+    assert np.allclose(got, [3 * math.sqrt(2) / 5, 2 * 4 * math.sqrt(2) / 5], atol=1e-15)
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((5, 16)); g = rng.standard_normal(16) * 0.1
+    assert np.allclose(O.gemma_rmsnorm(7.5 * x, g, 0.0), O.gemma_rmsnorm(x, g, 0.0), atol=1e-13)
+    y = O.gemma_rmsnorm(x, np.zeros(16), 0.0)
+    assert np.allclose(np.mean(y * y, axis=-1), 1.0, atol=1e-13)   # unit RMS before the gain
+    assert np.all(O.gemma_rmsnorm(np.zeros(8), np.zeros(8), 1e-6) == 0.0)
+
+
+def test_rope_neox_closed_forms():
+    x = np.array([1.0, 0.0, 0.0, 1.0])
+    # rotary 4, base 1: both pairs turn by the position; a quarter turn maps
+    # (x0, x2) = (1, 0) -> (0, 1) and (x1, x3) = (0, 1) -> (-1, 0)
+    assert np.allclose(O.rope_neox(x, math.pi / 2, 4, 1.0), [0.0, -1.0, 1.0, 0.0], atol=1e-15)
+    rng = np.random.default_rng(43)
+    v = rng.standard_normal(128)
+    assert np.array_equal(O.rope_neox(v, 0, 64, 1e4), v)                 # position 0: identity
+    assert np.array_equal(O.rope_neox(v, 123, 64, 1e4)[64:], v[64:])     # dims past rotary untouched
+    # pair i of a 64-dim rotary at base 1e4 turns by pos * 1e4^(-i/32): pair 16 at pos 100 -> 1 rad
+    e = np.zeros(128); e[16] = 1.0
+    r = O.rope_neox(e, 100, 64, 1e4)
+    assert abs(r[16] - math.cos(1.0)) < 1e-12 and abs(r[48] - math.sin(1.0)) < 1e-12
+    assert np.count_nonzero(np.abs(r) > 1e-15) == 2
+    # rotations: pair norms kept, composition adds angles, dot products see only the offset
+    a, b = 37, 1291
+    ra = O.rope_neox(v, a, 64, 1e4)
+    assert np.allclose(ra[:32] ** 2 + ra[32:64] ** 2, v[:32] ** 2 + v[32:64] ** 2, atol=1e-12)
+    assert np.allclose(O.rope_neox(ra, b, 64, 1e4), O.rope_neox(v, a + b, 64, 1e4), atol=1e-9)
+    q, k = rng.standard_normal(128), rng.standard_normal(128)
+    d1 = O.rope_neox(q, 5000, 64, 1e4)[:64] @ O.rope_neox(k, 4000, 64, 1e4)[:64]
+    d2 = O.rope_neox(q, 1000, 64, 1e4)[:64] @ k[:64]
+    assert abs(d1 - d2) < 1e-9
+
+
+def test_pre_indexed_blocks_norm_then_rope_at_the_first_position():
+    # raw keys constant over each block: the mean is that key; the compressed key
+    # must be RoPE(GemmaRMSNorm(key)) at the block's first position b * ratio
+    rng = np.random.default_rng(47)
+    dI, ratio = 128, 4
+    pre = O.PreIndexer(rng.standard_normal(dI) * 0.2, rng.standard_normal(dI) * 0.2, 1e-6, 1e4, 64)
+    st = O.SeqState(ratio, 1, 16, dI, 64, pre=pre)
+    keys = rng.integers(-8, 9, size=(5, dI)).astype(np.float64)
+    raw = np.repeat(keys, ratio, axis=0)
+    z = np.zeros((5 * ratio, 1, 16), np.uint16)
+    st.append(0, z, z, O.f64_to_bf16_bits(raw))
+    for b in range(5):
+        want = O.f64_to_bf16_bits(O.rope_neox(O.gemma_rmsnorm(keys[b], pre.gamma_k, 1e-6), b * ratio, 64, 1e4))
+        assert np.array_equal(st.idx_blk[b], want), b
+    # queries: per-head norm, then RoPE at the row's position
+    qh = rng.integers(-8, 9, size=(3, dI)).astype(np.float64)
+    got = O.pre_index_query(O.f64_to_bf16_bits(qh), 77, pre)
+    want = O.f64_to_bf16_bits(O.rope_neox(O.gemma_rmsnorm(qh, pre.gamma_q, 1e-6), 77, 64, 1e4))
+    assert np.array_equal(got, want)
+    # a block's score sees only the offset between the row and the block start
+    qn = O.gemma_rmsnorm(qh[0], pre.gamma_q, 1e-6)
+    kn = O.gemma_rmsnorm(keys[2], pre.gamma_k, 1e-6)
+    s1 = O.rope_neox(qn, 77, 64, 1e4) @ O.rope_neox(kn, 8, 64, 1e4)
+    s2 = O.rope_neox(qn, 77 + 4000, 64, 1e4) @ O.rope_neox(kn, 8 + 4000, 64, 1e4)
+    assert abs(s1 - s2) < 1e-9
+
+
+# ---------------------------------------------------------------------------
 # State: append / rewind / chunking / counters
 # ---------------------------------------------------------------------------
 
