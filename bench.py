@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--prefill-steps", type=int, default=10)
     ap.add_argument("--reuse-steps", type=int, default=300,
                     help="decode steps with a reused selection (MTP draft steps); 0 skips the leg")
+    ap.add_argument("--pre-steps", type=int, default=300,
+                    help="decode steps through the pre-indexer (norm + RoPE of queries and keys); 0 skips")
     ap.add_argument("--prefill-warmup", type=int, default=3)
     return ap.parse_args()
 
@@ -204,7 +206,8 @@ def run_gpu(args):
     B = wl.n_seq
     K, W = args.steps, args.warmup
     total_steps = W + K + args.breakdown_steps + args.e2e_steps + 4
-    adv_per_batch = math.ceil((W + K + min(K, 600) + args.e2e_steps + 4) / NB) + (62 if args.reuse_steps > 0 else 0)
+    adv_per_batch = (math.ceil((W + K + min(K, 600) + args.e2e_steps + 4) / NB) + (62 if args.reuse_steps > 0 else 0)
+                     + (math.ceil(args.pre_steps / NB) + 2 if args.pre_steps > 0 else 0))
     # center the prefixes of the main timed region on 32768
     start = wl.prefixes[0] - W // NB - K // (2 * NB)
     start = max(start, 8)
@@ -363,7 +366,47 @@ def run_gpu(args):
     out["ms_per_step_one_graph_per_step"] = round(ms_single, 5)
     if args.reuse_steps > 0:
         out["reuse"] = run_reuse(args, Q, torch, cfg, sh, cache, batches, ws, status, stream, NB, B, hbm_gbs)
+    if args.pre_steps > 0:
+        out["pre_indexer"] = run_pre(args, Q, S, torch, cfg, sh, cache, batches, status, stream, NB, B, hbm_gbs,
+                                     ms)
     return out, rank, world
+
+
+def run_pre(args, Q, S, torch, cfg, sh, cache, batches, status, stream, NB, B, hbm_gbs, ms_plain):
+    """The fused decode step through the pre-indexer (qsa_decode_pre): the step's
+    index queries get Gemma RMSNorm + NeoX RoPE, a block completed by the step
+    is pooled, normed and roped, then score, select, attend as in the plain step.
+    Timed on the decode leg's cache (its older blocks were pooled without the
+    pre-indexer, which changes the values scored, not the work done)."""
+    dev = cache.k_pool.device
+    d = sh.idx_dim
+    u = S.uniform01(7, 101, torch.arange(2 * d, dtype=torch.int64)).to(torch.float32)
+    pre = Q.PreIndexer((0.4 * (u[:d] - 0.5)).to(dev), (0.4 * (u[d:] - 0.5)).to(dev), 1e-6, 1e4, 64)
+    ws = Q.workspace_pre(cfg, B, cache.max_blocks, device=dev)
+    rot = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(rot, stream=stream):
+        for bt in batches:
+            Q.qsa_decode_pre(cfg, pre, Q.Rows(bt["ids"], bt["pos0"], 1, advance=True), cache, bt["k"], bt["v"],
+                             bt["idx"], bt["q_idx"], bt["w"], bt["q"], bt["out"], ws, status, stream=stream)
+    torch.cuda.synchronize()
+    n_rot = max(1, math.ceil(args.pre_steps / NB))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        rot.replay()  # warm-up rotation
+        e0.record(stream)
+        for _ in range(n_rot):
+            rot.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st == 0, f"device status {st}: {Q.qsa_strerror(st)}"
+    steps = n_rot * NB
+    ms = e0.elapsed_time(e1) / steps
+    return {"what": "fused decode step through the pre-indexer (qsa_decode_pre: query norm + RoPE, "
+                    "completed-block norm + RoPE, score, select, attend), batch 32 x 32k",
+            "steps": steps, "ms_per_step": round(ms, 5), "rows_per_s": round(B / (ms * 1e-3), 1),
+            "overhead_vs_plain_ms": round(ms - ms_plain, 5)}
 
 
 def run_reuse(args, Q, torch, cfg, sh, cache, batches, ws, status, stream, NB, B, hbm_gbs):

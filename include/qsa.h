@@ -247,6 +247,52 @@ int qsa_decode(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cac
                int32_t *sel_out, int32_t *n_sel_out, qsa_bf16 *out,
                void *ws, size_t ws_bytes, int32_t *status, cudaStream_t stream);
 
+/* Pre-indexer ("Agentic shootout", "Flash-Next support: vLLM vs Atlas", (a)
+ * item 6, and the same report's description of the fused pre-indexer kernel:
+ * the indexer's q/k heads go through Gemma RMSNorm -- gain weight + 1, fp32
+ * accumulation -- and the same NeoX RoPE as main attention; a compressed key is
+ * the mean-pool, then the norm, then RoPE at the block's first position).
+ *   y   = x / sqrt(mean(x^2) + eps) * (1 + gamma)
+ *   RoPE at position p: for i < rotary_dim/2 the pair (y_i, y_{i+rotary_dim/2})
+ *       turns by p * rope_theta^(-2i/rotary_dim); dims >= rotary_dim are kept.
+ * The pages leave epsilon and the RoPE base open: both are inputs. The angle is
+ * formed and reduced to [-pi, pi] in double (each pair's frequency computed once
+ * per call on the host); its sine / cosine, the norm and the rotation run in
+ * fp32; results are rounded to bf16. Raw index keys are stored as given. */
+typedef struct qsa_pre_indexer {
+  const float *gamma_q; /* device [d_I] fp32: query-norm gains */
+  const float *gamma_k; /* device [d_I] fp32: compressed-key-norm gains */
+  float eps;            /* >= 0 */
+  float rope_theta;     /* > 0 */
+  int rotary_dim;       /* 0 (no RoPE), 64, or d_I */
+} qsa_pre_indexer;
+
+/* qsa_append whose completed blocks go through the pre-indexer:
+ * k_b = bf16(RoPE_{b*ratio}(GemmaRMSNorm(mean of the block's raw keys))).
+ * A cache must be filled with one kind of append throughout. */
+int qsa_append_pre(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_rows *rows,
+                   const qsa_cache *cache, const qsa_bf16 *k_new, const qsa_bf16 *v_new,
+                   const qsa_bf16 *idx_k_new, int32_t *status, cudaStream_t stream);
+
+/* The index queries of the rows through the pre-indexer:
+ * q_out[row, h] = bf16(RoPE_{row position}(GemmaRMSNorm(q_idx[row, h]))).
+ *   q_idx, q_out  device [rows, H_I, d_I] bf16, distinct buffers */
+int qsa_pre_index_q(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_rows *rows,
+                    const qsa_bf16 *q_idx, qsa_bf16 *q_out, cudaStream_t stream);
+
+/* Bytes of workspace qsa_decode_pre needs: qsa_workspace_bytes plus the
+ * pre-indexed query rows. */
+size_t qsa_workspace_bytes_pre(const qsa_config *cfg, int max_rows, int max_blocks_per_row);
+
+/* The fused step through the pre-indexer: as qsa_decode, with the appended
+ * blocks pooled as in qsa_append_pre and the index queries pre-indexed (into
+ * the workspace; q_idx itself is not written) before scoring. */
+int qsa_decode_pre(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_rows *rows,
+                   const qsa_cache *cache, const qsa_bf16 *k_new, const qsa_bf16 *v_new,
+                   const qsa_bf16 *idx_k_new, const qsa_bf16 *q_idx, const float *w, const qsa_bf16 *q,
+                   int32_t *sel_out, int32_t *n_sel_out, qsa_bf16 *out, void *ws, size_t ws_bytes,
+                   int32_t *status, cudaStream_t stream);
+
 /* Tokens one row's attention can take: the split plan covers
  * ceil((budget + ratio - 1) / 112) splits of 112 tokens. A reused selection
  * (below) may be used while its token set stays within this count. Returns 0

@@ -6,6 +6,7 @@
 // aligned; sticky CUDA errors are fatal, never laundered into success) and
 // Defect 5 (capacity is checked when tokens are appended, against the pages
 // the caller's table provides, never as a mid-step abort).
+#include <cmath>
 #include <cstring>
 
 #include "qsa_internal.cuh"
@@ -137,6 +138,100 @@ WsLayout ws_layout(const Shape &sh, int rows, int ld) {
 
 int ld_for(int max_blocks) { return static_cast<int>(round_up(max_blocks > 0 ? max_blocks : 1, 4)); }
 
+// Bytes of the pre-indexed index queries of `rows` rows (fused step with a pre-indexer).
+size_t q_prep_bytes(const Shape &sh, int rows) {
+  return static_cast<size_t>(rows) * sh.h_idx * sh.d_idx * sizeof(uint16_t);
+}
+
+// Pre-indexer parameters: gains present where needed, eps >= 0, theta > 0,
+// rotary dims 0, 64 or d_I (whole NeoX pairs per warp lane).
+int check_pre(const qsa_config *c, const qsa_pre_indexer *p, bool need_q, bool need_k) {
+  if (!p) return QSA_ERR_INVALID_ARG;
+  if ((need_q && !p->gamma_q) || (need_k && !p->gamma_k)) return QSA_ERR_INVALID_ARG;
+  if (!(p->eps >= 0.f) || !(p->rope_theta > 0.f) || p->eps > 1e30f || p->rope_theta > 1e30f)
+    return QSA_ERR_INVALID_ARG;
+  if (p->rotary_dim != 0 && p->rotary_dim != 64 && p->rotary_dim != c->idx_dim) return QSA_ERR_UNSUPPORTED;
+  return QSA_OK;
+}
+
+PreArgs pre_args(const qsa_pre_indexer *p, const uint16_t *q_in, uint16_t *q_out) {
+  PreArgs a;
+  a.gamma_q = p->gamma_q;
+  a.gamma_k = p->gamma_k;
+  a.eps = p->eps;
+  a.rot = p->rotary_dim;
+  const double pi = std::acos(-1.0);
+  for (int i = 0; i < a.rot / 2; ++i)
+    a.half_turns[i] = std::pow(static_cast<double>(p->rope_theta), -2.0 * i / a.rot) / pi;
+  a.q_in = q_in;
+  a.q_out = q_out;
+  return a;
+}
+
+
+
+// The fused step; pre != nullptr: through the pre-indexer (the append kernel
+// pre-indexes the step's query rows into the workspace, the score kernel reads
+// them after its dependency wait).
+int decode_impl(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_rows *rows,
+                const qsa_cache *cache, const qsa_bf16 *k_new, const qsa_bf16 *v_new,
+                const qsa_bf16 *idx_k_new, const qsa_bf16 *q_idx, const float *w, const qsa_bf16 *q,
+                int32_t *sel_out, int32_t *n_sel_out, qsa_bf16 *out, void *ws, size_t ws_bytes,
+                int32_t *status, cudaStream_t stream) {
+  int rc;
+  if ((rc = check_cfg(cfg)) != QSA_OK) return rc;
+  if ((rc = check_rows(rows)) != QSA_OK) return rc;
+  if ((rc = check_cache(cache, true, true)) != QSA_OK) return rc;
+  if (!cache->ingested || !status) return QSA_ERR_INVALID_ARG;
+  const int n_rows = rows->n_seq * rows->rows_per_seq;
+  if (n_rows == 0) return QSA_OK;
+  if (!k_new || !v_new || !idx_k_new || !q_idx || !w || !q || !out || !ws)
+    return QSA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(idx_k_new) || !aligned16(q_idx) ||
+      !aligned16(q) || !aligned16(out) || !aligned16(ws))
+    return QSA_ERR_INVALID_ARG;
+  if ((rc = host_capacity_check(rows, cache, cfg->page_size)) != QSA_OK) return rc;
+  const Shape sh = make_shape(cfg);
+  const int cap_tokens = cache->max_pages * cfg->page_size;
+  const int ld = ld_for(cap_tokens / cfg->ratio);
+  const WsLayout L = ws_layout(sh, n_rows, ld);
+  const size_t need = L.total + (pre ? round_up(q_prep_bytes(sh, n_rows), 256) : 0);
+  if (ws_bytes < need) return QSA_ERR_WORKSPACE;
+  uint8_t *base = static_cast<uint8_t *>(ws);
+  float *scores = reinterpret_cast<float *>(base + L.scores);
+  int32_t *sel = sel_out ? sel_out : reinterpret_cast<int32_t *>(base + L.sel);
+  int32_t *n_sel = n_sel_out ? n_sel_out : reinterpret_cast<int32_t *>(base + L.n_sel);
+  uint16_t *q_pre = pre ? reinterpret_cast<uint16_t *>(base + L.total) : nullptr;
+  const CacheView cv = view(cache);
+  const int R = rows->rows_per_seq;
+
+  PreArgs pa;
+  if (pre) pa = pre_args(pre, q_idx, q_pre);
+  cudaError_t e = launch_append(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cache->page_table,
+                                cache->max_pages, cache->num_pages, cache->k_pool, cache->v_pool,
+                                cache->idxraw_pool, cache->idxblk_pool, cache->ingested, k_new,
+                                v_new, idx_k_new, status, true, stream, pre ? &pa : nullptr);
+  if (e == cudaSuccess)
+    e = launch_score(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, pre ? q_pre : q_idx, w, scores, ld,
+                     status, true, stream, pre != nullptr);
+  if (e == cudaSuccess)
+    e = launch_select(sh, rows->n_seq, R, rows->pos0, scores, ld, sel, n_sel, ld, cap_tokens,
+                      status, true, stream);
+  // the counter (and, with rows->advance, pos0) moves last, inside the merge
+  // kernel: every stage before it reads the pre-step position
+  CommitArgs commit;
+  commit.n_seq = rows->n_seq;
+  commit.R = R;
+  commit.capacity = cap_tokens;
+  commit.advance = rows->advance;
+  commit.seq_ids = rows->seq_ids;
+  commit.pos0 = rows->pos0;
+  commit.ingested = cache->ingested;
+  if (e == cudaSuccess)
+    e = launch_attn(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, q, sel, n_sel, out,
+                    base + L.partials, status, true, commit, stream);
+  return cuda_status(e);
+}
 }  // namespace
 }  // namespace qsa
 
@@ -267,55 +362,67 @@ int qsa_decode(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cac
                const qsa_bf16 *q_idx, const float *w, const qsa_bf16 *q, int32_t *sel_out,
                int32_t *n_sel_out, qsa_bf16 *out, void *ws, size_t ws_bytes, int32_t *status,
                cudaStream_t stream) {
+  return decode_impl(cfg, nullptr, rows, cache, k_new, v_new, idx_k_new, q_idx, w, q, sel_out, n_sel_out,
+                     out, ws, ws_bytes, status, stream);
+}
+
+size_t qsa_workspace_bytes_pre(const qsa_config *cfg, int max_rows, int max_blocks_per_row) {
+  if (check_cfg(cfg) != QSA_OK || max_rows < 0 || max_blocks_per_row < 0) return 0;
+  const Shape sh = make_shape(cfg);
+  const WsLayout L = ws_layout(sh, max_rows, ld_for(max_blocks_per_row));
+  return L.total + round_up(q_prep_bytes(sh, max_rows), 256);
+}
+
+int qsa_append_pre(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_rows *rows,
+                   const qsa_cache *cache, const qsa_bf16 *k_new, const qsa_bf16 *v_new,
+                   const qsa_bf16 *idx_k_new, int32_t *status, cudaStream_t stream) {
   int rc;
   if ((rc = check_cfg(cfg)) != QSA_OK) return rc;
+  if ((rc = check_pre(cfg, pre, false, true)) != QSA_OK) return rc;
   if ((rc = check_rows(rows)) != QSA_OK) return rc;
   if ((rc = check_cache(cache, true, true)) != QSA_OK) return rc;
   if (!cache->ingested || !status) return QSA_ERR_INVALID_ARG;
-  const int n_rows = rows->n_seq * rows->rows_per_seq;
+  const long long n_rows = static_cast<long long>(rows->n_seq) * rows->rows_per_seq;
   if (n_rows == 0) return QSA_OK;
-  if (!k_new || !v_new || !idx_k_new || !q_idx || !w || !q || !out || !ws)
-    return QSA_ERR_INVALID_ARG;
-  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(idx_k_new) || !aligned16(q_idx) ||
-      !aligned16(q) || !aligned16(out) || !aligned16(ws))
+  if (!k_new || !v_new || !idx_k_new || !aligned16(k_new) || !aligned16(v_new) || !aligned16(idx_k_new))
     return QSA_ERR_INVALID_ARG;
   if ((rc = host_capacity_check(rows, cache, cfg->page_size)) != QSA_OK) return rc;
   const Shape sh = make_shape(cfg);
-  const int cap_tokens = cache->max_pages * cfg->page_size;
-  const int ld = ld_for(cap_tokens / cfg->ratio);
-  const WsLayout L = ws_layout(sh, n_rows, ld);
-  if (ws_bytes < L.total) return QSA_ERR_WORKSPACE;
-  uint8_t *base = static_cast<uint8_t *>(ws);
-  float *scores = reinterpret_cast<float *>(base + L.scores);
-  int32_t *sel = sel_out ? sel_out : reinterpret_cast<int32_t *>(base + L.sel);
-  int32_t *n_sel = n_sel_out ? n_sel_out : reinterpret_cast<int32_t *>(base + L.n_sel);
-  const CacheView cv = view(cache);
-  const int R = rows->rows_per_seq;
-
-  cudaError_t e = launch_append(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cache->page_table,
-                                cache->max_pages, cache->num_pages, cache->k_pool, cache->v_pool,
-                                cache->idxraw_pool, cache->idxblk_pool, cache->ingested, k_new,
-                                v_new, idx_k_new, status, true, stream);
+  const PreArgs pa = pre_args(pre, nullptr, nullptr);
+  cudaError_t e = launch_append(sh, rows->n_seq, rows->rows_per_seq, rows->seq_ids, rows->pos0,
+                                cache->page_table, cache->max_pages, cache->num_pages,
+                                cache->k_pool, cache->v_pool, cache->idxraw_pool, cache->idxblk_pool,
+                                cache->ingested, k_new, v_new, idx_k_new, status, false, stream, &pa);
   if (e == cudaSuccess)
-    e = launch_score(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, q_idx, w, scores, ld,
-                     status, true, stream);
-  if (e == cudaSuccess)
-    e = launch_select(sh, rows->n_seq, R, rows->pos0, scores, ld, sel, n_sel, ld, cap_tokens,
-                      status, true, stream);
-  // the counter (and, with rows->advance, pos0) moves last, inside the merge
-  // kernel: every stage before it reads the pre-step position
-  CommitArgs commit;
-  commit.n_seq = rows->n_seq;
-  commit.R = R;
-  commit.capacity = cap_tokens;
-  commit.advance = rows->advance;
-  commit.seq_ids = rows->seq_ids;
-  commit.pos0 = rows->pos0;
-  commit.ingested = cache->ingested;
-  if (e == cudaSuccess)
-    e = launch_attn(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, q, sel, n_sel, out,
-                    base + L.partials, status, true, commit, stream);
+    e = launch_commit(rows->n_seq, rows->rows_per_seq, cache->max_pages * cfg->page_size,
+                      rows->seq_ids, rows->pos0, cache->ingested, rows->advance, false, stream);
   return cuda_status(e);
+}
+
+int qsa_pre_index_q(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_rows *rows,
+                    const qsa_bf16 *q_idx, qsa_bf16 *q_out, cudaStream_t stream) {
+  int rc;
+  if ((rc = check_cfg(cfg)) != QSA_OK) return rc;
+  if ((rc = check_pre(cfg, pre, true, false)) != QSA_OK) return rc;
+  if ((rc = check_rows(rows)) != QSA_OK) return rc;
+  if (static_cast<long long>(rows->n_seq) * rows->rows_per_seq == 0) return QSA_OK;
+  if (!q_idx || !q_out) return QSA_ERR_INVALID_ARG;
+  if (q_idx == q_out) return QSA_ERR_INVALID_ARG;  // not in place
+  const Shape sh = make_shape(cfg);
+  return cuda_status(launch_pre_index_q(sh, rows->n_seq, rows->rows_per_seq, rows->pos0,
+                                        pre_args(pre, nullptr, nullptr), q_idx, q_out, false, stream));
+}
+
+int qsa_decode_pre(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_rows *rows,
+                   const qsa_cache *cache, const qsa_bf16 *k_new, const qsa_bf16 *v_new,
+                   const qsa_bf16 *idx_k_new, const qsa_bf16 *q_idx, const float *w, const qsa_bf16 *q,
+                   int32_t *sel_out, int32_t *n_sel_out, qsa_bf16 *out, void *ws, size_t ws_bytes,
+                   int32_t *status, cudaStream_t stream) {
+  int rc;
+  if ((rc = check_cfg(cfg)) != QSA_OK) return rc;
+  if ((rc = check_pre(cfg, pre, true, true)) != QSA_OK) return rc;
+  return decode_impl(cfg, pre, rows, cache, k_new, v_new, idx_k_new, q_idx, w, q, sel_out, n_sel_out, out, ws,
+                     ws_bytes, status, stream);
 }
 
 int qsa_gather_attn_reuse(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,

@@ -17,6 +17,126 @@ namespace {
 
 constexpr int kAppendTokensPerCta = 32;
 constexpr int kAppendThreads = 256;
+constexpr int kQPrepCtas = 8 * 152;  // query pre-indexing CTAs of one launch, at most
+
+// cos / sin of the RoPE angle pos * theta^(-2i/rot) of pair i. The angle is formed
+// in half-turns in double (pos times the pair's frequency from the host) and
+// brought to [-1, 1] by subtracting the nearest even integer, which is exact in
+// double; only the sine and cosine of that small angle are taken in fp32, so the
+// angle itself carries no fp32 rounding at large positions.
+__device__ __forceinline__ float2 rope_cs(int pos, int i, const PreArgs &pre) {
+  const double t = static_cast<double>(pos) * pre.half_turns[i];
+  const double red = t - 2.0 * rint(0.5 * t);
+  float sn, cs;
+  sincospif(static_cast<float>(red), &sn, &cs);
+  return make_float2(cs, sn);
+}
+
+// One warp, one d_I-vector held as lane L: dims L + 32m (m < D32). Gemma RMSNorm
+// (gain 1 + gamma, fp32 sum of squares in a fixed shuffle order), then the NeoX
+// rotation of pairs (i, i + rot/2), i < rot/2; with rot/2 a multiple of 32 a
+// pair lives in one lane. cs(i) gives the pair's (cos, sin).
+template <int D32, typename CS>
+__device__ __forceinline__ void pre_index_lanes(float (&x)[D32], const float *__restrict__ gamma, float eps,
+                                                int rot, int d_idx, int lane, CS cs) {
+  float ss = 0.f;
+#pragma unroll
+  for (int m = 0; m < D32; ++m) ss += x[m] * x[m];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(d_idx) + eps);
+#pragma unroll
+  for (int m = 0; m < D32; ++m) x[m] = x[m] * inv * (1.0f + gamma[lane + 32 * m]);
+  const int hm = rot >> 6;  // pairs per lane: (rot / 2) / 32
+#pragma unroll
+  for (int m = 0; m < D32 / 2; ++m) {
+    if (m < hm) {
+      const float2 c = cs(lane + 32 * m);
+      const float x1 = x[m], x2 = x[m + hm];
+      x[m] = x1 * c.x - x2 * c.y;
+      x[m + hm] = x2 * c.x + x1 * c.y;
+    }
+  }
+}
+
+// The query vectors (row, index head) of sequence i: RoPE(GemmaRMSNorm) into
+// q_out, one warp per vector. Vector v is row i*R + v / h_idx at position
+// p0 + v / h_idx, head v % h_idx; a CTA takes vectors slot*8 + warp, striding by
+// n_slots*8, so a decode step's 64 heads spread over 8 CTAs.
+template <int D32>
+__device__ void pre_index_queries(const Shape &sh, const PreArgs &pre, int i, int R, int p0, int slot,
+                                  int n_slots) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
+  const int n_vec = R * sh.h_idx;
+  for (int v = slot * n_warps + warp; v < n_vec; v += n_slots * n_warps) {
+    const int t = v / sh.h_idx;
+    const size_t base = (static_cast<size_t>(i) * R * sh.h_idx + v) * sh.d_idx;
+    float x[D32];
+#pragma unroll
+    for (int m = 0; m < D32; ++m) x[m] = bf16_bits_to_float(pre.q_in[base + lane + 32 * m]);
+    pre_index_lanes<D32>(x, pre.gamma_q, pre.eps, pre.rot, sh.d_idx, lane,
+                         [&](int ip) { return rope_cs(p0 + t, ip, pre); });
+#pragma unroll
+    for (int m = 0; m < D32; ++m) {
+      const __nv_bfloat16 h = __float2bfloat16_rn(x[m]);
+      pre.q_out[base + lane + 32 * m] = *reinterpret_cast<const uint16_t *>(&h);
+    }
+  }
+}
+
+// Query-prep CTAs of one sequence for R rows of n_seq sequences: 8 vectors
+// (one per warp) each, capped so a launch holds at most kQPrepCtas of them.
+int q_prep_ctas(const Shape &sh, int n_seq, int R) {
+  const long long want = (static_cast<long long>(R) * sh.h_idx + 7) / 8;
+  const long long cap = kQPrepCtas / n_seq > 1 ? kQPrepCtas / n_seq : 1;
+  return static_cast<int>(want < cap ? want : cap);
+}
+
+// One warp: the compressed key of block b through the pre-indexer. Raw keys are
+// summed in position order in fp32 (as in the plain pooling), then scaled by 1/r.
+template <int D32>
+__device__ void pool_block_pre(const Shape &sh, const PreArgs &pre, int b, int i, int R, int p0,
+                               const int32_t *__restrict__ ptab, int num_pages,
+                               const uint16_t *__restrict__ raw_pool, uint16_t *__restrict__ blk_pool,
+                               const uint16_t *__restrict__ idx_new, float inv_r, int bpp, int lane,
+                               int32_t *status) {
+  const int r = sh.ratio, P = sh.page;
+  float x[D32];
+#pragma unroll
+  for (int m = 0; m < D32; ++m) x[m] = 0.f;
+  for (int jj = 0; jj < r; ++jj) {
+    const int pos = b * r + jj;
+    const uint16_t *src;
+    if (pos >= p0) {
+      src = idx_new + (static_cast<size_t>(i) * R + (pos - p0)) * sh.d_idx;
+    } else {
+      const int page = ptab[pos >> sh.log2_page];
+      if (page < 0 || page >= num_pages) {
+        if (lane == 0) report(status, QSA_ERR_PAGE);
+        return;
+      }
+      src = raw_pool + (static_cast<size_t>(page) * P + (pos & (P - 1))) * sh.d_idx;
+    }
+#pragma unroll
+    for (int m = 0; m < D32; ++m) x[m] += bf16_bits_to_float(src[lane + 32 * m]);
+  }
+  const int page_b = ptab[(b * r) >> sh.log2_page];
+  if (page_b < 0 || page_b >= num_pages) {
+    if (lane == 0) report(status, QSA_ERR_PAGE);
+    return;
+  }
+#pragma unroll
+  for (int m = 0; m < D32; ++m) x[m] *= inv_r;
+  const int first = b * r;
+  pre_index_lanes<D32>(x, pre.gamma_k, pre.eps, pre.rot, sh.d_idx, lane,
+                       [&](int ip) { return rope_cs(first, ip, pre); });
+  uint16_t *dst = blk_pool + static_cast<size_t>(page_b) * bpp * sh.d_idx;
+#pragma unroll
+  for (int m = 0; m < D32; ++m) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x[m]);
+    dst[blk_elem_offset(b & (bpp - 1), lane + 32 * m, bpp, sh.d_idx)] = *reinterpret_cast<const uint16_t *>(&h);
+  }
+}
 
 __global__ void __launch_bounds__(kAppendThreads)
 append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
@@ -25,14 +145,24 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
               uint16_t *__restrict__ v_pool, uint16_t *__restrict__ raw_pool,
               uint16_t *__restrict__ blk_pool, const int32_t *__restrict__ ingested,
               const uint16_t *__restrict__ k_new, const uint16_t *__restrict__ v_new,
-              const uint16_t *__restrict__ idx_new, int32_t *status) {
+              const uint16_t *__restrict__ idx_new, int32_t *status, int n_chunks,
+              const __grid_constant__ PreArgs pre) {
   // the previous step's commit (ingested, pos0) when launched as a dependent; only
   // then may the score kernel start: its prologue reads the positions
   pdl_wait();
   pdl_trigger();
   const int i = blockIdx.x;
-  const int s = seq_ids[i];
   const int p0 = pos0[i];
+  if (static_cast<int>(blockIdx.y) >= n_chunks) {
+    // the step's query rows through the pre-indexer (only when pre.q_out is set)
+    const int slot = blockIdx.y - n_chunks, n_slots = gridDim.y - n_chunks;
+    if (sh.d_idx == 128)
+      pre_index_queries<4>(sh, pre, i, R, p0, slot, n_slots);
+    else
+      pre_index_queries<2>(sh, pre, i, R, p0, slot, n_slots);
+    return;
+  }
+  const int s = seq_ids[i];
   const int P = sh.page;
   const int cap = max_pages * P;
   const bool lead = (threadIdx.x == 0 && blockIdx.y == 0);
@@ -91,6 +221,18 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
   const int half = sh.d_idx / 2;
   const int bpp = P >> sh.log2_ratio;  // blocks per page
   const float inv_r = 1.0f / static_cast<float>(r);
+  if (pre.gamma_k) {
+    // one warp per block: mean-pool, Gemma RMSNorm, RoPE at the block's first position
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
+    for (int bb = warp; bb < b_hi - b_lo; bb += n_warps) {
+      const int b = b_lo + bb;
+      if (sh.d_idx == 128)
+        pool_block_pre<4>(sh, pre, b, i, R, p0, ptab, num_pages, raw_pool, blk_pool, idx_new, inv_r, bpp, lane, status);
+      else
+        pool_block_pre<2>(sh, pre, b, i, R, p0, ptab, num_pages, raw_pool, blk_pool, idx_new, inv_r, bpp, lane, status);
+    }
+    return;
+  }
   for (int e = threadIdx.x; e < (b_hi - b_lo) * half; e += blockDim.x) {
     const int b = b_lo + e / half;
     const int d2 = (e % half) * 2;
@@ -123,6 +265,20 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
                     blk_elem_offset(b & (bpp - 1), d2, bpp, sh.d_idx);
     *reinterpret_cast<uint32_t *>(dst) = pack_bf16(s0 * inv_r, s1 * inv_r);
   }
+}
+
+// Standalone query pre-indexing: CTA (i, y) takes query vectors y*8 .. of
+// sequence i, striding by gridDim.y*8.
+__global__ void __launch_bounds__(kAppendThreads)
+pre_index_q_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const __grid_constant__ PreArgs pre) {
+  pdl_wait();  // positions
+  pdl_trigger();
+  const int i = blockIdx.x;
+  const int p0 = pos0[i];
+  if (sh.d_idx == 128)
+    pre_index_queries<4>(sh, pre, i, R, p0, blockIdx.y, gridDim.y);
+  else
+    pre_index_queries<2>(sh, pre, i, R, p0, blockIdx.y, gridDim.y);
 }
 
 __global__ void commit_kernel(int n_seq, int R, int capacity, const int32_t *__restrict__ seq_ids,
@@ -161,12 +317,25 @@ cudaError_t launch_append(const Shape &sh, int n_seq, int R, const int32_t *seq_
                           int num_pages, uint16_t *k_pool, uint16_t *v_pool,
                           uint16_t *idxraw_pool, uint16_t *idxblk_pool, const int32_t *ingested,
                           const uint16_t *k_new, const uint16_t *v_new,
-                          const uint16_t *idx_k_new, int32_t *status, bool pdl, cudaStream_t st) {
+                          const uint16_t *idx_k_new, int32_t *status, bool pdl, cudaStream_t st,
+                          const PreArgs *pre) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
-  dim3 grid(n_seq, (R + kAppendTokensPerCta - 1) / kAppendTokensPerCta);
+  const int n_chunks = (R + kAppendTokensPerCta - 1) / kAppendTokensPerCta;
+  const int n_q = pre && pre->q_out ? q_prep_ctas(sh, n_seq, R) : 0;
+  dim3 grid(n_seq, n_chunks + n_q);
   return launch_kernel(pdl, append_kernel, grid, dim3(kAppendThreads), 0, st, sh, R, seq_ids, pos0, page_table,
                        max_pages, num_pages, k_pool, v_pool, idxraw_pool, idxblk_pool, ingested, k_new, v_new,
-                       idx_k_new, status);
+                       idx_k_new, status, n_chunks, pre ? *pre : PreArgs{});
+}
+
+cudaError_t launch_pre_index_q(const Shape &sh, int n_seq, int R, const int32_t *pos0, const PreArgs &pre,
+                               const uint16_t *q_in, uint16_t *q_out, bool pdl, cudaStream_t st) {
+  if (n_seq == 0 || R == 0) return cudaSuccess;
+  PreArgs p = pre;
+  p.q_in = q_in;
+  p.q_out = q_out;
+  dim3 grid(n_seq, q_prep_ctas(sh, n_seq, R));
+  return launch_kernel(pdl, pre_index_q_kernel, grid, dim3(kAppendThreads), 0, st, sh, R, pos0, p);
 }
 
 cudaError_t launch_commit(int n_seq, int R, int capacity, const int32_t *seq_ids,

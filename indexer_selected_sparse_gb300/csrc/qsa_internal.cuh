@@ -34,6 +34,26 @@ __host__ __device__ __forceinline__ int blk_elem_offset(int rr, int d, int bpp, 
   return ((rr / g) * (d_idx >> 3) + (d >> 3)) * (g << 3) + (rr % g) * 8 + (d & 7);
 }
 
+// --- pre-indexer ------------------------------------------------------------
+// Gemma RMSNorm (gain 1 + gamma, fp32 accumulation) and NeoX RoPE of the index
+// queries and of every compressed key ("Agentic shootout", "Flash-Next support:
+// vLLM vs Atlas", (a) item 6 and its fused pre-indexer kernel). q_in / q_out:
+// when set, the append kernel also pre-indexes the step's query rows.
+// half_turns[i]: the frequency of rotary pair i, theta^(-2i/rot), in half-turns
+// per position (divided by pi), computed once per call on the host in double.
+// Kernels take the block as a __grid_constant__ parameter, so indexing the
+// table reads the parameter bank directly.
+constexpr int kMaxHalfRot = 64;  // rotary pairs of a head, at most (d_I = 128)
+struct PreArgs {
+  const float *gamma_q = nullptr;
+  const float *gamma_k = nullptr;
+  float eps = 0.f;
+  int rot = 0;  // rotary dims: 0, 64 or d_I
+  const uint16_t *q_in = nullptr;
+  uint16_t *q_out = nullptr;
+  double half_turns[kMaxHalfRot] = {};
+};
+
 // --- launch parameter blocks ---------------------------------------------
 
 struct CacheView {
@@ -173,7 +193,11 @@ cudaError_t launch_append(const Shape &sh, int n_seq, int R, const int32_t *seq_
                           int num_pages, uint16_t *k_pool, uint16_t *v_pool,
                           uint16_t *idxraw_pool, uint16_t *idxblk_pool, const int32_t *ingested,
                           const uint16_t *k_new, const uint16_t *v_new,
-                          const uint16_t *idx_k_new, int32_t *status, bool pdl, cudaStream_t st);
+                          const uint16_t *idx_k_new, int32_t *status, bool pdl, cudaStream_t st,
+                          const PreArgs *pre = nullptr);
+// query rows [rows, H_I, d_I] -> RoPE(GemmaRMSNorm) at each row's position
+cudaError_t launch_pre_index_q(const Shape &sh, int n_seq, int R, const int32_t *pos0, const PreArgs &pre,
+                               const uint16_t *q_in, uint16_t *q_out, bool pdl, cudaStream_t st);
 cudaError_t launch_commit(int n_seq, int R, int capacity, const int32_t *seq_ids,
                           int32_t *pos0, int32_t *ingested, int advance, bool pdl, cudaStream_t st);
 cudaError_t launch_rewind(int n_seq, const int32_t *seq_ids, const int32_t *n_drop,
@@ -181,12 +205,12 @@ cudaError_t launch_rewind(int n_seq, const int32_t *seq_ids, const int32_t *n_dr
 cudaError_t launch_score(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                          const int32_t *pos0, const CacheView &cv, const uint16_t *q_idx,
                          const float *w, float *scores, int ld_scores, int32_t *status, bool pdl,
-                         cudaStream_t st);
+                         cudaStream_t st, bool q_in_step = false);
 bool score_tc_supported(const Shape &sh);
 cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                             const int32_t *pos0, const CacheView &cv, const uint16_t *q_idx,
                             const float *w, float *scores, int ld, int32_t *status, bool pdl,
-                            cudaStream_t st);
+                            cudaStream_t st, bool q_in_step = false);
 cudaError_t launch_select(const Shape &sh, int n_seq, int R, const int32_t *pos0,
                           const float *scores, int ld_scores, int32_t *sel, int32_t *n_sel,
                           int max_blocks, int cap_tokens, int32_t *status, bool pdl,

@@ -154,12 +154,13 @@ cudaError_t launch_score_t(const Shape &sh, int n_seq, int R, const int32_t *seq
 cudaError_t launch_score(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                          const int32_t *pos0, const CacheView &cv, const uint16_t *q_idx,
                          const float *w, float *scores, int ld_scores, int32_t *status, bool pdl,
-                         cudaStream_t st) {
+                         cudaStream_t st, bool q_in_step) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
   // tcgen05 path whenever the TMA page boxes fit (8..32 blocks per page);
   // the mma.sync kernel below covers the remaining shapes (ratio 16)
   if (score_tc_supported(sh))
-    return launch_score_tc(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, pdl, st);
+    return launch_score_tc(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, pdl, st,
+                           q_in_step);
   const int nh = sh.h_idx <= 16 ? 16 : (sh.h_idx <= 32 ? 32 : 64);
   if (sh.d_idx == 128) {
     if (nh == 16) return launch_score_t<128, 16>(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, pdl, st);

@@ -197,6 +197,8 @@ struct TcArgs {
   int ld;
   int32_t *status;
   int n_groups;        // groups of rows (n_seq * groups_per_seq)
+  int q_in_step;       // the queries are written by this step's first kernel: load them only
+                       // after the dependency wait
 };
 
 constexpr int kMaxEpiWarps = 4 * kTcMaxGroup;  // one per (row of the group, TMEM lane quarter)
@@ -412,6 +414,21 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     Batch cur = load_batch(a, w, gi, lane, per_batch, pages_in_tile, bpp);
     int cur_g = -1, gseq = -1, k = 0;
     bool ok = true, waited = false;
+    // a query load held back until the dependency wait (queries written this step)
+    bool pend = false;
+    int pend_bs = 0, pend_row0 = 0;
+    auto wait_now = [&]() {
+      pdl_wait();  // blocks completed by this step come from the append kernel
+      pdl_trigger();
+      waited = true;
+      if (pend && lane == 0) {
+        mbar_arrive_expect_tx(b_full(pend_bs), b_slot);
+#pragma unroll
+        for (int hh = 0; hh < HALVES; ++hh)
+          tma_load_2d(b_u + pend_bs * b_slot + hh * b_half, &tm_q, b_full(pend_bs), hh * 64, pend_row0 * sh.h_idx);
+      }
+      pend = false;
+    };
     while (ok && w.left > 0) {
       Walker wn = w;
       for (int it = 0; it < cur.nb; ++it) walker_next(wn, a, n_groups);
@@ -419,8 +436,14 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       if (w.g != cur_g) {
         ++gseq;
         const int bs = gseq & 1;
+        // at most the first group's query load waits for the dependency wait
+        if (a.q_in_step && !waited && gseq >= 1) wait_now();
         if (gseq >= 2 && !mbar_wait_or_abort(b_empty(bs), ((gseq >> 1) - 1) & 1, abort_flag, a.status)) break;
-        if (lane == 0) {
+        if (a.q_in_step && !waited) {
+          pend = true;
+          pend_bs = bs;
+          pend_row0 = cur.row0;
+        } else if (lane == 0) {
           mbar_arrive_expect_tx(b_full(bs), b_slot);
 #pragma unroll
           for (int hh = 0; hh < HALVES; ++hh)
@@ -435,11 +458,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       const unsigned have_mask = __ballot_sync(0xffffffffu, load);
       for (int it = 0; it < cur.nb; ++it, ++k) {
         const int s = k % S;
-        if (!waited && (k >= S || (w.t + it + 1) * kTcTileBlocks > cur.nblk_old)) {
-          pdl_wait();  // blocks completed by this step come from the append kernel
-          pdl_trigger();
-          waited = true;
-        }
+        if (!waited && (k >= S || (w.t + it + 1) * kTcTileBlocks > cur.nblk_old)) wait_now();
         if (k >= S && !mbar_wait_or_abort(a_empty(s), ((k / S) - 1) & 1, abort_flag, a.status)) {
           ok = false;
           break;
@@ -458,10 +477,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       w = wn;
       cur = nxt;
     }
-    if (!waited) {
-      pdl_wait();
-      pdl_trigger();
-    }
+    if (!waited) wait_now();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     Walker w = walker_start(a, n_groups, lane);
@@ -615,9 +631,10 @@ bool score_tc_supported(const Shape &sh) {
 cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                             const int32_t *pos0, const CacheView &cv, const uint16_t *q_idx,
                             const float *w, float *scores, int ld, int32_t *status, bool pdl,
-                            cudaStream_t st) {
+                            cudaStream_t st, bool q_in_step) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
   TcArgs a;
+  a.q_in_step = q_in_step ? 1 : 0;
   a.sh = sh;
   a.R = R;
   a.G = (sh.h_idx % 16 == 0) ? min(min(R, kTcMaxGroup), 256 / sh.h_idx) : 1;

@@ -36,7 +36,8 @@ QSA_ERR_REUSE = 11
 EXPORTED = ("qsa_strerror", "qsa_config_check", "qsa_workspace_bytes", "qsa_append",
             "qsa_rewind", "qsa_index_score", "qsa_topk_select", "qsa_gather_attn", "qsa_decode",
             "qsa_gather_attn_static", "qsa_max_attend_tokens", "qsa_gather_attn_reuse",
-            "qsa_decode_reuse")
+            "qsa_decode_reuse", "qsa_append_pre", "qsa_pre_index_q", "qsa_workspace_bytes_pre",
+            "qsa_decode_pre")
 QSA_STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -56,6 +57,11 @@ class qsa_config(ctypes.Structure):
     _fields_ = [("ratio", ctypes.c_int), ("budget", ctypes.c_int), ("n_idx_heads", ctypes.c_int),
                 ("idx_dim", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("page_size", ctypes.c_int)]
+
+
+class qsa_pre_indexer(ctypes.Structure):
+    _fields_ = [("gamma_q", ctypes.c_void_p), ("gamma_k", ctypes.c_void_p), ("eps", ctypes.c_float),
+                ("rope_theta", ctypes.c_float), ("rotary_dim", ctypes.c_int)]
 
 
 class qsa_rows(ctypes.Structure):
@@ -103,6 +109,16 @@ LIB.qsa_gather_attn_reuse.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, _
 LIB.qsa_decode_reuse.restype = _I
 LIB.qsa_decode_reuse.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                  _P, _P]
+_PRE = ctypes.POINTER(qsa_pre_indexer)
+LIB.qsa_append_pre.restype = _I
+LIB.qsa_append_pre.argtypes = [_CFG, _PRE, _ROWS, _CACHE, _P, _P, _P, _P, _P]
+LIB.qsa_pre_index_q.restype = _I
+LIB.qsa_pre_index_q.argtypes = [_CFG, _PRE, _ROWS, _P, _P, _P]
+LIB.qsa_workspace_bytes_pre.restype = ctypes.c_size_t
+LIB.qsa_workspace_bytes_pre.argtypes = [_CFG, _I, _I]
+LIB.qsa_decode_pre.restype = _I
+LIB.qsa_decode_pre.argtypes = [_CFG, _PRE, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                               ctypes.c_size_t, _P, _P]
 LIB.qsa_decode.restype = _I
 LIB.qsa_decode.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                            ctypes.c_size_t, _P, _P]
@@ -329,6 +345,58 @@ def qsa_decode_reuse(cfg: Config, rows: Rows, cache: PagedCache, k_new, v_new, i
                               _ptr(out, torch.bfloat16), _ptr(ws), ws.numel() * ws.element_size(),
                               _ptr(status, torch.int32), _stream(stream))
     _check(rc, "qsa_decode_reuse", f"capacity {cache.capacity} tokens per sequence" if rc == QSA_ERR_CAPACITY else "")
+
+
+class PreIndexer:
+    """Pre-indexer parameters: per-dimension norm gains (device fp32 [d_I]; the
+    norm multiplies by 1 + gain), epsilon, RoPE base and rotary dims."""
+
+    def __init__(self, gamma_q: torch.Tensor, gamma_k: torch.Tensor, eps: float, rope_theta: float,
+                 rotary_dim: int):
+        self.gamma_q = gamma_q.to(torch.float32).contiguous()
+        self.gamma_k = gamma_k.to(torch.float32).contiguous()
+        self.eps, self.rope_theta, self.rotary_dim = float(eps), float(rope_theta), int(rotary_dim)
+
+    def c(self) -> qsa_pre_indexer:
+        return qsa_pre_indexer(_ptr(self.gamma_q), _ptr(self.gamma_k), self.eps, self.rope_theta,
+                               self.rotary_dim)
+
+
+def qsa_append_pre(cfg: Config, pre: PreIndexer, rows: Rows, cache: PagedCache, k_new, v_new, idx_k_new,
+                   status, stream=None) -> None:
+    rc = LIB.qsa_append_pre(ctypes.byref(cfg.c()), ctypes.byref(pre.c()), ctypes.byref(rows.c()),
+                            ctypes.byref(cache.c()), _ptr(k_new, torch.bfloat16), _ptr(v_new, torch.bfloat16),
+                            _ptr(idx_k_new, torch.bfloat16), _ptr(status, torch.int32), _stream(stream))
+    _check(rc, "qsa_append_pre", f"capacity {cache.capacity} tokens per sequence" if rc == QSA_ERR_CAPACITY else "")
+
+
+def qsa_pre_index_q(cfg: Config, pre: PreIndexer, rows: Rows, q_idx, q_out, stream=None) -> None:
+    rc = LIB.qsa_pre_index_q(ctypes.byref(cfg.c()), ctypes.byref(pre.c()), ctypes.byref(rows.c()),
+                             _ptr(q_idx, torch.bfloat16), _ptr(q_out, torch.bfloat16), _stream(stream))
+    _check(rc, "qsa_pre_index_q")
+
+
+def qsa_workspace_bytes_pre(cfg: Config, max_rows: int, max_blocks_per_row: int) -> int:
+    return LIB.qsa_workspace_bytes_pre(ctypes.byref(cfg.c()), max_rows, max_blocks_per_row)
+
+
+def workspace_pre(cfg: Config, max_rows: int, max_blocks_per_row: int, device="cuda") -> torch.Tensor:
+    """A device workspace of qsa_workspace_bytes_pre() bytes (uint8)."""
+    n = qsa_workspace_bytes_pre(cfg, max_rows, max_blocks_per_row)
+    if n == 0:
+        raise QsaError(QSA_ERR_UNSUPPORTED, "qsa_workspace_bytes_pre")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def qsa_decode_pre(cfg: Config, pre: PreIndexer, rows: Rows, cache: PagedCache, k_new, v_new, idx_k_new, q_idx,
+                   w, q, out, ws, status, sel_out=None, n_sel_out=None, stream=None) -> None:
+    rc = LIB.qsa_decode_pre(ctypes.byref(cfg.c()), ctypes.byref(pre.c()), ctypes.byref(rows.c()),
+                            ctypes.byref(cache.c()), _ptr(k_new, torch.bfloat16), _ptr(v_new, torch.bfloat16),
+                            _ptr(idx_k_new, torch.bfloat16), _ptr(q_idx, torch.bfloat16), _ptr(w, torch.float32),
+                            _ptr(q, torch.bfloat16), _ptr(sel_out, torch.int32), _ptr(n_sel_out, torch.int32),
+                            _ptr(out, torch.bfloat16), _ptr(ws), ws.numel() * ws.element_size(),
+                            _ptr(status, torch.int32), _stream(stream))
+    _check(rc, "qsa_decode_pre", f"capacity {cache.capacity} tokens per sequence" if rc == QSA_ERR_CAPACITY else "")
 
 
 def workspace(cfg: Config, max_rows: int, max_blocks_per_row: int, device="cuda") -> torch.Tensor:

@@ -121,3 +121,23 @@ def test_oracle_and_product_do_not_import_each_other():
         if f.endswith(".py"):
             text = open(os.path.join(ROOT, "oracle", f)).read()
             assert "indexer_selected_sparse_gb300" not in text, f
+
+
+def test_pre_indexer_arguments_checked_on_host(Q):
+    import torch
+    cfg = Q.Config(ratio=4, budget=2048, n_idx_heads=64, idx_dim=128, n_q_heads=32, n_kv_heads=4,
+                   head_dim=128, page_size=64)
+    rows = Q.Rows(torch.zeros(1, dtype=torch.int32), torch.zeros(1, dtype=torch.int32), 1)
+    g = torch.zeros(128)
+    q = torch.zeros(1, 64, 128, dtype=torch.bfloat16)
+    cases = [(Q.PreIndexer(g, g, 1e-6, 1e4, 32), Q.QSA_ERR_UNSUPPORTED),   # rotary dims not 0 / 64 / d_I
+             (Q.PreIndexer(g, g, -1.0, 1e4, 64), Q.QSA_ERR_INVALID_ARG),   # negative epsilon
+             (Q.PreIndexer(g, g, 1e-6, 0.0, 64), Q.QSA_ERR_INVALID_ARG)]   # RoPE base must be positive
+    for pre, code in cases:
+        rc = Q.LIB.qsa_pre_index_q(ctypes.byref(cfg.c()), ctypes.byref(pre.c()), ctypes.byref(rows.c()),
+                                   q.data_ptr(), q.data_ptr() + 2, None)
+        assert rc == code, (rc, code)
+    rc = Q.LIB.qsa_pre_index_q(ctypes.byref(cfg.c()), None, ctypes.byref(rows.c()), q.data_ptr(),
+                               q.data_ptr() + 2, None)
+    assert rc == Q.QSA_ERR_INVALID_ARG
+    assert Q.qsa_workspace_bytes_pre(cfg, 32, 8192) > Q.qsa_workspace_bytes(cfg, 32, 8192)
