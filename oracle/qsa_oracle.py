@@ -168,6 +168,76 @@ def pool_block_pre(raw_bits, first_pos: int, pre: PreIndexer) -> np.ndarray:
     return f64_to_bf16_bits(rope_neox(k, first_pos, pre.rotary_dim, pre.theta))
 
 
+# ---------------------------------------------------------------------------
+# MXFP8 index plane ("Agentic shootout", "Flash-Next support: vLLM vs Atlas",
+# the report whose (a) item 3 is "QSA sparse attention + n-gram indexer",
+# Scores bullet: with an MXFP8 indexer cache both the index queries and the
+# cached index keys are MXFP8-quantised before scoring; "ATOM Model Support
+# Guide", "Model architecture details", DeepSeek-V4.1, Cache bullet: an fp8
+# index plane, values and E8M0 scales held in two planes).
+#
+# The pages name the format but do not restate it; MXFP8 is the OCP
+# Microscaling format (MX specification v1.0): a block of 32 consecutive values
+# shares one scale 2^e stored as an E8M0 byte (e + 127), and each value is an FP8
+# E4M3 element (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; the
+# all-ones pattern is NaN, so the largest finite magnitude is 448). The scale
+# is 2^(floor(log2(amax)) - 8), 8 being the exponent of E4M3's largest binade,
+# so amax / scale lies in [256, 512); elements are value / scale rounded to
+# nearest-even on the E4M3 grid, magnitudes past 448 clamped to 448.
+# ---------------------------------------------------------------------------
+
+MX_BLOCK = 32
+E4M3_MAX = 448.0
+E4M3_EMAX = 8          # exponent of the largest E4M3 binade
+E8M0_MIN_EXP = -127    # smallest scale exponent an E8M0 byte holds (byte 0)
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Round fp64 values to the E4M3 grid, nearest-even, magnitudes clamped to
+    448. Normal binades [2^E, 2^(E+1)) for E = -6 .. 8 hold 8 values each
+    (quantum 2^(E-3)); below 2^-6 the subnormal quantum is 2^-9."""
+    v = np.asarray(v, np.float64)
+    a = np.minimum(np.abs(v), E4M3_MAX)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))          # a = m * 2^e, m in [0.5, 1)
+    lead = np.maximum(e - 1, -6)                        # exponent of the leading bit
+    quantum = np.ldexp(1.0, lead - 3)
+    r = np.rint(a / quantum) * quantum                  # rint: half to even
+    r = np.minimum(np.where(a > 0, r, 0.0), E4M3_MAX)
+    return np.copysign(r, v)
+
+
+def mxfp8_quantize(x) -> Tuple[np.ndarray, np.ndarray]:
+    """MXFP8 blocks of the last axis (a multiple of 32): returns the E4M3
+    element values [..., n] and the scale exponents [..., n / 32] (ints). A
+    block whose largest magnitude is 0 (or below 2^-126) takes the smallest
+    scale, 2^-127."""
+    x = np.asarray(x, np.float64)
+    n = x.shape[-1]
+    assert n % MX_BLOCK == 0, "MXFP8 blocks need a multiple of 32 values"
+    blocks = x.reshape(x.shape[:-1] + (n // MX_BLOCK, MX_BLOCK))
+    amax = np.abs(blocks).max(axis=-1)
+    _, e = np.frexp(np.where(amax > 0, amax, 1.0))
+    exp = np.where(amax >= 2.0 ** -126, (e - 1) - E4M3_EMAX, E8M0_MIN_EXP)
+    exp = np.maximum(exp, E8M0_MIN_EXP).astype(np.int64)
+    elems = e4m3_round(blocks / np.ldexp(1.0, exp)[..., None])
+    return elems.reshape(x.shape), exp
+
+
+def mxfp8_dequantize(elems, exps) -> np.ndarray:
+    """Values of MXFP8 blocks: element times 2^(its block's exponent)."""
+    elems = np.asarray(elems, np.float64)
+    n = elems.shape[-1]
+    scale = np.repeat(np.ldexp(1.0, np.asarray(exps)), MX_BLOCK, axis=-1)
+    assert scale.shape[-1] == n
+    return elems * scale
+
+
+def mxfp8_round_bits(bits) -> np.ndarray:
+    """bf16 vectors (last axis) through MXFP8 and back: the values the scores
+    see, as fp64 (every such value is exact in bf16)."""
+    return mxfp8_dequantize(*mxfp8_quantize(bf16_bits_to_f64(bits)))
+
+
 class SeqState:
     """Logical token arrays of one sequence: K, V, raw index keys (bf16 bits),
     the compressed key of every complete block, and the ingested counter.
@@ -243,6 +313,16 @@ def block_scores(q_idx_bits, w, blk_bits) -> np.ndarray:
     return np.asarray(w, np.float64) @ np.maximum(dots, 0.0)
 
 
+def block_scores_mxfp8(q_idx_bits, w, blk_bits) -> np.ndarray:
+    """block_scores with an MXFP8 index plane: every query head and every
+    compressed key (bf16) is MXFP8-quantised along d_I, and the score is the
+    same fp64 sum over the quantised values."""
+    q = mxfp8_round_bits(q_idx_bits)
+    k = mxfp8_round_bits(blk_bits)
+    dots = q @ k.T
+    return np.asarray(w, np.float64) @ np.maximum(dots, 0.0)
+
+
 def select_blocks(scores, topk: int) -> np.ndarray:
     """Top-K blocks by (score descending, block index ascending), returned in
     ascending block order. With n_blk <= K every block is selected, which makes
@@ -290,18 +370,21 @@ def gqa_attention(q_bits, k_bits, v_bits) -> np.ndarray:
     return out
 
 
-def attend_row(state: SeqState, pos: int, q_idx_bits, w, q_bits, topk: int) -> Dict:
+def attend_row(state: SeqState, pos: int, q_idx_bits, w, q_bits, topk: int,
+               index_format: str = "bf16") -> Dict:
     """The whole path for one query row at logical position pos.
 
     The row's token is already ingested, so V = pos + 1 tokens are visible and
-    n_blk = V // ratio blocks are complete."""
+    n_blk = V // ratio blocks are complete. index_format "mxfp8" scores with
+    the MXFP8 index plane (block_scores_mxfp8)."""
     r = state.ratio
     visible = pos + 1
     if visible > state.ingested:
         raise DesyncError(f"row at pos {pos} but only {state.ingested} ingested")
     n_blk = visible // r
     if n_blk > topk:
-        scores = block_scores(q_idx_bits, w, state.idx_blk[:n_blk])
+        score_fn = {"bf16": block_scores, "mxfp8": block_scores_mxfp8}[index_format]
+        scores = score_fn(q_idx_bits, w, state.idx_blk[:n_blk])
     else:
         scores = None                        # everything is selected; no scoring needed
     sel = select_blocks(scores if scores is not None else np.zeros(n_blk), topk)
@@ -379,7 +462,7 @@ def dense_attention(q_bits, k_bits, v_bits, n_kv_heads: int) -> np.ndarray:
 
 
 def step(states: List[SeqState], pos0: List[int], k_new, v_new, idx_new,
-         q_idx, w, q, topk: int, rows_per_seq: int) -> List[Dict]:
+         q_idx, w, q, topk: int, rows_per_seq: int, index_format: str = "bf16") -> List[Dict]:
     """Append each sequence's R new tokens, then run every row.
 
     k_new/v_new [n_seq*R, Hkv, D], idx_new [n_seq*R, d_I], q_idx
@@ -393,5 +476,5 @@ def step(states: List[SeqState], pos0: List[int], k_new, v_new, idx_new,
     for i, st in enumerate(states):
         for j in range(R):
             row = i * R + j
-            out.append(attend_row(st, pos0[i] + j, q_idx[row], w[row], q[row], topk))
+            out.append(attend_row(st, pos0[i] + j, q_idx[row], w[row], q[row], topk, index_format))
     return out

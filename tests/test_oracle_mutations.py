@@ -128,6 +128,46 @@ class StickyRewind(O.SeqState):
         # bug: forgets to move the counter
 
 
+def e4m3_truncating(v):
+    v = np.asarray(v, np.float64)
+    a = np.minimum(np.abs(v), O.E4M3_MAX)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))
+    q = np.ldexp(1.0, np.maximum(e - 1, -6) - 3)
+    return np.copysign(np.floor(a / q) * q, v)
+
+
+def e4m3_wrong_subnormal_quantum(v):
+    v = np.asarray(v, np.float64)
+    a = np.minimum(np.abs(v), O.E4M3_MAX)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))
+    q = np.ldexp(1.0, np.maximum(e - 1, -7) - 3)
+    return np.copysign(np.minimum(np.rint(a / q) * q, O.E4M3_MAX), v)
+
+
+def mxfp8_emax_7(x):
+    x = np.asarray(x, np.float64)
+    b = x.reshape(x.shape[:-1] + (-1, 32))
+    amax = np.abs(b).max(axis=-1)
+    _, e = np.frexp(np.where(amax > 0, amax, 1.0))
+    exp = np.where(amax > 0, e - 1 - 7, -127).astype(np.int64)
+    return O.e4m3_round(b / np.ldexp(1.0, exp)[..., None]).reshape(x.shape), exp
+
+
+def mxfp8_one_scale_per_vector(x):
+    x = np.asarray(x, np.float64)
+    amax = np.abs(x).max(axis=-1, keepdims=True)
+    _, e = np.frexp(np.where(amax > 0, amax, 1.0))
+    exp = np.where(amax > 0, e - 1 - 8, -127).astype(np.int64)
+    n = x.shape[-1] // 32
+    return O.e4m3_round(x / np.ldexp(1.0, exp)), np.repeat(exp, n, axis=-1)
+
+
+def mxfp8_scores_keys_only(q_idx_bits, w, blk_bits):
+    q = O.bf16_bits_to_f64(q_idx_bits)
+    k = O.mxfp8_round_bits(blk_bits)
+    return np.asarray(w, np.float64) @ np.maximum(q @ k.T, 0.0)
+
+
 MUTATIONS = [
     ("block_scores", no_relu, [P.test_score_closed_forms]),
     ("block_scores", relu_outside, [P.test_score_closed_forms]),
@@ -144,6 +184,11 @@ MUTATIONS = [
     ("pool_block_pre", pool_pre_rope_then_norm, [P.test_pre_indexed_blocks_norm_then_rope_at_the_first_position]),
     ("pool_block_pre", pool_pre_at_last_position, [P.test_pre_indexed_blocks_norm_then_rope_at_the_first_position]),
     ("gemma_rmsnorm", norm_without_unit_offset, [P.test_gemma_rmsnorm_closed_forms]),
+    ("e4m3_round", e4m3_truncating, [P.test_e4m3_rounding_is_nearest_even_by_brute_force]),
+    ("e4m3_round", e4m3_wrong_subnormal_quantum, [P.test_e4m3_grid_from_the_format_definition]),
+    ("mxfp8_quantize", mxfp8_emax_7, [P.test_mxfp8_scale_rule_on_hand_worked_blocks]),
+    ("mxfp8_quantize", mxfp8_one_scale_per_vector, [P.test_mxfp8_scales_are_per_32_value_block]),
+    ("block_scores_mxfp8", mxfp8_scores_keys_only, [P.test_mxfp8_scores_hand_worked_and_identity_on_small_integers]),
 ]
 
 

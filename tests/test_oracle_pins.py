@@ -523,3 +523,125 @@ def test_verify_rows_are_causal():
         res = O.attend_row(st, 38 + j, qi, w, q, 4)
         assert res["tokens"].max() == 38 + j
         assert res["n_blk"] == (38 + j + 1) // 4
+
+
+# ---------------------------------------------------------------------------
+# MXFP8 index plane. The format is the OCP Microscaling (MX v1.0) MXFP8: E4M3
+# elements, one E8M0 scale per 32 values. The pins decode E4M3 from its bit
+# definition, compare rounding with brute force and with torch's float8_e4m3fn
+# cast, and check the scale rule on hand-worked blocks.
+# ---------------------------------------------------------------------------
+
+
+def e4m3_table():
+    """Every finite non-negative E4M3 value, in code order 0x00 .. 0x7E, decoded
+    from the bit fields: sign | 4-bit exponent (bias 7) | 3-bit mantissa;
+    exponent field 0 is subnormal (m/8 * 2^-6); 0x7F is NaN."""
+    vals = []
+    for code in range(0x7F):
+        e, m = code >> 3, code & 7
+        vals.append(m / 8 * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    return np.array(vals)
+
+
+def test_e4m3_grid_from_the_format_definition():
+    t = e4m3_table()
+    assert np.all(np.diff(t) > 0)                       # codes are ordered by magnitude
+    assert t[-1] == 448.0 and t[1] == 2.0 ** -9
+    assert O.E4M3_MAX == 448.0
+    # every grid point, either sign, is a fixed point of the rounding
+    assert np.array_equal(O.e4m3_round(t), t)
+    assert np.array_equal(O.e4m3_round(-t[1:]), -t[1:])
+    # and nothing between two adjacent grid points is on the grid
+    mids = (t[1:] + t[:-1]) / 2
+    assert not np.any(O.e4m3_round(mids) == mids)
+
+
+def test_e4m3_rounding_is_nearest_even_by_brute_force():
+    t = e4m3_table()
+    rng = np.random.default_rng(53)
+    mags = np.exp2(rng.uniform(-12, 9.6, 4000))         # past 448 too
+    mids = (t[1:] + t[:-1]) / 2                         # exact halfway points
+    v = np.concatenate([mags, -mags, mids, -mids, [0.0, 448.0, 460.0, 464.0, 1e6]])
+    got = O.e4m3_round(v)
+    a = np.minimum(np.abs(v), 448.0)
+    d = np.abs(a[:, None] - t[None, :])
+    best = d.min(axis=1, keepdims=True)
+    cand = d == best
+    # ties: the code with an even mantissa (even code index)
+    idx = np.where(cand.sum(axis=1) > 1, np.argmax(cand & (np.arange(len(t)) % 2 == 0)[None, :], axis=1),
+                   np.argmax(cand, axis=1))
+    want = np.copysign(t[idx], v)
+    assert np.array_equal(np.abs(got), np.abs(want))
+    assert np.all((got == 0) | (np.sign(got) == np.sign(v)))
+
+
+def test_e4m3_rounding_matches_torch_float8():
+    rng = np.random.default_rng(59)
+    v = np.concatenate([rng.standard_normal(3000) * 40, np.exp2(rng.uniform(-11, 8.8, 3000))])
+    v = O.bf16_bits_to_f64(bf16(v))                     # bf16 values (exact in fp32)
+    v = v[np.abs(v) <= 448.0]
+    lib = torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(O.e4m3_round(v), lib)
+
+
+def test_mxfp8_scale_rule_on_hand_worked_blocks():
+    # amax 3 -> floor(log2 3) = 1 -> scale 2^(1-8) = 2^-7: 3*128 = 384 and
+    # -1.5*128 = -192 are on the grid; 0.1*128 = 12.8 lies in [8, 16) where the
+    # quantum is 1, so it becomes 13, i.e. 13/128 = 0.1015625
+    x = np.zeros(32); x[:3] = [3.0, -1.5, 0.1]
+    el, ex = O.mxfp8_quantize(x)
+    assert ex.tolist() == [-7]
+    assert el[:3].tolist() == [384.0, -192.0, 13.0] and not el[3:].any()
+    assert O.mxfp8_dequantize(el, ex)[:3].tolist() == [3.0, -1.5, 0.1015625]
+    # amax a power of two lands on 256; amax 1.99 -> 509.4 past 448 is clamped
+    y = np.zeros(32); y[0] = 4.0; y[1] = 1.0
+    el, ex = O.mxfp8_quantize(y)
+    assert ex.tolist() == [-6] and el[0] == 256.0 and el[1] == 64.0
+    z = np.zeros(32); z[5] = -1.99
+    el, ex = O.mxfp8_quantize(z)
+    assert ex.tolist() == [-8] and el[5] == -448.0
+    assert O.mxfp8_dequantize(el, ex)[5] == -1.75
+    # an all-zero block takes the smallest scale, 2^-127
+    el, ex = O.mxfp8_quantize(np.zeros(32))
+    assert ex.tolist() == [-127] and not el.any()
+
+
+def test_mxfp8_scales_are_per_32_value_block():
+    rng = np.random.default_rng(61)
+    x = rng.standard_normal((5, 128)) * np.array([1e-3, 1.0, 50.0, 3e3])[None, :].repeat(32, axis=1)
+    el, ex = O.mxfp8_quantize(x)
+    assert ex.shape == (5, 4)
+    for c in range(4):
+        blk = x[:, 32 * c:32 * (c + 1)]
+        amax = np.abs(blk).max(axis=1)
+        ratio = amax / np.exp2(ex[:, c])
+        assert np.all((ratio >= 256) & (ratio < 512))   # amax / scale in [256, 512)
+        e1, x1 = O.mxfp8_quantize(blk)
+        assert np.array_equal(e1, el[:, 32 * c:32 * (c + 1)]) and np.array_equal(x1[:, 0], ex[:, c])
+    # error: at most half an E4M3 quantum of the element's binade (unclamped), and idempotent
+    back = O.mxfp8_dequantize(el, ex)
+    scaled = np.abs(x) / np.repeat(np.exp2(ex), 32, axis=1)
+    lead = np.maximum(np.floor(np.log2(np.maximum(scaled, 2.0 ** -30))), -6)
+    half_q = np.exp2(lead - 4) * np.repeat(np.exp2(ex), 32, axis=1)
+    ok = scaled <= 448
+    assert np.all(np.abs(back - x)[ok] <= half_q[ok])
+    el2, ex2 = O.mxfp8_quantize(back)
+    assert np.array_equal(O.mxfp8_dequantize(el2, ex2), back)
+
+
+def test_mxfp8_scores_hand_worked_and_identity_on_small_integers():
+    # one 32-value block, one head, w = 1: q = (3, 0.1, 0, ...) -> (3, 0.1015625, ...)
+    # (first hand-worked block above); k = (1, 1, 0, ...) is on its grid (amax 1 ->
+    # scale 2^-8, 256 and 256). Score = 3 + 0.1015625.
+    q = np.zeros((1, 32)); q[0, :2] = [3.0, 0.1]
+    k = np.zeros((1, 32)); k[0, :2] = [1.0, 1.0]
+    s = O.block_scores_mxfp8(bf16(q), np.ones(1), bf16(k))
+    assert s.tolist() == [3.1015625]
+    # the synthetic recipe's integer queries in [-8, 8] are exact in MXFP8, so
+    # with keys of small integers the MXFP8 score is the bf16 score
+    rng = np.random.default_rng(67)
+    qi = bf16(rng.integers(-8, 9, size=(6, 64)))
+    kb = bf16(rng.integers(-8, 9, size=(20, 64)))
+    w = rng.standard_normal(6)
+    assert np.array_equal(O.block_scores_mxfp8(qi, w, kb), O.block_scores(qi, w, kb))
