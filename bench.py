@@ -61,6 +61,8 @@ def parse():
                     help="decode steps with a reused selection (MTP draft steps); 0 skips the leg")
     ap.add_argument("--pre-steps", type=int, default=300,
                     help="decode steps through the pre-indexer (norm + RoPE of queries and keys); 0 skips")
+    ap.add_argument("--mxfp8-steps", type=int, default=600,
+                    help="decode steps with the MXFP8 index plane (own cache); 0 skips")
     ap.add_argument("--prefill-warmup", type=int, default=3)
     return ap.parse_args()
 
@@ -78,12 +80,13 @@ def measured_peaks():
 # algorithmic bytes / flops (per row), from the method's definition
 # ---------------------------------------------------------------------------
 
-def row_work(sh, visible):
+def row_work(sh, visible, mxfp8=False):
     n_blk = visible // sh.ratio
     tail = visible - n_blk * sh.ratio
     active = n_blk > sh.topk
     n_tok = min(n_blk, sh.topk) * sh.ratio + tail
-    score_b = (n_blk * sh.idx_dim * 2 + sh.n_idx_heads * sh.idx_dim * 2 + 4 * sh.n_idx_heads) if active else 0
+    key_b = sh.idx_dim + sh.idx_dim // 32 if mxfp8 else sh.idx_dim * 2  # per compressed key
+    score_b = (n_blk * key_b + sh.n_idx_heads * sh.idx_dim * 2 + 4 * sh.n_idx_heads) if active else 0
     attn_b = n_tok * sh.n_kv_heads * sh.head_dim * 2 * 2 + 2 * sh.n_q_heads * sh.head_dim * 2
     append_b = (2 * sh.n_kv_heads * sh.head_dim + sh.idx_dim) * 2
     score_f = 2 * sh.n_idx_heads * sh.idx_dim * n_blk if active else 0
@@ -92,10 +95,10 @@ def row_work(sh, visible):
                 score_flops=score_f, attn_flops=attn_f, n_tok=n_tok, n_blk=n_blk)
 
 
-def sum_work(sh, visibles):
+def sum_work(sh, visibles, mxfp8=False):
     tot = {}
     for v in visibles:
-        for k, x in row_work(sh, v).items():
+        for k, x in row_work(sh, v, mxfp8).items():
             tot[k] = tot.get(k, 0) + x
     return tot
 
@@ -207,7 +210,8 @@ def run_gpu(args):
     K, W = args.steps, args.warmup
     total_steps = W + K + args.breakdown_steps + args.e2e_steps + 4
     adv_per_batch = (math.ceil((W + K + min(K, 600) + args.e2e_steps + 4) / NB) + (62 if args.reuse_steps > 0 else 0)
-                     + (math.ceil(args.pre_steps / NB) + 2 if args.pre_steps > 0 else 0))
+                     + (math.ceil(args.pre_steps / NB) + 2 if args.pre_steps > 0 else 0)
+                     + (math.ceil(args.mxfp8_steps / NB) + 2 if args.mxfp8_steps > 0 else 0))
     # center the prefixes of the main timed region on 32768
     start = wl.prefixes[0] - W // NB - K // (2 * NB)
     start = max(start, 8)
@@ -369,7 +373,67 @@ def run_gpu(args):
     if args.pre_steps > 0:
         out["pre_indexer"] = run_pre(args, Q, S, torch, cfg, sh, cache, batches, status, stream, NB, B, hbm_gbs,
                                      ms)
+    if args.mxfp8_steps > 0:
+        out["mxfp8"] = run_mxfp8(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, NB, B,
+                                 hbm_gbs, ms)
     return out, rank, world
+
+
+def run_mxfp8(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, NB, B, hbm_gbs, ms_plain):
+    """The same decode workload with the MXFP8 index plane (index_format
+    QSA_INDEX_MXFP8): compressed keys stored as E4M3 + E8M0 scales (132 bytes per
+    key instead of 256), index queries MXFP8-rounded inside the step. Its own
+    cache, filled through qsa_append with the same prefixes; the same step
+    inputs; one rotation graph of the NB batches, timed with CUDA events."""
+    dev = batches[0]["k"].device
+    cfg8 = Q.Config.of(sh, Q.QSA_INDEX_MXFP8)
+    n_slots = B * NB
+    cache8 = Q.PagedCache(cfg8, pt, n_slots * max_pages, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    chunk = 8192
+    for s_ in range(n_slots):
+        a = 0
+        while a < start:
+            m = min(chunk, start - a)
+            k, v, ix = S.token_rows(sh, wl.seed, s_, torch.arange(a, a + m), device=dev)
+            Q.qsa_append(cfg8, Q.Rows(torch.tensor([s_], device=dev), torch.tensor([a], device=dev,
+                                                                                 dtype=torch.int32), m),
+                         cache8, k, v, ix, status)
+            a += m
+    ws8 = Q.workspace(cfg8, B, cache8.max_blocks, device=dev)
+    pos8 = [torch.full((B,), start, dtype=torch.int32, device=dev) for _ in range(NB)]
+    rot = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(rot, stream=stream):
+        for b, bt in enumerate(batches):
+            Q.qsa_decode(cfg8, Q.Rows(bt["ids"], pos8[b], 1, advance=True), cache8, bt["k"], bt["v"], bt["idx"],
+                         bt["q_idx"], bt["w"], bt["q"], bt["out"], ws8, status, stream=stream)
+    torch.cuda.synchronize()
+    n_rot = max(1, math.ceil(args.mxfp8_steps / NB))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        rot.replay()  # warm-up rotation
+        e0.record(stream)
+        for _ in range(n_rot):
+            rot.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st == 0, f"device status {st}: {Q.qsa_strerror(st)}"
+    steps = n_rot * NB
+    ms = e0.elapsed_time(e1) / steps
+    # timed rows: every batch at positions start + 1 .. start + n_rot (one warm-up step each before)
+    visibles = [start + 1 + r + 1 for r in range(1, n_rot + 1) for _ in range(NB) for _ in range(B)]
+    work = sum_work(sh, visibles, mxfp8=True)
+    step_bytes = (work["score_bytes"] + work["attn_bytes"] + work["append_bytes"]) / steps
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    del cache8
+    return {"what": "the decode workload (batch 32 x 32k) with the MXFP8 index plane: compressed keys as "
+                    "E4M3 + one E8M0 scale per 32 values, index queries MXFP8-rounded in the step",
+            "steps": steps, "ms_per_step": round(ms, 5), "rows_per_s": round(B / (ms * 1e-3), 1),
+            "speedup_vs_bf16_plane": round(ms_plain / ms, 3), "bytes_per_step": int(step_bytes),
+            "achieved_gbs": round(gbs, 1), "hbm_roofline_frac": round(gbs / hbm_gbs, 4),
+            "bytes": "MXFP8 keys (d_I + d_I/32 per block), bf16 q_idx, w, K+V of the selected tokens, q, o, appends"}
 
 
 def run_pre(args, Q, S, torch, cfg, sh, cache, batches, status, stream, NB, B, hbm_gbs, ms_plain):

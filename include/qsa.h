@@ -87,7 +87,24 @@ typedef enum qsa_status {
  *              Hq / Hkv <= 8                    GQA
  *   head_dim   (D) 128
  *   page_size  (P) 64, multiple of ratio        tokens per cache page
- * The indexer has one key head (MQA), as the pages require. */
+ *   index_format QSA_INDEX_BF16 or QSA_INDEX_MXFP8 (the latter with
+ *              P / ratio >= 8 blocks per page)  compressed-key plane
+ * The indexer has one key head (MQA), as the pages require.
+ *
+ * Index formats. QSA_INDEX_BF16: compressed keys are bf16 and the index
+ * queries are scored as given. QSA_INDEX_MXFP8 ("Agentic shootout", "Flash-Next
+ * support: vLLM vs Atlas", the report whose (a) item 3 is "QSA sparse
+ * attention + n-gram indexer", Scores bullet: MXFP8 quantisation of the index
+ * queries and of the indexer cache; "ATOM Model Support Guide", DeepSeek-V4.1,
+ * Cache bullet: an fp8 index plane with E8M0 scales): every compressed key is
+ * stored as OCP MXFP8 -- per 32 consecutive values one E8M0 scale
+ * 2^(floor(log2 amax) - 8) (2^-127 for an all-zero block) and E4M3 elements,
+ * value / scale rounded to nearest-even and clamped to +-448 -- and the fused
+ * step puts each index query head through the same quantisation before
+ * scoring. The key quantised is the bf16 compressed key of QSA_INDEX_BF16;
+ * scores are exact sums of the quantised values' products in fp32. */
+#define QSA_INDEX_BF16 0
+#define QSA_INDEX_MXFP8 1
 typedef struct qsa_config {
   int ratio;
   int budget;
@@ -97,6 +114,7 @@ typedef struct qsa_config {
   int n_kv_heads;
   int head_dim;
   int page_size;
+  int index_format; /* QSA_INDEX_BF16 (0) or QSA_INDEX_MXFP8 (1) */
 } qsa_config;
 
 /* The query rows of one step. The step appends rows_per_seq (R) tokens to
@@ -140,7 +158,14 @@ typedef struct qsa_rows {
  *     ((rr / G) * (d_I / 8) + d / 8) * 8 * G + (rr % G) * 8 + d % 8
  * (the tensor cores' K-major core-matrix order), so one contiguous copy of a
  * page is a ready operand of the scoring contraction. The block pool is
- * written only by qsa_append and read only by qsa_index_score / qsa_decode. */
+ * written only by qsa_append and read only by qsa_index_score / qsa_decode.
+ *
+ * With QSA_INDEX_MXFP8 a block-pool page is qsa_idxblk_page_bytes() =
+ * bpp * (d_I + d_I/32) bytes (bpp = P/ratio blocks): first the E4M3 elements,
+ * element (rr, d) at byte
+ *     ((rr / 8) * (d_I / 16) + d / 16) * 128 + (rr % 8) * 16 + d % 16
+ * (core matrices of 8 blocks x 16 bytes), then the E8M0 scale bytes, scale
+ * (rr, c) of values 32c .. 32c+31 at byte bpp * d_I + rr * (d_I / 32) + c. */
 typedef struct qsa_cache {
   const int32_t *page_table; /* device [n_slots, max_pages] */
   int n_slots;
@@ -149,7 +174,8 @@ typedef struct qsa_cache {
   qsa_bf16 *k_pool;          /* device [num_pages, P, Hkv, D] */
   qsa_bf16 *v_pool;          /* device [num_pages, P, Hkv, D] */
   qsa_bf16 *idxraw_pool;     /* device [num_pages, P, d_I]   raw index keys */
-  qsa_bf16 *idxblk_pool;     /* device [num_pages, P/ratio * d_I] block keys (tiled, above) */
+  void *idxblk_pool;         /* device block keys (tiled, above): bf16 [num_pages, P/ratio * d_I],
+                                or with QSA_INDEX_MXFP8 bytes [num_pages, qsa_idxblk_page_bytes()] */
   int32_t *ingested;         /* device [n_slots]: tokens ingested per slot */
 } qsa_cache;
 
@@ -159,6 +185,11 @@ const char *qsa_strerror(int status);
 /* 0 (QSA_OK) if the configuration is in the supported set above, else
  * QSA_ERR_UNSUPPORTED (QSA_ERR_INVALID_ARG for a NULL pointer). */
 int qsa_config_check(const qsa_config *cfg);
+
+/* Bytes of one block-pool page for the configuration's index format
+ * (P/ratio * d_I * 2 for bf16, P/ratio * (d_I + d_I/32) for MXFP8); 0 on an
+ * invalid configuration. */
+size_t qsa_idxblk_page_bytes(const qsa_config *cfg);
 
 /* Bytes of workspace that qsa_decode and qsa_gather_attn need for up to
  * max_rows query rows and up to max_blocks_per_row complete blocks per row
@@ -195,7 +226,10 @@ int qsa_rewind(const qsa_config *cfg, int n_seq, const int32_t *seq_ids, const i
  * for every row with n_blk = V / ratio > K complete blocks, writes
  * scores[row * ld_scores + b] = sum_h w[row,h] * max(0, q_idx[row,h,:] . k_b)
  * for b < n_blk (bf16 products, fp32 accumulation). Rows with n_blk <= K are
- * skipped: every block is selected there, so no score is needed.
+ * skipped: every block is selected there, so no score is needed. With
+ * QSA_INDEX_MXFP8 the keys are the MXFP8 plane's values and the queries are
+ * scored as given: pass them through qsa_quantize_index_q first for the
+ * MXFP8 x MXFP8 score of the fused step.
  *   q_idx   device [rows, H_I, d_I] bf16
  *   w       device [rows, H_I] fp32
  *   scores  device [rows, ld_scores] fp32; ld_scores >= max_pages*P/ratio,
@@ -205,6 +239,13 @@ int qsa_rewind(const qsa_config *cfg, int n_seq, const int32_t *seq_ids, const i
 int qsa_index_score(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
                     const qsa_bf16 *q_idx, const float *w, float *scores, int ld_scores,
                     int32_t *status, cudaStream_t stream);
+
+/* MXFP8 round trip of index query heads (the query side of QSA_INDEX_MXFP8):
+ * each d_I vector's blocks of 32 values are quantised as the keys are and
+ * written back as bf16 (every MXFP8 value is exact in bf16).
+ *   q_idx, q_out  device [n_rows, H_I, d_I] bf16 (q_out == q_idx allowed) */
+int qsa_quantize_index_q(const qsa_config *cfg, int n_rows, const qsa_bf16 *q_idx, qsa_bf16 *q_out,
+                         cudaStream_t stream);
 
 /* Top-K select ([VA6] block top-k; ties to the lower block index): for every
  * row, if n_blk <= K all blocks are selected; otherwise the K blocks with
@@ -240,7 +281,9 @@ int qsa_gather_attn(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache
  *   sel_out, n_sel_out  optional device [rows, K] / [rows] int32 (NULL: kept
  *                       in the workspace)
  *   ws                  device workspace, ws_bytes >=
- *                       qsa_workspace_bytes(cfg, rows, max_pages*P/ratio) */
+ *                       qsa_workspace_bytes(cfg, rows, max_pages*P/ratio)
+ * With QSA_INDEX_MXFP8 the step quantises the index queries (as
+ * qsa_quantize_index_q, into the workspace) before scoring. */
 int qsa_decode(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
                const qsa_bf16 *k_new, const qsa_bf16 *v_new, const qsa_bf16 *idx_k_new,
                const qsa_bf16 *q_idx, const float *w, const qsa_bf16 *q,
@@ -268,14 +311,16 @@ typedef struct qsa_pre_indexer {
 } qsa_pre_indexer;
 
 /* qsa_append whose completed blocks go through the pre-indexer:
- * k_b = bf16(RoPE_{b*ratio}(GemmaRMSNorm(mean of the block's raw keys))).
+ * k_b = bf16(RoPE_{b*ratio}(GemmaRMSNorm(mean of the block's raw keys)))
+ * (then MXFP8-quantised with QSA_INDEX_MXFP8).
  * A cache must be filled with one kind of append throughout. */
 int qsa_append_pre(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_rows *rows,
                    const qsa_cache *cache, const qsa_bf16 *k_new, const qsa_bf16 *v_new,
                    const qsa_bf16 *idx_k_new, int32_t *status, cudaStream_t stream);
 
 /* The index queries of the rows through the pre-indexer:
- * q_out[row, h] = bf16(RoPE_{row position}(GemmaRMSNorm(q_idx[row, h]))).
+ * q_out[row, h] = bf16(RoPE_{row position}(GemmaRMSNorm(q_idx[row, h]))),
+ * then, with QSA_INDEX_MXFP8, the MXFP8 round trip of qsa_quantize_index_q.
  *   q_idx, q_out  device [rows, H_I, d_I] bf16, distinct buffers */
 int qsa_pre_index_q(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_rows *rows,
                     const qsa_bf16 *q_idx, qsa_bf16 *q_out, cudaStream_t stream);

@@ -36,6 +36,9 @@ int check_cfg(const qsa_config *c) {
   if (c->n_q_heads < c->n_kv_heads || c->n_q_heads % c->n_kv_heads != 0) return QSA_ERR_UNSUPPORTED;
   if (c->n_q_heads / c->n_kv_heads > 8) return QSA_ERR_UNSUPPORTED;
   if (c->page_size != 64 || c->page_size % c->ratio != 0) return QSA_ERR_UNSUPPORTED;
+  if (c->index_format != QSA_INDEX_BF16 && c->index_format != QSA_INDEX_MXFP8) return QSA_ERR_UNSUPPORTED;
+  // the MXFP8 plane is scored on the tensor-core path: 8 or more blocks per page
+  if (c->index_format == QSA_INDEX_MXFP8 && c->page_size / c->ratio < 8) return QSA_ERR_UNSUPPORTED;
   return QSA_OK;
 }
 
@@ -52,6 +55,7 @@ Shape make_shape(const qsa_config *c) {
   s.page = c->page_size;
   s.log2_ratio = ilog2(c->ratio);
   s.log2_page = ilog2(c->page_size);
+  s.idx_fp8 = c->index_format == QSA_INDEX_MXFP8 ? 1 : 0;
   return s;
 }
 
@@ -195,25 +199,30 @@ int decode_impl(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_row
   const int cap_tokens = cache->max_pages * cfg->page_size;
   const int ld = ld_for(cap_tokens / cfg->ratio);
   const WsLayout L = ws_layout(sh, n_rows, ld);
-  const size_t need = L.total + (pre ? round_up(q_prep_bytes(sh, n_rows), 256) : 0);
+  // the step's index queries are prepared into the workspace (pre-indexer and / or
+  // MXFP8 round trip) by the append kernel, and the score kernel reads them there
+  const bool q_prep = pre != nullptr || sh.idx_fp8;
+  const size_t need = L.total + (q_prep ? round_up(q_prep_bytes(sh, n_rows), 256) : 0);
   if (ws_bytes < need) return QSA_ERR_WORKSPACE;
   uint8_t *base = static_cast<uint8_t *>(ws);
   float *scores = reinterpret_cast<float *>(base + L.scores);
   int32_t *sel = sel_out ? sel_out : reinterpret_cast<int32_t *>(base + L.sel);
   int32_t *n_sel = n_sel_out ? n_sel_out : reinterpret_cast<int32_t *>(base + L.n_sel);
-  uint16_t *q_pre = pre ? reinterpret_cast<uint16_t *>(base + L.total) : nullptr;
+  uint16_t *q_pre = q_prep ? reinterpret_cast<uint16_t *>(base + L.total) : nullptr;
   const CacheView cv = view(cache);
   const int R = rows->rows_per_seq;
 
   PreArgs pa;
   if (pre) pa = pre_args(pre, q_idx, q_pre);
+  pa.q_in = q_prep ? q_idx : nullptr;
+  pa.q_out = q_pre;
   cudaError_t e = launch_append(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cache->page_table,
                                 cache->max_pages, cache->num_pages, cache->k_pool, cache->v_pool,
                                 cache->idxraw_pool, cache->idxblk_pool, cache->ingested, k_new,
-                                v_new, idx_k_new, status, true, stream, pre ? &pa : nullptr);
+                                v_new, idx_k_new, status, true, stream, &pa);
   if (e == cudaSuccess)
-    e = launch_score(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, pre ? q_pre : q_idx, w, scores, ld,
-                     status, true, stream, pre != nullptr);
+    e = launch_score(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, q_prep ? q_pre : q_idx, w, scores, ld,
+                     status, true, stream, q_prep);
   if (e == cudaSuccess)
     e = launch_select(sh, rows->n_seq, R, rows->pos0, scores, ld, sel, n_sel, ld, cap_tokens,
                       status, true, stream);
@@ -259,6 +268,26 @@ const char *qsa_strerror(int status) {
 
 int qsa_config_check(const qsa_config *cfg) { return check_cfg(cfg); }
 
+size_t qsa_idxblk_page_bytes(const qsa_config *cfg) {
+  if (check_cfg(cfg) != QSA_OK) return 0;
+  const int bpp = cfg->page_size / cfg->ratio;
+  return cfg->index_format == QSA_INDEX_MXFP8 ? static_cast<size_t>(fp8_page_bytes(bpp, cfg->idx_dim))
+                                              : static_cast<size_t>(bpp) * cfg->idx_dim * sizeof(uint16_t);
+}
+
+int qsa_quantize_index_q(const qsa_config *cfg, int n_rows, const qsa_bf16 *q_idx, qsa_bf16 *q_out,
+                         cudaStream_t stream) {
+  int rc;
+  if ((rc = check_cfg(cfg)) != QSA_OK) return rc;
+  if (n_rows < 0) return QSA_ERR_INVALID_ARG;
+  if (n_rows == 0) return QSA_OK;
+  if (!q_idx || !q_out) return QSA_ERR_INVALID_ARG;
+  Shape sh = make_shape(cfg);
+  sh.idx_fp8 = 1;  // the MXFP8 round trip whatever the cache's format
+  PreArgs pa;      // no pre-indexer: no gains, no positions
+  return cuda_status(launch_pre_index_q(sh, n_rows, 1, nullptr, pa, q_idx, q_out, false, stream));
+}
+
 int qsa_max_attend_tokens(const qsa_config *cfg) {
   if (check_cfg(cfg) != QSA_OK) return 0;
   return attn_max_tokens(make_shape(cfg));
@@ -267,7 +296,9 @@ int qsa_max_attend_tokens(const qsa_config *cfg) {
 size_t qsa_workspace_bytes(const qsa_config *cfg, int max_rows, int max_blocks_per_row) {
   if (check_cfg(cfg) != QSA_OK || max_rows < 0 || max_blocks_per_row < 0) return 0;
   const Shape sh = make_shape(cfg);
-  return ws_layout(sh, max_rows, ld_for(max_blocks_per_row)).total;
+  // with the MXFP8 plane the fused step also holds its MXFP8-rounded index queries
+  return ws_layout(sh, max_rows, ld_for(max_blocks_per_row)).total +
+         (sh.idx_fp8 ? round_up(q_prep_bytes(sh, max_rows), 256) : 0);
 }
 
 int qsa_append(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,

@@ -10,6 +10,8 @@
 // pre-append value ("Atlas Flash-Next defect investigations", Report A,
 // Defect 1: decode at pos requires pos == ingested; rewind subtracts the
 // dropped tokens).
+#include <cuda_fp16.h>
+
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -59,10 +61,51 @@ __device__ __forceinline__ void pre_index_lanes(float (&x)[D32], const float *__
   }
 }
 
-// The query vectors (row, index head) of sequence i: RoPE(GemmaRMSNorm) into
-// q_out, one warp per vector. Vector v is row i*R + v / h_idx at position
-// p0 + v / h_idx, head v % h_idx; a CTA takes vectors slot*8 + warp, striding by
-// n_slots*8, so a decode step's 64 heads spread over 8 CTAs.
+// ---- MXFP8 (OCP MX v1.0: E4M3 elements, one E8M0 scale per 32 values) ----
+
+// Scale exponent of a block with largest magnitude amax: floor(log2 amax) - 8
+// (8: exponent of E4M3's top binade), at least -127; -127 when amax is zero or
+// below 2^-126. Read off amax's exponent field.
+__device__ __forceinline__ int mx_scale_exp(float amax) {
+  const int biased = static_cast<int>(__float_as_uint(amax) >> 23);
+  return biased == 0 ? -127 : max(biased - 127 - 8, -127);
+}
+
+// E4M3 code of v: nearest-even, magnitudes past 448 saturate to 448.
+__device__ __forceinline__ uint32_t e4m3_code(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(v));
+  return r & 0xFFu;
+}
+
+// Value of an E4M3 code (exact in f16, then fp32).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(code)));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// One warp holding a d_I vector as lane L: dims L + 32m, so register m across
+// the warp is exactly MX block m. x must already be bf16 values. Returns each
+// lane's codes and every block's scale exponent.
+template <int D32>
+__device__ __forceinline__ void mx_quantize_lanes(const float (&x)[D32], uint32_t (&code)[D32], int (&ex)[D32]) {
+#pragma unroll
+  for (int m = 0; m < D32; ++m) {
+    const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(x[m]))));
+    ex[m] = mx_scale_exp(amax);
+    code[m] = e4m3_code(x[m] * exp2_int(-ex[m]));  // exact power-of-two scaling
+  }
+}
+
+// bf16 value of x (round to nearest even) as fp32.
+__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// The query vectors (row, index head) of sequence i into q_out, one warp per
+// vector: RoPE(GemmaRMSNorm) when pre.gamma_q is set, rounded to bf16, then
+// with the MXFP8 plane the MXFP8 round trip. Vector v is row i*R + v / h_idx at
+// position p0 + v / h_idx, head v % h_idx; a CTA takes vectors slot*8 + warp,
+// striding by n_slots*8, so a decode step's 64 heads spread over 8 CTAs.
 template <int D32>
 __device__ void pre_index_queries(const Shape &sh, const PreArgs &pre, int i, int R, int p0, int slot,
                                   int n_slots) {
@@ -74,8 +117,19 @@ __device__ void pre_index_queries(const Shape &sh, const PreArgs &pre, int i, in
     float x[D32];
 #pragma unroll
     for (int m = 0; m < D32; ++m) x[m] = bf16_bits_to_float(pre.q_in[base + lane + 32 * m]);
-    pre_index_lanes<D32>(x, pre.gamma_q, pre.eps, pre.rot, sh.d_idx, lane,
-                         [&](int ip) { return rope_cs(p0 + t, ip, pre); });
+    if (pre.gamma_q) {
+      pre_index_lanes<D32>(x, pre.gamma_q, pre.eps, pre.rot, sh.d_idx, lane,
+                           [&](int ip) { return rope_cs(p0 + t, ip, pre); });
+#pragma unroll
+      for (int m = 0; m < D32; ++m) x[m] = round_bf16(x[m]);
+    }
+    if (sh.idx_fp8) {
+      uint32_t code[D32];
+      int ex[D32];
+      mx_quantize_lanes<D32>(x, code, ex);
+#pragma unroll
+      for (int m = 0; m < D32; ++m) x[m] = e4m3_value(code[m]) * exp2_int(ex[m]);  // exact in bf16
+    }
 #pragma unroll
     for (int m = 0; m < D32; ++m) {
       const __nv_bfloat16 h = __float2bfloat16_rn(x[m]);
@@ -92,14 +146,16 @@ int q_prep_ctas(const Shape &sh, int n_seq, int R) {
   return static_cast<int>(want < cap ? want : cap);
 }
 
-// One warp: the compressed key of block b through the pre-indexer. Raw keys are
-// summed in position order in fp32 (as in the plain pooling), then scaled by 1/r.
+// One warp: the compressed key of block b. Raw keys are summed in position
+// order in fp32 (as in the plain pooling), then scaled by 1/r; through the
+// pre-indexer when pre.gamma_k is set; rounded to bf16; stored as bf16 tiles or,
+// with the MXFP8 plane, quantised into it.
 template <int D32>
-__device__ void pool_block_pre(const Shape &sh, const PreArgs &pre, int b, int i, int R, int p0,
-                               const int32_t *__restrict__ ptab, int num_pages,
-                               const uint16_t *__restrict__ raw_pool, uint16_t *__restrict__ blk_pool,
-                               const uint16_t *__restrict__ idx_new, float inv_r, int bpp, int lane,
-                               int32_t *status) {
+__device__ void pool_block_warp(const Shape &sh, const PreArgs &pre, int b, int i, int R, int p0,
+                                const int32_t *__restrict__ ptab, int num_pages,
+                                const uint16_t *__restrict__ raw_pool, void *__restrict__ blk_pool,
+                                const uint16_t *__restrict__ idx_new, float inv_r, int bpp, int lane,
+                                int32_t *status) {
   const int r = sh.ratio, P = sh.page;
   float x[D32];
 #pragma unroll
@@ -128,13 +184,31 @@ __device__ void pool_block_pre(const Shape &sh, const PreArgs &pre, int b, int i
 #pragma unroll
   for (int m = 0; m < D32; ++m) x[m] *= inv_r;
   const int first = b * r;
-  pre_index_lanes<D32>(x, pre.gamma_k, pre.eps, pre.rot, sh.d_idx, lane,
-                       [&](int ip) { return rope_cs(first, ip, pre); });
-  uint16_t *dst = blk_pool + static_cast<size_t>(page_b) * bpp * sh.d_idx;
+  if (pre.gamma_k)
+    pre_index_lanes<D32>(x, pre.gamma_k, pre.eps, pre.rot, sh.d_idx, lane,
+                         [&](int ip) { return rope_cs(first, ip, pre); });
+  const int rr = b & (bpp - 1);
+  if (sh.idx_fp8) {
+#pragma unroll
+    for (int m = 0; m < D32; ++m) x[m] = round_bf16(x[m]);
+    uint32_t code[D32];
+    int ex[D32];
+    mx_quantize_lanes<D32>(x, code, ex);
+    uint8_t *pg = static_cast<uint8_t *>(blk_pool) + static_cast<size_t>(page_b) * fp8_page_bytes(bpp, sh.d_idx);
+#pragma unroll
+    for (int m = 0; m < D32; ++m) pg[fp8_elem_offset(rr, lane + 32 * m, sh.d_idx)] = static_cast<uint8_t>(code[m]);
+    if (lane == 0) {
+#pragma unroll
+      for (int m = 0; m < D32; ++m)
+        pg[bpp * sh.d_idx + rr * (sh.d_idx / 32) + m] = static_cast<uint8_t>(ex[m] + 127);
+    }
+    return;
+  }
+  uint16_t *dst = static_cast<uint16_t *>(blk_pool) + static_cast<size_t>(page_b) * bpp * sh.d_idx;
 #pragma unroll
   for (int m = 0; m < D32; ++m) {
     const __nv_bfloat16 h = __float2bfloat16_rn(x[m]);
-    dst[blk_elem_offset(b & (bpp - 1), lane + 32 * m, bpp, sh.d_idx)] = *reinterpret_cast<const uint16_t *>(&h);
+    dst[blk_elem_offset(rr, lane + 32 * m, bpp, sh.d_idx)] = *reinterpret_cast<const uint16_t *>(&h);
   }
 }
 
@@ -143,7 +217,7 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
               const int32_t *__restrict__ pos0, const int32_t *__restrict__ page_table,
               int max_pages, int num_pages, uint16_t *__restrict__ k_pool,
               uint16_t *__restrict__ v_pool, uint16_t *__restrict__ raw_pool,
-              uint16_t *__restrict__ blk_pool, const int32_t *__restrict__ ingested,
+              void *__restrict__ blk_pool, const int32_t *__restrict__ ingested,
               const uint16_t *__restrict__ k_new, const uint16_t *__restrict__ v_new,
               const uint16_t *__restrict__ idx_new, int32_t *status, int n_chunks,
               const __grid_constant__ PreArgs pre) {
@@ -221,15 +295,16 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
   const int half = sh.d_idx / 2;
   const int bpp = P >> sh.log2_ratio;  // blocks per page
   const float inv_r = 1.0f / static_cast<float>(r);
-  if (pre.gamma_k) {
-    // one warp per block: mean-pool, Gemma RMSNorm, RoPE at the block's first position
+  if (pre.gamma_k || sh.idx_fp8) {
+    // one warp per block: mean-pool, (Gemma RMSNorm, RoPE at the block's first
+    // position), store as bf16 or into the MXFP8 plane
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
     for (int bb = warp; bb < b_hi - b_lo; bb += n_warps) {
       const int b = b_lo + bb;
       if (sh.d_idx == 128)
-        pool_block_pre<4>(sh, pre, b, i, R, p0, ptab, num_pages, raw_pool, blk_pool, idx_new, inv_r, bpp, lane, status);
+        pool_block_warp<4>(sh, pre, b, i, R, p0, ptab, num_pages, raw_pool, blk_pool, idx_new, inv_r, bpp, lane, status);
       else
-        pool_block_pre<2>(sh, pre, b, i, R, p0, ptab, num_pages, raw_pool, blk_pool, idx_new, inv_r, bpp, lane, status);
+        pool_block_warp<2>(sh, pre, b, i, R, p0, ptab, num_pages, raw_pool, blk_pool, idx_new, inv_r, bpp, lane, status);
     }
     return;
   }
@@ -261,7 +336,7 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
       continue;
     }
     // d2 is even, so (d2, d2 + 1) are adjacent in the tiled page layout
-    uint16_t *dst = blk_pool + static_cast<size_t>(page_b) * bpp * sh.d_idx +
+    uint16_t *dst = static_cast<uint16_t *>(blk_pool) + static_cast<size_t>(page_b) * bpp * sh.d_idx +
                     blk_elem_offset(b & (bpp - 1), d2, bpp, sh.d_idx);
     *reinterpret_cast<uint32_t *>(dst) = pack_bf16(s0 * inv_r, s1 * inv_r);
   }
@@ -274,7 +349,7 @@ pre_index_q_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const __gr
   pdl_wait();  // positions
   pdl_trigger();
   const int i = blockIdx.x;
-  const int p0 = pos0[i];
+  const int p0 = pos0 ? pos0[i] : 0;  // no positions: MXFP8 round trip only
   if (sh.d_idx == 128)
     pre_index_queries<4>(sh, pre, i, R, p0, blockIdx.y, gridDim.y);
   else
@@ -315,7 +390,7 @@ __global__ void rewind_kernel(int n_seq, const int32_t *__restrict__ seq_ids,
 cudaError_t launch_append(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                           const int32_t *pos0, const int32_t *page_table, int max_pages,
                           int num_pages, uint16_t *k_pool, uint16_t *v_pool,
-                          uint16_t *idxraw_pool, uint16_t *idxblk_pool, const int32_t *ingested,
+                          uint16_t *idxraw_pool, void *idxblk_pool, const int32_t *ingested,
                           const uint16_t *k_new, const uint16_t *v_new,
                           const uint16_t *idx_k_new, int32_t *status, bool pdl, cudaStream_t st,
                           const PreArgs *pre) {

@@ -6,6 +6,8 @@
 //   idxraw_pool     [num_pages][P][d_I]
 //   idxblk_pool     [num_pages][P/ratio * d_I]  shares the page table at 1/ratio density;
 //                                                rows tiled in 8 x 8 core matrices (blk_elem_offset)
+//                   MXFP8: [num_pages][bpp * (d_I + d_I/32)] bytes, E4M3 elements in
+//                   8 x 16-byte core matrices (fp8_elem_offset), then E8M0 scales
 //   page_table      [n_slots][max_pages] int32
 #pragma once
 
@@ -63,13 +65,30 @@ struct CacheView {
   const uint16_t *k_pool;
   const uint16_t *v_pool;
   const uint16_t *idxraw_pool;
-  const uint16_t *idxblk_pool;
+  const void *idxblk_pool;  // bf16 tiles, or the MXFP8 byte plane
 };
 
 struct Shape {
   int ratio, budget, topk, h_idx, d_idx, hq, hkv, d, page;
   int log2_ratio, log2_page;
+  int idx_fp8;  // compressed keys in the MXFP8 plane (index queries MXFP8-rounded)
 };
+
+// --- MXFP8 block-pool pages --------------------------------------------------
+// A page holds bpp = P/ratio blocks (bpp >= 8): bpp * d_I E4M3 bytes, element
+// (rr, d) at fp8_elem_offset (core matrices of 8 blocks x 16 bytes, the K-major
+// order of an 8-bit operand), then bpp * d_I/32 E8M0 scale bytes, scale (rr, c)
+// at bpp * d_I + rr * d_I/32 + c.
+__host__ __device__ __forceinline__ int fp8_elem_offset(int rr, int d, int d_idx) {
+  return ((rr >> 3) * (d_idx >> 4) + (d >> 4)) * 128 + (rr & 7) * 16 + (d & 15);
+}
+__host__ __device__ __forceinline__ int fp8_page_bytes(int bpp, int d_idx) { return bpp * (d_idx + d_idx / 32); }
+
+// 2^e as fp32 for e in [-149, 127] (subnormal below -126): an E8M0 scale byte u
+// is 2^(u - 127).
+__device__ __forceinline__ float exp2_int(int e) {
+  return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(1u << (e + 149));
+}
 
 // --- PTX wrappers ---------------------------------------------------------
 
@@ -191,7 +210,7 @@ cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 bloc
 cudaError_t launch_append(const Shape &sh, int n_seq, int R, const int32_t *seq_ids,
                           const int32_t *pos0, const int32_t *page_table, int max_pages,
                           int num_pages, uint16_t *k_pool, uint16_t *v_pool,
-                          uint16_t *idxraw_pool, uint16_t *idxblk_pool, const int32_t *ingested,
+                          uint16_t *idxraw_pool, void *idxblk_pool, const int32_t *ingested,
                           const uint16_t *k_new, const uint16_t *v_new,
                           const uint16_t *idx_k_new, int32_t *status, bool pdl, cudaStream_t st,
                           const PreArgs *pre = nullptr);

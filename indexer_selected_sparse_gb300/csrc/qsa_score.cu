@@ -58,7 +58,7 @@ score_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
     if (b < n_blk) {
       const int page = ptab[b >> bpp_log2];
       if (page >= 0 && page < cv.num_pages) {
-        src = cv.idxblk_pool + (static_cast<size_t>(page) << bpp_log2) * DI +
+        src = static_cast<const uint16_t *>(cv.idxblk_pool) + (static_cast<size_t>(page) << bpp_log2) * DI +
               blk_elem_offset(b & ((1 << bpp_log2) - 1), c * 8, 1 << bpp_log2, DI);
         bytes = 16;
       } else {
@@ -157,7 +157,8 @@ cudaError_t launch_score(const Shape &sh, int n_seq, int R, const int32_t *seq_i
                          cudaStream_t st, bool q_in_step) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
   // tcgen05 path whenever the TMA page boxes fit (8..32 blocks per page);
-  // the mma.sync kernel below covers the remaining shapes (ratio 16)
+  // the mma.sync kernel below covers the remaining shapes (ratio 16, bf16 keys only)
+  if (sh.idx_fp8 && !score_tc_supported(sh)) return cudaErrorInvalidValue;
   if (score_tc_supported(sh))
     return launch_score_tc(sh, n_seq, R, seq_ids, pos0, cv, q_idx, w, scores, ld_scores, status, pdl, st,
                            q_in_step);

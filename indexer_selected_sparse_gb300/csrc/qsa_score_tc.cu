@@ -19,6 +19,13 @@
 //     in by TMA (cp.async.bulk.tensor, 128B swizzle), one box per 64 dims.
 //   * One thread issues d_I/16 tcgen05.mma (kind::f16, bf16 in, fp32 accumulate
 //     in TMEM) and commits them to an mbarrier.
+//   * With the MXFP8 plane (E4M3 elements and E8M0 scales per 32 values, pages
+//     of bpp * (d_I + d_I/32) bytes), the producer copies those pages into a
+//     byte ring, and 4 converter warps rebuild each tile as bf16 in the same
+//     MMA-ready layout (one block row per thread: 16 E4M3 bytes -> f16 pairs by
+//     cvt, times the block's power-of-two scale in fp32, -> bf16 pairs; every
+//     MXFP8 value is exact in bf16), so the MMA and epilogue below are the bf16
+//     ones. The HBM stream is 132 bytes per block instead of 256.
 //   * 4 * G epilogue warps, one per (row of the group, TMEM lane quarter), read
 //     their 32 lanes with tcgen05.ld: the warp holds its row's head columns in
 //     registers, hands the TMEM buffer back at once, and reduces them with
@@ -30,6 +37,7 @@
 // QSA_ERR_TIMEOUT, waits (bounded) for its own copies, frees its TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 
 #include <mutex>
 
@@ -191,7 +199,7 @@ struct TcArgs {
   const int32_t *page_table;
   int max_pages;
   int num_pages;
-  const uint16_t *keys;  // compressed-key pool (tiled pages)
+  const uint8_t *keys;   // compressed-key pool (tiled pages: bf16, or the MXFP8 plane)
   const float *w;
   float *scores;
   int ld;
@@ -202,12 +210,17 @@ struct TcArgs {
 };
 
 constexpr int kMaxEpiWarps = 4 * kTcMaxGroup;  // one per (row of the group, TMEM lane quarter)
-constexpr int kMaxThreads = 64 + 32 * kMaxEpiWarps;  // warp 0: TMA producer, warp 1: MMA issuer, then epilogue
-constexpr int kMaxStages = 6;
+// warp 0: producer, warp 1: MMA issuer, then epilogue (and MXFP8 converter)
+// warps, and a second producer warp last
+constexpr int kMaxThreads = 64 + 32 * kMaxEpiWarps + 32;
+constexpr int kMaxStages = 8;      // producer ring (bf16 keys: at most kMaxStagesBf16)
+constexpr int kMaxStagesBf16 = 6;
+constexpr int kMaxCStages = 2;     // MXFP8: bf16 operand ring filled by the converter warps
+constexpr int kConvWarps = 8;      // MXFP8: converter warps, half a block row per thread
 constexpr int kRowCols = 64;  // head columns of one row, at most
 // shared memory of the epilogue: per warp the weights of its row [kRowCols]
 constexpr int kEpiFloats = kMaxEpiWarps * kRowCols;
-constexpr int kNumBars = 2 * kMaxStages + 8;
+constexpr int kNumBars = 2 * kMaxStages + 8 + 2 * kMaxCStages;
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -341,24 +354,56 @@ __device__ __forceinline__ Batch load_batch(const TcArgs &a, const Walker &w, Gr
   return b;
 }
 
-// Shared memory (1024-aligned): [A stages: S x DI/64 halves x 128 rows x 128 B]
-// [B slots: 2 x DI/64 halves x npad rows x 128 B][epilogue: kEpiFloats floats]
-// [barriers][tmem address][abort flag]
-template <int DI>
+// Two E4M3 bytes of w (moved by prmt selector SEL into bytes 1 and 3) -> a
+// bf16 pair, times the block scale 2^e. With an E4M3 byte as the high byte of a
+// 16-bit half, its sign is already the bf16 sign; its exponent and mantissa
+// bits, shifted right by 4, become a bf16's low exponent bits and top mantissa
+// bits, which read as a bf16 of value x * 2^-120 -- for subnormal E4M3 too (as a
+// bf16 subnormal) -- so one exact bf16 multiply by 2^(120 + e) finishes it:
+// prmt, shift, lop3, mul.bf16x2, no conversion instructions. sc2 holds
+// 2^(120 + e) in both halves (e <= 7), or 2^120 with a second multiply by 2^e
+// (sc2b) for larger scales.
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w, uint32_t sc2, uint32_t sc2b, bool two_step) {
+  uint32_t y, r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(y) : "r"(w), "n"(SEL));
+  const uint32_t t = (y & 0x80008000u) | ((y >> 4) & 0x07F007F0u);
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(sc2));
+  if (two_step) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(r), "r"(sc2b));
+  return r;
+}
+
+// bf16 bits of 2^e (e in [-126, 127]), in both halves of a word.
+__device__ __forceinline__ uint32_t bf16x2_pow2(int e) {
+  const uint32_t h = static_cast<uint32_t>(e + 127) << 7;
+  return h | (h << 16);
+}
+
+// Shared memory (1024-aligned):
+//   bf16 keys:  [A stages: S x tile][B slots][epilogue][barriers][tmem address][abort flag]
+//   MXFP8 keys: [operand stages: kMaxCStages x tile][B slots][byte ring: S x 128 blocks of
+//               d_I + d_I/32 bytes][epilogue][barriers][tmem address][abort flag]
+// A tile is 128 rows x d_I bf16 in the K-major core-matrix layout; a B slot is
+// DI/64 halves x npad rows x 128 B (128B swizzle).
+template <int DI, bool FP8>
 __global__ void __launch_bounds__(kMaxThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages) {
   constexpr int HALVES = DI / 64;
   constexpr int A_STAGE = kTcTileBlocks * DI * 2;  // one tile of keys, tiled pages back to back
+  constexpr int R_STAGE = FP8 ? kTcTileBlocks * (DI + DI / 32) : A_STAGE;  // one tile as copied
+  constexpr int N_OP = FP8 ? kMaxCStages : 0;      // operand stages besides the copy ring
+  constexpr int N_OPD = FP8 ? kMaxCStages : 1;     // the same as a divisor (bf16: unused)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base_u = (raw_u + 1023u) & ~1023u;
   uint8_t *base = smem_raw + (base_u - raw_u);
   const int S = n_stages;
-  const uint32_t a_u = base_u;
+  const uint32_t a_u = base_u;  // MMA operand tiles: the copy ring itself (bf16) or the converted ring
   const uint32_t b_half = a.npad * 128;
   const uint32_t b_slot = HALVES * b_half;
-  const uint32_t b_u = a_u + S * A_STAGE;
-  float *ws = reinterpret_cast<float *>(base + S * A_STAGE + 2 * b_slot);  // kEpiFloats floats
+  const uint32_t b_u = a_u + (FP8 ? N_OP : S) * A_STAGE;
+  const uint32_t r_u = FP8 ? b_u + 2 * b_slot : a_u;  // where the producer's copies land
+  float *ws = reinterpret_cast<float *>(base + (FP8 ? (r_u - base_u) + S * R_STAGE : S * A_STAGE + 2 * b_slot));
   const uint32_t bars = smem_u32(ws + kEpiFloats);
   // barrier addresses
   auto a_full = [&](int s) { return bars + 8u * s; };
@@ -367,6 +412,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
   auto b_empty = [&](int s) { return bars + 8u * (2 * kMaxStages + 2 + s); };
   auto t_full = [&](int s) { return bars + 8u * (2 * kMaxStages + 4 + s); };
   auto t_empty = [&](int s) { return bars + 8u * (2 * kMaxStages + 6 + s); };
+  auto c_full = [&](int s) { return bars + 8u * (2 * kMaxStages + 8 + s); };
+  auto c_empty = [&](int s) { return bars + 8u * (2 * kMaxStages + 8 + kMaxCStages + s); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ws + kEpiFloats + 2 * kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -377,7 +424,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(a_full(s), 1);
-      mbar_init(a_empty(s), 1);
+      mbar_init(a_empty(s), FP8 ? kConvWarps : 1);  // converter warps, or the MMA's commit
+    }
+    for (int s = 0; s < N_OP; ++s) {
+      mbar_init(c_full(s), kConvWarps);
+      mbar_init(c_empty(s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(b_full(s), 1);
@@ -395,10 +446,17 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
   const uint32_t tmem = *tmem_slot;
   const int bpp = 1 << a.bpp_log2;
   const int pages_in_tile = kTcTileBlocks >> a.bpp_log2;
-  const uint32_t page_bytes = static_cast<uint32_t>(bpp) * DI * 2;
+  const uint32_t page_bytes = FP8 ? static_cast<uint32_t>(fp8_page_bytes(bpp, DI)) : static_cast<uint32_t>(bpp) * DI * 2;
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
+  const int prod2 = static_cast<int>(blockDim.x >> 5) - 1;  // the second producer warp
+  if (warp == 0 || warp == prod2) {
+    // ---------------- producers ----------------
+    // Two producer warps issue alternate tiles (warp 0 the even ones and every
+    // query load): one warp's stream of page copies is limited by its own issue
+    // and completion round trips (about 1.2 G random pages/s per producer on
+    // this part), two independent streams carry nearly twice as many pages.
+    // Both walk the same (group, tile) sequence; the ring's stages and their
+    // barrier phases are shared, so which warp fills a stage does not matter.
     // Tiles are issued in batches of consecutive tiles of one group: lane L
     // holds the page id of page L of the batch. The page ids of the next batch
     // are loaded before the current batch's copies are issued, and the group's
@@ -407,6 +465,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     // (pooled by earlier steps) need nothing from the append kernel: up to a
     // ring's worth of them is issued before the dependency wait, so their HBM
     // latency overlaps the append.
+    const int par = warp == 0 ? 0 : 1;
     Walker w = walker_start(a, n_groups, lane);
     const uint64_t stream_policy = l2_evict_first();
     const int per_batch = 32 / pages_in_tile;
@@ -433,7 +492,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       Walker wn = w;
       for (int it = 0; it < cur.nb; ++it) walker_next(wn, a, n_groups);
       const Batch nxt = wn.left > 0 ? load_batch(a, wn, gi, lane, per_batch, pages_in_tile, bpp) : Batch{};
-      if (w.g != cur_g) {
+      if (par == 0 && w.g != cur_g) {
         ++gseq;
         const int bs = gseq & 1;
         // at most the first group's query load waits for the dependency wait
@@ -459,6 +518,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       for (int it = 0; it < cur.nb; ++it, ++k) {
         const int s = k % S;
         if (!waited && (k >= S || (w.t + it + 1) * kTcTileBlocks > cur.nblk_old)) wait_now();
+        if ((k & 1) != par) continue;  // the other producer's tile
         if (k >= S && !mbar_wait_or_abort(a_empty(s), ((k / S) - 1) & 1, abort_flag, a.status)) {
           ok = false;
           break;
@@ -470,7 +530,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         __syncwarp();
         if (load && ((mine >> lane) & 1u)) {
           const int slot = lane - it * pages_in_tile;
-          bulk_load_hint(a_u + s * A_STAGE + slot * page_bytes, a.keys + static_cast<size_t>(cur.pg) * bpp * DI,
+          bulk_load_hint(r_u + s * R_STAGE + slot * page_bytes, a.keys + static_cast<size_t>(cur.pg) * page_bytes,
                          page_bytes, a_full(s), stream_policy);
         }
       }
@@ -484,10 +544,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     int cur_g = -1, gseq = -1;
     const uint32_t idesc = idesc_bf16_f32(kTcTileBlocks, a.npad);
     for (int k = 0; w.left > 0; ++k) {
-      const int s = k % S;
+      const int s = FP8 ? k % N_OPD : k % S;  // operand stage
       const int buf = k & 1;
       bool ok = true;
-      if (lane == 0) ok = mbar_wait_or_abort(a_full(s), (k / S) & 1, abort_flag, a.status);
+      if (lane == 0)
+        ok = FP8 ? mbar_wait_or_abort(c_full(s), (k / N_OPD) & 1, abort_flag, a.status)
+                 : mbar_wait_or_abort(a_full(s), (k / S) & 1, abort_flag, a.status);
       int bs = gseq & 1;
       if (w.g != cur_g) {
         ++gseq;
@@ -509,11 +571,80 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
           const uint64_t bd = smem_desc_sw128(b_u + bs * b_slot + hh * b_half + k4 * 32);
           tc_mma(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
         }
-        tc_commit(a_empty(s));
+        tc_commit(FP8 ? c_empty(s) : a_empty(s));
         tc_commit(t_full(buf));
       }
       walker_next(w, a, n_groups);
       if (lane == 0 && (w.left <= 0 || w.g != cur_g)) tc_commit(b_empty(bs));
+    }
+  } else if (FP8 && warp >= 2 + 4 * a.G) {
+    // ---------------- MXFP8 converters (warps 2 + 4G .. 2 + 4G + 7) ----------------
+    // Thread t of converter warp c rebuilds half hf = c / 4 (d_I / 2 values) of
+    // block row b = 32 (c % 4) + t of each tile: page slot b / bpp, row
+    // rr = b % bpp of that page. 16 E4M3 bytes (a 16-byte core-matrix row) become
+    // two 16-byte bf16 core-matrix rows; lanes 0-7 of a warp touch one 128-byte
+    // run on both sides, so the accesses are bank-conflict free. Two warps per
+    // SM sub-partition keep the conversion's latency hidden.
+    const int cw = warp - 2 - 4 * a.G;
+    const int b = (cw & 3) * 32 + lane, hf = cw >> 2;
+    const int slot = b >> a.bpp_log2, rr = b & (bpp - 1);
+    const uint32_t src_row = slot * page_bytes + ((rr >> 3) * (DI / 16)) * 128 + (rr & 7) * 16;
+    const uint32_t scl_off = slot * page_bytes + bpp * DI + rr * (DI / 32);
+    const uint32_t dst_row = ((b >> 3) * (DI / 8)) * 128 + (b & 7) * 16;
+    Walker w = walker_start(a, n_groups, lane);
+    for (int k = 0; w.left > 0; ++k) {
+      const int s = k % S, c = k % N_OPD;
+      if (!mbar_wait_or_abort(a_full(s), (k / S) & 1, abort_flag, a.status)) break;
+      if (k >= N_OPD && !mbar_wait_or_abort(c_empty(c), ((k / N_OPD) - 1) & 1, abort_flag, a.status)) break;
+      const uint32_t src = r_u + s * R_STAGE;
+      uint32_t scl;
+      if (DI == 128)
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(scl) : "r"(src + scl_off));
+      else {
+        uint16_t s16;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(s16) : "r"(src + scl_off));
+        scl = s16;
+      }
+      const uint32_t dst = a_u + c * A_STAGE + dst_row;
+#pragma unroll
+      for (int jj = 0; jj < DI / 32; ++jj) {
+        const int j = hf * (DI / 32) + jj;  // this thread's 16-byte chunks of the row
+        uint32_t v0, v1, v2, v3;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                     : "r"(src + src_row + j * 128));
+        // the block's scale 2^e, e = byte - 127 in [-127, 127]: one multiply by
+        // 2^(120 + e) when that is a normal bf16 (e <= 7), else 2^120 then 2^e
+        const int e = static_cast<int>((scl >> (8 * (j >> 1))) & 0xFFu) - 127;
+        const bool two = e > 7;
+        const uint32_t sc2 = bf16x2_pow2(two ? 120 : 120 + e);
+        const uint32_t sc2b = bf16x2_pow2(two ? e : 0);
+        // prmt 0x1404: bytes 0, 1 of the word into bytes 1 and 3 (zeros below);
+        // 0x3424: bytes 2, 3
+        const uint32_t o0 = e4m3x2_to_bf16x2<0x1404>(v0, sc2, sc2b, two);
+        const uint32_t o1 = e4m3x2_to_bf16x2<0x3424>(v0, sc2, sc2b, two);
+        const uint32_t o2 = e4m3x2_to_bf16x2<0x1404>(v1, sc2, sc2b, two);
+        const uint32_t o3 = e4m3x2_to_bf16x2<0x3424>(v1, sc2, sc2b, two);
+        const uint32_t o4 = e4m3x2_to_bf16x2<0x1404>(v2, sc2, sc2b, two);
+        const uint32_t o5 = e4m3x2_to_bf16x2<0x3424>(v2, sc2, sc2b, two);
+        const uint32_t o6 = e4m3x2_to_bf16x2<0x1404>(v3, sc2, sc2b, two);
+        const uint32_t o7 = e4m3x2_to_bf16x2<0x3424>(v3, sc2, sc2b, two);
+        // dims 16j .. 16j+7 and 16j+8 .. 16j+15: bf16 core matrices 2j and 2j + 1
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (2 * j) * 128), "r"(o0), "r"(o1),
+                     "r"(o2), "r"(o3)
+                     : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (2 * j + 1) * 128), "r"(o4),
+                     "r"(o5), "r"(o6), "r"(o7)
+                     : "memory");
+      }
+      // the MMA reads the tile through the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(c_full(c));
+        mbar_arrive(a_empty(s));
+      }
+      walker_next(w, a, n_groups);
     }
   } else {
     // ---------------- epilogue (warps 2 .. 2 + 4G) ----------------
@@ -637,7 +768,10 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   a.q_in_step = q_in_step ? 1 : 0;
   a.sh = sh;
   a.R = R;
-  a.G = (sh.h_idx % 16 == 0) ? min(min(R, kTcMaxGroup), 256 / sh.h_idx) : 1;
+  // with the MXFP8 plane 8 converter warps join, so at most 2 rows share a tile
+  // (64 + 128 G + 256 + 32 threads within the 608 the kernel is built for)
+  const int g_max = sh.idx_fp8 ? (kMaxThreads - 96 - 32 * kConvWarps) / 128 : kTcMaxGroup;
+  a.G = (sh.h_idx % 16 == 0) ? min(min(R, g_max), 256 / sh.h_idx) : 1;
   a.groups_per_seq = (R + a.G - 1) / a.G;
   a.npad = (a.G * sh.h_idx + 15) / 16 * 16;
   a.hp = (a.G == 1) ? a.npad : sh.h_idx;
@@ -648,7 +782,7 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   a.page_table = cv.page_table;
   a.max_pages = cv.max_pages;
   a.num_pages = cv.num_pages;
-  a.keys = cv.idxblk_pool;
+  a.keys = static_cast<const uint8_t *>(cv.idxblk_pool);
   a.w = w;
   a.scores = scores;
   a.ld = ld;
@@ -661,14 +795,17 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
 
   a.n_groups = n_seq * a.groups_per_seq;
   const int halves = sh.d_idx / 64;
+  const bool fp8 = sh.idx_fp8 != 0;
   const size_t a_stage = static_cast<size_t>(kTcTileBlocks) * sh.d_idx * 2;
+  const size_t r_stage = fp8 ? static_cast<size_t>(kTcTileBlocks) * (sh.d_idx + sh.d_idx / 32) : a_stage;
   const size_t b_slots = 2ull * halves * a.npad * 128;
-  const size_t fixed = 1024 + b_slots + kEpiFloats * 4 + 8 * kNumBars + 16;
+  const size_t fixed = 1024 + (fp8 ? kMaxCStages * a_stage : 0) + b_slots + kEpiFloats * 4 + 8 * kNumBars + 16;
   const size_t smem_cap = 227 * 1024;
-  int stages = static_cast<int>((smem_cap - fixed) / a_stage);
-  if (stages > kMaxStages) stages = kMaxStages;
+  int stages = static_cast<int>((smem_cap - fixed) / r_stage);
+  const int max_stages = fp8 ? kMaxStages : kMaxStagesBf16;
+  if (stages > max_stages) stages = max_stages;
   if (stages < 2) return cudaErrorInvalidValue;
-  size_t smem = fixed + stages * a_stage;
+  size_t smem = fixed + stages * r_stage;
   // TMEM: resident CTAs x 2 accumulators x ncols must stay within the SM's 512
   // columns so tcgen05.alloc never waits on another CTA; raise the shared
   // memory request until at most 512 / (2 ncols) CTAs fit on an SM.
@@ -676,14 +813,15 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   const int max_ctas = 512 / (2 * a.ncols);
   const size_t min_smem = sm_smem / (max_ctas + 1) - 1024 + 1;
   if (smem < min_smem) smem = min_smem;
-  auto kern = sh.d_idx == 128 ? score_tc_kernel<128> : score_tc_kernel<64>;
+  auto kern = fp8 ? (sh.d_idx == 128 ? score_tc_kernel<128, true> : score_tc_kernel<64, true>)
+                  : (sh.d_idx == 128 ? score_tc_kernel<128, false> : score_tc_kernel<64, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0, per_sm = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int threads = 64 + 128 * a.G;
+  const int threads = 64 + 128 * a.G + (fp8 ? 32 * kConvWarps : 0) + 32;  // + the second producer
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem)) != cudaSuccess)
     return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;

@@ -33,11 +33,14 @@ QSA_ERR_REWIND = 9
 QSA_ERR_TIMEOUT = 10
 QSA_ERR_REUSE = 11
 
+QSA_INDEX_BF16 = 0
+QSA_INDEX_MXFP8 = 1
+
 EXPORTED = ("qsa_strerror", "qsa_config_check", "qsa_workspace_bytes", "qsa_append",
             "qsa_rewind", "qsa_index_score", "qsa_topk_select", "qsa_gather_attn", "qsa_decode",
             "qsa_gather_attn_static", "qsa_max_attend_tokens", "qsa_gather_attn_reuse",
             "qsa_decode_reuse", "qsa_append_pre", "qsa_pre_index_q", "qsa_workspace_bytes_pre",
-            "qsa_decode_pre")
+            "qsa_decode_pre", "qsa_idxblk_page_bytes", "qsa_quantize_index_q")
 QSA_STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -56,7 +59,7 @@ LIB_PATH = _LIB_PATH
 class qsa_config(ctypes.Structure):
     _fields_ = [("ratio", ctypes.c_int), ("budget", ctypes.c_int), ("n_idx_heads", ctypes.c_int),
                 ("idx_dim", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
-                ("head_dim", ctypes.c_int), ("page_size", ctypes.c_int)]
+                ("head_dim", ctypes.c_int), ("page_size", ctypes.c_int), ("index_format", ctypes.c_int)]
 
 
 class qsa_pre_indexer(ctypes.Structure):
@@ -116,6 +119,10 @@ LIB.qsa_pre_index_q.restype = _I
 LIB.qsa_pre_index_q.argtypes = [_CFG, _PRE, _ROWS, _P, _P, _P]
 LIB.qsa_workspace_bytes_pre.restype = ctypes.c_size_t
 LIB.qsa_workspace_bytes_pre.argtypes = [_CFG, _I, _I]
+LIB.qsa_idxblk_page_bytes.restype = ctypes.c_size_t
+LIB.qsa_idxblk_page_bytes.argtypes = [_CFG]
+LIB.qsa_quantize_index_q.restype = _I
+LIB.qsa_quantize_index_q.argtypes = [_CFG, _I, _P, _P, _P]
 LIB.qsa_decode_pre.restype = _I
 LIB.qsa_decode_pre.argtypes = [_CFG, _PRE, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                ctypes.c_size_t, _P, _P]
@@ -170,19 +177,21 @@ class Config:
     n_kv_heads: int
     head_dim: int = 128
     page_size: int = 64
+    index_format: int = QSA_INDEX_BF16
 
     def c(self) -> qsa_config:
         return qsa_config(self.ratio, self.budget, self.n_idx_heads, self.idx_dim,
-                          self.n_q_heads, self.n_kv_heads, self.head_dim, self.page_size)
+                          self.n_q_heads, self.n_kv_heads, self.head_dim, self.page_size,
+                          self.index_format)
 
     @property
     def topk(self) -> int:
         return self.budget // self.ratio
 
     @classmethod
-    def of(cls, shapes) -> "Config":
+    def of(cls, shapes, index_format: int = QSA_INDEX_BF16) -> "Config":
         return cls(shapes.ratio, shapes.budget, shapes.n_idx_heads, shapes.idx_dim,
-                   shapes.n_q_heads, shapes.n_kv_heads, shapes.head_dim, shapes.page_size)
+                   shapes.n_q_heads, shapes.n_kv_heads, shapes.head_dim, shapes.page_size, index_format)
 
 
 class PagedCache:
@@ -199,8 +208,13 @@ class PagedCache:
         self.k_pool = torch.zeros(num_pages, P, cfg.n_kv_heads, cfg.head_dim, dtype=torch.bfloat16, device=device)
         self.v_pool = torch.zeros_like(self.k_pool)
         self.idxraw_pool = torch.zeros(num_pages, P, cfg.idx_dim, dtype=torch.bfloat16, device=device)
-        # block keys: P/ratio rows of idx_dim per page, stored tiled (see qsa.h)
-        self.idxblk_pool = torch.zeros(num_pages, (P // cfg.ratio) * cfg.idx_dim, dtype=torch.bfloat16, device=device)
+        # block keys: P/ratio rows of idx_dim per page, stored tiled (see qsa.h); with the
+        # MXFP8 index format a byte plane of qsa_idxblk_page_bytes() per page
+        if cfg.index_format == QSA_INDEX_MXFP8:
+            self.idxblk_pool = torch.zeros(num_pages, qsa_idxblk_page_bytes(cfg), dtype=torch.uint8, device=device)
+        else:
+            self.idxblk_pool = torch.zeros(num_pages, (P // cfg.ratio) * cfg.idx_dim, dtype=torch.bfloat16,
+                                           device=device)
         self.ingested = torch.zeros(self.n_slots, dtype=torch.int32, device=device)
 
     @property
@@ -374,6 +388,21 @@ def qsa_pre_index_q(cfg: Config, pre: PreIndexer, rows: Rows, q_idx, q_out, stre
     rc = LIB.qsa_pre_index_q(ctypes.byref(cfg.c()), ctypes.byref(pre.c()), ctypes.byref(rows.c()),
                              _ptr(q_idx, torch.bfloat16), _ptr(q_out, torch.bfloat16), _stream(stream))
     _check(rc, "qsa_pre_index_q")
+
+
+def qsa_idxblk_page_bytes(cfg: Config) -> int:
+    """Bytes of one block-pool page for the configuration's index format (0: invalid)."""
+    return LIB.qsa_idxblk_page_bytes(ctypes.byref(cfg.c()))
+
+
+def qsa_quantize_index_q(cfg: Config, q_idx, q_out, stream=None) -> None:
+    """MXFP8 round trip of index query heads [rows, H_I, d_I] (bf16 in and out)."""
+    n_rows = q_idx.numel() // (cfg.n_idx_heads * cfg.idx_dim)
+    if q_out.numel() != q_idx.numel():
+        raise ValueError("q_out must match q_idx")
+    rc = LIB.qsa_quantize_index_q(ctypes.byref(cfg.c()), n_rows, _ptr(q_idx, torch.bfloat16),
+                                  _ptr(q_out, torch.bfloat16), _stream(stream))
+    _check(rc, "qsa_quantize_index_q")
 
 
 def qsa_workspace_bytes_pre(cfg: Config, max_rows: int, max_blocks_per_row: int) -> int:

@@ -36,6 +36,32 @@ def block_pool_index(bpp: int, d_idx: int) -> np.ndarray:
     return ((rr // g) * (d_idx // 8) + d // 8) * (8 * g) + (rr % g) * 8 + d % 8
 
 
+def e4m3_values() -> np.ndarray:
+    """Value of every E4M3 byte (256 entries), from the bit definition: sign |
+    4-bit exponent (bias 7) | 3-bit mantissa; exponent field 0 is subnormal
+    (m/8 * 2^-6); 0x7F / 0xFF are NaN."""
+    v = np.empty(256)
+    for code in range(256):
+        e, m = (code >> 3) & 15, code & 7
+        mag = m / 8 * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+        if e == 15 and m == 7:
+            mag = np.nan
+        v[code] = -mag if code & 0x80 else mag
+    return v
+
+
+def mxfp8_page_index(bpp: int, d_idx: int):
+    """Byte offsets of a block-pool page in the MXFP8 format the C ABI header
+    documents: elements [bpp, d_idx] in 8-block x 16-byte core matrices, then
+    scales [bpp, d_idx / 32]."""
+    rr = np.arange(bpp)[:, None]
+    d = np.arange(d_idx)[None, :]
+    el = ((rr // 8) * (d_idx // 16) + d // 16) * 128 + (rr % 8) * 16 + d % 16
+    c = np.arange(d_idx // 32)[None, :]
+    sc = bpp * d_idx + rr * (d_idx // 32) + c
+    return el, sc
+
+
 class History:
     """Per-sequence record of which epoch wrote each position (positions
     re-appended after a rewind carry fresh random rows)."""
@@ -73,13 +99,14 @@ class GpuState:
     """A workload's cache on the GPU, filled through qsa_append."""
 
     def __init__(self, wl: S.Workload, extra_tokens: int = 64, contiguous: Optional[bool] = None,
-                 page_seed: Optional[int] = None, device: str = "cuda", slots: Optional[List[int]] = None):
+                 page_seed: Optional[int] = None, device: str = "cuda", slots: Optional[List[int]] = None,
+                 index_format: int = 0):
         from indexer_selected_sparse_gb300 import qsa as Q
         self.Q = Q
         self.wl = wl
         self.sh = wl.shapes
         self.irange = wl.extra.get("int_range", (-8, 8))
-        self.cfg = Q.Config.of(self.sh)
+        self.cfg = Q.Config.of(self.sh, index_format)
         self.device = device
         P = self.sh.page_size
         need = max(wl.prefixes) + wl.rows_per_seq + extra_tokens
@@ -175,6 +202,20 @@ class GpuState:
         blk = self.cache.idxblk_pool.view(torch.int16).cpu().numpy().astype(np.uint16)
         return blk[pages[:, None], block_pool_index(bpp, sh.idx_dim)[b % bpp]]
 
+    def logical_blocks_mxfp8(self, s: int, n_blk: int):
+        """The MXFP8 plane's blocks 0..n_blk-1 of sequence s: E4M3 element values
+        [n_blk, d_I] and scale exponents [n_blk, d_I / 32]."""
+        sh = self.sh
+        bpp = sh.page_size // sh.ratio
+        pt = self.cache.page_table[s].cpu().numpy()
+        b = np.arange(n_blk)
+        pages = pt[b // bpp]
+        plane = self.cache.idxblk_pool.cpu().numpy()
+        el, sc = mxfp8_page_index(bpp, sh.idx_dim)
+        elems = e4m3_values()[plane[pages[:, None], el[b % bpp]]]
+        exps = plane[pages[:, None], sc[b % bpp]].astype(np.int64) - 127
+        return elems, exps
+
     def logical_rows(self, pool: torch.Tensor, s: int, positions: np.ndarray) -> np.ndarray:
         P = self.sh.page_size
         pt = self.cache.page_table[s].cpu().numpy()
@@ -222,7 +263,7 @@ class OracleSeq:
         self.st.V[need] = bits(v)
         self.filled[need] = True
 
-    def row(self, pos: int):
+    def row(self, pos: int, index_format: str = "bf16"):
         """Oracle result for the query row at `pos` (uses that row's q inputs)."""
         sh = self.sh
         ep = int(self.hist.epochs(np.array([pos]))[0])
@@ -230,12 +271,13 @@ class OracleSeq:
         visible = pos + 1
         n_blk = visible // sh.ratio
         if n_blk > sh.topk:
-            sc = O.block_scores(bits(qi[0]), w[0].numpy(), self.st.idx_blk[:n_blk])
+            score_fn = O.block_scores_mxfp8 if index_format == "mxfp8" else O.block_scores
+            sc = score_fn(bits(qi[0]), w[0].numpy(), self.st.idx_blk[:n_blk])
             sel = O.select_blocks(sc, sh.topk)
         else:
             sel = np.arange(n_blk)
         self.fill_kv(O.token_set(sel, n_blk, visible, sh.ratio))
-        return O.attend_row(self.st, pos, bits(qi[0]), w[0].numpy(), bits(q[0]), sh.topk)
+        return O.attend_row(self.st, pos, bits(qi[0]), w[0].numpy(), bits(q[0]), sh.topk, index_format)
 
 
 def compare_row(gpu_out_bits: np.ndarray, gpu_sel: np.ndarray, gpu_nsel: int, ref: Dict, topk: int):

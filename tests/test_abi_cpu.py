@@ -141,3 +141,25 @@ def test_pre_indexer_arguments_checked_on_host(Q):
                                q.data_ptr() + 2, None)
     assert rc == Q.QSA_ERR_INVALID_ARG
     assert Q.qsa_workspace_bytes_pre(cfg, 32, 8192) > Q.qsa_workspace_bytes(cfg, 32, 8192)
+
+
+def test_index_format_checked_and_page_bytes(Q):
+    mx = Q.QSA_INDEX_MXFP8
+    assert Q.qsa_config_check(Q.Config(4, 2048, 64, 128, 32, 4, index_format=mx)) == Q.QSA_OK
+    assert Q.qsa_config_check(Q.Config(8, 1024, 16, 64, 8, 1, index_format=mx)) == Q.QSA_OK
+    # 4 blocks per page (ratio 16): the MXFP8 plane is not supported there
+    assert Q.qsa_config_check(Q.Config(16, 2048, 64, 128, 32, 4, index_format=mx)) == Q.QSA_ERR_UNSUPPORTED
+    assert Q.qsa_config_check(Q.Config(4, 2048, 64, 128, 32, 4, index_format=2)) == Q.QSA_ERR_UNSUPPORTED
+    # page bytes: bf16 bpp * d_I * 2; MXFP8 bpp * (d_I + d_I / 32)
+    assert Q.qsa_idxblk_page_bytes(Q.Config(4, 2048, 64, 128, 32, 4)) == 16 * 128 * 2
+    assert Q.qsa_idxblk_page_bytes(Q.Config(4, 2048, 64, 128, 32, 4, index_format=mx)) == 16 * 132
+    assert Q.qsa_idxblk_page_bytes(Q.Config(8, 1024, 16, 64, 8, 1, index_format=mx)) == 8 * 66
+    assert Q.qsa_idxblk_page_bytes(Q.Config(3, 2048, 64, 128, 32, 4)) == 0
+    # the fused step's workspace holds the MXFP8-rounded index queries too
+    bf = Q.qsa_workspace_bytes(Q.Config(4, 2048, 64, 128, 32, 4), 32, 8200)
+    m8 = Q.qsa_workspace_bytes(Q.Config(4, 2048, 64, 128, 32, 4, index_format=mx), 32, 8200)
+    assert m8 - bf >= 32 * 64 * 128 * 2
+    cfg = Q.ctypes.byref(Q.Config(4, 2048, 64, 128, 32, 4).c())
+    assert Q.LIB.qsa_quantize_index_q(cfg, 0, None, None, None) == Q.QSA_OK      # nothing to do
+    assert Q.LIB.qsa_quantize_index_q(cfg, 3, None, None, None) == Q.QSA_ERR_INVALID_ARG
+    assert Q.LIB.qsa_quantize_index_q(cfg, -1, None, None, None) == Q.QSA_ERR_INVALID_ARG

@@ -1,7 +1,8 @@
 """GPU parity of the pre-indexer (Gemma RMSNorm + NeoX RoPE of the index
 queries and of every compressed key) against the CPU oracle.
 
-The GPU runs the norm and rotation in fp32 (angles in double) and rounds to
+The GPU forms the RoPE angles in double, reduced exactly to [-pi, pi], and
+runs their sine / cosine, the norm and the rotation in fp32, then rounds to
 bf16; the oracle computes in fp64 and rounds once. Stage results must agree to
 one bf16 ulp, almost all bit for bit. Scores of pre-indexed keys are real
 numbers, so a selected set may differ from the oracle's only by swapping
