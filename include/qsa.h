@@ -227,9 +227,9 @@ int qsa_rewind(const qsa_config *cfg, int n_seq, const int32_t *seq_ids, const i
  * scores[row * ld_scores + b] = sum_h w[row,h] * max(0, q_idx[row,h,:] . k_b)
  * for b < n_blk (bf16 products, fp32 accumulation). Rows with n_blk <= K are
  * skipped: every block is selected there, so no score is needed. With
- * QSA_INDEX_MXFP8 the keys are the MXFP8 plane's values and the queries are
- * scored as given: pass them through qsa_quantize_index_q first for the
- * MXFP8 x MXFP8 score of the fused step.
+ * QSA_INDEX_MXFP8 the keys are the MXFP8 plane's values and each query head is
+ * MXFP8-rounded inside the kernel (as qsa_quantize_index_q; rounding twice
+ * changes nothing), the score of the fused step.
  *   q_idx   device [rows, H_I, d_I] bf16
  *   w       device [rows, H_I] fp32
  *   scores  device [rows, ld_scores] fp32; ld_scores >= max_pages*P/ratio,
@@ -240,9 +240,10 @@ int qsa_index_score(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache
                     const qsa_bf16 *q_idx, const float *w, float *scores, int ld_scores,
                     int32_t *status, cudaStream_t stream);
 
-/* MXFP8 round trip of index query heads (the query side of QSA_INDEX_MXFP8):
- * each d_I vector's blocks of 32 values are quantised as the keys are and
- * written back as bf16 (every MXFP8 value is exact in bf16).
+/* MXFP8 round trip of index query heads (the query side of QSA_INDEX_MXFP8,
+ * which the scorer applies itself): each d_I vector's blocks of 32 values are
+ * quantised as the keys are and written back as bf16 (every MXFP8 value is
+ * exact in bf16).
  *   q_idx, q_out  device [n_rows, H_I, d_I] bf16 (q_out == q_idx allowed) */
 int qsa_quantize_index_q(const qsa_config *cfg, int n_rows, const qsa_bf16 *q_idx, qsa_bf16 *q_out,
                          cudaStream_t stream);
@@ -282,8 +283,8 @@ int qsa_gather_attn(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache
  *                       in the workspace)
  *   ws                  device workspace, ws_bytes >=
  *                       qsa_workspace_bytes(cfg, rows, max_pages*P/ratio)
- * With QSA_INDEX_MXFP8 the step quantises the index queries (as
- * qsa_quantize_index_q, into the workspace) before scoring. */
+ * With QSA_INDEX_MXFP8 the step's scorer MXFP8-rounds the index queries (as
+ * qsa_quantize_index_q) before scoring; q_idx itself is not written. */
 int qsa_decode(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,
                const qsa_bf16 *k_new, const qsa_bf16 *v_new, const qsa_bf16 *idx_k_new,
                const qsa_bf16 *q_idx, const float *w, const qsa_bf16 *q,

@@ -199,9 +199,10 @@ int decode_impl(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_row
   const int cap_tokens = cache->max_pages * cfg->page_size;
   const int ld = ld_for(cap_tokens / cfg->ratio);
   const WsLayout L = ws_layout(sh, n_rows, ld);
-  // the step's index queries are prepared into the workspace (pre-indexer and / or
-  // MXFP8 round trip) by the append kernel, and the score kernel reads them there
-  const bool q_prep = pre != nullptr || sh.idx_fp8;
+  // through the pre-indexer the step's index queries are prepared into the
+  // workspace by the append kernel, and the score kernel reads them there (with
+  // the MXFP8 plane the score kernel rounds its query tiles itself)
+  const bool q_prep = pre != nullptr;
   const size_t need = L.total + (q_prep ? round_up(q_prep_bytes(sh, n_rows), 256) : 0);
   if (ws_bytes < need) return QSA_ERR_WORKSPACE;
   uint8_t *base = static_cast<uint8_t *>(ws);
@@ -296,9 +297,7 @@ int qsa_max_attend_tokens(const qsa_config *cfg) {
 size_t qsa_workspace_bytes(const qsa_config *cfg, int max_rows, int max_blocks_per_row) {
   if (check_cfg(cfg) != QSA_OK || max_rows < 0 || max_blocks_per_row < 0) return 0;
   const Shape sh = make_shape(cfg);
-  // with the MXFP8 plane the fused step also holds its MXFP8-rounded index queries
-  return ws_layout(sh, max_rows, ld_for(max_blocks_per_row)).total +
-         (sh.idx_fp8 ? round_up(q_prep_bytes(sh, max_rows), 256) : 0);
+  return ws_layout(sh, max_rows, ld_for(max_blocks_per_row)).total;
 }
 
 int qsa_append(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,

@@ -63,28 +63,6 @@ __device__ __forceinline__ void pre_index_lanes(float (&x)[D32], const float *__
 
 // ---- MXFP8 (OCP MX v1.0: E4M3 elements, one E8M0 scale per 32 values) ----
 
-// Scale exponent of a block with largest magnitude amax: floor(log2 amax) - 8
-// (8: exponent of E4M3's top binade), at least -127; -127 when amax is zero or
-// below 2^-126. Read off amax's exponent field.
-__device__ __forceinline__ int mx_scale_exp(float amax) {
-  const int biased = static_cast<int>(__float_as_uint(amax) >> 23);
-  return biased == 0 ? -127 : max(biased - 127 - 8, -127);
-}
-
-// E4M3 code of v: nearest-even, magnitudes past 448 saturate to 448.
-__device__ __forceinline__ uint32_t e4m3_code(float v) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(v));
-  return r & 0xFFu;
-}
-
-// Value of an E4M3 code (exact in f16, then fp32).
-__device__ __forceinline__ float e4m3_value(uint32_t code) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(code)));
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
-}
-
 // One warp holding a d_I vector as lane L: dims L + 32m, so register m across
 // the warp is exactly MX block m. x must already be bf16 values. Returns each
 // lane's codes and every block's scale exponent.

@@ -13,6 +13,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "../../include/qsa.h"
@@ -88,6 +89,33 @@ __host__ __device__ __forceinline__ int fp8_page_bytes(int bpp, int d_idx) { ret
 // is 2^(u - 127).
 __device__ __forceinline__ float exp2_int(int e) {
   return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(1u << (e + 149));
+}
+
+// MX scale exponent of a block of 32 values with largest magnitude amax:
+// floor(log2 amax) - 8 (8: exponent of E4M3's top binade), at least -127; -127
+// when amax is zero or below 2^-126. Read off amax's exponent field.
+__device__ __forceinline__ int mx_scale_exp(float amax) {
+  const int biased = static_cast<int>(__float_as_uint(amax) >> 23);
+  return biased == 0 ? -127 : max(biased - 127 - 8, -127);
+}
+
+// E4M3 code of v: nearest-even, magnitudes past 448 saturate to 448.
+__device__ __forceinline__ uint32_t e4m3_code(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(v));
+  return r & 0xFFu;
+}
+
+// Value of an E4M3 code (exact in f16, then fp32).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(code)));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// x through MXFP8 and back, given its block's scale exponent e (exact in bf16).
+__device__ __forceinline__ float mx_round(float x, int e) {
+  return e4m3_value(e4m3_code(x * exp2_int(-e))) * exp2_int(e);
 }
 
 // --- PTX wrappers ---------------------------------------------------------

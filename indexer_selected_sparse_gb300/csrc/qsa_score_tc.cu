@@ -20,12 +20,14 @@
 //   * One thread issues d_I/16 tcgen05.mma (kind::f16, bf16 in, fp32 accumulate
 //     in TMEM) and commits them to an mbarrier.
 //   * With the MXFP8 plane (E4M3 elements and E8M0 scales per 32 values, pages
-//     of bpp * (d_I + d_I/32) bytes), the producer copies those pages into a
-//     byte ring, and 4 converter warps rebuild each tile as bf16 in the same
-//     MMA-ready layout (one block row per thread: 16 E4M3 bytes -> f16 pairs by
-//     cvt, times the block's power-of-two scale in fp32, -> bf16 pairs; every
-//     MXFP8 value is exact in bf16), so the MMA and epilogue below are the bf16
-//     ones. The HBM stream is 132 bytes per block instead of 256.
+//     of bpp * (d_I + d_I/32) bytes), the producers copy those pages into a
+//     byte ring, and 8 converter warps rebuild each tile as bf16 straight into
+//     tensor memory (a thread per half block row, one tcgen05.st; every MXFP8
+//     value is exact in bf16); the MMA reads that A operand from TMEM, the
+//     epilogue is the bf16 one. The HBM stream is 132 bytes per block instead
+//     of 256, and shared memory holds only copies, so the ring runs deep. The
+//     converter warps also MXFP8-round each group's query tile in place (the
+//     MMA waits for that), so the queries load as early as in the bf16 path.
 //   * 4 * G epilogue warps, one per (row of the group, TMEM lane quarter), read
 //     their 32 lanes with tcgen05.ld: the warp holds its row's head columns in
 //     registers, hands the TMEM buffer back at once, and reduces them with
@@ -155,11 +157,42 @@ __device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
+// The same MMA with the A operand in tensor memory: lane = row of A, 32-bit
+// column c = K elements 2c (low half) and 2c + 1.
+__device__ __forceinline__ void tc_mma_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
+
+// N consecutive 32-bit columns of this thread's TMEM lane from registers (N = 16 or 32).
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t *r) {
+  if constexpr (N == 32) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+  } else {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::
+            "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+  }
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 16 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
@@ -192,7 +225,8 @@ struct TcArgs {
   int groups_per_seq;  // ceil(R / G)
   int npad;            // MMA N (multiple of 16, <= 256)
   int hp;              // TMEM columns per row of the group (H_I, or npad when G == 1)
-  int ncols;           // TMEM columns allocated (power of two >= 32)
+  int ncols;           // TMEM columns of one accumulator (power of two >= 32)
+  int tmem_cols;       // TMEM columns allocated: 2 accumulators (+ MXFP8: the A stages), a power of two
   int bpp_log2;        // log2(blocks per page)
   const int32_t *seq_ids;
   const int32_t *pos0;
@@ -213,14 +247,14 @@ constexpr int kMaxEpiWarps = 4 * kTcMaxGroup;  // one per (row of the group, TME
 // warp 0: producer, warp 1: MMA issuer, then epilogue (and MXFP8 converter)
 // warps, and a second producer warp last
 constexpr int kMaxThreads = 64 + 32 * kMaxEpiWarps + 32;
-constexpr int kMaxStages = 8;      // producer ring (bf16 keys: at most kMaxStagesBf16)
+constexpr int kMaxStages = 12;     // producer ring (bf16 keys: at most kMaxStagesBf16)
 constexpr int kMaxStagesBf16 = 6;
-constexpr int kMaxCStages = 2;     // MXFP8: bf16 operand ring filled by the converter warps
-constexpr int kConvWarps = 8;      // MXFP8: converter warps, half a block row per thread
+constexpr int kMaxCStages = 4;     // MXFP8: bf16 A stages in TMEM filled by the converter warps
+constexpr int kConvWarps = 8;      // MXFP8: converter warps, 4 per copy ring, a block row per thread
 constexpr int kRowCols = 64;  // head columns of one row, at most
 // shared memory of the epilogue: per warp the weights of its row [kRowCols]
 constexpr int kEpiFloats = kMaxEpiWarps * kRowCols;
-constexpr int kNumBars = 2 * kMaxStages + 8 + 2 * kMaxCStages;
+constexpr int kNumBars = 2 * kMaxStages + 8 + 2 * kMaxCStages + 2;
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -381,10 +415,11 @@ __device__ __forceinline__ uint32_t bf16x2_pow2(int e) {
 
 // Shared memory (1024-aligned):
 //   bf16 keys:  [A stages: S x tile][B slots][epilogue][barriers][tmem address][abort flag]
-//   MXFP8 keys: [operand stages: kMaxCStages x tile][B slots][byte ring: S x 128 blocks of
-//               d_I + d_I/32 bytes][epilogue][barriers][tmem address][abort flag]
+//   MXFP8 keys: [B slots][byte ring: S x 128 blocks of d_I + d_I/32 bytes][epilogue]
+//               [barriers][tmem address][abort flag]; the bf16 A tiles live in TMEM
 // A tile is 128 rows x d_I bf16 in the K-major core-matrix layout; a B slot is
-// DI/64 halves x npad rows x 128 B (128B swizzle).
+// DI/64 halves x npad rows x 128 B (128B swizzle). TMEM: two accumulators of
+// ncols columns, then (MXFP8) kMaxCStages A tiles of d_I / 2 columns.
 template <int DI, bool FP8>
 __global__ void __launch_bounds__(kMaxThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages) {
@@ -398,12 +433,17 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
   const uint32_t base_u = (raw_u + 1023u) & ~1023u;
   uint8_t *base = smem_raw + (base_u - raw_u);
   const int S = n_stages;
-  const uint32_t a_u = base_u;  // MMA operand tiles: the copy ring itself (bf16) or the converted ring
+  // copy rings: MXFP8 keeps one per producer warp (even and odd tiles), each with
+  // its own converter warps, so a late page copy holds up only its own ring; bf16
+  // keeps one ring that both producers fill and the MMA drains
+  constexpr int NR = FP8 ? 2 : 1;
+  const int S_R = S / NR;
+  const uint32_t a_u = base_u;  // bf16: the copy ring holds the MMA's A tiles
   const uint32_t b_half = a.npad * 128;
   const uint32_t b_slot = HALVES * b_half;
-  const uint32_t b_u = a_u + (FP8 ? N_OP : S) * A_STAGE;
-  const uint32_t r_u = FP8 ? b_u + 2 * b_slot : a_u;  // where the producer's copies land
-  float *ws = reinterpret_cast<float *>(base + (FP8 ? (r_u - base_u) + S * R_STAGE : S * A_STAGE + 2 * b_slot));
+  const uint32_t b_u = FP8 ? base_u : a_u + S * A_STAGE;
+  const uint32_t r_u = FP8 ? b_u + 2 * b_slot : a_u;  // where the producers' copies land
+  float *ws = reinterpret_cast<float *>(base + (FP8 ? 2 * b_slot + S * R_STAGE : S * A_STAGE + 2 * b_slot));
   const uint32_t bars = smem_u32(ws + kEpiFloats);
   // barrier addresses
   auto a_full = [&](int s) { return bars + 8u * s; };
@@ -414,6 +454,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
   auto t_empty = [&](int s) { return bars + 8u * (2 * kMaxStages + 6 + s); };
   auto c_full = [&](int s) { return bars + 8u * (2 * kMaxStages + 8 + s); };
   auto c_empty = [&](int s) { return bars + 8u * (2 * kMaxStages + 8 + kMaxCStages + s); };
+  auto q_ready = [&](int s) { return bars + 8u * (2 * kMaxStages + 8 + 2 * kMaxCStages + s); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ws + kEpiFloats + 2 * kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -424,12 +465,14 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(a_full(s), 1);
-      mbar_init(a_empty(s), FP8 ? kConvWarps : 1);  // converter warps, or the MMA's commit
+      mbar_init(a_empty(s), FP8 ? kConvWarps / NR : 1);  // the ring's converter warps, or the MMA's commit
     }
     for (int s = 0; s < N_OP; ++s) {
-      mbar_init(c_full(s), kConvWarps);
+      mbar_init(c_full(s), kConvWarps / NR);  // the converter warps of the tile's ring
       mbar_init(c_empty(s), 1);
     }
+    if (FP8)
+      for (int s = 0; s < 2; ++s) mbar_init(q_ready(s), kConvWarps);  // the group's queries MXFP8-rounded
     for (int s = 0; s < 2; ++s) {
       mbar_init(b_full(s), 1);
       mbar_init(b_empty(s), 1);
@@ -439,7 +482,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 2 * a.ncols);
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -516,10 +559,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       const bool load = cur.have && !bad_page;
       const unsigned have_mask = __ballot_sync(0xffffffffu, load);
       for (int it = 0; it < cur.nb; ++it, ++k) {
-        const int s = k % S;
-        if (!waited && (k >= S || (w.t + it + 1) * kTcTileBlocks > cur.nblk_old)) wait_now();
+        // tile k: ring k % NR, that ring's tile kr = k / NR, stage kr % S_R of the ring
+        const int kr = k / NR;
+        const int s = (k % NR) * S_R + kr % S_R;
+        if (!waited && (kr >= S_R || (w.t + it + 1) * kTcTileBlocks > cur.nblk_old)) wait_now();
         if ((k & 1) != par) continue;  // the other producer's tile
-        if (k >= S && !mbar_wait_or_abort(a_empty(s), ((k / S) - 1) & 1, abort_flag, a.status)) {
+        if (kr >= S_R && !mbar_wait_or_abort(a_empty(s), ((kr / S_R) - 1) & 1, abort_flag, a.status)) {
           ok = false;
           break;
         }
@@ -554,7 +599,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       if (w.g != cur_g) {
         ++gseq;
         bs = gseq & 1;
-        if (lane == 0 && ok) ok = mbar_wait_or_abort(b_full(bs), (gseq >> 1) & 1, abort_flag, a.status);
+        if (lane == 0 && ok)
+          ok = mbar_wait_or_abort(FP8 ? q_ready(bs) : b_full(bs), (gseq >> 1) & 1, abort_flag, a.status);
         cur_g = w.g;
       }
       if (lane == 0 && ok && k >= 2) ok = mbar_wait_or_abort(t_empty(buf), ((k >> 1) - 1) & 1, abort_flag, a.status);
@@ -566,10 +612,15 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
 #pragma unroll
         for (int kk = 0; kk < DI / 16; ++kk) {
           const int hh = kk >> 2, k4 = kk & 3;
-          // K step kk: core matrices 2kk and 2kk+1 along K
-          const uint64_t ad = smem_desc_interleave(a_u + s * A_STAGE + kk * 256, 128, DI * 16);
           const uint64_t bd = smem_desc_sw128(b_u + bs * b_slot + hh * b_half + k4 * 32);
-          tc_mma(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          if (FP8) {
+            // K step kk: columns 8kk .. 8kk+7 of the A tile in TMEM
+            tc_mma_ta(d, tmem + 2 * a.ncols + s * (DI / 2) + kk * 8, bd, idesc, kk > 0 ? 1u : 0u);
+          } else {
+            // K step kk: core matrices 2kk and 2kk+1 along K
+            const uint64_t ad = smem_desc_interleave(a_u + s * A_STAGE + kk * 256, 128, DI * 16);
+            tc_mma(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          }
         }
         tc_commit(FP8 ? c_empty(s) : a_empty(s));
         tc_commit(t_full(buf));
@@ -579,22 +630,70 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     }
   } else if (FP8 && warp >= 2 + 4 * a.G) {
     // ---------------- MXFP8 converters (warps 2 + 4G .. 2 + 4G + 7) ----------------
-    // Thread t of converter warp c rebuilds half hf = c / 4 (d_I / 2 values) of
-    // block row b = 32 (c % 4) + t of each tile: page slot b / bpp, row
-    // rr = b % bpp of that page. 16 E4M3 bytes (a 16-byte core-matrix row) become
-    // two 16-byte bf16 core-matrix rows; lanes 0-7 of a warp touch one 128-byte
-    // run on both sides, so the accesses are bank-conflict free. Two warps per
-    // SM sub-partition keep the conversion's latency hidden.
+    // Converter warps 0-3 drain ring 0 (even tiles), 4-7 ring 1 (odd tiles).
+    // Thread t of converter warp w rebuilds block row b = 32 (w % 4) + t of its
+    // ring's tiles -- the TMEM lane quarter w % 4 is the one the warp may write --
+    // reading page slot b / bpp, row rr = b % bpp of that page (lanes 0-7 read
+    // one 128-byte run: no bank conflicts), and stores the bf16 values as d_I / 2
+    // columns of its lane, half a row per tcgen05.st. The A stage of tile k is
+    // k % kMaxCStages, so each A stage belongs to one ring.
     const int cw = warp - 2 - 4 * a.G;
-    const int b = (cw & 3) * 32 + lane, hf = cw >> 2;
+    const int q = warp & 3, rc = cw >> 2;
+    const int b = q * 32 + lane;
     const int slot = b >> a.bpp_log2, rr = b & (bpp - 1);
     const uint32_t src_row = slot * page_bytes + ((rr >> 3) * (DI / 16)) * 128 + (rr & 7) * 16;
     const uint32_t scl_off = slot * page_bytes + bpp * DI + rr * (DI / 32);
-    const uint32_t dst_row = ((b >> 3) * (DI / 8)) * 128 + (b & 7) * 16;
+    const uint32_t a_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + 2 * a.ncols;
     Walker w = walker_start(a, n_groups, lane);
+    int cur_gq = -1, gq = -1;
     for (int k = 0; w.left > 0; ++k) {
-      const int s = k % S, c = k % N_OPD;
-      if (!mbar_wait_or_abort(a_full(s), (k / S) & 1, abort_flag, a.status)) break;
+      if (w.g != cur_gq) {
+        // a new group: its query tile (TMA, 128B swizzle) is MXFP8-rounded in
+        // place before the MMA may use it. Thread unit u = (row r, 32-value
+        // block): the block's 4 chunks of 16 bytes sit at chunk positions
+        // (c ^ (r % 8)) of the row's 128-byte line in half c / 8 of the slot.
+        ++gq;
+        const int bs = gq & 1;
+        if (!mbar_wait_or_abort(b_full(bs), (gq >> 1) & 1, abort_flag, a.status)) break;
+        const int units = a.npad * (DI / 32);
+        for (int u = cw * 32 + lane; u < units; u += kConvWarps * 32) {
+          const int r = u / (DI / 32), blk = u - r * (DI / 32);
+          const uint32_t line = b_u + bs * b_slot + (blk >> 1) * b_half + r * 128;
+          uint32_t v[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v[4 * i]), "=r"(v[4 * i + 1]), "=r"(v[4 * i + 2]), "=r"(v[4 * i + 3])
+                         : "r"(line + ((((blk & 1) * 4 + i) ^ (r & 7)) << 4)));
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(v[i] << 16)), fabsf(__uint_as_float(v[i] & 0xFFFF0000u))));
+          const int e = mx_scale_exp(amax);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float lo = mx_round(__uint_as_float(v[i] << 16), e);
+            const float hi = mx_round(__uint_as_float(v[i] & 0xFFFF0000u), e);
+            v[i] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);  // exact in bf16
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(line + ((((blk & 1) * 4 + i) ^ (r & 7)) << 4)),
+                         "r"(v[4 * i]), "r"(v[4 * i + 1]), "r"(v[4 * i + 2]), "r"(v[4 * i + 3])
+                         : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the MMA reads through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_ready(bs));
+        cur_gq = w.g;
+      }
+      if ((k & 1) != rc) {  // the other ring's tile
+        walker_next(w, a, n_groups);
+        continue;
+      }
+      const int kr = k >> 1;
+      const int s = rc * S_R + kr % S_R, c = k % N_OPD;
+      if (!mbar_wait_or_abort(a_full(s), (kr / S_R) & 1, abort_flag, a.status)) break;
       if (k >= N_OPD && !mbar_wait_or_abort(c_empty(c), ((k / N_OPD) - 1) & 1, abort_flag, a.status)) break;
       const uint32_t src = r_u + s * R_STAGE;
       uint32_t scl;
@@ -605,10 +704,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         asm volatile("ld.shared.u16 %0, [%1];" : "=h"(s16) : "r"(src + scl_off));
         scl = s16;
       }
-      const uint32_t dst = a_u + c * A_STAGE + dst_row;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+      uint32_t o[DI / 4];  // half a row as bf16 pairs: d_I / 4 TMEM columns
 #pragma unroll
       for (int jj = 0; jj < DI / 32; ++jj) {
-        const int j = hf * (DI / 32) + jj;  // this thread's 16-byte chunks of the row
+        const int j = hf * (DI / 32) + jj;  // the half's 16-byte chunks of the row
         uint32_t v0, v1, v2, v3;
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
@@ -621,24 +722,21 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         const uint32_t sc2b = bf16x2_pow2(two ? e : 0);
         // prmt 0x1404: bytes 0, 1 of the word into bytes 1 and 3 (zeros below);
         // 0x3424: bytes 2, 3
-        const uint32_t o0 = e4m3x2_to_bf16x2<0x1404>(v0, sc2, sc2b, two);
-        const uint32_t o1 = e4m3x2_to_bf16x2<0x3424>(v0, sc2, sc2b, two);
-        const uint32_t o2 = e4m3x2_to_bf16x2<0x1404>(v1, sc2, sc2b, two);
-        const uint32_t o3 = e4m3x2_to_bf16x2<0x3424>(v1, sc2, sc2b, two);
-        const uint32_t o4 = e4m3x2_to_bf16x2<0x1404>(v2, sc2, sc2b, two);
-        const uint32_t o5 = e4m3x2_to_bf16x2<0x3424>(v2, sc2, sc2b, two);
-        const uint32_t o6 = e4m3x2_to_bf16x2<0x1404>(v3, sc2, sc2b, two);
-        const uint32_t o7 = e4m3x2_to_bf16x2<0x3424>(v3, sc2, sc2b, two);
-        // dims 16j .. 16j+7 and 16j+8 .. 16j+15: bf16 core matrices 2j and 2j + 1
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (2 * j) * 128), "r"(o0), "r"(o1),
-                     "r"(o2), "r"(o3)
-                     : "memory");
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (2 * j + 1) * 128), "r"(o4),
-                     "r"(o5), "r"(o6), "r"(o7)
-                     : "memory");
+        uint32_t *oj = o + jj * 8;  // dims 16j .. 16j+15 of the row
+        oj[0] = e4m3x2_to_bf16x2<0x1404>(v0, sc2, sc2b, two);
+        oj[1] = e4m3x2_to_bf16x2<0x3424>(v0, sc2, sc2b, two);
+        oj[2] = e4m3x2_to_bf16x2<0x1404>(v1, sc2, sc2b, two);
+        oj[3] = e4m3x2_to_bf16x2<0x3424>(v1, sc2, sc2b, two);
+        oj[4] = e4m3x2_to_bf16x2<0x1404>(v2, sc2, sc2b, two);
+        oj[5] = e4m3x2_to_bf16x2<0x3424>(v2, sc2, sc2b, two);
+        oj[6] = e4m3x2_to_bf16x2<0x1404>(v3, sc2, sc2b, two);
+        oj[7] = e4m3x2_to_bf16x2<0x3424>(v3, sc2, sc2b, two);
       }
-      // the MMA reads the tile through the async proxy
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_st<DI / 4>(a_lane + c * (DI / 2) + hf * (DI / 4), o);
+      }
+      // the MMA may read the stage once every store has landed
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(c_full(c));
@@ -714,7 +812,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     }
   }
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 2 * a.ncols);
+  if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -776,6 +874,8 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   a.npad = (a.G * sh.h_idx + 15) / 16 * 16;
   a.hp = (a.G == 1) ? a.npad : sh.h_idx;
   a.ncols = pow2_at_least(a.npad);
+  a.tmem_cols = sh.idx_fp8 ? pow2_at_least(2 * a.ncols + kMaxCStages * sh.d_idx / 2) : 2 * a.ncols;
+  if (a.tmem_cols > 512) return cudaErrorInvalidValue;
   a.bpp_log2 = sh.log2_page - sh.log2_ratio;
   a.seq_ids = seq_ids;
   a.pos0 = pos0;
@@ -799,18 +899,19 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   const size_t a_stage = static_cast<size_t>(kTcTileBlocks) * sh.d_idx * 2;
   const size_t r_stage = fp8 ? static_cast<size_t>(kTcTileBlocks) * (sh.d_idx + sh.d_idx / 32) : a_stage;
   const size_t b_slots = 2ull * halves * a.npad * 128;
-  const size_t fixed = 1024 + (fp8 ? kMaxCStages * a_stage : 0) + b_slots + kEpiFloats * 4 + 8 * kNumBars + 16;
+  const size_t fixed = 1024 + b_slots + kEpiFloats * 4 + 8 * kNumBars + 16;
   const size_t smem_cap = 227 * 1024;
   int stages = static_cast<int>((smem_cap - fixed) / r_stage);
   const int max_stages = fp8 ? kMaxStages : kMaxStagesBf16;
   if (stages > max_stages) stages = max_stages;
-  if (stages < 2) return cudaErrorInvalidValue;
+  if (fp8) stages &= ~1;  // two rings of equal depth
+  if (stages < (fp8 ? 4 : 2)) return cudaErrorInvalidValue;
   size_t smem = fixed + stages * r_stage;
-  // TMEM: resident CTAs x 2 accumulators x ncols must stay within the SM's 512
-  // columns so tcgen05.alloc never waits on another CTA; raise the shared
-  // memory request until at most 512 / (2 ncols) CTAs fit on an SM.
+  // TMEM: resident CTAs x tmem_cols must stay within the SM's 512 columns so
+  // tcgen05.alloc never waits on another CTA; raise the shared memory request
+  // until at most 512 / tmem_cols CTAs fit on an SM.
   const size_t sm_smem = 233472;  // shared memory per SM (228 KB)
-  const int max_ctas = 512 / (2 * a.ncols);
+  const int max_ctas = 512 / a.tmem_cols;
   const size_t min_smem = sm_smem / (max_ctas + 1) - 1024 + 1;
   if (smem < min_smem) smem = min_smem;
   auto kern = fp8 ? (sh.d_idx == 128 ? score_tc_kernel<128, true> : score_tc_kernel<64, true>)

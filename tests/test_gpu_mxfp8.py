@@ -123,6 +123,14 @@ def test_scores_bit_exact():
             ref = orc.row(pos0[i] + j, "mxfp8")
             nb = ref["n_blk"]
             assert np.array_equal(scores[i * 2 + j, :nb].cpu().numpy().astype(np.float64), ref["scores"])
+    # the scorer rounds its queries itself: unrounded queries score the same
+    scores2 = torch.full((n, ld), float("nan"), dtype=torch.float32, device="cuda")
+    Q.qsa_index_score(g.cfg, rows, g.cache, inp["q_idx"], inp["w"], scores2, ld, g.status)
+    torch.cuda.synchronize()
+    g.check_status()
+    for r in range(n):
+        nb = (pos0[r // 2] + r % 2 + 1) // 4
+        assert torch.equal(scores2[r, :nb], scores[r, :nb])
 
 
 FUSED = {
