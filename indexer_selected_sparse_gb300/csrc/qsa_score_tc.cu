@@ -244,9 +244,10 @@ struct TcArgs {
 };
 
 constexpr int kMaxEpiWarps = 4 * kTcMaxGroup;  // one per (row of the group, TMEM lane quarter)
-// warp 0: producer, warp 1: MMA issuer, then epilogue (and MXFP8 converter)
-// warps, and a second producer warp last
-constexpr int kMaxThreads = 64 + 32 * kMaxEpiWarps + 32;
+// warp 0: producer, warp 1: MMA issuer, then epilogue warps (bf16: up to 4 x 4);
+// MXFP8: then 8 converter warps and a second producer warp, with G <= 2
+constexpr int kMaxThreads = 64 + 32 * kMaxEpiWarps;       // bf16 keys
+constexpr int kMaxThreadsFp8 = 64 + 32 * 8 + 32 * 8 + 32;  // MXFP8 keys
 constexpr int kMaxStages = 12;     // producer ring (bf16 keys: at most kMaxStagesBf16)
 constexpr int kMaxStagesBf16 = 6;
 constexpr int kMaxCStages = 4;     // MXFP8: bf16 A stages in TMEM filled by the converter warps
@@ -254,7 +255,8 @@ constexpr int kConvWarps = 8;      // MXFP8: converter warps, 4 per copy ring, a
 constexpr int kRowCols = 64;  // head columns of one row, at most
 // shared memory of the epilogue: per warp the weights of its row [kRowCols]
 constexpr int kEpiFloats = kMaxEpiWarps * kRowCols;
-constexpr int kNumBars = 2 * kMaxStages + 8 + 2 * kMaxCStages + 2;
+constexpr int kNumBars = 2 * kMaxStages + 8 + 2 * kMaxCStages + 2;  // MXFP8 keys
+constexpr int kNumBarsBf16 = 2 * kMaxStagesBf16 + 8;                 // bf16 keys
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -421,7 +423,7 @@ __device__ __forceinline__ uint32_t bf16x2_pow2(int e) {
 // DI/64 halves x npad rows x 128 B (128B swizzle). TMEM: two accumulators of
 // ncols columns, then (MXFP8) kMaxCStages A tiles of d_I / 2 columns.
 template <int DI, bool FP8>
-__global__ void __launch_bounds__(kMaxThreads, 1)
+__global__ void __launch_bounds__(FP8 ? kMaxThreadsFp8 : kMaxThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages) {
   constexpr int HALVES = DI / 64;
   constexpr int A_STAGE = kTcTileBlocks * DI * 2;  // one tile of keys, tiled pages back to back
@@ -435,7 +437,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
   const int S = n_stages;
   // copy rings: MXFP8 keeps one per producer warp (even and odd tiles), each with
   // its own converter warps, so a late page copy holds up only its own ring; bf16
-  // keeps one ring that both producers fill and the MMA drains
+  // keeps one ring, filled by the one producer and drained by the MMA
   constexpr int NR = FP8 ? 2 : 1;
   const int S_R = S / NR;
   const uint32_t a_u = base_u;  // bf16: the copy ring holds the MMA's A tiles
@@ -444,18 +446,22 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
   const uint32_t b_u = FP8 ? base_u : a_u + S * A_STAGE;
   const uint32_t r_u = FP8 ? b_u + 2 * b_slot : a_u;  // where the producers' copies land
   float *ws = reinterpret_cast<float *>(base + (FP8 ? 2 * b_slot + S * R_STAGE : S * A_STAGE + 2 * b_slot));
+  // barriers: MS copy stages (full, then empty), 2 B slots (full, empty), 2 TMEM
+  // buffers (full, empty), then (MXFP8) the A stages (full, empty) and 2 query slots
+  constexpr int MS = FP8 ? kMaxStages : kMaxStagesBf16;
+  constexpr int NBARS = FP8 ? kNumBars : kNumBarsBf16;
   const uint32_t bars = smem_u32(ws + kEpiFloats);
   // barrier addresses
   auto a_full = [&](int s) { return bars + 8u * s; };
-  auto a_empty = [&](int s) { return bars + 8u * (kMaxStages + s); };
-  auto b_full = [&](int s) { return bars + 8u * (2 * kMaxStages + s); };
-  auto b_empty = [&](int s) { return bars + 8u * (2 * kMaxStages + 2 + s); };
-  auto t_full = [&](int s) { return bars + 8u * (2 * kMaxStages + 4 + s); };
-  auto t_empty = [&](int s) { return bars + 8u * (2 * kMaxStages + 6 + s); };
-  auto c_full = [&](int s) { return bars + 8u * (2 * kMaxStages + 8 + s); };
-  auto c_empty = [&](int s) { return bars + 8u * (2 * kMaxStages + 8 + kMaxCStages + s); };
-  auto q_ready = [&](int s) { return bars + 8u * (2 * kMaxStages + 8 + 2 * kMaxCStages + s); };
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ws + kEpiFloats + 2 * kNumBars);
+  auto a_empty = [&](int s) { return bars + 8u * (MS + s); };
+  auto b_full = [&](int s) { return bars + 8u * (2 * MS + s); };
+  auto b_empty = [&](int s) { return bars + 8u * (2 * MS + 2 + s); };
+  auto t_full = [&](int s) { return bars + 8u * (2 * MS + 4 + s); };
+  auto t_empty = [&](int s) { return bars + 8u * (2 * MS + 6 + s); };
+  auto c_full = [&](int s) { return bars + 8u * (2 * MS + 8 + s); };
+  auto c_empty = [&](int s) { return bars + 8u * (2 * MS + 8 + kMaxCStages + s); };
+  auto q_ready = [&](int s) { return bars + 8u * (2 * MS + 8 + 2 * kMaxCStages + s); };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ws + kEpiFloats + 2 * NBARS);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const Shape &sh = a.sh;
@@ -491,15 +497,14 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
   const int pages_in_tile = kTcTileBlocks >> a.bpp_log2;
   const uint32_t page_bytes = FP8 ? static_cast<uint32_t>(fp8_page_bytes(bpp, DI)) : static_cast<uint32_t>(bpp) * DI * 2;
 
-  const int prod2 = static_cast<int>(blockDim.x >> 5) - 1;  // the second producer warp
+  // MXFP8: a second producer warp (the last one) for the second copy ring
+  const int prod2 = FP8 ? static_cast<int>(blockDim.x >> 5) - 1 : -1;
   if (warp == 0 || warp == prod2) {
     // ---------------- producers ----------------
-    // Two producer warps issue alternate tiles (warp 0 the even ones and every
-    // query load): one warp's stream of page copies is limited by its own issue
-    // and completion round trips (about 1.2 G random pages/s per producer on
-    // this part), two independent streams carry nearly twice as many pages.
-    // Both walk the same (group, tile) sequence; the ring's stages and their
-    // barrier phases are shared, so which warp fills a stage does not matter.
+    // MXFP8: two producer warps issue alternate tiles (warp 0 the even ones and
+    // every query load), each into its own ring: one in-order stream of random
+    // page copies tops out near 1.3 G pages/s on this part, two independent
+    // ones carry nearly 1.8. Both walk the same (group, tile) sequence.
     // Tiles are issued in batches of consecutive tiles of one group: lane L
     // holds the page id of page L of the batch. The page ids of the next batch
     // are loaded before the current batch's copies are issued, and the group's
@@ -563,7 +568,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         const int kr = k / NR;
         const int s = (k % NR) * S_R + kr % S_R;
         if (!waited && (kr >= S_R || (w.t + it + 1) * kTcTileBlocks > cur.nblk_old)) wait_now();
-        if ((k & 1) != par) continue;  // the other producer's tile
+        if (NR == 2 && (k & 1) != par) continue;  // the other producer's tile
         if (kr >= S_R && !mbar_wait_or_abort(a_empty(s), ((kr / S_R) - 1) & 1, abort_flag, a.status)) {
           ok = false;
           break;
@@ -866,9 +871,9 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   a.q_in_step = q_in_step ? 1 : 0;
   a.sh = sh;
   a.R = R;
-  // with the MXFP8 plane 8 converter warps join, so at most 2 rows share a tile
-  // (64 + 128 G + 256 + 32 threads within the 608 the kernel is built for)
-  const int g_max = sh.idx_fp8 ? (kMaxThreads - 96 - 32 * kConvWarps) / 128 : kTcMaxGroup;
+  // with the MXFP8 plane 8 converter warps and a second producer join, so at most
+  // 2 rows share a tile (64 + 128 G + 256 + 32 threads within kMaxThreadsFp8)
+  const int g_max = sh.idx_fp8 ? (kMaxThreadsFp8 - 96 - 32 * kConvWarps) / 128 : kTcMaxGroup;
   a.G = (sh.h_idx % 16 == 0) ? min(min(R, g_max), 256 / sh.h_idx) : 1;
   a.groups_per_seq = (R + a.G - 1) / a.G;
   a.npad = (a.G * sh.h_idx + 15) / 16 * 16;
@@ -899,7 +904,7 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   const size_t a_stage = static_cast<size_t>(kTcTileBlocks) * sh.d_idx * 2;
   const size_t r_stage = fp8 ? static_cast<size_t>(kTcTileBlocks) * (sh.d_idx + sh.d_idx / 32) : a_stage;
   const size_t b_slots = 2ull * halves * a.npad * 128;
-  const size_t fixed = 1024 + b_slots + kEpiFloats * 4 + 8 * kNumBars + 16;
+  const size_t fixed = 1024 + b_slots + kEpiFloats * 4 + 8 * (fp8 ? kNumBars : kNumBarsBf16) + 16;
   const size_t smem_cap = 227 * 1024;
   int stages = static_cast<int>((smem_cap - fixed) / r_stage);
   const int max_stages = fp8 ? kMaxStages : kMaxStagesBf16;
@@ -922,7 +927,7 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   int dev = 0, sms = 0, per_sm = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int threads = 64 + 128 * a.G + (fp8 ? 32 * kConvWarps : 0) + 32;  // + the second producer
+  const int threads = 64 + 128 * a.G + (fp8 ? 32 * kConvWarps + 32 : 0);  // MXFP8: converters, second producer
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem)) != cudaSuccess)
     return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
