@@ -336,13 +336,27 @@ def select_blocks(scores, topk: int) -> np.ndarray:
     return np.sort(order[:topk])
 
 
-def token_set(sel, n_blk: int, visible: int, ratio: int) -> np.ndarray:
+def token_set(sel, n_blk: int, visible: int, ratio: int, window: int = 0) -> np.ndarray:
     """Selected blocks expanded to token positions, plus the tail
     [n_blk*ratio, visible) of the incomplete block ([VA6] expansion; [LC3]
-    tail always visible). Ascending."""
+    tail always visible). Ascending.
+
+    window > 0 also keeps the last `window` visible tokens ("Agentic shootout",
+    "Flash-Next support: llama.cpp vs Atlas", (d) adoption plan, phase 2, item 6
+    "Sparse attention gather": the last 128 tokens are always kept, a union with
+    the top-k set; the same report's (a) hparams bullet names llama.cpp's
+    indexer_local_blocks). Reading: the selection is
+    made as without the window; the token set is its union with
+    [visible - window, visible) and the tail, i.e. the selected tokens before
+    run_start = min(visible - window, n_blk*ratio) followed by the run
+    [run_start, visible)."""
     sel = np.asarray(sel, np.int64)
     body = (sel[:, None] * ratio + np.arange(ratio)[None, :]).reshape(-1)
-    tail = np.arange(n_blk * ratio, visible, dtype=np.int64)
+    run_start = n_blk * ratio
+    if window > 0:
+        run_start = min(run_start, max(0, visible - window))
+    body = body[body < run_start]
+    tail = np.arange(run_start, visible, dtype=np.int64)
     return np.concatenate([body, tail])
 
 
@@ -371,12 +385,13 @@ def gqa_attention(q_bits, k_bits, v_bits) -> np.ndarray:
 
 
 def attend_row(state: SeqState, pos: int, q_idx_bits, w, q_bits, topk: int,
-               index_format: str = "bf16") -> Dict:
+               index_format: str = "bf16", window: int = 0) -> Dict:
     """The whole path for one query row at logical position pos.
 
     The row's token is already ingested, so V = pos + 1 tokens are visible and
     n_blk = V // ratio blocks are complete. index_format "mxfp8" scores with
-    the MXFP8 index plane (block_scores_mxfp8)."""
+    the MXFP8 index plane (block_scores_mxfp8); window keeps the last `window`
+    tokens as well (token_set)."""
     r = state.ratio
     visible = pos + 1
     if visible > state.ingested:
@@ -388,13 +403,13 @@ def attend_row(state: SeqState, pos: int, q_idx_bits, w, q_bits, topk: int,
     else:
         scores = None                        # everything is selected; no scoring needed
     sel = select_blocks(scores if scores is not None else np.zeros(n_blk), topk)
-    toks = token_set(sel, n_blk, visible, r)
+    toks = token_set(sel, n_blk, visible, r, window)
     out = gqa_attention(q_bits, state.K[toks], state.V[toks])
     return {"n_blk": n_blk, "scores": scores, "sel": sel, "tokens": toks,
             "out": out, "out_bf16": f64_to_bf16_bits(out)}
 
 
-def attend_row_reused(state: SeqState, pos: int, sel, sel_pos: int, q_bits) -> Dict:
+def attend_row_reused(state: SeqState, pos: int, sel, sel_pos: int, q_bits, window: int = 0) -> Dict:
     """Attention of the row at logical position pos with a block selection made
     earlier, by the row at sel_pos <= pos ("Flash-Next support: vLLM vs Atlas",
     (a) item 6, MTP: later draft steps reuse the step-0 selection while the side
@@ -416,7 +431,7 @@ def attend_row_reused(state: SeqState, pos: int, sel, sel_pos: int, q_bits) -> D
     sel = np.asarray(sel, np.int64)
     if sel.size and (sel.min() < 0 or sel.max() >= n_blk_sel):
         raise ValueError("reused selection names a block that was not complete at sel_pos")
-    toks = token_set(sel, n_blk_sel, visible, r)
+    toks = token_set(sel, n_blk_sel, visible, r, window)
     out = gqa_attention(q_bits, state.K[toks], state.V[toks])
     return {"n_blk_sel": n_blk_sel, "sel": sel, "tokens": toks, "out": out,
             "out_bf16": f64_to_bf16_bits(out)}
@@ -462,7 +477,7 @@ def dense_attention(q_bits, k_bits, v_bits, n_kv_heads: int) -> np.ndarray:
 
 
 def step(states: List[SeqState], pos0: List[int], k_new, v_new, idx_new,
-         q_idx, w, q, topk: int, rows_per_seq: int, index_format: str = "bf16") -> List[Dict]:
+         q_idx, w, q, topk: int, rows_per_seq: int, index_format: str = "bf16", window: int = 0) -> List[Dict]:
     """Append each sequence's R new tokens, then run every row.
 
     k_new/v_new [n_seq*R, Hkv, D], idx_new [n_seq*R, d_I], q_idx
@@ -476,5 +491,5 @@ def step(states: List[SeqState], pos0: List[int], k_new, v_new, idx_new,
     for i, st in enumerate(states):
         for j in range(R):
             row = i * R + j
-            out.append(attend_row(st, pos0[i] + j, q_idx[row], w[row], q[row], topk, index_format))
+            out.append(attend_row(st, pos0[i] + j, q_idx[row], w[row], q[row], topk, index_format, window))
     return out

@@ -168,6 +168,21 @@ def mxfp8_scores_keys_only(q_idx_bits, w, blk_bits):
     return np.asarray(w, np.float64) @ np.maximum(q @ k.T, 0.0)
 
 
+def _token_set_with(run_start_fn, name):
+    def ts(sel, n_blk, visible, ratio, window=0):
+        sel = np.asarray(sel, np.int64)
+        body = (sel[:, None] * ratio + np.arange(ratio)[None, :]).reshape(-1)
+        rs = run_start_fn(n_blk * ratio, visible, window, ratio) if window > 0 else n_blk * ratio
+        return np.concatenate([body[body < rs], np.arange(rs, visible, dtype=np.int64)])
+    ts.__name__ = name
+    return ts
+
+
+window_block_aligned = _token_set_with(lambda t0, V, W, r: min(t0, max(0, (V - W) // r * r)), "window_block_aligned")
+window_off_by_one = _token_set_with(lambda t0, V, W, r: min(t0, max(0, V - W + 1)), "window_off_by_one")
+window_drops_tail = _token_set_with(lambda t0, V, W, r: max(0, V - W), "window_drops_tail")
+
+
 MUTATIONS = [
     ("block_scores", no_relu, [P.test_score_closed_forms]),
     ("block_scores", relu_outside, [P.test_score_closed_forms]),
@@ -189,6 +204,9 @@ MUTATIONS = [
     ("mxfp8_quantize", mxfp8_emax_7, [P.test_mxfp8_scale_rule_on_hand_worked_blocks]),
     ("mxfp8_quantize", mxfp8_one_scale_per_vector, [P.test_mxfp8_scales_are_per_32_value_block]),
     ("block_scores_mxfp8", mxfp8_scores_keys_only, [P.test_mxfp8_scores_hand_worked_and_identity_on_small_integers]),
+    ("token_set", window_block_aligned, [P.test_local_window_is_the_union_with_the_last_tokens]),
+    ("token_set", window_off_by_one, [P.test_local_window_is_the_union_with_the_last_tokens]),
+    ("token_set", window_drops_tail, [P.test_local_window_is_the_union_with_the_last_tokens]),
 ]
 
 

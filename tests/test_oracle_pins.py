@@ -645,3 +645,57 @@ def test_mxfp8_scores_hand_worked_and_identity_on_small_integers():
     kb = bf16(rng.integers(-8, 9, size=(20, 64)))
     w = rng.standard_normal(6)
     assert np.array_equal(O.block_scores_mxfp8(qi, w, kb), O.block_scores(qi, w, kb))
+
+
+# ---------------------------------------------------------------------------
+# Always-kept local window ("Flash-Next support: llama.cpp vs Atlas", (d)
+# adoption plan, phase 2, item 6: the last 128 tokens are kept, a union with
+# the top-k set).
+# ---------------------------------------------------------------------------
+
+
+def test_local_window_is_the_union_with_the_last_tokens():
+    rng = np.random.default_rng(73)
+    for _ in range(300):
+        r = int(rng.choice([2, 4, 8]))
+        V = int(rng.integers(1, 400))
+        n_blk = V // r
+        k = int(rng.integers(0, n_blk + 1))
+        sel = np.sort(rng.choice(n_blk, size=k, replace=False)) if k else np.zeros(0, np.int64)
+        W = int(rng.integers(0, 300))
+        got = O.token_set(sel, n_blk, V, r, W)
+        # brute force over positions: selected block, the tail, or among the last W
+        want = [t for t in range(V) if (t // r in set(sel.tolist()) and t < n_blk * r) or t >= n_blk * r
+                or (W > 0 and t >= V - W)]
+        assert got.tolist() == want
+    # window 0 is the plain token set; a window covering everything is dense
+    sel = np.array([1, 5, 9])
+    assert np.array_equal(O.token_set(sel, 12, 50, 4, 0), O.token_set(sel, 12, 50, 4))
+    assert O.token_set(sel, 12, 50, 4, 50).tolist() == list(range(50))
+
+
+def test_local_window_hand_worked_row():
+    # V = 5000 visible, ratio 4 (1250 complete blocks), window 128: the run starts
+    # at 4872 = block 1218. Selected blocks 3 and 1217 lie before it (8 tokens),
+    # block 1218 starts exactly at the run, block 1240 lies inside it: 8 + 128 tokens.
+    toks = O.token_set(np.array([3, 1217, 1218, 1240]), 1250, 5000, 4, 128)
+    assert toks.tolist() == [12, 13, 14, 15, 4868, 4869, 4870, 4871] + list(range(4872, 5000))
+    # a run start inside a selected block keeps that block's earlier tokens: V = 5001
+    # puts it at 4873 (inside block 1218): tokens 4872 plus the run 4873..5000
+    toks = O.token_set(np.array([1218]), 1250, 5001, 4, 128)
+    assert toks.tolist() == [4872] + list(range(4873, 5001))
+
+
+def test_attend_row_with_window_at_and_below_the_bound_is_dense():
+    rng = np.random.default_rng(79)
+    st = make_state(rng, 40, 4)                     # 40 tokens, K = 4 blocks
+    q = bf16(rng.standard_normal((4, 16)))
+    qi = bf16(rng.integers(-8, 9, size=(8,)))[None].repeat(1, 0).reshape(1, 8); w = np.ones(1)
+    # below the bound (n_blk <= K) the window changes nothing: dense
+    res0 = O.attend_row(st, 14, qi, w, q, 4)
+    res1 = O.attend_row(st, 14, qi, w, q, 4, window=8)
+    assert np.array_equal(res0["tokens"], np.arange(15)) and np.array_equal(res1["tokens"], np.arange(15))
+    # past the bound the window adds the recent tokens the selection left out
+    res = O.attend_row(st, 39, qi, w, q, 4, window=12)
+    assert set(range(28, 40)) <= set(res["tokens"].tolist())
+    assert set(O.token_set(res["sel"], 10, 40, 4).tolist()) <= set(res["tokens"].tolist())
