@@ -63,6 +63,8 @@ def parse():
                     help="decode steps through the pre-indexer (norm + RoPE of queries and keys); 0 skips")
     ap.add_argument("--mxfp8-steps", type=int, default=600,
                     help="decode steps with the MXFP8 index plane (own cache); 0 skips")
+    ap.add_argument("--window-steps", type=int, default=300,
+                    help="decode steps with a 128-token always-kept local window; 0 skips")
     ap.add_argument("--prefill-warmup", type=int, default=3)
     return ap.parse_args()
 
@@ -211,7 +213,8 @@ def run_gpu(args):
     total_steps = W + K + args.breakdown_steps + args.e2e_steps + 4
     adv_per_batch = (math.ceil((W + K + min(K, 600) + args.e2e_steps + 4) / NB) + (62 if args.reuse_steps > 0 else 0)
                      + (math.ceil(args.pre_steps / NB) + 2 if args.pre_steps > 0 else 0)
-                     + (math.ceil(args.mxfp8_steps / NB) + 2 if args.mxfp8_steps > 0 else 0))
+                     + (math.ceil(args.mxfp8_steps / NB) + 2 if args.mxfp8_steps > 0 else 0)
+                     + (math.ceil(args.window_steps / NB) + 2 if args.window_steps > 0 else 0))
     # center the prefixes of the main timed region on 32768
     start = wl.prefixes[0] - W // NB - K // (2 * NB)
     start = max(start, 8)
@@ -373,10 +376,46 @@ def run_gpu(args):
     if args.pre_steps > 0:
         out["pre_indexer"] = run_pre(args, Q, S, torch, cfg, sh, cache, batches, status, stream, NB, B, hbm_gbs,
                                      ms)
+    if args.window_steps > 0:
+        out["local_window"] = run_window(args, Q, torch, sh, cache, batches, status, stream, NB, B, ms)
     if args.mxfp8_steps > 0:
         out["mxfp8"] = run_mxfp8(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, NB, B,
                                  hbm_gbs, ms)
     return out, rank, world
+
+
+def run_window(args, Q, torch, sh, cache, batches, status, stream, NB, B, ms_plain, window=128):
+    """The decode step with an always-kept local window (local_window = 128: every
+    row also attends to its last 128 tokens, a union with the top-k set), on the
+    decode leg's cache and inputs: one rotation graph of the NB batches."""
+    dev = cache.k_pool.device
+    cfg_w = Q.Config.of(sh, Q.QSA_INDEX_BF16, window)
+    ws = Q.workspace(cfg_w, B, cache.max_blocks, device=dev)
+    rot = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(rot, stream=stream):
+        for bt in batches:
+            Q.qsa_decode(cfg_w, Q.Rows(bt["ids"], bt["pos0"], 1, advance=True), cache, bt["k"], bt["v"], bt["idx"],
+                         bt["q_idx"], bt["w"], bt["q"], bt["out"], ws, status, stream=stream)
+    torch.cuda.synchronize()
+    n_rot = max(1, math.ceil(args.window_steps / NB))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        rot.replay()  # warm-up rotation
+        e0.record(stream)
+        for _ in range(n_rot):
+            rot.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st == 0, f"device status {st}: {Q.qsa_strerror(st)}"
+    steps = n_rot * NB
+    ms = e0.elapsed_time(e1) / steps
+    return {"what": f"decode step with a {window}-token always-kept local window (union with the top-k set), "
+                    "batch 32 x 32k", "window": window,
+            "steps": steps, "ms_per_step": round(ms, 5), "rows_per_s": round(B / (ms * 1e-3), 1),
+            "overhead_vs_plain_ms": round(ms - ms_plain, 5),
+            "tokens_per_row": "selected tokens before the run + the last 128 (at most budget + 128 + ratio - 1)"}
 
 
 def run_mxfp8(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, NB, B, hbm_gbs, ms_plain):

@@ -89,6 +89,7 @@ typedef enum qsa_status {
  *   page_size  (P) 64, multiple of ratio        tokens per cache page
  *   index_format QSA_INDEX_BF16 or QSA_INDEX_MXFP8 (the latter with
  *              P / ratio >= 8 blocks per page)  compressed-key plane
+ *   local_window in [0, 16384]                  always-kept recent tokens
  * The indexer has one key head (MQA), as the pages require.
  *
  * Index formats. QSA_INDEX_BF16: compressed keys are bf16 and the index
@@ -102,7 +103,16 @@ typedef enum qsa_status {
  * value / scale rounded to nearest-even and clamped to +-448 -- and the fused
  * step puts each index query head through the same quantisation before
  * scoring. The key quantised is the bf16 compressed key of QSA_INDEX_BF16;
- * scores are exact sums of the quantised values' products in fp32. */
+ * scores are exact sums of the quantised values' products in fp32.
+ *
+ * Local window ("Agentic shootout", "Flash-Next support: llama.cpp vs Atlas",
+ * (d) adoption plan, phase 2, item 6: the last 128 tokens are always kept, a
+ * union with the top-k set; llama.cpp's indexer_local_blocks): with
+ * local_window = W > 0 every row attends to its selected blocks, its tail and
+ * its last W visible tokens. The selection itself is unchanged; the token set
+ * is the selected tokens before min(V - W, n_blk * ratio) followed by every
+ * token from there to the row. Attention then takes up to budget + W +
+ * ratio - 1 tokens (qsa_max_attend_tokens, qsa_workspace_bytes grow with W). */
 #define QSA_INDEX_BF16 0
 #define QSA_INDEX_MXFP8 1
 typedef struct qsa_config {
@@ -115,6 +125,7 @@ typedef struct qsa_config {
   int head_dim;
   int page_size;
   int index_format; /* QSA_INDEX_BF16 (0) or QSA_INDEX_MXFP8 (1) */
+  int local_window; /* always-kept recent tokens per row (0: none) */
 } qsa_config;
 
 /* The query rows of one step. The step appends rows_per_seq (R) tokens to

@@ -37,6 +37,7 @@ int check_cfg(const qsa_config *c) {
   if (c->n_q_heads / c->n_kv_heads > 8) return QSA_ERR_UNSUPPORTED;
   if (c->page_size != 64 || c->page_size % c->ratio != 0) return QSA_ERR_UNSUPPORTED;
   if (c->index_format != QSA_INDEX_BF16 && c->index_format != QSA_INDEX_MXFP8) return QSA_ERR_UNSUPPORTED;
+  if (c->local_window < 0 || c->local_window > kMaxLocalWindow) return QSA_ERR_UNSUPPORTED;
   // the MXFP8 plane is scored on the tensor-core path: 8 or more blocks per page
   if (c->index_format == QSA_INDEX_MXFP8 && c->page_size / c->ratio < 8) return QSA_ERR_UNSUPPORTED;
   return QSA_OK;
@@ -56,6 +57,7 @@ Shape make_shape(const qsa_config *c) {
   s.log2_ratio = ilog2(c->ratio);
   s.log2_page = ilog2(c->page_size);
   s.idx_fp8 = c->index_format == QSA_INDEX_MXFP8 ? 1 : 0;
+  s.window = c->local_window;
   return s;
 }
 

@@ -6,10 +6,16 @@
 // flash-decode over scattered slots needs a gather + flash pass).
 //
 // Token set of a row with V visible tokens, n_blk = V/ratio complete blocks
-// and n_sel selected blocks (ascending ids in sel):
-//   slot j <  n_sel*ratio : token sel[j/ratio]*ratio + j%ratio
-//   slot j >= n_sel*ratio : token n_blk*ratio + (j - n_sel*ratio)   (the tail)
-// n_slots = n_sel*ratio + (V - n_blk*ratio) <= budget + ratio - 1.
+// and n_sel selected blocks (ascending ids in sel): the selected tokens before
+// run0, then the run [run0, V), where run0 = n_blk*ratio (the tail), or with an
+// always-kept local window of W tokens ("Flash-Next support: llama.cpp vs
+// Atlas", (d) adoption plan, phase 2, item 6: the last 128 tokens are kept, a
+// union with the top-k set) run0 = min(n_blk*ratio, V - W):
+//   slot j <  n_body : token sel[j/ratio]*ratio + j%ratio
+//   slot j >= n_body : token run0 + (j - n_body)
+// n_body = the selected tokens before run0 (whole blocks, plus the part of a
+// selected block that run0 cuts); n_slots = n_body + V - run0 <=
+// budget + W + ratio - 1.
 //
 // A unit of work is one split (a fixed range of kSplitSlots slots) of one row.
 // A CTA takes up to kMaxUnitsPerCta units (u = blockIdx.x + k * gridDim.x),
@@ -51,16 +57,16 @@ struct AttnGeom {
   static constexpr int kStageBytes = 2 * kHalfStage;
 };
 
-__device__ __forceinline__ int slot_token(int j, int n_body, int log2r, int r, int tail0,
+__device__ __forceinline__ int slot_token(int j, int n_body, int log2r, int r, int run0,
                                           const int32_t *sel_row) {
-  return j < n_body ? sel_row[j >> log2r] * r + (j & (r - 1)) : tail0 + (j - n_body);
+  return j < n_body ? sel_row[j >> log2r] * r + (j & (r - 1)) : run0 + (j - n_body);
 }
 
 // One unit: split `sp` of row `row`, its slot range and token-set layout, and
 // where its sequence's page-table row sits in the CTA's page cache (-1: read
 // from global memory).
 struct AttnUnit {
-  int row, sp, seq, visible, n_blk, n_body, tail0, slot_lo, slot_hi, n_chunks, pc_off;
+  int row, sp, seq, visible, n_blk, n_body, run0, slot_lo, slot_hi, n_chunks, pc_off;
 };
 
 template <int HKV>
@@ -152,14 +158,15 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
   // boundary to the row ("Flash-Next support: vLLM vs Atlas", (a) item 6, MTP
   // skip_topk; "Flash-Next support: llama.cpp vs Atlas", (a) item 3, shared
   // indexer layers).
-  if (tid < nu) {
-    AttnUnit &U = s_unit[tid];
+  // One warp per unit (every lane computes the same values; lane 0 stores them).
+  if (warp < nu) {
+    AttnUnit &U = s_unit[warp];
     bool row_ok = U.n_blk >= 0;
     int n_blk = row_ok ? U.n_blk : 0;
     if (row_ok && sel_pos) {
       const int ps = sel_pos[U.row];
       if (ps < 0 || ps >= U.visible) {
-        if (U.sp == 0) report(status, QSA_ERR_REUSE);
+        if (U.sp == 0 && lane == 0) report(status, QSA_ERR_REUSE);
         row_ok = false;
         n_blk = 0;
       } else {
@@ -167,16 +174,39 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
       }
     }
     const int n_sel = row_ok ? min(max(n_sel_arr[U.row], 0), min(n_blk, sh.topk)) : 0;
-    U.n_body = n_sel * r;
-    U.tail0 = n_blk * r;
-    int n_slots = row_ok ? U.n_body + (U.visible - U.tail0) : 0;
+    int n_body = n_sel * r;
+    int run0 = n_blk * r;
+    if (row_ok && sh.window > 0 && U.visible - sh.window < run0) {
+      run0 = max(U.visible - sh.window, 0);
+      // selected blocks starting at or after run0 are a suffix of the ascending
+      // list: count them 32 at a time from the end
+      const int32_t *sel_row = sel + static_cast<size_t>(U.row) * sh.topk;
+      int keep = n_sel;
+      for (int top = n_sel - 1; top >= 0; top -= 32) {
+        const int idx = top - lane;
+        const unsigned late = __ballot_sync(0xffffffffu, idx >= 0 && sel_row[idx] * r >= run0);
+        keep -= __popc(late);
+        if (late != 0xffffffffu) break;
+      }
+      n_body = keep * r;
+      if (keep > 0) {  // run0 may cut the last selected block before it
+        const int b0 = sel_row[keep - 1] * r;
+        if (b0 + r > run0) n_body = (keep - 1) * r + (run0 - b0);
+      }
+    }
+    int n_slots = row_ok ? n_body + (U.visible - run0) : 0;
     if (n_slots > n_split * split_len) {  // a reused selection too old for the split plan
-      if (U.sp == 0) report(status, QSA_ERR_REUSE);
+      if (U.sp == 0 && lane == 0) report(status, QSA_ERR_REUSE);
       n_slots = n_split * split_len;
     }
-    U.slot_lo = min(n_slots, U.sp * split_len);  // fixed cut: independent of the batch
-    U.slot_hi = min(n_slots, U.slot_lo + split_len);
-    U.n_chunks = (U.slot_hi - U.slot_lo + G::kChunk - 1) / G::kChunk;
+    __syncwarp();
+    if (lane == 0) {
+      U.n_body = n_body;
+      U.run0 = run0;
+      U.slot_lo = min(n_slots, U.sp * split_len);  // fixed cut: independent of the batch
+      U.slot_hi = min(n_slots, U.slot_lo + split_len);
+      U.n_chunks = (U.slot_hi - U.slot_lo + G::kChunk - 1) / G::kChunk;
+    }
   }
   __syncthreads();
 
@@ -192,7 +222,7 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
         const AttnUnit &U = s_unit[k];
         const int j = U.slot_lo + tid;
         if (j < U.slot_hi)
-          tok[k] = slot_token(j, U.n_body, sh.log2_ratio, r, U.tail0, sel + static_cast<size_t>(U.row) * sh.topk);
+          tok[k] = slot_token(j, U.n_body, sh.log2_ratio, r, U.run0, sel + static_cast<size_t>(U.row) * sh.topk);
       }
     }
 #pragma unroll
@@ -530,7 +560,7 @@ struct SplitPlan {
 // bit for bit.
 SplitPlan plan_splits(const Shape &sh, int rows) {
   (void)rows;
-  const int max_slots = sh.budget + sh.ratio - 1;
+  const int max_slots = sh.budget + sh.window + sh.ratio - 1;
   return {(max_slots + kSplitSlots - 1) / kSplitSlots, kSplitSlots};
 }
 

@@ -21,6 +21,7 @@
 namespace qsa {
 
 constexpr int kMaxTopK = 2048;
+constexpr int kMaxLocalWindow = 16384;  // always-kept local window, tokens
 constexpr int kHeadDim = 128;
 
 // Device-side status codes go through a first-error-wins CAS.
@@ -73,6 +74,7 @@ struct Shape {
   int ratio, budget, topk, h_idx, d_idx, hq, hkv, d, page;
   int log2_ratio, log2_page;
   int idx_fp8;  // compressed keys in the MXFP8 plane (index queries MXFP8-rounded)
+  int window;   // always-kept local window: the last `window` tokens of every row (0: none)
 };
 
 // --- MXFP8 block-pool pages --------------------------------------------------

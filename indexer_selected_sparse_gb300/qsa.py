@@ -59,7 +59,8 @@ LIB_PATH = _LIB_PATH
 class qsa_config(ctypes.Structure):
     _fields_ = [("ratio", ctypes.c_int), ("budget", ctypes.c_int), ("n_idx_heads", ctypes.c_int),
                 ("idx_dim", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
-                ("head_dim", ctypes.c_int), ("page_size", ctypes.c_int), ("index_format", ctypes.c_int)]
+                ("head_dim", ctypes.c_int), ("page_size", ctypes.c_int), ("index_format", ctypes.c_int),
+                ("local_window", ctypes.c_int)]
 
 
 class qsa_pre_indexer(ctypes.Structure):
@@ -178,20 +179,22 @@ class Config:
     head_dim: int = 128
     page_size: int = 64
     index_format: int = QSA_INDEX_BF16
+    local_window: int = 0
 
     def c(self) -> qsa_config:
         return qsa_config(self.ratio, self.budget, self.n_idx_heads, self.idx_dim,
                           self.n_q_heads, self.n_kv_heads, self.head_dim, self.page_size,
-                          self.index_format)
+                          self.index_format, self.local_window)
 
     @property
     def topk(self) -> int:
         return self.budget // self.ratio
 
     @classmethod
-    def of(cls, shapes, index_format: int = QSA_INDEX_BF16) -> "Config":
+    def of(cls, shapes, index_format: int = QSA_INDEX_BF16, local_window: int = 0) -> "Config":
         return cls(shapes.ratio, shapes.budget, shapes.n_idx_heads, shapes.idx_dim,
-                   shapes.n_q_heads, shapes.n_kv_heads, shapes.head_dim, shapes.page_size, index_format)
+                   shapes.n_q_heads, shapes.n_kv_heads, shapes.head_dim, shapes.page_size, index_format,
+                   local_window)
 
 
 class PagedCache:

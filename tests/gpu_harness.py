@@ -100,13 +100,13 @@ class GpuState:
 
     def __init__(self, wl: S.Workload, extra_tokens: int = 64, contiguous: Optional[bool] = None,
                  page_seed: Optional[int] = None, device: str = "cuda", slots: Optional[List[int]] = None,
-                 index_format: int = 0):
+                 index_format: int = 0, local_window: int = 0):
         from indexer_selected_sparse_gb300 import qsa as Q
         self.Q = Q
         self.wl = wl
         self.sh = wl.shapes
         self.irange = wl.extra.get("int_range", (-8, 8))
-        self.cfg = Q.Config.of(self.sh, index_format)
+        self.cfg = Q.Config.of(self.sh, index_format, local_window)
         self.device = device
         P = self.sh.page_size
         need = max(wl.prefixes) + wl.rows_per_seq + extra_tokens
@@ -263,7 +263,7 @@ class OracleSeq:
         self.st.V[need] = bits(v)
         self.filled[need] = True
 
-    def row(self, pos: int, index_format: str = "bf16"):
+    def row(self, pos: int, index_format: str = "bf16", window: int = 0):
         """Oracle result for the query row at `pos` (uses that row's q inputs)."""
         sh = self.sh
         ep = int(self.hist.epochs(np.array([pos]))[0])
@@ -276,8 +276,8 @@ class OracleSeq:
             sel = O.select_blocks(sc, sh.topk)
         else:
             sel = np.arange(n_blk)
-        self.fill_kv(O.token_set(sel, n_blk, visible, sh.ratio))
-        return O.attend_row(self.st, pos, bits(qi[0]), w[0].numpy(), bits(q[0]), sh.topk, index_format)
+        self.fill_kv(O.token_set(sel, n_blk, visible, sh.ratio, window))
+        return O.attend_row(self.st, pos, bits(qi[0]), w[0].numpy(), bits(q[0]), sh.topk, index_format, window)
 
 
 def compare_row(gpu_out_bits: np.ndarray, gpu_sel: np.ndarray, gpu_nsel: int, ref: Dict, topk: int):

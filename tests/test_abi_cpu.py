@@ -163,3 +163,16 @@ def test_index_format_checked_and_page_bytes(Q):
     assert Q.LIB.qsa_quantize_index_q(cfg, 0, None, None, None) == Q.QSA_OK      # nothing to do
     assert Q.LIB.qsa_quantize_index_q(cfg, 3, None, None, None) == Q.QSA_ERR_INVALID_ARG
     assert Q.LIB.qsa_quantize_index_q(cfg, -1, None, None, None) == Q.QSA_ERR_INVALID_ARG
+
+
+def test_local_window_checked_and_sizes_grow(Q):
+    base = Q.Config(4, 2048, 64, 128, 32, 4)
+    win = Q.Config(4, 2048, 64, 128, 32, 4, local_window=128)
+    assert Q.qsa_config_check(win) == Q.QSA_OK
+    assert Q.qsa_config_check(Q.Config(4, 2048, 64, 128, 32, 4, local_window=-1)) == Q.QSA_ERR_UNSUPPORTED
+    assert Q.qsa_config_check(Q.Config(4, 2048, 64, 128, 32, 4, local_window=16385)) == Q.QSA_ERR_UNSUPPORTED
+    # the split plan covers budget + W + ratio - 1 tokens
+    assert Q.qsa_max_attend_tokens(win) >= 2048 + 128 + 3
+    assert Q.qsa_max_attend_tokens(base) >= 2048 + 3
+    assert Q.qsa_max_attend_tokens(win) > Q.qsa_max_attend_tokens(base)
+    assert Q.qsa_workspace_bytes(win, 32, 8200) > Q.qsa_workspace_bytes(base, 32, 8200)
