@@ -169,6 +169,45 @@ def pool_block_pre(raw_bits, first_pos: int, pre: PreIndexer) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# Main-attention options ("Agentic shootout", "Flash-Next support: vLLM vs
+# Atlas", (a) item 6, Dataflow bullet: the attention is GQA with a sigmoid
+# output gate, always on, and GemmaRMSNorm on the q and k heads; a fused
+# QK-norm + RoPE + gate path). The pages leave the gate's granularity, epsilon
+# and the RoPE base open. Readings: the gate is elementwise (one value per query
+# head and dimension), o' = o * sigmoid(g), applied before the output's bf16
+# rounding; each q and k head is Gemma-RMSNormed over D, then NeoX-roped at its
+# token's position (the same two functions as the pre-indexer), the key when it
+# is appended to the cache.
+# ---------------------------------------------------------------------------
+
+
+class AttnOptions:
+    """gamma_q, gamma_k: per-dimension gains [D] of the q and k head norms (None:
+    that side is not normed or roped); eps, theta, rotary_dim as in PreIndexer."""
+
+    def __init__(self, gamma_q=None, gamma_k=None, eps: float = 1e-6, theta: float = 1e4,
+                 rotary_dim: int = 64):
+        self.gamma_q = None if gamma_q is None else np.asarray(gamma_q, np.float64)
+        self.gamma_k = None if gamma_k is None else np.asarray(gamma_k, np.float64)
+        self.eps = float(eps)
+        self.theta = float(theta)
+        self.rotary_dim = int(rotary_dim)
+
+
+def prep_heads(x_bits, pos: int, gamma, eps: float, rotary_dim: int, theta: float) -> np.ndarray:
+    """Heads [H, D] of the token at pos: Gemma RMSNorm per head, then RoPE at pos;
+    bf16 bits."""
+    x = bf16_bits_to_f64(x_bits)
+    return f64_to_bf16_bits(rope_neox(gemma_rmsnorm(x, gamma, eps), pos, rotary_dim, theta))
+
+
+def sigmoid(x) -> np.ndarray:
+    """1 / (1 + exp(-x)), fp64."""
+    x = np.asarray(x, np.float64)
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+# ---------------------------------------------------------------------------
 # MXFP8 index plane ("Agentic shootout", "Flash-Next support: vLLM vs Atlas",
 # the report whose (a) item 3 is "QSA sparse attention + n-gram indexer",
 # Scores bullet: with an MXFP8 indexer cache both the index queries and the
@@ -248,9 +287,10 @@ class SeqState:
     """
 
     def __init__(self, ratio: int, n_kv_heads: int, head_dim: int, idx_dim: int,
-                 capacity: int, pre: "PreIndexer" = None):
+                 capacity: int, pre: "PreIndexer" = None, attn: "AttnOptions" = None):
         self.ratio = ratio
         self.pre = pre  # compressed keys through the pre-indexer when given
+        self.attn = attn  # key heads normed and roped as they are appended, when given
         self.capacity = capacity
         self.K = np.zeros((capacity, n_kv_heads, head_dim), np.uint16)
         self.V = np.zeros((capacity, n_kv_heads, head_dim), np.uint16)
@@ -275,6 +315,10 @@ class SeqState:
             raise DesyncError(f"append at pos {pos} but {self.ingested} tokens ingested")
         if pos + n > self.capacity:
             raise CapacityError(f"append of {n} at pos {pos} exceeds capacity {self.capacity}")
+        if self.attn is not None and self.attn.gamma_k is not None:
+            a = self.attn
+            k_bits = np.stack([prep_heads(k_bits[t], pos + t, a.gamma_k, a.eps, a.rotary_dim, a.theta)
+                               for t in range(n)]) if n else k_bits
         self.K[pos:pos + n] = k_bits
         self.V[pos:pos + n] = np.asarray(v_bits, np.uint16)
         self.idx_raw[pos:pos + n] = np.asarray(idx_bits, np.uint16)
@@ -385,13 +429,15 @@ def gqa_attention(q_bits, k_bits, v_bits) -> np.ndarray:
 
 
 def attend_row(state: SeqState, pos: int, q_idx_bits, w, q_bits, topk: int,
-               index_format: str = "bf16", window: int = 0) -> Dict:
+               index_format: str = "bf16", window: int = 0, attn: "AttnOptions" = None,
+               gate_bits=None) -> Dict:
     """The whole path for one query row at logical position pos.
 
     The row's token is already ingested, so V = pos + 1 tokens are visible and
     n_blk = V // ratio blocks are complete. index_format "mxfp8" scores with
     the MXFP8 index plane (block_scores_mxfp8); window keeps the last `window`
-    tokens as well (token_set)."""
+    tokens as well (token_set). attn (with gamma_q) norms and ropes the query
+    heads at pos; gate_bits [Hq, D] gates the output: o * sigmoid(g)."""
     r = state.ratio
     visible = pos + 1
     if visible > state.ingested:
@@ -404,7 +450,11 @@ def attend_row(state: SeqState, pos: int, q_idx_bits, w, q_bits, topk: int,
         scores = None                        # everything is selected; no scoring needed
     sel = select_blocks(scores if scores is not None else np.zeros(n_blk), topk)
     toks = token_set(sel, n_blk, visible, r, window)
+    if attn is not None and attn.gamma_q is not None:
+        q_bits = prep_heads(q_bits, pos, attn.gamma_q, attn.eps, attn.rotary_dim, attn.theta)
     out = gqa_attention(q_bits, state.K[toks], state.V[toks])
+    if gate_bits is not None:
+        out = out * sigmoid(bf16_bits_to_f64(gate_bits))
     return {"n_blk": n_blk, "scores": scores, "sel": sel, "tokens": toks,
             "out": out, "out_bf16": f64_to_bf16_bits(out)}
 

@@ -183,6 +183,27 @@ window_off_by_one = _token_set_with(lambda t0, V, W, r: min(t0, max(0, V - W + 1
 window_drops_tail = _token_set_with(lambda t0, V, W, r: max(0, V - W), "window_drops_tail")
 
 
+class KeysRopedAtZero(O.SeqState):
+    def append(self, pos, k_bits, v_bits, idx_bits):
+        if self.attn is not None and self.attn.gamma_k is not None:
+            a = self.attn
+            k_bits = np.asarray(k_bits, np.uint16)
+            k_bits = np.stack([O.prep_heads(k_bits[t], 0, a.gamma_k, a.eps, a.rotary_dim, a.theta)
+                               for t in range(len(k_bits))])
+            saved, self.attn = self.attn, None
+            try:
+                super().append(pos, k_bits, v_bits, idx_bits)
+            finally:
+                self.attn = saved
+        else:
+            super().append(pos, k_bits, v_bits, idx_bits)
+
+
+def sigmoid_of_minus(x):
+    x = np.asarray(x, np.float64)
+    return 1.0 / (1.0 + np.exp(x))
+
+
 MUTATIONS = [
     ("block_scores", no_relu, [P.test_score_closed_forms]),
     ("block_scores", relu_outside, [P.test_score_closed_forms]),
@@ -207,6 +228,8 @@ MUTATIONS = [
     ("token_set", window_block_aligned, [P.test_local_window_is_the_union_with_the_last_tokens]),
     ("token_set", window_off_by_one, [P.test_local_window_is_the_union_with_the_last_tokens]),
     ("token_set", window_drops_tail, [P.test_local_window_is_the_union_with_the_last_tokens]),
+    ("SeqState", KeysRopedAtZero, [P.test_attention_qk_norm_rope_and_gate_hand_worked]),
+    ("sigmoid", sigmoid_of_minus, [P.test_sigmoid_closed_forms, P.test_attention_qk_norm_rope_and_gate_hand_worked]),
 ]
 
 

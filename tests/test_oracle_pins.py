@@ -699,3 +699,50 @@ def test_attend_row_with_window_at_and_below_the_bound_is_dense():
     res = O.attend_row(st, 39, qi, w, q, 4, window=12)
     assert set(range(28, 40)) <= set(res["tokens"].tolist())
     assert set(O.token_set(res["sel"], 10, 40, 4).tolist()) <= set(res["tokens"].tolist())
+
+
+# ---------------------------------------------------------------------------
+# Main-attention options ("Flash-Next support: vLLM vs Atlas", (a) item 6,
+# Dataflow bullet: sigmoid output gate, GemmaRMSNorm q/k heads, QK-norm + RoPE).
+# ---------------------------------------------------------------------------
+
+
+def test_attention_qk_norm_rope_and_gate_hand_worked():
+    # D = 4, one head, gains 0, eps 0, rotary 4: a head [1, 0, 0, 0] normalises to
+    # [2, 0, 0, 0] (rms 1/2) and at position p becomes [2 cos p, 0, 2 sin p, 0]
+    # (pair (0, 2) turns by p, pair (1, 3) is zero). Keys at 0 and 1, the row at 1:
+    # q.k0 = 4 cos 1, q.k1 = 4; logits (scale 1/2) 2 cos 1 and 2; V0 = [1, 0, 1, 1],
+    # V1 = [0, 1, 1, -1], so out = [w0, 1 - w0, 1, 2 w0 - 1] with
+    # w0 = 1 / (1 + exp(2 - 2 cos 1)).
+    a = O.AttnOptions(np.zeros(4), np.zeros(4), eps=0.0, theta=1e4, rotary_dim=4)
+    st = O.SeqState(2, 1, 4, 8, 8, attn=a)
+    k = bf16([[[1, 0, 0, 0]], [[1, 0, 0, 0]]])
+    v = bf16([[[1, 0, 1, 1]], [[0, 1, 1, -1]]])
+    st.append(0, k, v, bf16(np.zeros((2, 8))))
+    q = bf16([[1, 0, 0, 0]])
+    res = O.attend_row(st, 1, bf16(np.zeros((1, 8))), np.ones(1), q, 4, attn=a)
+    w0 = 1.0 / (1.0 + math.exp(2.0 - 2.0 * math.cos(1.0)))
+    assert np.allclose(res["out"][0], [w0, 1 - w0, 1, 2 * w0 - 1], atol=1e-2)
+    assert abs(res["out"][0][0] - 0.285) < 1e-2
+    # the stored keys are the prepared ones: k0 = [2, 0, 0, 0], k1 = [2 cos 1, 0, 2 sin 1, 0]
+    kk = O.bf16_bits_to_f64(st.K[:2, 0])
+    assert np.allclose(kk[0], [2, 0, 0, 0]) and np.allclose(kk[1], [2 * math.cos(1), 0, 2 * math.sin(1), 0], atol=1e-2)
+    # gate: sigmoid(ln 3) = 3/4, sigmoid(0) = 1/2, sigmoid(-ln 3) = 1/4, sigmoid(30) = 1 - 1e-13
+    g = bf16([[math.log(3), 0.0, -math.log(3), 30.0]])
+    gl = O.bf16_bits_to_f64(g)[0]
+    gated = O.attend_row(st, 1, bf16(np.zeros((1, 8))), np.ones(1), q, 4, attn=a, gate_bits=g)
+    assert np.allclose(gated["out"][0] / res["out"][0],
+                       [1 / (1 + math.exp(-gl[0])), 0.5, 1 / (1 + math.exp(-gl[2])), 1.0], atol=1e-12)
+    assert abs(1 / (1 + math.exp(-gl[0])) - 0.75) < 2e-3 and abs(1 / (1 + math.exp(-gl[2])) - 0.25) < 2e-3
+    # without options the path is unchanged
+    st0 = O.SeqState(2, 1, 4, 8, 8)
+    st0.append(0, k, v, bf16(np.zeros((2, 8))))
+    plain = O.attend_row(st0, 1, bf16(np.zeros((1, 8))), np.ones(1), q, 4)
+    assert np.allclose(plain["out"][0], [0.5, 0.5, 1, 0])
+
+
+def test_sigmoid_closed_forms():
+    assert O.sigmoid(0.0) == 0.5
+    assert abs(O.sigmoid(math.log(3)) - 0.75) < 1e-15 and abs(O.sigmoid(-math.log(3)) - 0.25) < 1e-15
+    x = np.linspace(-20, 20, 81)
+    assert np.allclose(O.sigmoid(x) + O.sigmoid(-x), 1.0, atol=1e-15)
