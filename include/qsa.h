@@ -350,6 +350,48 @@ int qsa_decode_pre(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_
                    int32_t *sel_out, int32_t *n_sel_out, qsa_bf16 *out, void *ws, size_t ws_bytes,
                    int32_t *status, cudaStream_t stream);
 
+/* Main-attention options of the fused step ("Agentic shootout", "Flash-Next
+ * support: vLLM vs Atlas", (a) item 6, Dataflow bullet: GQA with a sigmoid
+ * output gate, always on, GemmaRMSNorm q/k heads, a fused QK-norm + RoPE +
+ * gate path). Each member is optional:
+ *   gamma_q  device [D] fp32: every query head of the step becomes
+ *            bf16(RoPE_{row position}(GemmaRMSNorm(q_h))) (gains 1 + gamma_q) in the
+ *            workspace; q itself is not written
+ *   gamma_k  device [D] fp32: every appended key head is stored as
+ *            bf16(RoPE_{token position}(GemmaRMSNorm(k_h))); a cache must be filled
+ *            with one kind of append throughout (qsa_append_ex with the same gamma_k)
+ *   eps, rope_theta, rotary_dim   as in qsa_pre_indexer (rotary_dim 0, 64 or D)
+ *   gate     device [rows, Hq, D] bf16: the output is o * sigmoid(gate),
+ *            elementwise, before its bf16 rounding
+ * The pages leave the gate's granularity, epsilon and the RoPE base open:
+ * elementwise, and both inputs. */
+typedef struct qsa_attn_options {
+  const float *gamma_q;
+  const float *gamma_k;
+  float eps;
+  float rope_theta;
+  int rotary_dim;
+  const qsa_bf16 *gate;
+} qsa_attn_options;
+
+/* qsa_append / qsa_append_pre with optional index pre-indexer and main
+ * attention options (only gamma_k acts here). Either pointer may be NULL. */
+int qsa_append_ex(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_attn_options *attn,
+                  const qsa_rows *rows, const qsa_cache *cache, const qsa_bf16 *k_new,
+                  const qsa_bf16 *v_new, const qsa_bf16 *idx_k_new, int32_t *status, cudaStream_t stream);
+
+/* Bytes of workspace qsa_decode_ex needs with any options: qsa_workspace_bytes
+ * plus the prepared index and main query rows. */
+size_t qsa_workspace_bytes_ex(const qsa_config *cfg, int max_rows, int max_blocks_per_row);
+
+/* The fused step with optional index pre-indexer (as qsa_decode_pre) and main
+ * attention options (above). With both NULL it is qsa_decode. */
+int qsa_decode_ex(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_attn_options *attn,
+                  const qsa_rows *rows, const qsa_cache *cache, const qsa_bf16 *k_new, const qsa_bf16 *v_new,
+                  const qsa_bf16 *idx_k_new, const qsa_bf16 *q_idx, const float *w, const qsa_bf16 *q,
+                  int32_t *sel_out, int32_t *n_sel_out, qsa_bf16 *out, void *ws, size_t ws_bytes,
+                  int32_t *status, cudaStream_t stream);
+
 /* Tokens one row's attention can take: the split plan covers
  * ceil((budget + ratio - 1) / 112) splits of 112 tokens. A reused selection
  * (below) may be used while its token set stays within this count. Returns 0

@@ -179,7 +179,38 @@ PreArgs pre_args(const qsa_pre_indexer *p, const uint16_t *q_in, uint16_t *q_out
 // The fused step; pre != nullptr: through the pre-indexer (the append kernel
 // pre-indexes the step's query rows into the workspace, the score kernel reads
 // them after its dependency wait).
-int decode_impl(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_rows *rows,
+// Main-attention options: gains present where given, eps >= 0, theta > 0,
+// rotary dims 0, 64 or D.
+int check_attn(const qsa_attn_options *a) {
+  if (!a) return QSA_OK;
+  if (!(a->eps >= 0.f) || !(a->rope_theta > 0.f) || a->eps > 1e30f || a->rope_theta > 1e30f)
+    return QSA_ERR_INVALID_ARG;
+  if (a->rotary_dim != 0 && a->rotary_dim != 64 && a->rotary_dim != kHeadDim) return QSA_ERR_UNSUPPORTED;
+  if (a->gate && !aligned16(a->gate)) return QSA_ERR_INVALID_ARG;
+  return QSA_OK;
+}
+
+AttnPrep attn_prep(const qsa_attn_options *a, const uint16_t *q_in, uint16_t *q_out) {
+  AttnPrep p;
+  p.gamma_q = a->gamma_q;
+  p.gamma_k = a->gamma_k;
+  p.eps = a->eps;
+  p.rot = a->rotary_dim;
+  p.q_in = q_in;
+  p.q_out = q_out;
+  const double pi = std::acos(-1.0);
+  for (int i = 0; i < p.rot / 2; ++i)
+    p.half_turns[i] = std::pow(static_cast<double>(a->rope_theta), -2.0 * i / p.rot) / pi;
+  return p;
+}
+
+// Bytes of the prepared main query rows of `rows` rows.
+size_t q_main_bytes(const Shape &sh, int rows) {
+  return static_cast<size_t>(rows) * sh.hq * kHeadDim * sizeof(uint16_t);
+}
+
+int decode_impl(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_attn_options *att,
+                const qsa_rows *rows,
                 const qsa_cache *cache, const qsa_bf16 *k_new, const qsa_bf16 *v_new,
                 const qsa_bf16 *idx_k_new, const qsa_bf16 *q_idx, const float *w, const qsa_bf16 *q,
                 int32_t *sel_out, int32_t *n_sel_out, qsa_bf16 *out, void *ws, size_t ws_bytes,
@@ -205,13 +236,16 @@ int decode_impl(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_row
   // workspace by the append kernel, and the score kernel reads them there (with
   // the MXFP8 plane the score kernel rounds its query tiles itself)
   const bool q_prep = pre != nullptr;
-  const size_t need = L.total + (q_prep ? round_up(q_prep_bytes(sh, n_rows), 256) : 0);
+  const bool q_main = att && att->gamma_q;  // main queries normed + roped into the workspace
+  const size_t idx_bytes = q_prep ? round_up(q_prep_bytes(sh, n_rows), 256) : 0;
+  const size_t need = L.total + idx_bytes + (q_main ? round_up(q_main_bytes(sh, n_rows), 256) : 0);
   if (ws_bytes < need) return QSA_ERR_WORKSPACE;
   uint8_t *base = static_cast<uint8_t *>(ws);
   float *scores = reinterpret_cast<float *>(base + L.scores);
   int32_t *sel = sel_out ? sel_out : reinterpret_cast<int32_t *>(base + L.sel);
   int32_t *n_sel = n_sel_out ? n_sel_out : reinterpret_cast<int32_t *>(base + L.n_sel);
   uint16_t *q_pre = q_prep ? reinterpret_cast<uint16_t *>(base + L.total) : nullptr;
+  uint16_t *q_att = q_main ? reinterpret_cast<uint16_t *>(base + L.total + idx_bytes) : nullptr;
   const CacheView cv = view(cache);
   const int R = rows->rows_per_seq;
 
@@ -219,10 +253,12 @@ int decode_impl(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_row
   if (pre) pa = pre_args(pre, q_idx, q_pre);
   pa.q_in = q_prep ? q_idx : nullptr;
   pa.q_out = q_pre;
+  AttnPrep ap;
+  if (att) ap = attn_prep(att, q_main ? q : nullptr, q_att);
   cudaError_t e = launch_append(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cache->page_table,
                                 cache->max_pages, cache->num_pages, cache->k_pool, cache->v_pool,
                                 cache->idxraw_pool, cache->idxblk_pool, cache->ingested, k_new,
-                                v_new, idx_k_new, status, true, stream, &pa);
+                                v_new, idx_k_new, status, true, stream, &pa, att ? &ap : nullptr);
   if (e == cudaSuccess)
     e = launch_score(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, q_prep ? q_pre : q_idx, w, scores, ld,
                      status, true, stream, q_prep);
@@ -240,8 +276,8 @@ int decode_impl(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_row
   commit.pos0 = rows->pos0;
   commit.ingested = cache->ingested;
   if (e == cudaSuccess)
-    e = launch_attn(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, q, sel, n_sel, out,
-                    base + L.partials, status, true, commit, stream);
+    e = launch_attn(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, q_main ? q_att : q, sel, n_sel, out,
+                    base + L.partials, status, true, commit, stream, nullptr, att ? att->gate : nullptr);
   return cuda_status(e);
 }
 }  // namespace
@@ -394,7 +430,7 @@ int qsa_decode(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cac
                const qsa_bf16 *q_idx, const float *w, const qsa_bf16 *q, int32_t *sel_out,
                int32_t *n_sel_out, qsa_bf16 *out, void *ws, size_t ws_bytes, int32_t *status,
                cudaStream_t stream) {
-  return decode_impl(cfg, nullptr, rows, cache, k_new, v_new, idx_k_new, q_idx, w, q, sel_out, n_sel_out,
+  return decode_impl(cfg, nullptr, nullptr, rows, cache, k_new, v_new, idx_k_new, q_idx, w, q, sel_out, n_sel_out,
                      out, ws, ws_bytes, status, stream);
 }
 
@@ -453,8 +489,59 @@ int qsa_decode_pre(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_
   int rc;
   if ((rc = check_cfg(cfg)) != QSA_OK) return rc;
   if ((rc = check_pre(cfg, pre, true, true)) != QSA_OK) return rc;
-  return decode_impl(cfg, pre, rows, cache, k_new, v_new, idx_k_new, q_idx, w, q, sel_out, n_sel_out, out, ws,
-                     ws_bytes, status, stream);
+  return decode_impl(cfg, pre, nullptr, rows, cache, k_new, v_new, idx_k_new, q_idx, w, q, sel_out, n_sel_out, out,
+                     ws, ws_bytes, status, stream);
+}
+
+size_t qsa_workspace_bytes_ex(const qsa_config *cfg, int max_rows, int max_blocks_per_row) {
+  if (check_cfg(cfg) != QSA_OK || max_rows < 0 || max_blocks_per_row < 0) return 0;
+  const Shape sh = make_shape(cfg);
+  const WsLayout L = ws_layout(sh, max_rows, ld_for(max_blocks_per_row));
+  return L.total + round_up(q_prep_bytes(sh, max_rows), 256) + round_up(q_main_bytes(sh, max_rows), 256);
+}
+
+int qsa_append_ex(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_attn_options *attn,
+                  const qsa_rows *rows, const qsa_cache *cache, const qsa_bf16 *k_new, const qsa_bf16 *v_new,
+                  const qsa_bf16 *idx_k_new, int32_t *status, cudaStream_t stream) {
+  int rc;
+  if ((rc = check_cfg(cfg)) != QSA_OK) return rc;
+  if (pre && (rc = check_pre(cfg, pre, false, true)) != QSA_OK) return rc;
+  if ((rc = check_attn(attn)) != QSA_OK) return rc;
+  if ((rc = check_rows(rows)) != QSA_OK) return rc;
+  if ((rc = check_cache(cache, true, true)) != QSA_OK) return rc;
+  if (!cache->ingested || !status) return QSA_ERR_INVALID_ARG;
+  const long long n_rows = static_cast<long long>(rows->n_seq) * rows->rows_per_seq;
+  if (n_rows == 0) return QSA_OK;
+  if (!k_new || !v_new || !idx_k_new || !aligned16(k_new) || !aligned16(v_new) || !aligned16(idx_k_new))
+    return QSA_ERR_INVALID_ARG;
+  if ((rc = host_capacity_check(rows, cache, cfg->page_size)) != QSA_OK) return rc;
+  const Shape sh = make_shape(cfg);
+  PreArgs pa;
+  if (pre) pa = pre_args(pre, nullptr, nullptr);
+  AttnPrep ap;
+  if (attn) ap = attn_prep(attn, nullptr, nullptr);  // keys only
+  cudaError_t e = launch_append(sh, rows->n_seq, rows->rows_per_seq, rows->seq_ids, rows->pos0,
+                                cache->page_table, cache->max_pages, cache->num_pages,
+                                cache->k_pool, cache->v_pool, cache->idxraw_pool, cache->idxblk_pool,
+                                cache->ingested, k_new, v_new, idx_k_new, status, false, stream, &pa,
+                                attn ? &ap : nullptr);
+  if (e == cudaSuccess)
+    e = launch_commit(rows->n_seq, rows->rows_per_seq, cache->max_pages * cfg->page_size,
+                      rows->seq_ids, rows->pos0, cache->ingested, rows->advance, false, stream);
+  return cuda_status(e);
+}
+
+int qsa_decode_ex(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_attn_options *attn,
+                  const qsa_rows *rows, const qsa_cache *cache, const qsa_bf16 *k_new, const qsa_bf16 *v_new,
+                  const qsa_bf16 *idx_k_new, const qsa_bf16 *q_idx, const float *w, const qsa_bf16 *q,
+                  int32_t *sel_out, int32_t *n_sel_out, qsa_bf16 *out, void *ws, size_t ws_bytes,
+                  int32_t *status, cudaStream_t stream) {
+  int rc;
+  if ((rc = check_cfg(cfg)) != QSA_OK) return rc;
+  if (pre && (rc = check_pre(cfg, pre, true, true)) != QSA_OK) return rc;
+  if ((rc = check_attn(attn)) != QSA_OK) return rc;
+  return decode_impl(cfg, pre, attn, rows, cache, k_new, v_new, idx_k_new, q_idx, w, q, sel_out, n_sel_out, out,
+                     ws, ws_bytes, status, stream);
 }
 
 int qsa_gather_attn_reuse(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache *cache,

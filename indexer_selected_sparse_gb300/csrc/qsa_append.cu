@@ -26,8 +26,8 @@ constexpr int kQPrepCtas = 8 * 152;  // query pre-indexing CTAs of one launch, a
 // brought to [-1, 1] by subtracting the nearest even integer, which is exact in
 // double; only the sine and cosine of that small angle are taken in fp32, so the
 // angle itself carries no fp32 rounding at large positions.
-__device__ __forceinline__ float2 rope_cs(int pos, int i, const PreArgs &pre) {
-  const double t = static_cast<double>(pos) * pre.half_turns[i];
+__device__ __forceinline__ float2 rope_cs(int pos, int i, const double *half_turns) {
+  const double t = static_cast<double>(pos) * half_turns[i];
   const double red = t - 2.0 * rint(0.5 * t);
   float sn, cs;
   sincospif(static_cast<float>(red), &sn, &cs);
@@ -79,47 +79,71 @@ __device__ __forceinline__ void mx_quantize_lanes(const float (&x)[D32], uint32_
 // bf16 value of x (round to nearest even) as fp32.
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-// The query vectors (row, index head) of sequence i into q_out, one warp per
-// vector: RoPE(GemmaRMSNorm) when pre.gamma_q is set, rounded to bf16, then
-// with the MXFP8 plane the MXFP8 round trip. Vector v is row i*R + v / h_idx at
-// position p0 + v / h_idx, head v % h_idx; a CTA takes vectors slot*8 + warp,
-// striding by n_slots*8, so a decode step's 64 heads spread over 8 CTAs.
+// One warp, one vector of 32 * D32 values at in[base] -> out[base]: RoPE(Gemma
+// RMSNorm) at pos when gamma is set, rounded to bf16, then the MXFP8 round trip
+// when fp8 is set.
 template <int D32>
-__device__ void pre_index_queries(const Shape &sh, const PreArgs &pre, int i, int R, int p0, int slot,
-                                  int n_slots) {
+__device__ __forceinline__ void prep_vector(const uint16_t *__restrict__ in, uint16_t *__restrict__ out,
+                                            size_t base, int pos, const float *gamma, float eps, int rot,
+                                            const double *half_turns, bool fp8, int lane) {
+  float x[D32];
+#pragma unroll
+  for (int m = 0; m < D32; ++m) x[m] = bf16_bits_to_float(in[base + lane + 32 * m]);
+  if (gamma) {
+    pre_index_lanes<D32>(x, gamma, eps, rot, 32 * D32, lane, [&](int ip) { return rope_cs(pos, ip, half_turns); });
+#pragma unroll
+    for (int m = 0; m < D32; ++m) x[m] = round_bf16(x[m]);
+  }
+  if (fp8) {
+    uint32_t code[D32];
+    int ex[D32];
+    mx_quantize_lanes<D32>(x, code, ex);
+#pragma unroll
+    for (int m = 0; m < D32; ++m) x[m] = e4m3_value(code[m]) * exp2_int(ex[m]);  // exact in bf16
+  }
+#pragma unroll
+  for (int m = 0; m < D32; ++m) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x[m]);
+    out[base + lane + 32 * m] = *reinterpret_cast<const uint16_t *>(&h);
+  }
+}
+
+// The step's query vectors of sequence i, one warp per vector: first the index
+// query heads (pre.q_out set: RoPE(GemmaRMSNorm) with pre.gamma_q, then with the
+// MXFP8 plane the MXFP8 round trip), then the main query heads (att.q_out set:
+// RoPE(GemmaRMSNorm) with att.gamma_q over D). Index vector v is row i*R + v / H_I
+// at position p0 + v / H_I; main vectors likewise with Hq. A CTA takes vectors
+// slot*8 + warp, striding by n_slots*8, so a decode step's heads spread over CTAs.
+__device__ void prep_queries(const Shape &sh, const PreArgs &pre, const AttnPrep &att, int i, int R, int p0,
+                             int slot, int n_slots) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
-  const int n_vec = R * sh.h_idx;
+  const int n_idx = pre.q_out ? R * sh.h_idx : 0;
+  const int n_vec = n_idx + (att.q_out ? R * sh.hq : 0);
   for (int v = slot * n_warps + warp; v < n_vec; v += n_slots * n_warps) {
-    const int t = v / sh.h_idx;
-    const size_t base = (static_cast<size_t>(i) * R * sh.h_idx + v) * sh.d_idx;
-    float x[D32];
-#pragma unroll
-    for (int m = 0; m < D32; ++m) x[m] = bf16_bits_to_float(pre.q_in[base + lane + 32 * m]);
-    if (pre.gamma_q) {
-      pre_index_lanes<D32>(x, pre.gamma_q, pre.eps, pre.rot, sh.d_idx, lane,
-                           [&](int ip) { return rope_cs(p0 + t, ip, pre); });
-#pragma unroll
-      for (int m = 0; m < D32; ++m) x[m] = round_bf16(x[m]);
-    }
-    if (sh.idx_fp8) {
-      uint32_t code[D32];
-      int ex[D32];
-      mx_quantize_lanes<D32>(x, code, ex);
-#pragma unroll
-      for (int m = 0; m < D32; ++m) x[m] = e4m3_value(code[m]) * exp2_int(ex[m]);  // exact in bf16
-    }
-#pragma unroll
-    for (int m = 0; m < D32; ++m) {
-      const __nv_bfloat16 h = __float2bfloat16_rn(x[m]);
-      pre.q_out[base + lane + 32 * m] = *reinterpret_cast<const uint16_t *>(&h);
+    if (v < n_idx) {
+      const int t = v / sh.h_idx;
+      const size_t base = (static_cast<size_t>(i) * R * sh.h_idx + v) * sh.d_idx;
+      if (sh.d_idx == 128)
+        prep_vector<4>(pre.q_in, pre.q_out, base, p0 + t, pre.gamma_q, pre.eps, pre.rot, pre.half_turns,
+                       sh.idx_fp8 != 0, lane);
+      else
+        prep_vector<2>(pre.q_in, pre.q_out, base, p0 + t, pre.gamma_q, pre.eps, pre.rot, pre.half_turns,
+                       sh.idx_fp8 != 0, lane);
+    } else {
+      const int vm = v - n_idx;
+      const int t = vm / sh.hq;
+      const size_t base = (static_cast<size_t>(i) * R * sh.hq + vm) * kHeadDim;
+      prep_vector<kHeadDim / 32>(att.q_in, att.q_out, base, p0 + t, att.gamma_q, att.eps, att.rot, att.half_turns,
+                                 false, lane);
     }
   }
 }
 
-// Query-prep CTAs of one sequence for R rows of n_seq sequences: 8 vectors
-// (one per warp) each, capped so a launch holds at most kQPrepCtas of them.
-int q_prep_ctas(const Shape &sh, int n_seq, int R) {
-  const long long want = (static_cast<long long>(R) * sh.h_idx + 7) / 8;
+// Query-prep CTAs of one sequence for R rows of n_seq sequences with `heads`
+// vectors per row: 8 vectors (one per warp) each, capped so a launch holds at
+// most kQPrepCtas of them.
+int q_prep_ctas(int heads, int n_seq, int R) {
+  const long long want = (static_cast<long long>(R) * heads + 7) / 8;
   const long long cap = kQPrepCtas / n_seq > 1 ? kQPrepCtas / n_seq : 1;
   return static_cast<int>(want < cap ? want : cap);
 }
@@ -164,7 +188,7 @@ __device__ void pool_block_warp(const Shape &sh, const PreArgs &pre, int b, int 
   const int first = b * r;
   if (pre.gamma_k)
     pre_index_lanes<D32>(x, pre.gamma_k, pre.eps, pre.rot, sh.d_idx, lane,
-                         [&](int ip) { return rope_cs(first, ip, pre); });
+                         [&](int ip) { return rope_cs(first, ip, pre.half_turns); });
   const int rr = b & (bpp - 1);
   if (sh.idx_fp8) {
 #pragma unroll
@@ -198,7 +222,7 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
               void *__restrict__ blk_pool, const int32_t *__restrict__ ingested,
               const uint16_t *__restrict__ k_new, const uint16_t *__restrict__ v_new,
               const uint16_t *__restrict__ idx_new, int32_t *status, int n_chunks,
-              const __grid_constant__ PreArgs pre) {
+              const __grid_constant__ PreArgs pre, const __grid_constant__ AttnPrep att) {
   // the previous step's commit (ingested, pos0) when launched as a dependent; only
   // then may the score kernel start: its prologue reads the positions
   pdl_wait();
@@ -206,12 +230,9 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
   const int i = blockIdx.x;
   const int p0 = pos0[i];
   if (static_cast<int>(blockIdx.y) >= n_chunks) {
-    // the step's query rows through the pre-indexer (only when pre.q_out is set)
-    const int slot = blockIdx.y - n_chunks, n_slots = gridDim.y - n_chunks;
-    if (sh.d_idx == 128)
-      pre_index_queries<4>(sh, pre, i, R, p0, slot, n_slots);
-    else
-      pre_index_queries<2>(sh, pre, i, R, p0, slot, n_slots);
+    // the step's query vectors: index queries (pre.q_out set) and main queries
+    // (att.q_out set)
+    prep_queries(sh, pre, att, i, R, p0, blockIdx.y - n_chunks, gridDim.y - n_chunks);
     return;
   }
   const int s = seq_ids[i];
@@ -232,6 +253,7 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
   if (t_begin >= t_end) return;
 
   // 1. copy rows: per token, Hkv*D/8 uint4 of K, the same of V, d_I/8 of raw key
+  // (K rows that go through the q/k norm are written in 1b instead)
   const int kv16 = sh.hkv * sh.d / 8;
   const int ix16 = sh.d_idx / 8;
   const int per_tok = 2 * kv16 + ix16;
@@ -239,6 +261,7 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
   for (int e = threadIdx.x; e < n_work; e += blockDim.x) {
     const int tl = e / per_tok;
     const int c = e - tl * per_tok;
+    if (att.gamma_k && c < kv16) continue;
     const int j = t_begin + tl;
     const int pos = p0 + j;
     const int page = ptab[pos >> sh.log2_page];
@@ -261,6 +284,34 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
       dst = reinterpret_cast<uint4 *>(raw_pool + slot * ix16 * 8) + (c - 2 * kv16);
     }
     *dst = __ldg(src);
+  }
+
+  // 1b. key heads through GemmaRMSNorm + RoPE at the token's position, one warp
+  // per (token, KV head)
+  if (att.gamma_k) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
+    for (int v = warp; v < (t_end - t_begin) * sh.hkv; v += n_warps) {
+      const int tl = v / sh.hkv, h = v - tl * sh.hkv;
+      const int j = t_begin + tl;
+      const int pos = p0 + j;
+      const int page = ptab[pos >> sh.log2_page];
+      if (page < 0 || page >= num_pages) {
+        if (lane == 0) report(status, QSA_ERR_PAGE);
+        continue;
+      }
+      const size_t src = ((static_cast<size_t>(i) * R + j) * sh.hkv + h) * kHeadDim;
+      float x[kHeadDim / 32];
+#pragma unroll
+      for (int m = 0; m < kHeadDim / 32; ++m) x[m] = bf16_bits_to_float(k_new[src + lane + 32 * m]);
+      pre_index_lanes<kHeadDim / 32>(x, att.gamma_k, att.eps, att.rot, kHeadDim, lane,
+                                     [&](int ip) { return rope_cs(pos, ip, att.half_turns); });
+      uint16_t *dst = k_pool + ((static_cast<size_t>(page) * P + (pos & (P - 1))) * sh.hkv + h) * kHeadDim;
+#pragma unroll
+      for (int m = 0; m < kHeadDim / 32; ++m) {
+        const __nv_bfloat16 hb = __float2bfloat16_rn(x[m]);
+        dst[lane + 32 * m] = *reinterpret_cast<const uint16_t *>(&hb);
+      }
+    }
   }
 
   // 2. pool the blocks whose last token is one of this CTA's tokens: block b
@@ -328,10 +379,7 @@ pre_index_q_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const __gr
   pdl_trigger();
   const int i = blockIdx.x;
   const int p0 = pos0 ? pos0[i] : 0;  // no positions: MXFP8 round trip only
-  if (sh.d_idx == 128)
-    pre_index_queries<4>(sh, pre, i, R, p0, blockIdx.y, gridDim.y);
-  else
-    pre_index_queries<2>(sh, pre, i, R, p0, blockIdx.y, gridDim.y);
+  prep_queries(sh, pre, AttnPrep{}, i, R, p0, blockIdx.y, gridDim.y);
 }
 
 __global__ void commit_kernel(int n_seq, int R, int capacity, const int32_t *__restrict__ seq_ids,
@@ -371,14 +419,15 @@ cudaError_t launch_append(const Shape &sh, int n_seq, int R, const int32_t *seq_
                           uint16_t *idxraw_pool, void *idxblk_pool, const int32_t *ingested,
                           const uint16_t *k_new, const uint16_t *v_new,
                           const uint16_t *idx_k_new, int32_t *status, bool pdl, cudaStream_t st,
-                          const PreArgs *pre) {
+                          const PreArgs *pre, const AttnPrep *att) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
   const int n_chunks = (R + kAppendTokensPerCta - 1) / kAppendTokensPerCta;
-  const int n_q = pre && pre->q_out ? q_prep_ctas(sh, n_seq, R) : 0;
+  const int q_heads = (pre && pre->q_out ? sh.h_idx : 0) + (att && att->q_out ? sh.hq : 0);
+  const int n_q = q_heads > 0 ? q_prep_ctas(q_heads, n_seq, R) : 0;
   dim3 grid(n_seq, n_chunks + n_q);
   return launch_kernel(pdl, append_kernel, grid, dim3(kAppendThreads), 0, st, sh, R, seq_ids, pos0, page_table,
                        max_pages, num_pages, k_pool, v_pool, idxraw_pool, idxblk_pool, ingested, k_new, v_new,
-                       idx_k_new, status, n_chunks, pre ? *pre : PreArgs{});
+                       idx_k_new, status, n_chunks, pre ? *pre : PreArgs{}, att ? *att : AttnPrep{});
 }
 
 cudaError_t launch_pre_index_q(const Shape &sh, int n_seq, int R, const int32_t *pos0, const PreArgs &pre,
@@ -387,7 +436,7 @@ cudaError_t launch_pre_index_q(const Shape &sh, int n_seq, int R, const int32_t 
   PreArgs p = pre;
   p.q_in = q_in;
   p.q_out = q_out;
-  dim3 grid(n_seq, q_prep_ctas(sh, n_seq, R));
+  dim3 grid(n_seq, q_prep_ctas(sh.h_idx, n_seq, R));
   return launch_kernel(pdl, pre_index_q_kernel, grid, dim3(kAppendThreads), 0, st, sh, R, pos0, p);
 }
 

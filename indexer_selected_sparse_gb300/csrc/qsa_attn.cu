@@ -476,7 +476,7 @@ constexpr int kMergeThreads = 256;
 __global__ void __launch_bounds__(kMergeThreads)
 merge_kernel(int hq, int hkv, int n_split, const float *__restrict__ part_m,
              const float *__restrict__ part_l, const float *__restrict__ part_acc,
-             uint16_t *__restrict__ out, CommitArgs cm) {
+             uint16_t *__restrict__ out, CommitArgs cm, const uint16_t *__restrict__ gate) {
   pdl_wait();  // the split partials come from the attention kernel
   pdl_trigger();
   const int row = blockIdx.x, g = blockIdx.y, t = threadIdx.x;
@@ -544,10 +544,22 @@ merge_kernel(int hq, int hkv, int n_split, const float *__restrict__ part_m,
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   const float inv = l > 0.f ? 1.f / l : 0.f;
+  float4 o = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+  const size_t off = (static_cast<size_t>(row) * hq + h) * kHeadDim + lane * 4;
+  if (gate) {
+    // sigmoid output gate, elementwise, before the bf16 rounding ("Flash-Next
+    // support: vLLM vs Atlas", (a) item 6, Dataflow bullet)
+    const uint2 g = *reinterpret_cast<const uint2 *>(gate + off);
+    auto sig = [](uint32_t bits) { return 1.f / (1.f + expf(-__uint_as_float(bits))); };
+    o.x *= sig(g.x << 16);
+    o.y *= sig(g.x & 0xFFFF0000u);
+    o.z *= sig(g.y << 16);
+    o.w *= sig(g.y & 0xFFFF0000u);
+  }
   uint2 packed;
-  packed.x = pack_bf16(a.x * inv, a.y * inv);
-  packed.y = pack_bf16(a.z * inv, a.w * inv);
-  *reinterpret_cast<uint2 *>(out + (static_cast<size_t>(row) * hq + h) * kHeadDim + lane * 4) = packed;
+  packed.x = pack_bf16(o.x, o.y);
+  packed.y = pack_bf16(o.z, o.w);
+  *reinterpret_cast<uint2 *>(out + off) = packed;
 }
 
 struct SplitPlan {
@@ -581,7 +593,7 @@ cudaError_t launch_attn_t(const Shape &sh, int n_seq, int R, const int32_t *seq_
                           const int32_t *pos0, const CacheView &cv, const uint16_t *q,
                           const int32_t *sel, const int32_t *n_sel, uint16_t *out, void *partials,
                           int32_t *status, bool pdl, const CommitArgs &commit, cudaStream_t st,
-                          const int32_t *sel_pos) {
+                          const int32_t *sel_pos, const uint16_t *gate) {
   const int rows = n_seq * R;
   const SplitPlan pl = plan_splits(sh, rows);
   const size_t n_part = static_cast<size_t>(rows) * pl.n_split * sh.hq;
@@ -609,7 +621,7 @@ cudaError_t launch_attn_t(const Shape &sh, int n_seq, int R, const int32_t *seq_
   if (e != cudaSuccess) return e;
   return launch_kernel(pdl, merge_kernel, dim3(rows, sh.hkv), dim3(kMergeThreads), 0, st, sh.hq, sh.hkv,
                        pl.n_split, static_cast<const float *>(pm), static_cast<const float *>(pl_),
-                       static_cast<const float *>(pa), out, commit);
+                       static_cast<const float *>(pa), out, commit, gate);
 }
 
 }  // namespace
@@ -631,12 +643,12 @@ cudaError_t launch_attn(const Shape &sh, int n_seq, int R, const int32_t *seq_id
                         const int32_t *pos0, const CacheView &cv, const uint16_t *q,
                         const int32_t *sel, const int32_t *n_sel, uint16_t *out, void *partials,
                         int32_t *status, bool pdl, const CommitArgs &commit, cudaStream_t st,
-                        const int32_t *sel_pos) {
+                        const int32_t *sel_pos, const uint16_t *gate) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
   switch (sh.hkv) {
-    case 1: return launch_attn_t<1>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st, sel_pos);
-    case 2: return launch_attn_t<2>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st, sel_pos);
-    case 4: return launch_attn_t<4>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st, sel_pos);
+    case 1: return launch_attn_t<1>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st, sel_pos, gate);
+    case 2: return launch_attn_t<2>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st, sel_pos, gate);
+    case 4: return launch_attn_t<4>(sh, n_seq, R, seq_ids, pos0, cv, q, sel, n_sel, out, partials, status, pdl, commit, st, sel_pos, gate);
     default: return cudaErrorInvalidValue;
   }
 }

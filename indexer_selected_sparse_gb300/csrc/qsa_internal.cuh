@@ -58,6 +58,22 @@ struct PreArgs {
   double half_turns[kMaxHalfRot] = {};
 };
 
+// --- main-attention options -------------------------------------------------
+// GemmaRMSNorm + NeoX RoPE of the attention's q heads (into q_out, read by the
+// attention kernel) and of the appended k heads (before they enter the K pool),
+// over D = 128 ("Agentic shootout", "Flash-Next support: vLLM vs Atlas", (a)
+// item 6, Dataflow bullet: GemmaRMSNorm q/k heads, fused QK-norm + RoPE + gate).
+// half_turns as in PreArgs (the main attention's own rotary dims).
+struct AttnPrep {
+  const float *gamma_q = nullptr;
+  const float *gamma_k = nullptr;
+  float eps = 0.f;
+  int rot = 0;
+  const uint16_t *q_in = nullptr;
+  uint16_t *q_out = nullptr;
+  double half_turns[kMaxHalfRot] = {};
+};
+
 // --- launch parameter blocks ---------------------------------------------
 
 struct CacheView {
@@ -243,7 +259,7 @@ cudaError_t launch_append(const Shape &sh, int n_seq, int R, const int32_t *seq_
                           uint16_t *idxraw_pool, void *idxblk_pool, const int32_t *ingested,
                           const uint16_t *k_new, const uint16_t *v_new,
                           const uint16_t *idx_k_new, int32_t *status, bool pdl, cudaStream_t st,
-                          const PreArgs *pre = nullptr);
+                          const PreArgs *pre = nullptr, const AttnPrep *att = nullptr);
 // query rows [rows, H_I, d_I] -> RoPE(GemmaRMSNorm) at each row's position
 cudaError_t launch_pre_index_q(const Shape &sh, int n_seq, int R, const int32_t *pos0, const PreArgs &pre,
                                const uint16_t *q_in, uint16_t *q_out, bool pdl, cudaStream_t st);
@@ -283,7 +299,7 @@ cudaError_t launch_attn(const Shape &sh, int n_seq, int R, const int32_t *seq_id
                         const int32_t *pos0, const CacheView &cv, const uint16_t *q,
                         const int32_t *sel, const int32_t *n_sel, uint16_t *out, void *partials,
                         int32_t *status, bool pdl, const CommitArgs &commit, cudaStream_t st,
-                        const int32_t *sel_pos = nullptr);
+                        const int32_t *sel_pos = nullptr, const uint16_t *gate = nullptr);
 // tokens a row's attention can take (splits x split length)
 int attn_max_tokens(const Shape &sh);
 

@@ -40,7 +40,8 @@ EXPORTED = ("qsa_strerror", "qsa_config_check", "qsa_workspace_bytes", "qsa_appe
             "qsa_rewind", "qsa_index_score", "qsa_topk_select", "qsa_gather_attn", "qsa_decode",
             "qsa_gather_attn_static", "qsa_max_attend_tokens", "qsa_gather_attn_reuse",
             "qsa_decode_reuse", "qsa_append_pre", "qsa_pre_index_q", "qsa_workspace_bytes_pre",
-            "qsa_decode_pre", "qsa_idxblk_page_bytes", "qsa_quantize_index_q")
+            "qsa_decode_pre", "qsa_idxblk_page_bytes", "qsa_quantize_index_q", "qsa_append_ex",
+            "qsa_workspace_bytes_ex", "qsa_decode_ex")
 QSA_STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -66,6 +67,11 @@ class qsa_config(ctypes.Structure):
 class qsa_pre_indexer(ctypes.Structure):
     _fields_ = [("gamma_q", ctypes.c_void_p), ("gamma_k", ctypes.c_void_p), ("eps", ctypes.c_float),
                 ("rope_theta", ctypes.c_float), ("rotary_dim", ctypes.c_int)]
+
+
+class qsa_attn_options(ctypes.Structure):
+    _fields_ = [("gamma_q", ctypes.c_void_p), ("gamma_k", ctypes.c_void_p), ("eps", ctypes.c_float),
+                ("rope_theta", ctypes.c_float), ("rotary_dim", ctypes.c_int), ("gate", ctypes.c_void_p)]
 
 
 class qsa_rows(ctypes.Structure):
@@ -124,6 +130,14 @@ LIB.qsa_idxblk_page_bytes.restype = ctypes.c_size_t
 LIB.qsa_idxblk_page_bytes.argtypes = [_CFG]
 LIB.qsa_quantize_index_q.restype = _I
 LIB.qsa_quantize_index_q.argtypes = [_CFG, _I, _P, _P, _P]
+_ATT = ctypes.POINTER(qsa_attn_options)
+LIB.qsa_append_ex.restype = _I
+LIB.qsa_append_ex.argtypes = [_CFG, _PRE, _ATT, _ROWS, _CACHE, _P, _P, _P, _P, _P]
+LIB.qsa_workspace_bytes_ex.restype = ctypes.c_size_t
+LIB.qsa_workspace_bytes_ex.argtypes = [_CFG, _I, _I]
+LIB.qsa_decode_ex.restype = _I
+LIB.qsa_decode_ex.argtypes = [_CFG, _PRE, _ATT, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                              ctypes.c_size_t, _P, _P]
 LIB.qsa_decode_pre.restype = _I
 LIB.qsa_decode_pre.argtypes = [_CFG, _PRE, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                ctypes.c_size_t, _P, _P]
@@ -391,6 +405,58 @@ def qsa_pre_index_q(cfg: Config, pre: PreIndexer, rows: Rows, q_idx, q_out, stre
     rc = LIB.qsa_pre_index_q(ctypes.byref(cfg.c()), ctypes.byref(pre.c()), ctypes.byref(rows.c()),
                              _ptr(q_idx, torch.bfloat16), _ptr(q_out, torch.bfloat16), _stream(stream))
     _check(rc, "qsa_pre_index_q")
+
+
+class AttnOptions:
+    """Main-attention options (qsa_attn_options): optional q / k norm gains
+    (device fp32 [D]; the norm multiplies by 1 + gain), eps, RoPE base, rotary
+    dims, and an optional sigmoid output gate (device bf16 [rows, Hq, D])."""
+
+    def __init__(self, gamma_q=None, gamma_k=None, eps: float = 1e-6, rope_theta: float = 1e4,
+                 rotary_dim: int = 64, gate=None):
+        self.gamma_q = None if gamma_q is None else gamma_q.to(torch.float32).contiguous()
+        self.gamma_k = None if gamma_k is None else gamma_k.to(torch.float32).contiguous()
+        self.eps, self.rope_theta, self.rotary_dim = float(eps), float(rope_theta), int(rotary_dim)
+        self.gate = gate
+
+    def c(self) -> qsa_attn_options:
+        return qsa_attn_options(_ptr(self.gamma_q), _ptr(self.gamma_k), self.eps, self.rope_theta,
+                                self.rotary_dim, _ptr(self.gate, torch.bfloat16))
+
+
+def _ref(x):
+    return None if x is None else ctypes.byref(x.c())
+
+
+def qsa_append_ex(cfg: Config, pre, attn, rows: Rows, cache: PagedCache, k_new, v_new, idx_k_new, status,
+                  stream=None) -> None:
+    rc = LIB.qsa_append_ex(ctypes.byref(cfg.c()), _ref(pre), _ref(attn), ctypes.byref(rows.c()),
+                           ctypes.byref(cache.c()), _ptr(k_new, torch.bfloat16), _ptr(v_new, torch.bfloat16),
+                           _ptr(idx_k_new, torch.bfloat16), _ptr(status, torch.int32), _stream(stream))
+    _check(rc, "qsa_append_ex", f"capacity {cache.capacity} tokens per sequence" if rc == QSA_ERR_CAPACITY else "")
+
+
+def qsa_workspace_bytes_ex(cfg: Config, max_rows: int, max_blocks_per_row: int) -> int:
+    return LIB.qsa_workspace_bytes_ex(ctypes.byref(cfg.c()), max_rows, max_blocks_per_row)
+
+
+def workspace_ex(cfg: Config, max_rows: int, max_blocks_per_row: int, device="cuda") -> torch.Tensor:
+    """A device workspace of qsa_workspace_bytes_ex() bytes (uint8)."""
+    n = qsa_workspace_bytes_ex(cfg, max_rows, max_blocks_per_row)
+    if n == 0:
+        raise QsaError(QSA_ERR_UNSUPPORTED, "qsa_workspace_bytes_ex")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def qsa_decode_ex(cfg: Config, pre, attn, rows: Rows, cache: PagedCache, k_new, v_new, idx_k_new, q_idx, w, q,
+                  out, ws, status, sel_out=None, n_sel_out=None, stream=None) -> None:
+    rc = LIB.qsa_decode_ex(ctypes.byref(cfg.c()), _ref(pre), _ref(attn), ctypes.byref(rows.c()),
+                           ctypes.byref(cache.c()), _ptr(k_new, torch.bfloat16), _ptr(v_new, torch.bfloat16),
+                           _ptr(idx_k_new, torch.bfloat16), _ptr(q_idx, torch.bfloat16), _ptr(w, torch.float32),
+                           _ptr(q, torch.bfloat16), _ptr(sel_out, torch.int32), _ptr(n_sel_out, torch.int32),
+                           _ptr(out, torch.bfloat16), _ptr(ws), ws.numel() * ws.element_size(),
+                           _ptr(status, torch.int32), _stream(stream))
+    _check(rc, "qsa_decode_ex", f"capacity {cache.capacity} tokens per sequence" if rc == QSA_ERR_CAPACITY else "")
 
 
 def qsa_idxblk_page_bytes(cfg: Config) -> int:
