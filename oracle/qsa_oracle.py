@@ -271,6 +271,60 @@ def mxfp8_dequantize(elems, exps) -> np.ndarray:
     return elems * scale
 
 
+# MXFP4 ("ATOM Model Support Guide", "Model architecture details",
+# DeepSeek-V4.1, Cache bullet: an fp4 index plane in "the official E2M1 + E8M0
+# arithmetic", values and scales in two planes). OCP MX v1.0 MXFP4: blocks of 32
+# values share an E8M0 scale 2^(floor(log2 amax) - 2) (2: the exponent of E2M1's
+# top binade), each value an E2M1 element (sign, 2 exponent bits with bias 1,
+# 1 mantissa bit: 0, 0.5, 1, 1.5, 2, 3, 4, 6), value / scale rounded
+# nearest-even on that grid and clamped to 6.
+
+E2M1_MAX = 6.0
+E2M1_EMAX = 2
+
+
+def e2m1_round(v) -> np.ndarray:
+    """Round fp64 values to the E2M1 grid, nearest-even, magnitudes clamped to 6.
+    Binades [2^E, 2^(E+1)) for E = 0 .. 2 hold 2 values each (quantum 2^(E-1));
+    below 1 the subnormal quantum is 0.5."""
+    v = np.asarray(v, np.float64)
+    a = np.minimum(np.abs(v), E2M1_MAX)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))
+    lead = np.maximum(e - 1, 0)
+    quantum = np.ldexp(1.0, lead - 1)
+    r = np.minimum(np.where(a > 0, np.rint(a / quantum) * quantum, 0.0), E2M1_MAX)
+    return np.copysign(r, v)
+
+
+def mxfp4_quantize(x) -> Tuple[np.ndarray, np.ndarray]:
+    """MXFP4 blocks of the last axis (a multiple of 32): E2M1 element values and
+    scale exponents, as mxfp8_quantize with E2M1's top binade 2."""
+    x = np.asarray(x, np.float64)
+    n = x.shape[-1]
+    assert n % MX_BLOCK == 0, "MXFP4 blocks need a multiple of 32 values"
+    blocks = x.reshape(x.shape[:-1] + (n // MX_BLOCK, MX_BLOCK))
+    amax = np.abs(blocks).max(axis=-1)
+    _, e = np.frexp(np.where(amax > 0, amax, 1.0))
+    exp = np.where(amax >= 2.0 ** -126, (e - 1) - E2M1_EMAX, E8M0_MIN_EXP)
+    exp = np.maximum(exp, E8M0_MIN_EXP).astype(np.int64)
+    elems = e2m1_round(blocks / np.ldexp(1.0, exp)[..., None])
+    return elems.reshape(x.shape), exp
+
+
+def mxfp4_round_bits(bits) -> np.ndarray:
+    """bf16 vectors (last axis) through MXFP4 and back (exact in bf16), fp64."""
+    return mxfp8_dequantize(*mxfp4_quantize(bf16_bits_to_f64(bits)))
+
+
+def block_scores_mxfp4(q_idx_bits, w, blk_bits) -> np.ndarray:
+    """block_scores with an MXFP4 index plane: query heads and compressed keys
+    MXFP4-quantised along d_I (the reading: both operands in the plane's
+    arithmetic), then the same fp64 sum."""
+    q = mxfp4_round_bits(q_idx_bits)
+    k = mxfp4_round_bits(blk_bits)
+    return np.asarray(w, np.float64) @ np.maximum(q @ k.T, 0.0)
+
+
 def mxfp8_round_bits(bits) -> np.ndarray:
     """bf16 vectors (last axis) through MXFP8 and back: the values the scores
     see, as fp64 (every such value is exact in bf16)."""
@@ -444,7 +498,7 @@ def attend_row(state: SeqState, pos: int, q_idx_bits, w, q_bits, topk: int,
         raise DesyncError(f"row at pos {pos} but only {state.ingested} ingested")
     n_blk = visible // r
     if n_blk > topk:
-        score_fn = {"bf16": block_scores, "mxfp8": block_scores_mxfp8}[index_format]
+        score_fn = {"bf16": block_scores, "mxfp8": block_scores_mxfp8, "mxfp4": block_scores_mxfp4}[index_format]
         scores = score_fn(q_idx_bits, w, state.idx_blk[:n_blk])
     else:
         scores = None                        # everything is selected; no scoring needed

@@ -204,6 +204,23 @@ def sigmoid_of_minus(x):
     return 1.0 / (1.0 + np.exp(x))
 
 
+def mxfp4_emax_3(x):
+    x = np.asarray(x, np.float64)
+    b = x.reshape(x.shape[:-1] + (-1, 32))
+    amax = np.abs(b).max(axis=-1)
+    _, e = np.frexp(np.where(amax > 0, amax, 1.0))
+    exp = np.where(amax > 0, e - 1 - 3, -127).astype(np.int64)
+    return O.e2m1_round(b / np.ldexp(1.0, exp)[..., None]).reshape(x.shape), exp
+
+
+def e2m1_ties_up(v):
+    v = np.asarray(v, np.float64)
+    a = np.minimum(np.abs(v), 6.0)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))
+    q = np.ldexp(1.0, np.maximum(e - 1, 0) - 1)
+    return np.copysign(np.minimum(np.floor(a / q + 0.5) * q, 6.0), v)
+
+
 MUTATIONS = [
     ("block_scores", no_relu, [P.test_score_closed_forms]),
     ("block_scores", relu_outside, [P.test_score_closed_forms]),
@@ -229,6 +246,8 @@ MUTATIONS = [
     ("token_set", window_off_by_one, [P.test_local_window_is_the_union_with_the_last_tokens]),
     ("token_set", window_drops_tail, [P.test_local_window_is_the_union_with_the_last_tokens]),
     ("SeqState", KeysRopedAtZero, [P.test_attention_qk_norm_rope_and_gate_hand_worked]),
+    ("mxfp4_quantize", mxfp4_emax_3, [P.test_mxfp4_scale_rule_on_a_hand_worked_block]),
+    ("e2m1_round", e2m1_ties_up, [P.test_e2m1_grid_and_nearest_even_rounding]),
     ("sigmoid", sigmoid_of_minus, [P.test_sigmoid_closed_forms, P.test_attention_qk_norm_rope_and_gate_hand_worked]),
 ]
 

@@ -746,3 +746,58 @@ def test_sigmoid_closed_forms():
     assert abs(O.sigmoid(math.log(3)) - 0.75) < 1e-15 and abs(O.sigmoid(-math.log(3)) - 0.25) < 1e-15
     x = np.linspace(-20, 20, 81)
     assert np.allclose(O.sigmoid(x) + O.sigmoid(-x), 1.0, atol=1e-15)
+
+
+# MXFP4 (OCP MX v1.0: E2M1 elements, one E8M0 scale per 32 values)
+
+
+def e2m1_table():
+    """The 8 non-negative E2M1 values in code order 0..7 from the bit fields:
+    2-bit exponent (bias 1) | 1-bit mantissa; exponent 0 is subnormal (m * 0.5)."""
+    return np.array([(m * 0.5) if e == 0 else (1 + m / 2) * 2.0 ** (e - 1) for e in range(4) for m in range(2)])
+
+
+def test_e2m1_grid_and_nearest_even_rounding():
+    t = e2m1_table()
+    assert t.tolist() == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert np.array_equal(O.e2m1_round(t), t) and np.array_equal(O.e2m1_round(-t), -t)
+    mids = (t[1:] + t[:-1]) / 2
+    assert not np.any(O.e2m1_round(mids) == mids)
+    rng = np.random.default_rng(83)
+    v = np.concatenate([rng.uniform(-8, 8, 5000), mids, -mids])
+    got = O.e2m1_round(v)
+    a = np.minimum(np.abs(v), 6.0)
+    d = np.abs(a[:, None] - t[None, :])
+    best = d.min(axis=1, keepdims=True)
+    cand = d == best
+    idx = np.where(cand.sum(axis=1) > 1, np.argmax(cand & (np.arange(8) % 2 == 0)[None, :], axis=1),
+                   np.argmax(cand, axis=1))
+    assert np.array_equal(np.abs(got), t[idx])
+
+
+def test_mxfp4_scale_rule_on_a_hand_worked_block():
+    # amax 3 -> floor(log2 3) - 2 = -1 -> scale 1/2: 3 -> 6, -1.5 -> -3, 0.1 -> 0.2
+    # (below the 0.25 midpoint: 0), 0.7 -> 1.4 (nearer 1.5 than 1)
+    x = np.zeros(32); x[:4] = [3.0, -1.5, 0.1, 0.7]
+    el, ex = O.mxfp4_quantize(x)
+    assert ex.tolist() == [-1] and el[:4].tolist() == [6.0, -3.0, 0.0, 1.5]
+    assert O.mxfp8_dequantize(el, ex)[:4].tolist() == [3.0, -1.5, 0.0, 0.75]
+    # amax / scale in [4, 8): values past 6 clamp (amax 7.9 at scale 1 -> 6)
+    y = np.zeros(32); y[0] = 7.9
+    el, ex = O.mxfp4_quantize(y)
+    assert ex.tolist() == [0] and el[0] == 6.0
+    rng = np.random.default_rng(89)
+    z = rng.standard_normal((4, 64)) * 10
+    el, ex = O.mxfp4_quantize(z)
+    amax = np.abs(z.reshape(4, 2, 32)).max(axis=-1)
+    assert np.all((amax / np.exp2(ex) >= 4) & (amax / np.exp2(ex) < 8))
+    # idempotent
+    back = O.mxfp8_dequantize(el, ex)
+    assert np.array_equal(O.mxfp8_dequantize(*O.mxfp4_quantize(back)), back)
+
+
+def test_mxfp4_scores_hand_worked():
+    # q = (3, 0.7, 0, ...) -> (3, 0.75); k = (1, 1, 0, ...) exact (scale 2^-2, 4 and 4)
+    q = np.zeros((1, 32)); q[0, :2] = [3.0, 0.7]
+    k = np.zeros((1, 32)); k[0, :2] = [1.0, 1.0]
+    assert O.block_scores_mxfp4(bf16(q), np.ones(1), bf16(k)).tolist() == [3.75]
