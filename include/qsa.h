@@ -87,8 +87,8 @@ typedef enum qsa_status {
  *              Hq / Hkv <= 8                    GQA
  *   head_dim   (D) 128
  *   page_size  (P) 64, multiple of ratio        tokens per cache page
- *   index_format QSA_INDEX_BF16 or QSA_INDEX_MXFP8 (the latter with
- *              P / ratio >= 8 blocks per page)  compressed-key plane
+ *   index_format QSA_INDEX_BF16, QSA_INDEX_MXFP8 or QSA_INDEX_MXFP4 (the
+ *              MX ones with P / ratio >= 8 blocks per page)  compressed-key plane
  *   local_window in [0, 16384]                  always-kept recent tokens
  * The indexer has one key head (MQA), as the pages require.
  *
@@ -115,6 +115,10 @@ typedef enum qsa_status {
  * ratio - 1 tokens (qsa_max_attend_tokens, qsa_workspace_bytes grow with W). */
 #define QSA_INDEX_BF16 0
 #define QSA_INDEX_MXFP8 1
+#define QSA_INDEX_MXFP4 2 /* as MXFP8 with E2M1 elements (0, 0.5, 1, 1.5, 2, 3, 4, 6)
+                             and scale 2^(floor(log2 amax) - 2) ("ATOM Model
+                             Support Guide", DeepSeek-V4.1, Cache bullet: an fp4
+                             index plane in E2M1 + E8M0 arithmetic); queries too */
 typedef struct qsa_config {
   int ratio;
   int budget;
@@ -176,7 +180,11 @@ typedef struct qsa_rows {
  * element (rr, d) at byte
  *     ((rr / 8) * (d_I / 16) + d / 16) * 128 + (rr % 8) * 16 + d % 16
  * (core matrices of 8 blocks x 16 bytes), then the E8M0 scale bytes, scale
- * (rr, c) of values 32c .. 32c+31 at byte bpp * d_I + rr * (d_I / 32) + c. */
+ * (rr, c) of values 32c .. 32c+31 at byte bpp * d_I + rr * (d_I / 32) + c.
+ * With QSA_INDEX_MXFP4 a page is bpp * (d_I/2 + d_I/32) bytes: E2M1 pairs,
+ * element (rr, d) in byte ((rr / 8) * (d_I / 32) + d / 32) * 128 + (rr % 8) * 16
+ * + (d % 32) / 2 (the low nibble for even d), then the scale bytes at
+ * bpp * d_I / 2 + rr * (d_I / 32) + c. */
 typedef struct qsa_cache {
   const int32_t *page_table; /* device [n_slots, max_pages] */
   int n_slots;
@@ -251,9 +259,10 @@ int qsa_index_score(const qsa_config *cfg, const qsa_rows *rows, const qsa_cache
                     const qsa_bf16 *q_idx, const float *w, float *scores, int ld_scores,
                     int32_t *status, cudaStream_t stream);
 
-/* MXFP8 round trip of index query heads (the query side of QSA_INDEX_MXFP8,
- * which the scorer applies itself): each d_I vector's blocks of 32 values are
- * quantised as the keys are and written back as bf16 (every MXFP8 value is
+/* MX round trip of index query heads (the query side of the MX planes, which
+ * the scorer applies itself): each d_I vector's blocks of 32 values are
+ * quantised as the keys are -- MXFP4 when cfg's index_format is
+ * QSA_INDEX_MXFP4, else MXFP8 -- and written back as bf16 (every MX value is
  * exact in bf16).
  *   q_idx, q_out  device [n_rows, H_I, d_I] bf16 (q_out == q_idx allowed) */
 int qsa_quantize_index_q(const qsa_config *cfg, int n_rows, const qsa_bf16 *q_idx, qsa_bf16 *q_out,

@@ -36,10 +36,11 @@ int check_cfg(const qsa_config *c) {
   if (c->n_q_heads < c->n_kv_heads || c->n_q_heads % c->n_kv_heads != 0) return QSA_ERR_UNSUPPORTED;
   if (c->n_q_heads / c->n_kv_heads > 8) return QSA_ERR_UNSUPPORTED;
   if (c->page_size != 64 || c->page_size % c->ratio != 0) return QSA_ERR_UNSUPPORTED;
-  if (c->index_format != QSA_INDEX_BF16 && c->index_format != QSA_INDEX_MXFP8) return QSA_ERR_UNSUPPORTED;
+  if (c->index_format != QSA_INDEX_BF16 && c->index_format != QSA_INDEX_MXFP8 && c->index_format != QSA_INDEX_MXFP4)
+    return QSA_ERR_UNSUPPORTED;
   if (c->local_window < 0 || c->local_window > kMaxLocalWindow) return QSA_ERR_UNSUPPORTED;
   // the MXFP8 plane is scored on the tensor-core path: 8 or more blocks per page
-  if (c->index_format == QSA_INDEX_MXFP8 && c->page_size / c->ratio < 8) return QSA_ERR_UNSUPPORTED;
+  if (c->index_format != QSA_INDEX_BF16 && c->page_size / c->ratio < 8) return QSA_ERR_UNSUPPORTED;
   return QSA_OK;
 }
 
@@ -56,7 +57,8 @@ Shape make_shape(const qsa_config *c) {
   s.page = c->page_size;
   s.log2_ratio = ilog2(c->ratio);
   s.log2_page = ilog2(c->page_size);
-  s.idx_fp8 = c->index_format == QSA_INDEX_MXFP8 ? 1 : 0;
+  s.idx_fp8 = c->index_format == QSA_INDEX_MXFP8 || c->index_format == QSA_INDEX_MXFP4 ? 1 : 0;
+  s.idx_fp4 = c->index_format == QSA_INDEX_MXFP4 ? 1 : 0;
   s.window = c->local_window;
   return s;
 }
@@ -310,6 +312,7 @@ int qsa_config_check(const qsa_config *cfg) { return check_cfg(cfg); }
 size_t qsa_idxblk_page_bytes(const qsa_config *cfg) {
   if (check_cfg(cfg) != QSA_OK) return 0;
   const int bpp = cfg->page_size / cfg->ratio;
+  if (cfg->index_format == QSA_INDEX_MXFP4) return static_cast<size_t>(fp4_page_bytes(bpp, cfg->idx_dim));
   return cfg->index_format == QSA_INDEX_MXFP8 ? static_cast<size_t>(fp8_page_bytes(bpp, cfg->idx_dim))
                                               : static_cast<size_t>(bpp) * cfg->idx_dim * sizeof(uint16_t);
 }
@@ -322,7 +325,7 @@ int qsa_quantize_index_q(const qsa_config *cfg, int n_rows, const qsa_bf16 *q_id
   if (n_rows == 0) return QSA_OK;
   if (!q_idx || !q_out) return QSA_ERR_INVALID_ARG;
   Shape sh = make_shape(cfg);
-  sh.idx_fp8 = 1;  // the MXFP8 round trip whatever the cache's format
+  sh.idx_fp8 = 1;  // an MX round trip whatever the cache's format: MXFP4 for an MXFP4 plane, else MXFP8
   PreArgs pa;      // no pre-indexer: no gains, no positions
   return cuda_status(launch_pre_index_q(sh, n_rows, 1, nullptr, pa, q_idx, q_out, false, stream));
 }

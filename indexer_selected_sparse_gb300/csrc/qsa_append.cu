@@ -65,14 +65,15 @@ __device__ __forceinline__ void pre_index_lanes(float (&x)[D32], const float *__
 
 // One warp holding a d_I vector as lane L: dims L + 32m, so register m across
 // the warp is exactly MX block m. x must already be bf16 values. Returns each
-// lane's codes and every block's scale exponent.
-template <int D32>
+// lane's codes (E4M3, or E2M1 with FP4) and every block's scale exponent.
+template <int D32, bool FP4 = false>
 __device__ __forceinline__ void mx_quantize_lanes(const float (&x)[D32], uint32_t (&code)[D32], int (&ex)[D32]) {
 #pragma unroll
   for (int m = 0; m < D32; ++m) {
     const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(x[m]))));
-    ex[m] = mx_scale_exp(amax);
-    code[m] = e4m3_code(x[m] * exp2_int(-ex[m]));  // exact power-of-two scaling
+    ex[m] = FP4 ? mx4_scale_exp(amax) : mx_scale_exp(amax);
+    const float sc = x[m] * exp2_int(-ex[m]);  // exact power-of-two scaling
+    code[m] = FP4 ? e2m1_code(sc) : e4m3_code(sc);
   }
 }
 
@@ -80,12 +81,12 @@ __device__ __forceinline__ void mx_quantize_lanes(const float (&x)[D32], uint32_
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
 // One warp, one vector of 32 * D32 values at in[base] -> out[base]: RoPE(Gemma
-// RMSNorm) at pos when gamma is set, rounded to bf16, then the MXFP8 round trip
-// when fp8 is set.
+// RMSNorm) at pos when gamma is set, rounded to bf16, then the MX round trip
+// (mx: 1 MXFP8, 2 MXFP4, 0 none).
 template <int D32>
 __device__ __forceinline__ void prep_vector(const uint16_t *__restrict__ in, uint16_t *__restrict__ out,
                                             size_t base, int pos, const float *gamma, float eps, int rot,
-                                            const double *half_turns, bool fp8, int lane) {
+                                            const double *half_turns, int mx, int lane) {
   float x[D32];
 #pragma unroll
   for (int m = 0; m < D32; ++m) x[m] = bf16_bits_to_float(in[base + lane + 32 * m]);
@@ -94,12 +95,18 @@ __device__ __forceinline__ void prep_vector(const uint16_t *__restrict__ in, uin
 #pragma unroll
     for (int m = 0; m < D32; ++m) x[m] = round_bf16(x[m]);
   }
-  if (fp8) {
+  if (mx == 1) {
     uint32_t code[D32];
     int ex[D32];
     mx_quantize_lanes<D32>(x, code, ex);
 #pragma unroll
     for (int m = 0; m < D32; ++m) x[m] = e4m3_value(code[m]) * exp2_int(ex[m]);  // exact in bf16
+  } else if (mx == 2) {
+    uint32_t code[D32];
+    int ex[D32];
+    mx_quantize_lanes<D32, true>(x, code, ex);
+#pragma unroll
+    for (int m = 0; m < D32; ++m) x[m] = e2m1_value(code[m]) * exp2_int(ex[m]);  // exact in bf16
   }
 #pragma unroll
   for (int m = 0; m < D32; ++m) {
@@ -123,18 +130,17 @@ __device__ void prep_queries(const Shape &sh, const PreArgs &pre, const AttnPrep
     if (v < n_idx) {
       const int t = v / sh.h_idx;
       const size_t base = (static_cast<size_t>(i) * R * sh.h_idx + v) * sh.d_idx;
+      const int mx = sh.idx_fp8 ? (sh.idx_fp4 ? 2 : 1) : 0;
       if (sh.d_idx == 128)
-        prep_vector<4>(pre.q_in, pre.q_out, base, p0 + t, pre.gamma_q, pre.eps, pre.rot, pre.half_turns,
-                       sh.idx_fp8 != 0, lane);
+        prep_vector<4>(pre.q_in, pre.q_out, base, p0 + t, pre.gamma_q, pre.eps, pre.rot, pre.half_turns, mx, lane);
       else
-        prep_vector<2>(pre.q_in, pre.q_out, base, p0 + t, pre.gamma_q, pre.eps, pre.rot, pre.half_turns,
-                       sh.idx_fp8 != 0, lane);
+        prep_vector<2>(pre.q_in, pre.q_out, base, p0 + t, pre.gamma_q, pre.eps, pre.rot, pre.half_turns, mx, lane);
     } else {
       const int vm = v - n_idx;
       const int t = vm / sh.hq;
       const size_t base = (static_cast<size_t>(i) * R * sh.hq + vm) * kHeadDim;
       prep_vector<kHeadDim / 32>(att.q_in, att.q_out, base, p0 + t, att.gamma_q, att.eps, att.rot, att.half_turns,
-                                 false, lane);
+                                 0, lane);
     }
   }
 }
@@ -190,6 +196,27 @@ __device__ void pool_block_warp(const Shape &sh, const PreArgs &pre, int b, int 
     pre_index_lanes<D32>(x, pre.gamma_k, pre.eps, pre.rot, sh.d_idx, lane,
                          [&](int ip) { return rope_cs(first, ip, pre.half_turns); });
   const int rr = b & (bpp - 1);
+  if (sh.idx_fp4) {
+#pragma unroll
+    for (int m = 0; m < D32; ++m) x[m] = round_bf16(x[m]);
+    uint32_t code[D32];
+    int ex[D32];
+    mx_quantize_lanes<D32, true>(x, code, ex);
+    uint8_t *pg = static_cast<uint8_t *>(blk_pool) + static_cast<size_t>(page_b) * fp4_page_bytes(bpp, sh.d_idx);
+#pragma unroll
+    for (int m = 0; m < D32; ++m) {
+      // dims lane and lane + 1 share a byte: the even lane stores both nibbles
+      const uint32_t hi = __shfl_down_sync(0xffffffffu, code[m], 1);
+      if ((lane & 1) == 0)
+        pg[fp4_byte_offset(rr, lane + 32 * m, sh.d_idx)] = static_cast<uint8_t>(code[m] | (hi << 4));
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int m = 0; m < D32; ++m)
+        pg[bpp * sh.d_idx / 2 + rr * (sh.d_idx / 32) + m] = static_cast<uint8_t>(ex[m] + 127);
+    }
+    return;
+  }
   if (sh.idx_fp8) {
 #pragma unroll
     for (int m = 0; m < D32; ++m) x[m] = round_bf16(x[m]);

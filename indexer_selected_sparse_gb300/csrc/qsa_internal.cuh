@@ -89,7 +89,8 @@ struct CacheView {
 struct Shape {
   int ratio, budget, topk, h_idx, d_idx, hq, hkv, d, page;
   int log2_ratio, log2_page;
-  int idx_fp8;  // compressed keys in the MXFP8 plane (index queries MXFP8-rounded)
+  int idx_fp8;  // compressed keys in an MX plane (index queries rounded through it)
+  int idx_fp4;  // ... and that plane is MXFP4 (E2M1 elements) rather than MXFP8
   int window;   // always-kept local window: the last `window` tokens of every row (0: none)
 };
 
@@ -102,6 +103,15 @@ __host__ __device__ __forceinline__ int fp8_elem_offset(int rr, int d, int d_idx
   return ((rr >> 3) * (d_idx >> 4) + (d >> 4)) * 128 + (rr & 7) * 16 + (d & 15);
 }
 __host__ __device__ __forceinline__ int fp8_page_bytes(int bpp, int d_idx) { return bpp * (d_idx + d_idx / 32); }
+
+// MXFP4 pages: bpp * d_I / 2 bytes of E2M1 pairs (element d in the low nibble
+// when d is even), 32 elements (one MX block) per 16-byte run, runs in 8-block
+// groups: element (rr, d) in byte fp4_byte_offset, then the E8M0 scales, scale
+// (rr, c) at bpp * d_I / 2 + rr * d_I/32 + c.
+__host__ __device__ __forceinline__ int fp4_byte_offset(int rr, int d, int d_idx) {
+  return ((rr >> 3) * (d_idx >> 5) + (d >> 5)) * 128 + (rr & 7) * 16 + ((d & 31) >> 1);
+}
+__host__ __device__ __forceinline__ int fp4_page_bytes(int bpp, int d_idx) { return bpp * (d_idx / 2 + d_idx / 32); }
 
 // 2^e as fp32 for e in [-149, 127] (subnormal below -126): an E8M0 scale byte u
 // is 2^(u - 127).
@@ -134,6 +144,34 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
 // x through MXFP8 and back, given its block's scale exponent e (exact in bf16).
 __device__ __forceinline__ float mx_round(float x, int e) {
   return e4m3_value(e4m3_code(x * exp2_int(-e))) * exp2_int(e);
+}
+
+// MXFP4: scale exponent floor(log2 amax) - 2 (2: E2M1's top binade).
+__device__ __forceinline__ int mx4_scale_exp(float amax) {
+  const int biased = static_cast<int>(__float_as_uint(amax) >> 23);
+  return biased == 0 ? -127 : max(biased - 127 - 2, -127);
+}
+
+// E2M1 code (sign << 3 | magnitude code 0..7) of v: nearest-even on
+// {0, 0.5, 1, 1.5, 2, 3, 4, 6}, magnitudes past 6 clamped. Each midpoint goes to
+// the even code: <= 0.25 -> 0, < 0.75 -> 1, <= 1.25 -> 2, < 1.75 -> 3,
+// <= 2.5 -> 4, < 3.5 -> 5, <= 5 -> 6, else 7.
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+  const float a = fabsf(v);
+  const uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.f);
+  return ((__float_as_uint(v) >> 31) << 3) | m;  // the sign kept, a zero's too
+}
+
+// Value of an E2M1 magnitude code 0..7 (with the sign bit 8).
+__device__ __forceinline__ float e2m1_value(uint32_t code) {
+  const uint32_t m = code & 7u;
+  const float mag = m < 2 ? 0.5f * m : __uint_as_float(static_cast<uint32_t>(126 + (m >> 1)) << 23) * (1.f + 0.5f * (m & 1));
+  return code & 8u ? -mag : mag;
+}
+
+// x through MXFP4 and back, given its block's scale exponent e (exact in bf16).
+__device__ __forceinline__ float mx4_round(float x, int e) {
+  return e2m1_value(e2m1_code(x * exp2_int(-e))) * exp2_int(e);
 }
 
 // --- PTX wrappers ---------------------------------------------------------

@@ -409,6 +409,22 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w, uint32_t sc2, u
   return r;
 }
 
+// Byte K of w (two E2M1 codes: the low nibble the even element) -> a bf16 pair,
+// times the block scale 2^e. An E2M1 code's magnitude bits placed as a bf16's
+// low exponent bits and top mantissa bit, its sign as the bf16 sign, read as
+// x * 2^-126 (the subnormal code 0.5 too), so one exact bf16 multiply by
+// 2^(126 + e) finishes it (sc2; e <= 1, else 2^126 and then 2^e in sc2b).
+template <int K>
+__device__ __forceinline__ uint32_t e2m1x2_to_bf16x2(uint32_t w, uint32_t sc2, uint32_t sc2b, bool two_step) {
+  const uint32_t b = (w >> (8 * K)) & 0xFFu;
+  const uint32_t y = b | (b << 12);  // low nibble at bits 0-3, high nibble at 16-19
+  const uint32_t t = ((y & 0x00070007u) << 6) | ((y & 0x00080008u) << 12);
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(sc2));
+  if (two_step) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(r), "r"(sc2b));
+  return r;
+}
+
 // bf16 bits of 2^e (e in [-126, 127]), in both halves of a word.
 __device__ __forceinline__ uint32_t bf16x2_pow2(int e) {
   const uint32_t h = static_cast<uint32_t>(e + 127) << 7;
@@ -422,12 +438,15 @@ __device__ __forceinline__ uint32_t bf16x2_pow2(int e) {
 // A tile is 128 rows x d_I bf16 in the K-major core-matrix layout; a B slot is
 // DI/64 halves x npad rows x 128 B (128B swizzle). TMEM: two accumulators of
 // ncols columns, then (MXFP8) kMaxCStages A tiles of d_I / 2 columns.
-template <int DI, bool FP8>
+template <int DI, bool FP8, bool FP4 = false>
 __global__ void __launch_bounds__(FP8 ? kMaxThreadsFp8 : kMaxThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages) {
+  // FP8: an MX plane (the converter path); FP4: that plane is MXFP4, else MXFP8
+  static_assert(!FP4 || FP8, "MXFP4 runs on the MX path");
   constexpr int HALVES = DI / 64;
   constexpr int A_STAGE = kTcTileBlocks * DI * 2;  // one tile of keys, tiled pages back to back
-  constexpr int R_STAGE = FP8 ? kTcTileBlocks * (DI + DI / 32) : A_STAGE;  // one tile as copied
+  constexpr int R_STAGE = FP4 ? kTcTileBlocks * (DI / 2 + DI / 32)
+                              : (FP8 ? kTcTileBlocks * (DI + DI / 32) : A_STAGE);  // one tile as copied
   constexpr int N_OP = FP8 ? kMaxCStages : 0;      // operand stages besides the copy ring
   constexpr int N_OPD = FP8 ? kMaxCStages : 1;     // the same as a divisor (bf16: unused)
   extern __shared__ uint8_t smem_raw[];
@@ -495,7 +514,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
   const uint32_t tmem = *tmem_slot;
   const int bpp = 1 << a.bpp_log2;
   const int pages_in_tile = kTcTileBlocks >> a.bpp_log2;
-  const uint32_t page_bytes = FP8 ? static_cast<uint32_t>(fp8_page_bytes(bpp, DI)) : static_cast<uint32_t>(bpp) * DI * 2;
+  const uint32_t page_bytes = FP4 ? static_cast<uint32_t>(fp4_page_bytes(bpp, DI))
+                              : (FP8 ? static_cast<uint32_t>(fp8_page_bytes(bpp, DI)) : static_cast<uint32_t>(bpp) * DI * 2);
 
   // MXFP8: a second producer warp (the last one) for the second copy ring
   const int prod2 = FP8 ? static_cast<int>(blockDim.x >> 5) - 1 : -1;
@@ -646,8 +666,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     const int q = warp & 3, rc = cw >> 2;
     const int b = q * 32 + lane;
     const int slot = b >> a.bpp_log2, rr = b & (bpp - 1);
-    const uint32_t src_row = slot * page_bytes + ((rr >> 3) * (DI / 16)) * 128 + (rr & 7) * 16;
-    const uint32_t scl_off = slot * page_bytes + bpp * DI + rr * (DI / 32);
+    // a 16-byte run of the row: 16 E4M3 elements, or 32 E2M1 (one MX block)
+    const uint32_t src_row = slot * page_bytes + ((rr >> 3) * (FP4 ? DI / 32 : DI / 16)) * 128 + (rr & 7) * 16;
+    const uint32_t scl_off = slot * page_bytes + bpp * (FP4 ? DI / 2 : DI) + rr * (DI / 32);
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + 2 * a.ncols;
     Walker w = walker_start(a, n_groups, lane);
     int cur_gq = -1, gq = -1;
@@ -674,11 +695,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(v[i] << 16)), fabsf(__uint_as_float(v[i] & 0xFFFF0000u))));
-          const int e = mx_scale_exp(amax);
+          const int e = FP4 ? mx4_scale_exp(amax) : mx_scale_exp(amax);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float lo = mx_round(__uint_as_float(v[i] << 16), e);
-            const float hi = mx_round(__uint_as_float(v[i] & 0xFFFF0000u), e);
+            const float xl = __uint_as_float(v[i] << 16), xh = __uint_as_float(v[i] & 0xFFFF0000u);
+            const float lo = FP4 ? mx4_round(xl, e) : mx_round(xl, e);
+            const float hi = FP4 ? mx4_round(xh, e) : mx_round(xh, e);
             v[i] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);  // exact in bf16
           }
 #pragma unroll
@@ -709,6 +731,44 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         asm volatile("ld.shared.u16 %0, [%1];" : "=h"(s16) : "r"(src + scl_off));
         scl = s16;
       }
+      if constexpr (FP4) {
+#pragma unroll
+        for (int hf = 0; hf < DI / 64; ++hf) {
+          uint32_t o[32];  // 64 dims (two MX blocks) as bf16 pairs: 32 TMEM columns
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const int j = hf * 2 + jj;  // MX block j: dims 32j .. 32j+31, one 16-byte run
+            uint32_t v0, v1, v2, v3;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                         : "r"(src + src_row + j * 128));
+            // scale 2^e: one multiply by 2^(126 + e) when that is a normal bf16
+            // (e <= 1), else 2^126 then 2^e
+            const int e = static_cast<int>((scl >> (8 * j)) & 0xFFu) - 127;
+            const bool two = e > 1;
+            const uint32_t sc2 = bf16x2_pow2(two ? 126 : 126 + e);
+            const uint32_t sc2b = bf16x2_pow2(two ? e : 0);
+            uint32_t *oj = o + jj * 16;  // byte k of the run: dims 32j + 2k, 32j + 2k + 1
+            oj[0] = e2m1x2_to_bf16x2<0>(v0, sc2, sc2b, two);
+            oj[1] = e2m1x2_to_bf16x2<1>(v0, sc2, sc2b, two);
+            oj[2] = e2m1x2_to_bf16x2<2>(v0, sc2, sc2b, two);
+            oj[3] = e2m1x2_to_bf16x2<3>(v0, sc2, sc2b, two);
+            oj[4] = e2m1x2_to_bf16x2<0>(v1, sc2, sc2b, two);
+            oj[5] = e2m1x2_to_bf16x2<1>(v1, sc2, sc2b, two);
+            oj[6] = e2m1x2_to_bf16x2<2>(v1, sc2, sc2b, two);
+            oj[7] = e2m1x2_to_bf16x2<3>(v1, sc2, sc2b, two);
+            oj[8] = e2m1x2_to_bf16x2<0>(v2, sc2, sc2b, two);
+            oj[9] = e2m1x2_to_bf16x2<1>(v2, sc2, sc2b, two);
+            oj[10] = e2m1x2_to_bf16x2<2>(v2, sc2, sc2b, two);
+            oj[11] = e2m1x2_to_bf16x2<3>(v2, sc2, sc2b, two);
+            oj[12] = e2m1x2_to_bf16x2<0>(v3, sc2, sc2b, two);
+            oj[13] = e2m1x2_to_bf16x2<1>(v3, sc2, sc2b, two);
+            oj[14] = e2m1x2_to_bf16x2<2>(v3, sc2, sc2b, two);
+            oj[15] = e2m1x2_to_bf16x2<3>(v3, sc2, sc2b, two);
+          }
+          tmem_st<32>(a_lane + c * (DI / 2) + hf * 32, o);
+        }
+      } else {
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
       uint32_t o[DI / 4];  // half a row as bf16 pairs: d_I / 4 TMEM columns
@@ -738,6 +798,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         oj[7] = e4m3x2_to_bf16x2<0x3424>(v3, sc2, sc2b, two);
       }
       tmem_st<DI / 4>(a_lane + c * (DI / 2) + hf * (DI / 4), o);
+      }
       }
       // the MMA may read the stage once every store has landed
       tmem_st_wait();
@@ -902,7 +963,9 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   const int halves = sh.d_idx / 64;
   const bool fp8 = sh.idx_fp8 != 0;
   const size_t a_stage = static_cast<size_t>(kTcTileBlocks) * sh.d_idx * 2;
-  const size_t r_stage = fp8 ? static_cast<size_t>(kTcTileBlocks) * (sh.d_idx + sh.d_idx / 32) : a_stage;
+  const bool fp4 = sh.idx_fp4 != 0;
+  const size_t r_stage = fp4 ? static_cast<size_t>(kTcTileBlocks) * (sh.d_idx / 2 + sh.d_idx / 32)
+                             : (fp8 ? static_cast<size_t>(kTcTileBlocks) * (sh.d_idx + sh.d_idx / 32) : a_stage);
   const size_t b_slots = 2ull * halves * a.npad * 128;
   const size_t fixed = 1024 + b_slots + kEpiFloats * 4 + 8 * (fp8 ? kNumBars : kNumBarsBf16) + 16;
   const size_t smem_cap = 227 * 1024;
@@ -919,8 +982,9 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   const int max_ctas = 512 / a.tmem_cols;
   const size_t min_smem = sm_smem / (max_ctas + 1) - 1024 + 1;
   if (smem < min_smem) smem = min_smem;
-  auto kern = fp8 ? (sh.d_idx == 128 ? score_tc_kernel<128, true> : score_tc_kernel<64, true>)
-                  : (sh.d_idx == 128 ? score_tc_kernel<128, false> : score_tc_kernel<64, false>);
+  auto kern = fp4 ? (sh.d_idx == 128 ? score_tc_kernel<128, true, true> : score_tc_kernel<64, true, true>)
+                  : fp8 ? (sh.d_idx == 128 ? score_tc_kernel<128, true> : score_tc_kernel<64, true>)
+                        : (sh.d_idx == 128 ? score_tc_kernel<128, false> : score_tc_kernel<64, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;

@@ -91,7 +91,8 @@ extern "C" int qsa_gather_attn_static(const qsa_config *cfg, const qsa_rows *row
   sh.page = cfg->page_size;
   sh.log2_ratio = ilog2(cfg->ratio);
   sh.log2_page = ilog2(cfg->page_size);
-  sh.idx_fp8 = cfg->index_format == QSA_INDEX_MXFP8 ? 1 : 0;
+  sh.idx_fp8 = cfg->index_format != QSA_INDEX_BF16 ? 1 : 0;
+  sh.idx_fp4 = cfg->index_format == QSA_INDEX_MXFP4 ? 1 : 0;
   sh.window = cfg->local_window;
   // the partials of this many rows must fit the fixed array
   if (attn_partial_bytes(sh, static_cast<int>(n_rows)) > kStaticScratchBytes) return QSA_ERR_WORKSPACE;

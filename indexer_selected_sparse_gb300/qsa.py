@@ -35,6 +35,7 @@ QSA_ERR_REUSE = 11
 
 QSA_INDEX_BF16 = 0
 QSA_INDEX_MXFP8 = 1
+QSA_INDEX_MXFP4 = 2
 
 EXPORTED = ("qsa_strerror", "qsa_config_check", "qsa_workspace_bytes", "qsa_append",
             "qsa_rewind", "qsa_index_score", "qsa_topk_select", "qsa_gather_attn", "qsa_decode",
@@ -227,7 +228,7 @@ class PagedCache:
         self.idxraw_pool = torch.zeros(num_pages, P, cfg.idx_dim, dtype=torch.bfloat16, device=device)
         # block keys: P/ratio rows of idx_dim per page, stored tiled (see qsa.h); with the
         # MXFP8 index format a byte plane of qsa_idxblk_page_bytes() per page
-        if cfg.index_format == QSA_INDEX_MXFP8:
+        if cfg.index_format in (QSA_INDEX_MXFP8, QSA_INDEX_MXFP4):
             self.idxblk_pool = torch.zeros(num_pages, qsa_idxblk_page_bytes(cfg), dtype=torch.uint8, device=device)
         else:
             self.idxblk_pool = torch.zeros(num_pages, (P // cfg.ratio) * cfg.idx_dim, dtype=torch.bfloat16,

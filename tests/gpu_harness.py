@@ -216,6 +216,29 @@ class GpuState:
         exps = plane[pages[:, None], sc[b % bpp]].astype(np.int64) - 127
         return elems, exps
 
+    def logical_blocks_mxfp4(self, s: int, n_blk: int):
+        """The MXFP4 plane's blocks 0..n_blk-1 of sequence s: E2M1 element values
+        [n_blk, d_I] (decoded from the nibbles: sign | 2-bit exponent, bias 1 |
+        1-bit mantissa) and scale exponents [n_blk, d_I / 32]."""
+        sh = self.sh
+        bpp = sh.page_size // sh.ratio
+        d = sh.idx_dim
+        pt = self.cache.page_table[s].cpu().numpy()
+        b = np.arange(n_blk)
+        pages = pt[b // bpp]
+        plane = self.cache.idxblk_pool.cpu().numpy()
+        rr = (b % bpp)[:, None]
+        dd = np.arange(d)[None, :]
+        byte = ((rr // 8) * (d // 32) + dd // 32) * 128 + (rr % 8) * 16 + (dd % 32) // 2
+        raw = plane[pages[:, None], byte]
+        nib = np.where(dd % 2 == 0, raw & 15, raw >> 4).astype(np.int64)
+        e, m = (nib >> 1) & 3, nib & 1
+        mag = np.where(e == 0, 0.5 * m, (1 + m / 2) * np.exp2(e - 1))
+        elems = np.where(nib & 8, -mag, mag)
+        sc = bpp * d // 2 + rr * (d // 32) + np.arange(d // 32)[None, :]
+        exps = plane[pages[:, None], sc].astype(np.int64) - 127
+        return elems, exps
+
     def logical_rows(self, pool: torch.Tensor, s: int, positions: np.ndarray) -> np.ndarray:
         P = self.sh.page_size
         pt = self.cache.page_table[s].cpu().numpy()
@@ -271,7 +294,8 @@ class OracleSeq:
         visible = pos + 1
         n_blk = visible // sh.ratio
         if n_blk > sh.topk:
-            score_fn = O.block_scores_mxfp8 if index_format == "mxfp8" else O.block_scores
+            score_fn = {"bf16": O.block_scores, "mxfp8": O.block_scores_mxfp8,
+                        "mxfp4": O.block_scores_mxfp4}[index_format]
             sc = score_fn(bits(qi[0]), w[0].numpy(), self.st.idx_blk[:n_blk])
             sel = O.select_blocks(sc, sh.topk)
         else:

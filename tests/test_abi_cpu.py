@@ -149,7 +149,12 @@ def test_index_format_checked_and_page_bytes(Q):
     assert Q.qsa_config_check(Q.Config(8, 1024, 16, 64, 8, 1, index_format=mx)) == Q.QSA_OK
     # 4 blocks per page (ratio 16): the MXFP8 plane is not supported there
     assert Q.qsa_config_check(Q.Config(16, 2048, 64, 128, 32, 4, index_format=mx)) == Q.QSA_ERR_UNSUPPORTED
-    assert Q.qsa_config_check(Q.Config(4, 2048, 64, 128, 32, 4, index_format=2)) == Q.QSA_ERR_UNSUPPORTED
+    assert Q.qsa_config_check(Q.Config(4, 2048, 64, 128, 32, 4, index_format=3)) == Q.QSA_ERR_UNSUPPORTED
+    m4 = Q.QSA_INDEX_MXFP4
+    assert Q.qsa_config_check(Q.Config(4, 2048, 64, 128, 32, 4, index_format=m4)) == Q.QSA_OK
+    assert Q.qsa_config_check(Q.Config(16, 2048, 64, 128, 32, 4, index_format=m4)) == Q.QSA_ERR_UNSUPPORTED
+    assert Q.qsa_idxblk_page_bytes(Q.Config(4, 2048, 64, 128, 32, 4, index_format=m4)) == 16 * (64 + 4)
+    assert Q.qsa_idxblk_page_bytes(Q.Config(8, 1024, 16, 64, 8, 1, index_format=m4)) == 8 * (32 + 2)
     # page bytes: bf16 bpp * d_I * 2; MXFP8 bpp * (d_I + d_I / 32)
     assert Q.qsa_idxblk_page_bytes(Q.Config(4, 2048, 64, 128, 32, 4)) == 16 * 128 * 2
     assert Q.qsa_idxblk_page_bytes(Q.Config(4, 2048, 64, 128, 32, 4, index_format=mx)) == 16 * 132
