@@ -63,6 +63,8 @@ def parse():
                     help="decode steps through the pre-indexer (norm + RoPE of queries and keys); 0 skips")
     ap.add_argument("--mxfp8-steps", type=int, default=600,
                     help="decode steps with the MXFP8 index plane (own cache); 0 skips")
+    ap.add_argument("--mxfp4-steps", type=int, default=600,
+                    help="decode steps with the MXFP4 index plane (own cache); 0 skips")
     ap.add_argument("--window-steps", type=int, default=300,
                     help="decode steps with a 128-token always-kept local window; 0 skips")
     ap.add_argument("--prefill-warmup", type=int, default=3)
@@ -82,12 +84,18 @@ def measured_peaks():
 # algorithmic bytes / flops (per row), from the method's definition
 # ---------------------------------------------------------------------------
 
-def row_work(sh, visible, mxfp8=False):
+def key_bytes(sh, fmt):
+    """Bytes of one stored compressed key: bf16, or MX elements + one scale byte per 32."""
+    return {"bf16": 2 * sh.idx_dim, "mxfp8": sh.idx_dim + sh.idx_dim // 32,
+            "mxfp4": sh.idx_dim // 2 + sh.idx_dim // 32}[fmt]
+
+
+def row_work(sh, visible, fmt="bf16"):
     n_blk = visible // sh.ratio
     tail = visible - n_blk * sh.ratio
     active = n_blk > sh.topk
     n_tok = min(n_blk, sh.topk) * sh.ratio + tail
-    key_b = sh.idx_dim + sh.idx_dim // 32 if mxfp8 else sh.idx_dim * 2  # per compressed key
+    key_b = key_bytes(sh, fmt)
     score_b = (n_blk * key_b + sh.n_idx_heads * sh.idx_dim * 2 + 4 * sh.n_idx_heads) if active else 0
     attn_b = n_tok * sh.n_kv_heads * sh.head_dim * 2 * 2 + 2 * sh.n_q_heads * sh.head_dim * 2
     append_b = (2 * sh.n_kv_heads * sh.head_dim + sh.idx_dim) * 2
@@ -97,10 +105,10 @@ def row_work(sh, visible, mxfp8=False):
                 score_flops=score_f, attn_flops=attn_f, n_tok=n_tok, n_blk=n_blk)
 
 
-def sum_work(sh, visibles, mxfp8=False):
+def sum_work(sh, visibles, fmt="bf16"):
     tot = {}
     for v in visibles:
-        for k, x in row_work(sh, v, mxfp8).items():
+        for k, x in row_work(sh, v, fmt).items():
             tot[k] = tot.get(k, 0) + x
     return tot
 
@@ -213,8 +221,8 @@ def run_gpu(args):
     total_steps = W + K + args.breakdown_steps + args.e2e_steps + 4
     adv_per_batch = (math.ceil((W + K + min(K, 600) + args.e2e_steps + 4) / NB) + (62 if args.reuse_steps > 0 else 0)
                      + (math.ceil(args.pre_steps / NB) + 2 if args.pre_steps > 0 else 0)
-                     + (math.ceil(args.mxfp8_steps / NB) + 2 if args.mxfp8_steps > 0 else 0)
-                     + (math.ceil(args.window_steps / NB) + 2 if args.window_steps > 0 else 0))
+                     + (math.ceil(args.window_steps / NB) + 2 if args.window_steps > 0 else 0)
+                     + max([math.ceil(n / NB) + 2 for n in (args.mxfp8_steps, args.mxfp4_steps) if n > 0] or [0]))
     # center the prefixes of the main timed region on 32768
     start = wl.prefixes[0] - W // NB - K // (2 * NB)
     start = max(start, 8)
@@ -378,9 +386,10 @@ def run_gpu(args):
                                      ms)
     if args.window_steps > 0:
         out["local_window"] = run_window(args, Q, torch, sh, cache, batches, status, stream, NB, B, ms)
-    if args.mxfp8_steps > 0:
-        out["mxfp8"] = run_mxfp8(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, NB, B,
-                                 hbm_gbs, ms)
+    for fmt, steps in (("mxfp8", args.mxfp8_steps), ("mxfp4", args.mxfp4_steps)):
+        if steps > 0:
+            out[fmt] = run_mx(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, NB, B, hbm_gbs,
+                              ms, fmt, steps)
     return out, rank, world
 
 
@@ -418,14 +427,24 @@ def run_window(args, Q, torch, sh, cache, batches, status, stream, NB, B, ms_pla
             "tokens_per_row": "selected tokens before the run + the last 128 (at most budget + 128 + ratio - 1)"}
 
 
-def run_mxfp8(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, NB, B, hbm_gbs, ms_plain):
-    """The same decode workload with the MXFP8 index plane (index_format
-    QSA_INDEX_MXFP8): compressed keys stored as E4M3 + E8M0 scales (132 bytes per
-    key instead of 256), index queries MXFP8-rounded inside the step. Its own
-    cache, filled through qsa_append with the same prefixes; the same step
-    inputs; one rotation graph of the NB batches, timed with CUDA events."""
+MX_LEGS = {
+    "mxfp8": ("QSA_INDEX_MXFP8", "E4M3"),
+    "mxfp4": ("QSA_INDEX_MXFP4", "E2M1"),
+}
+
+
+def run_mx(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, NB, B, hbm_gbs, ms_plain, fmt,
+           n_steps):
+    """The same decode workload with an MX index plane (index_format
+    QSA_INDEX_MXFP8 or QSA_INDEX_MXFP4): compressed keys stored as E4M3 or E2M1
+    elements + one E8M0 scale per 32 values (132 or 68 bytes per key instead of
+    256), index queries MX-rounded inside the step. Its own cache, filled through
+    qsa_append with the same prefixes (the positions the decode leg started
+    from); the same step inputs; one rotation graph of the NB batches, timed
+    with CUDA events."""
     dev = batches[0]["k"].device
-    cfg8 = Q.Config.of(sh, Q.QSA_INDEX_MXFP8)
+    const, elem = MX_LEGS[fmt]
+    cfg8 = Q.Config.of(sh, getattr(Q, const))
     n_slots = B * NB
     cache8 = Q.PagedCache(cfg8, pt, n_slots * max_pages, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -447,7 +466,7 @@ def run_mxfp8(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, 
             Q.qsa_decode(cfg8, Q.Rows(bt["ids"], pos8[b], 1, advance=True), cache8, bt["k"], bt["v"], bt["idx"],
                          bt["q_idx"], bt["w"], bt["q"], bt["out"], ws8, status, stream=stream)
     torch.cuda.synchronize()
-    n_rot = max(1, math.ceil(args.mxfp8_steps / NB))
+    n_rot = max(1, math.ceil(n_steps / NB))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -463,16 +482,25 @@ def run_mxfp8(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, 
     ms = e0.elapsed_time(e1) / steps
     # timed rows: every batch at positions start + 1 .. start + n_rot (one warm-up step each before)
     visibles = [start + 1 + r + 1 for r in range(1, n_rot + 1) for _ in range(NB) for _ in range(B)]
-    work = sum_work(sh, visibles, mxfp8=True)
+    work = sum_work(sh, visibles, fmt)
     step_bytes = (work["score_bytes"] + work["attn_bytes"] + work["append_bytes"]) / steps
     gbs = step_bytes / (ms * 1e-3) / 1e9
+    stages = None
+    if args.breakdown_steps > 0:
+        # per-stage graphs on this cache, at the positions the timed rotations reached
+        bts = [dict(bt, pos0=pos8[b]) for b, bt in enumerate(batches)]
+        _, stage_ms, _, _ = stage_breakdown(args, Q, torch, cfg8, sh, cache8, bts, ws8, status, stream,
+                                            [start + n_rot + 1] * NB, NB, B, hbm_gbs, "")
+        stages = {k_: round(v_, 5) for k_, v_ in stage_ms.items()}
     del cache8
-    return {"what": "the decode workload (batch 32 x 32k) with the MXFP8 index plane: compressed keys as "
-                    "E4M3 + one E8M0 scale per 32 values, index queries MXFP8-rounded in the step",
+    return {"what": f"the decode workload (batch 32 x 32k) with the {fmt.upper()} index plane: compressed keys "
+                    f"as {elem} + one E8M0 scale per 32 values, index queries {fmt.upper()}-rounded in the step",
             "steps": steps, "ms_per_step": round(ms, 5), "rows_per_s": round(B / (ms * 1e-3), 1),
             "speedup_vs_bf16_plane": round(ms_plain / ms, 3), "bytes_per_step": int(step_bytes),
+            "stages_ms": stages,
             "achieved_gbs": round(gbs, 1), "hbm_roofline_frac": round(gbs / hbm_gbs, 4),
-            "bytes": "MXFP8 keys (d_I + d_I/32 per block), bf16 q_idx, w, K+V of the selected tokens, q, o, appends"}
+            "bytes": f"{fmt.upper()} keys ({key_bytes(sh, fmt)} B per block), bf16 q_idx, w, K+V of the selected "
+                     "tokens, q, o, appends"}
 
 
 def run_pre(args, Q, S, torch, cfg, sh, cache, batches, status, stream, NB, B, hbm_gbs, ms_plain):

@@ -142,8 +142,19 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
 }
 
 // x through MXFP8 and back, given its block's scale exponent e (exact in bf16).
+// x through MXFP8 and back at scale 2^e, in the value domain (FMA-pipe
+// arithmetic only): a = |x| / 2^e is below 512 by the scale rule; E4M3's
+// quantum is 2^(floor(log2 a) - 3) from 2^-6 up and 2^-9 below it (the
+// subnormals); a / quantum (< 16) rounds half to even by adding and removing
+// 2^23, and the result clamps to 448 (satfinite). Equal, bit for bit, to
+// e4m3_value(e4m3_code(x / 2^e)) * 2^e.
 __device__ __forceinline__ float mx_round(float x, int e) {
-  return e4m3_value(e4m3_code(x * exp2_int(-e))) * exp2_int(e);
+  const float a = fabsf(x) * exp2_int(-e);
+  // exponent field below 3: the difference wraps to a negative float, and fmaxf keeps 2^-9
+  const float q = fmaxf(__uint_as_float((__float_as_uint(a) & 0x7F800000u) - (3u << 23)), 0x1p-9f);
+  const float inv_q = __uint_as_float((254u << 23) - __float_as_uint(q));
+  const float r = __fadd_rn(__fadd_rn(a * inv_q, 0x1p23f), -0x1p23f);
+  return copysignf(fminf(r * q, 448.f) * exp2_int(e), x);
 }
 
 // MXFP4: scale exponent floor(log2 amax) - 2 (2: E2M1's top binade).
@@ -170,8 +181,16 @@ __device__ __forceinline__ float e2m1_value(uint32_t code) {
 }
 
 // x through MXFP4 and back, given its block's scale exponent e (exact in bf16).
+// x through MXFP4 and back at scale 2^e, in the value domain (no code):
+// a = |x| / 2^e is below 8 by the scale rule; the E2M1 quantum is 0.5 below 2,
+// 1 in [2, 4) and 2 above, so rintf's ties-to-even land on the even code at
+// every midpoint; magnitudes past 6 clamp to 6. Equal, bit for bit and sign of
+// zero included, to e2m1_value(e2m1_code(x / 2^e)) * 2^e.
 __device__ __forceinline__ float mx4_round(float x, int e) {
-  return e2m1_value(e2m1_code(x * exp2_int(-e))) * exp2_int(e);
+  const float a = fabsf(x) * exp2_int(-e);
+  const float q = a < 2.f ? 0.5f : (a < 4.f ? 1.f : 2.f);
+  const float inv_q = a < 2.f ? 2.f : (a < 4.f ? 1.f : 0.5f);
+  return copysignf(fminf(rintf(a * inv_q) * q, 6.f) * exp2_int(e), x);
 }
 
 // --- PTX wrappers ---------------------------------------------------------

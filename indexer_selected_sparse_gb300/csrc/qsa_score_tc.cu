@@ -414,10 +414,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w, uint32_t sc2, u
 // low exponent bits and top mantissa bit, its sign as the bf16 sign, read as
 // x * 2^-126 (the subnormal code 0.5 too), so one exact bf16 multiply by
 // 2^(126 + e) finishes it (sc2; e <= 1, else 2^126 and then 2^e in sc2b).
+// w_hi = w >> 4 holds byte K's high nibble in its byte K's low bits, so one
+// prmt (byte K of w into byte 0, byte K of w_hi into byte 2) puts the low
+// nibble at bits 0-3 and the high nibble at 16-19; the other bits are masked.
 template <int K>
-__device__ __forceinline__ uint32_t e2m1x2_to_bf16x2(uint32_t w, uint32_t sc2, uint32_t sc2b, bool two_step) {
-  const uint32_t b = (w >> (8 * K)) & 0xFFu;
-  const uint32_t y = b | (b << 12);  // low nibble at bits 0-3, high nibble at 16-19
+__device__ __forceinline__ uint32_t e2m1x2_to_bf16x2(uint32_t w, uint32_t w_hi, uint32_t sc2, uint32_t sc2b,
+                                                     bool two_step) {
+  uint32_t y;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(y) : "r"(w), "r"(w_hi), "n"(K | (K << 4) | ((4 + K) << 8) | ((4 + K) << 12)));
   const uint32_t t = ((y & 0x00070007u) << 6) | ((y & 0x00080008u) << 12);
   uint32_t r;
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(sc2));
@@ -749,22 +753,22 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
             const uint32_t sc2 = bf16x2_pow2(two ? 126 : 126 + e);
             const uint32_t sc2b = bf16x2_pow2(two ? e : 0);
             uint32_t *oj = o + jj * 16;  // byte k of the run: dims 32j + 2k, 32j + 2k + 1
-            oj[0] = e2m1x2_to_bf16x2<0>(v0, sc2, sc2b, two);
-            oj[1] = e2m1x2_to_bf16x2<1>(v0, sc2, sc2b, two);
-            oj[2] = e2m1x2_to_bf16x2<2>(v0, sc2, sc2b, two);
-            oj[3] = e2m1x2_to_bf16x2<3>(v0, sc2, sc2b, two);
-            oj[4] = e2m1x2_to_bf16x2<0>(v1, sc2, sc2b, two);
-            oj[5] = e2m1x2_to_bf16x2<1>(v1, sc2, sc2b, two);
-            oj[6] = e2m1x2_to_bf16x2<2>(v1, sc2, sc2b, two);
-            oj[7] = e2m1x2_to_bf16x2<3>(v1, sc2, sc2b, two);
-            oj[8] = e2m1x2_to_bf16x2<0>(v2, sc2, sc2b, two);
-            oj[9] = e2m1x2_to_bf16x2<1>(v2, sc2, sc2b, two);
-            oj[10] = e2m1x2_to_bf16x2<2>(v2, sc2, sc2b, two);
-            oj[11] = e2m1x2_to_bf16x2<3>(v2, sc2, sc2b, two);
-            oj[12] = e2m1x2_to_bf16x2<0>(v3, sc2, sc2b, two);
-            oj[13] = e2m1x2_to_bf16x2<1>(v3, sc2, sc2b, two);
-            oj[14] = e2m1x2_to_bf16x2<2>(v3, sc2, sc2b, two);
-            oj[15] = e2m1x2_to_bf16x2<3>(v3, sc2, sc2b, two);
+            oj[0] = e2m1x2_to_bf16x2<0>(v0, v0 >> 4, sc2, sc2b, two);
+            oj[1] = e2m1x2_to_bf16x2<1>(v0, v0 >> 4, sc2, sc2b, two);
+            oj[2] = e2m1x2_to_bf16x2<2>(v0, v0 >> 4, sc2, sc2b, two);
+            oj[3] = e2m1x2_to_bf16x2<3>(v0, v0 >> 4, sc2, sc2b, two);
+            oj[4] = e2m1x2_to_bf16x2<0>(v1, v1 >> 4, sc2, sc2b, two);
+            oj[5] = e2m1x2_to_bf16x2<1>(v1, v1 >> 4, sc2, sc2b, two);
+            oj[6] = e2m1x2_to_bf16x2<2>(v1, v1 >> 4, sc2, sc2b, two);
+            oj[7] = e2m1x2_to_bf16x2<3>(v1, v1 >> 4, sc2, sc2b, two);
+            oj[8] = e2m1x2_to_bf16x2<0>(v2, v2 >> 4, sc2, sc2b, two);
+            oj[9] = e2m1x2_to_bf16x2<1>(v2, v2 >> 4, sc2, sc2b, two);
+            oj[10] = e2m1x2_to_bf16x2<2>(v2, v2 >> 4, sc2, sc2b, two);
+            oj[11] = e2m1x2_to_bf16x2<3>(v2, v2 >> 4, sc2, sc2b, two);
+            oj[12] = e2m1x2_to_bf16x2<0>(v3, v3 >> 4, sc2, sc2b, two);
+            oj[13] = e2m1x2_to_bf16x2<1>(v3, v3 >> 4, sc2, sc2b, two);
+            oj[14] = e2m1x2_to_bf16x2<2>(v3, v3 >> 4, sc2, sc2b, two);
+            oj[15] = e2m1x2_to_bf16x2<3>(v3, v3 >> 4, sc2, sc2b, two);
           }
           tmem_st<32>(a_lane + c * (DI / 2) + hf * 32, o);
         }

@@ -9,6 +9,10 @@ the CPU oracle.
   subnormal range, saturation at 448 and all-zero blocks.
 * Scores: bit-exact against the oracle's MXFP8 score (the synthetic integer
   inputs keep every sum of products exact in fp32).
+* The scorer's own query rounding, on real-valued queries that do round (both
+  MX formats): scores of unrounded queries equal, bit for bit, those of the
+  same queries rounded first by qsa_quantize_index_q, whose output equals the
+  oracle's rounding.
 * Fused steps (decode, verify, ragged prefixes, d_I 64 and 8 blocks per page):
   selected sets bit-exact against the oracle scoring with the same
   quantisation; outputs within the bf16 gates."""
@@ -131,6 +135,55 @@ def test_scores_bit_exact():
     for r in range(n):
         nb = (pos0[r // 2] + r % 2 + 1) // 4
         assert torch.equal(scores2[r, :nb], scores[r, :nb])
+
+
+def real_queries(n, h_i, d_i, seed=29):
+    """Gaussian bf16 index queries with magnitudes spread over 2^-20 .. 2^12 per
+    32-value block (so blocks land in every scale range), an all-zero block and
+    a block of one tiny value: values that round in both MX formats."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(n, h_i, d_i, generator=g, dtype=torch.float64)
+    mag = torch.pow(2.0, torch.randint(-20, 13, (n, h_i, d_i // 32), generator=g).double())
+    x = x * mag.repeat_interleave(32, dim=-1)
+    x[0, 0, :32] = 0.0
+    x[0, 1, :32] = 0.0
+    x[0, 1, 5] = -(2.0 ** -130)
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("fmt", [1, 2], ids=["mxfp8", "mxfp4"])
+def test_scorer_rounds_real_valued_queries(fmt):
+    wl = small_wl(4, 256, 64, 128, 32, 4, [3000, 9000, 20001], R=2)
+    g = GpuState(wl, index_format=fmt)
+    g.append_prefix()
+    Q = g.Q
+    pos0 = list(wl.prefixes)
+    g.decode(pos0, 2)
+    g.check_status()
+    n = len(pos0) * 2
+    q = real_queries(n, 64, 128).to("cuda")
+    w = (torch.rand(n, 64, generator=torch.Generator().manual_seed(31)) + 0.25).to("cuda")
+    q_hat = torch.empty_like(q)
+    Q.qsa_quantize_index_q(g.cfg, q, q_hat)
+    torch.cuda.synchronize()
+    rnd = O.mxfp8_round_bits if fmt == 1 else O.mxfp4_round_bits
+    want = rnd(bits(q).reshape(-1, 128))
+    got = O.bf16_bits_to_f64(bits(q_hat).reshape(-1, 128))
+    assert np.array_equal(got, want), "qsa_quantize_index_q differs from the oracle's rounding"
+    assert not np.array_equal(got, O.bf16_bits_to_f64(bits(q).reshape(-1, 128))), "nothing rounded"
+    rows = g.rows(pos0, 2)
+    ld = (g.cache.max_blocks + 3) // 4 * 4
+    out = []
+    for qq in (q_hat, q):
+        sc = torch.full((n, ld), float("nan"), dtype=torch.float32, device="cuda")
+        Q.qsa_index_score(g.cfg, rows, g.cache, qq, w, sc, ld, g.status)
+        torch.cuda.synchronize()
+        g.check_status()
+        out.append(sc)
+    for r in range(n):
+        nb = (pos0[r // 2] + r % 2 + 1) // 4
+        assert torch.equal(out[1][r, :nb], out[0][r, :nb]), f"row {r}"
+        assert torch.isfinite(out[0][r, :nb]).all()
 
 
 FUSED = {
