@@ -272,8 +272,8 @@ def mxfp8_dequantize(elems, exps) -> np.ndarray:
 
 
 # MXFP4 ("ATOM Model Support Guide", "Model architecture details",
-# DeepSeek-V4.1, Cache bullet: an fp4 index plane in "the official E2M1 + E8M0
-# arithmetic", values and scales in two planes). OCP MX v1.0 MXFP4: blocks of 32
+# DeepSeek-V4.1, Cache bullet: an fp4 index plane of E2M1 values with E8M0
+# scales, the two kept in separate planes). OCP MX v1.0 MXFP4: blocks of 32
 # values share an E8M0 scale 2^(floor(log2 amax) - 2) (2: the exponent of E2M1's
 # top binade), each value an E2M1 element (sign, 2 exponent bits with bias 1,
 # 1 mantissa bit: 0, 0.5, 1, 1.5, 2, 3, 4, 6), value / scale rounded
