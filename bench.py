@@ -176,6 +176,44 @@ class ClockSampler:
 # the GPU arm
 # ---------------------------------------------------------------------------
 
+# ---------------------------------------------------------------------------
+# replicas (one process per GPU, no data-path collective): host-side pieces
+# ---------------------------------------------------------------------------
+
+def rank_env():
+    """(world, rank, local rank) from the launcher's environment (torchrun sets
+    all three; a plain run is one rank)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def replica_seed(seed, rank):
+    """Each replica pages its own cache with its own seeded page table."""
+    return seed + 1000 * rank
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x, device):
+    """The largest x over all ranks (x itself without a process group): the
+    slowest replica sets the step time of the whole job."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(rows_per_rank, world, ms):
+    """Rows per second of the whole job: every rank's rows over the slowest
+    rank's step time (weak scaling: the rows per rank stay fixed as N grows)."""
+    return rows_per_rank * world / (ms * 1e-3)
+
+
 def traffic_for(kernel_key):
     """ncu DRAM bytes per launch for a kernel, if the committed counters were
     taken on the kernel source as it is now."""
@@ -202,9 +240,7 @@ def run_gpu(args):
     from indexer_selected_sparse_gb300 import qsa as Q
     from indexer_selected_sparse_gb300 import synth as S
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -229,7 +265,7 @@ def run_gpu(args):
     n_slots = B * NB
     P = sh.page_size
     max_pages = math.ceil((start + adv_per_batch + 8) / P)
-    pt = S.page_table(wl.seed + 1000 * rank, n_slots, max_pages, contiguous=False)
+    pt = S.page_table(replica_seed(wl.seed, rank), n_slots, max_pages, contiguous=False)
     cache = Q.PagedCache(cfg, pt, n_slots * max_pages, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
@@ -321,8 +357,7 @@ def run_gpu(args):
     time.sleep(0.5)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
+    barrier(dist)
     torch.cuda.synchronize()
     t0 = time.time()
     with torch.cuda.stream(stream):
@@ -334,15 +369,10 @@ def run_gpu(args):
         ev1.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
-    if dist is not None:
-        dist.barrier()
+    barrier(dist)
     clk.stop()
     clocks = clk.summary(t0, t1)
-    ms = ev0.elapsed_time(ev1) / K
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(dist, ev0.elapsed_time(ev1) / K, dev)
     st = int(status.item())
     assert st == 0, f"device status {st}: {Q.qsa_strerror(st)}"
     # the same steps with one graph launch per step (not the headline: the
@@ -359,7 +389,7 @@ def run_gpu(args):
     ms_single = es0.elapsed_time(es1) / KS
     assert int(status.item()) == 0, Q.qsa_strerror(int(status.item()))
     rows_per_step = B * world
-    value = rows_per_step / (ms * 1e-3)
+    value = whole_job_rate(B, world, ms)
     work = sum_work(sh, visibles)
     step_bytes = (work["score_bytes"] + work["attn_bytes"] + work["append_bytes"]) / K
     hbm_gbs, tf_peak, peak_kind = measured_peaks()
@@ -682,8 +712,7 @@ def run_e2e(args, Q, torch, cfg, cache, batches, ws, status, stream, NB, B, rows
         h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in ("k", "v", "idx", "q_idx", "w", "q"))
         d2h = host[0]["out"].numel() * host[0]["out"].element_size()
         e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
-        if dist is not None:
-            dist.barrier()
+        barrier(dist)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             e0.record(stream)
@@ -691,13 +720,10 @@ def run_e2e(args, Q, torch, cfg, cache, batches, ws, status, stream, NB, B, rows
                 e2e_graphs[i % NB].replay()
             e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1) / KE
-        if dist is not None:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
+        barrier(dist)
+        ems = max_over_ranks(dist, e0.elapsed_time(e1) / KE, dev)
         assert int(status.item()) == 0, Q.qsa_strerror(int(status.item()))
-        e2e = {"value": round(rows_per_step / (ems * 1e-3), 1), "unit": "rows/s",
+        e2e = {"value": round(rows_per_step / (ems * 1e-3), 1), "unit": "rows/s",  # rows of all ranks
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ems, 5),
                "path": "pinned host inputs -> H2D -> qsa_decode -> D2H output, per step (CUDA graph)"}
     return e2e
@@ -943,10 +969,9 @@ def cpu_baseline(rows_per_worker):
 
 
 def run_reference(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
+    world, rank, _ = rank_env()
     if rank != 0:
-        return
+        return  # the oracle runs once, on rank 0's host cores
     n = min(os.cpu_count() or 1, 16)
     K, W = args.steps, args.warmup
     # a step = one decode row (of the batch's 32) on the CPU; the K steps are
