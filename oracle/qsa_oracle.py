@@ -120,12 +120,13 @@ class PreIndexer:
     multiplies by 1 + gamma). rotary_dim: leading dimensions rotated (NeoX:
     dimension i pairs with i + rotary_dim / 2); 0 disables RoPE."""
 
-    def __init__(self, gamma_q, gamma_k, eps: float, theta: float, rotary_dim: int):
+    def __init__(self, gamma_q, gamma_k, eps: float, theta: float, rotary_dim: int, mrope_section=None):
         self.gamma_q = np.asarray(gamma_q, np.float64)
         self.gamma_k = np.asarray(gamma_k, np.float64)
         self.eps = float(eps)
         self.theta = float(theta)
         self.rotary_dim = int(rotary_dim)
+        self.mrope_section = check_mrope_section(mrope_section, self.rotary_dim)
 
 
 def gemma_rmsnorm(x, gamma, eps: float) -> np.ndarray:
@@ -135,16 +136,59 @@ def gemma_rmsnorm(x, gamma, eps: float) -> np.ndarray:
     return x / rms * (1.0 + np.asarray(gamma, np.float64))
 
 
-def rope_neox(x, pos, rotary_dim: int, theta: float) -> np.ndarray:
+# Interleaved MRoPE ("Agentic shootout", "Flash-Next support: vLLM vs Atlas",
+# (a) item 6: the indexer's RoPE is main attention's, interleaved MRoPE
+# included; the report on the fused pre-indexer kernel: temporal, height and
+# width rotary pairs interleave, a pair's axis chosen by its index modulo 3,
+# with bounds for the height and width sections; the notes on a dense sibling
+# model: mrope_section = [11, 11, 10] over 64 rotary dimensions). Reading: a
+# token's position is a triple (t, h, w); NeoX pair i turns by the height
+# position when i % 3 == 1 and i < 3 * section_h, by the width position when
+# i % 3 == 2 and i < 3 * section_w, and by the temporal one otherwise. The
+# sections add up to rotary_dim / 2. A text token has t = h = w = its position.
+
+
+def check_mrope_section(section, rotary_dim: int):
+    """(t, h, w) section sizes in rotary pairs, or None (plain RoPE)."""
+    if section is None:
+        return None
+    sec = tuple(int(v) for v in section)
+    if len(sec) != 3 or min(sec) < 0 or sum(sec) != rotary_dim // 2:
+        raise ValueError(f"mrope section {section} must be 3 counts adding up to {rotary_dim // 2}")
+    return sec
+
+
+def mrope_axes(rotary_dim: int, section) -> np.ndarray:
+    """Axis of each NeoX pair i < rotary_dim / 2: 0 temporal, 1 height, 2 width."""
+    i = np.arange(rotary_dim // 2)
+    ax = np.zeros(rotary_dim // 2, np.int64)
+    ax[(i % 3 == 1) & (i < 3 * section[1])] = 1
+    ax[(i % 3 == 2) & (i < 3 * section[2])] = 2
+    return ax
+
+
+def pair_positions(pos, rotary_dim: int, section) -> np.ndarray:
+    """The position each NeoX pair turns by: pos for plain RoPE (section None);
+    with MRoPE, pos is a (t, h, w) triple (an integer stands for (p, p, p))."""
+    half = rotary_dim // 2
+    if section is None:
+        return np.full(half, float(pos))
+    trip = np.broadcast_to(np.asarray(pos, np.float64), (3,))
+    return trip[mrope_axes(rotary_dim, section)]
+
+
+def rope_neox(x, pos, rotary_dim: int, theta: float, section=None) -> np.ndarray:
     """NeoX rotary embedding at position pos over the last axis: for
     i < rotary_dim/2 the pair (x_i, x_{i+rotary_dim/2}) is rotated by the angle
-    pos * theta^(-2i/rotary_dim); dimensions >= rotary_dim are unchanged."""
+    p_i * theta^(-2i/rotary_dim), p_i = pos (or, with an MRoPE section, the
+    coordinate of the triple pos that pair i takes); dimensions >= rotary_dim
+    are unchanged."""
     x = np.array(x, np.float64)
     if rotary_dim == 0:
         return x
     half = rotary_dim // 2
     i = np.arange(half, dtype=np.float64)
-    ang = float(pos) * theta ** (-2.0 * i / rotary_dim)
+    ang = pair_positions(pos, rotary_dim, section) * theta ** (-2.0 * i / rotary_dim)
     c, s = np.cos(ang), np.sin(ang)
     x1 = x[..., :half].copy()
     x2 = x[..., half:rotary_dim].copy()
@@ -153,19 +197,21 @@ def rope_neox(x, pos, rotary_dim: int, theta: float) -> np.ndarray:
     return x
 
 
-def pre_index_query(q_bits, pos: int, pre: PreIndexer) -> np.ndarray:
-    """Index query heads [H_I, d_I] of the row at pos: Gemma RMSNorm per head,
-    then RoPE at the row's position; bf16 bits."""
+def pre_index_query(q_bits, pos, pre: PreIndexer) -> np.ndarray:
+    """Index query heads [H_I, d_I] of the row at pos (a (t, h, w) triple with
+    MRoPE): Gemma RMSNorm per head, then RoPE at the row's position; bf16 bits."""
     q = bf16_bits_to_f64(q_bits)
-    return f64_to_bf16_bits(rope_neox(gemma_rmsnorm(q, pre.gamma_q, pre.eps), pos, pre.rotary_dim, pre.theta))
+    return f64_to_bf16_bits(rope_neox(gemma_rmsnorm(q, pre.gamma_q, pre.eps), pos, pre.rotary_dim, pre.theta,
+                                      pre.mrope_section))
 
 
-def pool_block_pre(raw_bits, first_pos: int, pre: PreIndexer) -> np.ndarray:
-    """Compressed key of the block whose first token is at first_pos: the mean
-    of its raw index keys, then Gemma RMSNorm, then RoPE at first_pos; bf16."""
+def pool_block_pre(raw_bits, first_pos, pre: PreIndexer) -> np.ndarray:
+    """Compressed key of the block whose first token is at first_pos (that
+    token's (t, h, w) triple with MRoPE): the mean of its raw index keys, then
+    Gemma RMSNorm, then RoPE at first_pos; bf16."""
     raw = bf16_bits_to_f64(raw_bits)
     k = gemma_rmsnorm(raw.mean(axis=0), pre.gamma_k, pre.eps)
-    return f64_to_bf16_bits(rope_neox(k, first_pos, pre.rotary_dim, pre.theta))
+    return f64_to_bf16_bits(rope_neox(k, first_pos, pre.rotary_dim, pre.theta, pre.mrope_section))
 
 
 # ---------------------------------------------------------------------------
@@ -186,19 +232,20 @@ class AttnOptions:
     that side is not normed or roped); eps, theta, rotary_dim as in PreIndexer."""
 
     def __init__(self, gamma_q=None, gamma_k=None, eps: float = 1e-6, theta: float = 1e4,
-                 rotary_dim: int = 64):
+                 rotary_dim: int = 64, mrope_section=None):
         self.gamma_q = None if gamma_q is None else np.asarray(gamma_q, np.float64)
         self.gamma_k = None if gamma_k is None else np.asarray(gamma_k, np.float64)
         self.eps = float(eps)
         self.theta = float(theta)
         self.rotary_dim = int(rotary_dim)
+        self.mrope_section = check_mrope_section(mrope_section, self.rotary_dim)
 
 
-def prep_heads(x_bits, pos: int, gamma, eps: float, rotary_dim: int, theta: float) -> np.ndarray:
-    """Heads [H, D] of the token at pos: Gemma RMSNorm per head, then RoPE at pos;
-    bf16 bits."""
+def prep_heads(x_bits, pos, gamma, eps: float, rotary_dim: int, theta: float, section=None) -> np.ndarray:
+    """Heads [H, D] of the token at pos (a (t, h, w) triple with an MRoPE
+    section): Gemma RMSNorm per head, then RoPE at pos; bf16 bits."""
     x = bf16_bits_to_f64(x_bits)
-    return f64_to_bf16_bits(rope_neox(gemma_rmsnorm(x, gamma, eps), pos, rotary_dim, theta))
+    return f64_to_bf16_bits(rope_neox(gemma_rmsnorm(x, gamma, eps), pos, rotary_dim, theta, section))
 
 
 def sigmoid(x) -> np.ndarray:
@@ -350,28 +397,42 @@ class SeqState:
         self.V = np.zeros((capacity, n_kv_heads, head_dim), np.uint16)
         self.idx_raw = np.zeros((capacity, idx_dim), np.uint16)
         self.idx_blk = np.zeros((capacity // ratio, idx_dim), np.uint16)
+        self.mpos = np.zeros((capacity, 3), np.int64)  # (t, h, w) of every token (MRoPE)
         self.ingested = 0
+
+    def rope_pos(self, p: int, section):
+        """The position token p turns by: its (t, h, w) triple with MRoPE, else p."""
+        return tuple(self.mpos[p]) if section is not None else p
+
+    def block_rope_pos(self, b: int):
+        """A compressed key turns at its block's first token ([VA6]: RoPE at the
+        group's first position)."""
+        return self.rope_pos(b * self.ratio, self.pre.mrope_section)
 
     @property
     def n_blocks(self) -> int:
         """pooled = ingested / ratio ([INV1])."""
         return self.ingested // self.ratio
 
-    def append(self, pos: int, k_bits, v_bits, idx_bits) -> None:
+    def append(self, pos: int, k_bits, v_bits, idx_bits, mpos=None) -> None:
         """Ingest n new tokens at positions pos..pos+n-1.
 
         Requires pos == ingested ([INV1]: decode at pos requires
         pos == ingested). Every block completed by the new tokens is pooled
-        from the raw keys it holds now."""
+        from the raw keys it holds now. mpos [n, 3]: the tokens' (t, h, w)
+        MRoPE positions (default: (p, p, p), a text token's)."""
         k_bits = np.asarray(k_bits, np.uint16)
         n = k_bits.shape[0]
         if pos != self.ingested:
             raise DesyncError(f"append at pos {pos} but {self.ingested} tokens ingested")
         if pos + n > self.capacity:
             raise CapacityError(f"append of {n} at pos {pos} exceeds capacity {self.capacity}")
+        p = np.arange(pos, pos + n, dtype=np.int64)
+        self.mpos[pos:pos + n] = np.stack([p, p, p], axis=1) if mpos is None else np.asarray(mpos, np.int64)
         if self.attn is not None and self.attn.gamma_k is not None:
             a = self.attn
-            k_bits = np.stack([prep_heads(k_bits[t], pos + t, a.gamma_k, a.eps, a.rotary_dim, a.theta)
+            k_bits = np.stack([prep_heads(k_bits[t], self.rope_pos(pos + t, a.mrope_section), a.gamma_k, a.eps,
+                                          a.rotary_dim, a.theta, a.mrope_section)
                                for t in range(n)]) if n else k_bits
         self.K[pos:pos + n] = k_bits
         self.V[pos:pos + n] = np.asarray(v_bits, np.uint16)
@@ -383,7 +444,7 @@ class SeqState:
             if self.pre is None:
                 self.idx_blk[b] = pool_block(self.idx_raw[b * r:(b + 1) * r])
             else:
-                self.idx_blk[b] = pool_block_pre(self.idx_raw[b * r:(b + 1) * r], b * r, self.pre)
+                self.idx_blk[b] = pool_block_pre(self.idx_raw[b * r:(b + 1) * r], self.block_rope_pos(b), self.pre)
         self.ingested = pos + n
 
     def rewind(self, n_drop: int) -> None:
@@ -484,14 +545,15 @@ def gqa_attention(q_bits, k_bits, v_bits) -> np.ndarray:
 
 def attend_row(state: SeqState, pos: int, q_idx_bits, w, q_bits, topk: int,
                index_format: str = "bf16", window: int = 0, attn: "AttnOptions" = None,
-               gate_bits=None) -> Dict:
+               gate_bits=None, q_mpos=None) -> Dict:
     """The whole path for one query row at logical position pos.
 
     The row's token is already ingested, so V = pos + 1 tokens are visible and
     n_blk = V // ratio blocks are complete. index_format "mxfp8" scores with
     the MXFP8 index plane (block_scores_mxfp8); window keeps the last `window`
     tokens as well (token_set). attn (with gamma_q) norms and ropes the query
-    heads at pos; gate_bits [Hq, D] gates the output: o * sigmoid(g)."""
+    heads at pos (at the triple q_mpos with an MRoPE section; default
+    (pos, pos, pos)); gate_bits [Hq, D] gates the output: o * sigmoid(g)."""
     r = state.ratio
     visible = pos + 1
     if visible > state.ingested:
@@ -505,7 +567,8 @@ def attend_row(state: SeqState, pos: int, q_idx_bits, w, q_bits, topk: int,
     sel = select_blocks(scores if scores is not None else np.zeros(n_blk), topk)
     toks = token_set(sel, n_blk, visible, r, window)
     if attn is not None and attn.gamma_q is not None:
-        q_bits = prep_heads(q_bits, pos, attn.gamma_q, attn.eps, attn.rotary_dim, attn.theta)
+        qp = pos if q_mpos is None else tuple(q_mpos)
+        q_bits = prep_heads(q_bits, qp, attn.gamma_q, attn.eps, attn.rotary_dim, attn.theta, attn.mrope_section)
     out = gqa_attention(q_bits, state.K[toks], state.V[toks])
     if gate_bits is not None:
         out = out * sigmoid(bf16_bits_to_f64(gate_bits))

@@ -221,6 +221,32 @@ def e2m1_ties_up(v):
     return np.copysign(np.minimum(np.floor(a / q + 0.5) * q, 6.0), v)
 
 
+def mrope_h_w_swapped(rotary_dim, section):
+    i = np.arange(rotary_dim // 2)
+    ax = np.zeros(rotary_dim // 2, np.int64)
+    ax[(i % 3 == 2) & (i < 3 * section[1])] = 1
+    ax[(i % 3 == 1) & (i < 3 * section[2])] = 2
+    return ax
+
+
+def mrope_bounds_not_tripled(rotary_dim, section):
+    i = np.arange(rotary_dim // 2)
+    ax = np.zeros(rotary_dim // 2, np.int64)
+    ax[(i % 3 == 1) & (i < section[1])] = 1
+    ax[(i % 3 == 2) & (i < section[2])] = 2
+    return ax
+
+
+def mrope_temporal_only(pos, rotary_dim, section):
+    p = pos if section is None else np.broadcast_to(np.asarray(pos, np.float64), (3,))[0]
+    return np.full(rotary_dim // 2, float(p))
+
+
+class MropeBlocksAtLastToken(O.SeqState):
+    def block_rope_pos(self, b):
+        return self.rope_pos((b + 1) * self.ratio - 1, self.pre.mrope_section)
+
+
 MUTATIONS = [
     ("block_scores", no_relu, [P.test_score_closed_forms]),
     ("block_scores", relu_outside, [P.test_score_closed_forms]),
@@ -248,6 +274,11 @@ MUTATIONS = [
     ("SeqState", KeysRopedAtZero, [P.test_attention_qk_norm_rope_and_gate_hand_worked]),
     ("mxfp4_quantize", mxfp4_emax_3, [P.test_mxfp4_scale_rule_on_a_hand_worked_block]),
     ("e2m1_round", e2m1_ties_up, [P.test_e2m1_grid_and_nearest_even_rounding]),
+    ("mrope_axes", mrope_h_w_swapped, [P.test_mrope_pairs_follow_the_interleave_and_its_section_bounds]),
+    ("mrope_axes", mrope_bounds_not_tripled, [P.test_mrope_pairs_follow_the_interleave_and_its_section_bounds]),
+    ("pair_positions", mrope_temporal_only, [P.test_mrope_pairs_follow_the_interleave_and_its_section_bounds,
+                                             P.test_mrope_is_plain_rope_for_text_and_sees_only_per_axis_offsets]),
+    ("SeqState", MropeBlocksAtLastToken, [P.test_mrope_blocks_rope_at_their_first_tokens_triple]),
     ("sigmoid", sigmoid_of_minus, [P.test_sigmoid_closed_forms, P.test_attention_qk_norm_rope_and_gate_hand_worked]),
 ]
 

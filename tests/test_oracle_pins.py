@@ -447,6 +447,118 @@ def test_pre_indexed_blocks_norm_then_rope_at_the_first_position():
     assert abs(s1 - s2) < 1e-9
 
 
+# Interleaved MRoPE: a position is a (t, h, w) triple; NeoX pair i turns by h
+# when i % 3 == 1 below 3 x the height section, by w when i % 3 == 2 below
+# 3 x the width section, and by t otherwise
+
+
+def pairs_moved_by_each_axis(section, rotary_dim=64, theta=1e4):
+    """For each coordinate of the position triple, the NeoX pairs it turns,
+    found by rotating unit vectors and moving one coordinate at a time."""
+    moved = {0: [], 1: [], 2: []}
+    for i in range(rotary_dim // 2):
+        e = np.zeros(rotary_dim); e[i] = 1.0
+        still = O.rope_neox(e, (0, 0, 0), rotary_dim, theta, section)
+        for ax in range(3):
+            p = [0, 0, 0]; p[ax] = 7
+            if not np.allclose(O.rope_neox(e, tuple(p), rotary_dim, theta, section), still, atol=1e-12):
+                moved[ax].append(i)
+    return moved
+
+
+def test_mrope_pairs_follow_the_interleave_and_its_section_bounds():
+    # the pages' sections [11, 11, 10] over 64 rotary dims: t, h, w in turn to the end
+    m = pairs_moved_by_each_axis((11, 11, 10))
+    assert m[0] == [0, 3, 6, 9, 12, 15, 18, 21, 24, 27, 30]
+    assert m[1] == [1, 4, 7, 10, 13, 16, 19, 22, 25, 28, 31]
+    assert m[2] == [2, 5, 8, 11, 14, 17, 20, 23, 26, 29]
+    # sections [16, 8, 8]: the height and width bounds end the interleave at pair 24
+    m = pairs_moved_by_each_axis((16, 8, 8))
+    assert m[0] == [0, 3, 6, 9, 12, 15, 18, 21] + list(range(24, 32))
+    assert m[1] == [1, 4, 7, 10, 13, 16, 19, 22]
+    assert m[2] == [2, 5, 8, 11, 14, 17, 20, 23]
+    # every pair turns with exactly one axis, as many pairs per axis as its section
+    for sec in ((11, 11, 10), (16, 8, 8), (12, 10, 10), (32, 0, 0)):
+        m = pairs_moved_by_each_axis(sec)
+        assert sorted(m[0] + m[1] + m[2]) == list(range(32))
+        assert [len(m[a]) for a in range(3)] == list(sec)
+    with pytest.raises(ValueError):
+        O.PreIndexer(np.zeros(128), np.zeros(128), 1e-6, 1e4, 64, mrope_section=(11, 11, 11))
+
+
+def test_mrope_is_plain_rope_for_text_and_sees_only_per_axis_offsets():
+    rng = np.random.default_rng(53)
+    sec = (11, 11, 10)
+    v = rng.standard_normal(128)
+    for p in (0, 5, 4097, 32768):   # a text token (t = h = w = p) turns as plain RoPE at p, bit for bit
+        assert np.array_equal(O.rope_neox(v, (p, p, p), 64, 1e4, sec), O.rope_neox(v, p, 64, 1e4))
+        assert np.array_equal(O.rope_neox(v, p, 64, 1e4, sec), O.rope_neox(v, p, 64, 1e4))
+    P1, P2 = (40, 3, 17), (900, 12, 5)
+    r1 = O.rope_neox(v, P1, 64, 1e4, sec)
+    assert np.allclose(r1[:32] ** 2 + r1[32:64] ** 2, v[:32] ** 2 + v[32:64] ** 2, atol=1e-12)
+    both = tuple(a + b for a, b in zip(P1, P2))
+    assert np.allclose(O.rope_neox(r1, P2, 64, 1e4, sec), O.rope_neox(v, both, 64, 1e4, sec), atol=1e-9)
+    assert np.array_equal(O.rope_neox(v, P1, 64, 1e4, sec)[64:], v[64:])
+    q, k = rng.standard_normal(128), rng.standard_normal(128)
+
+    def dot(pq, pk):
+        return O.rope_neox(q, pq, 64, 1e4, sec)[:64] @ O.rope_neox(k, pk, 64, 1e4, sec)[:64]
+    d1 = dot((5000, 40, 60), (4000, 30, 70))
+    assert abs(d1 - dot((1000, 10, 0), (0, 0, 10))) < 1e-9      # the same offsets on every axis
+    assert abs(d1 - dot((5000, 41, 60), (4000, 30, 70))) > 1e-6  # one row further down: another score
+
+
+def test_mrope_blocks_rope_at_their_first_tokens_triple():
+    rng = np.random.default_rng(59)
+    dI, ratio, sec = 128, 4, (11, 11, 10)
+    pre = O.PreIndexer(rng.standard_normal(dI) * 0.2, rng.standard_normal(dI) * 0.2, 1e-6, 1e4, 64,
+                       mrope_section=sec)
+    # an image run (t fixed, (h, w) walking a 4-wide grid), then text
+    mpos = np.array([(10, 10 + i // 4, 10 + i % 4) for i in range(12)] + [(14 + i, 14 + i, 14 + i) for i in range(8)])
+    keys = rng.integers(-8, 9, size=(5, dI)).astype(np.float64)
+    raw = O.f64_to_bf16_bits(np.repeat(keys, ratio, axis=0))
+    z = np.zeros((5 * ratio, 1, 16), np.uint16)
+    st = O.SeqState(ratio, 1, 16, dI, 64, pre=pre)
+    st.append(0, z, z, raw, mpos=mpos)
+    for b in range(5):
+        kn = O.gemma_rmsnorm(keys[b], pre.gamma_k, 1e-6)
+        assert np.array_equal(st.idx_blk[b], O.f64_to_bf16_bits(O.rope_neox(kn, tuple(mpos[b * ratio]), 64, 1e4, sec)))
+    # block 1 spans (10, 11, 10) .. (10, 11, 13): its last token's triple gives another key
+    kn = O.gemma_rmsnorm(keys[1], pre.gamma_k, 1e-6)
+    assert not np.array_equal(st.idx_blk[1], O.f64_to_bf16_bits(O.rope_neox(kn, tuple(mpos[7]), 64, 1e4, sec)))
+    # a block completed by a later append uses the triple stored with its first token
+    st2 = O.SeqState(ratio, 1, 16, dI, 64, pre=pre)
+    st2.append(0, z[:6], z[:6], raw[:6], mpos=mpos[:6])
+    st2.append(6, z[6:], z[6:], raw[6:], mpos=mpos[6:])
+    assert np.array_equal(st2.idx_blk[:5], st.idx_blk[:5])
+    # text positions (the default) reduce to the plain pre-indexer
+    plain = O.PreIndexer(pre.gamma_q, pre.gamma_k, 1e-6, 1e4, 64)
+    a, b_ = O.SeqState(ratio, 1, 16, dI, 64, pre=pre), O.SeqState(ratio, 1, 16, dI, 64, pre=plain)
+    a.append(0, z, z, raw); b_.append(0, z, z, raw)
+    assert np.array_equal(a.idx_blk[:5], b_.idx_blk[:5])
+
+
+def test_mrope_attention_heads_at_their_own_triples():
+    rng = np.random.default_rng(61)
+    sec, D, n = (11, 11, 10), 128, 9
+    att = O.AttnOptions(rng.standard_normal(D) * 0.1, rng.standard_normal(D) * 0.1, 1e-6, 1e4, 64, mrope_section=sec)
+    mpos = np.array([(3, 3 + i % 3, 3 + i // 3) for i in range(n)])
+    k, v = bf16(rng.standard_normal((n, 2, D))), bf16(rng.standard_normal((n, 2, D)))
+    st = O.SeqState(4, 2, D, 8, 16, attn=att)
+    st.append(0, k, v, np.zeros((n, 8), np.uint16), mpos=mpos)
+    for t in range(n):
+        assert np.array_equal(st.K[t], O.prep_heads(k[t], tuple(mpos[t]), att.gamma_k, 1e-6, 64, 1e4, sec))
+    # the row's query heads turn at the row's own triple
+    q = bf16(rng.standard_normal((4, D)))
+    qp = (6, 5, 4)
+    got = O.attend_row(st, n - 1, np.zeros((1, 8), np.uint16), np.ones(1), q, 4, attn=att, q_mpos=qp)
+    q_prep = O.prep_heads(q, qp, att.gamma_q, 1e-6, 64, 1e4, sec)
+    ref = O.attend_row(st, n - 1, np.zeros((1, 8), np.uint16), np.ones(1), q_prep, 4)
+    assert np.array_equal(got["out"], ref["out"])
+    other = O.attend_row(st, n - 1, np.zeros((1, 8), np.uint16), np.ones(1), q, 4, attn=att, q_mpos=(6, 5, 5))
+    assert not np.array_equal(got["out"], other["out"])
+
+
 # ---------------------------------------------------------------------------
 # State: append / rewind / chunking / counters
 # ---------------------------------------------------------------------------
