@@ -65,6 +65,9 @@ def parse():
                     help="decode steps with the MXFP8 index plane (own cache); 0 skips")
     ap.add_argument("--mxfp4-steps", type=int, default=600,
                     help="decode steps with the MXFP4 index plane (own cache); 0 skips")
+    ap.add_argument("--attn-steps", type=int, default=300,
+                    help="decode steps with the main-attention options (q/k norm + RoPE, output gate; own "
+                         "cache); 0 skips")
     ap.add_argument("--window-steps", type=int, default=300,
                     help="decode steps with a 128-token always-kept local window; 0 skips")
     ap.add_argument("--prefill-warmup", type=int, default=3)
@@ -258,7 +261,8 @@ def run_gpu(args):
     adv_per_batch = (math.ceil((W + K + min(K, 600) + args.e2e_steps + 4) / NB) + (62 if args.reuse_steps > 0 else 0)
                      + (math.ceil(args.pre_steps / NB) + 2 if args.pre_steps > 0 else 0)
                      + (math.ceil(args.window_steps / NB) + 2 if args.window_steps > 0 else 0)
-                     + max([math.ceil(n / NB) + 2 for n in (args.mxfp8_steps, args.mxfp4_steps) if n > 0] or [0]))
+                     + max([math.ceil(n / NB) + 2 for n in (args.mxfp8_steps, args.mxfp4_steps, args.attn_steps)
+                            if n > 0] or [0]))
     # center the prefixes of the main timed region on 32768
     start = wl.prefixes[0] - W // NB - K // (2 * NB)
     start = max(start, 8)
@@ -420,7 +424,73 @@ def run_gpu(args):
         if steps > 0:
             out[fmt] = run_mx(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, NB, B, hbm_gbs,
                               ms, fmt, steps)
+    if args.attn_steps > 0:
+        try:
+            out["attn_options"] = run_attn_options(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream,
+                                                   NB, B, ms)
+        except Exception as e:  # this leg's failure is reported; the headline line still prints
+            out["attn_options"] = {"error": f"{type(e).__name__}: {e}"}
     return out, rank, world
+
+
+def run_attn_options(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, NB, B, ms_plain):
+    """The decode workload with the main-attention options on (qsa_attn_options):
+    q and k heads GemmaRMSNormed (gain 1 + gamma) and NeoX-roped over 64 dims
+    (keys as they are appended, the step's queries inside the step) and a
+    sigmoid output gate, one bf16 gate value per output element. Its own cache,
+    filled through qsa_append_ex with the same prefixes; the decode leg's step
+    inputs plus a gate per batch; one rotation graph of the NB batches."""
+    dev = batches[0]["k"].device
+    cfg = Q.Config.of(sh)
+    n_slots = B * NB
+    cache_a = Q.PagedCache(cfg, pt, n_slots * max_pages, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    gen = torch.Generator().manual_seed(wl.seed + 77)
+    gq = (0.2 * torch.randn(sh.head_dim, generator=gen)).to(dev)
+    gk = (0.2 * torch.randn(sh.head_dim, generator=gen)).to(dev)
+    fill = Q.AttnOptions(None, gk, 1e-6, 1e4, 64)
+    chunk = 8192
+    for s_ in range(n_slots):
+        a = 0
+        while a < start:
+            m = min(chunk, start - a)
+            k, v, ix = S.token_rows(sh, wl.seed, s_, torch.arange(a, a + m), device=dev)
+            Q.qsa_append_ex(cfg, None, fill, Q.Rows(torch.tensor([s_], device=dev),
+                                                   torch.tensor([a], device=dev, dtype=torch.int32), m),
+                            cache_a, k, v, ix, status)
+            a += m
+    gates = [(2 * torch.randn(B, sh.n_q_heads, sh.head_dim, generator=gen)).to(torch.bfloat16).to(dev)
+             for _ in range(NB)]
+    opts = [Q.AttnOptions(gq, gk, 1e-6, 1e4, 64, gate=gates[b]) for b in range(NB)]
+    ws_a = Q.workspace_ex(cfg, B, cache_a.max_blocks, device=dev)
+    pos_a = [torch.full((B,), start, dtype=torch.int32, device=dev) for _ in range(NB)]
+    rot = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(rot, stream=stream):
+        for b, bt in enumerate(batches):
+            Q.qsa_decode_ex(cfg, None, opts[b], Q.Rows(bt["ids"], pos_a[b], 1, advance=True), cache_a, bt["k"],
+                            bt["v"], bt["idx"], bt["q_idx"], bt["w"], bt["q"], bt["out"], ws_a, status,
+                            stream=stream)
+    torch.cuda.synchronize()
+    n_rot = max(1, math.ceil(args.attn_steps / NB))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        rot.replay()  # warm-up rotation
+        e0.record(stream)
+        for _ in range(n_rot):
+            rot.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st == 0, f"device status {st}: {Q.qsa_strerror(st)}"
+    steps = n_rot * NB
+    ms = e0.elapsed_time(e1) / steps
+    del rot, cache_a
+    return {"what": "decode step with the main-attention options: q/k GemmaRMSNorm + NeoX RoPE (64 dims) and a "
+                    "sigmoid output gate, batch 32 x 32k",
+            "steps": steps, "ms_per_step": round(ms, 5), "rows_per_s": round(B / (ms * 1e-3), 1),
+            "overhead_vs_plain_ms": round(ms - ms_plain, 5),
+            "extra_bytes_per_row": sh.n_q_heads * sh.head_dim * 2}
 
 
 def run_window(args, Q, torch, sh, cache, batches, status, stream, NB, B, ms_plain, window=128):
