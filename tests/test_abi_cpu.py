@@ -181,3 +181,36 @@ def test_local_window_checked_and_sizes_grow(Q):
     assert Q.qsa_max_attend_tokens(base) >= 2048 + 3
     assert Q.qsa_max_attend_tokens(win) > Q.qsa_max_attend_tokens(base)
     assert Q.qsa_workspace_bytes(win, 32, 8200) > Q.qsa_workspace_bytes(base, 32, 8200)
+
+
+def test_attention_options_checked_on_host(Q):
+    cfg = Q.Config(4, 2048, 64, 128, 32, 4)
+    c = ctypes.byref(cfg.c())
+    lib = Q.LIB
+    cache = Q.qsa_cache(16, 1, 4, 4, 16, 16, 16, 16, 16)      # 4 pages of 64 tokens, fake aligned pointers
+    rows = Q.qsa_rows(1, 1, 16, 16, None, 0)
+
+    def opts(eps=1e-6, theta=1e4, rot=64, gate=None):
+        return Q.qsa_attn_options(16, 16, eps, theta, rot, gate)
+
+    def decode(o, ws_bytes=1 << 30):
+        return lib.qsa_decode_ex(c, None, ctypes.byref(o), ctypes.byref(rows), ctypes.byref(cache), 16, 16, 16,
+                                 16, 16, 16, None, None, 16, 16, ws_bytes, 16, None)
+
+    cases = [(opts(eps=-1.0), Q.QSA_ERR_INVALID_ARG),          # epsilon below zero
+             (opts(eps=float("nan")), Q.QSA_ERR_INVALID_ARG),
+             (opts(theta=0.0), Q.QSA_ERR_INVALID_ARG),         # RoPE base must be positive
+             (opts(rot=32), Q.QSA_ERR_UNSUPPORTED),            # rotary dims 0, 64 or D
+             (opts(gate=18), Q.QSA_ERR_INVALID_ARG)]           # the gate is read with 16-byte loads
+    for o, code in cases:
+        assert lib.qsa_append_ex(c, None, ctypes.byref(o), ctypes.byref(rows), ctypes.byref(cache), 16, 16, 16,
+                                 16, None) == code
+        assert decode(o) == code
+    # the step's prepared main queries live in the workspace: the plain size is refused before any launch
+    plain = Q.qsa_workspace_bytes(cfg, 1, 64)
+    ex = Q.qsa_workspace_bytes_ex(cfg, 1, 64)
+    assert ex >= plain + 32 * 128 * 2
+    assert decode(opts(), plain) == Q.QSA_ERR_WORKSPACE
+    # without a query norm (gate and key options only) the bar is the plain size: one byte less is refused
+    # (a size that passes would go on to launch kernels, which these fake pointers must never reach)
+    assert decode(Q.qsa_attn_options(None, 16, 1e-6, 1e4, 64, 16), plain - 1) == Q.QSA_ERR_WORKSPACE
