@@ -1,0 +1,49 @@
+"""The host arithmetic behind bench.py's roofline figures: algorithmic bytes
+and FLOPs per decode row, worked by hand for the batch-32 x 32k workload
+(ratio 4, budget 2048, H_I 64 x d_I 128, Hq 32 / Hkv 4, D 128)."""
+import pytest
+
+import bench
+from indexer_selected_sparse_gb300 import synth as S
+
+
+@pytest.fixture(scope="module")
+def sh():
+    return S.workload(2).shapes
+
+
+def test_decode_row_at_32k(sh):
+    # V = 32769 visible tokens: 8192 complete blocks, 512 of them selected plus a tail of 1
+    w = bench.row_work(sh, 32769)
+    assert (w["n_blk"], w["n_tok"]) == (8192, 2049)
+    # keys 8192 x 128 x 2 B, the row's index queries 64 x 128 x 2 B, its 64 fp32 weights
+    assert w["score_bytes"] == 2_097_152 + 16_384 + 256 == 2_113_792
+    # K and V of 2049 tokens x 4 heads x 128 x 2 B, then q and o (32 x 128 x 2 B each)
+    assert w["attn_bytes"] == 2049 * 4 * 128 * 2 * 2 + 2 * 32 * 128 * 2 == 4_212_736
+    # the appended token: K and V rows (4 x 128 x 2 B each) and its raw index key (128 x 2 B)
+    assert w["append_bytes"] == 2_304
+    assert w["score_flops"] == 2 * 64 * 128 * 8192
+    assert w["attn_flops"] == 4 * 32 * 128 * 2049
+    # a step of 32 rows at that prefix
+    step = 32 * (w["score_bytes"] + w["attn_bytes"] + w["append_bytes"])
+    assert step == 202_522_624
+
+
+def test_mx_planes_count_their_own_key_bytes(sh):
+    assert bench.key_bytes(sh, "bf16") == 256
+    assert bench.key_bytes(sh, "mxfp8") == 128 + 4      # E4M3 elements + one scale byte per 32
+    assert bench.key_bytes(sh, "mxfp4") == 64 + 4       # E2M1 pairs + one scale byte per 32
+    for fmt, kb in (("mxfp8", 132), ("mxfp4", 68)):
+        w = bench.row_work(sh, 32769, fmt)
+        assert w["score_bytes"] == 8192 * kb + 16_384 + 256
+        assert w["attn_bytes"] == bench.row_work(sh, 32769)["attn_bytes"]
+
+
+def test_rows_at_the_inert_bound_score_nothing(sh):
+    # up to budget + ratio - 1 = 2051 visible tokens every block is selected: no scoring
+    w = bench.row_work(sh, 2051)
+    assert w["score_bytes"] == 0 and w["score_flops"] == 0 and w["n_tok"] == 2051
+    w = bench.row_work(sh, 2052)   # one block past it: 513 blocks scored, 512 kept, no tail
+    assert w["score_bytes"] == 513 * 256 + 16_384 + 256 and w["n_tok"] == 2048
+    tot = bench.sum_work(sh, [2051, 2052])
+    assert tot["n_tok"] == 2051 + 2048
