@@ -47,3 +47,28 @@ def test_rows_at_the_inert_bound_score_nothing(sh):
     assert w["score_bytes"] == 513 * 256 + 16_384 + 256 and w["n_tok"] == 2048
     tot = bench.sum_work(sh, [2051, 2052])
     assert tot["n_tok"] == 2051 + 2048
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the CPU oracle arm) on a tiny run: one JSON
+    line with the contract's keys; a rank other than 0 prints nothing."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "4", "--warmup", "3"]
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "rows/s"
+    assert d["value"] > 0 and d["steps"] == 4 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    env1 = dict(env, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    res1 = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env1)
+    assert res1.returncode == 0 and res1.stdout.strip() == ""
