@@ -72,3 +72,27 @@ def test_reference_arm_prints_one_contract_line():
     env1 = dict(env, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
     res1 = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env1)
     assert res1.returncode == 0 and res1.stdout.strip() == ""
+
+
+def test_clock_summary_keeps_the_timed_window_and_its_reasons():
+    """The clock record is parsed from nvidia-smi's CSV lines: only samples
+    inside the timed window count; a reason counts when it is Active there."""
+    from datetime import datetime
+    cs = bench.ClockSampler.__new__(bench.ClockSampler)   # no nvidia-smi process
+    cs.proc = None
+    t0 = datetime(2026, 1, 5, 12, 0, 0).timestamp()
+
+    def line(dt, sm, reasons=("Not Active",) * 4):
+        ts = datetime.fromtimestamp(t0 + dt).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{ts}, 0, {sm}, 2070, 905.25, 0x0000000000000004, " + ", ".join(reasons)
+    cs.lines = [line(-1.0, 800, ("Active",) * 4),                          # before the window
+                line(0.1, 2070), line(0.2, 2055),
+                line(0.3, 2070, ("Not Active", "Not Active", "Not Active", "Active")),
+                line(5.0, 600, ("Active",) * 4)]                            # after it
+    s = cs.summary(t0, t0 + 1.0)
+    assert s["samples"] == 3 and s["sm_mhz"] == 2070 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"]
+    cs.lines = [line(0.5, 1900, ("Not Active", "Active", "Not Active", "Not Active"))]
+    assert cs.summary(t0, t0 + 1.0)["reasons"] == ["hw_thermal_slowdown"]
+    cs.lines = ["garbage", line(3.0, 2000)]
+    assert cs.summary(t0, t0 + 1.0)["samples"] == 0
