@@ -247,6 +247,31 @@ class MropeBlocksAtLastToken(O.SeqState):
         return self.rope_pos((b + 1) * self.ratio - 1, self.pre.mrope_section)
 
 
+def _rope_with(pairs, freq_exp, sin_sign, name):
+    def rope(x, pos, rotary_dim, theta, section=None):
+        x = np.array(x, np.float64)
+        if rotary_dim == 0:
+            return x
+        half = rotary_dim // 2
+        i = np.arange(half, dtype=np.float64)
+        ang = O.pair_positions(pos, rotary_dim, section) * theta ** (-freq_exp * i / rotary_dim)
+        c, sn = np.cos(ang), sin_sign * np.sin(ang)
+        a_idx, b_idx = pairs(half)
+        x1, x2 = x[..., a_idx].copy(), x[..., b_idx].copy()
+        x[..., a_idx] = x1 * c - x2 * sn
+        x[..., b_idx] = x2 * c + x1 * sn
+        return x
+    rope.__name__ = name
+    return rope
+
+
+_neox = lambda h: (np.arange(h), np.arange(h) + h)
+_gptj = lambda h: (2 * np.arange(h), 2 * np.arange(h) + 1)
+rope_sine_flipped = _rope_with(_neox, 2.0, -1.0, "rope_sine_flipped")
+rope_gptj_pairs = _rope_with(_gptj, 2.0, 1.0, "rope_gptj_pairs")
+rope_freq_exponent_halved = _rope_with(_neox, 1.0, 1.0, "rope_freq_exponent_halved")
+
+
 MUTATIONS = [
     ("block_scores", no_relu, [P.test_score_closed_forms]),
     ("block_scores", relu_outside, [P.test_score_closed_forms]),
@@ -279,6 +304,9 @@ MUTATIONS = [
     ("pair_positions", mrope_temporal_only, [P.test_mrope_pairs_follow_the_interleave_and_its_section_bounds,
                                              P.test_mrope_is_plain_rope_for_text_and_sees_only_per_axis_offsets]),
     ("SeqState", MropeBlocksAtLastToken, [P.test_mrope_blocks_rope_at_their_first_tokens_triple]),
+    ("rope_neox", rope_sine_flipped, [P.test_rope_neox_closed_forms]),
+    ("rope_neox", rope_gptj_pairs, [P.test_rope_neox_closed_forms]),
+    ("rope_neox", rope_freq_exponent_halved, [P.test_rope_neox_closed_forms]),
     ("sigmoid", sigmoid_of_minus, [P.test_sigmoid_closed_forms, P.test_attention_qk_norm_rope_and_gate_hand_worked]),
 ]
 
