@@ -272,6 +272,38 @@ rope_gptj_pairs = _rope_with(_gptj, 2.0, 1.0, "rope_gptj_pairs")
 rope_freq_exponent_halved = _rope_with(_neox, 1.0, 1.0, "rope_freq_exponent_halved")
 
 
+def bf16_ties_away(x):
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    m, e = np.frexp(np.where(np.isfinite(a) & (a > 0), a, 1.0))
+    quantum = np.ldexp(1.0, np.maximum(e - 1, -126) - 7)
+    r = np.where(a > 0, np.floor(a / quantum + 0.5) * quantum, 0.0)
+    r = np.where(r >= 2.0 ** 128, np.inf, r)
+    out = np.copysign(np.where(np.isfinite(a), r, np.inf), x)
+    bits = (out.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    return np.where(np.isnan(x), np.uint16(0x7FC0), bits).astype(np.uint16)
+
+
+def select_one_short(scores, topk):
+    s = np.asarray(scores, np.float64); n = s.shape[0]
+    if n <= topk:
+        return np.arange(n, dtype=np.int64)
+    return np.sort(np.lexsort((np.arange(n), -s))[:topk - 1])
+
+
+def e4m3_unclamped(v):
+    v = np.asarray(v, np.float64)
+    a = np.abs(v)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))
+    quantum = np.ldexp(1.0, np.maximum(e - 1, -6) - 3)
+    return np.copysign(np.where(a > 0, np.rint(a / quantum) * quantum, 0.0), v)
+
+
+def scores_ignore_weights(q_idx_bits, w, blk_bits):
+    q = O.bf16_bits_to_f64(q_idx_bits); k = O.bf16_bits_to_f64(blk_bits)
+    return np.ones(len(np.asarray(w))) @ np.maximum(q @ k.T, 0.0)
+
+
 MUTATIONS = [
     ("block_scores", no_relu, [P.test_score_closed_forms]),
     ("block_scores", relu_outside, [P.test_score_closed_forms]),
@@ -307,6 +339,12 @@ MUTATIONS = [
     ("rope_neox", rope_sine_flipped, [P.test_rope_neox_closed_forms]),
     ("rope_neox", rope_gptj_pairs, [P.test_rope_neox_closed_forms]),
     ("rope_neox", rope_freq_exponent_halved, [P.test_rope_neox_closed_forms]),
+    ("f64_to_bf16_bits", bf16_ties_away, [P.test_bf16_rounding_hand_cases,
+                                          P.test_bf16_rounding_matches_torch_on_fp32_values]),
+    ("select_blocks", select_one_short, [P.test_selection_brute_force_with_ties]),
+    ("e4m3_round", e4m3_unclamped, [P.test_e4m3_rounding_is_nearest_even_by_brute_force,
+                                    P.test_e4m3_rounding_matches_torch_float8]),
+    ("block_scores", scores_ignore_weights, [P.test_score_invariants, P.test_score_closed_forms]),
     ("sigmoid", sigmoid_of_minus, [P.test_sigmoid_closed_forms, P.test_attention_qk_norm_rope_and_gate_hand_worked]),
 ]
 
