@@ -19,15 +19,17 @@
 //     in by TMA (cp.async.bulk.tensor, 128B swizzle), one box per 64 dims.
 //   * One thread issues d_I/16 tcgen05.mma (kind::f16, bf16 in, fp32 accumulate
 //     in TMEM) and commits them to an mbarrier.
-//   * With the MXFP8 plane (E4M3 elements and E8M0 scales per 32 values, pages
-//     of bpp * (d_I + d_I/32) bytes), the producers copy those pages into a
-//     byte ring, and 8 converter warps rebuild each tile as bf16 straight into
-//     tensor memory (a thread per half block row, one tcgen05.st; every MXFP8
-//     value is exact in bf16); the MMA reads that A operand from TMEM, the
-//     epilogue is the bf16 one. The HBM stream is 132 bytes per block instead
-//     of 256, and shared memory holds only copies, so the ring runs deep. The
-//     converter warps also MXFP8-round each group's query tile in place (the
-//     MMA waits for that), so the queries load as early as in the bf16 path.
+//   * With an MX plane -- MXFP8 (E4M3 elements, pages of bpp * (d_I + d_I/32)
+//     bytes) or MXFP4 (E2M1 pairs, bpp * (d_I/2 + d_I/32) bytes), E8M0 scales
+//     per 32 values -- two producers copy those pages into two byte rings, and
+//     8 converter warps rebuild each tile as bf16 straight into tensor memory
+//     (a block row per thread, tcgen05.st; every MX value is exact in bf16);
+//     the MMA reads that A operand from TMEM, the epilogue is the bf16 one. The
+//     HBM stream is 132 or 68 bytes per block instead of 256, and shared memory
+//     holds only copies, so the rings run deep. The converter warps also round
+//     each group's query tile to the plane's format in place, in the value
+//     domain (the MMA waits for that), so the queries load as early as in the
+//     bf16 path.
 //   * 4 * G epilogue warps, one per (row of the group, TMEM lane quarter), read
 //     their 32 lanes with tcgen05.ld: the warp holds its row's head columns in
 //     registers, hands the TMEM buffer back at once, and reduces them with
@@ -501,7 +503,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       mbar_init(c_empty(s), 1);
     }
     if (FP8)
-      for (int s = 0; s < 2; ++s) mbar_init(q_ready(s), kConvWarps);  // the group's queries MXFP8-rounded
+      for (int s = 0; s < 2; ++s) mbar_init(q_ready(s), kConvWarps);  // the group's queries MX-rounded
     for (int s = 0; s < 2; ++s) {
       mbar_init(b_full(s), 1);
       mbar_init(b_empty(s), 1);
@@ -658,7 +660,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       if (lane == 0 && (w.left <= 0 || w.g != cur_g)) tc_commit(b_empty(bs));
     }
   } else if (FP8 && warp >= 2 + 4 * a.G) {
-    // ---------------- MXFP8 converters (warps 2 + 4G .. 2 + 4G + 7) ----------------
+    // ---------------- MX converters (warps 2 + 4G .. 2 + 4G + 7) ----------------
     // Converter warps 0-3 drain ring 0 (even tiles), 4-7 ring 1 (odd tiles).
     // Thread t of converter warp w rebuilds block row b = 32 (w % 4) + t of its
     // ring's tiles -- the TMEM lane quarter w % 4 is the one the warp may write --
@@ -678,7 +680,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     int cur_gq = -1, gq = -1;
     for (int k = 0; w.left > 0; ++k) {
       if (w.g != cur_gq) {
-        // a new group: its query tile (TMA, 128B swizzle) is MXFP8-rounded in
+        // a new group: its query tile (TMA, 128B swizzle) is MX-rounded in
         // place before the MMA may use it. Thread unit u = (row r, 32-value
         // block): the block's 4 chunks of 16 bytes sit at chunk positions
         // (c ^ (r % 8)) of the row's 128-byte line in half c / 8 of the slot.
