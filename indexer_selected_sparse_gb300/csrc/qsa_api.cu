@@ -39,7 +39,7 @@ int check_cfg(const qsa_config *c) {
   if (c->index_format != QSA_INDEX_BF16 && c->index_format != QSA_INDEX_MXFP8 && c->index_format != QSA_INDEX_MXFP4)
     return QSA_ERR_UNSUPPORTED;
   if (c->local_window < 0 || c->local_window > kMaxLocalWindow) return QSA_ERR_UNSUPPORTED;
-  // the MXFP8 plane is scored on the tensor-core path: 8 or more blocks per page
+  // an MX plane is scored on the tensor-core path: 8 or more blocks per page
   if (c->index_format != QSA_INDEX_BF16 && c->page_size / c->ratio < 8) return QSA_ERR_UNSUPPORTED;
   return QSA_OK;
 }
@@ -236,7 +236,7 @@ int decode_impl(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_att
   const WsLayout L = ws_layout(sh, n_rows, ld);
   // through the pre-indexer the step's index queries are prepared into the
   // workspace by the append kernel, and the score kernel reads them there (with
-  // the MXFP8 plane the score kernel rounds its query tiles itself)
+  // an MX plane the score kernel rounds its query tiles itself)
   const bool q_prep = pre != nullptr;
   const bool q_main = att && att->gamma_q;  // main queries normed + roped into the workspace
   const size_t idx_bytes = q_prep ? round_up(q_prep_bytes(sh, n_rows), 256) : 0;

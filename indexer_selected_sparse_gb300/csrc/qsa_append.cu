@@ -61,7 +61,7 @@ __device__ __forceinline__ void pre_index_lanes(float (&x)[D32], const float *__
   }
 }
 
-// ---- MXFP8 (OCP MX v1.0: E4M3 elements, one E8M0 scale per 32 values) ----
+// ---- MX planes (OCP MX v1.0: E4M3 or E2M1 elements, one E8M0 scale per 32 values) ----
 
 // One warp holding a d_I vector as lane L: dims L + 32m, so register m across
 // the warp is exactly MX block m. x must already be bf16 values. Returns each
@@ -117,7 +117,7 @@ __device__ __forceinline__ void prep_vector(const uint16_t *__restrict__ in, uin
 
 // The step's query vectors of sequence i, one warp per vector: first the index
 // query heads (pre.q_out set: RoPE(GemmaRMSNorm) with pre.gamma_q, then with the
-// MXFP8 plane the MXFP8 round trip), then the main query heads (att.q_out set:
+// MX plane that plane's round trip), then the main query heads (att.q_out set:
 // RoPE(GemmaRMSNorm) with att.gamma_q over D). Index vector v is row i*R + v / H_I
 // at position p0 + v / H_I; main vectors likewise with Hq. A CTA takes vectors
 // slot*8 + warp, striding by n_slots*8, so a decode step's heads spread over CTAs.
@@ -157,7 +157,7 @@ int q_prep_ctas(int heads, int n_seq, int R) {
 // One warp: the compressed key of block b. Raw keys are summed in position
 // order in fp32 (as in the plain pooling), then scaled by 1/r; through the
 // pre-indexer when pre.gamma_k is set; rounded to bf16; stored as bf16 tiles or,
-// with the MXFP8 plane, quantised into it.
+// with an MX plane, quantised into it.
 template <int D32>
 __device__ void pool_block_warp(const Shape &sh, const PreArgs &pre, int b, int i, int R, int p0,
                                 const int32_t *__restrict__ ptab, int num_pages,
@@ -353,7 +353,7 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
   const float inv_r = 1.0f / static_cast<float>(r);
   if (pre.gamma_k || sh.idx_fp8) {
     // one warp per block: mean-pool, (Gemma RMSNorm, RoPE at the block's first
-    // position), store as bf16 or into the MXFP8 plane
+    // position), store as bf16 or into the MX plane
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
     for (int bb = warp; bb < b_hi - b_lo; bb += n_warps) {
       const int b = b_lo + bb;
@@ -405,7 +405,7 @@ pre_index_q_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const __gr
   pdl_wait();  // positions
   pdl_trigger();
   const int i = blockIdx.x;
-  const int p0 = pos0 ? pos0[i] : 0;  // no positions: MXFP8 round trip only
+  const int p0 = pos0 ? pos0[i] : 0;  // no positions: MX round trip only
   prep_queries(sh, pre, AttnPrep{}, i, R, p0, blockIdx.y, gridDim.y);
 }
 

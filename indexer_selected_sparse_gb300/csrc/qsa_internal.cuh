@@ -83,7 +83,7 @@ struct CacheView {
   const uint16_t *k_pool;
   const uint16_t *v_pool;
   const uint16_t *idxraw_pool;
-  const void *idxblk_pool;  // bf16 tiles, or the MXFP8 byte plane
+  const void *idxblk_pool;  // bf16 tiles, or an MX byte plane
 };
 
 struct Shape {
@@ -141,7 +141,6 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
 }
 
-// x through MXFP8 and back, given its block's scale exponent e (exact in bf16).
 // x through MXFP8 and back at scale 2^e, in the value domain (FMA-pipe
 // arithmetic only): a = |x| / 2^e is below 512 by the scale rule; E4M3's
 // quantum is 2^(floor(log2 a) - 3) from 2^-6 up and 2^-9 below it (the

@@ -227,7 +227,7 @@ class PagedCache:
         self.v_pool = torch.zeros_like(self.k_pool)
         self.idxraw_pool = torch.zeros(num_pages, P, cfg.idx_dim, dtype=torch.bfloat16, device=device)
         # block keys: P/ratio rows of idx_dim per page, stored tiled (see qsa.h); with the
-        # MXFP8 index format a byte plane of qsa_idxblk_page_bytes() per page
+        # MXFP8 / MXFP4 index formats a byte plane of qsa_idxblk_page_bytes() per page
         if cfg.index_format in (QSA_INDEX_MXFP8, QSA_INDEX_MXFP4):
             self.idxblk_pool = torch.zeros(num_pages, qsa_idxblk_page_bytes(cfg), dtype=torch.uint8, device=device)
         else:
@@ -466,7 +466,8 @@ def qsa_idxblk_page_bytes(cfg: Config) -> int:
 
 
 def qsa_quantize_index_q(cfg: Config, q_idx, q_out, stream=None) -> None:
-    """MXFP8 round trip of index query heads [rows, H_I, d_I] (bf16 in and out)."""
+    """MX round trip of index query heads [rows, H_I, d_I] (bf16 in and out): MXFP4 for an
+    MXFP4 configuration, else MXFP8."""
     n_rows = q_idx.numel() // (cfg.n_idx_heads * cfg.idx_dim)
     if q_out.numel() != q_idx.numel():
         raise ValueError("q_out must match q_idx")
