@@ -96,3 +96,17 @@ def test_clock_summary_keeps_the_timed_window_and_its_reasons():
     assert cs.summary(t0, t0 + 1.0)["reasons"] == ["hw_thermal_slowdown"]
     cs.lines = ["garbage", line(3.0, 2000)]
     assert cs.summary(t0, t0 + 1.0)["samples"] == 0
+
+
+def test_packed_step_inputs_are_aligned_disjoint_views():
+    import torch
+    ts = [torch.randn(3, 5).to(torch.bfloat16), torch.randn(7), torch.arange(10, dtype=torch.int32).view(2, 5),
+          torch.randn(32, 4, 128).to(torch.bfloat16)]
+    buf, views = bench.packed(torch, ts, "cpu")
+    assert buf.dtype == torch.uint8 and buf.numel() == 256 + 256 + 256 + 32 * 4 * 128 * 2
+    for v, t in zip(views, ts):
+        assert v.shape == t.shape and v.dtype == t.dtype and v.is_contiguous()
+        assert (v.data_ptr() - buf.data_ptr()) % 256 == 0       # the C ABI wants 16-byte aligned inputs
+        v.copy_(t)
+    for v, t in zip(views, ts):                                  # nothing overwrote another view
+        assert torch.equal(v, t)
