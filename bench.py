@@ -427,13 +427,12 @@ def run_gpu(args):
         if steps > 0:
             out[fmt] = run_mx(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, NB, B, hbm_gbs,
                               ms, fmt, steps)
+    late = None
     if args.attn_steps > 0:
-        try:
-            out["attn_options"] = run_attn_options(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream,
-                                                   NB, B, ms)
-        except Exception as e:  # this leg's failure is reported; the headline line still prints
-            out["attn_options"] = {"error": f"{type(e).__name__}: {e}"}
-    return out, rank, world
+        # run last of all GPU work (after the prefill leg), so that nothing else depends on it
+        def late():
+            return run_attn_options(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, NB, B, ms)
+    return out, rank, world, late
 
 
 def run_attn_options(args, Q, S, torch, wl, sh, pt, max_pages, start, batches, stream, NB, B, ms_plain):
@@ -1107,10 +1106,15 @@ def main():
         if int(os.environ.get("RANK", "0")) == 0:
             print(json.dumps({"prefill": pre}), flush=True)
         return
-    out, rank, world = run_gpu(args)
+    out, rank, world, late = run_gpu(args)
     if "prefill" in legs:
         import torch
         out["prefill"] = run_prefill(args, torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))))
+    if late is not None:
+        try:
+            out["attn_options"] = late()
+        except Exception as e:  # this leg's failure is reported; the headline line still prints
+            out["attn_options"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(args.oracle_rows)
