@@ -159,6 +159,12 @@ typedef struct qsa_rows {
                                serving in Atlas", (c) item 4: the ingested
                                counter froze at the capture step while the
                                sequence advanced) */
+  const int32_t *mrope_pos; /* optional device [n_seq * rows_per_seq][3] int32:
+                               each row's (t, h, w) position for interleaved
+                               MRoPE (row i * R + j is token pos0[i] + j),
+                               read only when a pre-indexer or attention
+                               option has an MRoPE section; NULL: every row is
+                               a text token, (p, p, p) */
 } qsa_rows;
 
 /* Paged cache of all sequences ([VA6], [VP5]). Logical token t of the
@@ -196,6 +202,12 @@ typedef struct qsa_cache {
   void *idxblk_pool;         /* device block keys (tiled, above): bf16 [num_pages, P/ratio * d_I],
                                 or with QSA_INDEX_MXFP8 bytes [num_pages, qsa_idxblk_page_bytes()] */
   int32_t *ingested;         /* device [n_slots]: tokens ingested per slot */
+  int32_t *blkpos_pool;      /* device [num_pages, P/ratio, 4] int32, 16-byte aligned:
+                                the (t, h, w) triple of each block's first token
+                                (4th value unused), written by appends through a
+                                pre-indexer with an MRoPE section and read when a
+                                later append completes the block; NULL when no
+                                MRoPE section is used */
 } qsa_cache;
 
 /* Message for a status code (static string). */
@@ -329,6 +341,15 @@ typedef struct qsa_pre_indexer {
   float eps;            /* >= 0 */
   float rope_theta;     /* > 0 */
   int rotary_dim;       /* 0 (no RoPE), 64, or d_I */
+  int mrope_section[3]; /* interleaved MRoPE ("Agentic shootout", "Flash-Next
+                           support: vLLM vs Atlas", (a) item 6 and its fused
+                           pre-indexer notes): (t, h, w) section sizes in
+                           rotary pairs, adding up to rotary_dim / 2; NeoX pair
+                           i turns by the row's h when i % 3 == 1 and
+                           i < 3 * h, by its w when i % 3 == 2 and i < 3 * w,
+                           by its t otherwise; a compressed key turns at its
+                           block's first token's triple (the cache's
+                           blkpos_pool keeps it). All zero: plain RoPE. */
 } qsa_pre_indexer;
 
 /* qsa_append whose completed blocks go through the pre-indexer:
@@ -381,6 +402,9 @@ typedef struct qsa_attn_options {
   float rope_theta;
   int rotary_dim;
   const qsa_bf16 *gate;
+  int mrope_section[3]; /* as in qsa_pre_indexer: q and k heads turn at their
+                           own row's (t, h, w) (qsa_rows.mrope_pos); all zero:
+                           plain RoPE */
 } qsa_attn_options;
 
 /* qsa_append / qsa_append_pre with optional index pre-indexer and main

@@ -153,16 +153,61 @@ size_t q_prep_bytes(const Shape &sh, int rows) {
 
 // Pre-indexer parameters: gains present where needed, eps >= 0, theta > 0,
 // rotary dims 0, 64 or d_I (whole NeoX pairs per warp lane).
+// An MRoPE section: all zero (plain RoPE), or three non-negative pair counts
+// adding up to rotary_dim / 2.
+bool mrope_on(const int sec[3]) { return sec[0] != 0 || sec[1] != 0 || sec[2] != 0; }
+
+int check_mrope(const int sec[3], int rotary_dim) {
+  if (!mrope_on(sec)) return QSA_OK;
+  if (sec[0] < 0 || sec[1] < 0 || sec[2] < 0 || rotary_dim == 0) return QSA_ERR_INVALID_ARG;
+  if (static_cast<long long>(sec[0]) + sec[1] + sec[2] != rotary_dim / 2) return QSA_ERR_INVALID_ARG;
+  return QSA_OK;
+}
+
+// The rows' triples (4-byte aligned when given) with an MRoPE section, and the
+// cache's block-position pool when keys are pooled through one.
+int check_mrope_buffers(const qsa_rows *rows, const qsa_cache *cache, bool on_q, bool on_blk) {
+  if ((on_q || on_blk) && rows && rows->mrope_pos && (reinterpret_cast<uintptr_t>(rows->mrope_pos) & 3))
+    return QSA_ERR_INVALID_ARG;
+  if (on_blk && (!cache || !cache->blkpos_pool || !aligned16(cache->blkpos_pool))) return QSA_ERR_INVALID_ARG;
+  return QSA_OK;
+}
+
+// The MRoPE buffers one call needs: the rows' triples when any of its RoPE
+// uses a section, the cache's block-position pool when it pools keys through a
+// pre-indexer with one.
+int check_mrope_call(const qsa_pre_indexer *pre, const qsa_attn_options *att, const qsa_rows *rows,
+                     const qsa_cache *cache) {
+  const bool pre_on = pre && mrope_on(pre->mrope_section);
+  const bool on_q = pre_on || (att && mrope_on(att->mrope_section));
+  const bool on_blk = cache && pre_on && pre->gamma_k;
+  return check_mrope_buffers(rows, cache, on_q, on_blk);
+}
+
+Mrope mrope_of(const int sec[3], const qsa_rows *rows) {
+  Mrope m;
+  m.on = mrope_on(sec);
+  if (m.on) {
+    m.sec_h = sec[1];
+    m.sec_w = sec[2];
+    m.pos = rows ? rows->mrope_pos : nullptr;
+  }
+  return m;
+}
+
 int check_pre(const qsa_config *c, const qsa_pre_indexer *p, bool need_q, bool need_k) {
   if (!p) return QSA_ERR_INVALID_ARG;
   if ((need_q && !p->gamma_q) || (need_k && !p->gamma_k)) return QSA_ERR_INVALID_ARG;
   if (!(p->eps >= 0.f) || !(p->rope_theta > 0.f) || p->eps > 1e30f || p->rope_theta > 1e30f)
     return QSA_ERR_INVALID_ARG;
   if (p->rotary_dim != 0 && p->rotary_dim != 64 && p->rotary_dim != c->idx_dim) return QSA_ERR_UNSUPPORTED;
-  return QSA_OK;
+  return check_mrope(p->mrope_section, p->rotary_dim);
 }
 
-PreArgs pre_args(const qsa_pre_indexer *p, const uint16_t *q_in, uint16_t *q_out) {
+// rows: the call's rows (their MRoPE triples); cache: where blocks are pooled
+// (its block-position pool), nullptr for query-only calls.
+PreArgs pre_args(const qsa_pre_indexer *p, const uint16_t *q_in, uint16_t *q_out, const qsa_rows *rows,
+                 const qsa_cache *cache) {
   PreArgs a;
   a.gamma_q = p->gamma_q;
   a.gamma_k = p->gamma_k;
@@ -173,6 +218,8 @@ PreArgs pre_args(const qsa_pre_indexer *p, const uint16_t *q_in, uint16_t *q_out
     a.half_turns[i] = std::pow(static_cast<double>(p->rope_theta), -2.0 * i / a.rot) / pi;
   a.q_in = q_in;
   a.q_out = q_out;
+  a.mr = mrope_of(p->mrope_section, rows);
+  if (a.mr.on && cache) a.blkpos = cache->blkpos_pool;
   return a;
 }
 
@@ -189,11 +236,12 @@ int check_attn(const qsa_attn_options *a) {
     return QSA_ERR_INVALID_ARG;
   if (a->rotary_dim != 0 && a->rotary_dim != 64 && a->rotary_dim != kHeadDim) return QSA_ERR_UNSUPPORTED;
   if (a->gate && !aligned16(a->gate)) return QSA_ERR_INVALID_ARG;
-  return QSA_OK;
+  return check_mrope(a->mrope_section, a->rotary_dim);
 }
 
-AttnPrep attn_prep(const qsa_attn_options *a, const uint16_t *q_in, uint16_t *q_out) {
+AttnPrep attn_prep(const qsa_attn_options *a, const uint16_t *q_in, uint16_t *q_out, const qsa_rows *rows) {
   AttnPrep p;
+  p.mr = mrope_of(a->mrope_section, rows);
   p.gamma_q = a->gamma_q;
   p.gamma_k = a->gamma_k;
   p.eps = a->eps;
@@ -222,6 +270,7 @@ int decode_impl(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_att
   if ((rc = check_rows(rows)) != QSA_OK) return rc;
   if ((rc = check_cache(cache, true, true)) != QSA_OK) return rc;
   if (!cache->ingested || !status) return QSA_ERR_INVALID_ARG;
+  if ((rc = check_mrope_call(pre, att, rows, cache)) != QSA_OK) return rc;
   const int n_rows = rows->n_seq * rows->rows_per_seq;
   if (n_rows == 0) return QSA_OK;
   if (!k_new || !v_new || !idx_k_new || !q_idx || !w || !q || !out || !ws)
@@ -252,11 +301,11 @@ int decode_impl(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_att
   const int R = rows->rows_per_seq;
 
   PreArgs pa;
-  if (pre) pa = pre_args(pre, q_idx, q_pre);
+  if (pre) pa = pre_args(pre, q_idx, q_pre, rows, cache);
   pa.q_in = q_prep ? q_idx : nullptr;
   pa.q_out = q_pre;
   AttnPrep ap;
-  if (att) ap = attn_prep(att, q_main ? q : nullptr, q_att);
+  if (att) ap = attn_prep(att, q_main ? q : nullptr, q_att, rows);
   cudaError_t e = launch_append(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cache->page_table,
                                 cache->max_pages, cache->num_pages, cache->k_pool, cache->v_pool,
                                 cache->idxraw_pool, cache->idxblk_pool, cache->ingested, k_new,
@@ -457,9 +506,10 @@ int qsa_append_pre(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_
   if (n_rows == 0) return QSA_OK;
   if (!k_new || !v_new || !idx_k_new || !aligned16(k_new) || !aligned16(v_new) || !aligned16(idx_k_new))
     return QSA_ERR_INVALID_ARG;
+  if ((rc = check_mrope_call(pre, nullptr, rows, cache)) != QSA_OK) return rc;
   if ((rc = host_capacity_check(rows, cache, cfg->page_size)) != QSA_OK) return rc;
   const Shape sh = make_shape(cfg);
-  const PreArgs pa = pre_args(pre, nullptr, nullptr);
+  const PreArgs pa = pre_args(pre, nullptr, nullptr, rows, cache);
   cudaError_t e = launch_append(sh, rows->n_seq, rows->rows_per_seq, rows->seq_ids, rows->pos0,
                                 cache->page_table, cache->max_pages, cache->num_pages,
                                 cache->k_pool, cache->v_pool, cache->idxraw_pool, cache->idxblk_pool,
@@ -479,9 +529,11 @@ int qsa_pre_index_q(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa
   if (static_cast<long long>(rows->n_seq) * rows->rows_per_seq == 0) return QSA_OK;
   if (!q_idx || !q_out) return QSA_ERR_INVALID_ARG;
   if (q_idx == q_out) return QSA_ERR_INVALID_ARG;  // not in place
+  if ((rc = check_mrope_call(pre, nullptr, rows, nullptr)) != QSA_OK) return rc;
   const Shape sh = make_shape(cfg);
   return cuda_status(launch_pre_index_q(sh, rows->n_seq, rows->rows_per_seq, rows->pos0,
-                                        pre_args(pre, nullptr, nullptr), q_idx, q_out, false, stream));
+                                        pre_args(pre, nullptr, nullptr, rows, nullptr), q_idx, q_out, false,
+                                        stream));
 }
 
 int qsa_decode_pre(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_rows *rows,
@@ -517,12 +569,13 @@ int qsa_append_ex(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_a
   if (n_rows == 0) return QSA_OK;
   if (!k_new || !v_new || !idx_k_new || !aligned16(k_new) || !aligned16(v_new) || !aligned16(idx_k_new))
     return QSA_ERR_INVALID_ARG;
+  if ((rc = check_mrope_call(pre, attn, rows, cache)) != QSA_OK) return rc;
   if ((rc = host_capacity_check(rows, cache, cfg->page_size)) != QSA_OK) return rc;
   const Shape sh = make_shape(cfg);
   PreArgs pa;
-  if (pre) pa = pre_args(pre, nullptr, nullptr);
+  if (pre) pa = pre_args(pre, nullptr, nullptr, rows, cache);
   AttnPrep ap;
-  if (attn) ap = attn_prep(attn, nullptr, nullptr);  // keys only
+  if (attn) ap = attn_prep(attn, nullptr, nullptr, rows);  // keys only
   cudaError_t e = launch_append(sh, rows->n_seq, rows->rows_per_seq, rows->seq_ids, rows->pos0,
                                 cache->page_table, cache->max_pages, cache->num_pages,
                                 cache->k_pool, cache->v_pool, cache->idxraw_pool, cache->idxblk_pool,

@@ -34,6 +34,22 @@ __device__ __forceinline__ float2 rope_cs(int pos, int i, const double *half_tur
   return make_float2(cs, sn);
 }
 
+// Interleaved MRoPE: the position NeoX pair ip of a token at (t, h, w) = tp
+// turns by: h when ip % 3 == 1 and ip < 3 * sec_h, w when ip % 3 == 2 and
+// ip < 3 * sec_w, else t. Plain RoPE is tp = (p, p, p).
+__device__ __forceinline__ int pair_pos(int3 tp, int ip, int sec_h, int sec_w) {
+  const int m = ip % 3;
+  return (m == 1 && ip < 3 * sec_h) ? tp.y : ((m == 2 && ip < 3 * sec_w) ? tp.z : tp.x);
+}
+
+// The triple of the call's row `row`, a token at position pos: from the call's
+// array with MRoPE on, else (pos, pos, pos) (a text token, or plain RoPE).
+__device__ __forceinline__ int3 row_triple(const Mrope &mr, size_t row, int pos) {
+  if (!mr.on || !mr.pos) return make_int3(pos, pos, pos);
+  const int32_t *p = mr.pos + row * 3;
+  return make_int3(p[0], p[1], p[2]);
+}
+
 // One warp, one d_I-vector held as lane L: dims L + 32m (m < D32). Gemma RMSNorm
 // (gain 1 + gamma, fp32 sum of squares in a fixed shuffle order), then the NeoX
 // rotation of pairs (i, i + rot/2), i < rot/2; with rot/2 a multiple of 32 a
@@ -81,17 +97,18 @@ __device__ __forceinline__ void mx_quantize_lanes(const float (&x)[D32], uint32_
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
 // One warp, one vector of 32 * D32 values at in[base] -> out[base]: RoPE(Gemma
-// RMSNorm) at pos when gamma is set, rounded to bf16, then the MX round trip
-// (mx: 1 MXFP8, 2 MXFP4, 0 none).
+// RMSNorm) at the triple tp when gamma is set, rounded to bf16, then the MX
+// round trip (mx: 1 MXFP8, 2 MXFP4, 0 none).
 template <int D32>
 __device__ __forceinline__ void prep_vector(const uint16_t *__restrict__ in, uint16_t *__restrict__ out,
-                                            size_t base, int pos, const float *gamma, float eps, int rot,
-                                            const double *half_turns, int mx, int lane) {
+                                            size_t base, int3 tp, const Mrope &mr, const float *gamma, float eps,
+                                            int rot, const double *half_turns, int mx, int lane) {
   float x[D32];
 #pragma unroll
   for (int m = 0; m < D32; ++m) x[m] = bf16_bits_to_float(in[base + lane + 32 * m]);
   if (gamma) {
-    pre_index_lanes<D32>(x, gamma, eps, rot, 32 * D32, lane, [&](int ip) { return rope_cs(pos, ip, half_turns); });
+    pre_index_lanes<D32>(x, gamma, eps, rot, 32 * D32, lane,
+                         [&](int ip) { return rope_cs(pair_pos(tp, ip, mr.sec_h, mr.sec_w), ip, half_turns); });
 #pragma unroll
     for (int m = 0; m < D32; ++m) x[m] = round_bf16(x[m]);
   }
@@ -131,16 +148,20 @@ __device__ void prep_queries(const Shape &sh, const PreArgs &pre, const AttnPrep
       const int t = v / sh.h_idx;
       const size_t base = (static_cast<size_t>(i) * R * sh.h_idx + v) * sh.d_idx;
       const int mx = sh.idx_fp8 ? (sh.idx_fp4 ? 2 : 1) : 0;
+      const int3 tp = row_triple(pre.mr, static_cast<size_t>(i) * R + t, p0 + t);
       if (sh.d_idx == 128)
-        prep_vector<4>(pre.q_in, pre.q_out, base, p0 + t, pre.gamma_q, pre.eps, pre.rot, pre.half_turns, mx, lane);
+        prep_vector<4>(pre.q_in, pre.q_out, base, tp, pre.mr, pre.gamma_q, pre.eps, pre.rot, pre.half_turns, mx,
+                       lane);
       else
-        prep_vector<2>(pre.q_in, pre.q_out, base, p0 + t, pre.gamma_q, pre.eps, pre.rot, pre.half_turns, mx, lane);
+        prep_vector<2>(pre.q_in, pre.q_out, base, tp, pre.mr, pre.gamma_q, pre.eps, pre.rot, pre.half_turns, mx,
+                       lane);
     } else {
       const int vm = v - n_idx;
       const int t = vm / sh.hq;
       const size_t base = (static_cast<size_t>(i) * R * sh.hq + vm) * kHeadDim;
-      prep_vector<kHeadDim / 32>(att.q_in, att.q_out, base, p0 + t, att.gamma_q, att.eps, att.rot, att.half_turns,
-                                 0, lane);
+      const int3 tp = row_triple(att.mr, static_cast<size_t>(i) * R + t, p0 + t);
+      prep_vector<kHeadDim / 32>(att.q_in, att.q_out, base, tp, att.mr, att.gamma_q, att.eps, att.rot,
+                                 att.half_turns, 0, lane);
     }
   }
 }
@@ -192,10 +213,23 @@ __device__ void pool_block_warp(const Shape &sh, const PreArgs &pre, int b, int 
 #pragma unroll
   for (int m = 0; m < D32; ++m) x[m] *= inv_r;
   const int first = b * r;
-  if (pre.gamma_k)
-    pre_index_lanes<D32>(x, pre.gamma_k, pre.eps, pre.rot, sh.d_idx, lane,
-                         [&](int ip) { return rope_cs(first, ip, pre.half_turns); });
   const int rr = b & (bpp - 1);
+  if (pre.gamma_k) {
+    // RoPE at the block's first token: its triple comes with this call's rows,
+    // or was stored beside the page when an earlier call appended it
+    int3 tp = make_int3(first, first, first);
+    if (pre.mr.on) {
+      if (first >= p0) {
+        tp = row_triple(pre.mr, static_cast<size_t>(i) * R + (first - p0), first);
+      } else if (pre.blkpos) {  // the host requires the pool with an MRoPE section
+        const int4 q = reinterpret_cast<const int4 *>(pre.blkpos)[static_cast<size_t>(page_b) * bpp + rr];
+        tp = make_int3(q.x, q.y, q.z);
+      }
+    }
+    pre_index_lanes<D32>(x, pre.gamma_k, pre.eps, pre.rot, sh.d_idx, lane, [&](int ip) {
+      return rope_cs(pair_pos(tp, ip, pre.mr.sec_h, pre.mr.sec_w), ip, pre.half_turns);
+    });
+  }
   if (sh.idx_fp4) {
 #pragma unroll
     for (int m = 0; m < D32; ++m) x[m] = round_bf16(x[m]);
@@ -312,9 +346,23 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
     }
     *dst = __ldg(src);
   }
+  if (pre.mr.on && pre.blkpos) {
+    // the triple of every block's first token, beside its page, for the call
+    // that completes the block (it may come later)
+    const int bpp = P >> sh.log2_ratio;
+    for (int j = t_begin + threadIdx.x; j < t_end; j += blockDim.x) {
+      const int pos = p0 + j;
+      if (pos & (sh.ratio - 1)) continue;
+      const int page = ptab[pos >> sh.log2_page];
+      if (page < 0 || page >= num_pages) continue;  // reported by the copy above
+      const int3 tp = row_triple(pre.mr, static_cast<size_t>(i) * R + j, pos);
+      reinterpret_cast<int4 *>(pre.blkpos)[static_cast<size_t>(page) * bpp + ((pos & (P - 1)) >> sh.log2_ratio)] =
+          make_int4(tp.x, tp.y, tp.z, 0);
+    }
+  }
 
-  // 1b. key heads through GemmaRMSNorm + RoPE at the token's position, one warp
-  // per (token, KV head)
+  // 1b. key heads through GemmaRMSNorm + RoPE at the token's position (its
+  // triple with MRoPE), one warp per (token, KV head)
   if (att.gamma_k) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
     for (int v = warp; v < (t_end - t_begin) * sh.hkv; v += n_warps) {
@@ -330,8 +378,10 @@ append_kernel(Shape sh, int R, const int32_t *__restrict__ seq_ids,
       float x[kHeadDim / 32];
 #pragma unroll
       for (int m = 0; m < kHeadDim / 32; ++m) x[m] = bf16_bits_to_float(k_new[src + lane + 32 * m]);
-      pre_index_lanes<kHeadDim / 32>(x, att.gamma_k, att.eps, att.rot, kHeadDim, lane,
-                                     [&](int ip) { return rope_cs(pos, ip, att.half_turns); });
+      const int3 tp = row_triple(att.mr, static_cast<size_t>(i) * R + j, pos);
+      pre_index_lanes<kHeadDim / 32>(x, att.gamma_k, att.eps, att.rot, kHeadDim, lane, [&](int ip) {
+        return rope_cs(pair_pos(tp, ip, att.mr.sec_h, att.mr.sec_w), ip, att.half_turns);
+      });
       uint16_t *dst = k_pool + ((static_cast<size_t>(page) * P + (pos & (P - 1))) * sh.hkv + h) * kHeadDim;
 #pragma unroll
       for (int m = 0; m < kHeadDim / 32; ++m) {

@@ -48,6 +48,16 @@ __host__ __device__ __forceinline__ int blk_elem_offset(int rr, int d, int bpp, 
 // Kernels take the block as a __grid_constant__ parameter, so indexing the
 // table reads the parameter bank directly.
 constexpr int kMaxHalfRot = 64;  // rotary pairs of a head, at most (d_I = 128)
+// Interleaved MRoPE (same report, the fused pre-indexer notes: temporal,
+// height and width rotary pairs interleave by pair index modulo 3, bounded by
+// the height and width sections). A token's position is a triple (t, h, w);
+// plain RoPE is the case sec_h = sec_w = 0 with t = the token's position.
+struct Mrope {
+  bool on = false;               // position triples in use (a section was given)
+  int sec_h = 0, sec_w = 0;      // pairs of the height and width sections
+  const int32_t *pos = nullptr;  // device [rows][3]: the call's (t, h, w) per row; nullptr: (p, p, p)
+};
+
 struct PreArgs {
   const float *gamma_q = nullptr;
   const float *gamma_k = nullptr;
@@ -55,6 +65,8 @@ struct PreArgs {
   int rot = 0;  // rotary dims: 0, 64 or d_I
   const uint16_t *q_in = nullptr;
   uint16_t *q_out = nullptr;
+  Mrope mr;
+  int32_t *blkpos = nullptr;  // device [num_pages][P/ratio][4]: (t, h, w) of each block's first token
   double half_turns[kMaxHalfRot] = {};
 };
 
@@ -71,6 +83,7 @@ struct AttnPrep {
   int rot = 0;
   const uint16_t *q_in = nullptr;
   uint16_t *q_out = nullptr;
+  Mrope mr;
   double half_turns[kMaxHalfRot] = {};
 };
 

@@ -65,20 +65,24 @@ class qsa_config(ctypes.Structure):
                 ("local_window", ctypes.c_int)]
 
 
+_SEC3 = ctypes.c_int * 3
+
+
 class qsa_pre_indexer(ctypes.Structure):
     _fields_ = [("gamma_q", ctypes.c_void_p), ("gamma_k", ctypes.c_void_p), ("eps", ctypes.c_float),
-                ("rope_theta", ctypes.c_float), ("rotary_dim", ctypes.c_int)]
+                ("rope_theta", ctypes.c_float), ("rotary_dim", ctypes.c_int), ("mrope_section", _SEC3)]
 
 
 class qsa_attn_options(ctypes.Structure):
     _fields_ = [("gamma_q", ctypes.c_void_p), ("gamma_k", ctypes.c_void_p), ("eps", ctypes.c_float),
-                ("rope_theta", ctypes.c_float), ("rotary_dim", ctypes.c_int), ("gate", ctypes.c_void_p)]
+                ("rope_theta", ctypes.c_float), ("rotary_dim", ctypes.c_int), ("gate", ctypes.c_void_p),
+                ("mrope_section", _SEC3)]
 
 
 class qsa_rows(ctypes.Structure):
     _fields_ = [("n_seq", ctypes.c_int), ("rows_per_seq", ctypes.c_int),
                 ("seq_ids", ctypes.c_void_p), ("pos0", ctypes.c_void_p),
-                ("pos0_host", ctypes.c_void_p), ("advance", ctypes.c_int)]
+                ("pos0_host", ctypes.c_void_p), ("advance", ctypes.c_int), ("mrope_pos", ctypes.c_void_p)]
 
 
 class qsa_cache(ctypes.Structure):
@@ -86,7 +90,11 @@ class qsa_cache(ctypes.Structure):
                 ("max_pages", ctypes.c_int), ("num_pages", ctypes.c_int),
                 ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
                 ("idxraw_pool", ctypes.c_void_p), ("idxblk_pool", ctypes.c_void_p),
-                ("ingested", ctypes.c_void_p)]
+                ("ingested", ctypes.c_void_p), ("blkpos_pool", ctypes.c_void_p)]
+
+
+def _section(sec) -> "_SEC3":
+    return _SEC3(*(0, 0, 0) if sec is None else tuple(int(v) for v in sec))
 
 
 _P = ctypes.c_void_p
@@ -217,7 +225,8 @@ class PagedCache:
 
     page_table: [n_slots, max_pages] int32 (host or device; copied to device)."""
 
-    def __init__(self, cfg: Config, page_table: torch.Tensor, num_pages: int, device="cuda"):
+    def __init__(self, cfg: Config, page_table: torch.Tensor, num_pages: int, device="cuda",
+                 mrope: bool = False):
         self.cfg = cfg
         P = cfg.page_size
         self.page_table = page_table.to(device=device, dtype=torch.int32).contiguous()
@@ -234,6 +243,9 @@ class PagedCache:
             self.idxblk_pool = torch.zeros(num_pages, (P // cfg.ratio) * cfg.idx_dim, dtype=torch.bfloat16,
                                            device=device)
         self.ingested = torch.zeros(self.n_slots, dtype=torch.int32, device=device)
+        # mrope: the (t, h, w) of each block's first token, for a pre-indexer with an MRoPE section
+        self.blkpos_pool = (torch.zeros(num_pages, P // cfg.ratio, 4, dtype=torch.int32, device=device)
+                            if mrope else None)
 
     @property
     def capacity(self) -> int:
@@ -246,15 +258,19 @@ class PagedCache:
     def c(self) -> qsa_cache:
         return qsa_cache(_ptr(self.page_table), self.n_slots, self.max_pages, self.num_pages,
                          _ptr(self.k_pool), _ptr(self.v_pool), _ptr(self.idxraw_pool),
-                         _ptr(self.idxblk_pool), _ptr(self.ingested))
+                         _ptr(self.idxblk_pool), _ptr(self.ingested),
+                         None if self.blkpos_pool is None else _ptr(self.blkpos_pool))
 
 
 class Rows:
     """Row layout of a step: n_seq sequences x R rows, sequence-major."""
 
     def __init__(self, seq_ids: torch.Tensor, pos0: torch.Tensor, rows_per_seq: int,
-                 pos0_host: Optional[torch.Tensor] = None, advance: bool = False):
+                 pos0_host: Optional[torch.Tensor] = None, advance: bool = False,
+                 mrope_pos: Optional[torch.Tensor] = None):
         self.seq_ids = seq_ids.to(torch.int32).contiguous()
+        # [n_seq * R, 3] device int32: each row's (t, h, w) for MRoPE (None: text rows)
+        self.mrope_pos = None if mrope_pos is None else mrope_pos.to(torch.int32).contiguous()
         self.pos0 = pos0 if (pos0.dtype == torch.int32 and pos0.is_contiguous()) else pos0.to(torch.int32).contiguous()
         self.R = rows_per_seq
         self.pos0_host = None if pos0_host is None else pos0_host.to(torch.int32).cpu().contiguous()
@@ -270,7 +286,8 @@ class Rows:
 
     def c(self) -> qsa_rows:
         return qsa_rows(self.n_seq, self.R, _ptr(self.seq_ids), _ptr(self.pos0),
-                        None if self.pos0_host is None else _ptr(self.pos0_host), int(self.advance))
+                        None if self.pos0_host is None else _ptr(self.pos0_host), int(self.advance),
+                        None if self.mrope_pos is None else _ptr(self.mrope_pos))
 
 
 # ---------------------------------------------------------------------------
@@ -384,14 +401,15 @@ class PreIndexer:
     norm multiplies by 1 + gain), epsilon, RoPE base and rotary dims."""
 
     def __init__(self, gamma_q: torch.Tensor, gamma_k: torch.Tensor, eps: float, rope_theta: float,
-                 rotary_dim: int):
+                 rotary_dim: int, mrope_section=None):
         self.gamma_q = gamma_q.to(torch.float32).contiguous()
         self.gamma_k = gamma_k.to(torch.float32).contiguous()
         self.eps, self.rope_theta, self.rotary_dim = float(eps), float(rope_theta), int(rotary_dim)
+        self.mrope_section = mrope_section  # (t, h, w) pairs, or None: plain RoPE
 
     def c(self) -> qsa_pre_indexer:
         return qsa_pre_indexer(_ptr(self.gamma_q), _ptr(self.gamma_k), self.eps, self.rope_theta,
-                               self.rotary_dim)
+                               self.rotary_dim, _section(self.mrope_section))
 
 
 def qsa_append_pre(cfg: Config, pre: PreIndexer, rows: Rows, cache: PagedCache, k_new, v_new, idx_k_new,
@@ -414,15 +432,16 @@ class AttnOptions:
     dims, and an optional sigmoid output gate (device bf16 [rows, Hq, D])."""
 
     def __init__(self, gamma_q=None, gamma_k=None, eps: float = 1e-6, rope_theta: float = 1e4,
-                 rotary_dim: int = 64, gate=None):
+                 rotary_dim: int = 64, gate=None, mrope_section=None):
         self.gamma_q = None if gamma_q is None else gamma_q.to(torch.float32).contiguous()
         self.gamma_k = None if gamma_k is None else gamma_k.to(torch.float32).contiguous()
         self.eps, self.rope_theta, self.rotary_dim = float(eps), float(rope_theta), int(rotary_dim)
         self.gate = gate
+        self.mrope_section = mrope_section  # (t, h, w) pairs, or None: plain RoPE
 
     def c(self) -> qsa_attn_options:
         return qsa_attn_options(_ptr(self.gamma_q), _ptr(self.gamma_k), self.eps, self.rope_theta,
-                                self.rotary_dim, _ptr(self.gate, torch.bfloat16))
+                                self.rotary_dim, _ptr(self.gate, torch.bfloat16), _section(self.mrope_section))
 
 
 def _ref(x):

@@ -294,3 +294,26 @@ def reject_counts(seed: int, n_seq: int, max_reject: int = 2) -> List[int]:
     """Per-sequence number of rejected verify rows, uniform in {0..max_reject}."""
     b = token_base(seed, STREAM_REJECT, 0, 0, torch.arange(n_seq, dtype=torch.int64))
     return (b % (max_reject + 1)).tolist()
+
+
+def mrope_positions(n: int, img_start: int, grid_h: int, grid_w: int) -> torch.Tensor:
+    """(t, h, w) positions [n, 3] int32 of a multimodal sequence: text tokens
+    (p, p, p) before img_start; then an image of grid_h x grid_w patches in
+    row-major order at one temporal step (t = img_start, h = img_start + row,
+    w = img_start + column); then text again, its positions continuing from
+    img_start + max(grid_h, grid_w)."""
+    p = torch.arange(n, dtype=torch.int64)
+    out = torch.stack([p, p, p], dim=1)
+    n_img = grid_h * grid_w
+    k = torch.arange(n_img, dtype=torch.int64)
+    img = slice(img_start, min(n, img_start + n_img))
+    m = img.stop - img.start
+    if m > 0:
+        out[img, 0] = img_start
+        out[img, 1] = img_start + k[:m] // grid_w
+        out[img, 2] = img_start + k[:m] % grid_w
+    after = img_start + n_img
+    if after < n:
+        q = torch.arange(after, n, dtype=torch.int64) - after + img_start + max(grid_h, grid_w)
+        out[after:] = torch.stack([q, q, q], dim=1)
+    return out.to(torch.int32)

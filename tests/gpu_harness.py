@@ -100,7 +100,7 @@ class GpuState:
 
     def __init__(self, wl: S.Workload, extra_tokens: int = 64, contiguous: Optional[bool] = None,
                  page_seed: Optional[int] = None, device: str = "cuda", slots: Optional[List[int]] = None,
-                 index_format: int = 0, local_window: int = 0):
+                 index_format: int = 0, local_window: int = 0, mrope: bool = False):
         from indexer_selected_sparse_gb300 import qsa as Q
         self.Q = Q
         self.wl = wl
@@ -115,7 +115,7 @@ class GpuState:
         n_slots = max(self.slots) + 1
         contiguous = wl.contiguous_pages if contiguous is None else contiguous
         pt = S.page_table(wl.seed if page_seed is None else page_seed, n_slots, self.max_pages, contiguous)
-        self.cache = Q.PagedCache(self.cfg, pt, n_slots * self.max_pages, device=device)
+        self.cache = Q.PagedCache(self.cfg, pt, n_slots * self.max_pages, device=device, mrope=mrope)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.hist: Dict[int, History] = {s: History() for s in self.slots}
         for s in self.slots:

@@ -214,3 +214,44 @@ def test_attention_options_checked_on_host(Q):
     # without a query norm (gate and key options only) the bar is the plain size: one byte less is refused
     # (a size that passes would go on to launch kernels, which these fake pointers must never reach)
     assert decode(Q.qsa_attn_options(None, 16, 1e-6, 1e4, 64, 16), plain - 1) == Q.QSA_ERR_WORKSPACE
+
+
+def test_mrope_arguments_checked_on_host(Q):
+    cfg = Q.Config(4, 2048, 64, 128, 32, 4)
+    c = ctypes.byref(cfg.c())
+    lib = Q.LIB
+    # rows at 250 + 7 > 256 tokens: a call that passes every MRoPE check stops at the host capacity
+    # check (QSA_ERR_CAPACITY), so none of these fake pointers ever reaches a kernel
+    pos = (ctypes.c_int32 * 1)(250)
+    over = ctypes.cast(pos, ctypes.c_void_p)
+    rows = Q.qsa_rows(1, 7, 16, 16, over, 0, None)
+    rows_mis = Q.qsa_rows(1, 7, 16, 16, over, 0, 18)            # triples not 4-byte aligned
+    no_pool = Q.qsa_cache(16, 1, 4, 4, 16, 16, 16, 16, 16)       # 4 pages x 64 tokens
+    pool = Q.qsa_cache(16, 1, 4, 4, 16, 16, 16, 16, 16, 16)      # with a block-position pool
+
+    def pre(sec, rot=64):
+        return Q.qsa_pre_indexer(16, 16, 1e-6, 1e4, rot, Q._SEC3(*sec))
+
+    def append(p, r, cache):
+        return lib.qsa_append_pre(c, ctypes.byref(p), ctypes.byref(r), ctypes.byref(cache), 16, 16, 16, 16, None)
+
+    # a section is three non-negative pair counts adding up to rotary_dim / 2
+    for sec, rot in (((11, 11, 11), 64), ((-1, 17, 16), 64), ((11, 11, 10), 0), ((22, 22, 20), 64)):
+        assert append(pre(sec, rot), rows, pool) == Q.QSA_ERR_INVALID_ARG, sec
+    # keys pooled at stored triples need the cache's block-position pool; triples are int32-aligned
+    assert append(pre((11, 11, 10)), rows, no_pool) == Q.QSA_ERR_INVALID_ARG
+    assert append(pre((11, 11, 10)), rows_mis, pool) == Q.QSA_ERR_INVALID_ARG
+    assert append(pre((11, 11, 10)), rows, pool) == Q.QSA_ERR_CAPACITY          # every MRoPE check passed
+    assert append(pre((0, 0, 0)), rows, no_pool) == Q.QSA_ERR_CAPACITY          # plain RoPE needs no pool
+    assert append(pre((32, 0, 0), 64), rows, pool) == Q.QSA_ERR_CAPACITY       # temporal only is a section
+
+    # attention options: the same section rule; keys turn at their own row's triple, no pool needed
+    def attn(sec):
+        return Q.qsa_attn_options(16, 16, 1e-6, 1e4, 64, None, Q._SEC3(*sec))
+
+    def append_ex(a, r, cache):
+        return lib.qsa_append_ex(c, None, ctypes.byref(a), ctypes.byref(r), ctypes.byref(cache), 16, 16, 16, 16,
+                                 None)
+    assert append_ex(attn((11, 11, 11)), rows, no_pool) == Q.QSA_ERR_INVALID_ARG
+    assert append_ex(attn((11, 11, 10)), rows_mis, no_pool) == Q.QSA_ERR_INVALID_ARG
+    assert append_ex(attn((11, 11, 10)), rows, no_pool) == Q.QSA_ERR_CAPACITY
