@@ -34,16 +34,18 @@ def triples(n, img_start, gh, gw):
     return S.mrope_positions(n, img_start, gh, gw)
 
 
-def fill_pre(g, pre, s, n, mpos, chunks):
+def fill_pre(g, pre, s, n, mpos, chunks, data_seq=None):
     """Append tokens 0..n-1 of slot s through the pre-indexer in the given chunk sizes
-    (sizes that cut blocks, so some blocks complete in a later call)."""
+    (sizes that cut blocks, so some blocks complete in a later call). The token rows are
+    those of sequence `data_seq` (default s), so several slots can hold the same data."""
     Q = g.Q
+    src = s if data_seq is None else data_seq
     a = 0
     for m in chunks:
         m = min(m, n - a)
         if m <= 0:
             break
-        k, v, ix = gen_token_rows(g.sh, g.wl.seed, s, np.arange(a, a + m), np.zeros(m, np.int64), g.device)
+        k, v, ix = gen_token_rows(g.sh, g.wl.seed, src, np.arange(a, a + m), np.zeros(m, np.int64), g.device)
         Q.qsa_append_pre(g.cfg, pre, Q.Rows(torch.tensor([s], device=g.device),
                                             torch.tensor([a], dtype=torch.int32, device=g.device), m,
                                             mrope_pos=None if mpos is None else mpos[a:a + m].to(g.device)),
@@ -109,9 +111,10 @@ def test_text_triples_are_the_plain_path_bit_for_bit():
     pre_p, _ = pre_pair(Q, sh.idx_dim, g.device, None)
     text = triples(n, n, 1, 1)        # no image: (p, p, p) throughout
     a, b, c = g.slots
-    fill_pre(g, pre_p, a, n, None, [700, 700, 700])        # plain RoPE
-    fill_pre(g, pre_m, b, n, None, [701, 699, 700])        # MRoPE section, text rows (no triples)
-    fill_pre(g, pre_m, c, n, text, [333, 1000, 777])       # MRoPE section, explicit (p, p, p)
+    # the same token rows in all three slots
+    fill_pre(g, pre_p, a, n, None, [700, 700, 700], data_seq=a)        # plain RoPE
+    fill_pre(g, pre_m, b, n, None, [701, 699, 700], data_seq=a)        # MRoPE section, text rows (no triples)
+    fill_pre(g, pre_m, c, n, text, [333, 1000, 777], data_seq=a)       # MRoPE section, explicit (p, p, p)
     torch.cuda.synchronize()
     g.check_status()
     nb = n // sh.ratio
