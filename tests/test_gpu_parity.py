@@ -1,9 +1,12 @@
 """GPU parity against the CPU oracle on the five workloads, at their full sizes
 and in the launch configuration the benchmark times (the fused qsa_decode).
 
-Selected block sets must match bit-exactly; outputs within max-abs 2e-2 and
-rel-L2 1e-3 of the bf16-rounded oracle. At full size the oracle runs on
-sampled rows, which it computes one by one from the same seeded inputs."""
+Selected block sets must match bit-exactly on EVERY row of every step: the
+scores are exact, so the oracle's selection of a row (block_scores over its
+pooled keys, then select_blocks) is the one correct set and costs a matmul per
+row. Outputs must be within max-abs 2e-2 and rel-L2 1e-3 of the bf16-rounded
+oracle; at full size the oracle's attention runs on sampled rows, which it
+computes one by one from the same seeded inputs."""
 import numpy as np
 import pytest
 import torch
@@ -11,6 +14,7 @@ import torch
 from indexer_selected_sparse_gb300 import synth as S
 from oracle import qsa_oracle as O
 from tests.gpu_harness import GpuState, OracleSeq, bits, compare_row
+from tests.oracle_sets import assert_every_row, oracle_selections
 
 pytestmark = pytest.mark.gpu
 
@@ -29,6 +33,33 @@ def check_rows(g: GpuState, res, seqs_sampled, pos0, R, oracles):
             ref = oracles[s].row(pos0[i] + j)
             errs.append(compare_row(out[row], sel[row], int(nsel[row]), ref, topk))
     return errs
+
+
+class StepLog:
+    """The selections of every row of a series of steps, for one comparison
+    with the oracle's at the end: per sequence, its rows in step order."""
+
+    def __init__(self):
+        self.sel, self.nsel = [], []
+        self.rows = {}     # seq -> GPU rows in the concatenation
+        self.pos = {}      # seq -> positions of those rows
+        self.n = 0
+
+    def add(self, res, seqs, pos0, R):
+        self.sel.append(res["sel"].cpu().numpy())
+        self.nsel.append(res["n_sel"].cpu().numpy())
+        for i, s in enumerate(seqs):
+            for j in range(R):
+                self.rows.setdefault(s, []).append(self.n + i * R + j)
+                self.pos.setdefault(s, []).append(pos0[i] + j)
+        self.n += len(seqs) * R
+
+    def check(self, wl, hist=None):
+        """Every logged row against the oracle (hist: seq -> History of the
+        epochs its tokens were drawn with). Returns the number of rows."""
+        req = [(s, max(p) + 1, (hist[s].epoch_from if hist else [(0, 0)]), p) for s, p in self.pos.items()]
+        want = oracle_selections(wl, req)
+        return assert_every_row(np.concatenate(self.sel), np.concatenate(self.nsel), self.rows, want)
 
 
 def test_tiny_decode_every_row_and_pools():
@@ -57,13 +88,16 @@ def test_steady_decode_batch32_prefix32k_four_steps():
     sampled = [0, 13, 31]
     oracles = {s: OracleSeq(wl, s, wl.prefixes[0] + 4) for s in sampled}
     pos0 = list(wl.prefixes)
+    log = StepLog()
     for step in range(4):                       # the tail cycles 1 -> 2 -> 3 -> 0
         res = g.decode(pos0, 1)
         g.check_status()
+        log.add(res, g.slots, pos0, 1)
         pos0 = [p + 1 for p in pos0]
         assert g.cache.ingested.cpu().tolist() == pos0
         assert (res["n_sel"].cpu() == wl.shapes.topk).all()
         check_rows(g, res, set(sampled), [p - 1 for p in pos0], 1, oracles)
+    assert log.check(wl) == 4 * wl.n_seq      # every row of every step
 
 
 def test_ragged_decode_batch64_eight_steps():
@@ -76,9 +110,11 @@ def test_ragged_decode_batch64_eight_steps():
     sampled = sorted({by[2050], by[2051], by[2052], by[600], longest, 7, 40})
     oracles = {s: OracleSeq(wl, s, pre[s] + 8) for s in sampled}
     pos0 = list(pre)
+    log = StepLog()
     for step in range(8):
         res = g.decode(pos0, 1)
         g.check_status()
+        log.add(res, g.slots, pos0, 1)
         pos0 = [p + 1 for p in pos0]
         assert g.cache.ingested.cpu().tolist() == pos0     # ingested == pos after every append
         check_rows(g, res, set(sampled), [p - 1 for p in pos0], 1, oracles)
@@ -87,6 +123,7 @@ def test_ragged_decode_batch64_eight_steps():
         dense = vis // wl.shapes.ratio <= wl.shapes.topk
         assert np.array_equal(nsel[dense], vis[dense] // wl.shapes.ratio)
         assert (nsel[~dense] == wl.shapes.topk).all()
+    assert log.check(wl) == 8 * wl.n_seq
 
 
 def test_verify_then_rewind_then_decode():
@@ -101,6 +138,9 @@ def test_verify_then_rewind_then_decode():
     res = g.decode([p] * wl.n_seq, R)
     g.check_status()
     check_rows(g, res, set(sampled), [p] * wl.n_seq, R, oracles)
+    vlog = StepLog()
+    vlog.add(res, g.slots, [p] * wl.n_seq, R)
+    assert vlog.check(wl) == R * wl.n_seq     # every verify row, drawn before any rewind
     # reject 0..2 rows per sequence and rewind the counters
     rej = S.reject_counts(wl.seed, wl.n_seq)
     g.rewind(rej)
@@ -111,13 +151,17 @@ def test_verify_then_rewind_then_decode():
     steps = wl.extra["decode_after"]
     oracles = {s: OracleSeq(wl, s, pos0[s] + steps, hist=g.hist[s]) for s in sampled}
     outs = []
+    dlog = StepLog()
     for step in range(steps):
         res = g.decode(pos0, 1)
         g.check_status()
         check_rows(g, res, set(sampled), pos0, 1, oracles)
+        dlog.add(res, g.slots, pos0, 1)
         outs.append((bits(res["out"]), res["sel"].cpu().numpy()))
         pos0 = [q + 1 for q in pos0]
         assert g.cache.ingested.cpu().tolist() == pos0
+    # every decode row after the rewind, re-appended positions carrying fresh rows
+    assert dlog.check(wl, hist=g.hist) == steps * wl.n_seq
     # never drafting: append the accepted tokens directly, decode the same steps
     h = GpuState(wl, extra_tokens=16)
     for s in h.slots:
@@ -153,6 +197,9 @@ def test_chunked_prefill_8193_rows():
     for j in list(range(0, C, 512)) + [1, 2, 3, 4, C - 2, C - 1]:
         ref = orc.row(p + j)
         compare_row(out[j], sel[j], int(nsel[j]), ref, g.cfg.topk)
+    log = StepLog()
+    log.add(res, [0], [p], C)
+    assert log.check(wl) == C                  # all 8193 prefill rows
     # chunks {4096, 4097} give the same sets and outputs, bit for bit
     h = GpuState(wl, extra_tokens=16)
     h.append_prefix()
