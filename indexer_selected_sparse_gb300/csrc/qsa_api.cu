@@ -20,8 +20,13 @@ int ilog2(int v) {
   while ((1 << l) < v) ++l;
   return l;
 }
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+// Argument checks and conversions shared by every entry point (declared in
+// qsa_internal.cuh, so that every translation unit validates alike).
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_cfg(const qsa_config *c) {
   if (!c) return QSA_ERR_INVALID_ARG;
@@ -113,6 +118,8 @@ int cuda_status(cudaError_t e) {
       return QSA_ERR_CUDA;
   }
 }
+
+namespace {
 
 int host_capacity_check(const qsa_rows *r, const qsa_cache *c, int page_size) {
   if (!r->pos0_host) return QSA_OK;

@@ -372,4 +372,16 @@ cudaError_t launch_attn(const Shape &sh, int n_seq, int R, const int32_t *seq_id
 // tokens a row's attention can take (splits x split length)
 int attn_max_tokens(const Shape &sh);
 
+// Host-side argument checks and conversions of the entry points
+// (qsa_api.cu), shared so that every entry point validates alike.
+bool aligned16(const void *p);
+int check_cfg(const qsa_config *c);
+Shape make_shape(const qsa_config *c);
+int check_rows(const qsa_rows *r);
+int check_cache(const qsa_cache *c, bool need_kv, bool need_idx);
+CacheView view(const qsa_cache *c);
+// QSA_OK, QSA_ERR_CUDA (a non-sticky error, cleared) or QSA_ERR_CUDA_FATAL
+// (a sticky error: the context is lost).
+int cuda_status(cudaError_t e);
+
 }  // namespace qsa

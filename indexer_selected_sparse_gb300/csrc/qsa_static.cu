@@ -52,13 +52,6 @@ cudaError_t scratch_address(void **out) {
   return cudaSuccess;
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-int ilog2(int v) {
-  int l = 0;
-  while ((1 << l) < v) ++l;
-  return l;
-}
-
 }  // namespace
 }  // namespace qsa
 
@@ -68,53 +61,22 @@ extern "C" int qsa_gather_attn_static(const qsa_config *cfg, const qsa_rows *row
                                       const qsa_cache *cache, const qsa_bf16 *q,
                                       const int32_t *sel, const int32_t *n_sel, qsa_bf16 *out,
                                       int32_t *status, cudaStream_t stream) {
-  int rc = qsa_config_check(cfg);
-  if (rc != QSA_OK) return rc;
-  if (!rows || rows->n_seq < 0 || rows->rows_per_seq < 0) return QSA_ERR_INVALID_ARG;
-  const long long n_rows = static_cast<long long>(rows->n_seq) * rows->rows_per_seq;
+  // the same checks as qsa_gather_attn, bar the workspace
+  int rc;
+  if ((rc = check_cfg(cfg)) != QSA_OK) return rc;
+  if ((rc = check_rows(rows)) != QSA_OK) return rc;
+  if ((rc = check_cache(cache, true, false)) != QSA_OK) return rc;
+  const int n_rows = rows->n_seq * rows->rows_per_seq;
   if (n_rows == 0) return QSA_OK;
-  if (n_rows > 65535 || !rows->seq_ids || !rows->pos0) return QSA_ERR_INVALID_ARG;
-  if (!cache || !cache->page_table || cache->max_pages < 1 || cache->num_pages < 1 ||
-      !cache->k_pool || !cache->v_pool || !aligned16(cache->k_pool) || !aligned16(cache->v_pool))
-    return QSA_ERR_INVALID_ARG;
   if (!q || !sel || !n_sel || !out || !aligned16(q) || !aligned16(out)) return QSA_ERR_INVALID_ARG;
-
-  Shape sh;
-  sh.ratio = cfg->ratio;
-  sh.budget = cfg->budget;
-  sh.topk = cfg->budget / cfg->ratio;
-  sh.h_idx = cfg->n_idx_heads;
-  sh.d_idx = cfg->idx_dim;
-  sh.hq = cfg->n_q_heads;
-  sh.hkv = cfg->n_kv_heads;
-  sh.d = cfg->head_dim;
-  sh.page = cfg->page_size;
-  sh.log2_ratio = ilog2(cfg->ratio);
-  sh.log2_page = ilog2(cfg->page_size);
-  sh.idx_fp8 = cfg->index_format != QSA_INDEX_BF16 ? 1 : 0;
-  sh.idx_fp4 = cfg->index_format == QSA_INDEX_MXFP4 ? 1 : 0;
-  sh.window = cfg->local_window;
+  const Shape sh = make_shape(cfg);
   // the partials of this many rows must fit the fixed array
-  if (attn_partial_bytes(sh, static_cast<int>(n_rows)) > kStaticScratchBytes) return QSA_ERR_WORKSPACE;
+  if (attn_partial_bytes(sh, n_rows) > kStaticScratchBytes) return QSA_ERR_WORKSPACE;
 
   void *scratch = nullptr;
   cudaError_t e = scratch_address(&scratch);
-  if (e != cudaSuccess) return e == cudaErrorInvalidDevice ? QSA_ERR_INVALID_ARG : QSA_ERR_CUDA;
-
-  CacheView cv;
-  cv.page_table = cache->page_table;
-  cv.max_pages = cache->max_pages;
-  cv.num_pages = cache->num_pages;
-  cv.k_pool = cache->k_pool;
-  cv.v_pool = cache->v_pool;
-  cv.idxraw_pool = cache->idxraw_pool;
-  cv.idxblk_pool = cache->idxblk_pool;
-  e = launch_attn(sh, rows->n_seq, rows->rows_per_seq, rows->seq_ids, rows->pos0, cv, q, sel, n_sel,
-                  out, scratch, status, false, CommitArgs{}, stream);
-  if (e == cudaSuccess) return QSA_OK;
-  if (e == cudaErrorIllegalAddress || e == cudaErrorLaunchFailure || e == cudaErrorMisalignedAddress ||
-      e == cudaErrorIllegalInstruction)
-    return QSA_ERR_CUDA_FATAL;
-  cudaGetLastError();
-  return QSA_ERR_CUDA;
+  if (e == cudaErrorInvalidDevice) return QSA_ERR_INVALID_ARG;
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_attn(sh, rows->n_seq, rows->rows_per_seq, rows->seq_ids, rows->pos0, view(cache), q,
+                                 sel, n_sel, out, scratch, status, false, CommitArgs{}, stream));
 }
