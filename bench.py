@@ -217,6 +217,29 @@ def whole_job_rate(rows_per_rank, world, ms):
     return rows_per_rank * world / (ms * 1e-3)
 
 
+STICKY_CUDA = ("illegal memory access", "illegal instruction", "misaligned address", "unspecified launch failure",
+               "hardware stack error", "device-side assert", "launch timed out", "invalid program counter")
+
+
+def guarded(fn, dist, torch):
+    """Run one secondary leg. On a single rank its failure is reported in the
+    line (the device-timed headline still prints), with "ok": false; a sticky
+    CUDA error (the context is lost) is re-raised, and so is any failure when
+    several ranks run, since the other ranks would wait in mismatched
+    collectives."""
+    try:
+        return fn()
+    except Exception as e:
+        msg = f"{type(e).__name__}: {e}"
+        if dist is not None or any(k in msg.lower() for k in STICKY_CUDA):
+            raise
+        try:
+            torch.cuda.synchronize()
+        except Exception:
+            raise e
+        return {"ok": False, "error": msg}
+
+
 def traffic_for(kernel_key):
     """ncu DRAM bytes per launch for a kernel, if the committed counters were
     taken on the kernel source as it is now."""
@@ -405,11 +428,8 @@ def run_gpu(args):
         roofline, stage_ms, stage_bytes, stage_flops = stage_breakdown(
             args, Q, torch, cfg, sh, cache, batches, ws, status, stream, hpos, NB, B, hbm_gbs, peak_kind)
 
-    try:
-        out_e2e = run_e2e(args, Q, torch, cfg, cache, batches, ws, status, stream, NB, B, rows_per_step,
-                          decode_call, dist, dev)
-    except Exception as e:  # reported in the line; the device-timed headline still prints
-        out_e2e = {"error": f"{type(e).__name__}: {e}"}
+    out_e2e = guarded(lambda: run_e2e(args, Q, torch, cfg, cache, batches, ws, status, stream, NB, B,
+                                      rows_per_step, decode_call, dist, dev), dist, torch)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -786,7 +806,7 @@ def run_e2e(args, Q, torch, cfg, cache, batches, ws, status, stream, NB, B, rows
     KE = args.e2e_steps
     if KE > 0:
         e2e_graphs, keep = [], []
-        h2d = d2h = 0
+        h2d = d2h = h2d_copied = 0
         for bt in batches:
             ins = [bt[k] for k in STEP_INPUTS]
             dbuf, dviews = packed(torch, ins, dev)
@@ -797,7 +817,8 @@ def run_e2e(args, Q, torch, cfg, cache, batches, ws, status, stream, NB, B, rows
             ebt = dict(bt)
             ebt.update(zip(STEP_INPUTS, dviews))
             keep.append((dbuf, hbuf, hout, ebt))
-            h2d = hbuf.numel()
+            h2d = sum(t.numel() * t.element_size() for t in ins)   # the inputs' own bytes
+            h2d_copied = hbuf.numel()                               # with the 256-byte alignment gaps
             d2h = hout.numel() * hout.element_size()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
@@ -819,7 +840,8 @@ def run_e2e(args, Q, torch, cfg, cache, batches, ws, status, stream, NB, B, rows
         ems = max_over_ranks(dist, e0.elapsed_time(e1) / KE, dev)
         assert int(status.item()) == 0, Q.qsa_strerror(int(status.item()))
         e2e = {"value": round(rows_per_step / (ems * 1e-3), 1), "unit": "rows/s",  # rows of all ranks
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ems, 5),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "h2d_bytes_copied_per_step": h2d_copied,
+               "ms_per_step": round(ems, 5),
                "path": "pinned host inputs (one packed buffer) -> one H2D copy -> qsa_decode -> D2H output, "
                        "per step (CUDA graph)"}
     return e2e
@@ -1111,10 +1133,8 @@ def main():
         import torch
         out["prefill"] = run_prefill(args, torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))))
     if late is not None:
-        try:
-            out["attn_options"] = late()
-        except Exception as e:  # this leg's failure is reported; the headline line still prints
-            out["attn_options"] = {"error": f"{type(e).__name__}: {e}"}
+        import torch
+        out["attn_options"] = guarded(late, None if world == 1 else True, torch)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(args.oracle_rows)
