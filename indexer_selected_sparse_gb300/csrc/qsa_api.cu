@@ -333,8 +333,10 @@ int decode_impl(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_att
   commit.seq_ids = rows->seq_ids;
   commit.pos0 = rows->pos0;
   commit.ingested = cache->ingested;
+  // the attention derives each row's selected count (min(n_blk, K)) instead of
+  // loading n_sel: one dependent load less after its wait
   if (e == cudaSuccess)
-    e = launch_attn(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, q_main ? q_att : q, sel, n_sel, out,
+    e = launch_attn(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, cv, q_main ? q_att : q, sel, nullptr, out,
                     base + L.partials, status, true, commit, stream, nullptr, att ? att->gate : nullptr);
   return cuda_status(e);
 }

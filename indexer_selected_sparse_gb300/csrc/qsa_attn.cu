@@ -173,7 +173,11 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
         n_blk = (ps + 1) >> sh.log2_ratio;
       }
     }
-    const int n_sel = row_ok ? min(max(n_sel_arr[U.row], 0), min(n_blk, sh.topk)) : 0;
+    // n_sel_arr == nullptr: the selection was made by this step's select kernel,
+    // which takes min(n_blk, K) blocks of every row inside the page table, so
+    // the count needs no load (the stores of sel are the only wait)
+    const int cap_sel = min(n_blk, sh.topk);
+    const int n_sel = row_ok ? (n_sel_arr ? min(max(n_sel_arr[U.row], 0), cap_sel) : cap_sel) : 0;
     int n_body = n_sel * r;
     int run0 = n_blk * r;
     if (row_ok && sh.window > 0 && U.visible - sh.window < run0) {
@@ -477,11 +481,24 @@ __global__ void __launch_bounds__(kMergeThreads)
 merge_kernel(int hq, int hkv, int n_split, const float *__restrict__ part_m,
              const float *__restrict__ part_l, const float *__restrict__ part_acc,
              uint16_t *__restrict__ out, CommitArgs cm, const uint16_t *__restrict__ gate) {
+  const int row = blockIdx.x, g = blockIdx.y, t = threadIdx.x;
+  // the commit's first reads go out before the wait: no kernel of this step
+  // writes seq_ids, pos0 or ingested before the commit itself
+  const bool committer = cm.n_seq > 0 && row == 0 && g == 0;
+  int c_s = 0, c_p = 0, c_ing = 0;
+  if (committer && t < cm.n_seq) {
+    c_s = cm.seq_ids[t];
+    c_p = cm.pos0[t];
+    c_ing = cm.ingested[c_s];
+  }
   pdl_wait();  // the split partials come from the attention kernel
   pdl_trigger();
-  const int row = blockIdx.x, g = blockIdx.y, t = threadIdx.x;
-  if (cm.n_seq > 0 && row == 0 && g == 0) {
-    for (int i = t; i < cm.n_seq; i += kMergeThreads) {
+  if (committer) {
+    if (t < cm.n_seq && c_ing == c_p && c_p >= 0 && c_p + cm.R <= cm.capacity) {
+      cm.ingested[c_s] = c_p + cm.R;
+      if (cm.advance) cm.pos0[t] = c_p + cm.R;
+    }
+    for (int i = t + kMergeThreads; i < cm.n_seq; i += kMergeThreads) {
       const int s = cm.seq_ids[i];
       const int p0 = cm.pos0[i];
       if (cm.ingested[s] == p0 && p0 >= 0 && p0 + cm.R <= cm.capacity) {

@@ -35,8 +35,8 @@
 //     registers, hands the TMEM buffer back at once, and reduces them with
 //     paired fp32 FMAs (fma.rn.f32x2) in four independent chains combined in a
 //     fixed order -- the same for every group size, so a row's score does not
-//     depend on the batch shape. TMEM holds two accumulators, so the epilogue of
-//     one tile overlaps the MMA of the next.
+//     depend on the batch shape. TMEM holds up to four accumulators (as many as
+//     fit), so the MMAs of the next tiles run while a tile's epilogue reads.
 // Every mbarrier wait is bounded in time; on expiry the CTA records
 // QSA_ERR_TIMEOUT, waits (bounded) for its own copies, frees its TMEM and exits.
 #include <cuda.h>
@@ -228,7 +228,8 @@ struct TcArgs {
   int npad;            // MMA N (multiple of 16, <= 256)
   int hp;              // TMEM columns per row of the group (H_I, or npad when G == 1)
   int ncols;           // TMEM columns of one accumulator (power of two >= 32)
-  int tmem_cols;       // TMEM columns allocated: 2 accumulators (+ MXFP8: the A stages), a power of two
+  int acc_log2;        // log2 of the accumulators in TMEM (2 or 4)
+  int tmem_cols;       // TMEM columns allocated: the accumulators (+ MX: the A stages), a power of two
   int bpp_log2;        // log2(blocks per page)
   const int32_t *seq_ids;
   const int32_t *pos0;
@@ -255,10 +256,12 @@ constexpr int kMaxStagesBf16 = 6;
 constexpr int kMaxCStages = 4;     // MXFP8: bf16 A stages in TMEM filled by the converter warps
 constexpr int kConvWarps = 8;      // MXFP8: converter warps, 4 per copy ring, a block row per thread
 constexpr int kRowCols = 64;  // head columns of one row, at most
-// shared memory of the epilogue: per warp the weights of its row [kRowCols]
-constexpr int kEpiFloats = kMaxEpiWarps * kRowCols;
-constexpr int kNumBars = 2 * kMaxStages + 8 + 2 * kMaxCStages + 2;  // MXFP8 keys
-constexpr int kNumBarsBf16 = 2 * kMaxStagesBf16 + 8;                 // bf16 keys
+// shared memory of the epilogue: per warp the weights of its row in two
+// buffers [2][kRowCols] (the current group's, and the next one's fetched ahead)
+constexpr int kEpiFloats = kMaxEpiWarps * 2 * kRowCols;
+constexpr int kMaxAcc = 4;  // TMEM accumulators, at most
+constexpr int kNumBars = 2 * kMaxStages + 4 + 2 * kMaxAcc + 2 * kMaxCStages + 2;  // MX keys
+constexpr int kNumBarsBf16 = 2 * kMaxStagesBf16 + 4 + 2 * kMaxAcc;               // bf16 keys
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -280,17 +283,59 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
   }
 }
 
-// Tiles of 128 blocks that group g needs (0 when its last row is dense or its
-// position is outside the page table; the select kernel reports the latter).
-__device__ __forceinline__ int group_tiles(const TcArgs &a, int g) {
+// Tiles of 128 blocks that group g needs, its sequence's pos0 being p0 (0 when
+// its last row is dense or its position is outside the page table; the select
+// kernel reports the latter).
+__device__ __forceinline__ int group_tiles(const TcArgs &a, int g, int p0) {
   const int i = g / a.groups_per_seq;
   const int j0 = (g - i * a.groups_per_seq) * a.G;
   const int g_rows = min(a.G, a.R - j0);
-  const int p0 = a.pos0[i];
   const int vis_last = p0 + j0 + g_rows;
   if (p0 + j0 + 1 < 1 || vis_last > a.max_pages * a.sh.page) return 0;
   const int nb = vis_last >> a.sh.log2_ratio;
   return nb > a.sh.topk ? (nb + kTcTileBlocks - 1) / kTcTileBlocks : 0;
+}
+
+// 32 consecutive groups held by a warp, one per lane: the group's tile count,
+// and its sequence's pos0 and slot. Every role walks its items through such a
+// chunk, so moving from one group to the next is a shuffle, not a global load;
+// a new chunk costs one round trip (pos0 and seq_ids load side by side).
+struct GroupChunk {
+  int base = -1;  // first group of the chunk
+  int tiles = 0, p0 = 0, seq = 0;
+};
+
+__device__ __forceinline__ void chunk_load(GroupChunk &c, const TcArgs &a, int base, int lane) {
+  c.base = base;
+  const int g = base + lane;
+  c.tiles = 0;
+  c.p0 = 0;
+  c.seq = 0;
+  if (g < a.n_groups) {
+    const int i = g / a.groups_per_seq;
+    c.p0 = a.pos0[i];
+    c.seq = a.seq_ids[i];
+    c.tiles = group_tiles(a, g, c.p0);
+  }
+}
+
+// Warp-collective: moves the chunk to group g's 32 groups when needed; then
+// group g's entries are lane g - c.base's.
+__device__ __forceinline__ int chunk_lane(GroupChunk &c, const TcArgs &a, int g, int lane) {
+  if (g < c.base || g >= c.base + 32) chunk_load(c, a, g & ~31, lane);
+  return g - c.base;
+}
+__device__ __forceinline__ int chunk_tiles(GroupChunk &c, const TcArgs &a, int g, int lane) {
+  const int src = chunk_lane(c, a, g, lane);
+  return __shfl_sync(0xffffffffu, c.tiles, src);
+}
+__device__ __forceinline__ int chunk_p0(GroupChunk &c, const TcArgs &a, int g, int lane) {
+  const int src = chunk_lane(c, a, g, lane);
+  return __shfl_sync(0xffffffffu, c.p0, src);
+}
+__device__ __forceinline__ int chunk_seq(GroupChunk &c, const TcArgs &a, int g, int lane) {
+  const int src = chunk_lane(c, a, g, lane);
+  return __shfl_sync(0xffffffffu, c.seq, src);
 }
 
 // The work of a CTA is a contiguous range of the (group, tile) items in
@@ -308,13 +353,14 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
   return v;
 }
 
-// Warp-cooperative: total items, then this CTA's first item.
-__device__ Walker walker_start(const TcArgs &a, int n_groups, int lane) {
+// Warp-collective: total items, then this CTA's first item; leaves the chunk
+// of that item's group loaded.
+__device__ __forceinline__ Walker walker_start(const TcArgs &a, GroupChunk &c, int lane) {
+  const int n_groups = a.n_groups;
   int total = 0;
   for (int g0 = 0; g0 < n_groups; g0 += 32) {
-    const int g = g0 + lane;
-    const int tl = g < n_groups ? group_tiles(a, g) : 0;
-    total += __shfl_sync(0xffffffffu, warp_incl_scan(tl, lane), 31);
+    if (c.base != g0) chunk_load(c, a, g0, lane);
+    total += __shfl_sync(0xffffffffu, warp_incl_scan(c.tiles, lane), 31);
   }
   const long long first = static_cast<long long>(total) * blockIdx.x / gridDim.x;
   const long long last = static_cast<long long>(total) * (blockIdx.x + 1) / gridDim.x;
@@ -322,14 +368,13 @@ __device__ Walker walker_start(const TcArgs &a, int n_groups, int lane) {
   if (w.left <= 0) return w;
   int base = 0;
   for (int g0 = 0; g0 < n_groups; g0 += 32) {
-    const int g = g0 + lane;
-    const int tl = g < n_groups ? group_tiles(a, g) : 0;
-    const int incl = warp_incl_scan(tl, lane);
+    if (c.base != g0) chunk_load(c, a, g0, lane);
+    const int incl = warp_incl_scan(c.tiles, lane);
     const int tot = __shfl_sync(0xffffffffu, incl, 31);
     if (base + tot > first) {
       const unsigned m = __ballot_sync(0xffffffffu, base + incl > first);
       const int src = __ffs(m) - 1;
-      const int tl_s = __shfl_sync(0xffffffffu, tl, src);
+      const int tl_s = __shfl_sync(0xffffffffu, c.tiles, src);
       const int incl_s = __shfl_sync(0xffffffffu, incl, src);
       w.g = g0 + src;
       w.tiles = tl_s;
@@ -341,15 +386,23 @@ __device__ Walker walker_start(const TcArgs &a, int n_groups, int lane) {
   return w;
 }
 
-__device__ __forceinline__ void walker_next(Walker &w, const TcArgs &a, int n_groups) {
+// Warp-collective: the next item.
+__device__ __forceinline__ void walker_next(Walker &w, const TcArgs &a, GroupChunk &c, int lane) {
   --w.left;
   if (++w.t < w.tiles) return;
   w.t = 0;
   do {
     ++w.g;
-    w.tiles = w.g < n_groups ? group_tiles(a, w.g) : 0;
-  } while (w.g < n_groups && w.tiles == 0 && w.left > 0);
-  if (w.g >= n_groups) w.left = 0;
+    w.tiles = w.g < a.n_groups ? chunk_tiles(c, a, w.g, lane) : 0;
+  } while (w.g < a.n_groups && w.tiles == 0 && w.left > 0);
+  if (w.g >= a.n_groups) w.left = 0;
+}
+
+// Warp-collective: the first group after g with tiles to score in g's chunk
+// (-1 if none there): the group whose inputs a role may fetch ahead.
+__device__ __forceinline__ int chunk_next_group(const GroupChunk &c, int g, int lane) {
+  const unsigned m = __ballot_sync(0xffffffffu, c.base + lane > g && c.tiles > 0);
+  return m ? c.base + __ffs(m) - 1 : -1;
 }
 
 // A batch of up to 32 / pages_in_tile consecutive tiles of one group, as the
@@ -362,33 +415,25 @@ struct Batch {
   bool have = false; // this lane's page holds a visible block
 };
 
-// What a batch needs of its group: the first row, the blocks visible to its
-// last row and its sequence's page-table row. Loaded once per group, so a new
-// batch of the same group issues its page-id load without waiting on others.
-struct GroupInfo {
-  int g = -1, row0 = 0, nblk_last = 0, nblk_old = 0;
-  const int32_t *ptab = nullptr;
-};
-
-__device__ __forceinline__ Batch load_batch(const TcArgs &a, const Walker &w, GroupInfo &gi, int lane,
+// Warp-collective. The group's first row, the blocks visible to its last row
+// and its sequence's page-table row come from the chunk; the page ids are one
+// load per lane, issued a batch ahead of their use.
+__device__ __forceinline__ Batch load_batch(const TcArgs &a, const Walker &w, GroupChunk &c, int lane,
                                             int per_batch, int pages_in_tile, int bpp) {
-  if (w.g != gi.g) {
-    const int i = w.g / a.groups_per_seq;
-    const int j0 = (w.g - i * a.groups_per_seq) * a.G;
-    const int g_rows = min(a.G, a.R - j0);
-    gi.row0 = i * a.R + j0;
-    gi.nblk_last = (a.pos0[i] + j0 + g_rows) >> a.sh.log2_ratio;
-    gi.nblk_old = a.pos0[i] >> a.sh.log2_ratio;
-    gi.ptab = a.page_table + static_cast<size_t>(a.seq_ids[i]) * a.max_pages;
-    gi.g = w.g;
-  }
+  const int i = w.g / a.groups_per_seq;
+  const int j0 = (w.g - i * a.groups_per_seq) * a.G;
+  const int g_rows = min(a.G, a.R - j0);
+  const int p0 = chunk_p0(c, a, w.g, lane);
+  const int seq = chunk_seq(c, a, w.g, lane);
+  const int nblk_last = (p0 + j0 + g_rows) >> a.sh.log2_ratio;
+  const int32_t *ptab = a.page_table + static_cast<size_t>(seq) * a.max_pages;
   Batch b;
-  b.row0 = gi.row0;
-  b.nblk_old = gi.nblk_old;
+  b.row0 = i * a.R + j0;
+  b.nblk_old = p0 >> a.sh.log2_ratio;
   b.nb = min(min(per_batch, w.tiles - w.t), w.left);
   const int pidx = w.t * pages_in_tile + lane;
-  b.have = lane < b.nb * pages_in_tile && pidx * bpp < gi.nblk_last;
-  b.pg = b.have ? gi.ptab[pidx] : 0;
+  b.have = lane < b.nb * pages_in_tile && pidx * bpp < nblk_last;
+  b.pg = b.have ? ptab[pidx] : 0;
   return b;
 }
 
@@ -442,8 +487,8 @@ __device__ __forceinline__ uint32_t bf16x2_pow2(int e) {
 //   MXFP8 keys: [B slots][byte ring: S x 128 blocks of d_I + d_I/32 bytes][epilogue]
 //               [barriers][tmem address][abort flag]; the bf16 A tiles live in TMEM
 // A tile is 128 rows x d_I bf16 in the K-major core-matrix layout; a B slot is
-// DI/64 halves x npad rows x 128 B (128B swizzle). TMEM: two accumulators of
-// ncols columns, then (MXFP8) kMaxCStages A tiles of d_I / 2 columns.
+// DI/64 halves x npad rows x 128 B (128B swizzle). TMEM: 2 or 4 accumulators
+// of ncols columns, then (MX planes) kMaxCStages A tiles of d_I / 2 columns.
 template <int DI, bool FP8, bool FP4 = false>
 __global__ void __launch_bounds__(FP8 ? kMaxThreadsFp8 : kMaxThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages) {
@@ -482,10 +527,13 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
   auto b_full = [&](int s) { return bars + 8u * (2 * MS + s); };
   auto b_empty = [&](int s) { return bars + 8u * (2 * MS + 2 + s); };
   auto t_full = [&](int s) { return bars + 8u * (2 * MS + 4 + s); };
-  auto t_empty = [&](int s) { return bars + 8u * (2 * MS + 6 + s); };
-  auto c_full = [&](int s) { return bars + 8u * (2 * MS + 8 + s); };
-  auto c_empty = [&](int s) { return bars + 8u * (2 * MS + 8 + kMaxCStages + s); };
-  auto q_ready = [&](int s) { return bars + 8u * (2 * MS + 8 + 2 * kMaxCStages + s); };
+  auto t_empty = [&](int s) { return bars + 8u * (2 * MS + 4 + kMaxAcc + s); };
+  constexpr int CB = 2 * MS + 4 + 2 * kMaxAcc;  // first MX barrier
+  auto c_full = [&](int s) { return bars + 8u * (CB + s); };
+  auto c_empty = [&](int s) { return bars + 8u * (CB + kMaxCStages + s); };
+  auto q_ready = [&](int s) { return bars + 8u * (CB + 2 * kMaxCStages + s); };
+  // TMEM accumulators: tile k accumulates into buffer k % n_acc
+  const int n_acc = 1 << a.acc_log2, acc_mask = n_acc - 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ws + kEpiFloats + 2 * NBARS);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -507,6 +555,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     for (int s = 0; s < 2; ++s) {
       mbar_init(b_full(s), 1);
       mbar_init(b_empty(s), 1);
+    }
+    for (int s = 0; s < n_acc; ++s) {
       mbar_init(t_full(s), 1);
       mbar_init(t_empty(s), 32 * 4 * a.G);  // every epilogue thread
     }
@@ -514,17 +564,24 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     mbar_fence_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
   const int bpp = 1 << a.bpp_log2;
   const int pages_in_tile = kTcTileBlocks >> a.bpp_log2;
   const uint32_t page_bytes = FP4 ? static_cast<uint32_t>(fp4_page_bytes(bpp, DI))
                               : (FP8 ? static_cast<uint32_t>(fp8_page_bytes(bpp, DI)) : static_cast<uint32_t>(bpp) * DI * 2);
-
   // MXFP8: a second producer warp (the last one) for the second copy ring
   const int prod2 = FP8 ? static_cast<int>(blockDim.x >> 5) - 1 : -1;
+  const int per_batch = 32 / pages_in_tile;
+  // Every role's first item, and the producers' first page ids, before the
+  // block barrier: these two round trips (positions and slots side by side,
+  // then the page ids) overlap the barrier set-up and the TMEM allocation.
+  GroupChunk chunk;
+  const Walker w0 = walker_start(a, chunk, lane);
+  Batch cur0;
+  if ((warp == 0 || warp == prod2) && w0.left > 0) cur0 = load_batch(a, w0, chunk, lane, per_batch, pages_in_tile, bpp);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   if (warp == 0 || warp == prod2) {
     // ---------------- producers ----------------
     // MXFP8: two producer warps issue alternate tiles (warp 0 the even ones and
@@ -540,11 +597,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     // ring's worth of them is issued before the dependency wait, so their HBM
     // latency overlaps the append.
     const int par = warp == 0 ? 0 : 1;
-    Walker w = walker_start(a, n_groups, lane);
+    Walker w = w0;
     const uint64_t stream_policy = l2_evict_first();
-    const int per_batch = 32 / pages_in_tile;
-    GroupInfo gi;
-    Batch cur = load_batch(a, w, gi, lane, per_batch, pages_in_tile, bpp);
+    Batch cur = cur0;
     int cur_g = -1, gseq = -1, k = 0;
     bool ok = true, waited = false;
     // a query load held back until the dependency wait (queries written this step)
@@ -564,8 +619,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     };
     while (ok && w.left > 0) {
       Walker wn = w;
-      for (int it = 0; it < cur.nb; ++it) walker_next(wn, a, n_groups);
-      const Batch nxt = wn.left > 0 ? load_batch(a, wn, gi, lane, per_batch, pages_in_tile, bpp) : Batch{};
+      for (int it = 0; it < cur.nb; ++it) walker_next(wn, a, chunk, lane);
+      const Batch nxt = wn.left > 0 ? load_batch(a, wn, chunk, lane, per_batch, pages_in_tile, bpp) : Batch{};
       if (par == 0 && w.g != cur_g) {
         ++gseq;
         const int bs = gseq & 1;
@@ -616,12 +671,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     if (!waited) wait_now();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    Walker w = walker_start(a, n_groups, lane);
+    Walker w = w0;
     int cur_g = -1, gseq = -1;
     const uint32_t idesc = idesc_bf16_f32(kTcTileBlocks, a.npad);
     for (int k = 0; w.left > 0; ++k) {
       const int s = FP8 ? k % N_OPD : k % S;  // operand stage
-      const int buf = k & 1;
+      const int buf = k & acc_mask;
       bool ok = true;
       if (lane == 0)
         ok = FP8 ? mbar_wait_or_abort(c_full(s), (k / N_OPD) & 1, abort_flag, a.status)
@@ -634,7 +689,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
           ok = mbar_wait_or_abort(FP8 ? q_ready(bs) : b_full(bs), (gseq >> 1) & 1, abort_flag, a.status);
         cur_g = w.g;
       }
-      if (lane == 0 && ok && k >= 2) ok = mbar_wait_or_abort(t_empty(buf), ((k >> 1) - 1) & 1, abort_flag, a.status);
+      if (lane == 0 && ok && k >= n_acc)
+        ok = mbar_wait_or_abort(t_empty(buf), ((k >> a.acc_log2) - 1) & 1, abort_flag, a.status);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       if (lane == 0) {
@@ -646,7 +702,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
           const uint64_t bd = smem_desc_sw128(b_u + bs * b_slot + hh * b_half + k4 * 32);
           if (FP8) {
             // K step kk: columns 8kk .. 8kk+7 of the A tile in TMEM
-            tc_mma_ta(d, tmem + 2 * a.ncols + s * (DI / 2) + kk * 8, bd, idesc, kk > 0 ? 1u : 0u);
+            tc_mma_ta(d, tmem + n_acc * a.ncols + s * (DI / 2) + kk * 8, bd, idesc, kk > 0 ? 1u : 0u);
           } else {
             // K step kk: core matrices 2kk and 2kk+1 along K
             const uint64_t ad = smem_desc_interleave(a_u + s * A_STAGE + kk * 256, 128, DI * 16);
@@ -656,7 +712,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         tc_commit(FP8 ? c_empty(s) : a_empty(s));
         tc_commit(t_full(buf));
       }
-      walker_next(w, a, n_groups);
+      walker_next(w, a, chunk, lane);
       if (lane == 0 && (w.left <= 0 || w.g != cur_g)) tc_commit(b_empty(bs));
     }
   } else if (FP8 && warp >= 2 + 4 * a.G) {
@@ -675,8 +731,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     // a 16-byte run of the row: 16 E4M3 elements, or 32 E2M1 (one MX block)
     const uint32_t src_row = slot * page_bytes + ((rr >> 3) * (FP4 ? DI / 32 : DI / 16)) * 128 + (rr & 7) * 16;
     const uint32_t scl_off = slot * page_bytes + bpp * (FP4 ? DI / 2 : DI) + rr * (DI / 32);
-    const uint32_t a_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + 2 * a.ncols;
-    Walker w = walker_start(a, n_groups, lane);
+    const uint32_t a_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + n_acc * a.ncols;
+    Walker w = w0;
     int cur_gq = -1, gq = -1;
     for (int k = 0; w.left > 0; ++k) {
       if (w.g != cur_gq) {
@@ -721,7 +777,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         cur_gq = w.g;
       }
       if ((k & 1) != rc) {  // the other ring's tile
-        walker_next(w, a, n_groups);
+        walker_next(w, a, chunk, lane);
         continue;
       }
       const int kr = k >> 1;
@@ -814,7 +870,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         mbar_arrive(c_full(c));
         mbar_arrive(a_empty(s));
       }
-      walker_next(w, a, n_groups);
+      walker_next(w, a, chunk, lane);
     }
   } else {
     // ---------------- epilogue (warps 2 .. 2 + 4G) ----------------
@@ -823,46 +879,88 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     const int e = warp - 2;
     const int q = warp & 3;
     const int j = e >> 2;  // < G: the block has 4G epilogue warps
-    Walker w = walker_start(a, n_groups, lane);
+    Walker w = w0;
     const int n16 = a.hp >> 4;  // 16-column TMEM loads of the row (hp a multiple of 16, <= 64)
-    float *wrow = ws + e * kRowCols;  // this warp's row weights, zero beyond H_I
+    // The head weights of this warp's row in a group, copied into one of the
+    // warp's two weight buffers with 4-byte cp.async (zero past H_I or past the
+    // group's last row); the next group's copy runs while the current group's
+    // tiles are scored, so a group change costs no global round trip.
+    float *wbuf = ws + e * 2 * kRowCols;
+    auto fetch_weights = [&](int g, int half) {
+      const uint32_t dst = smem_u32(wbuf + half * kRowCols);
+      int i = 0, row = 0;
+      bool any = false;
+      if (g >= 0) {
+        i = g / a.groups_per_seq;
+        const int jj0 = (g - i * a.groups_per_seq) * a.G;
+        any = j < min(a.G, a.R - jj0);
+        row = i * a.R + jj0 + j;
+      }
+      for (int c = lane; c < kRowCols; c += 32) {
+        const bool ok = any && c < sh.h_idx;
+        const float *src = ok ? a.w + static_cast<size_t>(row) * sh.h_idx + c : a.w;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst + 4u * c), "l"(src), "r"(ok ? 4 : 0)
+                     : "memory");
+      }
+      cp_async_commit();
+    };
+    int cur_half = 0;                   // buffer of the current group's weights
+    int nw_g = w.left > 0 ? w.g : -1;   // group whose weights sit (or land) in the other buffer
+    fetch_weights(nw_g, 1);
+    const float *wrow = wbuf;
     int cur_g = -1, j0 = 0, g_rows = 0, row0 = 0, p0 = 0;
     for (int k = 0; w.left > 0; ++k) {
-      const int buf = k & 1;
+      const int buf = k & acc_mask;
       if (w.g != cur_g) {
         const int i = w.g / a.groups_per_seq;
         j0 = (w.g - i * a.groups_per_seq) * a.G;
         g_rows = min(a.G, a.R - j0);
         row0 = i * a.R + j0;
-        p0 = a.pos0[i];
+        p0 = chunk_p0(chunk, a, w.g, lane);
+        __syncwarp();  // every lane is done with the buffers' previous contents
+        if (nw_g != w.g) {  // not fetched ahead (the group lies past the chunk)
+          cp_async_wait<0>();
+          nw_g = w.g;
+          fetch_weights(nw_g, cur_half ^ 1);
+        }
+        cp_async_wait<0>();
         __syncwarp();
-        for (int c = lane; c < kRowCols; c += 32)
-          wrow[c] = (j < g_rows && c < sh.h_idx) ? a.w[static_cast<size_t>(row0 + j) * sh.h_idx + c] : 0.f;
-        __syncwarp();
+        cur_half ^= 1;
+        wrow = wbuf + cur_half * kRowCols;
         cur_g = w.g;
+        nw_g = chunk_next_group(chunk, w.g, lane);
+        fetch_weights(nw_g, cur_half ^ 1);
       }
-      if (!mbar_wait_or_abort(t_full(buf), (k >> 1) & 1, abort_flag, a.status)) break;
+      if (!mbar_wait_or_abort(t_full(buf), (k >> a.acc_log2) & 1, abort_flag, a.status)) break;
       tc_fence_after();
       const uint32_t lane_addr =
           tmem + buf * a.ncols + (static_cast<uint32_t>(q * 32) << 16) + j * a.hp;
-      float v[kRowCols];
-#pragma unroll
-      for (int c = 0; c < kRowCols / 16; ++c)
-        if (c < n16) tmem_ld16(lane_addr + c * 16, v + c * 16);
-      tmem_ld_wait();
-      // the row is in registers: hand the TMEM buffer back to the MMA warp
-      tc_fence_before();
-      mbar_arrive(t_empty(buf));
+      // the row's head columns in two halves of 32 (fewer live registers); the
+      // FMA chains take the columns in the same order either way
       const float4 *w4 = reinterpret_cast<const float4 *>(wrow);
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kRowCols / 8; ++c) {
-        if (c < 2 * n16) {
-          const float4 wa = w4[2 * c], wb = w4[2 * c + 1];
-          ffma2(acc[0], acc[1], wa.x, wa.y, fmaxf(v[8 * c], 0.f), fmaxf(v[8 * c + 1], 0.f));
-          ffma2(acc[2], acc[3], wa.z, wa.w, fmaxf(v[8 * c + 2], 0.f), fmaxf(v[8 * c + 3], 0.f));
-          ffma2(acc[4], acc[5], wb.x, wb.y, fmaxf(v[8 * c + 4], 0.f), fmaxf(v[8 * c + 5], 0.f));
-          ffma2(acc[6], acc[7], wb.z, wb.w, fmaxf(v[8 * c + 6], 0.f), fmaxf(v[8 * c + 7], 0.f));
+      for (int hf = 0; hf < kRowCols / 32; ++hf) {
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          if (2 * hf + c < n16) tmem_ld16(lane_addr + (2 * hf + c) * 16, v + c * 16);
+        tmem_ld_wait();
+        if (hf == kRowCols / 32 - 1) {
+          // the row is in registers: hand the TMEM buffer back to the MMA warp
+          tc_fence_before();
+          mbar_arrive(t_empty(buf));
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int cc = 4 * hf + c;  // 8-column group of the row
+          if (cc < 2 * n16) {
+            const float4 wa = w4[2 * cc], wb = w4[2 * cc + 1];
+            ffma2(acc[0], acc[1], wa.x, wa.y, fmaxf(v[8 * c], 0.f), fmaxf(v[8 * c + 1], 0.f));
+            ffma2(acc[2], acc[3], wa.z, wa.w, fmaxf(v[8 * c + 2], 0.f), fmaxf(v[8 * c + 3], 0.f));
+            ffma2(acc[4], acc[5], wb.x, wb.y, fmaxf(v[8 * c + 4], 0.f), fmaxf(v[8 * c + 5], 0.f));
+            ffma2(acc[6], acc[7], wb.z, wb.w, fmaxf(v[8 * c + 6], 0.f), fmaxf(v[8 * c + 7], 0.f));
+          }
         }
       }
       const float sc = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
@@ -871,8 +969,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         const int blk = w.t * kTcTileBlocks + q * 32 + lane;
         if (nb > sh.topk && blk < nb) a.scores[static_cast<size_t>(row0 + j) * a.ld + blk] = sc;
       }
-      walker_next(w, a, n_groups);
+      walker_next(w, a, chunk, lane);
     }
+    cp_async_wait<0>();  // a weight prefetch may still be in flight
   }
   tc_fence_before();
   __syncthreads();
@@ -946,7 +1045,12 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   a.npad = (a.G * sh.h_idx + 15) / 16 * 16;
   a.hp = (a.G == 1) ? a.npad : sh.h_idx;
   a.ncols = pow2_at_least(a.npad);
-  a.tmem_cols = sh.idx_fp8 ? pow2_at_least(2 * a.ncols + kMaxCStages * sh.d_idx / 2) : 2 * a.ncols;
+  // as many accumulators (4, else 2) as fit in the SM's 512 TMEM columns beside
+  // the MX A stages: the MMA then runs further ahead of the epilogue and frees
+  // its copy-ring stages sooner
+  const int mx_cols = sh.idx_fp8 ? kMaxCStages * sh.d_idx / 2 : 0;
+  a.acc_log2 = kMaxAcc * a.ncols + mx_cols <= 512 ? 2 : 1;
+  a.tmem_cols = pow2_at_least((1 << a.acc_log2) * a.ncols + mx_cols);
   if (a.tmem_cols > 512) return cudaErrorInvalidValue;
   a.bpp_log2 = sh.log2_page - sh.log2_ratio;
   a.seq_ids = seq_ids;

@@ -14,9 +14,10 @@
 // is the number of ties at T that must be taken. A stable compaction emits, in
 // ascending block order, every block with key > T and the lowest-indexed blocks
 // with key == T: exactly the top-K under (score desc, index asc).
-// Rows of up to 16k blocks keep their keys in registers and compact through
-// bitmaps; longer rows stage their keys in shared memory (or, past that, read
-// them from global memory). The selection stays on the device, so a step that
+// Rows of up to 16k blocks keep their keys in registers (each thread a run of
+// consecutive blocks) and compact with one block scan of per-thread counts;
+// longer rows stage their keys in shared memory (or, past that, read them from
+// global memory). The selection stays on the device, so a step that
 // contains it can be captured in a CUDA graph.
 #include "qsa_internal.cuh"
 
@@ -32,6 +33,16 @@ constexpr int kDigit = 11;
 constexpr int kBins = 1 << kDigit;
 constexpr int kBinsPerThread = kBins / kSelThreads;
 constexpr int kBatch = 8;  // keys a thread loads before it histograms them
+
+// Inclusive prefix sum over a warp.
+__device__ __forceinline__ int warp_incl_scan_sel(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
 
 // Exclusive prefix sums over the CTA of a pair of counts, with one barrier: every
 // warp scans the per-warp totals itself. Two calls must be separated by a barrier
@@ -272,80 +283,54 @@ __device__ __forceinline__ void select_row(Src src, int n, int K, uint32_t range
 }
 
 // ---------------------------------------------------------------------------
-// Rows of at most NV * 4 * kSelThreads blocks: thread t holds the keys of
-// blocks 4 * (v * kSelThreads + t) + j (v < NV, j < 4) in registers for the
-// whole selection, so the histogram and the candidate gather are one pass each
-// with independent work per thread. The compaction marks the blocks above the
-// threshold, and the ties at it, in two bitmaps; one scan over the bitmap words
-// (at most 512) then emits the selected blocks in index order.
+// Rows of at most 4 * NV * kSelThreads blocks: thread t holds the keys of the
+// 4 * NV consecutive blocks 4NV*t .. 4NV*t + 4NV - 1 in registers for the whole
+// selection. Warp reductions use redux.sync; the candidates of the chosen digit
+// are gathered with one shared atomic per warp; the compaction is one block
+// scan of each thread's counts above and at the threshold, after which every
+// thread writes its own selected blocks in index order (no bitmaps, no
+// atomics). Barriers: range 1, histogram 1, digit search 2, candidates 1,
+// ranking 1, compaction scan 1.
 // ---------------------------------------------------------------------------
-constexpr int kMaxBitmapWords = 16 * kSelThreads / 32;  // rows of up to 16k blocks
-
-// Candidates of the chosen digit: a warp with any candidate reserves its slots
-// with one atomic.
-__device__ __forceinline__ void offer_candidate(uint32_t k, bool c, uint32_t *cand, int *s_ncand) {
-  const unsigned bal = __ballot_sync(0xffffffffu, c);
-  if (bal == 0u) return;
-  const int lane = threadIdx.x & 31;
-  const int leader = __ffs(bal) - 1;
-  int off = 0;
-  if (lane == leader) off = atomicAdd(s_ncand, __popc(bal));
-  off = __shfl_sync(0xffffffffu, off, leader);
-  const int pos = off + __popc(bal & ((1u << lane) - 1u));
-  if (c && pos < kCandMax) cand[pos] = k;
-}
-
 template <int NV>
 __device__ __forceinline__ void select_in_registers(const float *__restrict__ srow, int n, int K,
                                                     int32_t *__restrict__ out, uint32_t *keys,
                                                     uint32_t *cand, int *hist, int2 *scan_tmp, int *s_res,
-                                                    int *s_ncand, uint32_t *red_min, uint32_t *red_max,
-                                                    uint32_t *sel_bits, uint32_t *tie_bits) {
+                                                    int *s_ncand, uint32_t *red_min, uint32_t *red_max) {
+  constexpr int NK = 4 * NV;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n4 = (n + 3) >> 2;  // 16-byte groups covering the row (ld is a multiple of 4)
-  const float4 *s4 = reinterpret_cast<const float4 *>(srow);
-  uint32_t d[NV][4];
+  const int x0 = NK * tid;  // first block of this thread
+  // 16-byte loads: ld is a multiple of 4, so a group that starts below n lies in the row
+  const float4 *s4 = reinterpret_cast<const float4 *>(srow) + NV * tid;
+  uint32_t d[NK];
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
-    const int x = v * kSelThreads + tid;
     float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (x < n4) f = s4[x];
-    d[v][0] = score_key(f.x);
-    d[v][1] = score_key(f.y);
-    d[v][2] = score_key(f.z);
-    d[v][3] = score_key(f.w);
+    if (x0 + 4 * v < n) f = s4[v];
+    d[4 * v] = score_key(f.x);
+    d[4 * v + 1] = score_key(f.y);
+    d[4 * v + 2] = score_key(f.z);
+    d[4 * v + 3] = score_key(f.w);
   }
-  auto valid = [&](int v, int j) { return 4 * (v * kSelThreads + tid) + j < n; };
+  auto valid = [&](int j) { return x0 + j < n; };
   uint32_t kmin = 0xffffffffu, kmax = 0u;
 #pragma unroll
-  for (int v = 0; v < NV; ++v)
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (valid(v, j)) {
-        kmin = min(kmin, d[v][j]);
-        kmax = max(kmax, d[v][j]);
-      }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  }
+  for (int j = 0; j < NK; ++j)
+    if (valid(j)) {
+      kmin = min(kmin, d[j]);
+      kmax = max(kmax, d[j]);
+    }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
   if (lane == 0) {
     red_min[warp] = kmin;
     red_max[warp] = kmax;
   }
   __syncthreads();
-  kmin = lane < kSelWarps ? red_min[lane] : 0xffffffffu;
-  kmax = lane < kSelWarps ? red_max[lane] : 0u;
+  kmin = __reduce_min_sync(0xffffffffu, lane < kSelWarps ? red_min[lane] : 0xffffffffu);
+  kmax = __reduce_max_sync(0xffffffffu, lane < kSelWarps ? red_max[lane] : 0u);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  }
-#pragma unroll
-  for (int v = 0; v < NV; ++v)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) d[v][j] -= kmin;  // invalid entries are never read
+  for (int j = 0; j < NK; ++j) d[j] -= kmin;  // invalid entries are never read
 
   const uint32_t range = kmax - kmin;
   int top = range ? 31 - __clz(range) : -1;
@@ -358,19 +343,28 @@ __device__ __forceinline__ void select_in_registers(const float *__restrict__ sr
     int shift = top + 1 - width;
     const uint32_t dmask = (1u << width) - 1u;
 #pragma unroll
-    for (int v = 0; v < NV; ++v)
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (valid(v, j)) atomicAdd(&hist[d[v][j] >> shift], 1);  // d <= range: the digit fits
+    for (int j = 0; j < NK; ++j)
+      if (valid(j)) atomicAdd(&hist[d[j] >> shift], 1);  // d <= range: the digit fits
     __syncthreads();
     digit_search(shift, dmask, prefix, mask, remaining, hist, scan_tmp, s_res);
     top = shift - 1;
     if (top >= 0) {
+      // the keys of the chosen digit: each warp reserves its slots with one atomic
+      int mine = 0;
 #pragma unroll
-      for (int v = 0; v < NV; ++v)
+      for (int j = 0; j < NK; ++j) mine += (valid(j) && (d[j] & mask) == prefix) ? 1 : 0;
+      const int incl = warp_incl_scan_sel(mine, lane);
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      int base = 0;
+      if (lane == 31 && total > 0) base = atomicAdd(s_ncand, total);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      int pos = base + incl - mine;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          offer_candidate(d[v][j], valid(v, j) && (d[v][j] & mask) == prefix, cand, s_ncand);
+      for (int j = 0; j < NK; ++j)
+        if (valid(j) && (d[j] & mask) == prefix) {
+          if (pos < kCandMax) cand[pos] = d[j];
+          ++pos;
+        }
       __syncthreads();
       const int nc = *s_ncand;
       if (nc <= kDirectMax) {
@@ -406,10 +400,8 @@ __device__ __forceinline__ void select_in_registers(const float *__restrict__ sr
         int m = nc;
         if (nc > kCandMax) {
 #pragma unroll
-          for (int v = 0; v < NV; ++v)
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (valid(v, j)) keys[4 * (v * kSelThreads + tid) + j] = d[v][j];
+          for (int j = 0; j < NK; ++j)
+            if (valid(j)) keys[x0 + j] = d[j];
           __syncthreads();
           list = keys;
           m = n;
@@ -427,43 +419,30 @@ __device__ __forceinline__ void select_in_registers(const float *__restrict__ sr
   const uint32_t thr = prefix;  // the K-th largest key
   const int need = remaining;   // ties at thr to take (>= 1)
 
-  // ---- compaction through the bitmaps (zeroed at kernel start)
+  // ---- compaction: the blocks before this thread's emit pre.x above thr and
+  // min(pre.y, need) ties; its own blocks follow in index order
+  int gt = 0, eq = 0;
 #pragma unroll
-  for (int v = 0; v < NV; ++v)
+  for (int j = 0; j < NK; ++j)
+    if (valid(j)) {
+      gt += d[j] > thr;
+      eq += d[j] == thr;
+    }
+  const int2 pre = block_exclusive_scan2(make_int2(gt, eq), scan_tmp);
+  int o = pre.x + min(pre.y, need);
+  int tie_rank = pre.y;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (!valid(v, j)) continue;
-      const int idx = 4 * (v * kSelThreads + tid) + j;
-      const uint32_t bit = 1u << (idx & 31);
-      if (d[v][j] > thr)
-        atomicOr(&sel_bits[idx >> 5], bit);
-      else if (d[v][j] == thr)
-        atomicOr(&tie_bits[idx >> 5], bit);
-    }
-  __syncthreads();
-  const int n_words = (n + 31) >> 5;  // <= kMaxBitmapWords <= kSelThreads
-  uint32_t sw = 0u, tw = 0u;
-  if (tid < n_words) {
-    sw = sel_bits[tid];
-    tw = tie_bits[tid];
-  }
-  const int2 pre = block_exclusive_scan2(make_int2(__popc(sw), __popc(tw)), scan_tmp);
-  if (tid < n_words) {
-    // the ties before this word come first: take the lowest-indexed `need`
-    const int take = min(max(need - pre.y, 0), __popc(tw));
-    uint32_t taken = 0u, rest = tw;
-    for (int q = 0; q < take; ++q) {
-      const uint32_t low = rest & (0u - rest);
-      taken |= low;
-      rest ^= low;
-    }
-    uint32_t all = sw | taken;
-    int o = pre.x + min(pre.y, need);
-    while (all) {
-      const int b = __ffs(all) - 1;
-      all &= all - 1u;
-      if (o < K) out[o] = 32 * tid + b;
+  for (int j = 0; j < NK; ++j) {
+    if (!valid(j)) continue;
+    if (d[j] > thr) {
+      if (o < K) out[o] = x0 + j;
       ++o;
+    } else if (d[j] == thr) {
+      if (tie_rank < need) {
+        if (o < K) out[o] = x0 + j;
+        ++o;
+      }
+      ++tie_rank;
     }
   }
 }
@@ -528,7 +507,6 @@ select_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__
   __shared__ int2 scan_tmp[kSelWarps];
   __shared__ uint32_t red_min[kSelWarps], red_max[kSelWarps];
   __shared__ int s_res[2], s_ncand;
-  __shared__ uint32_t sel_bits[kMaxBitmapWords], tie_bits[kMaxBitmapWords];
 
   const int row = blockIdx.x;
   const int i = row / R;
@@ -559,24 +537,17 @@ select_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__
 #pragma unroll
   for (int j = 0; j < kBinsPerThread; ++j) hist[kBinsPerThread * tid + j] = 0;
   if (tid == 0) s_ncand = 0;
-  for (int x = tid; x < kMaxBitmapWords; x += kSelThreads) {
-    sel_bits[x] = 0u;
-    tie_bits[x] = 0u;
-  }
   pdl_wait();  // scores come from the score kernel
   pdl_trigger();
   uint32_t *cand = keys + smem_keys;
   const float *srow = scores + static_cast<size_t>(row) * ld;
   // rows up to 16k blocks (64k tokens at ratio 4) keep their keys in registers
   if (n <= 4 * kSelThreads) {
-    select_in_registers<1>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max,
-                           sel_bits, tie_bits);
+    select_in_registers<1>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else if (n <= 8 * kSelThreads) {
-    select_in_registers<2>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max,
-                           sel_bits, tie_bits);
+    select_in_registers<2>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else if (n <= 16 * kSelThreads) {
-    select_in_registers<4>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max,
-                           sel_bits, tie_bits);
+    select_in_registers<4>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else {
     select_general(srow, n, K, out, keys, cand, smem_keys, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   }
