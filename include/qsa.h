@@ -213,6 +213,18 @@ typedef struct qsa_cache {
 /* Message for a status code (static string). */
 const char *qsa_strerror(int status);
 
+/* Test hook of the failure path ("Atlas Flash-Next defect investigations",
+ * Report A, Defect 4: an error is reported, never laundered into success).
+ * Sets the time limit, in nanoseconds, after which an internal wait of the
+ * index-score kernel gives up: the CTA records QSA_ERR_TIMEOUT in the status
+ * word, waits a bounded 2 ms for its own copies and tensor-core work to land,
+ * frees its tensor memory and returns, so the context stays usable. 0 restores
+ * the default (1 s); other values are clamped to [1 us, 10 s]. The value is
+ * read when a launch is issued (a captured graph keeps the value it was
+ * captured with). Returns the previous limit. Meant for tests; a production
+ * caller has no reason to change it. */
+unsigned long long qsa_set_wait_limit_ns(unsigned long long ns);
+
 /* 0 (QSA_OK) if the configuration is in the supported set above, else
  * QSA_ERR_UNSUPPORTED (QSA_ERR_INVALID_ARG for a NULL pointer). */
 int qsa_config_check(const qsa_config *cfg);

@@ -43,6 +43,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "qsa_internal.cuh"
@@ -52,7 +53,7 @@ namespace {
 
 constexpr int kTcTileBlocks = 128;
 constexpr int kTcMaxGroup = 4;
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s: the default limit of every wait
 
 // ---- PTX wrappers (tcgen05 / mbarrier / TMA) --------------------------------
 
@@ -74,15 +75,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 // Test for the completion of the phase with the given parity; while it is not
 // complete the thread may be suspended (not polling) until it completes or
-// kSuspendNs pass.
-constexpr uint32_t kSuspendNs = 100000;  // 100 us
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// suspend_ns pass.
+constexpr uint32_t kSuspendNs = 100000;  // 100 us, at most
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "r"(bar), "r"(parity), "r"(suspend_ns)
       : "memory");
   return ok != 0;
 }
@@ -241,6 +242,7 @@ struct TcArgs {
   float *scores;
   int ld;
   int32_t *status;
+  unsigned long long wait_limit_ns;  // limit of every mbarrier wait (qsa_set_wait_limit_ns)
   int n_groups;        // groups of rows (n_seq * groups_per_seq)
   int q_in_step;       // the queries are written by this step's first kernel: load them only
                        // after the dependency wait
@@ -268,19 +270,31 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 // Bounded wait that also gives up when another role has aborted the CTA.
+// limit_ns: the wait's time limit (kWaitLimitNs unless a test shortened it); the
+// suspend hint stays well below it, so an expired wait is noticed in time.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                                   int32_t *status) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                                   int32_t *status, unsigned long long limit_ns) {
+  const uint32_t hint = static_cast<uint32_t>(limit_ns / 4 < kSuspendNs ? limit_ns / 4 : kSuspendNs);
+  if (mbar_try_wait(bar, parity, hint)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, hint)) return true;
     if (*abort_flag) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       report(status, QSA_ERR_TIMEOUT);
       return false;
     }
   }
+}
+
+// The same wait taken by a whole warp (every lane polls): the verdict is made
+// warp-uniform, so a lane that saw the phase complete cannot run on while
+// another lane gave up (the warp's later full-mask shuffles and syncs would
+// then never complete).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                               int32_t *status, unsigned long long limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait_or_abort(bar, parity, abort_flag, status, limit_ns));
 }
 
 // Tiles of 128 blocks that group g needs, its sequence's pos0 being p0 (0 when
@@ -626,7 +640,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         const int bs = gseq & 1;
         // at most the first group's query load waits for the dependency wait
         if (a.q_in_step && !waited && gseq >= 1) wait_now();
-        if (gseq >= 2 && !mbar_wait_or_abort(b_empty(bs), ((gseq >> 1) - 1) & 1, abort_flag, a.status)) break;
+        if (gseq >= 2 && !mbar_wait_warp(b_empty(bs), ((gseq >> 1) - 1) & 1, abort_flag, a.status, a.wait_limit_ns)) break;
         if (a.q_in_step && !waited) {
           pend = true;
           pend_bs = bs;
@@ -650,7 +664,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         const int s = (k % NR) * S_R + kr % S_R;
         if (!waited && (kr >= S_R || (w.t + it + 1) * kTcTileBlocks > cur.nblk_old)) wait_now();
         if (NR == 2 && (k & 1) != par) continue;  // the other producer's tile
-        if (kr >= S_R && !mbar_wait_or_abort(a_empty(s), ((kr / S_R) - 1) & 1, abort_flag, a.status)) {
+        if (kr >= S_R && !mbar_wait_warp(a_empty(s), ((kr / S_R) - 1) & 1, abort_flag, a.status, a.wait_limit_ns)) {
           ok = false;
           break;
         }
@@ -679,18 +693,18 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       const int buf = k & acc_mask;
       bool ok = true;
       if (lane == 0)
-        ok = FP8 ? mbar_wait_or_abort(c_full(s), (k / N_OPD) & 1, abort_flag, a.status)
-                 : mbar_wait_or_abort(a_full(s), (k / S) & 1, abort_flag, a.status);
+        ok = FP8 ? mbar_wait_or_abort(c_full(s), (k / N_OPD) & 1, abort_flag, a.status, a.wait_limit_ns)
+                 : mbar_wait_or_abort(a_full(s), (k / S) & 1, abort_flag, a.status, a.wait_limit_ns);
       int bs = gseq & 1;
       if (w.g != cur_g) {
         ++gseq;
         bs = gseq & 1;
         if (lane == 0 && ok)
-          ok = mbar_wait_or_abort(FP8 ? q_ready(bs) : b_full(bs), (gseq >> 1) & 1, abort_flag, a.status);
+          ok = mbar_wait_or_abort(FP8 ? q_ready(bs) : b_full(bs), (gseq >> 1) & 1, abort_flag, a.status, a.wait_limit_ns);
         cur_g = w.g;
       }
       if (lane == 0 && ok && k >= n_acc)
-        ok = mbar_wait_or_abort(t_empty(buf), ((k >> a.acc_log2) - 1) & 1, abort_flag, a.status);
+        ok = mbar_wait_or_abort(t_empty(buf), ((k >> a.acc_log2) - 1) & 1, abort_flag, a.status, a.wait_limit_ns);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       if (lane == 0) {
@@ -742,7 +756,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         // (c ^ (r % 8)) of the row's 128-byte line in half c / 8 of the slot.
         ++gq;
         const int bs = gq & 1;
-        if (!mbar_wait_or_abort(b_full(bs), (gq >> 1) & 1, abort_flag, a.status)) break;
+        if (!mbar_wait_warp(b_full(bs), (gq >> 1) & 1, abort_flag, a.status, a.wait_limit_ns)) break;
         const int units = a.npad * (DI / 32);
         for (int u = cw * 32 + lane; u < units; u += kConvWarps * 32) {
           const int r = u / (DI / 32), blk = u - r * (DI / 32);
@@ -782,8 +796,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       }
       const int kr = k >> 1;
       const int s = rc * S_R + kr % S_R, c = k % N_OPD;
-      if (!mbar_wait_or_abort(a_full(s), (kr / S_R) & 1, abort_flag, a.status)) break;
-      if (k >= N_OPD && !mbar_wait_or_abort(c_empty(c), ((k / N_OPD) - 1) & 1, abort_flag, a.status)) break;
+      if (!mbar_wait_warp(a_full(s), (kr / S_R) & 1, abort_flag, a.status, a.wait_limit_ns)) break;
+      if (k >= N_OPD && !mbar_wait_warp(c_empty(c), ((k / N_OPD) - 1) & 1, abort_flag, a.status, a.wait_limit_ns)) break;
       const uint32_t src = r_u + s * R_STAGE;
       uint32_t scl;
       if (DI == 128)
@@ -931,7 +945,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
         nw_g = chunk_next_group(chunk, w.g, lane);
         fetch_weights(nw_g, cur_half ^ 1);
       }
-      if (!mbar_wait_or_abort(t_full(buf), (k >> a.acc_log2) & 1, abort_flag, a.status)) break;
+      if (!mbar_wait_warp(t_full(buf), (k >> a.acc_log2) & 1, abort_flag, a.status, a.wait_limit_ns)) break;
       tc_fence_after();
       const uint32_t lane_addr =
           tmem + buf * a.ncols + (static_cast<uint32_t>(q * 32) << 16) + j * a.hp;
@@ -985,6 +999,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
 }
+
+// The limit every mbarrier wait of the scorer gives up after (1 s by default);
+// qsa_set_wait_limit_ns lets a test shorten it to make a wait expire.
+std::atomic<unsigned long long> g_wait_limit_ns{kWaitLimitNs};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::once_flag once;
@@ -1063,6 +1081,7 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
   a.scores = scores;
   a.ld = ld;
   a.status = status;
+  a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
 
   CUtensorMap tm_q;
   const long long total_rows = static_cast<long long>(n_seq) * R;
@@ -1111,3 +1130,13 @@ cudaError_t launch_score_tc(const Shape &sh, int n_seq, int R, const int32_t *se
 }
 
 }  // namespace qsa
+
+// Test hook for the failure path: the limit of the scorer's mbarrier waits, in
+// nanoseconds (0 restores the default of 1 s; other values are clamped to
+// [1 us, 10 s]). Read when a launch is issued; returns the previous limit.
+extern "C" unsigned long long qsa_set_wait_limit_ns(unsigned long long ns) {
+  unsigned long long v = ns == 0 ? qsa::kWaitLimitNs : ns;
+  if (v < 1000ull) v = 1000ull;
+  if (v > 10000000000ull) v = 10000000000ull;
+  return qsa::g_wait_limit_ns.exchange(v);
+}

@@ -42,7 +42,7 @@ EXPORTED = ("qsa_strerror", "qsa_config_check", "qsa_workspace_bytes", "qsa_appe
             "qsa_gather_attn_static", "qsa_max_attend_tokens", "qsa_gather_attn_reuse",
             "qsa_decode_reuse", "qsa_append_pre", "qsa_pre_index_q", "qsa_workspace_bytes_pre",
             "qsa_decode_pre", "qsa_idxblk_page_bytes", "qsa_quantize_index_q", "qsa_append_ex",
-            "qsa_workspace_bytes_ex", "qsa_decode_ex")
+            "qsa_workspace_bytes_ex", "qsa_decode_ex", "qsa_set_wait_limit_ns")
 QSA_STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -121,6 +121,8 @@ LIB.qsa_gather_attn.restype = _I
 LIB.qsa_gather_attn.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 LIB.qsa_gather_attn_static.restype = _I
 LIB.qsa_gather_attn_static.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P]
+LIB.qsa_set_wait_limit_ns.restype = ctypes.c_ulonglong
+LIB.qsa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
 LIB.qsa_max_attend_tokens.restype = _I
 LIB.qsa_max_attend_tokens.argtypes = [_CFG]
 LIB.qsa_gather_attn_reuse.restype = _I
@@ -341,6 +343,12 @@ def qsa_gather_attn(cfg: Config, rows: Rows, cache: PagedCache, q, sel, n_sel, o
                              _ptr(out, torch.bfloat16), _ptr(ws), ws.numel() * ws.element_size(),
                              _ptr(status, torch.int32), _stream(stream))
     _check(rc, "qsa_gather_attn")
+
+
+def qsa_set_wait_limit_ns(ns: int) -> int:
+    """Test hook: the index-score kernel's wait limit in ns (0 = default 1 s);
+    returns the previous limit."""
+    return int(LIB.qsa_set_wait_limit_ns(ctypes.c_ulonglong(ns)))
 
 
 def qsa_gather_attn_static(cfg: Config, rows: Rows, cache: PagedCache, q, sel, n_sel, out,

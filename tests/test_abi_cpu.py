@@ -23,7 +23,8 @@ def Q():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|int|size_t)\s*(qsa_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|int|size_t|unsigned\s+long\s+long)\s*(qsa_\w+)\s*\(",
+                                 text, re.M)))
 
 
 def test_every_declared_symbol_is_exported(Q):
@@ -255,3 +256,14 @@ def test_mrope_arguments_checked_on_host(Q):
     assert append_ex(attn((11, 11, 11)), rows, no_pool) == Q.QSA_ERR_INVALID_ARG
     assert append_ex(attn((11, 11, 10)), rows_mis, no_pool) == Q.QSA_ERR_INVALID_ARG
     assert append_ex(attn((11, 11, 10)), rows, no_pool) == Q.QSA_ERR_CAPACITY
+
+
+def test_wait_limit_hook_clamps_and_restores(Q):
+    """The failure-path test hook (no GPU needed): 0 restores 1 s, values clamp to
+    [1 us, 10 s], and each call returns the previous limit."""
+    first = Q.qsa_set_wait_limit_ns(0)
+    assert Q.qsa_set_wait_limit_ns(5) == 1_000_000_000
+    assert Q.qsa_set_wait_limit_ns(20_000_000_000) == 1_000        # 5 ns clamped up to 1 us
+    assert Q.qsa_set_wait_limit_ns(0) == 10_000_000_000            # clamped down to 10 s
+    assert Q.qsa_set_wait_limit_ns(first) == 1_000_000_000
+    Q.qsa_set_wait_limit_ns(0)
