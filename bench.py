@@ -53,9 +53,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--n-batches", type=int, default=N_BATCHES,
                     help="rotating batches of 32 sequences (fewer: smaller device footprint, for profiling)")
-    ap.add_argument("--legs", default="decode,prefill",
+    ap.add_argument("--legs", default="decode,prefill,ragged,verify",
                     help="comma list of legs to run: decode (the headline), prefill (chunked-prefill "
-                         "index scoring against the bf16 tensor peak, and the fused prefill step)")
+                         "index scoring against the bf16 tensor peak, and the fused prefill step), ragged "
+                         "(batch 64, log-uniform prefixes), verify (R = 3 verify, rewind, 4 decode steps)")
     ap.add_argument("--prefill-steps", type=int, default=10)
     ap.add_argument("--reuse-steps", type=int, default=300,
                     help="decode steps with a reused selection (MTP draft steps); 0 skips the leg")
@@ -71,6 +72,10 @@ def parse():
     ap.add_argument("--window-steps", type=int, default=300,
                     help="decode steps with a 128-token always-kept local window; 0 skips")
     ap.add_argument("--prefill-warmup", type=int, default=3)
+    ap.add_argument("--ragged-steps", type=int, default=200, help="timed steps of the ragged-decode leg")
+    ap.add_argument("--ragged-warmup", type=int, default=5)
+    ap.add_argument("--verify-cycles", type=int, default=50, help="timed cycles of the verify + rewind leg")
+    ap.add_argument("--verify-warmup", type=int, default=3)
     return ap.parse_args()
 
 
@@ -994,6 +999,211 @@ def run_prefill(args, dev):
 
 
 # ---------------------------------------------------------------------------
+# ragged decode (batch 64, log-uniform prefixes) and verify + rewind legs
+# ---------------------------------------------------------------------------
+
+def fill_prefixes(Q, S, torch, cfg, sh, wl, cache, prefixes, status, dev, seqs=None):
+    """Every sequence's prefix through the library's own append (8192 tokens a call)."""
+    seqs = list(range(len(prefixes))) if seqs is None else seqs
+    for s_, n in zip(seqs, prefixes):
+        a = 0
+        while a < n:
+            m = min(8192, n - a)
+            k, v, ix = S.token_rows(sh, wl.seed, s_, torch.arange(a, a + m), device=dev)
+            Q.qsa_append(cfg, Q.Rows(torch.tensor([s_], device=dev), torch.tensor([a], device=dev, dtype=torch.int32),
+                                     m), cache, k, v, ix, status)
+            a += m
+
+
+def run_ragged(args, dev):
+    """Ragged decode (batch 64, prefixes log-uniform in [512, 131072] with the
+    inert-bound boundary 2050 / 2051 / 2052 and dense prefixes forced in): one
+    fused qsa_decode of the 64 rows per step, a CUDA graph replayed with the
+    positions advancing on the device. A step reads about 0.34 GB (more than L2),
+    so the data comes from HBM. Bytes per row from the method's definition
+    (keys only for rows past the inert bound)."""
+    import torch
+
+    from indexer_selected_sparse_gb300 import qsa as Q
+    from indexer_selected_sparse_gb300 import synth as S
+
+    wl = S.workload(3)
+    sh = wl.shapes
+    cfg = Q.Config.of(sh)
+    B = wl.n_seq
+    W, K = max(args.ragged_warmup, 3), max(args.ragged_steps, 1)
+    max_pages = math.ceil((max(wl.prefixes) + W + K + 8) / sh.page_size)
+    cache = Q.PagedCache(cfg, S.page_table(wl.seed, B, max_pages, contiguous=False), B * max_pages, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    fill_prefixes(Q, S, torch, cfg, sh, wl, cache, wl.prefixes, status, dev)
+    ids = torch.arange(B, dtype=torch.int32, device=dev)
+    pos0 = torch.tensor(wl.prefixes, dtype=torch.int32, device=dev)
+    k, v, ix = zip(*[S.token_rows(sh, wl.seed, s_, torch.tensor([p]), device=dev) for s_, p in enumerate(wl.prefixes)])
+    q, qi, w = zip(*[S.query_rows(sh, wl.seed, s_, torch.tensor([p]), device=dev) for s_, p in enumerate(wl.prefixes)])
+    cat = lambda xs: torch.cat(xs).contiguous()
+    k, v, ix, q, qi, w = map(cat, (k, v, ix, q, qi, w))
+    out = torch.empty(B, sh.n_q_heads, sh.head_dim, dtype=torch.bfloat16, device=dev)
+    ws = Q.workspace(cfg, B, cache.max_blocks, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        Q.qsa_decode(cfg, Q.Rows(ids, pos0, 1, advance=True), cache, k, v, ix, qi, w, q, out, ws, status,
+                     stream=stream)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st == 0, f"device status {st}: {Q.qsa_strerror(st)}"
+    ms = e0.elapsed_time(e1) / K
+    # timed rows: every sequence at prefixes + W .. prefixes + W + K - 1 (visible one more)
+    visibles = [p + W + t + 1 for t in range(K) for p in wl.prefixes]
+    work = sum_work(sh, visibles)
+    step_bytes = (work["score_bytes"] + work["attn_bytes"] + work["append_bytes"]) / K
+    hbm_gbs, _, peak_kind = measured_peaks()
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    dense = sum(1 for p in wl.prefixes if (p + W + 1) // sh.ratio <= sh.topk)
+    return {"workload": wl.name, "batch": B, "steps": K, "warmup": W, "ms_per_step": round(ms, 5),
+            "rows_per_s": round(B / (ms * 1e-3), 1), "bytes_per_step": int(step_bytes),
+            "achieved_gbs": round(gbs, 1), "hbm_roofline_frac": round(gbs / hbm_gbs, 4),
+            "peak_kind": peak_kind + " (hbm_gbs, copy)",
+            "rows_dense": dense, "prefix_range": [min(wl.prefixes), max(wl.prefixes)],
+            "bytes": "per row: compressed keys (rows past the inert bound), q_idx, w, K+V of the token set, q, o, "
+                     "appended rows",
+            "timing": f"{K} steps after {W} warm-up, one CUDA graph per step, positions advanced on the device; "
+                      f"{step_bytes / 1e9:.2f} GB per step (more than L2)"}
+
+
+def token_count(sel_rows, visibles, ratio):
+    """Distinct tokens of a sequence's rows: each row's selected blocks (expanded
+    to their ratio tokens) plus its tail [n_blk * ratio, visible)."""
+    toks = set()
+    for sel, vis in zip(sel_rows, visibles):
+        n_blk = vis // ratio
+        for b in sel:
+            if b >= 0:
+                toks.update(range(b * ratio, b * ratio + ratio))
+        toks.update(range(n_blk * ratio, vis))
+    return len(toks)
+
+
+def run_verify(args, dev):
+    """Speculative verify + rewind (batch 16, prefix 65536): a cycle is one fused
+    qsa_decode of R = 3 causal rows per sequence (2 drafts + 1), the rewind of
+    the rejected rows (0..2 per sequence, seeded), 4 decode steps on fresh rows
+    at the re-used positions, and a rewind back to the start so the cycle repeats
+    on the same data; one CUDA graph per cycle. Bytes per SURVEY's verify rule:
+    a sequence's compressed keys once for its 3 verify rows, K+V once per distinct
+    token of their sets (the union, from the step's own selections), plus the
+    decode rows as in the decode leg."""
+    import torch
+
+    from indexer_selected_sparse_gb300 import qsa as Q
+    from indexer_selected_sparse_gb300 import synth as S
+
+    wl = S.workload(4)
+    sh = wl.shapes
+    cfg = Q.Config.of(sh)
+    B, R, p = wl.n_seq, wl.rows_per_seq, wl.prefixes[0]
+    D = wl.extra["decode_after"]
+    rej = S.reject_counts(wl.seed, B)
+    max_pages = math.ceil((p + R + D + 8) / sh.page_size)
+    cache = Q.PagedCache(cfg, S.page_table(wl.seed, B, max_pages, contiguous=False), B * max_pages, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    fill_prefixes(Q, S, torch, cfg, sh, wl, cache, wl.prefixes, status, dev)
+    ids = torch.arange(B, dtype=torch.int32, device=dev)
+    cat = lambda xs: torch.cat(xs).contiguous()
+
+    def inputs(positions, epoch):
+        rows = [S.token_rows(sh, wl.seed, s_, torch.tensor(ps), epoch=epoch, device=dev) for s_, ps in positions]
+        qs = [S.query_rows(sh, wl.seed, s_, torch.tensor(ps), epoch=epoch, device=dev) for s_, ps in positions]
+        k, v, ix = (cat([r[i] for r in rows]) for i in range(3))
+        q, qi, w = (cat([x[i] for x in qs]) for i in range(3))
+        return dict(k=k, v=v, idx=ix, q=q, q_idx=qi, w=w)
+
+    ver = inputs([(s_, list(range(p, p + R))) for s_ in range(B)], 0)
+    acc = [R - r for r in rej]
+    dec = [inputs([(s_, [p + acc[s_] + j]) for s_ in range(B)], 1) for j in range(D)]
+    pos_v = torch.full((B,), p, dtype=torch.int32, device=dev)
+    pos_d = [torch.tensor([p + a + j for a in acc], dtype=torch.int32, device=dev) for j in range(D)]
+    drop_rej = torch.tensor(rej, dtype=torch.int32, device=dev)
+    drop_all = torch.tensor([a + D for a in acc], dtype=torch.int32, device=dev)
+    out_v = torch.empty(B * R, sh.n_q_heads, sh.head_dim, dtype=torch.bfloat16, device=dev)
+    out_d = torch.empty(B, sh.n_q_heads, sh.head_dim, dtype=torch.bfloat16, device=dev)
+    sel_v = torch.empty(B * R, cfg.topk, dtype=torch.int32, device=dev)
+    nsel_v = torch.empty(B * R, dtype=torch.int32, device=dev)
+    ws = Q.workspace(cfg, B * R, cache.max_blocks, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def cycle():
+        Q.qsa_decode(cfg, Q.Rows(ids, pos_v, R), cache, ver["k"], ver["v"], ver["idx"], ver["q_idx"], ver["w"],
+                     ver["q"], out_v, ws, status, sel_out=sel_v, n_sel_out=nsel_v, stream=stream)
+        Q.qsa_rewind(cfg, ids, drop_rej, cache.ingested, status, stream=stream)
+        for j in range(D):
+            d = dec[j]
+            Q.qsa_decode(cfg, Q.Rows(ids, pos_d[j], 1), cache, d["k"], d["v"], d["idx"], d["q_idx"], d["w"], d["q"],
+                         out_d, ws, status, stream=stream)
+        Q.qsa_rewind(cfg, ids, drop_all, cache.ingested, status, stream=stream)
+
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        cycle()
+    torch.cuda.synchronize()
+    W, K = max(args.verify_warmup, 3), max(args.verify_cycles, 1)
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st == 0, f"device status {st}: {Q.qsa_strerror(st)}"
+    assert cache.ingested.cpu().tolist() == [p] * B
+    ms = e0.elapsed_time(e1) / K
+    # bytes of a cycle: verify rows with the SURVEY rule, then the decode rows
+    sel_h = sel_v.cpu().tolist()
+    kb = key_bytes(sh, "bf16")
+    ver_bytes = 0
+    for s_ in range(B):
+        vis = [p + j + 1 for j in range(R)]
+        n_blk_last = vis[-1] // sh.ratio
+        ver_bytes += n_blk_last * kb if n_blk_last > sh.topk else 0
+        ver_bytes += R * (sh.n_idx_heads * sh.idx_dim * 2 + 4 * sh.n_idx_heads)
+        ver_bytes += token_count(sel_h[s_ * R:(s_ + 1) * R], vis, sh.ratio) * sh.n_kv_heads * sh.head_dim * 4
+        ver_bytes += R * (2 * sh.n_q_heads * sh.head_dim * 2 + (2 * sh.n_kv_heads * sh.head_dim + sh.idx_dim) * 2)
+    dw = sum_work(sh, [p + acc[s_] + j + 1 for j in range(D) for s_ in range(B)])
+    cyc_bytes = ver_bytes + dw["score_bytes"] + dw["attn_bytes"] + dw["append_bytes"]
+    hbm_gbs, _, peak_kind = measured_peaks()
+    rows = B * R + B * D
+    gbs = cyc_bytes / (ms * 1e-3) / 1e9
+    return {"workload": wl.name, "cycles": K, "warmup": W, "ms_per_cycle": round(ms, 5),
+            "rows_per_cycle": rows, "rows_per_s": round(rows / (ms * 1e-3), 1), "bytes_per_cycle": int(cyc_bytes),
+            "achieved_gbs": round(gbs, 1), "hbm_roofline_frac": round(gbs / hbm_gbs, 4),
+            "peak_kind": peak_kind + " (hbm_gbs, copy)", "rejected": rej,
+            "cycle": f"verify ({B} x {R} causal rows) -> rewind rejected -> {D} decode steps -> rewind to the start; "
+                     "one CUDA graph per cycle",
+            "bytes": "verify: keys once per sequence, K+V once per distinct token of its rows (union), q_idx, w, q, "
+                     "o and appends per row; decode rows as in the decode leg"}
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle (cpu_baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
 
@@ -1050,6 +1260,59 @@ def _oracle_worker(job):
     return times
 
 
+def _prefill_oracle_worker(job):
+    """Runs in a spawned process: the chunked-prefill sequence (prefix + chunk,
+    every token appended, as the fused step appends the chunk before any row
+    attends) built from the seeded generator (untimed), then the oracle row by
+    row for the rows given (score, select, attend), each timed."""
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["OMP_NUM_THREADS"] = "1"
+    os.environ["MKL_NUM_THREADS"] = "1"
+    import numpy as np
+    import torch
+    torch.set_num_threads(1)
+    from indexer_selected_sparse_gb300 import synth as S
+    from oracle import qsa_oracle as O
+
+    rows, wl_id = job
+    wl = S.workload(wl_id)
+    sh = wl.shapes
+    p, C = wl.prefixes[0], wl.rows_per_seq
+    n = p + C
+
+    def b(t):
+        return t.contiguous().view(torch.int16).numpy().astype(np.uint16)
+
+    k, v, ix = S.token_rows(sh, wl.seed, 0, torch.arange(n))
+    st = O.SeqState(sh.ratio, sh.n_kv_heads, sh.head_dim, sh.idx_dim, n)
+    st.append(0, b(k), b(v), b(ix))
+    q, qi, w = S.query_rows(sh, wl.seed, 0, torch.tensor([p + j for j in rows]))
+    times = []
+    for r, j in enumerate(rows):
+        t0 = time.perf_counter()
+        O.attend_row(st, p + j, b(qi[r]), w[r].numpy(), b(q[r]), sh.topk)
+        times.append((t0, time.perf_counter()))
+    return times
+
+
+def prefill_cpu_baseline(stride=16):
+    """The oracle on every stride-th row of the chunked-prefill workload, over up
+    to 16 single-thread worker processes; rows/s as for the decode baseline."""
+    import multiprocessing as mp
+    wl = __import__("indexer_selected_sparse_gb300.synth", fromlist=["synth"]).workload(PREFILL_WORKLOAD_ID)
+    rows = list(range(0, wl.rows_per_seq, stride))
+    n = min(os.cpu_count() or 1, 16, len(rows))
+    jobs = [(rows[i::n], PREFILL_WORKLOAD_ID) for i in range(n)]
+    with mp.get_context("spawn").Pool(n) as pool:
+        res = pool.map(_prefill_oracle_worker, jobs)
+    per_row = statistics.median([t1 - t0 for r in res for (t0, t1) in r])
+    return {"value": round(pool_rate(res), 2), "unit": "rows/s", "cores": n, "kind": "oracle",
+            "sample": f"a 1/{stride} subsample: rows 0, {stride}, 2*{stride}, ... of the 8193-row chunk "
+                      f"({len(rows)} rows) over {n} worker processes (1 BLAS thread each); each row = score, "
+                      "select, attend over the whole appended chunk; rate = sum of the workers' own rates",
+            "single_thread_rows_per_s": round(1.0 / per_row, 2), "cpu": cpu_model()}
+
+
 def oracle_pool_run(n_workers, prefix, n_warm, rows_per_worker):
     import multiprocessing as mp
     ctx = mp.get_context("spawn")
@@ -1071,18 +1334,27 @@ def cpu_model():
     return platform.machine()
 
 
+def pool_rate(res):
+    """Rows per second of the worker pool: the sum over workers of each worker's
+    own rate (its rows over the span from its first row's start to its last
+    row's end). The workers' set-up times differ, so a span from the earliest
+    start to the latest end would count their start skew as work time."""
+    rate = 0.0
+    for r in res:
+        span = r[-1][1] - r[0][0]
+        rate += len(r) / span if span > 0 else 0.0
+    return rate
+
+
 def cpu_baseline(rows_per_worker):
     n = min(os.cpu_count() or 1, 16)
     res = oracle_pool_run(n, 32768, 1, rows_per_worker)
-    starts = [r[0][0] for r in res]
-    ends = [r[-1][1] for r in res]
-    wall = max(ends) - min(starts)
     rows = sum(len(r) for r in res)
     per_row = statistics.median([t1 - t0 for r in res for (t0, t1) in r])
-    return {"value": round(rows / wall, 2), "unit": "rows/s", "cores": n, "kind": "oracle",
-            "sample": f"{n} worker processes x {rows_per_worker} decode rows each (1 BLAS thread each), "
-                      f"one sequence per worker at prefix 32768 of the batch-32 x 32k workload; "
-                      f"each row = append + score + select + attend, then rewind",
+    return {"value": round(pool_rate(res), 2), "unit": "rows/s", "cores": n, "kind": "oracle",
+            "sample": f"{rows} decode rows: {n} worker processes x {rows_per_worker} rows each (1 BLAS thread "
+                      f"each), one sequence per worker at prefix 32768 of the batch-32 x 32k workload; each row = "
+                      f"append + score + select + attend, then rewind; rate = sum of the workers' own rates",
             "single_thread_rows_per_s": round(1.0 / per_row, 2), "cpu": cpu_model()}
 
 
@@ -1095,11 +1367,9 @@ def run_reference(args):
     # a step = one decode row (of the batch's 32) on the CPU; the K steps are
     # spread over n worker processes that run in parallel
     res = oracle_pool_run(n, 32768, max(1, math.ceil(W / n)), math.ceil(K / n))
-    starts = [r[0][0] for r in res]
-    ends = [r[-1][1] for r in res]
-    wall = max(ends) - min(starts)
     rows = sum(len(r) for r in res)
-    value = rows / wall
+    value = pool_rate(res)   # the same method as the GPU arm's cpu_baseline
+    wall = rows / value
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "rows/s",
             "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(wall / K * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -1107,7 +1377,9 @@ def run_reference(args):
             "config": {"workload": "steady-decode b32 prefix32768 r4 B2048 HI64xdI128 Hq32/Hkv4",
                        "sample": f"each step: one decode row; {rows} rows over {n} CPU worker processes"},
             "cpu_baseline": {"value": round(value, 2), "unit": "rows/s", "cores": n, "kind": "oracle",
-                             "sample": f"{rows} decode rows at prefix 32768 over {n} workers", "cpu": cpu_model()},
+                             "sample": f"{rows} decode rows at prefix 32768: {n} workers x {math.ceil(K / n)} rows "
+                                       "each; rate = sum of the workers' own rates (as the GPU arm's cpu_baseline)",
+                             "cpu": cpu_model()},
             "e2e": {"value": round(value, 2), "unit": "rows/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -1129,15 +1401,22 @@ def main():
             print(json.dumps({"prefill": pre}), flush=True)
         return
     out, rank, world, late = run_gpu(args)
+    import torch
+    ldev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     if "prefill" in legs:
-        import torch
-        out["prefill"] = run_prefill(args, torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))))
+        out["prefill"] = run_prefill(args, ldev)
+    if "ragged" in legs:
+        out["ragged"] = guarded(lambda: run_ragged(args, ldev), None if world == 1 else True, torch)
+    if "verify" in legs:
+        out["verify"] = guarded(lambda: run_verify(args, ldev), None if world == 1 else True, torch)
     if late is not None:
         import torch
         out["attn_options"] = guarded(late, None if world == 1 else True, torch)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(args.oracle_rows)
+            if "prefill" in out:
+                out["prefill"]["cpu_baseline"] = prefill_cpu_baseline()
         else:
             out["cpu_baseline"] = None
         print(json.dumps(out), flush=True)

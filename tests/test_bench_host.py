@@ -110,3 +110,19 @@ def test_packed_step_inputs_are_aligned_disjoint_views():
         v.copy_(t)
     for v, t in zip(views, ts):                                  # nothing overwrote another view
         assert torch.equal(v, t)
+
+
+def test_pool_rate_ignores_worker_start_skew():
+    import bench
+    # two workers, 10 rows each at 0.1 s per row, the second starting 5 s later:
+    # 20 rows/s in all, whatever the skew
+    w1 = [(0.1 * i, 0.1 * (i + 1)) for i in range(10)]
+    w2 = [(5 + 0.1 * i, 5 + 0.1 * (i + 1)) for i in range(10)]
+    assert abs(bench.pool_rate([w1, w2]) - 20.0) < 1e-9
+
+
+def test_token_count_is_the_union_of_the_rows_sets():
+    import bench
+    # ratio 4: row A (V = 10: blocks 0, 1 complete, tail 8..9) selected block 1;
+    # row B (V = 13: 3 blocks, tail 12) selected blocks 1 and 2, -1 padded
+    assert bench.token_count([[1, -1], [1, 2]], [10, 13], 4) == len(set(range(4, 8)) | {8, 9} | set(range(4, 12)) | {12})
