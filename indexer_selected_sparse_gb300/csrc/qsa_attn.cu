@@ -44,7 +44,10 @@ constexpr int kAttnWarps = 4;
 constexpr int kStages = 3;
 constexpr int kSplitSlots = 112;  // 7 stages of 16 slots
 constexpr int kMaxUnitsPerCta = 4;
-constexpr int kPageCache = 2048;  // page-table entries a CTA copies to shared memory
+// page-table entries a CTA copies to shared memory: one region per distinct
+// sequence among its units (two decode rows' 32k-token tables); kept small so
+// that two attention CTAs fit on an SM beside a select CTA
+constexpr int kPageCache = 1040;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int HKV>
@@ -66,7 +69,7 @@ __device__ __forceinline__ int slot_token(int j, int n_body, int log2r, int r, i
 // where its sequence's page-table row sits in the CTA's page cache (-1: read
 // from global memory).
 struct AttnUnit {
-  int row, sp, seq, visible, n_blk, n_body, run0, slot_lo, slot_hi, n_chunks, pc_off;
+  int row, sp, seq, visible, n_blk, n_body, run0, slot_lo, slot_hi, n_chunks, pc_off, pc_len;
 };
 
 template <int HKV>
@@ -113,15 +116,27 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
     if (!row_ok && U.sp == 0) report(status, QSA_ERR_CAPACITY);
     U.n_blk = row_ok ? (U.visible >> sh.log2_ratio) : -1;  // -1: nothing to attend
     U.pc_off = -1;
+    U.pc_len = 0;
     s_unit[tid] = U;
   }
   __syncthreads();
-  if (tid == 0) {  // page-cache room, in unit order, while it lasts
+  if (tid == 0) {  // page-cache room, one region per sequence (its units' longest need), while it lasts
     int used = 0;
     for (int k = 0; k < nu; ++k) {
-      const int need = s_unit[k].n_blk >= 0 ? (s_unit[k].visible + P - 1) >> sh.log2_page : 0;
-      if (need > 0 && used + need <= kPageCache) {
+      if (s_unit[k].n_blk < 0) continue;
+      int j = 0;
+      while (j < k && !(s_unit[j].n_blk >= 0 && s_unit[j].seq == s_unit[k].seq)) ++j;
+      if (j < k) {  // an earlier unit of the same sequence holds the region
+        s_unit[k].pc_off = s_unit[j].pc_off;
+        continue;
+      }
+      int need = 0;
+      for (int m = k; m < nu; ++m)
+        if (s_unit[m].n_blk >= 0 && s_unit[m].seq == s_unit[k].seq)
+          need = max(need, (s_unit[m].visible + P - 1) >> sh.log2_page);
+      if (used + need <= kPageCache) {
         s_unit[k].pc_off = used;
+        s_unit[k].pc_len = need;
         used += need;
       }
     }
@@ -129,10 +144,9 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
   __syncthreads();
   for (int k = 0; k < nu; ++k) {
     const AttnUnit &U = s_unit[k];
-    if (U.pc_off < 0) continue;
-    const int need = (U.visible + P - 1) >> sh.log2_page;
+    if (U.pc_len == 0) continue;  // not a region's owner
     const int32_t *src = cv.page_table + static_cast<size_t>(U.seq) * cv.max_pages;
-    for (int e = tid; e < need; e += kAttnThreads) page_cache[U.pc_off + e] = src[e];
+    for (int e = tid; e < U.pc_len; e += kAttnThreads) page_cache[U.pc_off + e] = src[e];
   }
   // Q^T fragments (B operand of S^T = K Q^T) of a unit for the warp's 8 heads
   auto load_q = [&](int row, uint32_t (&qf)[8][2]) {
