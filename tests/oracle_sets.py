@@ -119,3 +119,31 @@ def assert_every_row(sel_gpu: np.ndarray, nsel_gpu: np.ndarray, row_of: Dict[int
                                f"{len(bad)} rows, first {rows[bad][:8].tolist()}")
         n += len(rows)
     return n
+
+
+class StepLog:
+    """The selections of every row of a series of steps, for one comparison
+    with the oracle's at the end: per sequence, its rows in step order."""
+
+    def __init__(self):
+        self.sel, self.nsel = [], []
+        self.rows = {}     # seq -> GPU rows in the concatenation
+        self.pos = {}      # seq -> positions of those rows
+        self.n = 0
+
+    def add(self, res, seqs, pos0, R):
+        self.sel.append(res["sel"].cpu().numpy())
+        self.nsel.append(res["n_sel"].cpu().numpy())
+        for i, s in enumerate(seqs):
+            for j in range(R):
+                self.rows.setdefault(s, []).append(self.n + i * R + j)
+                self.pos.setdefault(s, []).append(pos0[i] + j)
+        self.n += len(seqs) * R
+
+    def check(self, wl, hist=None, index_format="bf16"):
+        """Every logged row against the oracle (hist: seq -> History of the
+        epochs its tokens were drawn with; index_format: the plane the keys are
+        scored in). Returns the number of rows."""
+        req = [(s, max(p) + 1, (hist[s].epoch_from if hist else [(0, 0)]), p) for s, p in self.pos.items()]
+        want = oracle_selections(wl, req, index_format)
+        return assert_every_row(np.concatenate(self.sel), np.concatenate(self.nsel), self.rows, want)

@@ -23,6 +23,7 @@ import torch
 from indexer_selected_sparse_gb300 import synth as S
 from oracle import qsa_oracle as O
 from tests.gpu_harness import GpuState, OracleSeq, bits, compare_row, gen_token_rows
+from tests.oracle_sets import StepLog
 
 pytestmark = pytest.mark.gpu
 
@@ -212,17 +213,22 @@ def test_fused_step_every_row(name):
         check_plane(g, s, pos0[i] + R)
 
 
-def test_steady_decode_batch32_prefix32k_sampled_rows():
+def test_steady_decode_batch32_prefix32k_every_row():
+    """Batch 32 x 32k with the MXFP8 plane: every row's selection of two steps
+    against the oracle's MXFP8 scores; outputs on sampled rows."""
     wl = S.workload(2)
     g = GpuState(wl, extra_tokens=8, index_format=MX)
     g.append_prefix()
     sampled = [0, 17, 31]
     oracles = {s: OracleSeq(wl, s, wl.prefixes[0] + 2) for s in sampled}
     pos0 = list(wl.prefixes)
+    log = StepLog()
     for step in range(2):
         res = g.decode(pos0, 1)
         g.check_status()
+        log.add(res, g.slots, pos0, 1)
         sel = res["sel"].cpu().numpy(); nsel = res["n_sel"].cpu().numpy(); out = bits(res["out"])
         for s in sampled:
             compare_row(out[s], sel[s], int(nsel[s]), oracles[s].row(pos0[s], "mxfp8"), g.cfg.topk)
         pos0 = [p + 1 for p in pos0]
+    assert log.check(wl, index_format="mxfp8") == 2 * wl.n_seq

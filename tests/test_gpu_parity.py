@@ -14,7 +14,7 @@ import torch
 from indexer_selected_sparse_gb300 import synth as S
 from oracle import qsa_oracle as O
 from tests.gpu_harness import GpuState, OracleSeq, bits, compare_row
-from tests.oracle_sets import assert_every_row, oracle_selections
+from tests.oracle_sets import StepLog
 
 pytestmark = pytest.mark.gpu
 
@@ -33,33 +33,6 @@ def check_rows(g: GpuState, res, seqs_sampled, pos0, R, oracles):
             ref = oracles[s].row(pos0[i] + j)
             errs.append(compare_row(out[row], sel[row], int(nsel[row]), ref, topk))
     return errs
-
-
-class StepLog:
-    """The selections of every row of a series of steps, for one comparison
-    with the oracle's at the end: per sequence, its rows in step order."""
-
-    def __init__(self):
-        self.sel, self.nsel = [], []
-        self.rows = {}     # seq -> GPU rows in the concatenation
-        self.pos = {}      # seq -> positions of those rows
-        self.n = 0
-
-    def add(self, res, seqs, pos0, R):
-        self.sel.append(res["sel"].cpu().numpy())
-        self.nsel.append(res["n_sel"].cpu().numpy())
-        for i, s in enumerate(seqs):
-            for j in range(R):
-                self.rows.setdefault(s, []).append(self.n + i * R + j)
-                self.pos.setdefault(s, []).append(pos0[i] + j)
-        self.n += len(seqs) * R
-
-    def check(self, wl, hist=None):
-        """Every logged row against the oracle (hist: seq -> History of the
-        epochs its tokens were drawn with). Returns the number of rows."""
-        req = [(s, max(p) + 1, (hist[s].epoch_from if hist else [(0, 0)]), p) for s, p in self.pos.items()]
-        want = oracle_selections(wl, req)
-        return assert_every_row(np.concatenate(self.sel), np.concatenate(self.nsel), self.rows, want)
 
 
 def test_tiny_decode_every_row_and_pools():
