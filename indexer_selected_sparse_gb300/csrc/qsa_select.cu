@@ -9,7 +9,7 @@
 // first: a pass histograms the keys that match the prefix fixed so far and a
 // block-wide suffix scan finds the digit that holds the K-th largest key. Only
 // the first pass reads every key: the keys of the chosen digit are gathered
-// into a candidate list, which one warp ranks directly when it is short and
+// into a candidate list, which all warps rank at once when it is short and
 // further passes refine otherwise. The K-th largest key T is then exact, and so
 // is the number of ties at T that must be taken. A stable compaction emits, in
 // ascending block order, every block with key > T and the lowest-indexed blocks
@@ -28,7 +28,8 @@ constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;  // <= 32: the scan keeps one total per lane
 constexpr int kMaxSmemKeys = 48 * 1024 - 4096;  // keys held on chip (176 KB) ...
 constexpr int kCandMax = 4096;                   // ... plus the candidate list (16 KB)
-constexpr int kDirectMax = 64;  // candidate lists this short are ranked by one warp
+constexpr int kDirectMax = 128;  // candidate lists this short are ranked directly
+static_assert(kDirectMax <= 4 * kSelWarps && kDirectMax <= 4 * 32, "each warp ranks 4 candidates, each lane holds 4");
 constexpr int kDigit = 11;
 constexpr int kBins = 1 << kDigit;
 constexpr int kBinsPerThread = kBins / kSelThreads;
@@ -109,6 +110,45 @@ __device__ __forceinline__ void digit_search(int shift, uint32_t dmask, uint32_t
   remaining -= s_res[1];
 }
 
+// The remaining-th largest of a short candidate list (nc <= kDirectMax keys in
+// shared memory): warp w ranks candidates w, w + 32, ... against the whole list
+// (each lane holding up to four of its entries), so the ranking costs one pass
+// over four registers and a warp reduction. The candidate that has fewer than
+// `remaining` entries above it and at least that many at or above it is the
+// threshold; equal candidates agree, so any of their warps may write it. Ends
+// with a barrier; returns the threshold and the ties at it to take.
+__device__ __forceinline__ void rank_candidates(const uint32_t *cand, int nc, uint32_t &thr, int &remaining,
+                                                int *s_res) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t v[4];
+  bool ok[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    ok[k] = lane + 32 * k < nc;
+    v[k] = ok[k] ? cand[lane + 32 * k] : 0u;
+  }
+#pragma unroll
+  for (int i = 0; i < kDirectMax / kSelWarps; ++i) {
+    const int ci = warp + kSelWarps * i;  // warp-uniform
+    if (ci < nc) {
+      const uint32_t c = cand[ci];
+      int ge = 0;  // (entries above c) << 16 | (entries equal to c); both <= 128
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (ok[k]) ge += (v[k] > c ? 0x10000 : 0) + (v[k] == c ? 1 : 0);
+      ge = __reduce_add_sync(0xffffffffu, ge);
+      const int g = ge >> 16, e = ge & 0xffff;
+      if (lane == 0 && g < remaining && remaining <= g + e) {
+        s_res[0] = static_cast<int>(c);
+        s_res[1] = remaining - g;
+      }
+    }
+  }
+  __syncthreads();
+  thr = static_cast<uint32_t>(s_res[0]);
+  remaining = s_res[1];
+}
+
 // Key sources. Every key is taken relative to the row's smallest key, so the
 // radix digits cover the range the row's keys actually span: scores of one row
 // share sign and exponent bits, and digits of the raw key would pile most of the
@@ -166,7 +206,7 @@ template <typename Src>
 __device__ __forceinline__ void select_row(Src src, int n, int K, uint32_t range, uint32_t *cand,
                                            int32_t *out, int *hist, int2 *scan_tmp, int *s_res,
                                            int *s_ncand) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   int top = range ? 31 - __clz(range) : -1;  // highest bit any key of the row sets
   const uint32_t low_bits = (top >= 31) ? 0xffffffffu : (top >= 0 ? ((2u << top) - 1u) : 0u);
   uint32_t prefix = 0u;
@@ -194,32 +234,7 @@ __device__ __forceinline__ void select_row(Src src, int n, int K, uint32_t range
       __syncthreads();
       const int nc = *s_ncand;
       if (nc <= kDirectMax) {
-        // one warp ranks the candidates directly: the remaining-th largest has
-        // fewer than `remaining` candidates above it and at least that many at
-        // or above it
-        if (warp == 0) {
-          const uint32_t a = lane < nc ? cand[lane] : 0u;
-          const uint32_t b = lane + 32 < nc ? cand[lane + 32] : 0u;
-          int ga = 0, ea = 0, gb = 0, eb = 0;
-          for (int j = 0; j < nc; ++j) {
-            const uint32_t v = cand[j];
-            ga += v > a;
-            ea += v == a;
-            gb += v > b;
-            eb += v == b;
-          }
-          if (lane < nc && ga < remaining && remaining <= ga + ea) {
-            s_res[0] = static_cast<int>(a);
-            s_res[1] = remaining - ga;
-          }
-          if (lane + 32 < nc && gb < remaining && remaining <= gb + eb) {
-            s_res[0] = static_cast<int>(b);
-            s_res[1] = remaining - gb;
-          }
-        }
-        __syncthreads();
-        prefix = static_cast<uint32_t>(s_res[0]);
-        remaining = s_res[1];
+        rank_candidates(cand, nc, prefix, remaining, s_res);
       } else if (nc <= kCandMax) {
         while (top >= 0) {
           width = min(kDigit, top + 1);
@@ -286,7 +301,8 @@ __device__ __forceinline__ void select_row(Src src, int n, int K, uint32_t range
 // Rows of at most 4 * NV * kSelThreads blocks: thread t holds the keys of the
 // 4 * NV consecutive blocks 4NV*t .. 4NV*t + 4NV - 1 in registers for the whole
 // selection. Warp reductions use redux.sync; the candidates of the chosen digit
-// are gathered with one shared atomic per warp; the compaction is one block
+// are gathered with one shared atomic per warp and ranked by all warps at
+// once when at most kDirectMax; the compaction is one block
 // scan of each thread's counts above and at the threshold, after which every
 // thread writes its own selected blocks in index order (no bitmaps, no
 // atomics). Barriers: range 1, histogram 1, digit search 2, candidates 1,
@@ -368,31 +384,7 @@ __device__ __forceinline__ void select_in_registers(const float *__restrict__ sr
       __syncthreads();
       const int nc = *s_ncand;
       if (nc <= kDirectMax) {
-        // one warp ranks the candidates: the remaining-th largest has fewer than
-        // `remaining` candidates above it and at least that many at or above it
-        if (warp == 0) {
-          const uint32_t a = lane < nc ? cand[lane] : 0u;
-          const uint32_t b = lane + 32 < nc ? cand[lane + 32] : 0u;
-          int ga = 0, ea = 0, gb = 0, eb = 0;
-          for (int i = 0; i < nc; ++i) {
-            const uint32_t c = __shfl_sync(0xffffffffu, i < 32 ? a : b, i & 31);
-            ga += c > a;
-            ea += c == a;
-            gb += c > b;
-            eb += c == b;
-          }
-          if (lane < nc && ga < remaining && remaining <= ga + ea) {
-            s_res[0] = static_cast<int>(a);
-            s_res[1] = remaining - ga;
-          }
-          if (lane + 32 < nc && gb < remaining && remaining <= gb + eb) {
-            s_res[0] = static_cast<int>(b);
-            s_res[1] = remaining - gb;
-          }
-        }
-        __syncthreads();
-        prefix = static_cast<uint32_t>(s_res[0]);
-        remaining = s_res[1];
+        rank_candidates(cand, nc, prefix, remaining, s_res);
       } else {
         // long candidate lists: further passes over the list, or, when it
         // overflowed, over the whole row staged in shared memory

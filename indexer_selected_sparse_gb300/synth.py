@@ -246,7 +246,7 @@ def workload(i: int) -> Workload:
     raise ValueError(f"no workload {i}")
 
 
-SCORE_KINDS = ("spread", "nonneg", "cluster", "few_values", "signed_zero", "relu_sum")
+SCORE_KINDS = ("spread", "nonneg", "cluster", "few_values", "signed_zero", "relu_sum", "infinite")
 
 
 def select_scores(seed: int, n_rows: int, n: int, kind: str) -> torch.Tensor:
@@ -262,7 +262,9 @@ def select_scores(seed: int, n_rows: int, n: int, kind: str) -> torch.Tensor:
       signed_zero  +0.0 or -0.0 except about 1 in 64 positive values
       relu_sum     about N(270, 70^2), clipped at 0: the shape of a row of
                    sum_h w_h ReLU(q_h . k) over 64 heads with the decode
-                   workload's bf16 inputs (Irwin-Hall of 12 uniforms)"""
+                   workload's bf16 inputs (Irwin-Hall of 12 uniforms)
+      infinite     spread, with about 1 in 16 values +inf and 1 in 64 -inf
+                   (a row whose range is not finite; ties at +inf)"""
     rows = torch.arange(n_rows, dtype=torch.int64)[:, None]
     cols = torch.arange(n, dtype=torch.int64)[None, :]
     b = token_base(seed, STREAM_SCORES, 0, rows, cols)
@@ -285,6 +287,10 @@ def select_scores(seed: int, n_rows: int, n: int, kind: str) -> torch.Tensor:
     elif kind == "relu_sum":
         u12 = draws(b, 12).to(torch.float64) / 4294967296.0
         x = torch.clamp(270.0 + 70.0 * (u12.sum(-1) - 6.0), min=0.0)
+    elif kind == "infinite":
+        x = u * 8.0 - 4.0
+        x = torch.where((b >> 8) % 16 == 0, torch.full_like(x, float("inf")), x)
+        x = torch.where((b >> 12) % 64 == 1, torch.full_like(x, float("-inf")), x)
     else:
         raise ValueError(f"unknown score kind {kind}")
     return x.to(torch.float32)

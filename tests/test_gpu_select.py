@@ -71,3 +71,23 @@ def test_select_k2048(kind):
 def test_select_dense_rows_take_every_block():
     # n <= K: every block, in order, padded with -1
     run_select(4, 2048, [1, 2, 511, 512], "spread", seed=24)
+
+
+@pytest.mark.parametrize("kind", S.SCORE_KINDS)
+def test_select_short_rows_split_over_the_cluster(kind):
+    # rows of up to 16k blocks are split over four CTAs in runs of a multiple of
+    # 4 blocks: at 17 or 18 blocks the last CTA holds none and the third one or
+    # two; K = 16
+    run_select(4, 64, [17, 18, 23, 31, 64, 100, 1000, 16383], kind, seed=26)
+
+
+@pytest.mark.parametrize("kind", ["spread", "few_values", "signed_zero"])
+def test_select_k1(kind):
+    # K = 1: the single largest block, ties to the lowest index
+    run_select(4, 4, [2, 3, 5, 4097, 9000], kind, seed=27)
+
+
+@pytest.mark.parametrize("kind", ["spread", "cluster", "few_values", "relu_sum"])
+def test_select_k2048_in_registers(kind):
+    # K = 2048 with rows held in registers across the cluster
+    run_select(4, 8192, [2049, 4100, 8192, 12000, 16384], kind, seed=28)

@@ -65,7 +65,10 @@ def test_select_scores_kinds_are_seeded_and_shaped():
         a = S.select_scores(5, 3, 257, kind)
         b = S.select_scores(5, 3, 257, kind)
         assert a.shape == (3, 257) and a.dtype == torch.float32
-        assert torch.equal(a, b) and torch.isfinite(a).all()
+        assert torch.equal(a, b) and not torch.isnan(a).any()
+        assert torch.isfinite(a).all() or kind == "infinite"
+    inf = S.select_scores(5, 2, 8192, "infinite")
+    assert (inf == float("inf")).sum() > 600 and (inf == float("-inf")).sum() > 100
     z = S.select_scores(5, 2, 4096, "signed_zero")
     assert (torch.signbit(z) & (z == 0)).any() and (~torch.signbit(z) & (z == 0)).any()
     c = S.select_scores(5, 2, 4096, "cluster")
