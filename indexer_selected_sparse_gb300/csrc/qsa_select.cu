@@ -15,7 +15,8 @@
 // ascending block order, every block with key > T and the lowest-indexed blocks
 // with key == T: exactly the top-K under (score desc, index asc).
 // Rows of up to 16k blocks keep their keys in registers (each thread a run of
-// consecutive blocks) and compact with one block scan of per-thread counts;
+// consecutive blocks, plus one block of the row's tail for rows just past a
+// layout's size) and compact with one block scan of per-thread counts;
 // longer rows stage their keys in shared memory (or, past that, read them from
 // global memory). The selection stays on the device, so a step that
 // contains it can be captured in a CUDA graph.
@@ -46,9 +47,10 @@ __device__ __forceinline__ int warp_incl_scan_sel(int v, int lane) {
 }
 
 // Exclusive prefix sums over the CTA of a pair of counts, with one barrier: every
-// warp scans the per-warp totals itself. Two calls must be separated by a barrier
-// (the next call overwrites `tmp`).
-__device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2 *tmp) {
+// warp scans the per-warp totals itself (and, when `total` is given, leaves the
+// CTA's sums there). Two calls must be separated by a barrier (the next call
+// overwrites `tmp`).
+__device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2 *tmp, int2 *total = nullptr) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int2 x = v;
 #pragma unroll
@@ -77,6 +79,10 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2 *tmp) {
   before.x = __shfl_sync(0xffffffffu, t.x, src);
   before.y = __shfl_sync(0xffffffffu, t.y, src);
   if (warp == 0) before = make_int2(0, 0);
+  if (total) {
+    total->x = __shfl_sync(0xffffffffu, t.x, kSelWarps - 1);
+    total->y = __shfl_sync(0xffffffffu, t.y, kSelWarps - 1);
+  }
   return make_int2(before.x + x.x - v.x, before.y + x.y - v.y);
 }
 
@@ -298,24 +304,30 @@ __device__ __forceinline__ void select_row(Src src, int n, int K, uint32_t range
 }
 
 // ---------------------------------------------------------------------------
-// Rows of at most 4 * NV * kSelThreads blocks: thread t holds the keys of the
-// 4 * NV consecutive blocks 4NV*t .. 4NV*t + 4NV - 1 in registers for the whole
-// selection. Warp reductions use redux.sync; the candidates of the chosen digit
-// are gathered with one shared atomic per warp and ranked by all warps at
-// once when at most kDirectMax; the compaction is one block
-// scan of each thread's counts above and at the threshold, after which every
-// thread writes its own selected blocks in index order (no bitmaps, no
-// atomics). Barriers: range 1, histogram 1, digit search 2, candidates 1,
-// ranking 1, compaction scan 1.
+// Rows of at most (4 * NV + E) * kSelThreads blocks: thread t holds the keys of
+// the 4 * NV consecutive blocks 4NV*t .. 4NV*t + 4NV - 1 in registers for the
+// whole selection and, when E = 1, one more block from the row's tail, M + t
+// (M = 4 * NV * kSelThreads), so that a row just past a multiple of 4096 blocks
+// costs one key more per thread instead of four. Warp reductions use
+// redux.sync; the candidates of the chosen digit are gathered with one shared
+// atomic per warp and ranked by all warps at once when at most kDirectMax; the
+// compaction is one block scan of each thread's counts above and at the
+// threshold (for the contiguous runs and the tail, packed 16:16 in two words),
+// after which every thread writes its own selected blocks in index order (no
+// bitmaps, no atomics). Barriers: range 1, histogram 1, digit search 2,
+// candidates 1, ranking 1, compaction scan 1.
 // ---------------------------------------------------------------------------
-template <int NV>
+template <int NV, int E>
 __device__ __forceinline__ void select_in_registers(const float *__restrict__ srow, int n, int K,
                                                     int32_t *__restrict__ out, uint32_t *keys,
                                                     uint32_t *cand, int *hist, int2 *scan_tmp, int *s_res,
                                                     int *s_ncand, uint32_t *red_min, uint32_t *red_max) {
-  constexpr int NK = 4 * NV;
+  static_assert(E == 0 || E == 1, "at most one tail key per thread");
+  constexpr int NR = 4 * NV;   // keys of the contiguous run
+  constexpr int NK = NR + E;   // keys held
+  constexpr int M = NR * kSelThreads;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int x0 = NK * tid;  // first block of this thread
+  const int x0 = NR * tid;  // first block of this thread's run
   // 16-byte loads: ld is a multiple of 4, so a group that starts below n lies in the row
   const float4 *s4 = reinterpret_cast<const float4 *>(srow) + NV * tid;
   uint32_t d[NK];
@@ -328,7 +340,10 @@ __device__ __forceinline__ void select_in_registers(const float *__restrict__ sr
     d[4 * v + 2] = score_key(f.z);
     d[4 * v + 3] = score_key(f.w);
   }
-  auto valid = [&](int j) { return x0 + j < n; };
+  if (E == 1) d[NK - 1] = M + tid < n ? score_key(srow[M + tid]) : 0u;
+  // the block index of key j
+  auto blk = [&](int j) { return j < NR ? x0 + j : M + tid; };
+  auto valid = [&](int j) { return blk(j) < n; };
   uint32_t kmin = 0xffffffffu, kmax = 0u;
 #pragma unroll
   for (int j = 0; j < NK; ++j)
@@ -393,7 +408,7 @@ __device__ __forceinline__ void select_in_registers(const float *__restrict__ sr
         if (nc > kCandMax) {
 #pragma unroll
           for (int j = 0; j < NK; ++j)
-            if (valid(j)) keys[x0 + j] = d[j];
+            if (valid(j)) keys[blk(j)] = d[j];
           __syncthreads();
           list = keys;
           m = n;
@@ -411,27 +426,40 @@ __device__ __forceinline__ void select_in_registers(const float *__restrict__ sr
   const uint32_t thr = prefix;  // the K-th largest key
   const int need = remaining;   // ties at thr to take (>= 1)
 
-  // ---- compaction: the blocks before this thread's emit pre.x above thr and
-  // min(pre.y, need) ties; its own blocks follow in index order
-  int gt = 0, eq = 0;
+  // ---- compaction, in index order: the runs (segment 0), then the tail keys
+  // (segment 1, in thread order). The blocks before a key emit the keys above
+  // thr before it and the ties before it, capped at `need`. Per thread and
+  // segment the counts above and at thr are packed as above | at << 16 (each
+  // at most 16 * kSelThreads < 2^16 over the row).
+  uint32_t c0 = 0u, c1 = 0u;
 #pragma unroll
   for (int j = 0; j < NK; ++j)
     if (valid(j)) {
-      gt += d[j] > thr;
-      eq += d[j] == thr;
+      const uint32_t c = (d[j] > thr ? 1u : 0u) + (d[j] == thr ? 0x10000u : 0u);
+      if (j < NR)
+        c0 += c;
+      else
+        c1 += c;
     }
-  const int2 pre = block_exclusive_scan2(make_int2(gt, eq), scan_tmp);
-  int o = pre.x + min(pre.y, need);
-  int tie_rank = pre.y;
+  int2 tot;
+  const int2 pre = block_exclusive_scan2(make_int2(static_cast<int>(c0), static_cast<int>(c1)), scan_tmp, &tot);
+  const uint32_t p0 = static_cast<uint32_t>(pre.x);
+  const uint32_t p1 = static_cast<uint32_t>(pre.y) + static_cast<uint32_t>(tot.x);  // after every run
+  int o = static_cast<int>(p0 & 0xffffu) + min(static_cast<int>(p0 >> 16), need);
+  int tie_rank = static_cast<int>(p0 >> 16);
 #pragma unroll
   for (int j = 0; j < NK; ++j) {
+    if (j == NR) {  // the tail key: its own place in segment 1
+      o = static_cast<int>(p1 & 0xffffu) + min(static_cast<int>(p1 >> 16), need);
+      tie_rank = static_cast<int>(p1 >> 16);
+    }
     if (!valid(j)) continue;
     if (d[j] > thr) {
-      if (o < K) out[o] = x0 + j;
+      if (o < K) out[o] = blk(j);
       ++o;
     } else if (d[j] == thr) {
       if (tie_rank < need) {
-        if (o < K) out[o] = x0 + j;
+        if (o < K) out[o] = blk(j);
         ++o;
       }
       ++tie_rank;
@@ -534,12 +562,17 @@ select_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__
   uint32_t *cand = keys + smem_keys;
   const float *srow = scores + static_cast<size_t>(row) * ld;
   // rows up to 16k blocks (64k tokens at ratio 4) keep their keys in registers
+  // (a thread's run of 4 NV keys plus E tail keys; the smallest layout that holds the row)
   if (n <= 4 * kSelThreads) {
-    select_in_registers<1>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
+    select_in_registers<1, 0>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else if (n <= 8 * kSelThreads) {
-    select_in_registers<2>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
+    select_in_registers<2, 0>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
+  } else if (n <= 9 * kSelThreads) {
+    select_in_registers<2, 1>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
+  } else if (n <= 12 * kSelThreads) {
+    select_in_registers<3, 0>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else if (n <= 16 * kSelThreads) {
-    select_in_registers<4>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
+    select_in_registers<4, 0>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else {
     select_general(srow, n, K, out, keys, cand, smem_keys, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   }

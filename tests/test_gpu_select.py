@@ -91,3 +91,16 @@ def test_select_k1(kind):
 def test_select_k2048_in_registers(kind):
     # K = 2048 with rows held in registers across the cluster
     run_select(4, 8192, [2049, 4100, 8192, 12000, 16384], kind, seed=28)
+
+
+@pytest.mark.parametrize("kind", S.SCORE_KINDS)
+def test_select_rows_past_a_layout_boundary(kind):
+    # past 8192 blocks a thread holds its run of 8 keys plus one key from the
+    # row's tail (ties there come after every tie of the runs), past 9216 runs
+    # of 12, past 12288 runs of 16: each side of each boundary, K = 512
+    run_select(4, 2048, [8193, 8200, 8256, 9215, 9216, 9217, 12288, 12289], kind, seed=29)
+
+
+@pytest.mark.parametrize("kind", ["spread", "few_values", "signed_zero"])
+def test_select_k2048_with_tail_keys(kind):
+    run_select(4, 8192, [8193, 9000, 9216], kind, seed=30)
