@@ -46,10 +46,23 @@ __device__ __forceinline__ int warp_incl_scan_sel(int v, int lane) {
   return v;
 }
 
-// Exclusive prefix sums over the CTA of a pair of counts, with one barrier: every
-// warp scans the per-warp totals itself (and, when `total` is given, leaves the
-// CTA's sums there). Two calls must be separated by a barrier (the next call
-// overwrites `tmp`).
+// Exclusive prefix sums over the CTA, with one barrier: each warp scans its
+// lanes with shuffles and takes the sum of the warp totals below it with one
+// warp reduction (and, when `total` is given, the CTA's sum with another), so
+// no warp rescans the totals. Two calls must be separated by a barrier (the
+// next call overwrites `tmp`).
+__device__ __forceinline__ int block_exclusive_scan1(int v, int *tmp, int *total = nullptr) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int x = warp_incl_scan_sel(v, lane);
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  const int t = lane < kSelWarps ? tmp[lane] : 0;
+  const int before = __reduce_add_sync(0xffffffffu, lane < warp ? t : 0);
+  if (total) *total = __reduce_add_sync(0xffffffffu, t);
+  return before + x - v;
+}
+
+// The same for a pair of counts.
 __device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2 *tmp, int2 *total = nullptr) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int2 x = v;
@@ -64,25 +77,10 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2 *tmp, int2 *t
   }
   if (lane == 31) tmp[warp] = x;
   __syncthreads();
-  int2 t = lane < kSelWarps ? tmp[lane] : make_int2(0, 0);
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int yx = __shfl_up_sync(0xffffffffu, t.x, o);
-    const int yy = __shfl_up_sync(0xffffffffu, t.y, o);
-    if (lane >= o) {
-      t.x += yx;
-      t.y += yy;
-    }
-  }
-  const int src = warp > 0 ? warp - 1 : 0;
-  int2 before;
-  before.x = __shfl_sync(0xffffffffu, t.x, src);
-  before.y = __shfl_sync(0xffffffffu, t.y, src);
-  if (warp == 0) before = make_int2(0, 0);
-  if (total) {
-    total->x = __shfl_sync(0xffffffffu, t.x, kSelWarps - 1);
-    total->y = __shfl_sync(0xffffffffu, t.y, kSelWarps - 1);
-  }
+  const int2 t = lane < kSelWarps ? tmp[lane] : make_int2(0, 0);
+  const int2 before = make_int2(__reduce_add_sync(0xffffffffu, lane < warp ? t.x : 0),
+                                __reduce_add_sync(0xffffffffu, lane < warp ? t.y : 0));
+  if (total) *total = make_int2(__reduce_add_sync(0xffffffffu, t.x), __reduce_add_sync(0xffffffffu, t.y));
   return make_int2(before.x + x.x - v.x, before.y + x.y - v.y);
 }
 
@@ -101,7 +99,7 @@ __device__ __forceinline__ void digit_search(int shift, uint32_t dmask, uint32_t
     hist[top_bin - j] = 0;  // only this thread reads these bins
     sum += c[j];
   }
-  int above = block_exclusive_scan2(make_int2(sum, 0), scan_tmp).x;
+  int above = block_exclusive_scan1(sum, reinterpret_cast<int *>(scan_tmp));
 #pragma unroll
   for (int j = 0; j < kBinsPerThread; ++j) {
     if (above < remaining && remaining <= above + c[j]) {
@@ -309,10 +307,10 @@ __device__ __forceinline__ void select_row(Src src, int n, int K, uint32_t range
 // whole selection and, when E = 1, one more block from the row's tail, M + t
 // (M = 4 * NV * kSelThreads), so that a row just past a multiple of 4096 blocks
 // costs one key more per thread instead of four. Warp reductions use
-// redux.sync; the candidates of the chosen digit are gathered with one shared
-// atomic per warp and ranked by all warps at once when at most kDirectMax; the
-// compaction is one block scan of each thread's counts above and at the
-// threshold (for the contiguous runs and the tail, packed 16:16 in two words),
+// redux.sync; the candidates of the chosen digit are gathered with a shared
+// atomic per thread that holds any and ranked by all warps at once when at most
+// kDirectMax; the compaction is one block scan of each thread's counts above
+// and at the threshold (packed 16:16; a second word for the tail),
 // after which every thread writes its own selected blocks in index order (no
 // bitmaps, no atomics). Barriers: range 1, histogram 1, digit search 2,
 // candidates 1, ranking 1, compaction scan 1.
@@ -380,22 +378,22 @@ __device__ __forceinline__ void select_in_registers(const float *__restrict__ sr
     digit_search(shift, dmask, prefix, mask, remaining, hist, scan_tmp, s_res);
     top = shift - 1;
     if (top >= 0) {
-      // the keys of the chosen digit: each warp reserves its slots with one atomic
-      int mine = 0;
-#pragma unroll
-      for (int j = 0; j < NK; ++j) mine += (valid(j) && (d[j] & mask) == prefix) ? 1 : 0;
-      const int incl = warp_incl_scan_sel(mine, lane);
-      const int total = __shfl_sync(0xffffffffu, incl, 31);
-      int base = 0;
-      if (lane == 31 && total > 0) base = atomicAdd(s_ncand, total);
-      base = __shfl_sync(0xffffffffu, base, 31);
-      int pos = base + incl - mine;
+      // the keys of the chosen digit, in any order (only their values are
+      // ranked): usually a few threads hold one or two, so each of those
+      // reserves its slots with its own shared atomic
+      uint32_t member = 0u;
 #pragma unroll
       for (int j = 0; j < NK; ++j)
-        if (valid(j) && (d[j] & mask) == prefix) {
-          if (pos < kCandMax) cand[pos] = d[j];
-          ++pos;
-        }
+        if (valid(j) && (d[j] & mask) == prefix) member |= 1u << j;
+      if (member) {
+        int pos = atomicAdd(s_ncand, __popc(member));
+#pragma unroll
+        for (int j = 0; j < NK; ++j)
+          if ((member >> j) & 1u) {
+            if (pos < kCandMax) cand[pos] = d[j];
+            ++pos;
+          }
+      }
       __syncthreads();
       const int nc = *s_ncand;
       if (nc <= kDirectMax) {
@@ -441,10 +439,15 @@ __device__ __forceinline__ void select_in_registers(const float *__restrict__ sr
       else
         c1 += c;
     }
-  int2 tot;
-  const int2 pre = block_exclusive_scan2(make_int2(static_cast<int>(c0), static_cast<int>(c1)), scan_tmp, &tot);
-  const uint32_t p0 = static_cast<uint32_t>(pre.x);
-  const uint32_t p1 = static_cast<uint32_t>(pre.y) + static_cast<uint32_t>(tot.x);  // after every run
+  uint32_t p0, p1 = 0u;
+  if (E == 0) {
+    p0 = static_cast<uint32_t>(block_exclusive_scan1(static_cast<int>(c0), reinterpret_cast<int *>(scan_tmp)));
+  } else {
+    int2 tot;
+    const int2 pre = block_exclusive_scan2(make_int2(static_cast<int>(c0), static_cast<int>(c1)), scan_tmp, &tot);
+    p0 = static_cast<uint32_t>(pre.x);
+    p1 = static_cast<uint32_t>(pre.y) + static_cast<uint32_t>(tot.x);  // after every run
+  }
   int o = static_cast<int>(p0 & 0xffffu) + min(static_cast<int>(p0 >> 16), need);
   int tie_rank = static_cast<int>(p0 >> 16);
 #pragma unroll
