@@ -297,7 +297,8 @@ int qsa_quantize_index_q(const qsa_config *cfg, int n_rows, const qsa_bf16 *q_id
  * the largest score under the total order (score descending, block index
  * ascending). Writes sel[row*K + i] ascending, padded with -1 to K entries,
  * and n_sel[row] = number of selected blocks. Scores are compared as fp32
- * (+0 and -0 are equal).
+ * (+0 and -0 are equal; +inf and -inf are ordinary values; a NaN score is
+ * outside the contract and ranks above +inf).
  *   scores  device [rows, ld_scores] fp32 (from qsa_index_score), 16-byte
  *           aligned, ld_scores a multiple of 4 (else QSA_ERR_INVALID_ARG)
  *   sel     device [rows, K] int32;  n_sel  device [rows] int32 */
