@@ -425,13 +425,14 @@ struct Batch {
   int nb = 0;        // tiles in the batch
   int row0 = 0;      // first row of the group
   int nblk_old = 0;  // blocks of the sequence complete before this step's appends
-  int pg = 0;        // this lane's page id
+  int pg = 0;        // this lane's page id (fetch_page_id)
   bool have = false; // this lane's page holds a visible block
+  const int32_t *pid = nullptr;  // where this lane's page id is
 };
 
 // Warp-collective. The group's first row, the blocks visible to its last row
-// and its sequence's page-table row come from the chunk; the page ids are one
-// load per lane, issued a batch ahead of their use.
+// and its sequence's page-table row come from the chunk; the page id itself is
+// fetched by fetch_page_id, one load per lane, a batch ahead of its use.
 __device__ __forceinline__ Batch load_batch(const TcArgs &a, const Walker &w, GroupChunk &c, int lane,
                                             int per_batch, int pages_in_tile, int bpp) {
   const int i = w.g / a.groups_per_seq;
@@ -447,8 +448,22 @@ __device__ __forceinline__ Batch load_batch(const TcArgs &a, const Walker &w, Gr
   b.nb = min(min(per_batch, w.tiles - w.t), w.left);
   const int pidx = w.t * pages_in_tile + lane;
   b.have = lane < b.nb * pages_in_tile && pidx * bpp < nblk_last;
-  b.pg = b.have ? ptab[pidx] : 0;
+  b.pid = ptab + pidx;
   return b;
+}
+
+// The page id of a batch's lane: a predicated load straight into b.pg, issued
+// after any merge of Batch values. A page id merged with another value by a
+// select (a batch or an empty one) would be waited for at the select, not where
+// it is first used (a batch later), and hold up the current batch's copies by a
+// memory round trip.
+__device__ __forceinline__ void fetch_page_id(Batch &b) {
+  b.pg = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p ld.global.b32 %0, [%1];\n}"
+      : "+r"(b.pg)
+      : "l"(b.pid), "r"(static_cast<unsigned>(b.have))
+      : "memory");
 }
 
 // Two E4M3 bytes of w (moved by prmt selector SEL into bytes 1 and 3) -> a
@@ -592,6 +607,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
   const Walker w0 = walker_start(a, chunk, lane);
   Batch cur0;
   if ((warp == 0 || warp == prod2) && w0.left > 0) cur0 = load_batch(a, w0, chunk, lane, per_batch, pages_in_tile, bpp);
+  fetch_page_id(cur0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -603,10 +619,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
     // page copies tops out near 1.3 G pages/s on this part, two independent
     // ones carry nearly 1.8. Both walk the same (group, tile) sequence.
     // Tiles are issued in batches of consecutive tiles of one group: lane L
-    // holds the page id of page L of the batch. The page ids of the next batch
-    // are loaded before the current batch's copies are issued, and the group's
-    // page-table row is cached, so no global-memory latency sits between two
-    // batches of a group. Tiles whose blocks were all complete before this step
+    // holds the page id of page L of the batch. The next batch is worked out
+    // (walker, page ids) once the current batch's copies are out, so its
+    // page-id loads overlap the ring's draining rather than delaying the
+    // current copies (worked out first, the next batch held the current one's
+    // copies back by about 0.8 us per step). Tiles whose blocks were all complete before this step
     // (pooled by earlier steps) need nothing from the append kernel: up to a
     // ring's worth of them is issued before the dependency wait, so their HBM
     // latency overlaps the append.
@@ -632,9 +649,6 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
       pend = false;
     };
     while (ok && w.left > 0) {
-      Walker wn = w;
-      for (int it = 0; it < cur.nb; ++it) walker_next(wn, a, chunk, lane);
-      const Batch nxt = wn.left > 0 ? load_batch(a, wn, chunk, lane, per_batch, pages_in_tile, bpp) : Batch{};
       if (par == 0 && w.g != cur_g) {
         ++gseq;
         const int bs = gseq & 1;
@@ -679,8 +693,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, TcArgs a, int n_stages
                          page_bytes, a_full(s), stream_policy);
         }
       }
-      w = wn;
-      cur = nxt;
+      // the next batch, once this one's copies are out: its page ids arrive
+      // while the ring drains
+      for (int it = 0; it < cur.nb; ++it) walker_next(w, a, chunk, lane);
+      cur = w.left > 0 ? load_batch(a, w, chunk, lane, per_batch, pages_in_tile, bpp) : Batch{};
+      fetch_page_id(cur);
     }
     if (!waited) wait_now();
   } else if (warp == 1) {
