@@ -103,7 +103,7 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
 
   // ---- before the wait, everything the select kernel does not write: the
   // units' rows and positions, their sequences' page-table rows (copied to the
-  // page cache) and the first unit's query
+  // page cache) and the loads of the first unit's query
   if (tid < nu) {
     AttnUnit U;
     const int u = blockIdx.x + tid * gridDim.x;
@@ -148,85 +148,105 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
     const int32_t *src = cv.page_table + static_cast<size_t>(U.seq) * cv.max_pages;
     for (int e = tid; e < U.pc_len; e += kAttnThreads) page_cache[U.pc_off + e] = src[e];
   }
-  // Q^T fragments (B operand of S^T = K Q^T) of a unit for the warp's 8 heads
+  // Q^T fragments (B operand of S^T = K Q^T) of a unit for the warp's 8 heads.
+  // The loads are unconditional (a lane past the group reads the group's first
+  // head) and mask_q zeroes those lanes' fragments later, so nothing waits on
+  // the loads where they are issued.
   auto load_q = [&](int row, uint32_t (&qf)[8][2]) {
     const int hl = lane >> 2;
-    const bool ok = hl < group;
     const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-        q + (static_cast<size_t>(row) * sh.hq + g * group + (ok ? hl : 0)) * kHeadDim);
+        q + (static_cast<size_t>(row) * sh.hq + g * group + (hl < group ? hl : 0)) * kHeadDim);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      qf[ks][0] = ok ? qrow[ks * 8 + (lane & 3)] : 0u;
-      qf[ks][1] = ok ? qrow[ks * 8 + 4 + (lane & 3)] : 0u;
+      qf[ks][0] = qrow[ks * 8 + (lane & 3)];
+      qf[ks][1] = qrow[ks * 8 + 4 + (lane & 3)];
+    }
+  };
+  auto mask_q = [&](uint32_t (&qf)[8][2]) {
+    if ((lane >> 2) >= group) {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) qf[ks][0] = qf[ks][1] = 0u;
     }
   };
   uint32_t qf[8][2];
   load_q(s_unit[0].row, qf);
 
-  pdl_wait();  // sel / n_sel come from the select kernel
-  pdl_trigger();
-
-  // ---- the units' slot ranges (the selected count comes from the select kernel).
-  // A reused selection (sel_pos given) was made by the row at sel_pos[row]: its
-  // blocks are complete at that position, and the tail runs from that block
-  // boundary to the row ("Flash-Next support: vLLM vs Atlas", (a) item 6, MTP
-  // skip_topk; "Flash-Next support: llama.cpp vs Atlas", (a) item 3, shared
-  // indexer layers).
+  // ---- the units' slot ranges. A reused selection (sel_pos given) was made by
+  // the row at sel_pos[row]: its blocks are complete at that position, and the
+  // tail runs from that block boundary to the row ("Flash-Next support: vLLM vs
+  // Atlas", (a) item 6, MTP skip_topk; "Flash-Next support: llama.cpp vs Atlas",
+  // (a) item 3, shared indexer layers).
   // One warp per unit (every lane computes the same values; lane 0 stores them).
-  if (warp < nu) {
-    AttnUnit &U = s_unit[warp];
-    bool row_ok = U.n_blk >= 0;
-    int n_blk = row_ok ? U.n_blk : 0;
-    if (row_ok && sel_pos) {
-      const int ps = sel_pos[U.row];
-      if (ps < 0 || ps >= U.visible) {
+  // Without a local window the ranges read nothing the select kernel writes (the
+  // count of a fused step needs no load; a loaded count or a reused selection
+  // was written before this step), so they are set before the dependency wait;
+  // a window's cut reads the selection, so it waits.
+  auto unit_ranges = [&]() {
+    if (warp < nu) {
+      AttnUnit &U = s_unit[warp];
+      bool row_ok = U.n_blk >= 0;
+      int n_blk = row_ok ? U.n_blk : 0;
+      if (row_ok && sel_pos) {
+        const int ps = sel_pos[U.row];
+        if (ps < 0 || ps >= U.visible) {
+          if (U.sp == 0 && lane == 0) report(status, QSA_ERR_REUSE);
+          row_ok = false;
+          n_blk = 0;
+        } else {
+          n_blk = (ps + 1) >> sh.log2_ratio;
+        }
+      }
+      // n_sel_arr == nullptr: the selection was made by this step's select kernel,
+      // which takes min(n_blk, K) blocks of every row inside the page table, so
+      // the count needs no load (the stores of sel are the only wait)
+      const int cap_sel = min(n_blk, sh.topk);
+      const int n_sel = row_ok ? (n_sel_arr ? min(max(n_sel_arr[U.row], 0), cap_sel) : cap_sel) : 0;
+      int n_body = n_sel * r;
+      int run0 = n_blk * r;
+      if (row_ok && sh.window > 0 && U.visible - sh.window < run0) {
+        run0 = max(U.visible - sh.window, 0);
+        // selected blocks starting at or after run0 are a suffix of the ascending
+        // list: count them 32 at a time from the end
+        const int32_t *sel_row = sel + static_cast<size_t>(U.row) * sh.topk;
+        int keep = n_sel;
+        for (int top = n_sel - 1; top >= 0; top -= 32) {
+          const int idx = top - lane;
+          const unsigned late = __ballot_sync(0xffffffffu, idx >= 0 && sel_row[idx] * r >= run0);
+          keep -= __popc(late);
+          if (late != 0xffffffffu) break;
+        }
+        n_body = keep * r;
+        if (keep > 0) {  // run0 may cut the last selected block before it
+          const int b0 = sel_row[keep - 1] * r;
+          if (b0 + r > run0) n_body = (keep - 1) * r + (run0 - b0);
+        }
+      }
+      int n_slots = row_ok ? n_body + (U.visible - run0) : 0;
+      if (n_slots > n_split * split_len) {  // a reused selection too old for the split plan
         if (U.sp == 0 && lane == 0) report(status, QSA_ERR_REUSE);
-        row_ok = false;
-        n_blk = 0;
-      } else {
-        n_blk = (ps + 1) >> sh.log2_ratio;
+        n_slots = n_split * split_len;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        U.n_body = n_body;
+        U.run0 = run0;
+        U.slot_lo = min(n_slots, U.sp * split_len);  // fixed cut: independent of the batch
+        U.slot_hi = min(n_slots, U.slot_lo + split_len);
+        U.n_chunks = (U.slot_hi - U.slot_lo + G::kChunk - 1) / G::kChunk;
       }
     }
-    // n_sel_arr == nullptr: the selection was made by this step's select kernel,
-    // which takes min(n_blk, K) blocks of every row inside the page table, so
-    // the count needs no load (the stores of sel are the only wait)
-    const int cap_sel = min(n_blk, sh.topk);
-    const int n_sel = row_ok ? (n_sel_arr ? min(max(n_sel_arr[U.row], 0), cap_sel) : cap_sel) : 0;
-    int n_body = n_sel * r;
-    int run0 = n_blk * r;
-    if (row_ok && sh.window > 0 && U.visible - sh.window < run0) {
-      run0 = max(U.visible - sh.window, 0);
-      // selected blocks starting at or after run0 are a suffix of the ascending
-      // list: count them 32 at a time from the end
-      const int32_t *sel_row = sel + static_cast<size_t>(U.row) * sh.topk;
-      int keep = n_sel;
-      for (int top = n_sel - 1; top >= 0; top -= 32) {
-        const int idx = top - lane;
-        const unsigned late = __ballot_sync(0xffffffffu, idx >= 0 && sel_row[idx] * r >= run0);
-        keep -= __popc(late);
-        if (late != 0xffffffffu) break;
-      }
-      n_body = keep * r;
-      if (keep > 0) {  // run0 may cut the last selected block before it
-        const int b0 = sel_row[keep - 1] * r;
-        if (b0 + r > run0) n_body = (keep - 1) * r + (run0 - b0);
-      }
-    }
-    int n_slots = row_ok ? n_body + (U.visible - run0) : 0;
-    if (n_slots > n_split * split_len) {  // a reused selection too old for the split plan
-      if (U.sp == 0 && lane == 0) report(status, QSA_ERR_REUSE);
-      n_slots = n_split * split_len;
-    }
-    __syncwarp();
-    if (lane == 0) {
-      U.n_body = n_body;
-      U.run0 = run0;
-      U.slot_lo = min(n_slots, U.sp * split_len);  // fixed cut: independent of the batch
-      U.slot_hi = min(n_slots, U.slot_lo + split_len);
-      U.n_chunks = (U.slot_hi - U.slot_lo + G::kChunk - 1) / G::kChunk;
-    }
+  };
+  const bool ranges_early = sh.window == 0;
+  if (ranges_early) {
+    unit_ranges();
+    __syncthreads();
   }
-  __syncthreads();
+  pdl_wait();  // sel (and a window's cut) come from the select kernel
+  pdl_trigger();
+  if (!ranges_early) {
+    unit_ranges();
+    __syncthreads();
+  }
 
   // ---- resolve every slot of every unit to its cache row, all in parallel:
   // the stage loads below need no global lookups. Entries past a split's end
@@ -316,6 +336,7 @@ attn_kernel(Shape sh, int R, int n_units, int n_split, int split_len, const int3
   for (int k = 0; k < nu; ++k) {
     const AttnUnit U = s_unit[k];
     if (k > 0) load_q(U.row, qf);
+    mask_q(qf);
     float acc[8][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
