@@ -729,49 +729,59 @@ def run_reuse(args, Q, torch, cfg, sh, cache, batches, ws, status, stream, NB, B
 
 def stage_breakdown(args, Q, torch, cfg, sh, cache, batches, ws, status, stream, hpos, NB, B, hbm_gbs,
                     peak_kind):
+    """Per-stage device time of the decode step: each stage is one CUDA graph
+    holding that stage's calls for all NB rotating batches back to back (so a
+    graph launch is spread over NB launches and the batches' data, NB x the
+    step's bytes, does not fit in L2), timed with CUDA events around each replay
+    and divided by NB. Stages run in step order (every batch's append, then every
+    batch's scoring, ...); each batch has its own score rows and selection."""
     dev = cache.k_pool.device
     ld = (cache.max_blocks + 3) // 4 * 4
-    scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
-    sel = torch.empty(B, cfg.topk, dtype=torch.int32, device=dev)
-    nsel = torch.empty(B, dtype=torch.int32, device=dev)
+    scores = [torch.empty(B, ld, dtype=torch.float32, device=dev) for _ in batches]
+    sel = [torch.empty(B, cfg.topk, dtype=torch.int32, device=dev) for _ in batches]
+    nsel = [torch.empty(B, dtype=torch.int32, device=dev) for _ in batches]
     one = torch.ones(B, dtype=torch.int32, device=dev)
-    stage_graphs = []
-    for bt in batches:
+    calls = []
+    for b, bt in enumerate(batches):
         rows = Q.Rows(bt["ids"], bt["pos0"], 1)
-        gs = []
-        for fn in (lambda: Q.qsa_append(cfg, rows, cache, bt["k"], bt["v"], bt["idx"], status),
-                   lambda: Q.qsa_index_score(cfg, rows, cache, bt["q_idx"], bt["w"], scores, ld, status),
-                   lambda: Q.qsa_topk_select(cfg, rows, scores, ld, sel, nsel, status),
-                   lambda: Q.qsa_gather_attn(cfg, rows, cache, bt["q"], sel, nsel, bt["out"], ws, status),
-                   lambda: Q.qsa_rewind(cfg, bt["ids"], one, cache.ingested, status)):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                fn()
-            gs.append(g)
-        stage_graphs.append(gs)
+        calls.append((
+            lambda bt=bt, rows=rows: Q.qsa_append(cfg, rows, cache, bt["k"], bt["v"], bt["idx"], status),
+            lambda bt=bt, rows=rows, b=b: Q.qsa_index_score(cfg, rows, cache, bt["q_idx"], bt["w"], scores[b], ld,
+                                                            status),
+            lambda rows=rows, b=b: Q.qsa_topk_select(cfg, rows, scores[b], ld, sel[b], nsel[b], status),
+            lambda bt=bt, rows=rows, b=b: Q.qsa_gather_attn(cfg, rows, cache, bt["q"], sel[b], nsel[b], bt["out"],
+                                                            ws, status),
+            lambda bt=bt: Q.qsa_rewind(cfg, bt["ids"], one, cache.ingested, status)))
+    stage_graphs = []
+    for j in range(5):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c in calls:
+                c[j]()
+        stage_graphs.append(g)
     torch.cuda.synchronize()
-    KB = args.breakdown_steps
+    KB = max(1, math.ceil(args.breakdown_steps / NB))  # rotations
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(KB)]
     with torch.cuda.stream(stream):
         for i in range(KB):
-            gs = stage_graphs[i % NB]
             e = evs[i]
             for j in range(4):
                 e[j].record(stream)
-                gs[j].replay()
+                stage_graphs[j].replay()
             e[4].record(stream)
-            gs[4].replay()
+            stage_graphs[4].replay()
     torch.cuda.synchronize()
     assert int(status.item()) == 0, Q.qsa_strerror(int(status.item()))
     names = ["append", "index_score", "topk_select", "gather_attn"]
-    stage_ms = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(KB)) / KB for j, n in enumerate(names)}
+    stage_ms = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(KB)) / (KB * NB)
+                for j, n in enumerate(names)}
     bvis = []
-    for i in range(KB):
-        bvis += [hpos[i % NB] + 1] * B
+    for b in range(NB):
+        bvis += [hpos[b] + 1] * B
     bw = sum_work(sh, bvis)
-    stage_bytes = {"append": bw["append_bytes"] / KB, "index_score": bw["score_bytes"] / KB,
-                   "gather_attn": bw["attn_bytes"] / KB, "topk_select": 0}
-    stage_flops = {"index_score": bw["score_flops"] / KB, "gather_attn": bw["attn_flops"] / KB}
+    stage_bytes = {"append": bw["append_bytes"] / NB, "index_score": bw["score_bytes"] / NB,
+                   "gather_attn": bw["attn_bytes"] / NB, "topk_select": 0}
+    stage_flops = {"index_score": bw["score_flops"] / NB, "gather_attn": bw["attn_flops"] / NB}
     dominant = max(stage_ms, key=lambda n: stage_ms[n])
     if dominant == "topk_select":
         dominant = "gather_attn" if stage_ms["gather_attn"] >= stage_ms["index_score"] else "index_score"
