@@ -671,7 +671,11 @@ cudaError_t launch_attn_t(const Shape &sh, int n_seq, int R, const int32_t *seq_
                     static_cast<int>(n_units), pl.n_split, pl.split_len, seq_ids, pos0, cv, q, sel, n_sel, pm,
                     pl_, pa, status, sel_pos);
   if (e != cudaSuccess) return e;
-  return launch_kernel(pdl, merge_kernel, dim3(rows, sh.hkv), dim3(kMergeThreads), 0, st, sh.hq, sh.hkv,
+  // The merge always launches as a programmatic dependent: its predecessor is
+  // the attention kernel above, whatever launched that, and it reads nothing
+  // before its wait that the attention writes, so its launch overlaps the
+  // attention's tail instead of following it.
+  return launch_kernel(true, merge_kernel, dim3(rows, sh.hkv), dim3(kMergeThreads), 0, st, sh.hq, sh.hkv,
                        pl.n_split, static_cast<const float *>(pm), static_cast<const float *>(pl_),
                        static_cast<const float *>(pa), out, commit, gate);
 }
