@@ -87,7 +87,8 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2 *tmp, int2 *t
 // After a histogram pass (hist filled, then a barrier): the digit that holds
 // the remaining-th largest key. Thread t owns the kBinsPerThread digits below
 // kBins - kBinsPerThread * t; a suffix scan from the top digit finds it. Updates
-// prefix / mask / remaining and leaves `hist` all zero.
+// prefix / mask / remaining, leaves the digit's key count in s_res[2] and `hist`
+// all zero.
 __device__ __forceinline__ void digit_search(int shift, uint32_t dmask, uint32_t &prefix, uint32_t &mask,
                                              int &remaining, int *hist, int2 *scan_tmp, int *s_res) {
   const int top_bin = kBins - 1 - kBinsPerThread * threadIdx.x;
@@ -105,6 +106,7 @@ __device__ __forceinline__ void digit_search(int shift, uint32_t dmask, uint32_t
     if (above < remaining && remaining <= above + c[j]) {
       s_res[0] = top_bin - j;
       s_res[1] = above;
+      s_res[2] = c[j];
     }
     above += c[j];
   }
@@ -470,6 +472,167 @@ __device__ __forceinline__ void select_in_registers(const float *__restrict__ sr
   }
 }
 
+// ---------------------------------------------------------------------------
+// Rows of at most (4 * NV + NS) * kSelThreads blocks: thread t holds the run of
+// 4 * NV + NS = 32 consecutive blocks starting at 32 t, the first 4 * NV keys in
+// registers and the other NS in the row's copy in shared memory (padded so that
+// a warp's accesses fall in distinct banks). The selection is the
+// register path's: the range, a histogram pass over the top digit, and, while
+// the chosen digit holds more than kDirectMax keys, further passes over the
+// thread's own keys under the prefix fixed so far; then the chosen keys are
+// ranked by all warps and one block scan compacts. The shared-memory keys stay
+// raw and are taken relative to the row minimum as they are read.
+// ---------------------------------------------------------------------------
+template <int NV, int NS>
+__device__ __forceinline__ void select_in_runs(const float *__restrict__ srow, int n, int K,
+                                               int32_t *__restrict__ out, uint32_t *keys, uint32_t *cand,
+                                               int *hist, int2 *scan_tmp, int *s_res, int *s_ncand,
+                                               uint32_t *red_min, uint32_t *red_max) {
+  constexpr int NR = 4 * NV;  // keys in registers
+  constexpr int RUN = NR + NS;
+  static_assert(RUN == 32, "a run is one 32-key row of the padded staging layout");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int x0 = RUN * tid;
+  // The row goes to shared memory first, read with lane-contiguous 16-byte
+  // loads (each thread reading its own run would spread a warp's load over 32
+  // lines), at index b + b / 32: thread t's run is then words 33 t .. 33 t + 31,
+  // so a warp reading key j of every run touches 32 distinct banks. ld is a
+  // multiple of 4, so the 16-byte groups that start below n lie in the row.
+  {
+    const float4 *r4 = reinterpret_cast<const float4 *>(srow);
+    for (int i = tid; 4 * i < n; i += kSelThreads) {
+      const float4 f = r4[i];
+      const int b = 4 * i;
+      keys[b + (b >> 5)] = score_key(f.x);  // b .. b + 3 share one 32-block row
+      keys[b + 1 + (b >> 5)] = score_key(f.y);
+      keys[b + 2 + (b >> 5)] = score_key(f.z);
+      keys[b + 3 + (b >> 5)] = score_key(f.w);
+    }
+  }
+  __syncthreads();
+  const uint32_t *ks = keys + 33 * tid;  // this thread's run
+  uint32_t d[NR];
+  // (only words of the staged row are read: x0 + j < n)
+#pragma unroll
+  for (int j = 0; j < NR; ++j) d[j] = x0 + j < n ? ks[j] : 0u;
+  ks += NR;  // the run's keys kept in shared memory
+  auto valid = [&](int j) { return x0 + j < n; };
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+  for (int j = 0; j < NR; ++j)
+    if (valid(j)) {
+      kmin = min(kmin, d[j]);
+      kmax = max(kmax, d[j]);
+    }
+#pragma unroll 4
+  for (int j = 0; j < NS; ++j)
+    if (valid(NR + j)) {
+      const uint32_t k = ks[j];
+      kmin = min(kmin, k);
+      kmax = max(kmax, k);
+    }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) {
+    red_min[warp] = kmin;
+    red_max[warp] = kmax;
+  }
+  __syncthreads();
+  kmin = __reduce_min_sync(0xffffffffu, lane < kSelWarps ? red_min[lane] : 0xffffffffu);
+  kmax = __reduce_max_sync(0xffffffffu, lane < kSelWarps ? red_max[lane] : 0u);
+#pragma unroll
+  for (int j = 0; j < NR; ++j) d[j] -= kmin;  // invalid entries are never read
+  auto skey = [&](int j) { return ks[j] - kmin; };
+
+  const uint32_t range = kmax - kmin;
+  int top = range ? 31 - __clz(range) : -1;
+  const uint32_t low_bits = (top >= 31) ? 0xffffffffu : (top >= 0 ? ((2u << top) - 1u) : 0u);
+  uint32_t prefix = 0u;
+  uint32_t mask = ~low_bits;
+  int remaining = K;
+  while (top >= 0) {
+    // a pass over the keys under the prefix: histogram of the next digit
+    const int width = min(kDigit, top + 1);
+    const int shift = top + 1 - width;
+    const uint32_t dmask = (1u << width) - 1u;
+#pragma unroll
+    for (int j = 0; j < NR; ++j)
+      if (valid(j) && (d[j] & mask) == prefix) atomicAdd(&hist[(d[j] >> shift) & dmask], 1);
+#pragma unroll 4
+    for (int j = 0; j < NS; ++j) {
+      if (!valid(NR + j)) continue;
+      const uint32_t k = skey(j);
+      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & dmask], 1);
+    }
+    __syncthreads();
+    digit_search(shift, dmask, prefix, mask, remaining, hist, scan_tmp, s_res);  // leaves hist zero
+    top = shift - 1;
+    if (top < 0) break;  // the prefix is the whole key: the threshold
+    if (s_res[2] <= kDirectMax) {
+      // the keys under the prefix: few, ranked by all warps at once
+      int pos = -1;
+      uint32_t member = 0u;
+#pragma unroll
+      for (int j = 0; j < NR; ++j)
+        if (valid(j) && (d[j] & mask) == prefix) member |= 1u << j;
+      int extra = 0;
+#pragma unroll 4
+      for (int j = 0; j < NS; ++j) extra += (valid(NR + j) && (skey(j) & mask) == prefix) ? 1 : 0;
+      const int mine = __popc(member) + extra;
+      if (mine) pos = atomicAdd(s_ncand, mine);
+#pragma unroll
+      for (int j = 0; j < NR; ++j)
+        if ((member >> j) & 1u) cand[pos++] = d[j];
+      if (extra) {
+        for (int j = 0; j < NS; ++j) {
+          if (!valid(NR + j)) continue;
+          const uint32_t k = skey(j);
+          if ((k & mask) == prefix) cand[pos++] = k;
+        }
+      }
+      __syncthreads();
+      rank_candidates(cand, *s_ncand, prefix, remaining, s_res);
+      break;
+    }
+  }
+  const uint32_t thr = prefix;  // the K-th largest key
+  const int need = remaining;   // ties at thr to take (>= 1)
+
+  // ---- compaction: the blocks before this thread's emit the keys above thr
+  // before it and the ties before it, capped at `need` (counts packed 16:16)
+  uint32_t c0 = 0u;
+#pragma unroll
+  for (int j = 0; j < NR; ++j)
+    if (valid(j)) c0 += (d[j] > thr ? 1u : 0u) + (d[j] == thr ? 0x10000u : 0u);
+#pragma unroll 4
+  for (int j = 0; j < NS; ++j)
+    if (valid(NR + j)) {
+      const uint32_t k = skey(j);
+      c0 += (k > thr ? 1u : 0u) + (k == thr ? 0x10000u : 0u);
+    }
+  const uint32_t p0 =
+      static_cast<uint32_t>(block_exclusive_scan1(static_cast<int>(c0), reinterpret_cast<int *>(scan_tmp)));
+  int o = static_cast<int>(p0 & 0xffffu) + min(static_cast<int>(p0 >> 16), need);
+  int tie_rank = static_cast<int>(p0 >> 16);
+  auto emit = [&](uint32_t k, int blk) {
+    if (k > thr) {
+      if (o < K) out[o] = blk;
+      ++o;
+    } else if (k == thr) {
+      if (tie_rank < need) {
+        if (o < K) out[o] = blk;
+        ++o;
+      }
+      ++tie_rank;
+    }
+  };
+#pragma unroll
+  for (int j = 0; j < NR; ++j)
+    if (valid(j)) emit(d[j], x0 + j);
+  for (int j = 0; j < NS; ++j)
+    if (valid(NR + j)) emit(skey(j), x0 + NR + j);
+}
+
 // Longer rows: keys staged in shared memory (or read from global memory when
 // the row does not fit there either).
 __device__ __noinline__ void select_general(const float *__restrict__ srow, int n, int K,
@@ -529,7 +692,7 @@ select_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__
   __shared__ int hist[kBins];
   __shared__ int2 scan_tmp[kSelWarps];
   __shared__ uint32_t red_min[kSelWarps], red_max[kSelWarps];
-  __shared__ int s_res[2], s_ncand;
+  __shared__ int s_res[3], s_ncand;
 
   const int row = blockIdx.x;
   const int i = row / R;
@@ -576,6 +739,8 @@ select_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__
     select_in_registers<3, 0>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else if (n <= 16 * kSelThreads) {
     select_in_registers<4, 0>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
+  } else if (n <= 32 * kSelThreads) {  // runs of 32: 16 keys in registers, 16 in shared memory
+    select_in_runs<4, 16>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else {
     select_general(srow, n, K, out, keys, cand, smem_keys, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   }
@@ -589,8 +754,11 @@ cudaError_t launch_select(const Shape &sh, int n_seq, int R, const int32_t *pos0
                           int max_blocks, int cap_tokens, int32_t *status, bool pdl,
                           cudaStream_t st) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
-  // rows of more than kMaxSmemKeys blocks read their scores from global memory
-  const int cap = max_blocks < kMaxSmemKeys ? max_blocks : kMaxSmemKeys;
+  // rows of more than kMaxSmemKeys blocks read their scores from global memory;
+  // runs of 32 take their row padded by one word per 32 blocks
+  int want = max_blocks + max_blocks / 32 + 1;
+  if (max_blocks > 16 * kSelThreads && want < 33 * kSelThreads) want = 33 * kSelThreads;
+  const int cap = want < kMaxSmemKeys ? want : kMaxSmemKeys;
   const size_t smem = (static_cast<size_t>(cap) + kCandMax) * 4;
   cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));

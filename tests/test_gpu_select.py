@@ -104,3 +104,15 @@ def test_select_rows_past_a_layout_boundary(kind):
 @pytest.mark.parametrize("kind", ["spread", "few_values", "signed_zero"])
 def test_select_k2048_with_tail_keys(kind):
     run_select(4, 8192, [8193, 9000, 9216], kind, seed=30)
+
+
+@pytest.mark.parametrize("kind", S.SCORE_KINDS)
+def test_select_runs_of_32(kind):
+    # past 16384 blocks (up to 32768) a thread's run is 32 keys, 16 in registers
+    # and 16 in shared memory; 32769 takes the shared-memory path
+    run_select(4, 2048, [16385, 20000, 24577, 32767, 32768, 32769], kind, seed=31)
+
+
+@pytest.mark.parametrize("kind", ["spread", "few_values", "cluster"])
+def test_select_runs_of_32_k2048(kind):
+    run_select(4, 8192, [16385, 30000, 32768], kind, seed=32)
