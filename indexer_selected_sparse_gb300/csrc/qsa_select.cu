@@ -309,18 +309,19 @@ __device__ __forceinline__ void select_row(Src src, int n, int K, uint32_t range
 // whole selection and, when E = 1, one more block from the row's tail, M + t
 // (M = 4 * NV * kSelThreads), so that a row just past a multiple of 4096 blocks
 // costs one key more per thread instead of four. Warp reductions use
-// redux.sync; the candidates of the chosen digit are gathered with a shared
-// atomic per thread that holds any and ranked by all warps at once when at most
-// kDirectMax; the compaction is one block scan of each thread's counts above
-// and at the threshold (packed 16:16; a second word for the tail),
+// redux.sync; while the chosen digit holds more than kDirectMax keys, a further
+// pass over the thread's own keys under the prefix fixed so far takes the next
+// digit; then the chosen keys are gathered with a shared atomic per thread that
+// holds any and ranked by all warps at once; the compaction is one block scan of
+// each thread's counts above and at the threshold (packed 16:16; a second word
+// for the tail),
 // after which every thread writes its own selected blocks in index order (no
 // bitmaps, no atomics). Barriers: range 1, histogram 1, digit search 2,
 // candidates 1, ranking 1, compaction scan 1.
 // ---------------------------------------------------------------------------
 template <int NV, int E>
 __device__ __forceinline__ void select_in_registers(const float *__restrict__ srow, int n, int K,
-                                                    int32_t *__restrict__ out, uint32_t *keys,
-                                                    uint32_t *cand, int *hist, int2 *scan_tmp, int *s_res,
+                                                    int32_t *__restrict__ out, uint32_t *cand, int *hist, int2 *scan_tmp, int *s_res,
                                                     int *s_ncand, uint32_t *red_min, uint32_t *red_max) {
   static_assert(E == 0 || E == 1, "at most one tail key per thread");
   constexpr int NR = 4 * NV;   // keys of the contiguous run
@@ -369,17 +370,19 @@ __device__ __forceinline__ void select_in_registers(const float *__restrict__ sr
   uint32_t prefix = 0u;
   uint32_t mask = ~low_bits;
   int remaining = K;
-  if (top >= 0) {
-    int width = min(kDigit, top + 1);
-    int shift = top + 1 - width;
+  while (top >= 0) {
+    // a pass over the keys under the prefix: histogram of the next digit
+    const int width = min(kDigit, top + 1);
+    const int shift = top + 1 - width;
     const uint32_t dmask = (1u << width) - 1u;
 #pragma unroll
     for (int j = 0; j < NK; ++j)
-      if (valid(j)) atomicAdd(&hist[d[j] >> shift], 1);  // d <= range: the digit fits
+      if (valid(j) && (d[j] & mask) == prefix) atomicAdd(&hist[(d[j] >> shift) & dmask], 1);
     __syncthreads();
-    digit_search(shift, dmask, prefix, mask, remaining, hist, scan_tmp, s_res);
+    digit_search(shift, dmask, prefix, mask, remaining, hist, scan_tmp, s_res);  // leaves hist zero
     top = shift - 1;
-    if (top >= 0) {
+    if (top < 0) break;  // the prefix is the whole key: the threshold
+    if (s_res[2] <= kDirectMax) {
       // the keys of the chosen digit, in any order (only their values are
       // ranked): usually a few threads hold one or two, so each of those
       // reserves its slots with its own shared atomic
@@ -391,36 +394,11 @@ __device__ __forceinline__ void select_in_registers(const float *__restrict__ sr
         int pos = atomicAdd(s_ncand, __popc(member));
 #pragma unroll
         for (int j = 0; j < NK; ++j)
-          if ((member >> j) & 1u) {
-            if (pos < kCandMax) cand[pos] = d[j];
-            ++pos;
-          }
+          if ((member >> j) & 1u) cand[pos++] = d[j];
       }
       __syncthreads();
-      const int nc = *s_ncand;
-      if (nc <= kDirectMax) {
-        rank_candidates(cand, nc, prefix, remaining, s_res);
-      } else {
-        // long candidate lists: further passes over the list, or, when it
-        // overflowed, over the whole row staged in shared memory
-        const uint32_t *list = cand;
-        int m = nc;
-        if (nc > kCandMax) {
-#pragma unroll
-          for (int j = 0; j < NK; ++j)
-            if (valid(j)) keys[blk(j)] = d[j];
-          __syncthreads();
-          list = keys;
-          m = n;
-        }
-        while (top >= 0) {
-          width = min(kDigit, top + 1);
-          shift = top + 1 - width;
-          radix_pass(SmemKeys{list, 0u}, m, shift, (1u << width) - 1u, prefix, mask, remaining, hist,
-                     scan_tmp, s_res);
-          top = shift - 1;
-        }
-      }
+      rank_candidates(cand, *s_ncand, prefix, remaining, s_res);
+      break;
     }
   }
   const uint32_t thr = prefix;  // the K-th largest key
@@ -730,15 +708,15 @@ select_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__
   // rows up to 16k blocks (64k tokens at ratio 4) keep their keys in registers
   // (a thread's run of 4 NV keys plus E tail keys; the smallest layout that holds the row)
   if (n <= 4 * kSelThreads) {
-    select_in_registers<1, 0>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
+    select_in_registers<1, 0>(srow, n, K, out, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else if (n <= 8 * kSelThreads) {
-    select_in_registers<2, 0>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
+    select_in_registers<2, 0>(srow, n, K, out, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else if (n <= 9 * kSelThreads) {
-    select_in_registers<2, 1>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
+    select_in_registers<2, 1>(srow, n, K, out, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else if (n <= 12 * kSelThreads) {
-    select_in_registers<3, 0>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
+    select_in_registers<3, 0>(srow, n, K, out, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else if (n <= 16 * kSelThreads) {
-    select_in_registers<4, 0>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
+    select_in_registers<4, 0>(srow, n, K, out, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else if (n <= 32 * kSelThreads) {  // runs of 32: 16 keys in registers, 16 in shared memory
     select_in_runs<4, 16>(srow, n, K, out, keys, cand, hist, scan_tmp, s_res, &s_ncand, red_min, red_max);
   } else {
