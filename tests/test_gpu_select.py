@@ -84,7 +84,7 @@ def test_select_short_rows_split_over_the_cluster(kind):
 @pytest.mark.parametrize("kind", ["spread", "few_values", "signed_zero"])
 def test_select_k1(kind):
     # K = 1: the single largest block, ties to the lowest index
-    run_select(4, 4, [2, 3, 5, 4097, 9000], kind, seed=27)
+    run_select(4, 4, [2, 3, 5, 4097, 9000, 20000, 32768], kind, seed=27)
 
 
 @pytest.mark.parametrize("kind", ["spread", "cluster", "few_values", "relu_sum"])
@@ -116,3 +116,28 @@ def test_select_runs_of_32(kind):
 @pytest.mark.parametrize("kind", ["spread", "few_values", "cluster"])
 def test_select_runs_of_32_k2048(kind):
     run_select(4, 8192, [16385, 30000, 32768], kind, seed=32)
+
+
+def test_select_all_equal_rows_take_the_lowest_indices():
+    # a row whose scores are all equal has an empty key range: every layout
+    # (runs of 4 .. 32, the shared-memory path) takes the K lowest block indices
+    cfg = Q.Config(4, 2048, 64, 128, 32, 4)
+    K = cfg.topk
+    ns = [600, 8193, 12000, 16384, 20000, 32768, 40000]
+    ld = (max(ns) + 3) // 4 * 4
+    scores = torch.full((len(ns), ld), 2.5, dtype=torch.float32)
+    scores[1, :] = -0.0  # signed zeros compare equal to +0
+    scores[1, ::3] = 0.0
+    pos0 = torch.tensor([n * 4 + 2 for n in ns], dtype=torch.int32)
+    rows = Q.Rows(torch.arange(len(ns), dtype=torch.int32, device="cuda"), pos0.cuda(), 1)
+    sel = torch.full((len(ns), K), -7, dtype=torch.int32, device="cuda")
+    nsel = torch.full((len(ns),), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Q.qsa_topk_select(cfg, rows, scores.cuda(), ld, sel, nsel, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    sel = sel.cpu().numpy()
+    for r, n in enumerate(ns):
+        want = O.select_blocks(scores[r, :n].numpy().astype(np.float64), K)
+        assert np.array_equal(want, np.arange(K))
+        assert nsel[r].item() == K and np.array_equal(sel[r], want), (r, n)
