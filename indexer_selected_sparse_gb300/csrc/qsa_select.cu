@@ -725,6 +725,392 @@ select_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__
   if (tid == 0) n_sel[row] = K;
 }
 
+// ---------------------------------------------------------------------------
+// Long rows on a thread-block cluster of C CTAs (1024 threads each) per row.
+// CTA rank c holds the consecutive blocks [c * per, (c + 1) * per) of the row
+// (per a multiple of 4) in the register layout of per blocks (runs of 4 NV keys
+// per thread), so a row of 16k blocks costs 8 keys per thread on 2 SMs instead
+// of 16 on one. The CTAs share what each phase needs through distributed
+// shared memory: the row's range (each CTA's min and max), each radix pass's
+// histograms (every CTA sums the cluster's into its own copy and runs the same
+// digit search, so all reach the same digit; the search also counts the keys
+// above the digit held by lower-ranked CTAs) and the final short candidate list
+// (every CTA copies the cluster's lists in rank order and ranks the merged
+// list, counting the lower-ranked CTAs' candidates above and at the threshold).
+// Those lower-rank counts are where a CTA's selected blocks start in the output,
+// so the compaction is a local block scan. A CTA reads another's shared memory
+// only after a cluster barrier that follows the owner's last write of it, and a
+// split barrier (arrive after the last remote read, wait before exit) keeps
+// every CTA resident while another may still read from it. The histograms are
+// double-buffered: a buffer is cleared only after the next cluster barrier.
+// ---------------------------------------------------------------------------
+
+// Distributed shared memory: the address of p's counterpart in cluster CTA
+// `rank`, loads from such an address, and the cluster barrier.
+__device__ __forceinline__ uint32_t cluster_addr(const void *p, int rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 ld_cluster_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ int4 ld_cluster_v4(uint32_t addr) {
+  int4 v;
+  asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
+}
+
+// After a cluster barrier that follows every CTA's histogram of this pass (hb:
+// the pass's buffer, at the same offset in every CTA): the digit that holds the
+// remaining-th largest key of the row. The C histograms are summed into hsum
+// (all CTAs) and hlow (CTAs ranked below crank), each thread reading runs of 4
+// bins, so a warp's remote reads are contiguous; then thread t owns the
+// kBinsPerThread digits below kBins - kBinsPerThread * t. Leaves in s_res: [0]
+// the digit, [1] the row's keys above it, [2] the row's keys in it, [3] and [4]
+// the same two counts over the lower-ranked CTAs.
+template <int C>
+__device__ __forceinline__ void cluster_digit_search(int remaining, int crank, const int *hb, int *hsum, int *hlow,
+                                                     int2 *scan_tmp, int *s_res) {
+  const int tid = threadIdx.x;
+  static_assert(kBins / 4 <= kSelThreads, "a thread reads at most one run of 4 bins");
+  if (tid < kBins / 4) {
+    const int b = 4 * tid;
+    int4 s = make_int4(0, 0, 0, 0), l = make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int r = 0; r < C; ++r) {
+      const int4 v = ld_cluster_v4(cluster_addr(hb + b, r));
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+      if (r < crank) {
+        l.x += v.x;
+        l.y += v.y;
+        l.z += v.z;
+        l.w += v.w;
+      }
+    }
+    *reinterpret_cast<int4 *>(hsum + b) = s;
+    *reinterpret_cast<int4 *>(hlow + b) = l;
+  }
+  __syncthreads();
+  const int top_bin = kBins - 1 - kBinsPerThread * tid;
+  int c_all[kBinsPerThread], c_low[kBinsPerThread];
+  int s_all = 0, s_low = 0;
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    c_all[j] = hsum[top_bin - j];
+    c_low[j] = hlow[top_bin - j];
+    s_all += c_all[j];
+    s_low += c_low[j];
+  }
+  int2 above = block_exclusive_scan2(make_int2(s_all, s_low), scan_tmp);
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    if (above.x < remaining && remaining <= above.x + c_all[j]) {
+      s_res[0] = top_bin - j;
+      s_res[1] = above.x;
+      s_res[2] = c_all[j];
+      s_res[3] = above.y;
+      s_res[4] = c_low[j];
+    }
+    above.x += c_all[j];
+    above.y += c_low[j];
+  }
+  __syncthreads();
+}
+
+template <int C, int NV>
+__device__ __forceinline__ void select_cluster_row(const float *__restrict__ srow, int n, int K, int crank,
+                                                   int32_t *__restrict__ out, int (*hist)[kBins], int *hsum,
+                                                   int *hlow, uint32_t *cand, uint32_t *mcand, int2 *scan_tmp,
+                                                   int *s_res, int *s_ncand, uint32_t *red_min, uint32_t *red_max,
+                                                   uint2 *s_mm) {
+  constexpr int NK = 4 * NV;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = ((n + 4 * C - 1) / (4 * C)) * 4;  // blocks per CTA, a multiple of 4
+  const int lo = crank * per;
+  const int hi = min(n, lo + per);
+  const int x0 = lo + NK * tid;  // this thread's first block
+  // 16-byte loads: ld and x0 are multiples of 4, so a group that starts below n lies in the row
+  const float4 *s4 = reinterpret_cast<const float4 *>(srow + x0);
+  uint32_t d[NK];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (x0 + 4 * v < hi) f = s4[v];
+    d[4 * v] = score_key(f.x);
+    d[4 * v + 1] = score_key(f.y);
+    d[4 * v + 2] = score_key(f.z);
+    d[4 * v + 3] = score_key(f.w);
+  }
+  auto valid = [&](int j) { return x0 + j < hi; };
+
+  // ---- the row's range: every CTA publishes its min and max, then reads all
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+  for (int j = 0; j < NK; ++j)
+    if (valid(j)) {
+      kmin = min(kmin, d[j]);
+      kmax = max(kmax, d[j]);
+    }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) {
+    red_min[warp] = kmin;
+    red_max[warp] = kmax;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    kmin = __reduce_min_sync(0xffffffffu, lane < kSelWarps ? red_min[lane] : 0xffffffffu);
+    kmax = __reduce_max_sync(0xffffffffu, lane < kSelWarps ? red_max[lane] : 0u);
+    if (lane == 0) *s_mm = make_uint2(kmin, kmax);
+  }
+  // the first cluster barrier: every CTA has started and published its range
+  cluster_sync();
+  kmin = 0xffffffffu;
+  kmax = 0u;
+#pragma unroll
+  for (int r = 0; r < C; ++r) {
+    const uint2 m = ld_cluster_v2(cluster_addr(s_mm, r));
+    kmin = min(kmin, m.x);
+    kmax = max(kmax, m.y);
+  }
+#pragma unroll
+  for (int j = 0; j < NK; ++j) d[j] -= kmin;  // invalid entries are never read
+
+  const uint32_t range = kmax - kmin;
+  int top = range ? 31 - __clz(range) : -1;
+  const uint32_t low_bits = (top >= 31) ? 0xffffffffu : (top >= 0 ? ((2u << top) - 1u) : 0u);
+  uint32_t prefix = 0u;
+  uint32_t mask = ~low_bits;
+  int remaining = K;
+  int gt_low = 0;  // keys above the threshold held by lower-ranked CTAs
+  int eq_low = 0;  // keys at the threshold held by lower-ranked CTAs
+  if (top < 0) {
+    // every key of the row is equal: the threshold is that key
+#pragma unroll
+    for (int r = 0; r < C; ++r)
+      if (r < crank) eq_low += max(0, min(n, (r + 1) * per) - r * per);
+  }
+  for (int pass = 0; top >= 0; ++pass) {
+    // a pass over the keys under the prefix: histogram of the next digit
+    const int width = min(kDigit, top + 1);
+    const int shift = top + 1 - width;
+    const uint32_t dmask = (1u << width) - 1u;
+    int *hb = hist[pass & 1];
+    if (pass >= 2) {  // this buffer's remote readers passed the previous pass's barrier
+      for (int b = tid; b < kBins; b += kSelThreads) hb[b] = 0;
+      __syncthreads();
+    }
+#pragma unroll
+    for (int j = 0; j < NK; ++j)
+      if (valid(j) && (d[j] & mask) == prefix) atomicAdd(&hb[(d[j] >> shift) & dmask], 1);
+    cluster_sync();
+    cluster_digit_search<C>(remaining, crank, hb, hsum, hlow, scan_tmp, s_res);
+    prefix |= static_cast<uint32_t>(s_res[0]) << shift;
+    mask |= dmask << shift;
+    remaining -= s_res[1];
+    gt_low += s_res[3];
+    top = shift - 1;
+    if (top < 0) {  // the prefix is the whole key: the threshold
+      eq_low = s_res[4];
+      break;
+    }
+    if (s_res[2] <= kDirectMax) {
+      // the keys under the prefix (at most kDirectMax over the row): each CTA
+      // lists its own, then every CTA copies the cluster's lists in rank order
+      // (CTA r's entries at offs[r]) and ranks the merged list
+      uint32_t member = 0u;
+#pragma unroll
+      for (int j = 0; j < NK; ++j)
+        if (valid(j) && (d[j] & mask) == prefix) member |= 1u << j;
+      if (member) {
+        int pos = atomicAdd(s_ncand, __popc(member));
+#pragma unroll
+        for (int j = 0; j < NK; ++j)
+          if ((member >> j) & 1u) cand[pos++] = d[j];
+      }
+      cluster_sync();
+      int cnt[C], offs[C + 1];
+      offs[0] = 0;
+#pragma unroll
+      for (int r = 0; r < C; ++r) {
+        cnt[r] = static_cast<int>(ld_cluster_u32(cluster_addr(s_ncand, r)));
+        offs[r + 1] = offs[r] + cnt[r];
+      }
+      const int nc = offs[C];
+      int my_off = 0;  // the lower-ranked CTAs' entries (static indices only: no local memory)
+#pragma unroll
+      for (int q = 0; q < C; ++q)
+        if (q < crank) my_off += cnt[q];
+      if (tid < nc) {
+        int r = 0, base = 0;
+#pragma unroll
+        for (int q = 1; q < C; ++q)
+          if (tid >= offs[q]) {
+            r = q;
+            base = offs[q];
+          }
+        mcand[tid] = ld_cluster_u32(cluster_addr(cand + (tid - base), r));
+      }
+      __syncthreads();
+      rank_candidates(mcand, nc, prefix, remaining, s_res);
+      // the lower-ranked CTAs' candidates above and at the threshold: the
+      // merged list holds them first, my_off of them
+      if (warp == 0) {
+        int g = 0, e = 0;
+        for (int i = lane; i < my_off; i += 32) {
+          g += mcand[i] > prefix ? 1 : 0;
+          e += mcand[i] == prefix ? 1 : 0;
+        }
+        g = __reduce_add_sync(0xffffffffu, g);
+        e = __reduce_add_sync(0xffffffffu, e);
+        if (lane == 0) {
+          s_res[3] = g;
+          s_res[4] = e;
+        }
+      }
+      __syncthreads();
+      gt_low += s_res[3];
+      eq_low = s_res[4];
+      break;
+    }
+  }
+  // every remote access of this CTA is done: the others may leave once all
+  // have arrived here
+  cluster_arrive();
+  const uint32_t thr = prefix;  // the K-th largest key
+  const int need = remaining;   // ties at thr to take (>= 1)
+
+  // ---- compaction: the blocks before this thread's emit gt_low plus the keys
+  // above thr before it in this CTA, and min(eq_low + the ties before it, need)
+  // ties; its own blocks follow in index order (counts packed 16:16)
+  uint32_t c0 = 0u;
+#pragma unroll
+  for (int j = 0; j < NK; ++j)
+    if (valid(j)) c0 += (d[j] > thr ? 1u : 0u) + (d[j] == thr ? 0x10000u : 0u);
+  const uint32_t p0 =
+      static_cast<uint32_t>(block_exclusive_scan1(static_cast<int>(c0), reinterpret_cast<int *>(scan_tmp)));
+  int tie_rank = eq_low + static_cast<int>(p0 >> 16);
+  int o = gt_low + static_cast<int>(p0 & 0xffffu) + min(tie_rank, need);
+#pragma unroll
+  for (int j = 0; j < NK; ++j) {
+    if (!valid(j)) continue;
+    if (d[j] > thr) {
+      if (o < K) out[o] = x0 + j;
+      ++o;
+    } else if (d[j] == thr) {
+      if (tie_rank < need) {
+        if (o < K) out[o] = x0 + j;
+        ++o;
+      }
+      ++tie_rank;
+    }
+  }
+  cluster_wait();
+}
+
+template <int C>
+__global__ void __launch_bounds__(kSelThreads)
+select_cluster_kernel(Shape sh, int R, const int32_t *__restrict__ pos0, const float *__restrict__ scores, int ld,
+                      int32_t *__restrict__ sel, int32_t *__restrict__ n_sel, int cap_tokens, int32_t *status) {
+  __shared__ __align__(16) int hist[2][kBins];
+  __shared__ __align__(16) int hsum[kBins];
+  __shared__ __align__(16) int hlow[kBins];
+  __shared__ uint32_t cand[kDirectMax], mcand[kDirectMax];
+  __shared__ int2 scan_tmp[kSelWarps];
+  __shared__ uint32_t red_min[kSelWarps], red_max[kSelWarps];
+  __shared__ uint2 s_mm;
+  __shared__ int s_res[5], s_ncand;
+
+  uint32_t crank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+  const int row = blockIdx.x / C;
+  const int i = row / R;
+  const int visible = pos0[i] + (row - i * R) + 1;
+  const int n = visible >> sh.log2_ratio;
+  const int K = sh.topk;
+  int32_t *out = sel + static_cast<size_t>(row) * K;
+  const int tid = threadIdx.x;
+
+  // rows that need no ranking are written by rank 0 alone, with no cluster
+  // barrier (the same branch in every CTA of the cluster: n is the row's)
+  if (visible < 1 || visible > cap_tokens || n > ld || n > 4 * 4 * kSelThreads * C) {
+    pdl_wait();
+    pdl_trigger();
+    if (crank != 0) return;
+    for (int x = tid; x < K; x += kSelThreads) out[x] = -1;
+    if (tid == 0) {
+      n_sel[row] = 0;
+      report(status, QSA_ERR_CAPACITY);
+    }
+    return;
+  }
+  if (n <= K) {  // every block is selected: exactly dense attention
+    pdl_wait();
+    pdl_trigger();
+    if (crank != 0) return;
+    for (int x = tid; x < K; x += kSelThreads) out[x] = x < n ? x : -1;
+    if (tid == 0) n_sel[row] = n;
+    return;
+  }
+
+  for (int b = tid; b < 2 * kBins; b += kSelThreads) (&hist[0][0])[b] = 0;
+  if (tid == 0) s_ncand = 0;
+  pdl_wait();  // scores come from the score kernel
+  pdl_trigger();
+  const float *srow = scores + static_cast<size_t>(row) * ld;
+  const int per = ((n + 4 * C - 1) / (4 * C)) * 4;
+  const int r = static_cast<int>(crank);
+  if (per <= 4 * kSelThreads)
+    select_cluster_row<C, 1>(srow, n, K, r, out, hist, hsum, hlow, cand, mcand, scan_tmp, s_res, &s_ncand, red_min,
+                             red_max, &s_mm);
+  else if (per <= 8 * kSelThreads)
+    select_cluster_row<C, 2>(srow, n, K, r, out, hist, hsum, hlow, cand, mcand, scan_tmp, s_res, &s_ncand, red_min,
+                             red_max, &s_mm);
+  else if (per <= 12 * kSelThreads)
+    select_cluster_row<C, 3>(srow, n, K, r, out, hist, hsum, hlow, cand, mcand, scan_tmp, s_res, &s_ncand, red_min,
+                             red_max, &s_mm);
+  else
+    select_cluster_row<C, 4>(srow, n, K, r, out, hist, hsum, hlow, cand, mcand, scan_tmp, s_res, &s_ncand, red_min,
+                             red_max, &s_mm);
+  if (crank == 0 && tid == 0) n_sel[row] = K;
+}
+
+int sm_count() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      sms = v;
+  }
+  return sms;
+}
+
 }  // namespace
 
 cudaError_t launch_select(const Shape &sh, int n_seq, int R, const int32_t *pos0,
@@ -732,6 +1118,24 @@ cudaError_t launch_select(const Shape &sh, int n_seq, int R, const int32_t *pos0
                           int max_blocks, int cap_tokens, int32_t *status, bool pdl,
                           cudaStream_t st) {
   if (n_seq == 0 || R == 0) return cudaSuccess;
+  // Rows past 9216 blocks (beyond the one-CTA layouts of at most 9 keys per
+  // thread) go to a cluster of C CTAs per row when the launch's C * rows CTAs
+  // fit on the GPU at once (1024 threads at 64 registers: one CTA per SM) and
+  // every row fits C CTAs' register runs of at most 16 keys
+  const long long rows = static_cast<long long>(n_seq) * R;
+  const int sms = sm_count();
+  if (max_blocks > 9 * kSelThreads && sms > 0) {
+    const int c = (rows * 4 <= sms && max_blocks <= 4 * 16 * kSelThreads) ? 4
+                  : (rows * 2 <= sms && max_blocks <= 2 * 16 * kSelThreads) ? 2 : 1;
+    if (c == 4)
+      return launch_kernel_cluster(pdl, 4, select_cluster_kernel<4>, dim3(static_cast<unsigned>(rows * 4)),
+                                   dim3(kSelThreads), 0, st, sh, R, pos0, scores, ld_scores, sel, n_sel, cap_tokens,
+                                   status);
+    if (c == 2)
+      return launch_kernel_cluster(pdl, 2, select_cluster_kernel<2>, dim3(static_cast<unsigned>(rows * 2)),
+                                   dim3(kSelThreads), 0, st, sh, R, pos0, scores, ld_scores, sel, n_sel, cap_tokens,
+                                   status);
+  }
   // rows of more than kMaxSmemKeys blocks read their scores from global memory;
   // runs of 32 take their row padded by one word per 32 blocks
   int want = max_blocks + max_blocks / 32 + 1;

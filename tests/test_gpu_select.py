@@ -141,3 +141,14 @@ def test_select_all_equal_rows_take_the_lowest_indices():
         want = O.select_blocks(scores[r, :n].numpy().astype(np.float64), K)
         assert np.array_equal(want, np.arange(K))
         assert nsel[r].item() == K and np.array_equal(sel[r], want), (r, n)
+
+
+@pytest.mark.parametrize("n_rows", [8, 40, 80])
+@pytest.mark.parametrize("kind", ["spread", "few_values", "relu_sum", "infinite"])
+def test_select_cluster_sizes_and_one_cta_layouts(n_rows, kind):
+    # rows past 9216 blocks go to a cluster of 4 CTAs per row when 4 x rows
+    # CTAs fit on the GPU (8 rows), of 2 when 2 x rows fit (40 rows), else (80
+    # rows) to one CTA per row: runs of 12 or 16 register keys, runs of 32
+    cycle = [9217, 12288, 12289, 16384, 16385, 20000, 32768, 513, 8193, 600, 30001]
+    ns = [cycle[i % len(cycle)] for i in range(n_rows)]
+    run_select(4, 2048, ns, kind, seed=33 + n_rows)
