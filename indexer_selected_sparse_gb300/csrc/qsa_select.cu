@@ -3,23 +3,31 @@
 // review ... (Claude's review)", (a): top-512 + tail, inert below
 // budget + ratio - 1 visible tokens).
 //
-// One CTA per row. Scores become order-preserving uint32 keys (-0 folded onto
-// +0), each taken relative to the row's smallest key so that the radix digits
-// span exactly the range the row covers. Digits are 11 bits, most significant
-// first: a pass histograms the keys that match the prefix fixed so far and a
-// block-wide suffix scan finds the digit that holds the K-th largest key. Only
-// the first pass reads every key: the keys of the chosen digit are gathered
-// into a candidate list, which all warps rank at once when it is short and
-// further passes refine otherwise. The K-th largest key T is then exact, and so
-// is the number of ties at T that must be taken. A stable compaction emits, in
+// Scores become order-preserving uint32 keys (-0 folded onto +0), each taken
+// relative to the row's smallest key so that the radix digits span exactly the
+// range the row covers. Digits are 11 bits, most significant first: a pass
+// histograms the keys that match the prefix fixed so far and a block-wide
+// suffix scan finds the digit that holds the K-th largest key. Once the chosen
+// digit holds at most 128 keys, they are gathered into a candidate list that
+// all warps rank at once. The K-th largest key T is then exact, and so is the
+// number of ties at T that must be taken. A stable compaction emits, in
 // ascending block order, every block with key > T and the lowest-indexed blocks
 // with key == T: exactly the top-K under (score desc, index asc).
-// Rows of up to 16k blocks keep their keys in registers (each thread a run of
-// consecutive blocks, plus one block of the row's tail for rows just past a
-// layout's size) and compact with one block scan of per-thread counts;
-// longer rows stage their keys in shared memory (or, past that, read them from
-// global memory). The selection stays on the device, so a step that
-// contains it can be captured in a CUDA graph.
+//
+// Layouts, by the longest row of a launch:
+//   * one CTA per row, keys in registers (each thread a run of consecutive
+//     blocks, plus one block of the row's tail just past a layout's size), up to
+//     16k blocks; further digits by passes over each thread's own keys;
+//   * past 9216 blocks, when they fit on the GPU at once, a thread-block cluster
+//     of 2 or 4 CTAs per row, each holding a part of the row in registers and
+//     exchanging ranges, histograms and candidates through distributed shared
+//     memory;
+//   * one CTA per row with runs of 32 keys (16 in registers, 16 in a padded
+//     shared-memory copy of the row) up to 32k blocks;
+//   * longer rows staged in shared memory (or, past that, read from global
+//     memory) with candidate lists refined by passes over the list.
+// The selection stays on the device, so a step that contains it can be
+// captured in a CUDA graph.
 #include "qsa_internal.cuh"
 
 namespace qsa {
