@@ -839,33 +839,26 @@ def run_e2e(args, Q, torch, cfg, cache, batches, ws, status, stream, NB, B, rows
             h2d = sum(t.numel() * t.element_size() for t in ins)   # the inputs' own bytes
             h2d_copied = hbuf.numel()                               # with the 256-byte alignment gaps
             d2h = hout.numel() * hout.element_size()
-        h2d_stream = torch.cuda.Stream(device=dev)
         d2h_stream = torch.cuda.Stream(device=dev)
         ev_fork = torch.cuda.Event()
-        ev_in = [torch.cuda.Event() for _ in range(NB)]
         ev_step = [torch.cuda.Event() for _ in range(NB)]
-        ev_join = [torch.cuda.Event() for _ in range(2)]
+        ev_join = torch.cuda.Event()
         g = torch.cuda.CUDAGraph()
         torch.cuda.synchronize()
         with torch.cuda.graph(g, stream=stream):
             ev_fork.record(stream)
-            h2d_stream.wait_event(ev_fork)
             d2h_stream.wait_event(ev_fork)
             for b, (dbuf, hbuf, hout, ebt) in enumerate(keep):
-                with torch.cuda.stream(h2d_stream):
-                    dbuf.copy_(hbuf, non_blocking=True)
-                    ev_in[b].record(h2d_stream)
-            for b, (dbuf, hbuf, hout, ebt) in enumerate(keep):
-                stream.wait_event(ev_in[b])
+                # the inputs cross by qsa_stage_in, a copy kernel in the step's own
+                # programmatic chain (a copy-engine node would break the chain)
+                Q.qsa_stage_in(dbuf, hbuf, stream=stream)
                 decode_call(ebt)
                 ev_step[b].record(stream)
                 with torch.cuda.stream(d2h_stream):
                     d2h_stream.wait_event(ev_step[b])
                     hout.copy_(batches[b]["out"], non_blocking=True)
-            ev_join[0].record(h2d_stream)
-            ev_join[1].record(d2h_stream)
-            stream.wait_event(ev_join[0])
-            stream.wait_event(ev_join[1])
+            ev_join.record(d2h_stream)
+            stream.wait_event(ev_join)
         torch.cuda.synchronize()
         n_rot = max(1, math.ceil(KE / NB))
         with torch.cuda.stream(stream):
@@ -887,9 +880,10 @@ def run_e2e(args, Q, torch, cfg, cache, batches, ws, status, stream, NB, B, rows
         e2e = {"value": round(rows_per_step / (ems * 1e-3), 1), "unit": "rows/s",  # rows of all ranks
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "h2d_bytes_copied_per_step": h2d_copied,
                "ms_per_step": round(ems, 5), "steps": steps,
-               "path": "per step: pinned host inputs (one packed buffer) -> one H2D copy -> qsa_decode -> D2H "
-                       f"of the output; one CUDA graph per rotation of the {NB} independent batches, the H2D "
-                       "copies on one copy stream ahead of their steps and the D2H copies on another after them"}
+               "path": "per step: pinned host inputs (one packed buffer) -> qsa_stage_in (a copy kernel in the "
+                       "step's programmatic launch chain, overlapping the previous step's last kernel) -> "
+                       f"qsa_decode -> D2H of the output; one CUDA graph per rotation of the {NB} independent "
+                       "batches, the D2H copies on a copy stream after their steps"}
     return e2e
 
 

@@ -499,6 +499,26 @@ int qsa_gather_attn_static(const qsa_config *cfg, const qsa_rows *rows, const qs
                            const qsa_bf16 *q, const int32_t *sel, const int32_t *n_sel,
                            qsa_bf16 *out, int32_t *status, cudaStream_t stream);
 
+/* Host-to-device copy of a step's inputs inside the stream's chain of kernels
+ * (the pages have no counterpart: this is the library's way to feed a fused
+ * step from host memory without breaking the programmatic launch chain that a
+ * copy-engine node would break). A kernel reads `bytes` bytes at `src` in host
+ * memory the device can reach -- pinned (cudaHostAlloc, cudaHostRegister), or
+ * any host memory where the GPU accesses pageable memory through a coherent
+ * CPU-GPU link; checked with cudaHostGetDevicePointer -- and writes them to
+ * `dst` in device memory. It is launched as a programmatic dependent of the previous kernel on
+ * the stream and copies before it waits for that kernel, so the copy overlaps
+ * the kernel's tail; a library kernel launched after it on the stream sees the
+ * copy and everything before it.
+ *   dst    device, 16-byte aligned; must not be read by the kernel launched
+ *          just before this call on the stream (give each step its own buffer)
+ *   src    host memory the device can reach, 16-byte aligned
+ *   bytes  a multiple of 16
+ * Returns QSA_ERR_INVALID_ARG for a NULL or misaligned pointer, a size that is
+ * not a multiple of 16, or a source the device cannot reach (nothing is
+ * launched then). */
+int qsa_stage_in(void *dst, const void *src, size_t bytes, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -340,6 +340,31 @@ int decode_impl(const qsa_config *cfg, const qsa_pre_indexer *pre, const qsa_att
                     base + L.partials, status, true, commit, stream, nullptr, att ? att->gate : nullptr);
   return cuda_status(e);
 }
+
+// A step's inputs from pinned host memory into device memory, as a kernel in
+// the stream's programmatic chain: every CTA copies its 16-byte pieces, then
+// waits for the previous kernel and only then lets the next one launch, so the
+// copy overlaps the previous kernel's tail and the chain's ordering (a kernel
+// never overlaps one two back) is kept.
+constexpr int kStageThreads = 256;
+
+__global__ void __launch_bounds__(kStageThreads)
+stage_in_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src, size_t n16) {
+  // four loads in flight per thread before their stores (host memory is a
+  // long round trip away)
+  const size_t stride = static_cast<size_t>(gridDim.x) * kStageThreads;
+  for (size_t i0 = static_cast<size_t>(blockIdx.x) * kStageThreads + threadIdx.x; i0 < n16; i0 += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + u * stride < n16) v[u] = src[i0 + u * stride];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + u * stride < n16) dst[i0 + u * stride] = v[u];
+  }
+  pdl_wait();
+  pdl_trigger();
+}
 }  // namespace
 }  // namespace qsa
 
@@ -667,6 +692,24 @@ int qsa_decode_reuse(const qsa_config *cfg, const qsa_rows *rows, const qsa_cach
     e = launch_attn(sh, rows->n_seq, R, rows->seq_ids, rows->pos0, view(cache), q, sel, n_sel, out,
                     static_cast<uint8_t *>(ws) + L.partials, status, true, commit, stream, sel_pos);
   return cuda_status(e);
+}
+
+int qsa_stage_in(void *dst, const void *src, size_t bytes, cudaStream_t stream) {
+  if (!dst || !src || !aligned16(dst) || !aligned16(src) || bytes % 16 != 0) return QSA_ERR_INVALID_ARG;
+  if (bytes == 0) return QSA_OK;
+  // the device's address of the host buffer (the same pointer under unified
+  // addressing); a buffer the device cannot reach is refused before any launch
+  void *dev_src = nullptr;
+  if (cudaHostGetDevicePointer(&dev_src, const_cast<void *>(src), 0) != cudaSuccess || !dev_src) {
+    cudaGetLastError();  // the failed lookup leaves no error behind
+    return QSA_ERR_INVALID_ARG;
+  }
+  const size_t n16 = bytes / 16;
+  // enough CTAs to keep the C2C link busy, a few pieces each
+  const size_t want = (n16 + 4 * kStageThreads - 1) / (4 * kStageThreads);
+  const unsigned grid = static_cast<unsigned>(want < 256 ? (want > 0 ? want : 1) : 256);
+  return cuda_status(launch_kernel(true, stage_in_kernel, dim3(grid), dim3(kStageThreads), 0, stream,
+                                   static_cast<uint4 *>(dst), static_cast<const uint4 *>(dev_src), n16));
 }
 
 }  // extern "C"

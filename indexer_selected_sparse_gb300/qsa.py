@@ -42,7 +42,7 @@ EXPORTED = ("qsa_strerror", "qsa_config_check", "qsa_workspace_bytes", "qsa_appe
             "qsa_gather_attn_static", "qsa_max_attend_tokens", "qsa_gather_attn_reuse",
             "qsa_decode_reuse", "qsa_append_pre", "qsa_pre_index_q", "qsa_workspace_bytes_pre",
             "qsa_decode_pre", "qsa_idxblk_page_bytes", "qsa_quantize_index_q", "qsa_append_ex",
-            "qsa_workspace_bytes_ex", "qsa_decode_ex", "qsa_set_wait_limit_ns")
+            "qsa_workspace_bytes_ex", "qsa_decode_ex", "qsa_set_wait_limit_ns", "qsa_stage_in")
 QSA_STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -123,6 +123,8 @@ LIB.qsa_gather_attn_static.restype = _I
 LIB.qsa_gather_attn_static.argtypes = [_CFG, _ROWS, _CACHE, _P, _P, _P, _P, _P, _P]
 LIB.qsa_set_wait_limit_ns.restype = ctypes.c_ulonglong
 LIB.qsa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+LIB.qsa_stage_in.restype = _I
+LIB.qsa_stage_in.argtypes = [_P, _P, ctypes.c_size_t, _P]
 LIB.qsa_max_attend_tokens.restype = _I
 LIB.qsa_max_attend_tokens.argtypes = [_CFG]
 LIB.qsa_gather_attn_reuse.restype = _I
@@ -349,6 +351,18 @@ def qsa_set_wait_limit_ns(ns: int) -> int:
     """Test hook: the index-score kernel's wait limit in ns (0 = default 1 s);
     returns the previous limit."""
     return int(LIB.qsa_set_wait_limit_ns(ctypes.c_ulonglong(ns)))
+
+
+def qsa_stage_in(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:
+    """Copy the bytes of pinned host tensor `src` into device tensor `dst` (same
+    byte size, a multiple of 16) with a kernel in the stream's programmatic
+    chain (see include/qsa.h)."""
+    if not src.is_pinned() or dst.device.type != "cuda":
+        raise ValueError("qsa_stage_in copies a pinned host tensor into a device tensor")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("qsa_stage_in: source and destination sizes differ")
+    _check(LIB.qsa_stage_in(_ptr(dst), _ptr(src), nbytes, _stream(stream)), "qsa_stage_in")
 
 
 def qsa_gather_attn_static(cfg: Config, rows: Rows, cache: PagedCache, q, sel, n_sel, out,

@@ -267,3 +267,17 @@ def test_wait_limit_hook_clamps_and_restores(Q):
     assert Q.qsa_set_wait_limit_ns(0) == 10_000_000_000            # clamped down to 10 s
     assert Q.qsa_set_wait_limit_ns(first) == 1_000_000_000
     Q.qsa_set_wait_limit_ns(0)
+
+
+def test_stage_in_arguments_checked_on_host(Q):
+    """qsa_stage_in refuses null or misaligned pointers and sizes that are not a
+    multiple of 16 before touching CUDA; a zero-byte copy is a no-op."""
+    buf = ctypes.create_string_buffer(256)
+    a16 = (ctypes.addressof(buf) + 15) // 16 * 16
+    lib = Q.LIB
+    assert lib.qsa_stage_in(None, a16, 16, None) == Q.QSA_ERR_INVALID_ARG
+    assert lib.qsa_stage_in(a16, None, 16, None) == Q.QSA_ERR_INVALID_ARG
+    assert lib.qsa_stage_in(a16 + 4, a16, 16, None) == Q.QSA_ERR_INVALID_ARG
+    assert lib.qsa_stage_in(a16, a16 + 8, 16, None) == Q.QSA_ERR_INVALID_ARG
+    assert lib.qsa_stage_in(a16, a16, 24, None) == Q.QSA_ERR_INVALID_ARG
+    assert lib.qsa_stage_in(a16, a16, 0, None) == Q.QSA_OK
