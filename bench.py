@@ -1137,7 +1137,7 @@ def run_verify(args, dev):
     qsa_decode of R = 3 causal rows per sequence (2 drafts + 1), the rewind of
     the rejected rows (0..2 per sequence, seeded), 4 decode steps on fresh rows
     at the re-used positions, and a rewind back to the start so the cycle repeats
-    on the same data; one CUDA graph per cycle. Bytes per SURVEY's verify rule:
+    on the same data; one CUDA graph per cycle. Algorithmic bytes of the verify rows:
     a sequence's compressed keys once for its 3 verify rows, K+V once per distinct
     token of their sets (the union, from the step's own selections), plus the
     decode rows as in the decode leg."""
@@ -1212,7 +1212,8 @@ def run_verify(args, dev):
     assert st == 0, f"device status {st}: {Q.qsa_strerror(st)}"
     assert cache.ingested.cpu().tolist() == [p] * B
     ms = e0.elapsed_time(e1) / K
-    # bytes of a cycle: verify rows with the SURVEY rule, then the decode rows
+    # bytes of a cycle: the verify rows (keys once per sequence, K+V once per
+    # distinct selected token), then the decode rows
     sel_h = sel_v.cpu().tolist()
     kb = key_bytes(sh, "bf16")
     ver_bytes = 0
